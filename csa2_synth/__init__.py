@@ -122,3 +122,43 @@ def choose_channels(seed: int, n_channels: int, count: int) -> np.ndarray:
 def seq_lengths(seed: int, batch: int, lo: int, hi: int) -> np.ndarray:
     """Per-sequence token counts drawn uniformly in [lo, hi]."""
     return uniform_int(stream_key(seed, S_LENGTHS, 0), 0, batch, lo, hi)
+
+
+# ---------------------------------------------------------------- device twin
+_dev_lib = None
+
+
+def _device_lib():
+    global _dev_lib
+    if _dev_lib is None:
+        import ctypes
+        import os
+        path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcsa2synth.so")
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is missing: build it with __graft_entry__.build()")
+        L = ctypes.CDLL(path)
+        for name in ("csa2_synth_fill_f32", "csa2_synth_fill_bf16"):
+            fn = getattr(L, name)
+            fn.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_float,
+                           ctypes.c_void_p, ctypes.c_void_p]
+            fn.restype = ctypes.c_int
+        _dev_lib = L
+    return _dev_lib
+
+
+def device_fill(t, key: int, first: int = 0, scale: float = 1.0, stream=None):
+    """Fill a contiguous CUDA tensor (float32 or bfloat16) with elements
+    ``first ..`` of the stream with ``key``; ``scale`` must be a power of two.
+    Bit-identical to ``normal_f32`` / ``normal_bf16`` times ``scale``."""
+    import ctypes
+    import torch
+    assert t.is_cuda and t.is_contiguous()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    L = _device_lib()
+    fn = L.csa2_synth_fill_f32 if t.dtype == torch.float32 else L.csa2_synth_fill_bf16
+    assert t.dtype in (torch.float32, torch.bfloat16)
+    rc = fn(key & 0xFFFFFFFFFFFFFFFF, first, t.numel(), scale, ctypes.c_void_p(t.data_ptr()),
+            ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise RuntimeError(f"csa2_synth fill failed: cuda error {rc}")
+    return t

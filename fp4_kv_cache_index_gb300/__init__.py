@@ -1,0 +1,302 @@
+"""GB300-native CSA2 sparse attention over an FP4 global KV cache.
+
+Thin Python binding of ``libcsa2.so`` (the C ABI in ``include/csa2.h``).  It
+only marshals arguments: torch tensors become device pointers, the current
+torch stream becomes the launch stream, and output tensors are created with
+torch when the caller passes none.  Every step of the attention path runs in
+the library's CUDA kernels; there is no fallback.  If the library has not been
+built the import of this module raises.
+
+Function names follow the C ABI (``csa2_index_topk_decode`` ...).  ``Cache``
+owns the device buffer of one CSA2 group's global cache and its handle.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcsa2.so")
+
+CSA2_KV_L32_UE8M0 = 0
+CSA2_KV_L16_E4M3 = 1
+
+STATUS = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTED",
+          3: "CSA2_ERR_CAPACITY", 4: "CSA2_ERR_CUDA", 5: "CSA2_ERR_OOM",
+          6: "CSA2_ERR_TIMEOUT", 7: "CSA2_ERR_DEVICE"}
+
+
+class Csa2Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("n_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("idx_heads", ctypes.c_int32), ("idx_dim", ctypes.c_int32),
+                ("topk", ctypes.c_int32), ("swa", ctypes.c_int32),
+                ("ratio", ctypes.c_int32), ("layout", ctypes.c_int32)]
+
+
+def config(n_heads=64, head_dim=512, idx_heads=32, idx_dim=128, topk=512, swa=128, ratio=1,
+           layout=CSA2_KV_L32_UE8M0) -> Config:
+    """Layer shapes of the V4.1 report, section 4.2.1, as defaults."""
+    return Config(n_heads, head_dim, idx_heads, idx_dim, topk, swa, ratio, layout)
+
+
+class CacheViews(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("idx_k", ctypes.c_void_p), ("lengths", ctypes.c_void_p),
+                ("entry_offset", ctypes.POINTER(ctypes.c_int64)), ("total", ctypes.c_int64),
+                ("batch", ctypes.c_int32), ("group", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                          "(the CSA2 path has no CPU fallback)")
+    L = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    pcfg = ctypes.POINTER(Config)
+    sigs = {
+        "csa2_version": ([], i32),
+        "csa2_status_string": ([i32], ctypes.c_char_p),
+        "csa2_cache_bytes": ([pcfg, i32, P], sz),
+        "csa2_cache_create": ([pcfg, i32, P, P, sz, P, ctypes.POINTER(P)], i32),
+        "csa2_cache_destroy": ([P], i32),
+        "csa2_cache_reset": ([P, P], i32),
+        "csa2_cache_length": ([P, i32, ctypes.POINTER(i64)], i32),
+        "csa2_cache_views": ([P, ctypes.POINTER(CacheViews)], i32),
+        "csa2_compress": ([i32, i64, i32, P, P, P, P], i32),
+        "csa2_append_entries": ([P, i32, P, P, P, P, P], i32),
+        "csa2_append_tokens": ([P, i32, P, P, P, P, P, P, P], i32),
+        "csa2_index_workspace_bytes": ([P, i32], sz),
+        "csa2_index_topk_decode": ([P, i32, P, P, P, P, P, P, sz, P], i32),
+        "csa2_index_topk_prefill": ([P, i32, i32, i64, P, P, P, P, P, sz, P], i32),
+        "csa2_topk_workspace_bytes": ([i32], sz),
+        "csa2_topk": ([i32, P, i64, P, i32, P, P, P, sz, P], i32),
+        "csa2_sparse_attn_decode": ([P, i32, P, P, P, P, P, ctypes.c_float, P, P, P], i32),
+        "csa2_sparse_attn_prefill": ([P, i32, i32, i64, P, P, i64, i64, P, ctypes.c_float, P, P,
+                                      P], i32),
+        "csa2_get_device_error": ([P, P, ctypes.POINTER(i32)], i32),
+    }
+    for name, (args, res) in sigs.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    return L
+
+
+lib = _load()
+
+
+def _check(st: int, what: str):
+    if st != 0:
+        raise Csa2Error(st, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("expected a contiguous CUDA tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _i32_array(xs: Optional[Sequence[int]]):
+    if xs is None:
+        return None
+    return (ctypes.c_int32 * len(xs))(*[int(x) for x in xs])
+
+
+def _i64_array(xs: Sequence[int]):
+    return (ctypes.c_int64 * len(xs))(*[int(x) for x in xs])
+
+
+class Cache:
+    """One CSA2 group's global KV cache in a torch-owned device buffer."""
+
+    def __init__(self, cfg: Config, capacity: Sequence[int], device=None, stream=None):
+        self.cfg = cfg
+        self.batch = len(capacity)
+        caps = _i64_array(capacity)
+        nbytes = lib.csa2_cache_bytes(ctypes.byref(cfg), self.batch, caps)
+        if nbytes == 0:
+            raise Csa2Error(1, "csa2_cache_bytes")
+        device = torch.device("cuda") if device is None else torch.device(device)
+        self.buffer = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+        self._off = (-self.buffer.data_ptr()) % 256
+        self.handle = ctypes.c_void_p()
+        _check(lib.csa2_cache_create(ctypes.byref(cfg), self.batch, caps,
+                                     ctypes.c_void_p(self.buffer.data_ptr() + self._off),
+                                     nbytes, _stream(stream), ctypes.byref(self.handle)),
+               "csa2_cache_create")
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value:
+            lib.csa2_cache_destroy(h)
+            self.handle = None
+
+    def length(self, seq: int) -> int:
+        n = ctypes.c_int64()
+        _check(lib.csa2_cache_length(self.handle, seq, ctypes.byref(n)), "csa2_cache_length")
+        return n.value
+
+    def reset(self, stream=None):
+        _check(lib.csa2_cache_reset(self.handle, _stream(stream)), "csa2_cache_reset")
+
+    def views(self) -> dict:
+        """codes [total, 256] u8, scales [total, 512/g] u8, idx_k [total, 128]
+        bf16, lengths [batch] int32, entry_offset (list), group."""
+        v = CacheViews()
+        _check(lib.csa2_cache_views(self.handle, ctypes.byref(v)), "csa2_cache_views")
+        base = self.buffer.data_ptr()
+        total = v.total
+
+        def sl(ptr, nbytes):
+            o = ptr - base
+            return self.buffer[o:o + nbytes]
+
+        g = v.group
+        return {
+            "codes": sl(v.codes, total * 256).view(total, 256),
+            "scales": sl(v.scales, total * (512 // g)).view(total, 512 // g),
+            "idx_k": sl(v.idx_k, total * 256).view(torch.bfloat16).view(total, 128),
+            "lengths": sl(v.lengths, 4 * self.batch).view(torch.int32),
+            "entry_offset": [v.entry_offset[i] for i in range(self.batch + 1)],
+            "group": g,
+        }
+
+    def device_error(self, stream=None) -> int:
+        st = ctypes.c_int32()
+        _check(lib.csa2_get_device_error(self.handle, _stream(stream), ctypes.byref(st)),
+               "csa2_get_device_error")
+        return st.value
+
+
+# ------------------------------------------------------------------ compress / append
+def csa2_compress(ratio: int, c_tok: torch.Tensor, z_tok: torch.Tensor,
+                  out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    t, dim = c_tok.shape
+    n_out = t // ratio
+    if out is None:
+        out = torch.empty(n_out, dim, dtype=torch.float32, device=c_tok.device)
+    _check(lib.csa2_compress(ratio, n_out, dim, _ptr(c_tok), _ptr(z_tok), _ptr(out),
+                             _stream(stream)), "csa2_compress")
+    return out
+
+
+def csa2_append_entries(cache: Cache, seq_ids: Sequence[int], n_new: Sequence[int],
+                        entries: torch.Tensor, idx_k: torch.Tensor, stream=None):
+    _check(lib.csa2_append_entries(cache.handle, len(seq_ids), _i32_array(seq_ids),
+                                   _i32_array(n_new), _ptr(entries), _ptr(idx_k),
+                                   _stream(stream)), "csa2_append_entries")
+
+
+def csa2_append_tokens(cache: Cache, seq_ids: Sequence[int], n_tok: Sequence[int],
+                       c_tok: torch.Tensor, z_tok: torch.Tensor, idx_k: torch.Tensor,
+                       entries_out: Optional[torch.Tensor] = None, stream=None):
+    _check(lib.csa2_append_tokens(cache.handle, len(seq_ids), _i32_array(seq_ids),
+                                  _i32_array(n_tok), _ptr(c_tok), _ptr(z_tok), _ptr(idx_k),
+                                  _ptr(entries_out), _stream(stream)), "csa2_append_tokens")
+
+
+# ------------------------------------------------------------------ indexer + top-k
+def csa2_index_workspace_bytes(cache: Cache, n_queries: int) -> int:
+    return int(lib.csa2_index_workspace_bytes(cache.handle, n_queries))
+
+
+def _workspace(nbytes: int, device, workspace):
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+    return workspace
+
+
+def csa2_index_topk_decode(cache: Cache, q_idx: torch.Tensor, w: torch.Tensor,
+                           seq_ids: Optional[Sequence[int]] = None,
+                           topk_idx: Optional[torch.Tensor] = None,
+                           topk_score: Optional[torch.Tensor] = None,
+                           workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    nq = q_idx.shape[0]
+    dev = q_idx.device
+    if topk_idx is None:
+        topk_idx = torch.empty(nq, cache.cfg.topk, dtype=torch.int32, device=dev)
+    ws = _workspace(csa2_index_workspace_bytes(cache, nq), dev, workspace)
+    _check(lib.csa2_index_topk_decode(cache.handle, nq, _ptr(q_idx), _ptr(w),
+                                      _i32_array(seq_ids), _ptr(topk_idx), _ptr(topk_score),
+                                      _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "csa2_index_topk_decode")
+    return topk_idx
+
+
+def csa2_index_topk_prefill(cache: Cache, seq: int, pos0: int, q_idx: torch.Tensor,
+                            w: torch.Tensor, topk_idx: Optional[torch.Tensor] = None,
+                            topk_score: Optional[torch.Tensor] = None,
+                            workspace: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
+    nq = q_idx.shape[0]
+    dev = q_idx.device
+    if topk_idx is None:
+        topk_idx = torch.empty(nq, cache.cfg.topk, dtype=torch.int32, device=dev)
+    cap = cache.views()["entry_offset"]
+    ld = max(4, (cap[seq + 1] - cap[seq] + 3) // 4 * 4)
+    ws = _workspace(nq * ld * 4, dev, workspace)
+    _check(lib.csa2_index_topk_prefill(cache.handle, seq, nq, pos0, _ptr(q_idx), _ptr(w),
+                                       _ptr(topk_idx), _ptr(topk_score), _ptr(ws),
+                                       ws.numel() * ws.element_size(), _stream(stream)),
+           "csa2_index_topk_prefill")
+    return topk_idx
+
+
+def csa2_topk(scores: torch.Tensor, n_valid: Sequence[int], k: int,
+              idx_out: Optional[torch.Tensor] = None, score_out: Optional[torch.Tensor] = None,
+              stream=None):
+    rows, ld = scores.shape
+    if idx_out is None:
+        idx_out = torch.empty(rows, k, dtype=torch.int32, device=scores.device)
+    _check(lib.csa2_topk(rows, _ptr(scores), ld, _i64_array(n_valid), k, _ptr(idx_out),
+                         _ptr(score_out), None, 0, _stream(stream)), "csa2_topk")
+    return idx_out
+
+
+# ------------------------------------------------------------------ attention
+def csa2_sparse_attn_decode(cache: Cache, q: torch.Tensor, swa_kv: Optional[torch.Tensor],
+                            topk_idx: torch.Tensor, scale: float,
+                            swa_len: Optional[torch.Tensor] = None,
+                            seq_ids: Optional[Sequence[int]] = None,
+                            out: Optional[torch.Tensor] = None,
+                            lse: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    nq = q.shape[0]
+    if out is None:
+        out = torch.empty_like(q)
+    _check(lib.csa2_sparse_attn_decode(cache.handle, nq, _i32_array(seq_ids), _ptr(q),
+                                       _ptr(swa_kv), _ptr(swa_len), _ptr(topk_idx),
+                                       float(scale), _ptr(out), _ptr(lse), _stream(stream)),
+           "csa2_sparse_attn_decode")
+    return out
+
+
+def csa2_sparse_attn_prefill(cache: Cache, seq: int, pos0: int, q: torch.Tensor,
+                             swa_kv: Optional[torch.Tensor], swa_pos0: int,
+                             topk_idx: torch.Tensor, scale: float,
+                             out: Optional[torch.Tensor] = None,
+                             lse: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    nq = q.shape[0]
+    if out is None:
+        out = torch.empty_like(q)
+    n_rows = swa_kv.shape[0] if swa_kv is not None else 0
+    _check(lib.csa2_sparse_attn_prefill(cache.handle, seq, nq, pos0, _ptr(q), _ptr(swa_kv),
+                                        swa_pos0, n_rows, _ptr(topk_idx), float(scale),
+                                        _ptr(out), _ptr(lse), _stream(stream)),
+           "csa2_sparse_attn_prefill")
+    return out

@@ -1,0 +1,650 @@
+// csa2_api.cu -- the C ABI declared in include/csa2.h: argument checks, the
+// cache layout in caller memory, TMA tensor maps, and launch scheduling of
+// the kernels in k_append.cu, k_index.cu, k_topk.cu and k_attn.cu.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "csa2.h"
+#include "csa2_kernels.h"
+
+using namespace csa2;
+
+struct csa2_cache {
+  csa2_config_t cfg;
+  int32_t batch;
+  int32_t group;       // channels per scale
+  int32_t scale_bytes; // per entry
+  std::vector<int64_t> cap, off, len;
+  int64_t total;
+  int64_t max_cap;
+  uint8_t* base;
+  size_t bytes;
+  int32_t* d_len;
+  uint32_t* d_err;
+  uint8_t* codes;
+  uint8_t* scales;
+  uint16_t* idxk;
+  CUtensorMap tm_k;
+  int num_sms;
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+csa2_status_t check_cfg(const csa2_config_t* c) {
+  if (!c) return CSA2_ERR_INVALID_ARG;
+  if (c->head_dim != kHeadDim || c->idx_dim != kIdxDim || c->idx_heads != kIdxHeads)
+    return CSA2_ERR_UNSUPPORTED;
+  if (c->n_heads <= 0 || c->n_heads % 32 != 0 || c->n_heads > 128) return CSA2_ERR_UNSUPPORTED;
+  if (c->topk <= 0 || c->topk % 128 != 0 || c->topk > 2048) return CSA2_ERR_UNSUPPORTED;
+  if (c->swa < 0 || c->swa > 128) return CSA2_ERR_UNSUPPORTED;
+  if (c->ratio < 1 || c->ratio > 16) return CSA2_ERR_UNSUPPORTED;
+  if (c->layout != CSA2_KV_L32_UE8M0 && c->layout != CSA2_KV_L16_E4M3) return CSA2_ERR_UNSUPPORTED;
+  return CSA2_OK;
+}
+
+struct Layout {
+  size_t len_off, err_off, codes_off, scales_off, idxk_off, total;
+};
+
+Layout layout_for(const csa2_config_t* c, int64_t total) {
+  Layout L;
+  const int g = c->layout == CSA2_KV_L16_E4M3 ? 16 : 32;
+  L.len_off = 0;
+  L.err_off = 0;  // filled below
+  L.codes_off = 0;
+  size_t o = 0;
+  L.len_off = o;
+  o = align_up(o + 4096 * sizeof(int32_t), kAlign);  // up to 4096 sequences of lengths
+  L.err_off = o;
+  o = align_up(o + sizeof(uint32_t), kAlign);
+  L.codes_off = o;
+  o = align_up(o + (size_t)total * (kHeadDim / 2), kAlign);
+  L.scales_off = o;
+  o = align_up(o + (size_t)total * (kHeadDim / g), kAlign);
+  L.idxk_off = o;
+  o = align_up(o + (size_t)total * kIdxDim * 2, kAlign);
+  L.total = o;
+  return L;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (row stride cols * 2 bytes), 128B-swizzled
+// boxes of [box_rows, box_cols]; out-of-range rows read as zero.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+              uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows == 0) return false;
+  cuuint64_t gdim[2] = {cols, rows};
+  cuuint64_t gstride[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaStream_t S(csa2_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+csa2_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
+
+int64_t score_ld(int64_t n) { return std::max<int64_t>(4, (n + 3) / 4 * 4); }
+
+// Append / compress segments: rows of one launch grouped by sequence.
+csa2_status_t run_append(csa2_cache* c, int mode, int32_t n_seqs, const int32_t* seq_ids,
+                         const int32_t* n_rows_in, const float* entries, const void* c_tok,
+                         const float* z_tok, const void* idx_k, float* entries_out,
+                         csa2_stream_t stream) {
+  if (!c || n_seqs < 0 || (n_seqs > 0 && (!seq_ids || !n_rows_in))) return CSA2_ERR_INVALID_ARG;
+  const int m = c->cfg.ratio;
+  std::vector<int64_t> new_len(c->len);
+  int64_t total_rows = 0;
+  for (int i = 0; i < n_seqs; ++i) {
+    const int32_t s = seq_ids[i];
+    const int32_t n = n_rows_in[i];
+    if (s < 0 || s >= c->batch || n < 0) return CSA2_ERR_INVALID_ARG;
+    if (mode == 2 && n % m != 0) return CSA2_ERR_INVALID_ARG;
+    const int64_t ne = mode == 2 ? n / m : n;
+    new_len[s] += ne;
+    if (new_len[s] > c->cap[s]) return CSA2_ERR_CAPACITY;
+    total_rows += ne;
+  }
+  if (total_rows == 0) return CSA2_OK;
+  if (!idx_k || !aligned16(idx_k)) return CSA2_ERR_INVALID_ARG;
+  if (mode == 1 && (!entries || !aligned16(entries))) return CSA2_ERR_INVALID_ARG;
+  if (mode == 2 && (!c_tok || !z_tok || !aligned16(c_tok) || !aligned16(z_tok)))
+    return CSA2_ERR_INVALID_ARG;
+  if (entries_out && !aligned16(entries_out)) return CSA2_ERR_INVALID_ARG;
+
+  std::vector<int64_t> cur(c->len);
+  int64_t src = 0;
+  int i = 0;
+  while (i < n_seqs) {
+    AppendParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.mode = mode;
+    p.ratio = m;
+    p.layout = c->cfg.layout;
+    p.dim = kHeadDim;
+    p.entries = entries;
+    p.c_tok = static_cast<const uint16_t*>(c_tok);
+    p.z_tok = z_tok;
+    p.idx_k = static_cast<const uint16_t*>(idx_k);
+    p.entries_out = entries_out;
+    p.codes = c->codes;
+    p.scales = c->scales;
+    p.cache_idxk = c->idxk;
+    p.d_len = c->d_len;
+    int64_t rows = 0;
+    while (i < n_seqs && p.n_segs < kMaxAppendSegs) {
+      const int32_t s = seq_ids[i];
+      const int64_t ne = mode == 2 ? n_rows_in[i] / m : n_rows_in[i];
+      AppendSeg& g = p.seg[p.n_segs++];
+      g.first = rows;
+      g.src_row = src;
+      g.dst_row = c->off[s] + cur[s];
+      g.seq = s;
+      cur[s] += ne;
+      g.new_len = (int32_t)cur[s];
+      rows += ne;
+      src += ne;
+      ++i;
+    }
+    p.rows = rows;
+    cudaError_t e = launch_append(p, S(stream));
+    if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  }
+  c->len = new_len;
+  return CSA2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t csa2_version(void) { return 1; }
+
+const char* csa2_status_string(csa2_status_t s) {
+  switch (s) {
+    case CSA2_OK: return "ok";
+    case CSA2_ERR_INVALID_ARG: return "invalid argument";
+    case CSA2_ERR_UNSUPPORTED: return "unsupported configuration";
+    case CSA2_ERR_CAPACITY: return "capacity exceeded";
+    case CSA2_ERR_CUDA: return "CUDA error";
+    case CSA2_ERR_OOM: return "out of memory";
+    case CSA2_ERR_TIMEOUT: return "device wait timed out";
+    case CSA2_ERR_DEVICE: return "device-side check failed";
+  }
+  return "unknown status";
+}
+
+size_t csa2_cache_bytes(const csa2_config_t* cfg, int32_t batch, const int64_t* capacity) {
+  if (check_cfg(cfg) != CSA2_OK || batch <= 0 || batch > 4096 || !capacity) return 0;
+  int64_t total = 0;
+  for (int i = 0; i < batch; ++i) {
+    if (capacity[i] < 0 || capacity[i] > (int64_t)INT32_MAX) return 0;
+    total += capacity[i];
+  }
+  if (total <= 0) return 0;
+  return layout_for(cfg, total).total;
+}
+
+csa2_status_t csa2_cache_create(const csa2_config_t* cfg, int32_t batch, const int64_t* capacity,
+                                void* dev_mem, size_t bytes, csa2_stream_t stream,
+                                csa2_cache_t** out) {
+  if (!out) return CSA2_ERR_INVALID_ARG;
+  *out = nullptr;
+  csa2_status_t st = check_cfg(cfg);
+  if (st != CSA2_OK) return st;
+  if (batch <= 0 || batch > 4096 || !capacity || !dev_mem) return CSA2_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(dev_mem) & (kAlign - 1)) != 0) return CSA2_ERR_INVALID_ARG;
+  const size_t need = csa2_cache_bytes(cfg, batch, capacity);
+  if (need == 0) return CSA2_ERR_INVALID_ARG;
+  if (bytes < need) return CSA2_ERR_CAPACITY;
+
+  csa2_cache* c = new (std::nothrow) csa2_cache();
+  if (!c) return CSA2_ERR_OOM;
+  c->cfg = *cfg;
+  c->batch = batch;
+  c->group = cfg->layout == CSA2_KV_L16_E4M3 ? 16 : 32;
+  c->scale_bytes = kHeadDim / c->group;
+  c->cap.assign(capacity, capacity + batch);
+  c->off.resize(batch + 1);
+  c->len.assign(batch, 0);
+  c->off[0] = 0;
+  c->max_cap = 0;
+  for (int i = 0; i < batch; ++i) {
+    c->off[i + 1] = c->off[i] + capacity[i];
+    c->max_cap = std::max(c->max_cap, capacity[i]);
+  }
+  c->total = c->off[batch];
+  const Layout L = layout_for(cfg, c->total);
+  c->base = static_cast<uint8_t*>(dev_mem);
+  c->bytes = bytes;
+  c->d_len = reinterpret_cast<int32_t*>(c->base + L.len_off);
+  c->d_err = reinterpret_cast<uint32_t*>(c->base + L.err_off);
+  c->codes = c->base + L.codes_off;
+  c->scales = c->base + L.scales_off;
+  c->idxk = reinterpret_cast<uint16_t*>(c->base + L.idxk_off);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    delete c;
+    return CSA2_ERR_CUDA;
+  }
+  if (!make_map(&c->tm_k, c->idxk, (uint64_t)c->total, kIdxDim, 64, 128)) {
+    delete c;
+    return CSA2_ERR_CUDA;
+  }
+  if (cudaMemsetAsync(c->base, 0, L.codes_off, S(stream)) != cudaSuccess) {
+    delete c;
+    return CSA2_ERR_CUDA;
+  }
+  *out = c;
+  return CSA2_OK;
+}
+
+csa2_status_t csa2_cache_destroy(csa2_cache_t* c) {
+  if (!c) return CSA2_ERR_INVALID_ARG;
+  delete c;
+  return CSA2_OK;
+}
+
+csa2_status_t csa2_cache_reset(csa2_cache_t* c, csa2_stream_t stream) {
+  if (!c) return CSA2_ERR_INVALID_ARG;
+  std::fill(c->len.begin(), c->len.end(), 0);
+  return cuda_status(cudaMemsetAsync(c->d_len, 0, sizeof(int32_t) * c->batch, S(stream)));
+}
+
+csa2_status_t csa2_cache_length(const csa2_cache_t* c, int32_t seq, int64_t* n) {
+  if (!c || !n || seq < 0 || seq >= c->batch) return CSA2_ERR_INVALID_ARG;
+  *n = c->len[seq];
+  return CSA2_OK;
+}
+
+csa2_status_t csa2_cache_views(const csa2_cache_t* c, csa2_cache_views_t* v) {
+  if (!c || !v) return CSA2_ERR_INVALID_ARG;
+  v->codes = c->codes;
+  v->scales = c->scales;
+  v->idx_k = c->idxk;
+  v->lengths = c->d_len;
+  v->entry_offset = c->off.data();
+  v->total = c->total;
+  v->batch = c->batch;
+  v->group = c->group;
+  return CSA2_OK;
+}
+
+csa2_status_t csa2_compress(int32_t ratio, int64_t n_out, int32_t dim, const void* c_tok,
+                            const float* z_tok, float* out, csa2_stream_t stream) {
+  if (ratio < 1 || ratio > 16 || n_out < 0 || dim <= 0 || dim % 16 != 0 || dim > kHeadDim)
+    return ratio > 16 || dim > kHeadDim ? CSA2_ERR_UNSUPPORTED : CSA2_ERR_INVALID_ARG;
+  if (n_out == 0) return CSA2_OK;
+  if (!c_tok || !z_tok || !out || !aligned16(c_tok) || !aligned16(z_tok) || !aligned16(out))
+    return CSA2_ERR_INVALID_ARG;
+  AppendParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.mode = 0;
+  p.ratio = ratio;
+  p.dim = dim;
+  p.n_segs = 1;
+  p.rows = n_out;
+  p.seg[0].first = 0;
+  p.c_tok = static_cast<const uint16_t*>(c_tok);
+  p.z_tok = z_tok;
+  p.entries_out = out;
+  return cuda_status(launch_append(p, S(stream)));
+}
+
+csa2_status_t csa2_append_entries(csa2_cache_t* c, int32_t n_seqs, const int32_t* seq_ids,
+                                  const int32_t* n_new, const float* entries, const void* idx_k,
+                                  csa2_stream_t stream) {
+  return run_append(c, 1, n_seqs, seq_ids, n_new, entries, nullptr, nullptr, idx_k, nullptr,
+                    stream);
+}
+
+csa2_status_t csa2_append_tokens(csa2_cache_t* c, int32_t n_seqs, const int32_t* seq_ids,
+                                 const int32_t* n_tok, const void* c_tok, const float* z_tok,
+                                 const void* idx_k, float* entries_out, csa2_stream_t stream) {
+  return run_append(c, 2, n_seqs, seq_ids, n_tok, nullptr, c_tok, z_tok, idx_k, entries_out,
+                    stream);
+}
+
+size_t csa2_index_workspace_bytes(const csa2_cache_t* c, int32_t n_queries) {
+  if (!c || n_queries < 0) return 0;
+  return (size_t)n_queries * (size_t)score_ld(c->max_cap) * sizeof(float);
+}
+
+size_t csa2_topk_workspace_bytes(int32_t) { return 0; }
+
+csa2_status_t csa2_topk(int32_t n_rows, const float* scores, int64_t ld, const int64_t* n_valid,
+                        int32_t k, int32_t* idx_out, float* score_out, void*, size_t,
+                        csa2_stream_t stream) {
+  if (n_rows < 0 || k <= 0 || k > 4096) return CSA2_ERR_INVALID_ARG;
+  if (n_rows == 0) return CSA2_OK;
+  if (!scores || !n_valid || !idx_out || ld < 0) return CSA2_ERR_INVALID_ARG;
+  for (int r = 0; r < n_rows; ++r)
+    if (n_valid[r] < 0 || n_valid[r] > ld || n_valid[r] > (int64_t)INT32_MAX)
+      return CSA2_ERR_INVALID_ARG;
+  for (int r0 = 0; r0 < n_rows; r0 += kTopkTab) {
+    const int nr = std::min(kTopkTab, n_rows - r0);
+    TopkParams* p = new (std::nothrow) TopkParams();
+    if (!p) return CSA2_ERR_OOM;
+    p->scores = scores + (int64_t)r0 * ld;
+    p->ld = ld;
+    p->rows = nr;
+    p->k = k;
+    p->idx_out = idx_out + (int64_t)r0 * k;
+    p->score_out = score_out ? score_out + (int64_t)r0 * k : nullptr;
+    p->formula = 0;
+    for (int r = 0; r < nr; ++r) p->n_valid[r] = n_valid[r0 + r];
+    cudaError_t e = launch_topk(*p, S(stream));
+    delete p;
+    if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  }
+  return CSA2_OK;
+}
+
+csa2_status_t csa2_index_topk_decode(const csa2_cache_t* c, int32_t nq, const void* q_idx,
+                                     const float* w, const int32_t* seq_ids, int32_t* topk_idx,
+                                     float* topk_score, void* workspace, size_t ws_bytes,
+                                     csa2_stream_t stream) {
+  if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
+  if (nq == 0) return CSA2_OK;
+  if (!q_idx || !w || !topk_idx || !workspace || !aligned16(q_idx) || !aligned16(w) ||
+      !aligned16(workspace))
+    return CSA2_ERR_INVALID_ARG;
+  if (ws_bytes < csa2_index_workspace_bytes(c, nq)) return CSA2_ERR_CAPACITY;
+  if (seq_ids)
+    for (int i = 0; i < nq; ++i)
+      if (seq_ids[i] < 0 || seq_ids[i] >= c->batch) return CSA2_ERR_INVALID_ARG;
+  const int64_t ld = score_ld(c->max_cap);
+  float* scores = static_cast<float*>(workspace);
+  const int k = c->cfg.topk;
+  const uint16_t* qb = static_cast<const uint16_t*>(q_idx);
+
+  IndexParams* ip = new (std::nothrow) IndexParams();
+  TopkParams* tp = new (std::nothrow) TopkParams();
+  if (!ip || !tp) { delete ip; delete tp; return CSA2_ERR_OOM; }
+  csa2_status_t st = CSA2_OK;
+  for (int q0 = 0; q0 < nq && st == CSA2_OK; q0 += kMaxIdxGroups) {
+    const int n = std::min(kMaxIdxGroups, nq - q0);
+    std::memset(ip, 0, sizeof(IndexParams));
+    ip->w = w + (int64_t)q0 * kIdxHeads;
+    ip->scores = scores + (int64_t)q0 * ld;
+    ip->ld = ld;
+    ip->err = c->d_err;
+    ip->nq = n;
+    ip->qpg = 1;
+    ip->n_groups = n;
+    ip->prefill = 0;
+    ip->ratio = c->cfg.ratio;
+    ip->tile_prefix[0] = 0;
+    std::memset(tp, 0, sizeof(TopkParams));
+    for (int i = 0; i < n; ++i) {
+      const int s = seq_ids ? seq_ids[q0 + i] : q0 + i;
+      if (s >= c->batch) { st = CSA2_ERR_INVALID_ARG; break; }
+      const int64_t nv = c->len[s];
+      ip->entry_base[i] = c->off[s];
+      ip->nvis[i] = (int32_t)nv;
+      ip->tile_prefix[i + 1] = ip->tile_prefix[i] + (int32_t)((nv + 127) / 128);
+      tp->n_valid[i] = nv;
+    }
+    if (st != CSA2_OK) break;
+    CUtensorMap tm_q;
+    if (!make_map(&tm_q, qb + (int64_t)q0 * kIdxHeads * kIdxDim, (uint64_t)n * kIdxHeads,
+                  kIdxDim, 64, 32)) {
+      st = CSA2_ERR_CUDA;
+      break;
+    }
+    const int tiles = ip->tile_prefix[n];
+    if (tiles > 0) {
+      const int grid = std::min(c->num_sms, tiles);
+      if (launch_index(*ip, c->tm_k, tm_q, grid, S(stream)) != cudaSuccess) {
+        st = CSA2_ERR_CUDA;
+        break;
+      }
+    }
+    tp->scores = ip->scores;
+    tp->ld = ld;
+    tp->rows = n;
+    tp->k = k;
+    tp->idx_out = topk_idx + (int64_t)q0 * k;
+    tp->score_out = topk_score ? topk_score + (int64_t)q0 * k : nullptr;
+    tp->formula = 0;
+    if (launch_topk(*tp, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
+  }
+  delete ip;
+  delete tp;
+  return st;
+}
+
+csa2_status_t csa2_index_topk_prefill(const csa2_cache_t* c, int32_t seq, int32_t nq, int64_t pos0,
+                                      const void* q_idx, const float* w, int32_t* topk_idx,
+                                      float* topk_score, void* workspace, size_t ws_bytes,
+                                      csa2_stream_t stream) {
+  if (!c || nq < 0 || seq < 0 || seq >= c->batch || pos0 < 0) return CSA2_ERR_INVALID_ARG;
+  if (nq == 0) return CSA2_OK;
+  if (!q_idx || !w || !topk_idx || !workspace || !aligned16(q_idx) || !aligned16(w) ||
+      !aligned16(workspace))
+    return CSA2_ERR_INVALID_ARG;
+  const int64_t ld = score_ld(c->cap[seq]);
+  if (ws_bytes < (size_t)nq * (size_t)ld * sizeof(float)) return CSA2_ERR_CAPACITY;
+  constexpr int kQpg = 8;
+  const int m = c->cfg.ratio;
+  const int64_t len = c->len[seq];
+  float* scores = static_cast<float*>(workspace);
+  const int k = c->cfg.topk;
+  const uint16_t* qb = static_cast<const uint16_t*>(q_idx);
+  IndexParams* ip = new (std::nothrow) IndexParams();
+  TopkParams* tp = new (std::nothrow) TopkParams();
+  if (!ip || !tp) { delete ip; delete tp; return CSA2_ERR_OOM; }
+  csa2_status_t st = CSA2_OK;
+  const int per_launch = kMaxIdxGroups * kQpg;
+  for (int q0 = 0; q0 < nq && st == CSA2_OK; q0 += per_launch) {
+    const int n = std::min(per_launch, nq - q0);
+    const int groups = (n + kQpg - 1) / kQpg;
+    std::memset(ip, 0, sizeof(IndexParams));
+    ip->w = w + (int64_t)q0 * kIdxHeads;
+    ip->scores = scores + (int64_t)q0 * ld;
+    ip->ld = ld;
+    ip->err = c->d_err;
+    ip->nq = n;
+    ip->qpg = kQpg;
+    ip->n_groups = groups;
+    ip->prefill = 1;
+    ip->pre_base = c->off[seq];
+    ip->pos0 = pos0 + q0;
+    ip->pre_len = (int32_t)len;
+    ip->ratio = m;
+    ip->tile_prefix[0] = 0;
+    for (int g = 0; g < groups; ++g) {
+      const int64_t last = std::min<int64_t>((int64_t)g * kQpg + kQpg, n) - 1;
+      const int64_t nv = std::min<int64_t>(len, (ip->pos0 + last + 1) / m);
+      ip->tile_prefix[g + 1] = ip->tile_prefix[g] + (int32_t)((nv + 127) / 128);
+    }
+    CUtensorMap tm_q;
+    if (!make_map(&tm_q, qb + (int64_t)q0 * kIdxHeads * kIdxDim, (uint64_t)n * kIdxHeads,
+                  kIdxDim, 64, 32 * kQpg)) {
+      st = CSA2_ERR_CUDA;
+      break;
+    }
+    const int tiles = ip->tile_prefix[groups];
+    if (tiles > 0) {
+      const int grid = std::min(c->num_sms, tiles);
+      if (launch_index(*ip, c->tm_k, tm_q, grid, S(stream)) != cudaSuccess) {
+        st = CSA2_ERR_CUDA;
+        break;
+      }
+    }
+    std::memset(tp, 0, sizeof(TopkParams));
+    tp->scores = ip->scores;
+    tp->ld = ld;
+    tp->rows = n;
+    tp->k = k;
+    tp->idx_out = topk_idx + (int64_t)q0 * k;
+    tp->score_out = topk_score ? topk_score + (int64_t)q0 * k : nullptr;
+    tp->formula = 1;
+    tp->pre_len = (int32_t)len;
+    tp->ratio = m;
+    tp->pos0 = pos0 + q0;
+    if (launch_topk(*tp, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
+  }
+  delete ip;
+  delete tp;
+  return st;
+}
+
+csa2_status_t csa2_sparse_attn_decode(const csa2_cache_t* c, int32_t nq, const int32_t* seq_ids,
+                                      const void* q, const void* swa_kv, const int32_t* swa_len,
+                                      const int32_t* topk_idx, float scale, void* out, float* lse,
+                                      csa2_stream_t stream) {
+  if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
+  if (nq == 0) return CSA2_OK;
+  const int W = c->cfg.swa;
+  if (!q || !topk_idx || !out || !aligned16(q) || !aligned16(out) || !aligned16(topk_idx))
+    return CSA2_ERR_INVALID_ARG;
+  if (W > 0 && (!swa_kv || !aligned16(swa_kv))) return CSA2_ERR_INVALID_ARG;
+  if (lse && !aligned16(lse)) return CSA2_ERR_INVALID_ARG;
+  if (seq_ids)
+    for (int i = 0; i < nq; ++i)
+      if (seq_ids[i] < 0 || seq_ids[i] >= c->batch) return CSA2_ERR_INVALID_ARG;
+  if (!seq_ids && nq > c->batch) return CSA2_ERR_INVALID_ARG;
+  const int H = c->cfg.n_heads, k = c->cfg.topk;
+  AttnParams* p = new (std::nothrow) AttnParams();
+  if (!p) return CSA2_ERR_OOM;
+  csa2_status_t st = CSA2_OK;
+  for (int q0 = 0; q0 < nq; q0 += kAttnTab) {
+    const int n = std::min(kAttnTab, nq - q0);
+    std::memset(p, 0, sizeof(AttnParams));
+    p->topk_idx = topk_idx + (int64_t)q0 * k;
+    p->swa_len = swa_len ? swa_len + q0 : nullptr;
+    p->codes = c->codes;
+    p->scales = c->scales;
+    p->out = static_cast<uint16_t*>(out) + (int64_t)q0 * H * kHeadDim;
+    p->lse = lse ? lse + (int64_t)q0 * H : nullptr;
+    p->err = c->d_err;
+    p->nq = n;
+    p->n_heads = H;
+    p->topk = k;
+    p->swa = W;
+    p->layout = c->cfg.layout;
+    p->scale = scale;
+    p->scale_log2 = scale * 1.4426950408889634f;
+    p->prefill = 0;
+    for (int i = 0; i < n; ++i) {
+      const int s = seq_ids ? seq_ids[q0 + i] : q0 + i;
+      p->q_base[i] = c->off[s];
+      p->q_len[i] = (int32_t)c->len[s];
+    }
+    CUtensorMap tm_q, tm_swa;
+    const uint16_t* qb = static_cast<const uint16_t*>(q) + (int64_t)q0 * H * kHeadDim;
+    if (!make_map(&tm_q, qb, (uint64_t)n * H, kHeadDim, 64, 32)) { st = CSA2_ERR_CUDA; break; }
+    if (W > 0) {
+      const uint16_t* sb = static_cast<const uint16_t*>(swa_kv) + (int64_t)q0 * W * kHeadDim;
+      if (!make_map(&tm_swa, sb, (uint64_t)n * W, kHeadDim, 64, 128)) { st = CSA2_ERR_CUDA; break; }
+    } else {
+      tm_swa = tm_q;
+    }
+    if (launch_attn(*p, tm_q, tm_swa, S(stream)) != cudaSuccess) { st = CSA2_ERR_CUDA; break; }
+  }
+  delete p;
+  return st;
+}
+
+csa2_status_t csa2_sparse_attn_prefill(const csa2_cache_t* c, int32_t seq, int32_t nq,
+                                       int64_t pos0, const void* q, const void* swa_kv,
+                                       int64_t swa_pos0, int64_t n_swa_rows,
+                                       const int32_t* topk_idx, float scale, void* out, float* lse,
+                                       csa2_stream_t stream) {
+  if (!c || nq < 0 || seq < 0 || seq >= c->batch || pos0 < 0) return CSA2_ERR_INVALID_ARG;
+  if (nq == 0) return CSA2_OK;
+  const int W = c->cfg.swa;
+  if (!q || !topk_idx || !out || !aligned16(q) || !aligned16(out) || !aligned16(topk_idx))
+    return CSA2_ERR_INVALID_ARG;
+  if (lse && !aligned16(lse)) return CSA2_ERR_INVALID_ARG;
+  if (W > 0) {
+    if (!swa_kv || !aligned16(swa_kv) || swa_pos0 < 0 || swa_pos0 > pos0 || n_swa_rows <= 0 ||
+        pos0 + nq - 1 - swa_pos0 >= n_swa_rows)
+      return CSA2_ERR_INVALID_ARG;
+  }
+  const int H = c->cfg.n_heads, k = c->cfg.topk;
+  AttnParams* p = new (std::nothrow) AttnParams();
+  if (!p) return CSA2_ERR_OOM;
+  std::memset(p, 0, sizeof(AttnParams));
+  p->topk_idx = topk_idx;
+  p->codes = c->codes;
+  p->scales = c->scales;
+  p->out = static_cast<uint16_t*>(out);
+  p->lse = lse;
+  p->err = c->d_err;
+  p->nq = nq;
+  p->n_heads = H;
+  p->topk = k;
+  p->swa = W;
+  p->layout = c->cfg.layout;
+  p->scale = scale;
+  p->scale_log2 = scale * 1.4426950408889634f;
+  p->prefill = 1;
+  p->pre_base = c->off[seq];
+  p->pre_len = (int32_t)c->len[seq];
+  p->pos0 = pos0;
+  p->swa_pos0 = swa_pos0;
+  csa2_status_t st = CSA2_OK;
+  CUtensorMap tm_q, tm_swa;
+  if (!make_map(&tm_q, q, (uint64_t)nq * H, kHeadDim, 64, 32)) st = CSA2_ERR_CUDA;
+  if (st == CSA2_OK) {
+    if (W > 0) {
+      if (!make_map(&tm_swa, swa_kv, (uint64_t)n_swa_rows, kHeadDim, 64, 128)) st = CSA2_ERR_CUDA;
+    } else {
+      tm_swa = tm_q;
+    }
+  }
+  if (st == CSA2_OK && launch_attn(*p, tm_q, tm_swa, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
+  delete p;
+  return st;
+}
+
+csa2_status_t csa2_get_device_error(const csa2_cache_t* c, csa2_stream_t stream,
+                                    int32_t* device_status) {
+  if (!c || !device_status) return CSA2_ERR_INVALID_ARG;
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, c->d_err, sizeof(word), cudaMemcpyDeviceToHost, S(stream)) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(S(stream)) != cudaSuccess)
+    return CSA2_ERR_CUDA;
+  if (word && cudaMemsetAsync(c->d_err, 0, sizeof(uint32_t), S(stream)) != cudaSuccess)
+    return CSA2_ERR_CUDA;
+  *device_status = (word & kErrTimeoutBit) ? CSA2_ERR_TIMEOUT
+                   : (word & kErrIndexBit) ? CSA2_ERR_DEVICE
+                                           : CSA2_OK;
+  return CSA2_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,119 @@
+// csa2_kernels.h -- host-side launch interface between the C ABI layer
+// (csa2_api.cu) and the kernel translation units.  Internal to the library.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace csa2 {
+
+// Sticky device error word bits (see csa2_get_device_error).
+constexpr uint32_t kErrTimeoutBit = 1u;
+constexpr uint32_t kErrIndexBit = 2u;
+
+constexpr int kHeadDim = 512;     // main-KV latent / attention head dim
+constexpr int kIdxDim = 128;      // indexer head dim
+constexpr int kIdxHeads = 32;     // indexer heads
+constexpr int kCodeBytes = kHeadDim / 2;
+
+// ---------------------------------------------------------------- append
+constexpr int kMaxAppendSegs = 64;
+struct AppendSeg {
+  int64_t first;     // first output row of this segment within the launch
+  int64_t src_row;   // first input entry row (entries mode) or entry-block row
+  int64_t dst_row;   // first cache row
+  int32_t seq;
+  int32_t new_len;   // sequence length after the append
+};
+struct AppendParams {
+  int32_t mode;      // 0 compress only, 1 append entries, 2 append tokens
+  int32_t ratio;
+  int32_t layout;    // 0 = L32_UE8M0, 1 = L16_E4M3
+  int32_t dim;       // channels (compress-only may differ from kHeadDim)
+  int32_t n_segs;
+  int64_t rows;      // output rows in this launch
+  AppendSeg seg[kMaxAppendSegs];
+  const float* entries;
+  const uint16_t* c_tok;
+  const float* z_tok;
+  const uint16_t* idx_k;
+  float* entries_out;
+  uint8_t* codes;
+  uint8_t* scales;
+  uint16_t* cache_idxk;
+  int32_t* d_len;
+};
+cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
+
+// ---------------------------------------------------------------- indexer
+constexpr int kMaxIdxGroups = 1024;
+struct IndexParams {
+  const float* w;          // [nq, 32]
+  float* scores;           // [nq, ld]
+  int64_t ld;
+  uint32_t* err;
+  int32_t nq;
+  int32_t qpg;             // queries per group (1 decode, 8 prefill)
+  int32_t n_groups;
+  int32_t prefill;         // 1: visibility from positions
+  int64_t pre_base;        // prefill: entry offset of the sequence
+  int64_t pos0;            // prefill: position of query 0
+  int32_t pre_len;         // prefill: entries in the sequence
+  int32_t ratio;
+  int32_t tile_prefix[kMaxIdxGroups + 1];  // cumulative 128-entry tiles per group
+  int64_t entry_base[kMaxIdxGroups];       // decode: entry offset of the group's sequence
+  int32_t nvis[kMaxIdxGroups];             // decode: visible entries of the group's query
+};
+int index_smem_bytes(int qpg);
+cudaError_t launch_index(const IndexParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_q,
+                         int grid, cudaStream_t s);
+
+// ---------------------------------------------------------------- top-k
+constexpr int kTopkMaxRowsPerLaunch = 65535;
+constexpr int kTopkTab = 1024;
+struct TopkParams {
+  const float* scores;       // row r at scores + r * ld
+  int64_t ld;
+  int32_t rows;
+  int32_t k;
+  int32_t* idx_out;          // [rows, k]
+  float* score_out;          // nullable [rows, k]
+  int32_t formula;           // 1: n_valid(r) = min(len, (pos0 + r + 1) / ratio)
+  int32_t pre_len;
+  int32_t ratio;
+  int64_t pos0;
+  int64_t n_valid[kTopkTab]; // formula == 0: per-row valid counts
+};
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
+
+// ---------------------------------------------------------------- attention
+constexpr int kAttnTab = 1024;
+struct AttnParams {
+  const int32_t* topk_idx;   // [nq, topk]
+  const int32_t* swa_len;    // decode: nullable [nq]
+  const uint8_t* codes;
+  const uint8_t* scales;
+  uint16_t* out;             // bf16 [nq, n_heads, 512]
+  float* lse;                // nullable [nq, n_heads]
+  uint32_t* err;
+  int32_t nq;
+  int32_t n_heads;
+  int32_t topk;
+  int32_t swa;               // window size W
+  int32_t layout;
+  float scale_log2;          // scale * log2(e)
+  float scale;
+  int32_t prefill;
+  int64_t pre_base;          // prefill: entry offset of the sequence
+  int32_t pre_len;           // prefill: entries in the sequence
+  int64_t pos0;              // prefill: position of query 0
+  int64_t swa_pos0;          // prefill: position of swa row 0
+  int64_t q_base[kAttnTab];  // decode: entry offset of each query's sequence
+  int32_t q_len[kAttnTab];   // decode: entries of each query's sequence
+};
+int attn_smem_bytes();
+cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_swa,
+                        cudaStream_t s);
+
+}  // namespace csa2

@@ -1,0 +1,445 @@
+// k_attn.cu -- CSA2 sparse shared-KV attention over FP4 cache entries plus
+// the sliding window, one joint softmax.
+//
+// Method: the selected compressed entries are both key and value (blog
+// reading of the DeepSeek-V4 report, section 4.1, "shared key-value MQA");
+// the window rows join the same softmax (same blog, section 4.3; neshdevtech
+// article section 3.3.1, "readout concatenates the SWA and the selected main
+// KV into a single joint sparse attention"); entries are dequantised from
+// FP4 before attention (V4.1 report, section 2.4.4).
+//
+// One CTA = one query x 32 heads.  Candidates come in tiles of 128 rows: the
+// window tile (TMA straight into swizzled shared memory) and the top-k tiles
+// (cp.async gather of 256 B codes + scales per entry, one tile ahead, then
+// E2M1 -> bf16 via byte permutes and a bf16 scale multiply).  With the
+// candidate rows as the MMA M dimension:
+//     S^T[128 x 32]  = KV[128 x 512] * Q[32 x 512]^T        (K-major A and B)
+//     O^T[512 x 32] += KV^T[512 x 128] * P^T[128 x 32]^T     (MN-major A)
+// both on tcgen05 with fp32 accumulators in TMEM; the same swizzled KV tile
+// serves as the K-major A of the first product and the MN-major A of the
+// second.  Online softmax (base 2) runs across TMEM lanes: each thread holds
+// one candidate row, per-head maxima and sums use a warp reduce-scatter and a
+// 4-way combine through shared memory; O^T is rescaled in TMEM when a
+// head's running maximum grows.
+#include "csa2_device.cuh"
+#include "csa2_kernels.h"
+
+namespace csa2 {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kHG = 32;               // heads per CTA
+constexpr int kRows = 128;            // candidates per tile
+constexpr int kStageStride = 272;     // padded staging row for 256 B of codes
+constexpr int kMaxTiles = 2048 / kRows + 1;
+
+// shared memory map (offsets from a 1024-aligned base)
+constexpr int kKvOff = 0;                              // 8 x [128 x 128 B]
+constexpr int kQOff = kKvOff + kRows * kHeadDim * 2;   // 8 x [32 x 128 B]
+constexpr int kPOff = kQOff + kHG * kHeadDim * 2;      // 2 x [32 x 128 B]
+constexpr int kStCodesOff = kPOff + kHG * kRows * 2;
+constexpr int kStScalesOff = kStCodesOff + kRows * kStageStride;
+constexpr int kSmallOff = kStScalesOff + kRows * 32;
+struct Small {
+  float red_max[4][kHG];
+  float red_sum[4][kHG];
+  float m[kHG];
+  float l[kHG];
+  float alpha[kHG];
+  int32_t tile_list[kMaxTiles];
+  int32_t tile_any[kMaxTiles];
+  uint8_t row_valid[kRows];
+  int32_t n_tiles;
+  int32_t need_rescale;
+  uint32_t tmem;
+  uint64_t bar_q, bar_kv, bar_mma;
+};
+constexpr int kSmemBytes = kSmallOff + (int)sizeof(Small) + 1024;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Reduce-scatter over the 32 lanes of a warp: v[0..15] (16 heads) in, lane L
+// ends with the reduction for head (L >> 1) in v[0].
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce_scatter16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool up = lane & 16;
+    const float send = up ? v[i] : v[i + 8];
+    const float keep = up ? v[i + 8] : v[i];
+    const float r = __shfl_xor_sync(0xffffffffu, send, 16);
+    v[i] = kMax ? fmaxf(keep, r) : keep + r;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const bool up = lane & 8;
+    const float send = up ? v[i] : v[i + 4];
+    const float keep = up ? v[i + 4] : v[i];
+    const float r = __shfl_xor_sync(0xffffffffu, send, 8);
+    v[i] = kMax ? fmaxf(keep, r) : keep + r;
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const bool up = lane & 4;
+    const float send = up ? v[i] : v[i + 2];
+    const float keep = up ? v[i + 2] : v[i];
+    const float r = __shfl_xor_sync(0xffffffffu, send, 4);
+    v[i] = kMax ? fmaxf(keep, r) : keep + r;
+  }
+  {
+    const bool up = lane & 2;
+    const float send = up ? v[0] : v[1];
+    const float keep = up ? v[1] : v[0];
+    const float r = __shfl_xor_sync(0xffffffffu, send, 2);
+    v[0] = kMax ? fmaxf(keep, r) : keep + r;
+  }
+  const float r = __shfl_xor_sync(0xffffffffu, v[0], 1);
+  return kMax ? fmaxf(v[0], r) : v[0] + r;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_attn(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_q,
+           const __grid_constant__ CUtensorMap tm_swa) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* kv = smem + kKvOff;
+  uint8_t* qs = smem + kQOff;
+  uint8_t* ps = smem + kPOff;
+  uint8_t* st_codes = smem + kStCodesOff;
+  uint8_t* st_scales = smem + kStScalesOff;
+  Small& sm = *reinterpret_cast<Small*>(smem + kSmallOff);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hgs = p.n_heads / kHG;
+  const int q = blockIdx.x / hgs, hg = blockIdx.x % hgs;
+  const int n_topk_tiles = p.topk / kRows;
+  const int32_t* idx_row = p.topk_idx + (int64_t)q * p.topk;
+
+  // ---- per-query geometry
+  int64_t base;
+  int32_t len;
+  int32_t swa_row0, swa_count;
+  if (p.prefill) {
+    base = p.pre_base;
+    len = p.pre_len;
+    const int64_t pos = p.pos0 + q;
+    const int64_t lo = (pos - p.swa + 1 > p.swa_pos0) ? pos - p.swa + 1 : p.swa_pos0;
+    swa_row0 = (int32_t)(lo - p.swa_pos0);
+    swa_count = (p.swa > 0) ? (int32_t)(pos - lo + 1) : 0;
+  } else {
+    base = p.q_base[q];
+    len = p.q_len[q];
+    swa_row0 = q * p.swa;
+    int32_t c = p.swa_len ? p.swa_len[q] : p.swa;
+    swa_count = c < 0 ? 0 : (c > p.swa ? p.swa : c);
+  }
+
+  if (tid == 0) {
+    mbar_init(&sm.bar_q, 1);
+    mbar_init(&sm.bar_kv, 1);
+    mbar_init(&sm.bar_mma, 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_swa);
+  }
+  if (tid < kMaxTiles) sm.tile_any[tid] = 0;
+  if (tid < kHG) { sm.m[tid] = -INFINITY; sm.l[tid] = 0.0f; }
+  if (warp == 0) { tmem_alloc(&sm.tmem, 256); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem;
+  const uint32_t s_col = 0, o_col = 32;
+
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&sm.bar_q, kHG * kHeadDim * 2);
+    for (int c = 0; c < 8; ++c)
+      tma_load_2d(qs + c * (kHG * 128), &tm_q, 64 * c, q * p.n_heads + hg * kHG, &sm.bar_q);
+  }
+  // which top-k tiles hold at least one usable index
+  bool bad = false;
+  for (int i = tid; i < p.topk; i += kThreads) {
+    const int32_t s = idx_row[i];
+    if (s >= 0 && s < len) sm.tile_any[i / kRows] = 1;
+    else if (s >= len) bad = true;
+  }
+  if (bad) set_error(p.err, kErrIndex);
+  __syncthreads();
+  if (tid == 0) {
+    int n = 0;
+    if (swa_count > 0) sm.tile_list[n++] = -1;
+    for (int j = 0; j < n_topk_tiles; ++j)
+      if (sm.tile_any[j]) sm.tile_list[n++] = j;
+    sm.n_tiles = n;
+  }
+  __syncthreads();
+  const int n_tiles = sm.n_tiles;
+
+  // gather of one top-k tile into the staging buffers (zero-fill for unused slots)
+  auto stage_tile = [&](int j) {
+    const int e = tid >> 1, half = tid & 1;
+    const int32_t s = idx_row[j * kRows + e];
+    const bool ok = (s >= 0 && s < len);
+    const int64_t row = ok ? base + s : 0;
+    const uint8_t* src = p.codes + row * kCodeBytes + half * 128;
+    const uint32_t dst = smem_u32(st_codes + e * kStageStride + half * 128);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) cp_async16(dst + 16 * c, src + 16 * c, ok ? 16u : 0u);
+    const int sbytes = (p.layout == 0) ? 16 : 32;
+    if (half * 16 < sbytes)
+      cp_async16(smem_u32(st_scales + e * 32 + half * 16),
+                 p.scales + row * sbytes + half * 16, ok ? 16u : 0u);
+    cp_async_commit();
+  };
+
+  int next_topk = 0;  // position in tile_list of the next tile to stage
+  while (next_topk < n_tiles && sm.tile_list[next_topk] < 0) ++next_topk;
+  if (next_topk < n_tiles) stage_tile(sm.tile_list[next_topk]);
+
+  uint32_t mma_phase = 0;
+  bool ok = true;
+  const int quad = warp & 3, hh = warp >> 2;
+  const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+
+  for (int ti = 0; ti < n_tiles && ok; ++ti) {
+    const int tile = sm.tile_list[ti];
+    if (tid == 0) sm.need_rescale = 0;
+    // ------------------------------------------------ A: candidate rows -> kv
+    if (tile < 0) {
+      if (tid == 0) {
+        mbar_arrive_expect_tx(&sm.bar_kv, kRows * kHeadDim * 2);
+        for (int c = 0; c < 8; ++c)
+          tma_load_2d(kv + c * (kRows * 128), &tm_swa, 64 * c, swa_row0, &sm.bar_kv);
+      }
+      if (tid < kRows) sm.row_valid[tid] = tid < swa_count;
+      ok = mbar_wait(&sm.bar_kv, 0, p.err);
+      ok = __syncthreads_and(ok);
+      if (!ok) break;
+    } else {
+      cp_async_wait_all();
+      __syncthreads();
+      if (tid < kRows) {
+        const int32_t s = idx_row[tile * kRows + tid];
+        sm.row_valid[tid] = (s >= 0 && s < len);
+      }
+      // dequantise: warp w owns entries [16 w, 16 w + 16)
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        const int e = warp * 16 + half * 8 + (lane & 7);
+#pragma unroll 2
+        for (int round = 0; round < 8; ++round) {
+          const int j = round * 4 + (lane >> 3);  // 16-channel group
+          const uint2 c = *reinterpret_cast<const uint2*>(st_codes + e * kStageStride + j * 8);
+          uint32_t sb;
+          float sf;
+          if (p.layout == 0) {
+            sb = st_scales[e * 32 + (j >> 1)];
+            sf = ue8m0_value(sb);
+          } else {
+            sb = st_scales[e * 32 + j];
+            sf = fabsf(e4m3_value(sb));
+          }
+          const uint32_t s16 = float_to_bf16_bits(sf);
+          const uint32_t s2 = s16 | (s16 << 16);
+          uint32_t lo[4], hi[4];
+          e2m1x8_to_bf16x8(c.x, lo);
+          e2m1x8_to_bf16x8(c.y, hi);
+          uint4 w0, w1;
+          w0.x = bf16x2_mul(lo[0], s2); w0.y = bf16x2_mul(lo[1], s2);
+          w0.z = bf16x2_mul(lo[2], s2); w0.w = bf16x2_mul(lo[3], s2);
+          w1.x = bf16x2_mul(hi[0], s2); w1.y = bf16x2_mul(hi[1], s2);
+          w1.z = bf16x2_mul(hi[2], s2); w1.w = bf16x2_mul(hi[3], s2);
+          const int cb = j >> 2, ch = 2 * (j & 3);
+          uint8_t* rowp = kv + cb * (kRows * 128) + e * 128;
+          *reinterpret_cast<uint4*>(rowp + (((ch) ^ (e & 7)) << 4)) = w0;
+          *reinterpret_cast<uint4*>(rowp + (((ch + 1) ^ (e & 7)) << 4)) = w1;
+        }
+      }
+      __syncthreads();
+      // staging is free again: fetch the next top-k tile behind this one
+      ++next_topk;
+      while (next_topk < n_tiles && sm.tile_list[next_topk] < 0) ++next_topk;
+      if (next_topk < n_tiles) stage_tile(sm.tile_list[next_topk]);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    // ------------------------------------------------ B: S^T = KV * Q^T
+    if (tid == 0) {
+      if (ti == 0) ok = mbar_wait(&sm.bar_q, 0, p.err);
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16_f32(128, kHG, false, false);
+      const uint32_t a0 = smem_u32(kv), b0 = smem_u32(qs);
+#pragma unroll 4
+      for (int ks = 0; ks < kHeadDim / 16; ++ks) {
+        const uint32_t ao = (uint32_t)((ks >> 2) * (kRows * 128) + (ks & 3) * 32);
+        const uint32_t bo = (uint32_t)((ks >> 2) * (kHG * 128) + (ks & 3) * 32);
+        umma_bf16(tmem + s_col, sdesc_sw128(a0 + ao, 16, 1024), sdesc_sw128(b0 + bo, 16, 1024),
+                  idesc, ks > 0 ? 1u : 0u);
+      }
+      umma_commit(&sm.bar_mma);
+    }
+    ok = mbar_wait(&sm.bar_mma, mma_phase, p.err) && ok;
+    mma_phase ^= 1;
+    ok = __syncthreads_and(ok);
+    if (!ok) break;
+    tc_fence_after();
+
+    // ------------------------------------------------ C: online softmax
+    const int row = quad * 32 + lane;
+    const bool valid = sm.row_valid[row] != 0;
+    float x[16], v[16];
+    {
+      uint32_t r[16];
+      tmem_ld16(tmem + lane_addr + s_col + 16 * hh, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        x[i] = valid ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
+        v[i] = x[i];
+      }
+    }
+    {
+      const float mx = warp_reduce_scatter16<true>(v, lane);
+      if ((lane & 1) == 0) sm.red_max[quad][16 * hh + (lane >> 1)] = mx;
+    }
+    __syncthreads();
+    if (tid < kHG) {
+      const float tmax = fmaxf(fmaxf(sm.red_max[0][tid], sm.red_max[1][tid]),
+                               fmaxf(sm.red_max[2][tid], sm.red_max[3][tid]));
+      const float mo = sm.m[tid];
+      const float mn = fmaxf(mo, tmax);
+      const float a = (mn == -INFINITY) ? 1.0f : fast_exp2(mo - mn);
+      sm.m[tid] = mn;
+      sm.alpha[tid] = a;
+      if (a != 1.0f && ti > 0) sm.need_rescale = 1;
+    }
+    __syncthreads();
+    {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int h = 16 * hh + i;
+        const float pr = (x[i] == -INFINITY) ? 0.0f : fast_exp2(x[i] - sm.m[h]);
+        const uint32_t pb = float_to_bf16_bits(pr);
+        v[i] = bf16_bits_to_float(pb);
+        // P^T is the K-major B operand: row h, column = candidate row
+        uint8_t* prow = ps + (row >> 6) * (kHG * 128) + h * 128;
+        const int chunk = (row & 63) >> 3;
+        *reinterpret_cast<uint16_t*>(prow + ((chunk ^ (h & 7)) << 4) + (row & 7) * 2) =
+            (uint16_t)pb;
+      }
+      const float sum = warp_reduce_scatter16<false>(v, lane);
+      if ((lane & 1) == 0) sm.red_sum[quad][16 * hh + (lane >> 1)] = sum;
+    }
+    __syncthreads();
+    if (tid < kHG)
+      sm.l[tid] = sm.alpha[tid] * sm.l[tid] + ((sm.red_sum[0][tid] + sm.red_sum[1][tid]) +
+                                               (sm.red_sum[2][tid] + sm.red_sum[3][tid]));
+    if (sm.need_rescale) {
+      // O^T lanes are head-dim rows, columns are heads: scale column h by alpha[h]
+#pragma unroll 1
+      for (int i = 0; i < 4; ++i) {
+        uint32_t r[16];
+        const uint32_t a = tmem + lane_addr + o_col + 32 * i + 16 * hh;
+        tmem_ld16(a, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          r[c] = __float_as_uint(__uint_as_float(r[c]) * sm.alpha[16 * hh + c]);
+        tmem_st16(a, r);
+      }
+      tmem_wait_st();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // ------------------------------------------------ D: O^T += KV^T * P^T
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16_f32(128, kHG, true, false);
+      const uint32_t a0 = smem_u32(kv), b0 = smem_u32(ps);
+#pragma unroll 1
+      for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int ks = 0; ks < kRows / 16; ++ks) {
+          const uint32_t ao = (uint32_t)((2 * i) * (kRows * 128) + ks * 2048);
+          const uint32_t bo = (uint32_t)((ks >> 2) * (kHG * 128) + (ks & 3) * 32);
+          umma_bf16(tmem + o_col + 32 * i, sdesc_sw128(a0 + ao, kRows * 128, 1024),
+                    sdesc_sw128(b0 + bo, 16, 1024), idesc, (ti > 0 || ks > 0) ? 1u : 0u);
+        }
+      }
+      umma_commit(&sm.bar_mma);
+    }
+    ok = mbar_wait(&sm.bar_mma, mma_phase, p.err);
+    mma_phase ^= 1;
+    ok = __syncthreads_and(ok);
+    tc_fence_after();
+  }
+  cp_async_wait_all();
+
+  // ------------------------------------------------ epilogue
+  __syncthreads();
+  if (ok && n_tiles > 0) {
+    if (tid < kHG) {
+      const float l = sm.l[tid];
+      sm.alpha[tid] = l > 0.0f ? 1.0f / l : 0.0f;
+      if (p.lse)
+        p.lse[(int64_t)q * p.n_heads + hg * kHG + tid] =
+            l > 0.0f ? (sm.m[tid] + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int i = 0; i < 4; ++i) {
+      uint32_t r[16];
+      tmem_ld16(tmem + lane_addr + o_col + 32 * i + 16 * hh, r);
+      tmem_wait_ld();
+      const int d = 128 * i + quad * 32 + lane;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int h = hg * kHG + 16 * hh + c;
+        const float o = __uint_as_float(r[c]) * sm.alpha[16 * hh + c];
+        p.out[((int64_t)q * p.n_heads + h) * kHeadDim + d] = (uint16_t)float_to_bf16_bits(o);
+      }
+    }
+  } else if (n_tiles == 0) {
+    // no candidate at all: output 0, lse -inf
+    for (int i = tid; i < kHG * kHeadDim; i += kThreads)
+      p.out[((int64_t)q * p.n_heads + hg * kHG) * kHeadDim + i] = 0;
+    if (p.lse && tid < kHG) p.lse[(int64_t)q * p.n_heads + hg * kHG + tid] = -INFINITY;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+}  // namespace
+
+int attn_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_swa,
+                        cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int64_t blocks = (int64_t)p.nq * (p.n_heads / kHG);
+  if (blocks <= 0) return cudaSuccess;
+  k_attn<<<(unsigned)blocks, kThreads, kSmemBytes, s>>>(p, tm_q, tm_swa);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

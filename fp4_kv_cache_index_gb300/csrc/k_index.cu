@@ -1,0 +1,228 @@
+// k_index.cu -- CSA2 indexer scores on the 5th-generation tensor cores.
+//
+// Score (blog reading of the DeepSeek-V4 report, section 4.1, "lightning
+// indexer"; V4.1 report section 2.3 keeps the same indexer):
+//     I[q, s] = sum_h w[q, h] * ReLU(q_idx[q, h] . K_I[s])
+// with 32 heads of dim 128 (V4.1 report, section 4.2.1).
+//
+// Mapping: one MMA tile is D[128 entries x 32*qpg] = K_I[128 x 128] *
+// Q[32*qpg x 128]^T (M = 128 entries, N = heads of qpg queries, K = 128), bf16
+// operands from 128B-swizzled shared memory, fp32 accumulators in TMEM.  The
+// ReLU and the head-weighted sum run in the epilogue on the accumulator rows.
+// Decode uses qpg = 1 (each query reads its own sequence); prefill groups 8
+// consecutive queries of one sequence so that a K_I tile feeds 256 columns.
+//
+// Persistent CTAs walk a balanced contiguous range of (group, tile) items.
+// Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner),
+// warps 2-5 = epilogue (TMEM -> registers -> scores).  Every wait is bounded.
+#include "csa2_device.cuh"
+#include "csa2_kernels.h"
+
+namespace csa2 {
+namespace {
+
+constexpr int kTileE = 128;
+constexpr int kStages = 4;
+constexpr int kKStageBytes = kTileE * kIdxDim * 2;  // 32 KB
+constexpr int kThreads = 192;
+
+struct SmemLayout {
+  int q_off, w_off, bar_off, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int qpg) {
+  SmemLayout L;
+  L.q_off = kStages * kKStageBytes;
+  L.w_off = L.q_off + qpg * 32 * kIdxDim * 2;
+  L.bar_off = L.w_off + qpg * 32 * 4;
+  L.total = L.bar_off + 16 * 8 + 16 + 1024;  // barriers, tmem slot, alignment slack
+  return L;
+}
+
+__device__ __forceinline__ int group_nvis_query(const IndexParams& p, int g, int j) {
+  if (!p.prefill) return p.nvis[g];
+  const int64_t q = (int64_t)g * p.qpg + j;
+  const int64_t v = (p.pos0 + q + 1) / p.ratio;
+  return (int)(v < p.pre_len ? v : p.pre_len);
+}
+
+__device__ __forceinline__ int64_t group_base(const IndexParams& p, int g) {
+  return p.prefill ? p.pre_base : p.entry_base[g];
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_index(const __grid_constant__ IndexParams p, const __grid_constant__ CUtensorMap tm_k,
+            const __grid_constant__ CUtensorMap tm_q) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const SmemLayout L = smem_layout(p.qpg);
+  uint8_t* kbuf = smem;
+  uint8_t* qbuf = smem + L.q_off;
+  float* wbuf = reinterpret_cast<float*>(smem + L.w_off);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+  uint64_t* k_full = bars;              // [kStages]
+  uint64_t* k_empty = bars + 4;         // [kStages]
+  uint64_t* acc_full = bars + 8;        // [2]
+  uint64_t* acc_empty = bars + 10;      // [2]
+  uint64_t* q_full = bars + 12;
+  uint64_t* q_empty = bars + 13;
+  uint64_t* drain = bars + 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = 32 * p.qpg;               // MMA N (columns per accumulator)
+  const int qrows = 32 * p.qpg;
+  const uint32_t tmem_cols = (N * 2 <= 32) ? 32u : (uint32_t)(N * 2);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) { mbar_init(k_full + i, 1); mbar_init(k_empty + i, 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, 128); }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    mbar_init(drain, 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_q);
+  }
+  if (warp == 1) { tmem_alloc(tmem_slot, tmem_cols); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total = p.tile_prefix[p.n_groups];
+  const int begin = (int)(((int64_t)total * blockIdx.x) / gridDim.x);
+  const int end = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
+  int g0 = 0;
+  while (g0 < p.n_groups && p.tile_prefix[g0 + 1] <= begin) ++g0;
+
+  if (warp == 0 && lane == 0 && begin < end) {
+    // ------------------------------------------------ TMA producer
+    int g = g0, cur = -1, stage = 0;
+    uint32_t ph = 0, qph = 0;
+    uint32_t armed[kStages] = {0, 0, 0, 0};   // phase parity of each stage's last fill + 1
+    bool ok = true;
+    for (int it = begin; it < end && ok; ++it) {
+      while (p.tile_prefix[g + 1] <= it) ++g;
+      if (g != cur) {
+        ok = mbar_wait(q_empty, qph ^ 1, p.err);
+        qph ^= 1;
+        if (!ok) break;
+        mbar_arrive_expect_tx(q_full, (uint32_t)(qrows * kIdxDim * 2));
+        tma_load_2d(qbuf, &tm_q, 0, g * qrows, q_full);
+        tma_load_2d(qbuf + qrows * 128, &tm_q, 64, g * qrows, q_full);
+        cur = g;
+      }
+      ok = mbar_wait(k_empty + stage, ph ^ 1, p.err);
+      if (!ok) break;
+      const int t = it - p.tile_prefix[g];
+      const int64_t row = group_base(p, g) + (int64_t)t * kTileE;
+      uint8_t* dst = kbuf + stage * kKStageBytes;
+      mbar_arrive_expect_tx(k_full + stage, kKStageBytes);
+      tma_load_2d(dst, &tm_k, 0, (int32_t)row, k_full + stage);
+      tma_load_2d(dst + kKStageBytes / 2, &tm_k, 64, (int32_t)row, k_full + stage);
+      armed[stage] = ph + 1;
+      if (++stage == kStages) { stage = 0; ph ^= 1; }
+    }
+    // make sure no bulk copy is still writing into this CTA's shared memory
+    for (int s = 0; s < kStages; ++s)
+      if (armed[s]) mbar_wait(k_full + s, armed[s] - 1, p.err);
+    if (cur >= 0) mbar_wait(q_full, qph ^ 1, p.err);
+  } else if (warp == 1 && lane == 0 && begin < end) {
+    // ------------------------------------------------ MMA issuer
+    const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)N, false, false);
+    int g = g0, cur = -1, stage = 0, acc = 0;
+    uint32_t ph = 0, qph = 0, aph = 0;
+    bool ok = true;
+    for (int it = begin; it < end && ok; ++it) {
+      while (p.tile_prefix[g + 1] <= it) ++g;
+      if (g != cur) {
+        ok = mbar_wait(q_full, qph, p.err);
+        qph ^= 1;
+        if (!ok) break;
+        cur = g;
+      }
+      ok = mbar_wait(k_full + stage, ph, p.err) && mbar_wait(acc_empty + acc, aph ^ 1, p.err);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(kbuf + stage * kKStageBytes);
+      const uint32_t b0 = smem_u32(qbuf);
+      const uint32_t d = tmem_base + (uint32_t)(acc * N);
+#pragma unroll
+      for (int ks = 0; ks < kIdxDim / 16; ++ks) {
+        const uint32_t ao = (uint32_t)((ks >> 2) * (kKStageBytes / 2) + (ks & 3) * 32);
+        const uint32_t bo = (uint32_t)((ks >> 2) * (qrows * 128) + (ks & 3) * 32);
+        umma_bf16(d, sdesc_sw128(a0 + ao, 16, 1024), sdesc_sw128(b0 + bo, 16, 1024), idesc,
+                  ks > 0 ? 1u : 0u);
+      }
+      umma_commit(k_empty + stage);
+      umma_commit(acc_full + acc);
+      const bool last_of_group = (it + 1 == end) || (p.tile_prefix[g + 1] <= it + 1);
+      if (last_of_group) umma_commit(q_empty);
+      if (++stage == kStages) { stage = 0; ph ^= 1; }
+      if (++acc == 2) { acc = 0; aph ^= 1; }
+    }
+    umma_commit(drain);
+    mbar_wait(drain, 0, p.err);
+  } else if (warp >= 2) {
+    // ------------------------------------------------ epilogue
+    const int quad = warp & 3;                 // TMEM lane quadrant of this warp
+    const int row = quad * 32 + lane;          // entry within the tile
+    const int et = threadIdx.x - 64;           // 0..127
+    int g = g0, cur = -1, acc = 0;
+    uint32_t aph = 0;
+    for (int it = begin; it < end; ++it) {
+      while (p.tile_prefix[g + 1] <= it) ++g;
+      if (g != cur) {
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        for (int i = et; i < qrows; i += 128) {
+          const int q = g * p.qpg + (i >> 5);
+          wbuf[i] = (q < p.nq) ? __ldg(p.w + (int64_t)q * kIdxHeads + (i & 31)) : 0.0f;
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        cur = g;
+      }
+      if (!mbar_wait(acc_full + acc, aph, p.err)) break;
+      tc_fence_after();
+      const int t = it - p.tile_prefix[g];
+      const int e = t * kTileE + row;
+      for (int j = 0; j < p.qpg; ++j) {
+        uint32_t r[32];
+        tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * N + j * 32), r);
+        tmem_wait_ld();
+        const float* wj = wbuf + j * 32;
+        float s = 0.0f;
+#pragma unroll
+        for (int h = 0; h < 32; ++h) s = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.0f), s);
+        const int q = g * p.qpg + j;
+        if (q < p.nq && e < group_nvis_query(p, g, j)) p.scores[(int64_t)q * p.ld + e] = s;
+      }
+      tc_fence_before();
+      mbar_arrive(acc_empty + acc);
+      if (++acc == 2) { acc = 0; aph ^= 1; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, tmem_cols);
+  }
+}
+
+}  // namespace
+
+int index_smem_bytes(int qpg) { return smem_layout(qpg).total; }
+
+cudaError_t launch_index(const IndexParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_q,
+                         int grid, cudaStream_t s) {
+  const int smem = index_smem_bytes(p.qpg);
+  cudaError_t e = cudaFuncSetAttribute(k_index, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  k_index<<<grid, kThreads, smem, s>>>(p, tm_k, tm_q);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

@@ -1,0 +1,280 @@
+/*
+ * csa2.h -- C ABI of the CSA2 (Compressed Sparse Attention 2) attention step
+ * over an FP4 global KV cache, for one GB300 (sm_103a) GPU.
+ *
+ * The method (sources are web pages; each declaration cites the passage that
+ * defines the operation):
+ *   [V41] "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression"
+ *         (technical report, PaperTrace mirror)
+ *   [V4B] blog reading of the DeepSeek-V4 report (gzher.com)
+ *   [NDT] neshdevtech article on DeepSeek-V4.1-Flash
+ *
+ * One CSA2 group (a Full layer and the Reuse layers that follow it) owns one
+ * global cache: per sequence, compressed main-KV entries (FP4 E2M1 codes plus
+ * per-block scales) and indexer keys ([V41 sec 2.3.1], [NDT sec 3.1]).
+ * Sliding-window (SWA) KV is per layer and is passed in by the caller.
+ *
+ * Conventions (every call):
+ *   - "dev" pointers are CUDA device pointers owned by the caller; "host"
+ *     pointers are host memory read before the call returns.  Device
+ *     tensors are dense row-major and 16-byte aligned, else the call
+ *     returns CSA2_ERR_INVALID_ARG.
+ *   - bf16 tensors are passed as void* to raw 16-bit bf16 values.
+ *   - Calls are stream-ordered on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream), never synchronise the device and never allocate
+ *     device memory.  Scratch memory comes from the caller (`workspace`).
+ *   - Errors found on the host return a status before anything is
+ *     launched.  Errors found inside a kernel (a bounded wait that ran out,
+ *     an index out of range) set a sticky device error word that
+ *     csa2_get_device_error() reads.
+ *   - Entry indices are positions in a sequence's list of compressed
+ *     entries (not token positions).
+ */
+#ifndef CSA2_H
+#define CSA2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* csa2_stream_t; /* a cudaStream_t */
+
+typedef enum {
+  CSA2_OK = 0,
+  CSA2_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned tensor      */
+  CSA2_ERR_UNSUPPORTED = 2, /* configuration outside what the kernels support */
+  CSA2_ERR_CAPACITY = 3,    /* append beyond a sequence's capacity, or a too  */
+                            /* small workspace / cache buffer                 */
+  CSA2_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed           */
+  CSA2_ERR_OOM = 5,         /* reserved: the library itself never allocates   */
+  CSA2_ERR_TIMEOUT = 6,     /* device error word: a bounded wait ran out      */
+  CSA2_ERR_DEVICE = 7       /* device error word: bad index seen by a kernel  */
+} csa2_status_t;
+
+/* FP4 main-KV layouts.  [V41 sec 2.4.4] names both the OCP MXFP4 format
+ * (E2M1 + one power-of-two UE8M0 scale per 32 channels) and the format it
+ * selects for the main KV (E2M1 + one E4M3 scale per 16 channels, no global
+ * scale; largest magnitude 448 * 6 = 2688).
+ *   L32_UE8M0: scale byte = floor(log2(amax)) - 2 + 127 (OCP MX rule,
+ *              clamped to [0, 254]); 256 B codes + 16 B scales per entry.
+ *   L16_E4M3 : scale = E4M3(amax / 6), round to nearest even, saturating at
+ *              448; 256 B codes + 32 B scales per entry.
+ * Codes are E2M1 of x / scale, round to nearest even, saturating at 6, the
+ * sign kept; two per byte, the even channel in the low nibble.             */
+typedef enum { CSA2_KV_L32_UE8M0 = 0, CSA2_KV_L16_E4M3 = 1 } csa2_kv_layout_t;
+
+/* Shapes of one CSA2 layer.  [V41 sec 4.2.1]: 64 query heads of dim 512,
+ * 32 indexer heads of dim 128, top-k 512, window 128, ratio m = 2 (encoder)
+ * or 1 (decoder).  Supported: head_dim 512, idx_dim 128, idx_heads 32,
+ * n_heads a multiple of 32 up to 128, topk a multiple of 128 up to 2048,
+ * 0 <= swa <= 128, 1 <= ratio <= 16.                                      */
+typedef struct {
+  int32_t n_heads;
+  int32_t head_dim;
+  int32_t idx_heads;
+  int32_t idx_dim;
+  int32_t topk;
+  int32_t swa;
+  int32_t ratio;
+  int32_t layout; /* csa2_kv_layout_t */
+} csa2_config_t;
+
+typedef struct csa2_cache csa2_cache_t; /* opaque host handle, one per group */
+
+/* Device views of a cache, for inspection.  Entry e of sequence b is row
+ * entry_offset[b] + e of every array.                                       */
+typedef struct {
+  uint8_t* codes;        /* dev [total, head_dim / 2]                         */
+  uint8_t* scales;       /* dev [total, head_dim / group]                     */
+  void* idx_k;           /* dev bf16 [total, idx_dim]                         */
+  int32_t* lengths;      /* dev [batch]: entries appended so far              */
+  const int64_t* entry_offset; /* host [batch + 1]                           */
+  int64_t total;         /* sum of capacities                                 */
+  int32_t batch;
+  int32_t group;         /* 32 or 16 channels per scale                       */
+} csa2_cache_views_t;
+
+int32_t csa2_version(void);
+const char* csa2_status_string(csa2_status_t status);
+
+/* ---- cache ------------------------------------------------------------- */
+
+/* Bytes of device memory a cache for `batch` sequences with the given
+ * per-sequence capacities (in compressed entries, host [batch]) needs.
+ * Returns 0 for an invalid or unsupported configuration.                    */
+size_t csa2_cache_bytes(const csa2_config_t* cfg, int32_t batch,
+                        const int64_t* capacity);
+
+/* Lays a cache out in caller-owned device memory `dev_mem` (`bytes` long,
+ * 256-byte aligned) and zeroes its lengths on `stream`.  The handle (host
+ * memory) is returned in *out.  The caller keeps dev_mem alive until
+ * csa2_cache_destroy.  [V41 sec 2.3.1]: main KV and indexer K are shared by
+ * every layer of the group, so one cache serves all of them.              */
+csa2_status_t csa2_cache_create(const csa2_config_t* cfg, int32_t batch,
+                                const int64_t* capacity, void* dev_mem,
+                                size_t bytes, csa2_stream_t stream,
+                                csa2_cache_t** out);
+
+/* Frees the host handle only; the device memory stays the caller's. */
+csa2_status_t csa2_cache_destroy(csa2_cache_t* cache);
+
+/* Empties every sequence (host lengths and, on `stream`, device lengths). */
+csa2_status_t csa2_cache_reset(csa2_cache_t* cache, csa2_stream_t stream);
+
+/* Entries appended so far to sequence `seq` (host-side count). */
+csa2_status_t csa2_cache_length(const csa2_cache_t* cache, int32_t seq,
+                                int64_t* n_entries);
+
+csa2_status_t csa2_cache_views(const csa2_cache_t* cache,
+                               csa2_cache_views_t* out);
+
+/* ---- compress / append ------------------------------------------------- */
+
+/* CSA2 compressor ([V41 sec 2.3]: no overlap between blocks, no positional
+ * bias; pooling form of [V4B sec 4.2]): out[i, c] = sum_j softmax_j(z[j, c])
+ * * c_tok[j, c] over the `ratio` tokens j of block i, in fp32 with a fixed
+ * order.  At ratio 1 it is the identity ([NDT sec 3.3.2]).
+ *   c_tok: dev bf16 [n_out * ratio, dim];  z_tok: dev fp32 [n_out * ratio,
+ *   dim];  out: dev fp32 [n_out, dim].  dim must be a multiple of 16.     */
+csa2_status_t csa2_compress(int32_t ratio, int64_t n_out, int32_t dim,
+                            const void* c_tok, const float* z_tok, float* out,
+                            csa2_stream_t stream);
+
+/* Quantises compressed entries to the cache's FP4 layout and appends them
+ * with their indexer keys ([V41 sec 2.4.4]: FP4 main KV cache, quantised
+ * after RoPE; [V41 sec 2.3]: indexer K is projected from the main KV by the
+ * caller).  Rows of `entries` / `idx_k` are grouped by sequence in the order
+ * of seq_ids: n_new[i] rows for sequence seq_ids[i].
+ *   seq_ids, n_new: host [n_seqs];  entries: dev fp32 [sum n_new, head_dim];
+ *   idx_k: dev bf16 [sum n_new, idx_dim].
+ * Returns CSA2_ERR_CAPACITY (nothing written) if a sequence would overflow. */
+csa2_status_t csa2_append_entries(csa2_cache_t* cache, int32_t n_seqs,
+                                  const int32_t* seq_ids, const int32_t* n_new,
+                                  const float* entries, const void* idx_k,
+                                  csa2_stream_t stream);
+
+/* Fused compress + quantise + append of whole blocks of tokens: n_tok[i] (a
+ * multiple of the ratio) tokens of sequence seq_ids[i] become n_tok[i] /
+ * ratio entries, bit-identical to csa2_compress followed by
+ * csa2_append_entries.  The unfinished tail of a block stays with the caller
+ * (it is not yet causally visible, [V4B sec 4.3]).
+ *   c_tok: dev bf16 [sum n_tok, head_dim];  z_tok: dev fp32 [sum n_tok,
+ *   head_dim];  idx_k: dev bf16 [sum n_tok / ratio, idx_dim];
+ *   entries_out: nullable dev fp32 [sum n_tok / ratio, head_dim].          */
+csa2_status_t csa2_append_tokens(csa2_cache_t* cache, int32_t n_seqs,
+                                 const int32_t* seq_ids, const int32_t* n_tok,
+                                 const void* c_tok, const float* z_tok,
+                                 const void* idx_k, float* entries_out,
+                                 csa2_stream_t stream);
+
+/* ---- indexer + top-k --------------------------------------------------- */
+
+/* Workspace bytes csa2_index_topk_decode / _prefill need for n_queries
+ * queries against this cache (fp32 scores for every visible entry of every
+ * query plus selection state).                                            */
+size_t csa2_index_workspace_bytes(const csa2_cache_t* cache, int32_t n_queries);
+
+/* Full-mode selection for decode queries, one query per sequence, each the
+ * newest token of its sequence so every appended entry is visible.
+ * Index score ([V4B sec 4.1]):  I[q, s] = sum_h w[q, h] * ReLU(q_idx[q, h] .
+ * K_I[s]), fp32; then the top-k entries ([V41 sec 4.2.1]: k = 512) with
+ * ties to the lower index, listed in ascending index order, padded with -1
+ * when fewer than k entries exist.
+ *   q_idx: dev bf16 [n_queries, idx_heads, idx_dim];  w: dev fp32
+ *   [n_queries, idx_heads];  seq_ids: host [n_queries] (NULL: query i reads
+ *   sequence i);  topk_idx: dev int32 [n_queries, topk];  topk_score:
+ *   nullable dev fp32 [n_queries, topk] (the scores of topk_idx, 0 for -1).
+ * A Reuse layer ([V41 sec 2.3.1]) calls nothing here: it passes the Full
+ * layer's topk_idx to csa2_sparse_attn_decode unchanged.                  */
+csa2_status_t csa2_index_topk_decode(const csa2_cache_t* cache,
+                                     int32_t n_queries, const void* q_idx,
+                                     const float* w, const int32_t* seq_ids,
+                                     int32_t* topk_idx, float* topk_score,
+                                     void* workspace, size_t workspace_bytes,
+                                     csa2_stream_t stream);
+
+/* Full-mode selection for a prefill chunk of one sequence: query i is the
+ * token at absolute position pos0 + i and sees entry s iff its block is
+ * complete, (s + 1) * ratio - 1 <= pos0 + i ([V41 sec 2.3.2] "causally
+ * visible"; [V4B sec 4.3]).  Same score, top-k and output rules as decode.
+ *   q_idx: dev bf16 [n_queries, idx_heads, idx_dim];  w: dev fp32
+ *   [n_queries, idx_heads];  topk_idx: dev int32 [n_queries, topk].        */
+csa2_status_t csa2_index_topk_prefill(const csa2_cache_t* cache, int32_t seq,
+                                      int32_t n_queries, int64_t pos0,
+                                      const void* q_idx, const float* w,
+                                      int32_t* topk_idx, float* topk_score,
+                                      void* workspace, size_t workspace_bytes,
+                                      csa2_stream_t stream);
+
+/* Workspace bytes of csa2_topk for n_rows rows. */
+size_t csa2_topk_workspace_bytes(int32_t n_rows);
+
+/* Stand-alone top-k over caller scores (the selection step of the indexer):
+ * row r has n_valid[r] fp32 scores at scores + r * ld; the k largest are
+ * returned, ties to the lower index, ascending index order, -1 padded.  -0
+ * and +0 compare equal; NaN is not allowed.
+ *   scores: dev fp32;  n_valid: host int64 [n_rows];  idx_out: dev int32
+ *   [n_rows, k];  score_out: nullable dev fp32 [n_rows, k].                 */
+csa2_status_t csa2_topk(int32_t n_rows, const float* scores, int64_t ld,
+                        const int64_t* n_valid, int32_t k, int32_t* idx_out,
+                        float* score_out, void* workspace,
+                        size_t workspace_bytes, csa2_stream_t stream);
+
+/* ---- sparse attention -------------------------------------------------- */
+
+/* Decode readout of one layer ([V4B sec 4.1] shared-KV MQA: the selected
+ * compressed entries are both key and value; [V4B sec 4.3] and [NDT sec
+ * 3.3.1]: the window rows join the same softmax): for query q and head h,
+ *   l_j = scale * q[q, h] . kv_j   over j in {selected entries} U {window},
+ *   out[q, h] = sum_j softmax(l)_j kv_j,   lse[q, h] = ln sum_j exp(l_j),
+ * with the selected entries dequantised from FP4 on chip.  Full and Reuse
+ * layers make the same call; a Reuse layer passes its group's topk_idx.
+ *   q: dev bf16 [n_queries, n_heads, head_dim];  swa_kv: dev bf16
+ *   [n_queries, swa, head_dim], the first swa_len[q] rows of query q are its
+ *   window;  swa_len: nullable dev int32 [n_queries] (NULL: all swa rows);
+ *   topk_idx: dev int32 [n_queries, topk] (-1 = unused slot);  seq_ids: host
+ *   [n_queries] or NULL (query i reads sequence i);  out: dev bf16
+ *   [n_queries, n_heads, head_dim];  lse: nullable dev fp32 [n_queries,
+ *   n_heads].  An index >= the sequence's length is skipped and sets
+ *   CSA2_ERR_DEVICE in the device error word.                               */
+csa2_status_t csa2_sparse_attn_decode(const csa2_cache_t* cache,
+                                      int32_t n_queries, const int32_t* seq_ids,
+                                      const void* q, const void* swa_kv,
+                                      const int32_t* swa_len,
+                                      const int32_t* topk_idx, float scale,
+                                      void* out, float* lse,
+                                      csa2_stream_t stream);
+
+/* Prefill readout of one layer for a chunk of sequence `seq`: query i sits
+ * at absolute position p = pos0 + i and its window is the token rows of
+ * positions [max(swa_pos0, p - swa + 1), p] ([V41 sec 3.2.2]: a replay that
+ * starts at swa_pos0 truncates the window there).
+ *   q: dev bf16 [n_queries, n_heads, head_dim];  swa_kv: dev bf16
+ *   [n_swa_rows, head_dim], row r holds the token at position swa_pos0 + r
+ *   (requires pos0 + n_queries - 1 - swa_pos0 < n_swa_rows and
+ *   swa_pos0 <= pos0);  topk_idx: dev int32 [n_queries, topk];  out, lse as
+ *   for decode.                                                            */
+csa2_status_t csa2_sparse_attn_prefill(const csa2_cache_t* cache, int32_t seq,
+                                       int32_t n_queries, int64_t pos0,
+                                       const void* q, const void* swa_kv,
+                                       int64_t swa_pos0, int64_t n_swa_rows,
+                                       const int32_t* topk_idx, float scale,
+                                       void* out, float* lse,
+                                       csa2_stream_t stream);
+
+/* ---- errors ------------------------------------------------------------ */
+
+/* Reads and clears the cache's sticky device error word (synchronises
+ * `stream`).  *device_status receives CSA2_OK, CSA2_ERR_TIMEOUT or
+ * CSA2_ERR_DEVICE.                                                          */
+csa2_status_t csa2_get_device_error(const csa2_cache_t* cache,
+                                    csa2_stream_t stream,
+                                    int32_t* device_status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA2_H */

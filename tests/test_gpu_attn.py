@@ -1,0 +1,134 @@
+"""GPU sparse attention (FP4 gather-dequant + tcgen05 QK^T / PV + window +
+joint softmax) against the oracle's fp64 attention: max-abs 1e-2 and
+mean-abs 1e-3 on the bf16 outputs, lse within 1e-3."""
+import numpy as np
+import pytest
+
+import csa2_synth as S
+import oracle as O
+from tests._parity import bf16_dev, bf16_host, check_attn, f32_dev
+
+pytestmark = pytest.mark.gpu
+SCALE = np.float32(512 ** -0.5)
+
+
+@pytest.fixture(scope="module")
+def C():
+    import fp4_kv_cache_index_gb300 as C
+    return C
+
+
+def _cache(C, lens, cap, seed, layout=0, ratio=1, outlier=None):
+    cache = C.Cache(C.config(layout=layout, ratio=ratio), [cap] * len(lens))
+    ents = []
+    for s, n in enumerate(lens):
+        e = S.normal_f32(S.stream_key(seed, S.S_ENTRIES, s), 0, n * 512).reshape(n, 512)
+        if outlier is not None:
+            e[:, outlier] *= 8
+        k = S.normal_bf16(S.stream_key(seed, S.S_IDXK, s), 0, n * 128).reshape(n, 128)
+        if n:
+            C.csa2_append_entries(cache, [s], [n], f32_dev(e), bf16_dev(k))
+        ents.append(e)
+    return cache, ents
+
+
+def _sel(rng, n, k=512, fill=None):
+    m = min(n, k) if fill is None else fill
+    idx = np.sort(rng.choice(n, m, replace=False)) if m else np.zeros(0, np.int64)
+    out = np.full(k, -1, np.int32)
+    out[:m] = idx
+    return out
+
+
+@pytest.mark.parametrize("layout", [0, 1])
+def test_decode_matches_oracle(C, layout):
+    import torch
+    rng = np.random.default_rng(layout)
+    lens = [700, 300, 1000, 5000]
+    outl = np.array([3, 77, 200, 301, 511])
+    cache, ents = _cache(C, lens, 5120, 31, layout, outlier=outl)
+    nq = len(lens)
+    q = S.normal_bf16(S.stream_key(32, S.S_Q, 0), 0, nq * 64 * 512).reshape(nq, 64, 512)
+    swa = S.normal_f32(S.stream_key(32, S.S_SWA, 0), 0, nq * 128 * 512).reshape(nq, 128, 512)
+    swa[..., outl] *= 8
+    swa = S.f32_to_bf16_bits(swa)
+    swa_len = np.array([128, 50, 0, 1], np.int32)
+    idx = np.stack([_sel(rng, n) for n in lens])
+    idx[3, 100:] = -1                      # a query with 100 selected entries only
+    lse = torch.zeros(nq, 64, dtype=torch.float32, device="cuda")
+    out = C.csa2_sparse_attn_decode(cache, bf16_dev(q), bf16_dev(swa), torch.from_numpy(idx).cuda(),
+                                    float(SCALE), swa_len=torch.from_numpy(swa_len).cuda(), lse=lse)
+    out = bf16_host(out)
+    lse = lse.cpu().numpy()
+    for i in range(nq):
+        codes, scales = O.quantise(ents[i], layout)
+        _, o, ol = O.sparse_attention(q[i], codes, scales, layout, idx[i], swa[i, :swa_len[i]],
+                                      SCALE)
+        check_attn(out[i], o)
+        assert np.allclose(lse[i], ol, atol=1e-3, rtol=0)
+    assert cache.device_error() == 0
+
+
+def test_sharper_softmax_and_reuse_identity(C):
+    """A larger scale concentrates the weights (exercises the running-max
+    rescale); a Reuse layer with the Full layer's indices, q and window
+    reproduces its output bit for bit."""
+    import torch
+    rng = np.random.default_rng(5)
+    cache, ents = _cache(C, [4000, 4000], 4096, 33)
+    q = S.normal_bf16(S.stream_key(34, S.S_Q, 0), 0, 2 * 64 * 512).reshape(2, 64, 512)
+    swa = S.normal_bf16(S.stream_key(34, S.S_SWA, 0), 0, 2 * 128 * 512).reshape(2, 128, 512)
+    idx = np.stack([_sel(rng, 4000), _sel(rng, 4000)])
+    ti = torch.from_numpy(idx).cuda()
+    for scale in (np.float32(0.25), np.float32(0.01)):
+        a = C.csa2_sparse_attn_decode(cache, bf16_dev(q), bf16_dev(swa), ti, float(scale))
+        b = C.csa2_sparse_attn_decode(cache, bf16_dev(q), bf16_dev(swa), ti, float(scale))
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        out = bf16_host(a)
+        for i in range(2):
+            codes, scales = O.quantise(ents[i], 0)
+            _, o, _ = O.sparse_attention(q[i], codes, scales, 0, idx[i], swa[i], scale)
+            check_attn(out[i], o)
+
+
+def test_empty_candidates_and_bad_index(C):
+    import torch
+    cache, ents = _cache(C, [10, 10], 64, 35)
+    q = S.normal_bf16(S.stream_key(36, S.S_Q, 0), 0, 2 * 64 * 512).reshape(2, 64, 512)
+    swa = S.normal_bf16(S.stream_key(36, S.S_SWA, 0), 0, 2 * 128 * 512).reshape(2, 128, 512)
+    idx = np.full((2, 512), -1, np.int32)
+    idx[1, :3] = [2, 9, 10]                # 10 is out of range: skipped and reported
+    lse = torch.zeros(2, 64, device="cuda")
+    out = C.csa2_sparse_attn_decode(cache, bf16_dev(q), bf16_dev(swa), torch.from_numpy(idx).cuda(),
+                                    float(SCALE), swa_len=torch.tensor([0, 5], dtype=torch.int32,
+                                                                       device="cuda"), lse=lse)
+    o = bf16_host(out)
+    assert np.all(o[0] == 0) and np.all(np.isneginf(lse[0].cpu().numpy()))
+    codes, scales = O.quantise(ents[1], 0)
+    _, ref, _ = O.sparse_attention(q[1], codes, scales, 0, np.array([2, 9], np.int32),
+                                   swa[1, :5], SCALE)
+    check_attn(o[1], ref)
+    assert cache.device_error() == 7
+    assert cache.device_error() == 0       # reading clears the word
+
+
+@pytest.mark.parametrize("ratio", [1, 2])
+def test_prefill_window_band(C, ratio):
+    import torch
+    rng = np.random.default_rng(ratio)
+    n_ent = 800
+    cache, ents = _cache(C, [n_ent], 1024, 37, ratio=ratio)
+    nq, pos0 = 20, 1500 if ratio == 2 else 700
+    swa_pos0 = pos0 - 60                   # a replay that starts 60 tokens back
+    rows = S.normal_bf16(S.stream_key(38, S.S_SWA, 1), 0, (nq + 60) * 512).reshape(nq + 60, 512)
+    q = S.normal_bf16(S.stream_key(38, S.S_Q, 1), 0, nq * 64 * 512).reshape(nq, 64, 512)
+    idx = np.stack([_sel(rng, O.visible_entries(n_ent, ratio, pos0 + i)) for i in range(nq)])
+    out = C.csa2_sparse_attn_prefill(cache, 0, pos0, bf16_dev(q), bf16_dev(rows), swa_pos0,
+                                     torch.from_numpy(idx).cuda(), float(SCALE))
+    out = bf16_host(out)
+    codes, scales = O.quantise(ents[0], 0)
+    for i in range(nq):
+        lo, hi = O.swa_rows(pos0 + i, 128, swa_pos0)
+        _, o, _ = O.sparse_attention(q[i], codes, scales, 0, idx[i],
+                                     rows[lo - swa_pos0:hi - swa_pos0], SCALE)
+        check_attn(out[i], o)

@@ -1,0 +1,73 @@
+"""GPU top-k (csa2_topk) against the oracle's full sort on identical fp32
+scores: the index lists must be identical (ties to the lower index,
+ascending order, -1 padding)."""
+import numpy as np
+import pytest
+
+import oracle as O
+from tests._parity import f32_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def C():
+    import fp4_kv_cache_index_gb300 as C
+    return C
+
+
+def _rows(kind, n, rng):
+    if kind == "normal":
+        return rng.standard_normal(n).astype(np.float32)
+    if kind == "ints":          # many exact ties everywhere
+        return rng.integers(-30, 30, n).astype(np.float32)
+    if kind == "equal":         # one crowded bin, all ties
+        return np.full(n, 2.5, np.float32)
+    if kind == "crowded":       # > 8192 keys share the top 11 bits, distinct below
+        return (1.0 + rng.random(n) * 2.0 ** -3).astype(np.float32)
+    if kind == "signed_zero":
+        x = rng.choice(np.float32([0.0, -0.0, 1.0, -1.0]), n)
+        return x.astype(np.float32)
+    if kind == "relu_like":     # many exact zeros, as after ReLU with few heads
+        x = rng.standard_normal(n).astype(np.float32)
+        x[x < 1.0] = 0.0
+        return x
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("kind", ["normal", "ints", "equal", "crowded", "signed_zero", "relu_like"])
+@pytest.mark.parametrize("n", [0, 1, 511, 512, 513, 4097, 70001])
+def test_topk_matches_full_sort(C, kind, n):
+    rng = np.random.default_rng(n + len(kind))
+    s = _rows(kind, max(n, 1), rng)[:n]
+    ld = max(4, (n + 3) // 4 * 4)
+    buf = np.zeros((1, ld), np.float32)
+    buf[0, :n] = s
+    sc = f32_dev(buf)
+    import torch
+    so = torch.zeros(1, 512, dtype=torch.float32, device="cuda")
+    got = C.csa2_topk(sc, [n], 512, score_out=so).cpu().numpy()[0]
+    want = O.topk(s, 512)
+    assert np.array_equal(got, want)
+    keff = min(n, 512)
+    assert np.array_equal(so.cpu().numpy()[0, :keff], s[got[:keff]])
+
+
+@pytest.mark.parametrize("k", [128, 512, 2048])
+def test_ragged_rows_odd_stride(C, k):
+    rng = np.random.default_rng(k)
+    ns = [0, 5, k - 1, k, k + 1, 3000, 9999, 262147]
+    ld = 262147 + 2            # odd row stride: rows are not 16-byte aligned
+    buf = rng.standard_normal((len(ns), ld)).astype(np.float32)
+    buf[2, :] = np.round(buf[2, :] * 4)
+    got = C.csa2_topk(f32_dev(buf), ns, k).cpu().numpy()
+    for r, n in enumerate(ns):
+        assert np.array_equal(got[r], O.topk(buf[r, :n], k)), r
+
+
+def test_long_row(C):
+    rng = np.random.default_rng(3)
+    n = 524288
+    s = (rng.standard_normal(n) * 50).astype(np.float32)
+    got = C.csa2_topk(f32_dev(s[None]), [n], 512).cpu().numpy()[0]
+    assert np.array_equal(got, O.topk(s, 512))
