@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Benchmark of the CSA2 decode step over an FP4 global KV cache on GB300.
+
+One step = one decode token for every sequence of the batch through one
+CSA2 group: Full-layer index scores + top-512 selection, then the sparse
+attention of the Full layer and of each Reuse layer (which reuses the Full
+layer's indices).  Default workload: batch 64, 131072 compressed entries per
+sequence (128K context, ratio 1), 1 Full + 3 Reuse layers, FP4 main KV with
+one power-of-two scale per 32 channels, 1% outlier channels scaled by 8.
+
+value  : query-tokens/s with every input resident in HBM (device-timed).
+e2e    : the same metric through the public API with host (pinned) inputs and
+         outputs, host<->device copies inside the timed region.
+roofline: the indexer-score kernel (the dominant one) against measured HBM
+         bandwidth; its duration is taken with CUDA events on its stream.
+--impl reference times the CPU oracle (test infrastructure) on the box's
+host cores on a bounded sample of the same workload.
+
+Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
+torch.distributed.run, one process per GPU, each running its own replica
+(sequences are independent: weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA2 decode query-tokens/s at 128K ctx, B=64; achieved HBM GB/s vs peak"
+UNIT = "query-tokens/s"
+INDEXER_SRC = os.path.join(ROOT, "fp4_kv_cache_index_gb300", "csrc", "k_index.cu")
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "k_index_decode_traffic.txt")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["csa2", "reference"], default="csa2")
+    p.add_argument("--workload", type=int, default=2)
+    p.add_argument("--layout", type=int, default=0, help="0 = L32_UE8M0, 1 = L16_E4M3")
+    p.add_argument("--batch", type=int, default=None,
+                   help="override the workload's batch (smaller profiling cases only)")
+    p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target CPU time of the oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------- distributed helpers
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- peaks and clocks
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        if self.out is not None:
+            self.out.flush()
+            with open(self.out.name) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) < 9:
+                        continue
+                    try:
+                        sm.append(float(parts[1]))
+                        mx.append(float(parts[2]))
+                    except ValueError:
+                        continue
+                    for n, v in zip(names, parts[5:9]):
+                        if v.lower().startswith("active"):
+                            reasons.add(n)
+            os.unlink(self.out.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+class OracleSample:
+    """Host inputs of a few sequences of the workload, generated once, and the
+    oracle's full decode step for one of them."""
+
+    def __init__(self, wl, layout, n_seqs=4):
+        self.wl, self.layout = wl, layout
+        self.seqs = list(range(min(n_seqs, wl.batch)))
+        self.inputs = {}
+
+    def _inputs(self, b):
+        if b not in self.inputs:
+            wl = self.wl
+            self.inputs[b] = (wl.idx_k(b), wl.q_idx(b, 1)[0], wl.w(b, 1)[0],
+                              [wl.q(l, b, 1)[0] for l in range(wl.layers)],
+                              [wl.swa(l, b, 1)[0] for l in range(wl.layers)])
+        return self.inputs[b]
+
+    def step(self, i, k=512):
+        """Oracle time (s) of one query's decode step: fp64 index scores over
+        every entry, top-k, then every layer's attention over the selected
+        entries and the window.  Generating the selected entries is not timed."""
+        import numpy as np
+        import oracle as O
+        b = self.seqs[i % len(self.seqs)]
+        kk, qi, w, qs, sw = self._inputs(b)
+        t0 = time.perf_counter()
+        idx, _ = O.index_topk(kk, qi, w, k)
+        t1 = time.perf_counter()
+        sel = idx[idx >= 0]
+        rows = self.wl.entry_rows(b, sel)
+        t2 = time.perf_counter()
+        codes, scales = O.quantise(rows, self.layout)
+        local = np.arange(len(sel), dtype=np.int32)
+        for l in range(self.wl.layers):
+            O.sparse_attention(qs[l], codes, scales, self.layout, local, sw[l],
+                               np.float32(512 ** -0.5))
+        return (t1 - t0) + (time.perf_counter() - t2)
+
+
+def cpu_baseline(wl, target_s, layout):
+    import oracle as O
+    smp = OracleSample(wl, layout)
+    smp.step(0)                       # warm-up (also generates the inputs)
+    done, spent = 0, 0.0
+    while done == 0 or (spent < target_s and done < 64):
+        spent += smp.step(done)
+        done += 1
+    return {"value": done / spent, "unit": UNIT, "cores": O.num_threads(), "kind": "oracle",
+            "sample": f"{done} query decode steps of the workload over sequences "
+                      f"{smp.seqs} (fp64 index over all entries, top-k, {wl.layers} "
+                      f"attention layers each); input generation not timed; "
+                      f"{spent:.1f} s of oracle time"}
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, budget_s=150.0):
+    """The oracle on the host cores, one query's decode step per step; the
+    run stops early once `budget_s` of oracle time is spent so that any
+    --steps finishes within minutes (the line reports the steps timed)."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from csa2_synth.workloads import WORKLOADS
+    import oracle as O
+    wl = WORKLOADS[args.workload]
+    smp = OracleSample(wl, args.layout)
+    for i in range(max(1, min(args.warmup, 3))):
+        smp.step(i)
+    spent, n = 0.0, 0
+    while n < args.steps and (n == 0 or spent < budget_s):
+        spent += smp.step(n)
+        n += 1
+    value = n / spent
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": n, "warmup": args.warmup, "ms_per_step": 1000 * spent / n,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(wl, args.layout),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": O.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"{n} of {args.steps} requested steps (oracle-time budget "
+                                   f"{budget_s:.0f} s); each step is one query's full decode "
+                                   "step of the workload on the CPU oracle, input generation "
+                                   "not timed"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(wl, layout):
+    n = wl.n_entries()
+    return {"workload": wl.name, "batch": wl.batch, "ctx_tokens": int(wl.ctx),
+            "entries_per_seq": int(n[0]) if len(set(n.tolist())) == 1 else n.tolist(),
+            "ratio": wl.ratio, "layers": f"1 Full + {wl.layers - 1} Reuse",
+            "heads": 64, "head_dim": 512, "idx_heads": 32, "idx_dim": 128, "topk": 512,
+            "swa": 128, "layout": "L32_UE8M0" if layout == 0 else "L16_E4M3",
+            "outliers": "1% channels x8" if wl.outliers else "none",
+            "l2": "inputs larger than L2: every step streams all indexer keys "
+                  f"({int(n.sum()) * 256 / 1e9:.2f} GB) through the 129 MB L2",
+            "parallelism": "replica per GPU (sequences are independent)"}
+
+
+def kernel_traffic_record():
+    """ncu DRAM bytes per indexer launch, if recorded for this exact source."""
+    try:
+        src = hashlib.sha256(open(INDEXER_SRC, "rb").read()).hexdigest()
+        rec = {}
+        with open(TRAFFIC_RECORD) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    rec[k.strip()] = v.strip()
+        if rec.get("k_index.cu sha256") == src and rec.get("workload") is not None:
+            return rec
+    except OSError:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_csa2(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import fp4_kv_cache_index_gb300 as C
+    from csa2_synth import workloads as W
+    wl = W.WORKLOADS[args.workload]
+    if args.batch is not None:
+        import dataclasses
+        wl = dataclasses.replace(wl, batch=args.batch, name=f"{wl.name}@batch{args.batch}")
+    assert not wl.prefill, "the decode benchmark takes a decode workload"
+    L = wl.layers
+    B = wl.batch
+    n_ent = wl.n_entries()
+    cfg = C.config(ratio=wl.ratio, layout=args.layout)
+    cache = C.Cache(cfg, [int(x) for x in n_ent], device=dev)
+    W.fill_cache(wl, cache)
+    q_idx = W.dev_q_idx(wl)
+    w = W.dev_w(wl)
+    qs = [W.dev_q(wl, l) for l in range(L)]
+    swas = [W.dev_swa(wl, l) for l in range(L)]
+    ld = max(4, (int(n_ent.max()) + 3) // 4 * 4)
+    scores = torch.empty(B, ld, dtype=torch.float32, device=dev)
+    topk = torch.empty(B, 512, dtype=torch.int32, device=dev)
+    outs = [torch.empty(B, 64, 512, dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    lses = [torch.empty(B, 64, dtype=torch.float32, device=dev) for _ in range(L)]
+    n_valid = [int(x) for x in n_ent]
+    scale = 512 ** -0.5
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        C.csa2_index_scores_decode(cache, q_idx, w, scores)
+        if ev is not None:
+            ev[1].record(stream)
+        C.csa2_topk(scores, n_valid, 512, idx_out=topk)
+        if ev is not None:
+            ev[2].record(stream)
+        for l in range(L):
+            C.csa2_sparse_attn_decode(cache, qs[l], swas[l], topk, scale, out=outs[l],
+                                      lse=lses[l])
+        if ev is not None:
+            ev[3].record(stream)
+
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local).start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    # per-step events give the per-kernel split; the whole region is bracketed too
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    elapsed = t_start.elapsed_time(t_end) / 1000.0
+    clocks = sampler.stop()
+    t_idx = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps / 1000.0
+    t_topk = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps / 1000.0
+    t_attn = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps / 1000.0
+    if cache.device_error() != 0:
+        raise RuntimeError("device error word set during the benchmark")
+    elapsed_max = max_over_ranks(elapsed, world, dev)
+
+    # ---- end to end: host inputs -> device -> host outputs, per step
+    e2e_steps = args.e2e_steps or max(3, min(args.steps, 200))
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+    h_in = [pin(q_idx), pin(w)] + [pin(x) for x in qs] + [pin(x) for x in swas]
+    d_in = [q_idx, w] + qs + swas
+    h_out = [torch.empty(topk.shape, dtype=topk.dtype, pin_memory=True)] + \
+        [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs] + \
+        [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in lses]
+    d_out = [topk] + outs + lses
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def e2e_step():
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        step()
+        for h, d in zip(h_out, d_out):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_elapsed = max_over_ranks(a.elapsed_time(b) / 1000.0, world, dev)
+
+    # ---- accounting
+    hbm_peak, peak_kind = measured_peaks()
+    tot_ent = int(n_ent.sum())
+    idx_bytes = tot_ent * 256 + B * (32 * 128 * 2 + 32 * 4)
+    entry_bytes = 256 + (16 if args.layout == 0 else 32)
+    attn_bytes = L * B * (512 * entry_bytes + 128 * 512 * 2 + 2 * 64 * 512 * 2)
+    step_bytes = idx_bytes + attn_bytes
+    ms = 1000 * elapsed_max / args.steps
+    achieved = idx_bytes / t_idx / 1e9
+    rec = kernel_traffic_record()
+    traffic = None
+    if rec is not None and rec.get("workload") == wl.name:
+        traffic = float(rec["dram_bytes_per_launch"])
+    launches_per_step = (B + 1023) // 1024 + (B + 1023) // 1024 + L * ((B + 1023) // 1024)
+    line = {
+        "metric": METRIC, "value": B * world * args.steps / elapsed_max, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": workload_config(wl, args.layout),
+        "roofline": {"kernel": "k_index (indexer scores, tcgen05)", "bound": "hbm",
+                     "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": traffic,
+                     "peak_kind": f"{peak_kind} (copy bandwidth)",
+                     "algorithmic_bytes_per_launch": idx_bytes},
+        "step_hbm": {"achieved": step_bytes / (ms / 1000) / 1e9, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": step_bytes / (ms / 1000) / 1e9 / hbm_peak,
+                     "algorithmic_bytes_per_step": step_bytes},
+        "kernel_ms": {"index_scores": 1000 * t_idx, "topk": 1000 * t_topk,
+                      "sparse_attn_all_layers": 1000 * t_attn},
+        "e2e": {"value": B * world * e2e_steps / e2e_elapsed, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds, args.layout)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_csa2(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

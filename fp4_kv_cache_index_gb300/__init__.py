@@ -75,6 +75,7 @@ def _load():
         "csa2_append_entries": ([P, i32, P, P, P, P, P], i32),
         "csa2_append_tokens": ([P, i32, P, P, P, P, P, P, P], i32),
         "csa2_index_workspace_bytes": ([P, i32], sz),
+        "csa2_index_scores_decode": ([P, i32, P, P, P, P, i64, P], i32),
         "csa2_index_topk_decode": ([P, i32, P, P, P, P, P, P, sz, P], i32),
         "csa2_index_topk_prefill": ([P, i32, i32, i64, P, P, P, P, P, sz, P], i32),
         "csa2_topk_workspace_bytes": ([i32], sz),
@@ -220,6 +221,16 @@ def _workspace(nbytes: int, device, workspace):
     if workspace is None:
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
     return workspace
+
+
+def csa2_index_scores_decode(cache: Cache, q_idx: torch.Tensor, w: torch.Tensor,
+                             scores: torch.Tensor, seq_ids: Optional[Sequence[int]] = None,
+                             stream=None) -> torch.Tensor:
+    """scores: fp32 [n_queries, ld] (ld a multiple of 4, >= every length)."""
+    _check(lib.csa2_index_scores_decode(cache.handle, q_idx.shape[0], _ptr(q_idx), _ptr(w),
+                                        _i32_array(seq_ids), _ptr(scores), scores.shape[1],
+                                        _stream(stream)), "csa2_index_scores_decode")
+    return scores
 
 
 def csa2_index_topk_decode(cache: Cache, q_idx: torch.Tensor, w: torch.Tensor,

@@ -371,29 +371,17 @@ csa2_status_t csa2_topk(int32_t n_rows, const float* scores, int64_t ld, const i
   return CSA2_OK;
 }
 
-csa2_status_t csa2_index_topk_decode(const csa2_cache_t* c, int32_t nq, const void* q_idx,
-                                     const float* w, const int32_t* seq_ids, int32_t* topk_idx,
-                                     float* topk_score, void* workspace, size_t ws_bytes,
-                                     csa2_stream_t stream) {
-  if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
-  if (nq == 0) return CSA2_OK;
-  if (!q_idx || !w || !topk_idx || !workspace || !aligned16(q_idx) || !aligned16(w) ||
-      !aligned16(workspace))
-    return CSA2_ERR_INVALID_ARG;
-  if (ws_bytes < csa2_index_workspace_bytes(c, nq)) return CSA2_ERR_CAPACITY;
-  if (seq_ids)
-    for (int i = 0; i < nq; ++i)
-      if (seq_ids[i] < 0 || seq_ids[i] >= c->batch) return CSA2_ERR_INVALID_ARG;
-  const int64_t ld = score_ld(c->max_cap);
-  float* scores = static_cast<float*>(workspace);
-  const int k = c->cfg.topk;
-  const uint16_t* qb = static_cast<const uint16_t*>(q_idx);
+}  // extern "C"
 
-  IndexParams* ip = new (std::nothrow) IndexParams();
-  TopkParams* tp = new (std::nothrow) TopkParams();
-  if (!ip || !tp) { delete ip; delete tp; return CSA2_ERR_OOM; }
-  csa2_status_t st = CSA2_OK;
-  for (int q0 = 0; q0 < nq && st == CSA2_OK; q0 += kMaxIdxGroups) {
+namespace {
+
+// Scores of decode queries [q0, q0 + n) into scores (row stride ld): one
+// indexer launch per chunk of up to kMaxIdxGroups queries.
+csa2_status_t run_index_decode(const csa2_cache_t* c, int32_t nq, const void* q_idx,
+                               const float* w, const int32_t* seq_ids, float* scores, int64_t ld,
+                               csa2_stream_t stream, IndexParams* ip) {
+  const uint16_t* qb = static_cast<const uint16_t*>(q_idx);
+  for (int q0 = 0; q0 < nq; q0 += kMaxIdxGroups) {
     const int n = std::min(kMaxIdxGroups, nq - q0);
     std::memset(ip, 0, sizeof(IndexParams));
     ip->w = w + (int64_t)q0 * kIdxHeads;
@@ -406,38 +394,87 @@ csa2_status_t csa2_index_topk_decode(const csa2_cache_t* c, int32_t nq, const vo
     ip->prefill = 0;
     ip->ratio = c->cfg.ratio;
     ip->tile_prefix[0] = 0;
-    std::memset(tp, 0, sizeof(TopkParams));
     for (int i = 0; i < n; ++i) {
       const int s = seq_ids ? seq_ids[q0 + i] : q0 + i;
-      if (s >= c->batch) { st = CSA2_ERR_INVALID_ARG; break; }
       const int64_t nv = c->len[s];
       ip->entry_base[i] = c->off[s];
       ip->nvis[i] = (int32_t)nv;
       ip->tile_prefix[i + 1] = ip->tile_prefix[i] + (int32_t)((nv + 127) / 128);
-      tp->n_valid[i] = nv;
     }
-    if (st != CSA2_OK) break;
     CUtensorMap tm_q;
     if (!make_map(&tm_q, qb + (int64_t)q0 * kIdxHeads * kIdxDim, (uint64_t)n * kIdxHeads,
-                  kIdxDim, 64, 32)) {
-      st = CSA2_ERR_CUDA;
-      break;
-    }
+                  kIdxDim, 64, 32))
+      return CSA2_ERR_CUDA;
     const int tiles = ip->tile_prefix[n];
     if (tiles > 0) {
       const int grid = std::min(c->num_sms, tiles);
-      if (launch_index(*ip, c->tm_k, tm_q, grid, S(stream)) != cudaSuccess) {
-        st = CSA2_ERR_CUDA;
-        break;
-      }
+      if (launch_index(*ip, c->tm_k, tm_q, grid, S(stream)) != cudaSuccess) return CSA2_ERR_CUDA;
     }
-    tp->scores = ip->scores;
+  }
+  return CSA2_OK;
+}
+
+csa2_status_t check_decode_queries(const csa2_cache_t* c, int32_t nq, const void* q_idx,
+                                   const float* w, const int32_t* seq_ids) {
+  if (!q_idx || !w || !aligned16(q_idx) || !aligned16(w)) return CSA2_ERR_INVALID_ARG;
+  if (seq_ids) {
+    for (int i = 0; i < nq; ++i)
+      if (seq_ids[i] < 0 || seq_ids[i] >= c->batch) return CSA2_ERR_INVALID_ARG;
+  } else if (nq > c->batch) {
+    return CSA2_ERR_INVALID_ARG;
+  }
+  return CSA2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+csa2_status_t csa2_index_scores_decode(const csa2_cache_t* c, int32_t nq, const void* q_idx,
+                                       const float* w, const int32_t* seq_ids, float* scores,
+                                       int64_t ld, csa2_stream_t stream) {
+  if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
+  if (nq == 0) return CSA2_OK;
+  csa2_status_t st = check_decode_queries(c, nq, q_idx, w, seq_ids);
+  if (st != CSA2_OK) return st;
+  if (!scores || !aligned16(scores) || ld % 4 != 0) return CSA2_ERR_INVALID_ARG;
+  for (int i = 0; i < nq; ++i)
+    if (c->len[seq_ids ? seq_ids[i] : i] > ld) return CSA2_ERR_CAPACITY;
+  IndexParams* ip = new (std::nothrow) IndexParams();
+  if (!ip) return CSA2_ERR_OOM;
+  st = run_index_decode(c, nq, q_idx, w, seq_ids, scores, ld, stream, ip);
+  delete ip;
+  return st;
+}
+
+csa2_status_t csa2_index_topk_decode(const csa2_cache_t* c, int32_t nq, const void* q_idx,
+                                     const float* w, const int32_t* seq_ids, int32_t* topk_idx,
+                                     float* topk_score, void* workspace, size_t ws_bytes,
+                                     csa2_stream_t stream) {
+  if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
+  if (nq == 0) return CSA2_OK;
+  csa2_status_t st = check_decode_queries(c, nq, q_idx, w, seq_ids);
+  if (st != CSA2_OK) return st;
+  if (!topk_idx || !workspace || !aligned16(workspace)) return CSA2_ERR_INVALID_ARG;
+  if (ws_bytes < csa2_index_workspace_bytes(c, nq)) return CSA2_ERR_CAPACITY;
+  const int64_t ld = score_ld(c->max_cap);
+  float* scores = static_cast<float*>(workspace);
+  IndexParams* ip = new (std::nothrow) IndexParams();
+  TopkParams* tp = new (std::nothrow) TopkParams();
+  if (!ip || !tp) { delete ip; delete tp; return CSA2_ERR_OOM; }
+  st = run_index_decode(c, nq, q_idx, w, seq_ids, scores, ld, stream, ip);
+  const int k = c->cfg.topk;
+  for (int q0 = 0; q0 < nq && st == CSA2_OK; q0 += kTopkTab) {
+    const int n = std::min(kTopkTab, nq - q0);
+    std::memset(tp, 0, sizeof(TopkParams));
+    tp->scores = scores + (int64_t)q0 * ld;
     tp->ld = ld;
     tp->rows = n;
     tp->k = k;
     tp->idx_out = topk_idx + (int64_t)q0 * k;
     tp->score_out = topk_score ? topk_score + (int64_t)q0 * k : nullptr;
     tp->formula = 0;
+    for (int i = 0; i < n; ++i) tp->n_valid[i] = c->len[seq_ids ? seq_ids[q0 + i] : q0 + i];
     if (launch_topk(*tp, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
   }
   delete ip;

@@ -177,6 +177,19 @@ csa2_status_t csa2_append_tokens(csa2_cache_t* cache, int32_t n_seqs,
  * query plus selection state).                                            */
 size_t csa2_index_workspace_bytes(const csa2_cache_t* cache, int32_t n_queries);
 
+/* Index scores only (the scoring step of csa2_index_topk_decode, for callers
+ * that select on their own or time the steps apart): for decode query q,
+ * scores[q * ld + s] = sum_h w[q, h] * ReLU(q_idx[q, h] . K_I[s]) for every
+ * entry s of its sequence ([V4B sec 4.1]); entries past a sequence's length
+ * are left untouched.
+ *   scores: dev fp32 [n_queries, ld], ld >= the longest sequence's length
+ *   and a multiple of 4;  other arguments as for csa2_index_topk_decode.    */
+csa2_status_t csa2_index_scores_decode(const csa2_cache_t* cache,
+                                       int32_t n_queries, const void* q_idx,
+                                       const float* w, const int32_t* seq_ids,
+                                       float* scores, int64_t ld,
+                                       csa2_stream_t stream);
+
 /* Full-mode selection for decode queries, one query per sequence, each the
  * newest token of its sequence so every appended entry is visible.
  * Index score ([V4B sec 4.1]):  I[q, s] = sum_h w[q, h] * ReLU(q_idx[q, h] .

@@ -1,0 +1,102 @@
+"""Parity on the five workloads at full size, in the launch configuration the
+benchmark times (whole batch on the GPU), checked on sampled queries that
+the oracle recomputes one by one: top-k sets (near-ties logged) and every
+layer's attention output (max-abs 1e-2, or one bf16 ulp where the output
+is so large that bf16 cannot resolve 1e-2 -- the x8 outlier channels reach
+|o| ~ 12 -- and mean-abs 1e-3)."""
+import numpy as np
+import pytest
+
+import oracle as O
+from csa2_synth import workloads as W
+from tests._parity import bf16_host, check_attn, check_topk
+
+pytestmark = pytest.mark.gpu
+SCALE = np.float32(512 ** -0.5)
+
+
+@pytest.fixture(scope="module")
+def C():
+    import fp4_kv_cache_index_gb300 as C
+    return C
+
+
+def _decode_case(C, wid, sample):
+    import torch
+    wl = W.WORKLOADS[wid]
+    n_ent = wl.n_entries()
+    cache = C.Cache(C.config(ratio=wl.ratio), [int(x) for x in n_ent])
+    W.fill_cache(wl, cache)
+    q_idx, w = W.dev_q_idx(wl), W.dev_w(wl)
+    idx = C.csa2_index_topk_decode(cache, q_idx, w)
+    outs, lses = [], []
+    for l in range(wl.layers):
+        lse = torch.empty(wl.batch, 64, device="cuda")
+        outs.append(bf16_host(C.csa2_sparse_attn_decode(cache, W.dev_q(wl, l), W.dev_swa(wl, l),
+                                                         idx, float(SCALE), lse=lse)))
+        lses.append(lse.cpu().numpy())
+    idx = idx.cpu().numpy()
+    assert cache.device_error() == 0
+    log = []
+    for b in sample:
+        o_idx, o_sc = O.index_topk(wl.idx_k(b), wl.q_idx(b, 1)[0], wl.w(b, 1)[0], 512)
+        check_topk(idx[b], o_idx, o_sc, 512, log)
+        sel = idx[b][idx[b] >= 0]
+        codes, scales = O.quantise(wl.entry_rows(b, sel), 0)
+        local = np.arange(len(sel), dtype=np.int32)
+        for l in range(wl.layers):
+            _, o, ol = O.sparse_attention(wl.q(l, b, 1)[0], codes, scales, 0, local,
+                                          wl.swa(l, b, 1)[0], SCALE)
+            check_attn(outs[l][b], o)
+            assert np.allclose(lses[l][b], ol, atol=1e-3, rtol=0)
+    print(f"workload {wid}: near-ties {log}")
+
+
+def test_workload0_full(C):
+    _decode_case(C, 0, [0])
+
+
+def test_workload1_full(C):
+    _decode_case(C, 1, list(range(16)))
+
+
+def test_workload2_sampled(C):
+    _decode_case(C, 2, [0, 37, 63])
+
+
+def test_workload3_ragged(C):
+    _decode_case(C, 3, [0, 1, 2, 3])
+
+
+def test_workload4_prefill_sampled(C):
+    import torch
+    wl = W.WORKLOADS[4]
+    n_ent = wl.n_entries()
+    cache = C.Cache(C.config(ratio=wl.ratio), [int(n_ent[0])])
+    W.fill_cache(wl, cache)
+    nq = wl.n_queries()
+    idx = C.csa2_index_topk_prefill(cache, 0, wl.pos0, W.dev_q_idx(wl), W.dev_w(wl))
+    sample = [0, 1, 2, 1000, 4095, 4096, 6001, nq - 1]
+    outs = []
+    for l in range(wl.layers):
+        out = C.csa2_sparse_attn_prefill(cache, 0, wl.pos0, W.dev_q(wl, l), W.dev_swa(wl, l),
+                                         wl.swa_pos0, idx, float(SCALE))
+        outs.append(bf16_host(out[sample]))
+    idx = idx.cpu().numpy()
+    assert cache.device_error() == 0
+    kk = wl.idx_k(0)
+    qi, w = wl.q_idx(), wl.w()
+    rows_all = [wl.swa(l) for l in range(wl.layers)]
+    for si, i in enumerate(sample):
+        p = wl.pos0 + i
+        nv = O.visible_entries(int(n_ent[0]), wl.ratio, p)
+        o_idx, o_sc = O.index_topk(kk, qi[i], w[i], 512, nv)
+        check_topk(idx[i], o_idx, o_sc, 512)
+        sel = idx[i][idx[i] >= 0]
+        codes, scales = O.quantise(wl.entry_rows(0, sel), 0)
+        local = np.arange(len(sel), dtype=np.int32)
+        lo, hi = O.swa_rows(p, 128, wl.swa_pos0)
+        for l in range(wl.layers):
+            _, o, _ = O.sparse_attention(wl.q(l, i, 1)[0], codes, scales, 0, local,
+                                         rows_all[l][lo - wl.swa_pos0:hi - wl.swa_pos0], SCALE)
+            check_attn(outs[l][si], o)
