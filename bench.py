@@ -294,6 +294,9 @@ def run_csa2(args):
     ld = max(4, (int(n_ent.max()) + 3) // 4 * 4)
     scores = torch.empty(B, ld, dtype=torch.float32, device=dev)
     topk = torch.empty(B, 512, dtype=torch.int32, device=dev)
+    key_hist = torch.empty(B, 2048, dtype=torch.int32, device=dev)
+    topk_ws = torch.empty(max(16, C.csa2_topk_workspace_bytes(B, int(n_ent.max()))),
+                          dtype=torch.uint8, device=dev)
     outs = [torch.empty(B, 64, 512, dtype=torch.bfloat16, device=dev) for _ in range(L)]
     lses = [torch.empty(B, 64, dtype=torch.float32, device=dev) for _ in range(L)]
     n_valid = [int(x) for x in n_ent]
@@ -303,10 +306,10 @@ def run_csa2(args):
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        C.csa2_index_scores_decode(cache, q_idx, w, scores)
+        C.csa2_index_scores_decode(cache, q_idx, w, scores, key_hist=key_hist)
         if ev is not None:
             ev[1].record(stream)
-        C.csa2_topk(scores, n_valid, 512, idx_out=topk)
+        C.csa2_topk(scores, n_valid, 512, idx_out=topk, key_hist=key_hist, workspace=topk_ws)
         if ev is not None:
             ev[2].record(stream)
         for l in range(L):
@@ -387,7 +390,9 @@ def run_csa2(args):
     traffic = None
     if rec is not None and rec.get("workload") == wl.name:
         traffic = float(rec["dram_bytes_per_launch"])
-    launches_per_step = (B + 1023) // 1024 + (B + 1023) // 1024 + L * ((B + 1023) // 1024)
+    # per step: histogram memset + indexer, top-k segments + top-k, one
+    # attention launch per layer
+    launches_per_step = (2 + 2 + L) * ((B + 1023) // 1024)
     line = {
         "metric": METRIC, "value": B * world * args.steps / elapsed_max, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,

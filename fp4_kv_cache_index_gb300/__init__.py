@@ -75,11 +75,11 @@ def _load():
         "csa2_append_entries": ([P, i32, P, P, P, P, P], i32),
         "csa2_append_tokens": ([P, i32, P, P, P, P, P, P, P], i32),
         "csa2_index_workspace_bytes": ([P, i32], sz),
-        "csa2_index_scores_decode": ([P, i32, P, P, P, P, i64, P], i32),
+        "csa2_index_scores_decode": ([P, i32, P, P, P, P, i64, P, P], i32),
         "csa2_index_topk_decode": ([P, i32, P, P, P, P, P, P, sz, P], i32),
         "csa2_index_topk_prefill": ([P, i32, i32, i64, P, P, P, P, P, sz, P], i32),
-        "csa2_topk_workspace_bytes": ([i32], sz),
-        "csa2_topk": ([i32, P, i64, P, i32, P, P, P, sz, P], i32),
+        "csa2_topk_workspace_bytes": ([i32, i64], sz),
+        "csa2_topk": ([i32, P, i64, P, i32, P, P, P, P, sz, P], i32),
         "csa2_sparse_attn_decode": ([P, i32, P, P, P, P, P, ctypes.c_float, P, P, P], i32),
         "csa2_sparse_attn_prefill": ([P, i32, i32, i64, P, P, i64, i64, P, ctypes.c_float, P, P,
                                       P], i32),
@@ -225,11 +225,14 @@ def _workspace(nbytes: int, device, workspace):
 
 def csa2_index_scores_decode(cache: Cache, q_idx: torch.Tensor, w: torch.Tensor,
                              scores: torch.Tensor, seq_ids: Optional[Sequence[int]] = None,
+                             key_hist: Optional[torch.Tensor] = None,
                              stream=None) -> torch.Tensor:
-    """scores: fp32 [n_queries, ld] (ld a multiple of 4, >= every length)."""
+    """scores: fp32 [n_queries, ld] (ld a multiple of 4, >= every length);
+    key_hist: optional int32 [n_queries, 2048] score-key histogram output."""
     _check(lib.csa2_index_scores_decode(cache.handle, q_idx.shape[0], _ptr(q_idx), _ptr(w),
                                         _i32_array(seq_ids), _ptr(scores), scores.shape[1],
-                                        _stream(stream)), "csa2_index_scores_decode")
+                                        _ptr(key_hist), _stream(stream)),
+           "csa2_index_scores_decode")
     return scores
 
 
@@ -269,14 +272,21 @@ def csa2_index_topk_prefill(cache: Cache, seq: int, pos0: int, q_idx: torch.Tens
     return topk_idx
 
 
+def csa2_topk_workspace_bytes(n_rows: int, max_valid: int) -> int:
+    return int(lib.csa2_topk_workspace_bytes(n_rows, max_valid))
+
+
 def csa2_topk(scores: torch.Tensor, n_valid: Sequence[int], k: int,
               idx_out: Optional[torch.Tensor] = None, score_out: Optional[torch.Tensor] = None,
+              key_hist: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
               stream=None):
     rows, ld = scores.shape
     if idx_out is None:
         idx_out = torch.empty(rows, k, dtype=torch.int32, device=scores.device)
-    _check(lib.csa2_topk(rows, _ptr(scores), ld, _i64_array(n_valid), k, _ptr(idx_out),
-                         _ptr(score_out), None, 0, _stream(stream)), "csa2_topk")
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.csa2_topk(rows, _ptr(scores), ld, _i64_array(n_valid), k, _ptr(key_hist),
+                         _ptr(idx_out), _ptr(score_out), _ptr(workspace), ws_bytes,
+                         _stream(stream)), "csa2_topk")
     return idx_out
 
 

@@ -338,20 +338,32 @@ csa2_status_t csa2_append_tokens(csa2_cache_t* c, int32_t n_seqs, const int32_t*
 
 size_t csa2_index_workspace_bytes(const csa2_cache_t* c, int32_t n_queries) {
   if (!c || n_queries < 0) return 0;
-  return (size_t)n_queries * (size_t)score_ld(c->max_cap) * sizeof(float);
+  return (size_t)n_queries * ((size_t)score_ld(c->max_cap) * sizeof(float) +
+                              kKeyHistBinsHost * sizeof(uint32_t)) +
+         topk_seg_bytes(n_queries, c->max_cap);
 }
 
-size_t csa2_topk_workspace_bytes(int32_t) { return 0; }
+size_t csa2_topk_workspace_bytes(int32_t n_rows, int64_t max_valid) {
+  if (n_rows < 0 || max_valid < 0) return 0;
+  return topk_seg_bytes(n_rows, max_valid);
+}
 
 csa2_status_t csa2_topk(int32_t n_rows, const float* scores, int64_t ld, const int64_t* n_valid,
-                        int32_t k, int32_t* idx_out, float* score_out, void*, size_t,
-                        csa2_stream_t stream) {
+                        int32_t k, const uint32_t* key_hist, int32_t* idx_out, float* score_out,
+                        void* workspace, size_t ws_bytes, csa2_stream_t stream) {
   if (n_rows < 0 || k <= 0 || k > 4096) return CSA2_ERR_INVALID_ARG;
   if (n_rows == 0) return CSA2_OK;
   if (!scores || !n_valid || !idx_out || ld < 0) return CSA2_ERR_INVALID_ARG;
-  for (int r = 0; r < n_rows; ++r)
+  int64_t max_valid = 0;
+  for (int r = 0; r < n_rows; ++r) {
     if (n_valid[r] < 0 || n_valid[r] > ld || n_valid[r] > (int64_t)INT32_MAX)
       return CSA2_ERR_INVALID_ARG;
+    max_valid = std::max(max_valid, n_valid[r]);
+  }
+  const bool seg = key_hist && workspace && aligned16(workspace) &&
+                   ws_bytes >= topk_seg_bytes(n_rows, max_valid) &&
+                   topk_segments(max_valid) <= 1024;
+  const int n_seg = topk_segments(max_valid);
   for (int r0 = 0; r0 < n_rows; r0 += kTopkTab) {
     const int nr = std::min(kTopkTab, n_rows - r0);
     TopkParams* p = new (std::nothrow) TopkParams();
@@ -362,6 +374,11 @@ csa2_status_t csa2_topk(int32_t n_rows, const float* scores, int64_t ld, const i
     p->k = k;
     p->idx_out = idx_out + (int64_t)r0 * k;
     p->score_out = score_out ? score_out + (int64_t)r0 * k : nullptr;
+    p->key_hist = key_hist ? key_hist + (int64_t)r0 * kKeyHistBinsHost : nullptr;
+    p->seg_ws = seg ? static_cast<uint32_t*>(workspace) +
+                          (size_t)r0 * topk_seg_bytes(1, max_valid) / sizeof(uint32_t)
+                    : nullptr;
+    p->n_seg = seg ? n_seg : 0;
     p->formula = 0;
     for (int r = 0; r < nr; ++r) p->n_valid[r] = n_valid[r0 + r];
     cudaError_t e = launch_topk(*p, S(stream));
@@ -379,14 +396,19 @@ namespace {
 // indexer launch per chunk of up to kMaxIdxGroups queries.
 csa2_status_t run_index_decode(const csa2_cache_t* c, int32_t nq, const void* q_idx,
                                const float* w, const int32_t* seq_ids, float* scores, int64_t ld,
-                               csa2_stream_t stream, IndexParams* ip) {
+                               uint32_t* key_hist, csa2_stream_t stream, IndexParams* ip) {
   const uint16_t* qb = static_cast<const uint16_t*>(q_idx);
+  if (key_hist &&
+      cudaMemsetAsync(key_hist, 0, (size_t)nq * kKeyHistBinsHost * sizeof(uint32_t), S(stream)) !=
+          cudaSuccess)
+    return CSA2_ERR_CUDA;
   for (int q0 = 0; q0 < nq; q0 += kMaxIdxGroups) {
     const int n = std::min(kMaxIdxGroups, nq - q0);
     std::memset(ip, 0, sizeof(IndexParams));
     ip->w = w + (int64_t)q0 * kIdxHeads;
     ip->scores = scores + (int64_t)q0 * ld;
     ip->ld = ld;
+    ip->key_hist = key_hist ? key_hist + (int64_t)q0 * kKeyHistBinsHost : nullptr;
     ip->err = c->d_err;
     ip->nq = n;
     ip->qpg = 1;
@@ -432,7 +454,7 @@ extern "C" {
 
 csa2_status_t csa2_index_scores_decode(const csa2_cache_t* c, int32_t nq, const void* q_idx,
                                        const float* w, const int32_t* seq_ids, float* scores,
-                                       int64_t ld, csa2_stream_t stream) {
+                                       int64_t ld, uint32_t* key_hist, csa2_stream_t stream) {
   if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
   if (nq == 0) return CSA2_OK;
   csa2_status_t st = check_decode_queries(c, nq, q_idx, w, seq_ids);
@@ -442,7 +464,8 @@ csa2_status_t csa2_index_scores_decode(const csa2_cache_t* c, int32_t nq, const 
     if (c->len[seq_ids ? seq_ids[i] : i] > ld) return CSA2_ERR_CAPACITY;
   IndexParams* ip = new (std::nothrow) IndexParams();
   if (!ip) return CSA2_ERR_OOM;
-  st = run_index_decode(c, nq, q_idx, w, seq_ids, scores, ld, stream, ip);
+  if (key_hist && !aligned16(key_hist)) { delete ip; return CSA2_ERR_INVALID_ARG; }
+  st = run_index_decode(c, nq, q_idx, w, seq_ids, scores, ld, key_hist, stream, ip);
   delete ip;
   return st;
 }
@@ -459,10 +482,12 @@ csa2_status_t csa2_index_topk_decode(const csa2_cache_t* c, int32_t nq, const vo
   if (ws_bytes < csa2_index_workspace_bytes(c, nq)) return CSA2_ERR_CAPACITY;
   const int64_t ld = score_ld(c->max_cap);
   float* scores = static_cast<float*>(workspace);
+  uint32_t* key_hist = reinterpret_cast<uint32_t*>(scores + (int64_t)nq * ld);
+  uint32_t* seg_ws = key_hist + (int64_t)nq * kKeyHistBinsHost;
   IndexParams* ip = new (std::nothrow) IndexParams();
   TopkParams* tp = new (std::nothrow) TopkParams();
   if (!ip || !tp) { delete ip; delete tp; return CSA2_ERR_OOM; }
-  st = run_index_decode(c, nq, q_idx, w, seq_ids, scores, ld, stream, ip);
+  st = run_index_decode(c, nq, q_idx, w, seq_ids, scores, ld, key_hist, stream, ip);
   const int k = c->cfg.topk;
   for (int q0 = 0; q0 < nq && st == CSA2_OK; q0 += kTopkTab) {
     const int n = std::min(kTopkTab, nq - q0);
@@ -473,6 +498,11 @@ csa2_status_t csa2_index_topk_decode(const csa2_cache_t* c, int32_t nq, const vo
     tp->k = k;
     tp->idx_out = topk_idx + (int64_t)q0 * k;
     tp->score_out = topk_score ? topk_score + (int64_t)q0 * k : nullptr;
+    tp->key_hist = key_hist + (int64_t)q0 * kKeyHistBinsHost;
+    const bool use_seg = topk_segments(c->max_cap) <= 1024;
+    tp->seg_ws = use_seg ? seg_ws + (size_t)q0 * topk_seg_bytes(1, c->max_cap) / sizeof(uint32_t)
+                         : nullptr;
+    tp->n_seg = use_seg ? topk_segments(c->max_cap) : 0;
     tp->formula = 0;
     for (int i = 0; i < n; ++i) tp->n_valid[i] = c->len[seq_ids ? seq_ids[q0 + i] : q0 + i];
     if (launch_topk(*tp, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;

@@ -211,6 +211,20 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- score keys
+// Order-preserving 32-bit key of an fp32 score (-0 folded to +0): the
+// sign bit is set for non-negative values, all bits are inverted for
+// negative ones, so unsigned key order is score order.
+__device__ __forceinline__ uint32_t score_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u << 1) == 0u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_score(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+constexpr int kKeyHistBins = kKeyHistBinsHost;   // top 11 bits of the key
+
 // ---------------------------------------------------------------- numerics
 // E2M1 code of v (round to nearest, ties to the even code, saturating at 6);
 // the sign bit of v becomes bit 3.  Decision boundaries are the midpoints of
@@ -265,12 +279,18 @@ __device__ __forceinline__ void e2m1x8_to_bf16x8(uint32_t codes, uint32_t (&out)
   constexpr uint32_t kLoA = 0xC0800000u, kLoB = 0xC0804000u;
   constexpr uint32_t kHiA = 0x3F3F3F00u, kHiB = 0x40404040u;
   const uint32_t s0 = codes & 0x7777u, s1 = (codes >> 16) & 0x7777u;
-  const uint32_t l0 = prmt(kLoA, kLoB, s0), h0 = prmt(kHiA, kHiB, s0);
-  const uint32_t l1 = prmt(kLoA, kLoB, s1), h1 = prmt(kHiA, kHiB, s1);
-  out[0] = prmt(l0, h0, 0x5140u) | ((codes << 12) & 0x8000u) | ((codes << 24) & 0x80000000u);
-  out[1] = prmt(l0, h0, 0x7362u) | ((codes << 4) & 0x8000u) | ((codes << 16) & 0x80000000u);
-  out[2] = prmt(l1, h1, 0x5140u) | ((codes >> 4) & 0x8000u) | ((codes << 8) & 0x80000000u);
-  out[3] = prmt(l1, h1, 0x7362u) | ((codes >> 12) & 0x8000u) | (codes & 0x80000000u);
+  // sign bytes: PRMT's sign-replicate mode copies bit 7 of the selected byte;
+  // bit 7 of byte i holds the sign of code 2i+1, and after a shift by 4 the
+  // sign of code 2i.
+  const uint32_t ev = codes << 4;
+  const uint32_t sg0 = prmt(ev, codes, 0xD9C8u) & 0x80808080u;  // codes 0..3
+  const uint32_t sg1 = prmt(ev, codes, 0xFBEAu) & 0x80808080u;  // codes 4..7
+  const uint32_t l0 = prmt(kLoA, kLoB, s0), h0 = prmt(kHiA, kHiB, s0) | sg0;
+  const uint32_t l1 = prmt(kLoA, kLoB, s1), h1 = prmt(kHiA, kHiB, s1) | sg1;
+  out[0] = prmt(l0, h0, 0x5140u);
+  out[1] = prmt(l0, h0, 0x7362u);
+  out[2] = prmt(l1, h1, 0x5140u);
+  out[3] = prmt(l1, h1, 0x7362u);
 }
 
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {

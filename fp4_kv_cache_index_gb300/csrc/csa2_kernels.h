@@ -16,6 +16,7 @@ constexpr int kHeadDim = 512;     // main-KV latent / attention head dim
 constexpr int kIdxDim = 128;      // indexer head dim
 constexpr int kIdxHeads = 32;     // indexer heads
 constexpr int kCodeBytes = kHeadDim / 2;
+constexpr int kKeyHistBinsHost = 2048;   // score-key histogram bins (top 11 key bits)
 
 // ---------------------------------------------------------------- append
 constexpr int kMaxAppendSegs = 64;
@@ -52,6 +53,7 @@ struct IndexParams {
   const float* w;          // [nq, 32]
   float* scores;           // [nq, ld]
   int64_t ld;
+  uint32_t* key_hist;      // nullable [nq, 2048] score-key histogram (qpg == 1 only)
   uint32_t* err;
   int32_t nq;
   int32_t qpg;             // queries per group (1 decode, 8 prefill)
@@ -77,14 +79,22 @@ struct TopkParams {
   int64_t ld;
   int32_t rows;
   int32_t k;
+  const uint32_t* key_hist;  // nullable [rows, 2048] score-key histogram
   int32_t* idx_out;          // [rows, k]
   float* score_out;          // nullable [rows, k]
   int32_t formula;           // 1: n_valid(r) = min(len, (pos0 + r + 1) / ratio)
   int32_t pre_len;
   int32_t ratio;
   int64_t pos0;
+  uint32_t* seg_ws;          // nullable: per-segment candidate buffers (see topk_seg_bytes)
+  int32_t n_seg;             // segments per row when seg_ws is set
   int64_t n_valid[kTopkTab]; // formula == 0: per-row valid counts
 };
+// Segmented candidate compaction (rows with a score-key histogram): scratch
+// bytes for `rows` rows of up to `max_valid` scores, and its segment count.
+constexpr int kTopkSegLen = 8192;
+int topk_segments(int64_t max_valid);
+size_t topk_seg_bytes(int32_t rows, int64_t max_valid);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
 
 // ---------------------------------------------------------------- attention

@@ -10,8 +10,9 @@
 //
 // One CTA = one query x 32 heads.  Candidates come in tiles of 128 rows: the
 // window tile (TMA straight into swizzled shared memory) and the top-k tiles
-// (cp.async gather of 256 B codes + scales per entry, one tile ahead, then
-// E2M1 -> bf16 via byte permutes and a bf16 scale multiply).  With the
+// (each thread loads a quarter of an entry's 256 B of codes plus its scale
+// bytes into registers, one tile ahead; then E2M1 -> bf16 via byte permutes
+// and a bf16 scale multiply, written to shared memory in the MMA layout).  With the
 // candidate rows as the MMA M dimension:
 //     S^T[128 x 32]  = KV[128 x 512] * Q[32 x 512]^T        (K-major A and B)
 //     O^T[512 x 32] += KV^T[512 x 128] * P^T[128 x 32]^T     (MN-major A)
@@ -27,19 +28,17 @@
 namespace csa2 {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;     // 16 warps: all gather/dequantise, warps 0-7 run the softmax
 constexpr int kHG = 32;               // heads per CTA
 constexpr int kRows = 128;            // candidates per tile
-constexpr int kStageStride = 272;     // padded staging row for 256 B of codes
 constexpr int kMaxTiles = 2048 / kRows + 1;
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kKvOff = 0;                              // 8 x [128 x 128 B]
 constexpr int kQOff = kKvOff + kRows * kHeadDim * 2;   // 8 x [32 x 128 B]
 constexpr int kPOff = kQOff + kHG * kHeadDim * 2;      // 2 x [32 x 128 B]
-constexpr int kStCodesOff = kPOff + kHG * kRows * 2;
-constexpr int kStScalesOff = kStCodesOff + kRows * kStageStride;
-constexpr int kSmallOff = kStScalesOff + kRows * 32;
+constexpr int kIdxOff = kPOff + kHG * kRows * 2;        // the query's top-k row
+constexpr int kSmallOff = kIdxOff + 2048 * 4;
 struct Small {
   float red_max[4][kHG];
   float red_sum[4][kHG];
@@ -47,7 +46,7 @@ struct Small {
   float l[kHG];
   float alpha[kHG];
   int32_t tile_list[kMaxTiles];
-  int32_t tile_any[kMaxTiles];
+  int32_t tile_any[kMaxTiles];   // top-k tile holds a usable index
   uint8_t row_valid[kRows];
   int32_t n_tiles;
   int32_t need_rescale;
@@ -55,18 +54,6 @@ struct Small {
   uint64_t bar_q, bar_kv, bar_mma;
 };
 constexpr int kSmemBytes = kSmallOff + (int)sizeof(Small) + 1024;
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
-}
 
 // Reduce-scatter over the 32 lanes of a warp: v[0..15] (16 heads) in, lane L
 // ends with the reduction for head (L >> 1) in v[0].
@@ -116,8 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* kv = smem + kKvOff;
   uint8_t* qs = smem + kQOff;
   uint8_t* ps = smem + kPOff;
-  uint8_t* st_codes = smem + kStCodesOff;
-  uint8_t* st_scales = smem + kStScalesOff;
+  int32_t* idx_s = reinterpret_cast<int32_t*>(smem + kIdxOff);
   Small& sm = *reinterpret_cast<Small*>(smem + kSmallOff);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -167,12 +153,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < 8; ++c)
       tma_load_2d(qs + c * (kHG * 128), &tm_q, 64 * c, q * p.n_heads + hg * kHG, &sm.bar_q);
   }
-  // which top-k tiles hold at least one usable index
+  // the top-k row into shared memory (unusable slots become -1), and which
+  // tiles hold at least one usable index
   bool bad = false;
   for (int i = tid; i < p.topk; i += kThreads) {
-    const int32_t s = idx_row[i];
+    int32_t s = idx_row[i];
     if (s >= 0 && s < len) sm.tile_any[i / kRows] = 1;
-    else if (s >= len) bad = true;
+    else {
+      if (s >= len) bad = true;
+      s = -1;
+    }
+    idx_s[i] = s;
   }
   if (bad) set_error(p.err, kErrIndex);
   __syncthreads();
@@ -186,30 +177,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   const int n_tiles = sm.n_tiles;
 
-  // gather of one top-k tile into the staging buffers (zero-fill for unused slots)
-  auto stage_tile = [&](int j) {
-    const int e = tid >> 1, half = tid & 1;
-    const int32_t s = idx_row[j * kRows + e];
-    const bool ok = (s >= 0 && s < len);
-    const int64_t row = ok ? base + s : 0;
-    const uint8_t* src = p.codes + row * kCodeBytes + half * 128;
-    const uint32_t dst = smem_u32(st_codes + e * kStageStride + half * 128);
+  // Gather of one top-k tile into registers: thread (entry e = 8 warp +
+  // lane % 8, quarter q = lane / 8) loads bytes [64 q, 64 q + 64) of entry e's
+  // codes and the scales of its 128 channels.  Issued one tile ahead, so the
+  // loads are in flight while the previous tile runs on the tensor cores.
+  const int g_e = warp * 8 + (lane & 7), g_q = lane >> 3;
+  uint4 cw[4];
+  uint2 scw;
+  auto prefetch_tile = [&](int j) {
+    const int32_t s = idx_s[j * kRows + g_e];
+    if (s >= 0) {
+      const int64_t row = base + s;
+      const uint4* src = reinterpret_cast<const uint4*>(p.codes + row * kCodeBytes + g_q * 64);
 #pragma unroll
-    for (int c = 0; c < 8; ++c) cp_async16(dst + 16 * c, src + 16 * c, ok ? 16u : 0u);
-    const int sbytes = (p.layout == 0) ? 16 : 32;
-    if (half * 16 < sbytes)
-      cp_async16(smem_u32(st_scales + e * 32 + half * 16),
-                 p.scales + row * sbytes + half * 16, ok ? 16u : 0u);
-    cp_async_commit();
+      for (int i = 0; i < 4; ++i) cw[i] = __ldg(src + i);
+      if (p.layout == 0)
+        scw = make_uint2(__ldg(reinterpret_cast<const uint32_t*>(p.scales + row * 16) + g_q), 0u);
+      else
+        scw = __ldg(reinterpret_cast<const uint2*>(p.scales + row * 32) + g_q);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cw[i] = make_uint4(0u, 0u, 0u, 0u);
+      scw = make_uint2(0u, 0u);
+    }
   };
 
-  int next_topk = 0;  // position in tile_list of the next tile to stage
+  int next_topk = 0;  // position in tile_list of the next tile to gather
   while (next_topk < n_tiles && sm.tile_list[next_topk] < 0) ++next_topk;
-  if (next_topk < n_tiles) stage_tile(sm.tile_list[next_topk]);
+  if (next_topk < n_tiles) prefetch_tile(sm.tile_list[next_topk]);
 
   uint32_t mma_phase = 0;
   bool ok = true;
-  const int quad = warp & 3, hh = warp >> 2;
+  const int quad = warp & 3, hh = (warp >> 2) & 1;
   const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
 
   for (int ti = 0; ti < n_tiles && ok; ++ti) {
@@ -227,53 +226,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __syncthreads_and(ok);
       if (!ok) break;
     } else {
-      cp_async_wait_all();
-      __syncthreads();
-      if (tid < kRows) {
-        const int32_t s = idx_row[tile * kRows + tid];
-        sm.row_valid[tid] = (s >= 0 && s < len);
-      }
-      // dequantise: warp w owns entries [16 w, 16 w + 16)
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        const int e = warp * 16 + half * 8 + (lane & 7);
-#pragma unroll 2
-        for (int round = 0; round < 8; ++round) {
-          const int j = round * 4 + (lane >> 3);  // 16-channel group
-          const uint2 c = *reinterpret_cast<const uint2*>(st_codes + e * kStageStride + j * 8);
-          uint32_t sb;
-          float sf;
-          if (p.layout == 0) {
-            sb = st_scales[e * 32 + (j >> 1)];
-            sf = ue8m0_value(sb);
-          } else {
-            sb = st_scales[e * 32 + j];
-            sf = fabsf(e4m3_value(sb));
-          }
-          const uint32_t s16 = float_to_bf16_bits(sf);
-          const uint32_t s2 = s16 | (s16 << 16);
-          uint32_t lo[4], hi[4];
-          e2m1x8_to_bf16x8(c.x, lo);
-          e2m1x8_to_bf16x8(c.y, hi);
-          uint4 w0, w1;
-          w0.x = bf16x2_mul(lo[0], s2); w0.y = bf16x2_mul(lo[1], s2);
-          w0.z = bf16x2_mul(lo[2], s2); w0.w = bf16x2_mul(lo[3], s2);
-          w1.x = bf16x2_mul(hi[0], s2); w1.y = bf16x2_mul(hi[1], s2);
-          w1.z = bf16x2_mul(hi[2], s2); w1.w = bf16x2_mul(hi[3], s2);
-          const int cb = j >> 2, ch = 2 * (j & 3);
-          uint8_t* rowp = kv + cb * (kRows * 128) + e * 128;
-          *reinterpret_cast<uint4*>(rowp + (((ch) ^ (e & 7)) << 4)) = w0;
-          *reinterpret_cast<uint4*>(rowp + (((ch + 1) ^ (e & 7)) << 4)) = w1;
+      if (tid < kRows) sm.row_valid[tid] = idx_s[tile * kRows + tid] >= 0;
+      // dequantise the registers of this thread: channels [128 q, 128 q + 128)
+      // of entry e, 32 channels (4 words of codes) per step
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t s2a, s2b;
+        if (p.layout == 0) {
+          const uint32_t b = (scw.x >> (8 * i)) & 0xFFu;          // one scale per 32
+          const uint32_t s16 = float_to_bf16_bits(ue8m0_value(b));
+          s2a = s2b = s16 | (s16 << 16);
+        } else {
+          const uint32_t w = i < 2 ? scw.x : scw.y;               // one scale per 16
+          const uint32_t ba = (w >> (16 * (i & 1))) & 0xFFu, bb = (w >> (16 * (i & 1) + 8)) & 0xFFu;
+          const uint32_t sa = float_to_bf16_bits(fabsf(e4m3_value(ba)));
+          const uint32_t sb = float_to_bf16_bits(fabsf(e4m3_value(bb)));
+          s2a = sa | (sa << 16);
+          s2b = sb | (sb << 16);
+        }
+        const uint32_t words[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
+        const int cb = 2 * g_q + (i >> 1);
+        uint8_t* rowp = kv + cb * (kRows * 128) + g_e * 128;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint32_t v[4];
+          e2m1x8_to_bf16x8(words[k], v);
+          const uint32_t s2 = k < 2 ? s2a : s2b;
+          uint4 o;
+          o.x = bf16x2_mul(v[0], s2); o.y = bf16x2_mul(v[1], s2);
+          o.z = bf16x2_mul(v[2], s2); o.w = bf16x2_mul(v[3], s2);
+          const int chunk = (i & 1) * 4 + k;
+          *reinterpret_cast<uint4*>(rowp + ((chunk ^ (g_e & 7)) << 4)) = o;
         }
       }
-      __syncthreads();
-      // staging is free again: fetch the next top-k tile behind this one
-      ++next_topk;
-      while (next_topk < n_tiles && sm.tile_list[next_topk] < 0) ++next_topk;
-      if (next_topk < n_tiles) stage_tile(sm.tile_list[next_topk]);
     }
     fence_proxy_async_smem();
     __syncthreads();
+    if (tile >= 0) {
+      // the registers are free: fetch the next top-k tile behind this one
+      // (after the proxy fence, which would otherwise wait for these loads)
+      ++next_topk;
+      while (next_topk < n_tiles && sm.tile_list[next_topk] < 0) ++next_topk;
+      if (next_topk < n_tiles) prefetch_tile(sm.tile_list[next_topk]);
+    }
 
     // ------------------------------------------------ B: S^T = KV * Q^T
     if (tid == 0) {
@@ -296,21 +291,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) break;
     tc_fence_after();
 
-    // ------------------------------------------------ C: online softmax
+    // ------------------------------------------------ C: online softmax (warps 0-7)
+    const bool sw = warp < 8;
     const int row = quad * 32 + lane;
     const bool valid = sm.row_valid[row] != 0;
     float x[16], v[16];
-    {
+    if (sw) {
       uint32_t r[16];
       tmem_ld16(tmem + lane_addr + s_col + 16 * hh, r);
-      tmem_wait_ld();
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         x[i] = valid ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
         v[i] = x[i];
       }
-    }
-    {
       const float mx = warp_reduce_scatter16<true>(v, lane);
       if ((lane & 1) == 0) sm.red_max[quad][16 * hh + (lane >> 1)] = mx;
     }
@@ -326,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (a != 1.0f && ti > 0) sm.need_rescale = 1;
     }
     __syncthreads();
-    {
+    if (sw) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int h = 16 * hh + i;
@@ -346,14 +339,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid < kHG)
       sm.l[tid] = sm.alpha[tid] * sm.l[tid] + ((sm.red_sum[0][tid] + sm.red_sum[1][tid]) +
                                                (sm.red_sum[2][tid] + sm.red_sum[3][tid]));
-    if (sm.need_rescale) {
+    if (sw && sm.need_rescale) {
       // O^T lanes are head-dim rows, columns are heads: scale column h by alpha[h]
 #pragma unroll 1
       for (int i = 0; i < 4; ++i) {
         uint32_t r[16];
         const uint32_t a = tmem + lane_addr + o_col + 32 * i + 16 * hh;
         tmem_ld16(a, r);
-        tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           r[c] = __float_as_uint(__uint_as_float(r[c]) * sm.alpha[16 * hh + c]);
@@ -387,11 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = __syncthreads_and(ok);
     tc_fence_after();
   }
-  cp_async_wait_all();
-
   // ------------------------------------------------ epilogue
   __syncthreads();
   if (ok && n_tiles > 0) {
+    const bool ew = warp < 8;
     if (tid < kHG) {
       const float l = sm.l[tid];
       sm.alpha[tid] = l > 0.0f ? 1.0f / l : 0.0f;
@@ -401,10 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
 #pragma unroll 1
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 4 && ew; ++i) {
       uint32_t r[16];
       tmem_ld16(tmem + lane_addr + o_col + 32 * i + 16 * hh, r);
-      tmem_wait_ld();
       const int d = 128 * i + quad * 32 + lane;
 #pragma unroll
       for (int c = 0; c < 16; ++c) {

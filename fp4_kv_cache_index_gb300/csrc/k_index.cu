@@ -27,14 +27,15 @@ constexpr int kKStageBytes = kTileE * kIdxDim * 2;  // 32 KB
 constexpr int kThreads = 192;
 
 struct SmemLayout {
-  int q_off, w_off, bar_off, total;
+  int q_off, w_off, hist_off, bar_off, total;
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int qpg) {
   SmemLayout L;
   L.q_off = kStages * kKStageBytes;
   L.w_off = L.q_off + qpg * 32 * kIdxDim * 2;
-  L.bar_off = L.w_off + qpg * 32 * 4;
+  L.hist_off = L.w_off + qpg * 32 * 4;
+  L.bar_off = L.hist_off + kKeyHistBins * 4;
   L.total = L.bar_off + 16 * 8 + 16 + 1024;  // barriers, tmem slot, alignment slack
   return L;
 }
@@ -60,6 +61,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* kbuf = smem;
   uint8_t* qbuf = smem + L.q_off;
   float* wbuf = reinterpret_cast<float*>(smem + L.w_off);
+  uint32_t* hs = reinterpret_cast<uint32_t*>(smem + L.hist_off);  // score-key histogram
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* k_full = bars;              // [kStages]
   uint64_t* k_empty = bars + 4;         // [kStages]
@@ -170,11 +172,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;                 // TMEM lane quadrant of this warp
     const int row = quad * 32 + lane;          // entry within the tile
     const int et = threadIdx.x - 64;           // 0..127
+    const bool use_hist = p.key_hist != nullptr && p.qpg == 1;
+    // adds this CTA's counts of query `qq` to the global histogram, clears hs
+    auto flush = [&](int qq) {
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      for (int i = et; i < kKeyHistBins; i += 128) {
+        const uint32_t v = hs[i];
+        if (v) atomicAdd(p.key_hist + (int64_t)qq * kKeyHistBins + i, v);
+        hs[i] = 0u;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+    };
+    if (use_hist) {
+      for (int i = et; i < kKeyHistBins; i += 128) hs[i] = 0u;
+    }
     int g = g0, cur = -1, acc = 0;
     uint32_t aph = 0;
     for (int it = begin; it < end; ++it) {
       while (p.tile_prefix[g + 1] <= it) ++g;
       if (g != cur) {
+        if (use_hist && cur >= 0) flush(cur);
         asm volatile("bar.sync 1, 128;" ::: "memory");
         for (int i = et; i < qrows; i += 128) {
           const int q = g * p.qpg + (i >> 5);
@@ -190,18 +207,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < p.qpg; ++j) {
         uint32_t r[32];
         tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * N + j * 32), r);
-        tmem_wait_ld();
         const float* wj = wbuf + j * 32;
         float s = 0.0f;
 #pragma unroll
         for (int h = 0; h < 32; ++h) s = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.0f), s);
         const int q = g * p.qpg + j;
-        if (q < p.nq && e < group_nvis_query(p, g, j)) p.scores[(int64_t)q * p.ld + e] = s;
+        if (q < p.nq && e < group_nvis_query(p, g, j)) {
+          p.scores[(int64_t)q * p.ld + e] = s;
+          if (use_hist) atomicAdd(hs + (score_key(s) >> 21), 1u);
+        }
       }
       tc_fence_before();
       mbar_arrive(acc_empty + acc);
       if (++acc == 2) { acc = 0; aph ^= 1; }
     }
+    if (use_hist && cur >= 0) flush(cur);
   }
 
   tc_fence_before();

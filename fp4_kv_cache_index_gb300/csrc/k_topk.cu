@@ -3,15 +3,22 @@
 // V4.1 report section 4.2.1: k = 512).
 //
 // One CTA per row.  Scores become order-preserving 32-bit keys (-0 folded to
-// +0).  A radix select over the digits [31:21], [20:10], [9:0] finds the k-th
-// largest key T and the count of keys above it:
-//   - digit 1 is a shared-memory histogram of the whole row;
-//   - when the bin holding T is small, its keys are gathered into shared
-//     memory and digits 2-3 run there; otherwise digits 2-3 re-read the row.
-// A final ordered pass emits, in increasing index order, every key > T and
-// the first (k - count_above) keys == T, so ties go to the lower index and
-// the output is sorted by index.  Integer atomics only: the result is the
-// same on every run.
+// +0).  The k-th largest key T is found by a radix select over the digits
+// [31:21], [20:10], [9:0]:
+//   1. the digit-1 histogram comes from the indexer (score-key histogram) or
+//      from one pass over the row into eight replicated shared histograms;
+//      it gives the bin b1 that holds T and the count of keys above b1;
+//   2. when those candidates (keys in bins >= b1, a few thousand for
+//      continuous scores) fit in shared memory, one ordered pass compacts
+//      them, in index order, and digits 2-3 plus the emission run there;
+//      With a score-key histogram and a scratch buffer, that compaction is
+//      split over segments of 8192 scores, one CTA each (k_topk_seg), and
+//      the row's CTA reads the segments back in order;
+//   3. otherwise (many equal or nearly equal scores) digits 2-3 and the
+//      emission re-read the row.
+// Emission writes, in increasing index order, every key > T and the first
+// (k - count above T) keys == T: ties go to the lower index.  Integer
+// atomics only, so the result is the same on every run.
 #include "csa2_device.cuh"
 #include "csa2_kernels.h"
 
@@ -22,24 +29,24 @@ constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kCandCap = 8192;
+constexpr int kSubHists = 8;
 
-__device__ __forceinline__ uint32_t score_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  if ((u << 1) == 0u) u = 0u;  // -0 == +0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 struct Shared {
   uint32_t hist[kBins];
-  uint32_t cand[kCandCap];
+  union {
+    struct {
+      uint32_t key[kCandCap];
+      int32_t idx[kCandCap];
+    } cand;
+    uint32_t sub[kSubHists][kBins];
+  } u;
   uint32_t warp_sum[kWarps];
-  uint32_t n_cand;
   uint32_t sel_bin;
   uint32_t sel_above;
-  uint32_t done;
 };
 
-// Inclusive suffix sum over the block (thread t gets sum over t' >= t).
+// Inclusive suffix sum over the block (thread t gets the sum over t' >= t).
 __device__ __forceinline__ uint32_t block_suffix_sum(uint32_t v, Shared& sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -56,7 +63,7 @@ __device__ __forceinline__ uint32_t block_suffix_sum(uint32_t v, Shared& sh) {
       const uint32_t n = __shfl_down_sync(0xffffffffu, w, o);
       if (lane + o < 32) w += n;
     }
-    sh.warp_sum[lane] = w;  // inclusive suffix over warps
+    sh.warp_sum[lane] = w;
   }
   __syncthreads();
   const uint32_t later = (warp + 1 < kWarps) ? sh.warp_sum[warp + 1] : 0u;
@@ -64,7 +71,7 @@ __device__ __forceinline__ uint32_t block_suffix_sum(uint32_t v, Shared& sh) {
   return v + later;
 }
 
-// Inclusive prefix sum over the block.
+// Inclusive prefix sum over the block; `total` gets the block sum.
 __device__ __forceinline__ uint32_t block_prefix_sum(uint32_t v, Shared& sh, uint32_t& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -90,21 +97,22 @@ __device__ __forceinline__ uint32_t block_prefix_sum(uint32_t v, Shared& sh, uin
   return v + before;
 }
 
-// Adds one to hist[bin] for every active lane, one atomic per distinct bin.
-__device__ __forceinline__ void hist_add(uint32_t* hist, bool active, uint32_t bin) {
+// One atomic per distinct bin of the warp (for rows whose keys may all be
+// equal); called by full warps only.
+__device__ __forceinline__ void hist_add_aggregated(uint32_t* hist, bool active, uint32_t bin) {
   const uint32_t key = active ? bin : 0xFFFFFFFFu;
   const uint32_t peers = __match_any_sync(0xffffffffu, key);
-  const int lane = threadIdx.x & 31;
-  if (active && lane == __ffs(peers) - 1) atomicAdd(hist + bin, (uint32_t)__popc(peers));
+  if (active && (int)(threadIdx.x & 31) == __ffs(peers) - 1)
+    atomicAdd(hist + bin, (uint32_t)__popc(peers));
 }
 
-// Picks the bin holding the rem-th largest key among those counted in hist
-// (nbins <= 2 * kThreads); records it and the count strictly above it.
+// Bin holding the rem-th largest key counted in hist (nbins <= 2 * kThreads);
+// records it and the count strictly above it.
 __device__ __forceinline__ void select_bin(Shared& sh, int nbins, uint32_t rem) {
   const int t = threadIdx.x;
   const uint32_t h0 = (2 * t < nbins) ? sh.hist[2 * t] : 0u;
   const uint32_t h1 = (2 * t + 1 < nbins) ? sh.hist[2 * t + 1] : 0u;
-  const uint32_t suf = block_suffix_sum(h0 + h1, sh);  // sum over bins >= 2t
+  const uint32_t suf = block_suffix_sum(h0 + h1, sh);  // bins >= 2t
   const uint32_t suf1 = suf - h0;                        // bins >= 2t+1
   const uint32_t suf2 = suf1 - h1;                       // bins >= 2t+2
   if (2 * t + 1 < nbins && suf1 >= rem && suf2 < rem) { sh.sel_bin = 2 * t + 1; sh.sel_above = suf2; }
@@ -112,19 +120,133 @@ __device__ __forceinline__ void select_bin(Shared& sh, int nbins, uint32_t rem) 
   __syncthreads();
 }
 
-__device__ __forceinline__ void load4(const float* row, int64_t e, int64_t n, bool vec, float (&v)[4]) {
-  if (vec && e + 3 < n) {
-    const float4 f = __ldg(reinterpret_cast<const float4*>(row + e));
-    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+// Each thread takes kPer consecutive scores per chunk (four 16-byte loads in
+// flight when the row is 16-byte aligned).
+constexpr int kPer = 8;
+__device__ __forceinline__ void load_run(const float* row, int64_t e, int64_t n, bool vec,
+                                         float (&v)[kPer]) {
+  if (vec && e + kPer - 1 < n) {
+#pragma unroll
+    for (int q = 0; q < kPer / 4; ++q) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(row + e) + q);
+      v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+    }
   } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = (e + i < n) ? __ldg(row + e + i) : 0.0f;
+    for (int i = 0; i < kPer; ++i) v[i] = (e + i < n) ? __ldg(row + e + i) : 0.0f;
   }
 }
 
-__device__ __forceinline__ void clear_hist(Shared& sh) {
-  for (int i = threadIdx.x; i < kBins; i += kThreads) sh.hist[i] = 0u;
+__device__ __forceinline__ void clear(uint32_t* h, int n) {
+  for (int i = threadIdx.x; i < n; i += kThreads) h[i] = 0u;
   __syncthreads();
+}
+
+// Scratch of one (row, segment): [count][pad to 16 B][key x cap][idx x cap].
+constexpr int kSegWords = 4 + 2 * kCandCap;
+
+__device__ __forceinline__ int64_t row_valid_count(const TopkParams& p, int row) {
+  if (p.formula) {
+    const int64_t v = (p.pos0 + row + 1) / p.ratio;
+    return v < p.pre_len ? v : p.pre_len;
+  }
+  return p.n_valid[row];
+}
+
+// Ordered compaction of one segment's candidates (keys in bins >= b1).  256
+// threads, each owning 32 consecutive scores whose loads are issued before
+// the threshold is computed from the histogram.
+constexpr int kSegThreads = 256;
+constexpr int kSegPer = kTopkSegLen / kSegThreads;  // 32
+struct SegShared {
+  uint32_t hist[kBins];
+  uint32_t warp_sum[kSegThreads / 32];
+  uint32_t sel_bin, sel_above;
+};
+
+__global__ void __launch_bounds__(kSegThreads) k_topk_seg(const __grid_constant__ TopkParams p,
+                                                          int row0) {
+  __shared__ SegShared sh;
+  const int row = row0 + blockIdx.y, seg = blockIdx.x, tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  if (row >= p.rows) return;
+  const int64_t n = row_valid_count(p, row);
+  uint32_t* out = p.seg_ws + ((int64_t)row * p.n_seg + seg) * kSegWords;
+  const int64_t s0 = (int64_t)seg * kTopkSegLen;
+  if (n <= p.k || s0 >= n) {
+    if (tid == 0) out[0] = 0u;
+    return;
+  }
+  const float* srow = p.scores + (int64_t)row * p.ld;
+  const int64_t e0 = s0 + (int64_t)tid * kSegPer;
+  float v[kSegPer];
+  const bool vec = ((reinterpret_cast<uintptr_t>(srow) & 15u) == 0) && e0 + kSegPer <= n;
+  if (vec) {
+#pragma unroll
+    for (int q = 0; q < kSegPer / 4; ++q) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(srow + e0) + q);
+      v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kSegPer; ++i) v[i] = (e0 + i < n) ? __ldg(srow + e0 + i) : 0.0f;
+  }
+  // threshold bin from the histogram (bins >= 2t over 256 threads x 8 bins)
+  const uint32_t* hrow = p.key_hist + (int64_t)row * kBins;
+  uint32_t h[8], hs = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) { h[i] = hrow[8 * tid + i]; hs += h[i]; }
+  uint32_t suf = hs;  // inclusive suffix over threads
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_down_sync(0xffffffffu, suf, o);
+    if (lane + o < 32) suf += t;
+  }
+  if (lane == 0) sh.warp_sum[warp] = suf;
+  __syncthreads();
+  uint32_t later = 0;
+  for (int w = warp + 1; w < kSegThreads / 32; ++w) later += sh.warp_sum[w];
+  suf += later;                       // keys in bins >= 8 tid
+  const uint32_t k = (uint32_t)p.k;
+  uint32_t above_mine = suf - hs;     // keys in bins >= 8 tid + 8
+#pragma unroll
+  for (int i = 7; i >= 0; --i) {
+    if (above_mine < k && above_mine + h[i] >= k) { sh.sel_bin = 8 * tid + i; sh.sel_above = above_mine; }
+    above_mine += h[i];
+  }
+  __syncthreads();
+  const uint32_t b1 = sh.sel_bin;
+  if (sh.sel_above + p.key_hist[(int64_t)row * kBins + b1] > (uint32_t)kCandCap) return;
+  // ordered compaction
+  uint32_t cnt = 0;
+#pragma unroll
+  for (int i = 0; i < kSegPer; ++i) cnt += (e0 + i < n && (score_key(v[i]) >> 21) >= b1);
+  uint32_t incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  __syncthreads();
+  if (lane == 31) sh.warp_sum[warp] = incl;
+  __syncthreads();
+  uint32_t before = 0, total = 0;
+  for (int w = 0; w < kSegThreads / 32; ++w) {
+    const uint32_t ws = sh.warp_sum[w];
+    if (w < warp) before += ws;
+    total += ws;
+  }
+  uint32_t pos = before + incl - cnt;
+#pragma unroll
+  for (int i = 0; i < kSegPer; ++i) {
+    const uint32_t key = score_key(v[i]);
+    if (e0 + i < n && (key >> 21) >= b1 && pos < (uint32_t)kCandCap) {
+      out[4 + pos] = key;
+      out[4 + kCandCap + pos] = (uint32_t)(e0 + i);
+      ++pos;
+    }
+  }
+  if (tid == 0) out[0] = total < (uint32_t)kCandCap ? total : (uint32_t)kCandCap;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ TopkParams p,
@@ -133,157 +255,217 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
   const int row = row0 + blockIdx.x;
   if (row >= p.rows) return;
-  int64_t n;
-  if (p.formula) {
-    const int64_t v = (p.pos0 + row + 1) / p.ratio;
-    n = v < p.pre_len ? v : p.pre_len;
-  } else {
-    n = p.n_valid[row];
-  }
+  const int64_t n = row_valid_count(p, row);
   const int k = p.k;
   const float* srow = p.scores + (int64_t)row * p.ld;
   int32_t* orow = p.idx_out + (int64_t)row * k;
   float* osc = p.score_out ? p.score_out + (int64_t)row * k : nullptr;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5;
 
   if (n <= k) {
     for (int i = tid; i < k; i += kThreads) {
       orow[i] = (i < n) ? i : -1;
-      if (osc) osc[i] = (i < n) ? srow[i] : 0.0f;
+      if (osc) osc[i] = (i < n) ? key_score(score_key(srow[i])) : 0.0f;
     }
     return;
   }
   const bool vec = ((reinterpret_cast<uintptr_t>(srow) & 15u) == 0);
-  const int64_t chunk = (int64_t)kThreads * 4;
+  const int64_t chunk = (int64_t)kThreads * kPer;
 
-  // ---- digit 1: keys [31:21] over the whole row
-  clear_hist(sh);
-  if (tid == 0) sh.n_cand = 0;
-  // every loop below runs the same trip count in all threads (block-uniform
-  // chunk loop) so that the warp-collective intrinsics see full warps
-  for (int64_t c0 = 0; c0 < n; c0 += chunk) {
-    const int64_t e = c0 + (int64_t)tid * 4;
-    float v[4];
-    load4(srow, e, n, vec, v);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) hist_add(sh.hist, e + i < n, score_key(v[i]) >> 21);
-  }
-  __syncthreads();
-  select_bin(sh, kBins, (uint32_t)k);
-  uint32_t prefix = sh.sel_bin;  // high bits of T found so far
-  uint32_t above = sh.sel_above;
-  const uint32_t in_bin = sh.hist[prefix];
-  __syncthreads();
-
-  if (in_bin <= (uint32_t)kCandCap) {
-    // ---- gather the keys of the selected bin, then digits 2 and 3 in smem
-    for (int64_t c0 = 0; c0 < n; c0 += chunk) {
-      const int64_t e = c0 + (int64_t)tid * 4;
-      float v[4];
-      load4(srow, e, n, vec, v);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t key = score_key(v[i]);
-        const bool hit = (e + i < n) && (key >> 21) == prefix;
-        const uint32_t b = __ballot_sync(0xffffffffu, hit);
-        uint32_t base = 0;
-        if ((tid & 31) == 0 && b) base = atomicAdd(&sh.n_cand, (uint32_t)__popc(b));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        if (hit) sh.cand[base + __popc(b & ((1u << (tid & 31)) - 1u))] = key;
-      }
-    }
-    __syncthreads();
-    const uint32_t nc = sh.n_cand;
-    // digit 2: bits [20:10]
-    clear_hist(sh);
-    for (uint32_t i = tid; i < ((nc + 31u) & ~31u); i += kThreads) {
-      const bool ok = i < nc;
-      const uint32_t key = ok ? sh.cand[i] : 0u;
-      hist_add(sh.hist, ok, (key >> 10) & 0x7FFu);
-    }
-    __syncthreads();
-    select_bin(sh, kBins, (uint32_t)k - above);
-    prefix = (prefix << 11) | sh.sel_bin;
-    above += sh.sel_above;
-    __syncthreads();
-    // digit 3: bits [9:0]
-    clear_hist(sh);
-    for (uint32_t i = tid; i < ((nc + 31u) & ~31u); i += kThreads) {
-      const bool ok = i < nc && (sh.cand[i] >> 10) == prefix;
-      const uint32_t key = (i < nc) ? sh.cand[i] : 0u;
-      hist_add(sh.hist, ok, key & 0x3FFu);
-    }
-    __syncthreads();
-    select_bin(sh, 1024, (uint32_t)k - above);
-    prefix = (prefix << 10) | sh.sel_bin;
-    above += sh.sel_above;
+  // ---- digit 1: keys [31:21]
+  if (p.key_hist) {
+    const uint32_t* hrow = p.key_hist + (int64_t)row * kBins;
+    for (int i = tid; i < kBins; i += kThreads) sh.hist[i] = hrow[i];
     __syncthreads();
   } else {
-    // ---- a crowded bin (many equal or near-equal scores): digits 2 and 3
-    //      re-read the row with the prefix as a filter
-    clear_hist(sh);
+    clear(&sh.u.sub[0][0], kSubHists * kBins);
+    uint32_t* mine = sh.u.sub[warp & (kSubHists - 1)];
     for (int64_t c0 = 0; c0 < n; c0 += chunk) {
-      const int64_t e = c0 + (int64_t)tid * 4;
-      float v[4];
-      load4(srow, e, n, vec, v);
+      const int64_t e = c0 + (int64_t)tid * kPer;
+      float v[kPer];
+      load_run(srow, e, n, vec, v);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t key = score_key(v[i]);
-        hist_add(sh.hist, (e + i < n) && (key >> 21) == prefix, (key >> 10) & 0x7FFu);
+      for (int i = 0; i < kPer; ++i)
+        if (e + i < n) atomicAdd(mine + (score_key(v[i]) >> 21), 1u);
+    }
+    __syncthreads();
+    for (int i = tid; i < kBins; i += kThreads) {
+      uint32_t s = 0;
+#pragma unroll
+      for (int j = 0; j < kSubHists; ++j) s += sh.u.sub[j][i];
+      sh.hist[i] = s;
+    }
+    __syncthreads();
+  }
+  select_bin(sh, kBins, (uint32_t)k);
+  const uint32_t b1 = sh.sel_bin;
+  uint32_t above = sh.sel_above;
+  const uint32_t n_cand = above + sh.hist[b1];
+  __syncthreads();
+
+  uint32_t T;
+  if (n_cand <= (uint32_t)kCandCap && p.seg_ws && p.key_hist) {
+    // ---- candidates from the segments, concatenated in segment order: all
+    //      counts are read at once (one segment per thread), their exclusive
+    //      prefix goes to sh.hist (free until digit 2), and each candidate
+    //      position finds its segment by binary search
+    const int nseg = (int)((n + kTopkSegLen - 1) / kTopkSegLen);   // <= kThreads
+    const uint32_t cnt = (tid < nseg) ? p.seg_ws[((int64_t)row * p.n_seg + tid) * kSegWords] : 0u;
+    uint32_t tot;
+    const uint32_t incl = block_prefix_sum(cnt, sh, tot);
+    if (tid < nseg) sh.hist[tid] = incl - cnt;
+    __syncthreads();
+    for (uint32_t pos = tid; pos < tot && pos < (uint32_t)kCandCap; pos += kThreads) {
+      int lo = 0, hi = nseg - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (sh.hist[mid] <= pos) lo = mid;
+        else hi = mid - 1;
       }
+      const uint32_t* src = p.seg_ws + ((int64_t)row * p.n_seg + lo) * kSegWords;
+      const uint32_t i = pos - sh.hist[lo];
+      sh.u.cand.key[pos] = src[4 + i];
+      sh.u.cand.idx[pos] = (int32_t)src[4 + kCandCap + i];
+    }
+    __syncthreads();
+  } else if (n_cand <= (uint32_t)kCandCap) {
+    // ---- ordered compaction of every key in bins >= b1
+    uint32_t base = 0;
+    for (int64_t c0 = 0; c0 < n; c0 += chunk) {
+      const int64_t e = c0 + (int64_t)tid * kPer;
+      float v[kPer];
+      load_run(srow, e, n, vec, v);
+      uint32_t key[kPer], cnt = 0;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        key[i] = score_key(v[i]);
+        cnt += (e + i < n && (key[i] >> 21) >= b1);
+      }
+      uint32_t tot;
+      uint32_t pos = base + block_prefix_sum(cnt, sh, tot) - cnt;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i)
+        if (e + i < n && (key[i] >> 21) >= b1 && pos < (uint32_t)kCandCap) {
+          sh.u.cand.key[pos] = key[i];
+          sh.u.cand.idx[pos] = (int32_t)(e + i);
+          ++pos;
+        }
+      base += tot;
+    }
+  }
+  if (n_cand <= (uint32_t)kCandCap) {
+    // ---- digit 2 (bits [20:10]) and digit 3 (bits [9:0]) on the candidates
+    clear(sh.hist, kBins);
+    for (uint32_t i = tid; i < n_cand; i += kThreads) {
+      const uint32_t key = sh.u.cand.key[i];
+      if ((key >> 21) == b1) atomicAdd(sh.hist + ((key >> 10) & 0x7FFu), 1u);
     }
     __syncthreads();
     select_bin(sh, kBins, (uint32_t)k - above);
-    prefix = (prefix << 11) | sh.sel_bin;
+    const uint32_t p2 = (b1 << 11) | sh.sel_bin;
     above += sh.sel_above;
     __syncthreads();
-    clear_hist(sh);
-    for (int64_t c0 = 0; c0 < n; c0 += chunk) {
-      const int64_t e = c0 + (int64_t)tid * 4;
-      float v[4];
-      load4(srow, e, n, vec, v);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t key = score_key(v[i]);
-        hist_add(sh.hist, (e + i < n) && (key >> 10) == prefix, key & 0x3FFu);
-      }
+    clear(sh.hist, 1024);
+    for (uint32_t i = tid; i < n_cand; i += kThreads) {
+      const uint32_t key = sh.u.cand.key[i];
+      if ((key >> 10) == p2) atomicAdd(sh.hist + (key & 0x3FFu), 1u);
     }
     __syncthreads();
     select_bin(sh, 1024, (uint32_t)k - above);
-    prefix = (prefix << 10) | sh.sel_bin;
+    T = (p2 << 10) | sh.sel_bin;
     above += sh.sel_above;
     __syncthreads();
+    // ---- emission from the candidates (already in index order)
+    const uint32_t need_eq = (uint32_t)k - above;
+    const uint32_t per = (n_cand + kThreads - 1) / kThreads;  // <= 8
+    const uint32_t i0 = tid * per;
+    uint32_t gt = 0, eq = 0;
+    for (uint32_t i = i0; i < i0 + per && i < n_cand; ++i) {
+      gt += sh.u.cand.key[i] > T;
+      eq += sh.u.cand.key[i] == T;
+    }
+    uint32_t tot;
+    const uint32_t packed = gt | (eq << 16);
+    const uint32_t before = block_prefix_sum(packed, sh, tot) - packed;
+    uint32_t g_before = before & 0xFFFFu, q_before = before >> 16;
+    for (uint32_t i = i0; i < i0 + per && i < n_cand; ++i) {
+      const uint32_t key = sh.u.cand.key[i];
+      const bool is_gt = key > T, is_eq = key == T;
+      if (is_gt || (is_eq && q_before < need_eq)) {
+        const uint32_t pos = g_before + (q_before < need_eq ? q_before : need_eq);
+        orow[pos] = sh.u.cand.idx[i];
+        if (osc) osc[pos] = key_score(key);
+      }
+      g_before += is_gt;
+      q_before += is_eq;
+    }
+    return;
   }
 
-  // ---- ordered emission: keys > T, then the first (k - above) keys == T
-  const uint32_t T = prefix;
+  // ---- crowded bin: digits 2 and 3 re-read the row
+  uint32_t prefix = b1;
+  clear(sh.hist, kBins);
+  for (int64_t c0 = 0; c0 < n; c0 += chunk) {
+    const int64_t e = c0 + (int64_t)tid * kPer;
+    float v[kPer];
+    load_run(srow, e, n, vec, v);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const uint32_t key = score_key(v[i]);
+      hist_add_aggregated(sh.hist, (e + i < n) && (key >> 21) == prefix, (key >> 10) & 0x7FFu);
+    }
+  }
+  __syncthreads();
+  select_bin(sh, kBins, (uint32_t)k - above);
+  prefix = (prefix << 11) | sh.sel_bin;
+  above += sh.sel_above;
+  __syncthreads();
+  clear(sh.hist, kBins);
+  for (int64_t c0 = 0; c0 < n; c0 += chunk) {
+    const int64_t e = c0 + (int64_t)tid * kPer;
+    float v[kPer];
+    load_run(srow, e, n, vec, v);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const uint32_t key = score_key(v[i]);
+      hist_add_aggregated(sh.hist, (e + i < n) && (key >> 10) == prefix, key & 0x3FFu);
+    }
+  }
+  __syncthreads();
+  select_bin(sh, 1024, (uint32_t)k - above);
+  T = (prefix << 10) | sh.sel_bin;
+  above += sh.sel_above;
+  __syncthreads();
+
+  // ---- ordered emission over the row: keys > T, then the first keys == T
   const uint32_t need_eq = (uint32_t)k - above;
   uint32_t base_gt = 0, base_eq = 0;
   for (int64_t c0 = 0; c0 < n; c0 += chunk) {
-    const int64_t e = c0 + (int64_t)tid * 4;
-    float v[4];
-    load4(srow, e, n, vec, v);
+    const int64_t e = c0 + (int64_t)tid * kPer;
+    float v[kPer];
+    load_run(srow, e, n, vec, v);
     uint32_t gt = 0, eq = 0;
-    uint32_t key[4];
+    uint32_t key[kPer];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kPer; ++i) {
       key[i] = score_key(v[i]);
       const bool ok = e + i < n;
       gt += (ok && key[i] > T);
       eq += (ok && key[i] == T);
     }
     uint32_t tot;
-    const uint32_t incl = block_prefix_sum(gt | (eq << 16), sh, tot);
-    uint32_t g_before = base_gt + ((incl - (gt | (eq << 16))) & 0xFFFFu);
-    uint32_t q_before = base_eq + ((incl - (gt | (eq << 16))) >> 16);
+    const uint32_t packed = gt | (eq << 16);
+    const uint32_t before = block_prefix_sum(packed, sh, tot) - packed;
+    uint32_t g_before = base_gt + (before & 0xFFFFu);
+    uint32_t q_before = base_eq + (before >> 16);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kPer; ++i) {
       if (e + i >= n) break;
       const bool is_gt = key[i] > T, is_eq = key[i] == T;
       if (is_gt || (is_eq && q_before < need_eq)) {
         const uint32_t pos = g_before + (q_before < need_eq ? q_before : need_eq);
         orow[pos] = (int32_t)(e + i);
-        if (osc) osc[pos] = v[i];
+        if (osc) osc[pos] = key_score(key[i]);
       }
       g_before += is_gt;
       q_before += is_eq;
@@ -296,12 +478,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
 
 }  // namespace
 
+int topk_segments(int64_t max_valid) {
+  return (int)((max_valid + kTopkSegLen - 1) / kTopkSegLen);
+}
+
+size_t topk_seg_bytes(int32_t rows, int64_t max_valid) {
+  return (size_t)rows * (size_t)topk_segments(max_valid) * kSegWords * sizeof(uint32_t);
+}
+
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
   const int smem = (int)sizeof(Shared);
   cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   for (int r0 = 0; r0 < p.rows; r0 += kTopkMaxRowsPerLaunch) {
     const int nr = (p.rows - r0 < kTopkMaxRowsPerLaunch) ? p.rows - r0 : kTopkMaxRowsPerLaunch;
+    if (p.seg_ws && p.key_hist && p.n_seg > 0) {
+      k_topk_seg<<<dim3(p.n_seg, nr), kSegThreads, 0, s>>>(p, r0);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
     k_topk<<<nr, kThreads, smem, s>>>(p, r0);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

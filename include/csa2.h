@@ -177,18 +177,27 @@ csa2_status_t csa2_append_tokens(csa2_cache_t* cache, int32_t n_seqs,
  * query plus selection state).                                            */
 size_t csa2_index_workspace_bytes(const csa2_cache_t* cache, int32_t n_queries);
 
+/* Score-key histogram.  Scores are ordered through a 32-bit key: the fp32
+ * bit pattern with the sign bit set for non-negative values and all bits
+ * inverted for negative ones (-0 counts as +0), so that keys compare like
+ * the scores.  key_hist[r, b] (uint32, 2048 bins per row) counts the valid
+ * scores of row r whose key has b in its top 11 bits.  csa2_index_scores_*
+ * can produce it while scoring; csa2_topk then skips its own first pass.    */
+
 /* Index scores only (the scoring step of csa2_index_topk_decode, for callers
  * that select on their own or time the steps apart): for decode query q,
  * scores[q * ld + s] = sum_h w[q, h] * ReLU(q_idx[q, h] . K_I[s]) for every
  * entry s of its sequence ([V4B sec 4.1]); entries past a sequence's length
  * are left untouched.
  *   scores: dev fp32 [n_queries, ld], ld >= the longest sequence's length
- *   and a multiple of 4;  other arguments as for csa2_index_topk_decode.    */
+ *   and a multiple of 4;  key_hist: nullable dev uint32 [n_queries, 2048],
+ *   overwritten with the score-key histogram of each row;  other arguments
+ *   as for csa2_index_topk_decode.                                         */
 csa2_status_t csa2_index_scores_decode(const csa2_cache_t* cache,
                                        int32_t n_queries, const void* q_idx,
                                        const float* w, const int32_t* seq_ids,
                                        float* scores, int64_t ld,
-                                       csa2_stream_t stream);
+                                       uint32_t* key_hist, csa2_stream_t stream);
 
 /* Full-mode selection for decode queries, one query per sequence, each the
  * newest token of its sequence so every appended entry is visible.
@@ -222,17 +231,25 @@ csa2_status_t csa2_index_topk_prefill(const csa2_cache_t* cache, int32_t seq,
                                       void* workspace, size_t workspace_bytes,
                                       csa2_stream_t stream);
 
-/* Workspace bytes of csa2_topk for n_rows rows. */
-size_t csa2_topk_workspace_bytes(int32_t n_rows);
+/* Workspace bytes with which csa2_topk splits each row's candidate search
+ * over several CTAs (used when key_hist is given), for n_rows rows of at
+ * most max_valid scores.  A smaller workspace (or none) is allowed: the
+ * selection is the same, one CTA per row.                                   */
+size_t csa2_topk_workspace_bytes(int32_t n_rows, int64_t max_valid);
 
 /* Stand-alone top-k over caller scores (the selection step of the indexer):
  * row r has n_valid[r] fp32 scores at scores + r * ld; the k largest are
  * returned, ties to the lower index, ascending index order, -1 padded.  -0
- * and +0 compare equal; NaN is not allowed.
- *   scores: dev fp32;  n_valid: host int64 [n_rows];  idx_out: dev int32
- *   [n_rows, k];  score_out: nullable dev fp32 [n_rows, k].                 */
+ * and +0 compare equal (a selected -0 is reported as +0); NaN is not
+ * allowed.
+ *   scores: dev fp32;  n_valid: host int64 [n_rows];  key_hist: nullable
+ *   dev uint32 [n_rows, 2048], the score-key histogram of each row if the
+ *   caller has it (see above), which saves one pass over the scores;
+ *   idx_out: dev int32 [n_rows, k];  score_out: nullable dev fp32
+ *   [n_rows, k].  k <= 4096.                                                */
 csa2_status_t csa2_topk(int32_t n_rows, const float* scores, int64_t ld,
-                        const int64_t* n_valid, int32_t k, int32_t* idx_out,
+                        const int64_t* n_valid, int32_t k,
+                        const uint32_t* key_hist, int32_t* idx_out,
                         float* score_out, void* workspace,
                         size_t workspace_bytes, csa2_stream_t stream);
 

@@ -79,11 +79,11 @@ def test_host_argument_errors(lib):
     assert L.csa2_compress(0, 4, 512, None, None, None, None) == 1
     assert L.csa2_compress(2, 0, 512, None, None, None, None) == 0
     assert L.csa2_compress(32, 4, 512, None, None, None, None) == 2
-    assert L.csa2_topk(0, None, 0, None, 512, None, None, None, 0, None) == 0
-    assert L.csa2_topk(1, None, 0, None, 512, None, None, None, 0, None) == 1
+    assert L.csa2_topk(0, None, 0, None, 512, None, None, None, None, 0, None) == 0
+    assert L.csa2_topk(1, None, 0, None, 512, None, None, None, None, 0, None) == 1
     nv = (ctypes.c_int64 * 1)(10)
-    assert L.csa2_topk(1, ctypes.c_void_p(0x1000), 4, nv, 512, ctypes.c_void_p(0x2000), None,
-                       None, 0, None) == 1          # n_valid > ld
+    assert L.csa2_topk(1, ctypes.c_void_p(0x1000), 4, nv, 512, None, ctypes.c_void_p(0x2000),
+                       None, None, 0, None) == 1    # n_valid > ld
     assert L.csa2_index_topk_decode(None, 1, None, None, None, None, None, None, 0, None) == 1
     assert L.csa2_sparse_attn_decode(None, 1, None, None, None, None, None, 1.0, None, None,
                                      None) == 1

@@ -88,3 +88,36 @@ def test_prefill_causal(C, pos0, ratio):
         nv = O.visible_entries(n_ent, ratio, pos0 + i)
         o_idx, o_sc = O.index_topk(ks[0], qi[i], w[i], 512, nv)
         check_topk(idx[i], o_idx, o_sc, 512)
+
+
+def _key_hist(scores):
+    u = np.ascontiguousarray(scores, np.float32).view(np.uint32).copy()
+    u[(u << np.uint32(1)) == 0] = 0
+    key = np.where(u & np.uint32(0x80000000), ~u, u | np.uint32(0x80000000))
+    return np.bincount((key >> np.uint32(21)).astype(np.int64), minlength=2048)
+
+
+def test_scores_and_key_histogram(C):
+    """csa2_index_scores_decode: every score close to the fp64 oracle, the
+    score-key histogram exactly that of the returned scores, and top-k from
+    the histogram identical to top-k without it."""
+    import torch
+    lens = [5000, 0, 700, 3001]
+    cache, ks = _fill(C, lens, 5120, 41)
+    qi, w = _queries(42, len(lens))
+    ld = 5120
+    sc = torch.full((len(lens), ld), float("nan"), device="cuda")
+    kh = torch.zeros(len(lens), 2048, dtype=torch.int32, device="cuda")
+    C.csa2_index_scores_decode(cache, bf16_dev(qi), f32_dev(w), sc, key_hist=kh)
+    sc_h, kh_h = sc.cpu().numpy(), kh.cpu().numpy()
+    for i, n in enumerate(lens):
+        assert np.all(np.isnan(sc_h[i, n:]))          # past the length: untouched
+        if n:
+            o = O.index_scores(ks[i], qi[i], w[i])
+            assert np.allclose(sc_h[i, :n], o, rtol=2e-5, atol=2e-5 * np.abs(o).max())
+        assert np.array_equal(kh_h[i], _key_hist(sc_h[i, :n]))
+    a = C.csa2_topk(sc, lens, 512, key_hist=kh).cpu().numpy()
+    b = C.csa2_topk(sc, lens, 512).cpu().numpy()
+    assert np.array_equal(a, b)
+    for i, n in enumerate(lens):
+        assert np.array_equal(a[i], O.topk(sc_h[i, :n], 512))

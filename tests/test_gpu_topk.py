@@ -71,3 +71,38 @@ def test_long_row(C):
     s = (rng.standard_normal(n) * 50).astype(np.float32)
     got = C.csa2_topk(f32_dev(s[None]), [n], 512).cpu().numpy()[0]
     assert np.array_equal(got, O.topk(s, 512))
+
+
+@pytest.mark.parametrize("kind", ["normal", "ints", "equal", "crowded", "relu_like"])
+def test_topk_with_key_histogram(C, kind):
+    """Given the score-key histogram, the selection is the same."""
+    import torch
+    from tests.test_gpu_index import _key_hist
+    rng = np.random.default_rng(7)
+    n = 131072
+    s = _rows(kind, n, rng)
+    kh = torch.from_numpy(_key_hist(s).astype(np.int32)[None]).cuda()
+    got = C.csa2_topk(f32_dev(s[None]), [n], 512, key_hist=kh).cpu().numpy()[0]
+    assert np.array_equal(got, O.topk(s, 512))
+    ws = torch.empty(C.csa2_topk_workspace_bytes(1, n), dtype=torch.uint8, device="cuda")
+    got = C.csa2_topk(f32_dev(s[None]), [n], 512, key_hist=kh, workspace=ws).cpu().numpy()[0]
+    assert np.array_equal(got, O.topk(s, 512))
+
+
+def test_segmented_ragged_rows(C):
+    """Segmented candidate search over rows of different lengths (some shorter
+    than one segment, some not a multiple of it) and a crowded row."""
+    import torch
+    from tests.test_gpu_index import _key_hist
+    rng = np.random.default_rng(11)
+    ns = [100, 512, 513, 16383, 16385, 70001, 140000, 140000]
+    ld = 140000
+    buf = rng.standard_normal((len(ns), ld)).astype(np.float32)
+    buf[7] = np.round(buf[7])               # crowded: falls back to the row scan
+    kh = np.stack([_key_hist(buf[r, :n]) for r, n in enumerate(ns)]).astype(np.int32)
+    ws = torch.empty(C.csa2_topk_workspace_bytes(len(ns), max(ns)), dtype=torch.uint8,
+                     device="cuda")
+    got = C.csa2_topk(f32_dev(buf), ns, 512, key_hist=torch.from_numpy(kh).cuda(),
+                      workspace=ws).cpu().numpy()
+    for r, n in enumerate(ns):
+        assert np.array_equal(got[r], O.topk(buf[r, :n], 512)), r
