@@ -80,7 +80,8 @@ def _load():
         "csa2_index_topk_prefill": ([P, i32, i32, i64, P, P, P, P, P, sz, P], i32),
         "csa2_topk_workspace_bytes": ([i32, i64], sz),
         "csa2_topk": ([i32, P, i64, P, i32, P, P, P, P, sz, P], i32),
-        "csa2_sparse_attn_decode": ([P, i32, P, P, P, P, P, ctypes.c_float, P, P, P], i32),
+        "csa2_sparse_attn_workspace_bytes": ([P, i32], sz),
+        "csa2_sparse_attn_decode": ([P, i32, P, P, P, P, P, ctypes.c_float, P, P, P, sz, P], i32),
         "csa2_sparse_attn_prefill": ([P, i32, i32, i64, P, P, i64, i64, P, ctypes.c_float, P, P,
                                       P], i32),
         "csa2_get_device_error": ([P, P, ctypes.POINTER(i32)], i32),
@@ -291,18 +292,32 @@ def csa2_topk(scores: torch.Tensor, n_valid: Sequence[int], k: int,
 
 
 # ------------------------------------------------------------------ attention
+def csa2_sparse_attn_workspace_bytes(cache: Cache, n_queries: int) -> int:
+    return int(lib.csa2_sparse_attn_workspace_bytes(cache.handle, n_queries))
+
+
 def csa2_sparse_attn_decode(cache: Cache, q: torch.Tensor, swa_kv: Optional[torch.Tensor],
                             topk_idx: torch.Tensor, scale: float,
                             swa_len: Optional[torch.Tensor] = None,
                             seq_ids: Optional[Sequence[int]] = None,
                             out: Optional[torch.Tensor] = None,
-                            lse: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                            lse: Optional[torch.Tensor] = None,
+                            workspace: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
+    """workspace=None allocates one of csa2_sparse_attn_workspace_bytes; pass
+    an empty tensor to run without (one CTA per query)."""
     nq = q.shape[0]
     if out is None:
         out = torch.empty_like(q)
+    if workspace is None:
+        workspace = torch.empty(max(16, csa2_sparse_attn_workspace_bytes(cache, nq)),
+                                dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
     _check(lib.csa2_sparse_attn_decode(cache.handle, nq, _i32_array(seq_ids), _ptr(q),
                                        _ptr(swa_kv), _ptr(swa_len), _ptr(topk_idx),
-                                       float(scale), _ptr(out), _ptr(lse), _stream(stream)),
+                                       float(scale), _ptr(out), _ptr(lse),
+                                       _ptr(workspace) if ws_bytes else None, ws_bytes,
+                                       _stream(stream)),
            "csa2_sparse_attn_decode")
     return out
 

@@ -42,7 +42,8 @@ csa2_status_t check_cfg(const csa2_config_t* c) {
   if (!c) return CSA2_ERR_INVALID_ARG;
   if (c->head_dim != kHeadDim || c->idx_dim != kIdxDim || c->idx_heads != kIdxHeads)
     return CSA2_ERR_UNSUPPORTED;
-  if (c->n_heads <= 0 || c->n_heads % 32 != 0 || c->n_heads > 128) return CSA2_ERR_UNSUPPORTED;
+  if (c->n_heads <= 0 || c->n_heads % kAttnHeadGroup != 0 || c->n_heads > 128)
+    return CSA2_ERR_UNSUPPORTED;
   if (c->topk <= 0 || c->topk % 128 != 0 || c->topk > 2048) return CSA2_ERR_UNSUPPORTED;
   if (c->swa < 0 || c->swa > 128) return CSA2_ERR_UNSUPPORTED;
   if (c->ratio < 1 || c->ratio > 16) return CSA2_ERR_UNSUPPORTED;
@@ -588,10 +589,15 @@ csa2_status_t csa2_index_topk_prefill(const csa2_cache_t* c, int32_t seq, int32_
   return st;
 }
 
+size_t csa2_sparse_attn_workspace_bytes(const csa2_cache_t* c, int32_t n_queries) {
+  if (!c || n_queries < 0) return 0;
+  return attn_part_bytes(n_queries, c->cfg.n_heads / kAttnHeadGroup);
+}
+
 csa2_status_t csa2_sparse_attn_decode(const csa2_cache_t* c, int32_t nq, const int32_t* seq_ids,
                                       const void* q, const void* swa_kv, const int32_t* swa_len,
                                       const int32_t* topk_idx, float scale, void* out, float* lse,
-                                      csa2_stream_t stream) {
+                                      void* workspace, size_t ws_bytes, csa2_stream_t stream) {
   if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
   if (nq == 0) return CSA2_OK;
   const int W = c->cfg.swa;
@@ -599,16 +605,20 @@ csa2_status_t csa2_sparse_attn_decode(const csa2_cache_t* c, int32_t nq, const i
     return CSA2_ERR_INVALID_ARG;
   if (W > 0 && (!swa_kv || !aligned16(swa_kv))) return CSA2_ERR_INVALID_ARG;
   if (lse && !aligned16(lse)) return CSA2_ERR_INVALID_ARG;
+  if (workspace && !aligned16(workspace)) return CSA2_ERR_INVALID_ARG;
   if (seq_ids)
     for (int i = 0; i < nq; ++i)
       if (seq_ids[i] < 0 || seq_ids[i] >= c->batch) return CSA2_ERR_INVALID_ARG;
   if (!seq_ids && nq > c->batch) return CSA2_ERR_INVALID_ARG;
-  const int H = c->cfg.n_heads, k = c->cfg.topk;
+  const int H = c->cfg.n_heads, k = c->cfg.topk, G = H / kAttnHeadGroup;
   AttnParams* p = new (std::nothrow) AttnParams();
   if (!p) return CSA2_ERR_OOM;
   csa2_status_t st = CSA2_OK;
   for (int q0 = 0; q0 < nq; q0 += kAttnTab) {
     const int n = std::min(kAttnTab, nq - q0);
+    // two CTAs per (query, head group) when one each would leave SMs idle
+    const bool split = workspace && ws_bytes >= attn_part_bytes(n, G) &&
+                       (int64_t)n * G < c->num_sms;
     std::memset(p, 0, sizeof(AttnParams));
     p->topk_idx = topk_idx + (int64_t)q0 * k;
     p->swa_len = swa_len ? swa_len + q0 : nullptr;
@@ -625,6 +635,16 @@ csa2_status_t csa2_sparse_attn_decode(const csa2_cache_t* c, int32_t nq, const i
     p->scale = scale;
     p->scale_log2 = scale * 1.4426950408889634f;
     p->prefill = 0;
+    p->splits = split ? 2 : 1;
+    if (split) {
+      p->part = static_cast<float*>(workspace);
+      p->counter = reinterpret_cast<uint32_t*>(
+          static_cast<uint8_t*>(workspace) + attn_part_bytes(n, G) - (size_t)n * G * 4);
+      if (cudaMemsetAsync(p->counter, 0, (size_t)n * G * 4, S(stream)) != cudaSuccess) {
+        st = CSA2_ERR_CUDA;
+        break;
+      }
+    }
     for (int i = 0; i < n; ++i) {
       const int s = seq_ids ? seq_ids[q0 + i] : q0 + i;
       p->q_base[i] = c->off[s];
@@ -632,7 +652,7 @@ csa2_status_t csa2_sparse_attn_decode(const csa2_cache_t* c, int32_t nq, const i
     }
     CUtensorMap tm_q, tm_swa;
     const uint16_t* qb = static_cast<const uint16_t*>(q) + (int64_t)q0 * H * kHeadDim;
-    if (!make_map(&tm_q, qb, (uint64_t)n * H, kHeadDim, 64, 32)) { st = CSA2_ERR_CUDA; break; }
+    if (!make_map(&tm_q, qb, (uint64_t)n * H, kHeadDim, 64, kAttnHeadGroup)) { st = CSA2_ERR_CUDA; break; }
     if (W > 0) {
       const uint16_t* sb = static_cast<const uint16_t*>(swa_kv) + (int64_t)q0 * W * kHeadDim;
       if (!make_map(&tm_swa, sb, (uint64_t)n * W, kHeadDim, 64, 128)) { st = CSA2_ERR_CUDA; break; }
@@ -683,9 +703,10 @@ csa2_status_t csa2_sparse_attn_prefill(const csa2_cache_t* c, int32_t seq, int32
   p->pre_len = (int32_t)c->len[seq];
   p->pos0 = pos0;
   p->swa_pos0 = swa_pos0;
+  p->splits = 1;
   csa2_status_t st = CSA2_OK;
   CUtensorMap tm_q, tm_swa;
-  if (!make_map(&tm_q, q, (uint64_t)nq * H, kHeadDim, 64, 32)) st = CSA2_ERR_CUDA;
+  if (!make_map(&tm_q, q, (uint64_t)nq * H, kHeadDim, 64, kAttnHeadGroup)) st = CSA2_ERR_CUDA;
   if (st == CSA2_OK) {
     if (W > 0) {
       if (!make_map(&tm_swa, swa_kv, (uint64_t)n_swa_rows, kHeadDim, 64, 128)) st = CSA2_ERR_CUDA;

@@ -8,14 +8,19 @@
 // KV into a single joint sparse attention"); entries are dequantised from
 // FP4 before attention (V4.1 report, section 2.4.4).
 //
-// One CTA = one query x 32 heads.  Candidates come in tiles of 128 rows: the
+// One CTA = one query x 64 heads x one share of the candidate tiles.  With
+// `splits` = 2 (decode with a workspace) the tiles of a query alternate
+// between two CTAs, each writes its unnormalised fp32 partial (running max,
+// sum, O) to the workspace, and the second to finish merges both in a fixed
+// operand order (threadfence + atomic counter, no waiting); with splits = 1 a
+// CTA takes every tile.  Candidates come in tiles of 128 rows: the
 // window tile (TMA straight into swizzled shared memory) and the top-k tiles
 // (each thread loads a quarter of an entry's 256 B of codes plus its scale
 // bytes into registers, one tile ahead; then E2M1 -> bf16 via byte permutes
 // and a bf16 scale multiply, written to shared memory in the MMA layout).  With the
 // candidate rows as the MMA M dimension:
-//     S^T[128 x 32]  = KV[128 x 512] * Q[32 x 512]^T        (K-major A and B)
-//     O^T[512 x 32] += KV^T[512 x 128] * P^T[128 x 32]^T     (MN-major A)
+//     S^T[128 x 64]  = KV[128 x 512] * Q[64 x 512]^T        (K-major A and B)
+//     O^T[512 x 64] += KV^T[512 x 128] * P^T[128 x 64]^T     (MN-major A)
 // both on tcgen05 with fp32 accumulators in TMEM; the same swizzled KV tile
 // serves as the K-major A of the first product and the MN-major A of the
 // second.  Online softmax (base 2) runs across TMEM lanes: each thread holds
@@ -28,28 +33,32 @@
 namespace csa2 {
 namespace {
 
-constexpr int kThreads = 512;     // 16 warps: all gather/dequantise, warps 0-7 run the softmax
-constexpr int kHG = 32;               // heads per CTA
+constexpr int kThreads = 512;     // 16 warps
+constexpr int kHG = 64;               // heads per CTA
 constexpr int kRows = 128;            // candidates per tile
 constexpr int kMaxTiles = 2048 / kRows + 1;
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kKvOff = 0;                              // 8 x [128 x 128 B]
-constexpr int kQOff = kKvOff + kRows * kHeadDim * 2;   // 8 x [32 x 128 B]
-constexpr int kPOff = kQOff + kHG * kHeadDim * 2;      // 2 x [32 x 128 B]
+constexpr int kQOff = kKvOff + kRows * kHeadDim * 2;   // 8 x [64 x 128 B]
+constexpr int kPOff = kQOff + kHG * kHeadDim * 2;      // 2 x [64 x 128 B]
 constexpr int kIdxOff = kPOff + kHG * kRows * 2;        // the query's top-k row
 constexpr int kSmallOff = kIdxOff + 2048 * 4;
+constexpr int kPartFloats = 2 * kHG + kHG * kHeadDim;   // m, l, O of one split
 struct Small {
   float red_max[4][kHG];
   float red_sum[4][kHG];
   float m[kHG];
   float l[kHG];
   float alpha[kHG];
-  int32_t tile_list[kMaxTiles];
+  int32_t tile_list[kMaxTiles];  // every tile of the query, window first
+  int32_t my_list[kMaxTiles];    // this CTA's share
   int32_t tile_any[kMaxTiles];   // top-k tile holds a usable index
   uint8_t row_valid[kRows];
   int32_t n_tiles;
+  int32_t n_all;
   int32_t need_rescale;
+  int32_t merge;
   uint32_t tmem;
   uint64_t bar_q, bar_kv, bar_mma;
 };
@@ -108,7 +117,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hgs = p.n_heads / kHG;
-  const int q = blockIdx.x / hgs, hg = blockIdx.x % hgs;
+  const int split = blockIdx.x % p.splits;
+  const int qh = blockIdx.x / p.splits;            // (query, head group)
+  const int q = qh / hgs, hg = qh % hgs;
   const int n_topk_tiles = p.topk / kRows;
   const int32_t* idx_row = p.topk_idx + (int64_t)q * p.topk;
 
@@ -141,17 +152,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid < kMaxTiles) sm.tile_any[tid] = 0;
   if (tid < kHG) { sm.m[tid] = -INFINITY; sm.l[tid] = 0.0f; }
-  if (warp == 0) { tmem_alloc(&sm.tmem, 256); tmem_relinquish(); }
+  if (warp == 0) { tmem_alloc(&sm.tmem, 512); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem;
-  const uint32_t s_col = 0, o_col = 32;
+  const uint32_t s_col = 0, o_col = 64;   // S^T: 64 columns; O^T: 4 d-tiles x 64
 
+  // the window tile is always first in the tile list: the CTA that owns it
+  // (split 0) starts its load now, before scanning the top-k row
+  const bool swa_first = swa_count > 0 && split == 0;
   if (tid == 0) {
     mbar_arrive_expect_tx(&sm.bar_q, kHG * kHeadDim * 2);
     for (int c = 0; c < 8; ++c)
       tma_load_2d(qs + c * (kHG * 128), &tm_q, 64 * c, q * p.n_heads + hg * kHG, &sm.bar_q);
+    if (swa_first) {
+      mbar_arrive_expect_tx(&sm.bar_kv, kRows * kHeadDim * 2);
+      for (int c = 0; c < 8; ++c)
+        tma_load_2d(kv + c * (kRows * 128), &tm_swa, 64 * c, swa_row0, &sm.bar_kv);
+    }
   }
   // the top-k row into shared memory (unusable slots become -1), and which
   // tiles hold at least one usable index
@@ -172,7 +191,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (swa_count > 0) sm.tile_list[n++] = -1;
     for (int j = 0; j < n_topk_tiles; ++j)
       if (sm.tile_any[j]) sm.tile_list[n++] = j;
-    sm.n_tiles = n;
+    sm.n_all = n;
+    int m = 0;
+    for (int i = split; i < n; i += p.splits) sm.my_list[m++] = sm.tile_list[i];
+    sm.n_tiles = m;
   }
   __syncthreads();
   const int n_tiles = sm.n_tiles;
@@ -203,24 +225,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   int next_topk = 0;  // position in tile_list of the next tile to gather
-  while (next_topk < n_tiles && sm.tile_list[next_topk] < 0) ++next_topk;
-  if (next_topk < n_tiles) prefetch_tile(sm.tile_list[next_topk]);
+  while (next_topk < n_tiles && sm.my_list[next_topk] < 0) ++next_topk;
+  if (next_topk < n_tiles) prefetch_tile(sm.my_list[next_topk]);
 
   uint32_t mma_phase = 0;
   bool ok = true;
-  const int quad = warp & 3, hh = (warp >> 2) & 1;
+  const int quad = warp & 3, hh = warp >> 2;   // TMEM lane quadrant, 16-head slice
   const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
 
   for (int ti = 0; ti < n_tiles && ok; ++ti) {
-    const int tile = sm.tile_list[ti];
+    const int tile = sm.my_list[ti];
     if (tid == 0) sm.need_rescale = 0;
     // ------------------------------------------------ A: candidate rows -> kv
     if (tile < 0) {
-      if (tid == 0) {
-        mbar_arrive_expect_tx(&sm.bar_kv, kRows * kHeadDim * 2);
-        for (int c = 0; c < 8; ++c)
-          tma_load_2d(kv + c * (kRows * 128), &tm_swa, 64 * c, swa_row0, &sm.bar_kv);
-      }
+      // issued at kernel entry
       if (tid < kRows) sm.row_valid[tid] = tid < swa_count;
       ok = mbar_wait(&sm.bar_kv, 0, p.err);
       ok = __syncthreads_and(ok);
@@ -262,13 +280,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_proxy_async_smem();
     __syncthreads();
-    if (tile >= 0) {
-      // the registers are free: fetch the next top-k tile behind this one
-      // (after the proxy fence, which would otherwise wait for these loads)
-      ++next_topk;
-      while (next_topk < n_tiles && sm.tile_list[next_topk] < 0) ++next_topk;
-      if (next_topk < n_tiles) prefetch_tile(sm.tile_list[next_topk]);
-    }
 
     // ------------------------------------------------ B: S^T = KV * Q^T
     if (tid == 0) {
@@ -285,18 +296,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       umma_commit(&sm.bar_mma);
     }
+    if (tile >= 0) {
+      // the registers are free: fetch the next top-k tile behind this one,
+      // while the tensor core works (after the proxy fence, which would
+      // otherwise wait for these loads)
+      ++next_topk;
+      while (next_topk < n_tiles && sm.my_list[next_topk] < 0) ++next_topk;
+      if (next_topk < n_tiles) prefetch_tile(sm.my_list[next_topk]);
+    }
     ok = mbar_wait(&sm.bar_mma, mma_phase, p.err) && ok;
     mma_phase ^= 1;
     ok = __syncthreads_and(ok);
     if (!ok) break;
     tc_fence_after();
 
-    // ------------------------------------------------ C: online softmax (warps 0-7)
-    const bool sw = warp < 8;
+    // ------------------------------------------------ C: online softmax
     const int row = quad * 32 + lane;
     const bool valid = sm.row_valid[row] != 0;
     float x[16], v[16];
-    if (sw) {
+    {
       uint32_t r[16];
       tmem_ld16(tmem + lane_addr + s_col + 16 * hh, r);
 #pragma unroll
@@ -319,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (a != 1.0f && ti > 0) sm.need_rescale = 1;
     }
     __syncthreads();
-    if (sw) {
+    {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int h = 16 * hh + i;
@@ -339,12 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid < kHG)
       sm.l[tid] = sm.alpha[tid] * sm.l[tid] + ((sm.red_sum[0][tid] + sm.red_sum[1][tid]) +
                                                (sm.red_sum[2][tid] + sm.red_sum[3][tid]));
-    if (sw && sm.need_rescale) {
+    if (sm.need_rescale) {
       // O^T lanes are head-dim rows, columns are heads: scale column h by alpha[h]
 #pragma unroll 1
       for (int i = 0; i < 4; ++i) {
         uint32_t r[16];
-        const uint32_t a = tmem + lane_addr + o_col + 32 * i + 16 * hh;
+        const uint32_t a = tmem + lane_addr + o_col + 64 * i + 16 * hh;
         tmem_ld16(a, r);
 #pragma unroll
         for (int c = 0; c < 16; ++c)
@@ -368,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ks = 0; ks < kRows / 16; ++ks) {
           const uint32_t ao = (uint32_t)((2 * i) * (kRows * 128) + ks * 2048);
           const uint32_t bo = (uint32_t)((ks >> 2) * (kHG * 128) + (ks & 3) * 32);
-          umma_bf16(tmem + o_col + 32 * i, sdesc_sw128(a0 + ao, kRows * 128, 1024),
+          umma_bf16(tmem + o_col + 64 * i, sdesc_sw128(a0 + ao, kRows * 128, 1024),
                     sdesc_sw128(b0 + bo, 16, 1024), idesc, (ti > 0 || ks > 0) ? 1u : 0u);
         }
       }
@@ -381,52 +399,126 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // ------------------------------------------------ epilogue
   __syncthreads();
-  if (ok && n_tiles > 0) {
-    const bool ew = warp < 8;
-    if (tid < kHG) {
-      const float l = sm.l[tid];
-      sm.alpha[tid] = l > 0.0f ? 1.0f / l : 0.0f;
-      if (p.lse)
-        p.lse[(int64_t)q * p.n_heads + hg * kHG + tid] =
-            l > 0.0f ? (sm.m[tid] + log2f(l)) * 0.69314718055994531f : -INFINITY;
-    }
-    __syncthreads();
+  const int64_t out_row = (int64_t)q * p.n_heads + hg * kHG;   // first head of this CTA
+  if (p.splits == 1) {
+    if (ok && n_tiles > 0) {
+      if (tid < kHG) {
+        const float l = sm.l[tid];
+        sm.alpha[tid] = l > 0.0f ? 1.0f / l : 0.0f;
+        if (p.lse)
+          p.lse[out_row + tid] =
+              l > 0.0f ? (sm.m[tid] + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      }
+      __syncthreads();
 #pragma unroll 1
-    for (int i = 0; i < 4 && ew; ++i) {
-      uint32_t r[16];
-      tmem_ld16(tmem + lane_addr + o_col + 32 * i + 16 * hh, r);
-      const int d = 128 * i + quad * 32 + lane;
+      for (int i = 0; i < 4; ++i) {
+        uint32_t r[16];
+        tmem_ld16(tmem + lane_addr + o_col + 64 * i + 16 * hh, r);
+        const int d = 128 * i + quad * 32 + lane;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int h = hg * kHG + 16 * hh + c;
-        const float o = __uint_as_float(r[c]) * sm.alpha[16 * hh + c];
-        p.out[((int64_t)q * p.n_heads + h) * kHeadDim + d] = (uint16_t)float_to_bf16_bits(o);
+        for (int c = 0; c < 16; ++c) {
+          const float o = __uint_as_float(r[c]) * sm.alpha[16 * hh + c];
+          p.out[(out_row + 16 * hh + c) * kHeadDim + d] = (uint16_t)float_to_bf16_bits(o);
+        }
+      }
+    } else if (n_tiles == 0) {
+      // no candidate at all: output 0, lse -inf
+      for (int i = tid; i < kHG * kHeadDim; i += kThreads) p.out[out_row * kHeadDim + i] = 0;
+      if (p.lse && tid < kHG) p.lse[out_row + tid] = -INFINITY;
+    }
+  } else if (ok) {
+    // ---- split-KV: the CTA that finishes second merges.  If the partner has
+    //      already published its partial, this CTA merges at once without
+    //      publishing its own; otherwise it publishes, then counts itself in.
+    float* mine = p.part + ((int64_t)qh * 2 + split) * kPartFloats;
+    float* other = p.part + ((int64_t)qh * 2 + (split ^ 1)) * kPartFloats;
+    if (tid == 0) sm.merge = atomicAdd(p.counter + qh, 0u) == 1u;
+    __syncthreads();
+    if (!sm.merge) {
+    if (tid < kHG) {
+      mine[tid] = n_tiles > 0 ? sm.m[tid] : -INFINITY;
+      mine[kHG + tid] = n_tiles > 0 ? sm.l[tid] : 0.0f;
+    }
+    if (n_tiles > 0) {
+#pragma unroll 1
+      for (int i = 0; i < 4; ++i) {
+        uint32_t r[16];
+        tmem_ld16(tmem + lane_addr + o_col + 64 * i + 16 * hh, r);
+        const int d = 128 * i + quad * 32 + lane;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) mine[2 * kHG + (16 * hh + c) * kHeadDim + d] = __uint_as_float(r[c]);
       }
     }
-  } else if (n_tiles == 0) {
-    // no candidate at all: output 0, lse -inf
-    for (int i = tid; i < kHG * kHeadDim; i += kThreads)
-      p.out[((int64_t)q * p.n_heads + hg * kHG) * kHeadDim + i] = 0;
-    if (p.lse && tid < kHG) p.lse[(int64_t)q * p.n_heads + hg * kHG + tid] = -INFINITY;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) sm.merge = atomicAdd(p.counter + qh, 1u) == 1u;
+    __syncthreads();
+    }
+    if (sm.merge) {
+      __threadfence();
+      // final = (a0 * O_0 + a1 * O_1) / (a0 * l0 + a1 * l1), operands in split
+      // order; this CTA's O comes from TMEM, the partner's from the workspace
+      if (tid < kHG) {
+        const float m_me = sm.m[tid], l_me = n_tiles > 0 ? sm.l[tid] : 0.0f;
+        const float m_me2 = n_tiles > 0 ? m_me : -INFINITY;
+        const float m_ot = __ldcg(other + tid), l_ot = __ldcg(other + kHG + tid);
+        const float m0 = split == 0 ? m_me2 : m_ot, m1 = split == 0 ? m_ot : m_me2;
+        const float l0 = split == 0 ? l_me : l_ot, l1 = split == 0 ? l_ot : l_me;
+        const float M = fmaxf(m0, m1);
+        const float a0 = (M == -INFINITY) ? 0.0f : fast_exp2(m0 - M);
+        const float a1 = (M == -INFINITY) ? 0.0f : fast_exp2(m1 - M);
+        const float L = a0 * l0 + a1 * l1;
+        const float c_me = L > 0.0f ? (split == 0 ? a0 : a1) / L : 0.0f;
+        const float c_ot = L > 0.0f ? (split == 0 ? a1 : a0) / L : 0.0f;
+        sm.alpha[tid] = (n_tiles > 0) ? c_me : 0.0f;     // weight of this CTA's O
+        sm.red_max[0][tid] = (l_ot > 0.0f) ? c_ot : 0.0f; // weight of the partner's O
+        if (p.lse) p.lse[out_row + tid] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+      }
+      __syncthreads();
+      const bool have_me = n_tiles > 0;
+#pragma unroll 1
+      for (int i = 0; i < 4; ++i) {
+        const int d = 128 * i + quad * 32 + lane;
+        float po[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) po[c] = __ldcg(other + 2 * kHG + (16 * hh + c) * kHeadDim + d);
+        uint32_t r[16];
+        if (have_me) tmem_ld16(tmem + lane_addr + o_col + 64 * i + 16 * hh, r);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int h = 16 * hh + c;
+          const float w_ot = sm.red_max[0][h];
+          const float o_me = have_me ? sm.alpha[h] * __uint_as_float(r[c]) : 0.0f;
+          const float o_ot = w_ot != 0.0f ? w_ot * po[c] : 0.0f;
+          // fixed order: split 0's term first
+          const float o = split == 0 ? o_me + o_ot : o_ot + o_me;
+          p.out[(out_row + h) * kHeadDim + d] = (uint16_t)float_to_bf16_bits(o);
+        }
+      }
+      if (tid == 0) p.counter[qh] = 0u;   // ready for the next call
+    }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
 }  // namespace
 
 int attn_smem_bytes() { return kSmemBytes; }
+size_t attn_part_bytes(int64_t nq, int head_groups) {
+  return (size_t)nq * head_groups * (2 * kPartFloats * sizeof(float) + sizeof(uint32_t));
+}
 
 cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_swa,
                         cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int64_t blocks = (int64_t)p.nq * (p.n_heads / kHG);
+  const int64_t blocks = (int64_t)p.nq * (p.n_heads / kHG) * p.splits;
   if (blocks <= 0) return cudaSuccess;
   k_attn<<<(unsigned)blocks, kThreads, kSmemBytes, s>>>(p, tm_q, tm_swa);
   return cudaGetLastError();

@@ -153,15 +153,17 @@ __device__ __forceinline__ int64_t row_valid_count(const TopkParams& p, int row)
   return p.n_valid[row];
 }
 
-// Ordered compaction of one segment's candidates (keys in bins >= b1).  256
-// threads, each owning 32 consecutive scores whose loads are issued before
-// the threshold is computed from the histogram.
-constexpr int kSegThreads = 256;
-constexpr int kSegPer = kTopkSegLen / kSegThreads;  // 32
+// Ordered compaction of one segment's candidates (keys in bins >= b1).  512
+// threads, each owning 16 consecutive scores; the score loads and the
+// histogram loads are independent and issued together, and the threshold
+// bin's count travels through shared memory, so a CTA waits on memory once.
+constexpr int kSegThreads = 512;
+constexpr int kSegWarps = kSegThreads / 32;
+constexpr int kSegPer = kTopkSegLen / kSegThreads;  // 16
+constexpr int kSegBinsPer = kBins / kSegThreads;    // 4
 struct SegShared {
-  uint32_t hist[kBins];
-  uint32_t warp_sum[kSegThreads / 32];
-  uint32_t sel_bin, sel_above;
+  uint32_t warp_sum[kSegWarps];
+  uint32_t sel_bin, sel_above, sel_count;
 };
 
 __global__ void __launch_bounds__(kSegThreads) k_topk_seg(const __grid_constant__ TopkParams p,
@@ -191,12 +193,11 @@ __global__ void __launch_bounds__(kSegThreads) k_topk_seg(const __grid_constant_
 #pragma unroll
     for (int i = 0; i < kSegPer; ++i) v[i] = (e0 + i < n) ? __ldg(srow + e0 + i) : 0.0f;
   }
-  // threshold bin from the histogram (bins >= 2t over 256 threads x 8 bins)
-  const uint32_t* hrow = p.key_hist + (int64_t)row * kBins;
-  uint32_t h[8], hs = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) { h[i] = hrow[8 * tid + i]; hs += h[i]; }
-  uint32_t suf = hs;  // inclusive suffix over threads
+  // threshold bin: thread t holds bins [4t, 4t + 4)
+  const uint4 hv = __ldg(reinterpret_cast<const uint4*>(p.key_hist + (int64_t)row * kBins) + tid);
+  const uint32_t h[kSegBinsPer] = {hv.x, hv.y, hv.z, hv.w};
+  const uint32_t hs = h[0] + h[1] + h[2] + h[3];
+  uint32_t suf = hs;  // inclusive suffix over the threads of the warp
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t t = __shfl_down_sync(0xffffffffu, suf, o);
@@ -204,19 +205,21 @@ __global__ void __launch_bounds__(kSegThreads) k_topk_seg(const __grid_constant_
   }
   if (lane == 0) sh.warp_sum[warp] = suf;
   __syncthreads();
-  uint32_t later = 0;
-  for (int w = warp + 1; w < kSegThreads / 32; ++w) later += sh.warp_sum[w];
-  suf += later;                       // keys in bins >= 8 tid
+  for (int w = warp + 1; w < kSegWarps; ++w) suf += sh.warp_sum[w];   // bins >= 4 tid
   const uint32_t k = (uint32_t)p.k;
-  uint32_t above_mine = suf - hs;     // keys in bins >= 8 tid + 8
+  uint32_t above_mine = suf - hs;                                      // bins >= 4 tid + 4
 #pragma unroll
-  for (int i = 7; i >= 0; --i) {
-    if (above_mine < k && above_mine + h[i] >= k) { sh.sel_bin = 8 * tid + i; sh.sel_above = above_mine; }
+  for (int i = kSegBinsPer - 1; i >= 0; --i) {
+    if (above_mine < k && above_mine + h[i] >= k) {
+      sh.sel_bin = kSegBinsPer * tid + i;
+      sh.sel_above = above_mine;
+      sh.sel_count = h[i];
+    }
     above_mine += h[i];
   }
   __syncthreads();
   const uint32_t b1 = sh.sel_bin;
-  if (sh.sel_above + p.key_hist[(int64_t)row * kBins + b1] > (uint32_t)kCandCap) return;
+  if (sh.sel_above + sh.sel_count > (uint32_t)kCandCap) return;  // the row falls back
   // ordered compaction
   uint32_t cnt = 0;
 #pragma unroll
@@ -227,11 +230,11 @@ __global__ void __launch_bounds__(kSegThreads) k_topk_seg(const __grid_constant_
     const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += t;
   }
-  __syncthreads();
+  __syncthreads();   // every warp has read the warp_sum values of the first scan
   if (lane == 31) sh.warp_sum[warp] = incl;
   __syncthreads();
   uint32_t before = 0, total = 0;
-  for (int w = 0; w < kSegThreads / 32; ++w) {
+  for (int w = 0; w < kSegWarps; ++w) {
     const uint32_t ws = sh.warp_sum[w];
     if (w < warp) before += ws;
     total += ws;

@@ -69,7 +69,7 @@ typedef enum { CSA2_KV_L32_UE8M0 = 0, CSA2_KV_L16_E4M3 = 1 } csa2_kv_layout_t;
 /* Shapes of one CSA2 layer.  [V41 sec 4.2.1]: 64 query heads of dim 512,
  * 32 indexer heads of dim 128, top-k 512, window 128, ratio m = 2 (encoder)
  * or 1 (decoder).  Supported: head_dim 512, idx_dim 128, idx_heads 32,
- * n_heads a multiple of 32 up to 128, topk a multiple of 128 up to 2048,
+ * n_heads 64 or 128, topk a multiple of 128 up to 2048,
  * 0 <= swa <= 128, 1 <= ratio <= 16.                                      */
 typedef struct {
   int32_t n_heads;
@@ -255,6 +255,10 @@ csa2_status_t csa2_topk(int32_t n_rows, const float* scores, int64_t ld,
 
 /* ---- sparse attention -------------------------------------------------- */
 
+/* Workspace bytes of csa2_sparse_attn_decode for n_queries queries. */
+size_t csa2_sparse_attn_workspace_bytes(const csa2_cache_t* cache,
+                                        int32_t n_queries);
+
 /* Decode readout of one layer ([V4B sec 4.1] shared-KV MQA: the selected
  * compressed entries are both key and value; [V4B sec 4.3] and [NDT sec
  * 3.3.1]: the window rows join the same softmax): for query q and head h,
@@ -268,14 +272,20 @@ csa2_status_t csa2_topk(int32_t n_rows, const float* scores, int64_t ld,
  *   topk_idx: dev int32 [n_queries, topk] (-1 = unused slot);  seq_ids: host
  *   [n_queries] or NULL (query i reads sequence i);  out: dev bf16
  *   [n_queries, n_heads, head_dim];  lse: nullable dev fp32 [n_queries,
- *   n_heads].  An index >= the sequence's length is skipped and sets
- *   CSA2_ERR_DEVICE in the device error word.                               */
+ *   n_heads];  workspace: nullable dev scratch of
+ *   csa2_sparse_attn_workspace_bytes(cache, n_queries) bytes -- with it a
+ *   small batch spreads each query's candidates over two CTAs whose partial
+ *   softmax states are merged exactly (the output is the same function;
+ *   without it one CTA per query does all the work).  An index >= the
+ *   sequence's length is skipped and sets CSA2_ERR_DEVICE in the device
+ *   error word.                                                             */
 csa2_status_t csa2_sparse_attn_decode(const csa2_cache_t* cache,
                                       int32_t n_queries, const int32_t* seq_ids,
                                       const void* q, const void* swa_kv,
                                       const int32_t* swa_len,
                                       const int32_t* topk_idx, float scale,
-                                      void* out, float* lse,
+                                      void* out, float* lse, void* workspace,
+                                      size_t workspace_bytes,
                                       csa2_stream_t stream);
 
 /* Prefill readout of one layer for a chunk of sequence `seq`: query i sits

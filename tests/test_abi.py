@@ -55,7 +55,7 @@ def test_cache_bytes_and_config_checks(lib):
     assert n32 >= 1024 * (256 + 16 + 256) and n16 - n32 >= 1024 * 16
     assert n16 < 1024 * (256 + 32 + 256) + 64 * 1024
     for bad in (dict(head_dim=256), dict(topk=500), dict(swa=200), dict(ratio=0),
-                dict(layout=5), dict(n_heads=48), dict(idx_heads=16)):
+                dict(layout=5), dict(n_heads=48), dict(n_heads=32), dict(idx_heads=16)):
         assert f(ctypes.byref(_cfg(**bad)), 2, caps) == 0
     assert f(ctypes.byref(_cfg()), 0, caps) == 0
     assert f(None, 2, caps) == 0
@@ -86,6 +86,6 @@ def test_host_argument_errors(lib):
                        None, None, 0, None) == 1    # n_valid > ld
     assert L.csa2_index_topk_decode(None, 1, None, None, None, None, None, None, 0, None) == 1
     assert L.csa2_sparse_attn_decode(None, 1, None, None, None, None, None, 1.0, None, None,
-                                     None) == 1
+                                     None, 0, None) == 1
     st = ctypes.c_int32()
     assert L.csa2_get_device_error(None, None, ctypes.byref(st)) == 1

@@ -132,3 +132,32 @@ def test_prefill_window_band(C, ratio):
         _, o, _ = O.sparse_attention(q[i], codes, scales, 0, idx[i],
                                      rows[lo - swa_pos0:hi - swa_pos0], SCALE)
         check_attn(out[i], o)
+
+
+@pytest.mark.parametrize("n_q", [3, 200])
+def test_split_and_single_cta_paths_agree_with_oracle(C, n_q):
+    """With a workspace, a small batch splits each query's candidate tiles
+    over two CTAs and merges their softmax states; without one (or for a
+    large batch) one CTA takes every tile.  Both match the oracle."""
+    import torch
+    rng = np.random.default_rng(n_q)
+    lens = [int(x) for x in rng.integers(100, 3000, n_q)]
+    cache, ents = _cache(C, lens, 3072, 51)
+    q = S.normal_bf16(S.stream_key(52, S.S_Q, 0), 0, n_q * 64 * 512).reshape(n_q, 64, 512)
+    swa = S.normal_bf16(S.stream_key(52, S.S_SWA, 0), 0, n_q * 128 * 512).reshape(n_q, 128, 512)
+    idx = np.stack([_sel(rng, n) for n in lens])
+    swa_len = torch.from_numpy(rng.integers(0, 129, n_q).astype(np.int32)).cuda()
+    outs = []
+    for ws in (None, torch.empty(0, dtype=torch.uint8, device="cuda")):
+        lse = torch.zeros(n_q, 64, device="cuda")
+        o = C.csa2_sparse_attn_decode(cache, bf16_dev(q), bf16_dev(swa), torch.from_numpy(idx).cuda(),
+                                      float(SCALE), swa_len=swa_len, lse=lse, workspace=ws)
+        outs.append((bf16_host(o), lse.cpu().numpy()))
+    sl = swa_len.cpu().numpy()
+    for i in range(0, n_q, max(1, n_q // 7)):
+        codes, scales = O.quantise(ents[i], 0)
+        _, ref, rl = O.sparse_attention(q[i], codes, scales, 0, idx[i], swa[i, :sl[i]], SCALE)
+        for o, l in outs:
+            check_attn(o[i], ref)
+            assert np.allclose(l[i], rl, atol=1e-3, rtol=0)
+    assert cache.device_error() == 0
