@@ -78,6 +78,7 @@ def _load():
         "csa2_index_scores_decode": ([P, i32, P, P, P, P, i64, P, P], i32),
         "csa2_index_topk_decode": ([P, i32, P, P, P, P, P, P, sz, P], i32),
         "csa2_index_topk_prefill": ([P, i32, i32, i64, P, P, P, P, P, sz, P], i32),
+        "csa2_index_topk_decode_static": ([P, i32, P, P, P, P, P, P], i32),
         "csa2_topk_workspace_bytes": ([i32, i64], sz),
         "csa2_topk": ([i32, P, i64, P, i32, P, P, P, P, sz, P], i32),
         "csa2_sparse_attn_workspace_bytes": ([P, i32], sz),

@@ -10,6 +10,10 @@
 #include "csa2.h"
 #include "csa2_kernels.h"
 
+// Scratch of csa2_index_topk_decode_static, for callers that cannot allocate:
+// a fixed array in the library's device image (one per GPU that loads it).
+static __device__ __align__(256) uint8_t g_static_scratch[CSA2_STATIC_SCRATCH_BYTES];
+
 using namespace csa2;
 
 struct csa2_cache {
@@ -716,6 +720,62 @@ csa2_status_t csa2_sparse_attn_prefill(const csa2_cache_t* c, int32_t seq, int32
   }
   if (st == CSA2_OK && launch_attn(*p, tm_q, tm_swa, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
   delete p;
+  return st;
+}
+
+// Device address of g_static_scratch on the current device, looked up once
+// per device (host code cannot use the symbol itself as a device pointer).
+static void* static_scratch_ptr() {
+  static std::mutex mu;
+  static void* ptrs[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
+csa2_status_t csa2_index_topk_decode_static(const csa2_cache_t* c, int32_t nq, const void* q_idx,
+                                            const float* w, const int32_t* seq_ids,
+                                            int32_t* topk_idx, float* topk_score,
+                                            csa2_stream_t stream) {
+  if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
+  if (nq == 0) return CSA2_OK;
+  csa2_status_t st = check_decode_queries(c, nq, q_idx, w, seq_ids);
+  if (st != CSA2_OK) return st;
+  if (!topk_idx) return CSA2_ERR_INVALID_ARG;
+  const int64_t ld = score_ld(c->max_cap);
+  const size_t need = (size_t)nq * ((size_t)ld * sizeof(float) + kKeyHistBinsHost * sizeof(uint32_t));
+  if (need > CSA2_STATIC_SCRATCH_BYTES) return CSA2_ERR_CAPACITY;
+  void* scratch = static_scratch_ptr();
+  if (!scratch) return CSA2_ERR_CUDA;
+  float* scores = static_cast<float*>(scratch);
+  uint32_t* key_hist = reinterpret_cast<uint32_t*>(scores + (int64_t)nq * ld);
+  // parameter blocks on the stack: this path touches no heap
+  IndexParams ip;
+  st = run_index_decode(c, nq, q_idx, w, seq_ids, scores, ld, key_hist, stream, &ip);
+  const int k = c->cfg.topk;
+  TopkParams tp;
+  for (int q0 = 0; q0 < nq && st == CSA2_OK; q0 += kTopkTab) {
+    const int n = std::min(kTopkTab, nq - q0);
+    std::memset(&tp, 0, sizeof(TopkParams));
+    tp.scores = scores + (int64_t)q0 * ld;
+    tp.ld = ld;
+    tp.rows = n;
+    tp.k = k;
+    tp.idx_out = topk_idx + (int64_t)q0 * k;
+    tp.score_out = topk_score ? topk_score + (int64_t)q0 * k : nullptr;
+    tp.key_hist = key_hist + (int64_t)q0 * kKeyHistBinsHost;
+    tp.seg_ws = nullptr;   // one CTA per row: no segment scratch
+    tp.n_seg = 0;
+    tp.formula = 0;
+    for (int i = 0; i < n; ++i) tp.n_valid[i] = c->len[seq_ids ? seq_ids[q0 + i] : q0 + i];
+    if (launch_topk(tp, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
+  }
   return st;
 }
 

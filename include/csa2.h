@@ -218,6 +218,38 @@ csa2_status_t csa2_index_topk_decode(const csa2_cache_t* cache,
                                      void* workspace, size_t workspace_bytes,
                                      csa2_stream_t stream);
 
+/* The same selection as csa2_index_topk_decode for callers that cannot
+ * allocate device memory.  The pages have no counterpart: this is an
+ * integration entry point, not part of the method.
+ *
+ * Some callers cannot call cudaMalloc or hand over a workspace: code that
+ * runs while a CUDA graph is being captured (allocation is not a capturable
+ * operation), runtimes that own every byte of device memory through their
+ * own pool and give kernels no scratch, and plain C hosts that want a
+ * single call with nothing to size or free.  This entry point keeps its
+ * scratch (fp32 scores and score-key histograms) in a fixed array inside
+ * the library, CSA2_STATIC_SCRATCH_BYTES long; every GPU that loads the
+ * library holds that array until the process exits.
+ *   - Requests needing more than the array (n_queries * (4 * ld + 8192)
+ *     bytes, ld = the longest capacity rounded up to a multiple of 4) return
+ *     CSA2_ERR_CAPACITY and launch nothing.
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call uses the same array, so two calls that overlap on the GPU
+ *     (different streams without ordering between them) race; calls on one
+ *     stream are safe.
+ *   - Allocates nothing: no cudaMalloc / cudaFree, no host heap.
+ * Arguments and outputs as for csa2_index_topk_decode.                     */
+#define CSA2_STATIC_SCRATCH_BYTES ((size_t)48 << 20)
+csa2_status_t csa2_index_topk_decode_static(const csa2_cache_t* cache,
+                                            int32_t n_queries,
+                                            const void* q_idx, const float* w,
+                                            const int32_t* seq_ids,
+                                            int32_t* topk_idx,
+                                            float* topk_score,
+                                            csa2_stream_t stream);
+
 /* Full-mode selection for a prefill chunk of one sequence: query i is the
  * token at absolute position pos0 + i and sees entry s iff its block is
  * complete, (s + 1) * ratio - 1 <= pos0 + i ([V41 sec 2.3.2] "causally
