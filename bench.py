@@ -307,18 +307,25 @@ def run_csa2(args):
     scale = 512 ** -0.5
     stream = torch.cuda.current_stream()
 
-    def step(ev=None):
+    # two sets of per-step device buffers (inputs and outputs): set 0 for the
+    # device-resident timing, both for the double-buffered end-to-end leg
+    bufs = [dict(q_idx=q_idx, w=w, qs=qs, swas=swas, topk=topk, outs=outs, lses=lses)]
+    bufs.append({k: ([x.clone() for x in v] if isinstance(v, list) else v.clone())
+                 for k, v in bufs[0].items()})
+
+    def step(ev=None, b=0):
+        d = bufs[b]
         if ev is not None:
             ev[0].record(stream)
-        C.csa2_index_scores_decode(cache, q_idx, w, scores, key_hist=key_hist)
+        C.csa2_index_scores_decode(cache, d["q_idx"], d["w"], scores, key_hist=key_hist)
         if ev is not None:
             ev[1].record(stream)
-        C.csa2_topk(scores, n_valid, 512, idx_out=topk, key_hist=key_hist, workspace=topk_ws)
+        C.csa2_topk(scores, n_valid, 512, idx_out=d["topk"], key_hist=key_hist, workspace=topk_ws)
         if ev is not None:
             ev[2].record(stream)
         for l in range(L):
-            C.csa2_sparse_attn_decode(cache, qs[l], swas[l], topk, scale, out=outs[l],
-                                      lse=lses[l], workspace=attn_ws)
+            C.csa2_sparse_attn_decode(cache, d["qs"][l], d["swas"][l], d["topk"], scale,
+                                      out=d["outs"][l], lse=d["lses"][l], workspace=attn_ws)
         if ev is not None:
             ev[3].record(stream)
 
@@ -330,20 +337,23 @@ def run_csa2(args):
 
     # ---- the step captured once as a CUDA graph (every call is stream-ordered
     #      and allocation-free), replayed for the headline timing
-    graph = None
+    graphs = None
     if not args.no_graph:
         side = torch.cuda.Stream()
         side.wait_stream(stream)
         with torch.cuda.stream(side):
-            step()
+            step(b=0)
+            step(b=1)
         stream.wait_stream(side)
         torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            step()
+        graphs = [torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()]
+        for b in range(2):
+            with torch.cuda.graph(graphs[b]):
+                step(b=b)
         for _ in range(max(3, args.warmup)):
-            graph.replay()
+            graphs[0].replay()
         torch.cuda.synchronize()
+    graph = graphs[0] if graphs else None
 
     barrier(world)
     t_start = torch.cuda.Event(enable_timing=True)
@@ -380,38 +390,66 @@ def run_csa2(args):
         raise RuntimeError("device error word set during the benchmark")
     elapsed_max = max_over_ranks(elapsed, world, dev)
 
-    # ---- end to end: host inputs -> device -> host outputs, per step
+    # ---- end to end: every step's inputs go host -> device and its outputs
+    #      device -> host inside the timed region, double-buffered the way a
+    #      serving loop would run it: the copies of step i+1's inputs and of
+    #      step i-1's outputs run on a copy stream while step i computes
     e2e_steps = args.e2e_steps or max(3, min(args.steps, 200))
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
-    h_in = [pin(q_idx), pin(w)] + [pin(x) for x in qs] + [pin(x) for x in swas]
-    d_in = [q_idx, w] + qs + swas
-    h_out = [torch.empty(topk.shape, dtype=topk.dtype, pin_memory=True)] + \
-        [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs] + \
-        [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in lses]
-    d_out = [topk] + outs + lses
+    names_in = ["q_idx", "w", "qs", "swas"]
+    names_out = ["topk", "outs", "lses"]
+    flat = lambda d, names: [x for n in names for x in (d[n] if isinstance(d[n], list) else [d[n]])]
+    h_in = [pin(t) for t in flat(bufs[0], names_in)]
+    h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in flat(bufs[0], names_out)]
+             for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in h_in)
-    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0])
+    copy_stream = torch.cuda.Stream()
 
-    def e2e_step():
-        for h, d in zip(h_in, d_in):
-            d.copy_(h, non_blocking=True)
-        step()
-        for h, d in zip(h_out, d_out):
-            h.copy_(d, non_blocking=True)
+    def run_e2e(n):
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+        out_free = [torch.cuda.Event() for _ in range(2)]
+        with torch.cuda.stream(copy_stream):
+            for h, d in zip(h_in, flat(bufs[0], names_in)):
+                d.copy_(h, non_blocking=True)
+            in_ready[0].record(copy_stream)
+        for i in range(n):
+            b = i % 2
+            stream.wait_event(in_ready[b])
+            if i >= 2:
+                stream.wait_event(out_free[b])
+            if graphs:
+                graphs[b].replay()
+            else:
+                step(b=b)
+            done[b].record(stream)
+            with torch.cuda.stream(copy_stream):
+                if i + 1 < n:
+                    if i >= 1:
+                        copy_stream.wait_event(done[1 - b])
+                    for h, d in zip(h_in, flat(bufs[1 - b], names_in)):
+                        d.copy_(h, non_blocking=True)
+                    in_ready[1 - b].record(copy_stream)
+                copy_stream.wait_event(done[b])
+                for h, d in zip(h_out[b], flat(bufs[b], names_out)):
+                    h.copy_(d, non_blocking=True)
+                out_free[b].record(copy_stream)
+        stream.wait_stream(copy_stream)
 
-    for _ in range(3):
-        e2e_step()
+    run_e2e(3)
     torch.cuda.synchronize()
     barrier(world)
     a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
+    b_ = torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    b.record(stream)
+    copy_stream.wait_stream(stream)
+    run_e2e(e2e_steps)
+    b_.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    e2e_elapsed = max_over_ranks(a.elapsed_time(b) / 1000.0, world, dev)
+    e2e_elapsed_local = a.elapsed_time(b_) / 1000.0
+    e2e_elapsed = max_over_ranks(e2e_elapsed_local, world, dev)
 
     # ---- accounting
     hbm_peak, peak_kind = measured_peaks()
@@ -447,7 +485,9 @@ def run_csa2(args):
                       "eager_step": eager_ms, "timed_as": "cuda graph replay" if graph is not None
                       else "eager calls"},
         "e2e": {"value": B * world * e2e_steps / e2e_elapsed, "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "pipelining": "inputs of step i+1 and outputs of step i-1 copied on a "
+                              "second stream while step i computes (pinned host buffers)"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
@@ -461,10 +501,116 @@ def run_csa2(args):
     return 0
 
 
+def run_prefill(args):
+    """Chunked prefill of one sequence (workload 4): 8192 new tokens on a
+    131072-token prefix, ratio 2; per step the Full layer's causal index
+    scores and top-512, then the attention of the Full and the Reuse layers."""
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import fp4_kv_cache_index_gb300 as C
+    from csa2_synth import workloads as W
+    wl = W.WORKLOADS[args.workload]
+    L, T = wl.layers, wl.n_queries()
+    n_ent = int(wl.n_entries()[0])
+    cache = C.Cache(C.config(ratio=wl.ratio, layout=args.layout), [n_ent], device=dev)
+    W.fill_cache(wl, cache)
+    q_idx, w = W.dev_q_idx(wl), W.dev_w(wl)
+    qs = [W.dev_q(wl, l) for l in range(L)]
+    rows = [W.dev_swa(wl, l) for l in range(L)]
+    ld = (n_ent + 3) // 4 * 4
+    scores = torch.empty(T, ld, dtype=torch.float32, device=dev)
+    topk = torch.empty(T, 512, dtype=torch.int32, device=dev)
+    outs = [torch.empty(T, 64, 512, dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    n_valid = [min(n_ent, (wl.pos0 + i + 1) // wl.ratio) for i in range(T)]
+    scale = 512 ** -0.5
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        C.csa2_index_scores_prefill(cache, 0, wl.pos0, q_idx, w, scores)
+        if ev is not None:
+            ev[1].record(stream)
+        C.csa2_topk(scores, n_valid, 512, idx_out=topk)
+        if ev is not None:
+            ev[2].record(stream)
+        for l in range(L):
+            C.csa2_sparse_attn_prefill(cache, 0, wl.pos0, qs[l], rows[l], wl.swa_pos0, topk,
+                                       scale, out=outs[l])
+        if ev is not None:
+            ev[3].record(stream)
+
+    sampler = ClockSampler(local).start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    elapsed = max_over_ranks(a.elapsed_time(b) / 1000.0, world, dev)
+    t_idx = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps / 1000.0
+    t_topk = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps / 1000.0
+    t_attn = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps / 1000.0
+    if cache.device_error() != 0:
+        raise RuntimeError("device error word set during the benchmark")
+    idx_flops = 2.0 * 32 * 128 * sum(n_valid)            # visible entries only
+    cand = [min(512, n) + min(128, wl.pos0 + i - wl.swa_pos0 + 1) for i, n in enumerate(n_valid)]
+    attn_flops = L * 64 * 512 * 4.0 * sum(cand)
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = float(peaks.get("bf16_tflops_sustained", 1700.0))
+    ms = 1000 * elapsed / args.steps
+    line = {
+        "metric": "CSA2 prefill query-tokens/s, 8192 tokens on a 128K prefix; indexer "
+                  "tensor-pipe TFLOP/s vs peak",
+        "value": T * world * args.steps / elapsed, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": 1, "new_tokens": T, "prefix_tokens": wl.ctx,
+                   "entries": n_ent, "ratio": wl.ratio,
+                   "layers": f"1 Full + {L - 1} Reuse",
+                   "layout": "L32_UE8M0" if args.layout == 0 else "L16_E4M3",
+                   "l2": "inputs larger than L2 (2.3 GB of scores and 4.4 GB of "
+                         "indexer-key reads per step)"},
+        "roofline": {"kernel": "k_index (prefill, 8 queries x 32 heads per MMA tile)",
+                     "bound": "tensor", "achieved": idx_flops / t_idx / 1e12, "peak": peak,
+                     "unit": "TFLOP/s", "frac": idx_flops / t_idx / 1e12 / peak,
+                     "traffic": None, "peak_kind": "measured bf16 cuBLAS, sustained"},
+        "step_tensor": {"achieved": (idx_flops + attn_flops) / (ms / 1000) / 1e12, "peak": peak,
+                        "unit": "TFLOP/s",
+                        "frac": (idx_flops + attn_flops) / (ms / 1000) / 1e12 / peak,
+                        "flops_per_step": idx_flops + attn_flops},
+        "kernel_ms": {"index_scores": 1000 * t_idx, "topk": 1000 * t_topk,
+                      "sparse_attn_all_layers": 1000 * t_attn},
+        "gpu_launches": args.steps * (1 + (T + 1023) // 1024 + L),
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    from csa2_synth.workloads import WORKLOADS
+    if WORKLOADS[args.workload].prefill:
+        return run_prefill(args)
     return run_csa2(args)
 
 

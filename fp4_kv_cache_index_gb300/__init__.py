@@ -79,6 +79,7 @@ def _load():
         "csa2_index_topk_decode": ([P, i32, P, P, P, P, P, P, sz, P], i32),
         "csa2_index_topk_prefill": ([P, i32, i32, i64, P, P, P, P, P, sz, P], i32),
         "csa2_index_topk_decode_static": ([P, i32, P, P, P, P, P, P], i32),
+        "csa2_index_scores_prefill": ([P, i32, i32, i64, P, P, P, i64, P], i32),
         "csa2_topk_workspace_bytes": ([i32, i64], sz),
         "csa2_topk": ([i32, P, i64, P, i32, P, P, P, P, sz, P], i32),
         "csa2_sparse_attn_workspace_bytes": ([P, i32], sz),
@@ -253,6 +254,15 @@ def csa2_index_topk_decode(cache: Cache, q_idx: torch.Tensor, w: torch.Tensor,
                                       _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "csa2_index_topk_decode")
     return topk_idx
+
+
+def csa2_index_scores_prefill(cache: Cache, seq: int, pos0: int, q_idx: torch.Tensor,
+                              w: torch.Tensor, scores: torch.Tensor, stream=None):
+    """scores: fp32 [n_queries, ld] (ld a multiple of 4, >= the length)."""
+    _check(lib.csa2_index_scores_prefill(cache.handle, seq, q_idx.shape[0], pos0, _ptr(q_idx),
+                                         _ptr(w), _ptr(scores), scores.shape[1],
+                                         _stream(stream)), "csa2_index_scores_prefill")
+    return scores
 
 
 def csa2_index_topk_prefill(cache: Cache, seq: int, pos0: int, q_idx: torch.Tensor,

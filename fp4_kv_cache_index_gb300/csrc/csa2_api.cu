@@ -517,26 +517,21 @@ csa2_status_t csa2_index_topk_decode(const csa2_cache_t* c, int32_t nq, const vo
   return st;
 }
 
-csa2_status_t csa2_index_topk_prefill(const csa2_cache_t* c, int32_t seq, int32_t nq, int64_t pos0,
-                                      const void* q_idx, const float* w, int32_t* topk_idx,
-                                      float* topk_score, void* workspace, size_t ws_bytes,
-                                      csa2_stream_t stream) {
+csa2_status_t csa2_index_scores_prefill(const csa2_cache_t* c, int32_t seq, int32_t nq,
+                                        int64_t pos0, const void* q_idx, const float* w,
+                                        float* scores, int64_t ld, csa2_stream_t stream) {
   if (!c || nq < 0 || seq < 0 || seq >= c->batch || pos0 < 0) return CSA2_ERR_INVALID_ARG;
   if (nq == 0) return CSA2_OK;
-  if (!q_idx || !w || !topk_idx || !workspace || !aligned16(q_idx) || !aligned16(w) ||
-      !aligned16(workspace))
+  if (!q_idx || !w || !scores || !aligned16(q_idx) || !aligned16(w) || !aligned16(scores) ||
+      ld % 4 != 0)
     return CSA2_ERR_INVALID_ARG;
-  const int64_t ld = score_ld(c->cap[seq]);
-  if (ws_bytes < (size_t)nq * (size_t)ld * sizeof(float)) return CSA2_ERR_CAPACITY;
-  constexpr int kQpg = 8;
+  if (ld < c->len[seq]) return CSA2_ERR_CAPACITY;
+  constexpr int kQpg = 8;   // queries sharing one K_I tile in the MMA (N = 256)
   const int m = c->cfg.ratio;
   const int64_t len = c->len[seq];
-  float* scores = static_cast<float*>(workspace);
-  const int k = c->cfg.topk;
   const uint16_t* qb = static_cast<const uint16_t*>(q_idx);
   IndexParams* ip = new (std::nothrow) IndexParams();
-  TopkParams* tp = new (std::nothrow) TopkParams();
-  if (!ip || !tp) { delete ip; delete tp; return CSA2_ERR_OOM; }
+  if (!ip) return CSA2_ERR_OOM;
   csa2_status_t st = CSA2_OK;
   const int per_launch = kMaxIdxGroups * kQpg;
   for (int q0 = 0; q0 < nq && st == CSA2_OK; q0 += per_launch) {
@@ -570,25 +565,38 @@ csa2_status_t csa2_index_topk_prefill(const csa2_cache_t* c, int32_t seq, int32_
     const int tiles = ip->tile_prefix[groups];
     if (tiles > 0) {
       const int grid = std::min(c->num_sms, tiles);
-      if (launch_index(*ip, c->tm_k, tm_q, grid, S(stream)) != cudaSuccess) {
-        st = CSA2_ERR_CUDA;
-        break;
-      }
+      if (launch_index(*ip, c->tm_k, tm_q, grid, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
     }
-    std::memset(tp, 0, sizeof(TopkParams));
-    tp->scores = ip->scores;
-    tp->ld = ld;
-    tp->rows = n;
-    tp->k = k;
-    tp->idx_out = topk_idx + (int64_t)q0 * k;
-    tp->score_out = topk_score ? topk_score + (int64_t)q0 * k : nullptr;
-    tp->formula = 1;
-    tp->pre_len = (int32_t)len;
-    tp->ratio = m;
-    tp->pos0 = pos0 + q0;
-    if (launch_topk(*tp, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
   }
   delete ip;
+  return st;
+}
+
+csa2_status_t csa2_index_topk_prefill(const csa2_cache_t* c, int32_t seq, int32_t nq, int64_t pos0,
+                                      const void* q_idx, const float* w, int32_t* topk_idx,
+                                      float* topk_score, void* workspace, size_t ws_bytes,
+                                      csa2_stream_t stream) {
+  if (!c || nq < 0 || seq < 0 || seq >= c->batch || pos0 < 0) return CSA2_ERR_INVALID_ARG;
+  if (nq == 0) return CSA2_OK;
+  if (!topk_idx || !workspace || !aligned16(workspace)) return CSA2_ERR_INVALID_ARG;
+  const int64_t ld = score_ld(c->cap[seq]);
+  if (ws_bytes < (size_t)nq * (size_t)ld * sizeof(float)) return CSA2_ERR_CAPACITY;
+  float* scores = static_cast<float*>(workspace);
+  csa2_status_t st = csa2_index_scores_prefill(c, seq, nq, pos0, q_idx, w, scores, ld, stream);
+  if (st != CSA2_OK) return st;
+  TopkParams* tp = new (std::nothrow) TopkParams();
+  if (!tp) return CSA2_ERR_OOM;
+  tp->scores = scores;
+  tp->ld = ld;
+  tp->rows = nq;
+  tp->k = c->cfg.topk;
+  tp->idx_out = topk_idx;
+  tp->score_out = topk_score;
+  tp->formula = 1;
+  tp->pre_len = (int32_t)c->len[seq];
+  tp->ratio = c->cfg.ratio;
+  tp->pos0 = pos0;
+  if (launch_topk(*tp, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
   delete tp;
   return st;
 }

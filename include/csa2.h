@@ -263,6 +263,19 @@ csa2_status_t csa2_index_topk_prefill(const csa2_cache_t* cache, int32_t seq,
                                       void* workspace, size_t workspace_bytes,
                                       csa2_stream_t stream);
 
+/* Index scores only for a prefill chunk (the scoring step of
+ * csa2_index_topk_prefill): query i at position pos0 + i, scores[i * ld + s]
+ * for every entry s visible to it ((s + 1) * ratio - 1 <= pos0 + i);
+ * other entries are left untouched.  Eight consecutive queries share each
+ * tile of indexer keys on the tensor cores.
+ *   scores: dev fp32 [n_queries, ld], ld >= the sequence's length and a
+ *   multiple of 4;  other arguments as for csa2_index_topk_prefill.         */
+csa2_status_t csa2_index_scores_prefill(const csa2_cache_t* cache, int32_t seq,
+                                        int32_t n_queries, int64_t pos0,
+                                        const void* q_idx, const float* w,
+                                        float* scores, int64_t ld,
+                                        csa2_stream_t stream);
+
 /* Workspace bytes with which csa2_topk splits each row's candidate search
  * over several CTAs (used when key_hist is given), for n_rows rows of at
  * most max_valid scores.  A smaller workspace (or none) is allowed: the
