@@ -14,7 +14,8 @@
 //
 // Persistent CTAs walk a balanced contiguous range of (group, tile) items.
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner),
-// warps 2-5 = epilogue (TMEM -> registers -> scores).  Every wait is bounded.
+// warps 2-9 = epilogue (TMEM -> registers -> scores), two warps per TMEM lane
+// quadrant splitting the queries of a group.  Every wait is bounded.
 #include "csa2_device.cuh"
 #include "csa2_kernels.h"
 
@@ -24,7 +25,8 @@ namespace {
 constexpr int kTileE = 128;
 constexpr int kStages = 4;
 constexpr int kKStageBytes = kTileE * kIdxDim * 2;  // 32 KB
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 256;   // warps 2-9
 
 struct SmemLayout {
   int q_off, w_off, hist_off, bar_off, total;
@@ -79,7 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) { mbar_init(k_full + i, 1); mbar_init(k_empty + i, 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, 128); }
+    for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, kEpiThreads); }
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     mbar_init(drain, 1);
@@ -171,20 +173,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ epilogue
     const int quad = warp & 3;                 // TMEM lane quadrant of this warp
     const int row = quad * 32 + lane;          // entry within the tile
-    const int et = threadIdx.x - 64;           // 0..127
+    const int et = threadIdx.x - 64;           // 0..255
+    const int half = (warp - 2) >> 2;          // which queries of the group
+    const int jq = (p.qpg + 1) >> 1;
+    const int j0 = half * jq, j1 = min(p.qpg, j0 + jq);
     const bool use_hist = p.key_hist != nullptr && p.qpg == 1;
     // adds this CTA's counts of query `qq` to the global histogram, clears hs
     auto flush = [&](int qq) {
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      for (int i = et; i < kKeyHistBins; i += 128) {
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      for (int i = et; i < kKeyHistBins; i += kEpiThreads) {
         const uint32_t v = hs[i];
         if (v) atomicAdd(p.key_hist + (int64_t)qq * kKeyHistBins + i, v);
         hs[i] = 0u;
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, 256;" ::: "memory");
     };
     if (use_hist) {
-      for (int i = et; i < kKeyHistBins; i += 128) hs[i] = 0u;
+      for (int i = et; i < kKeyHistBins; i += kEpiThreads) hs[i] = 0u;
     }
     int g = g0, cur = -1, acc = 0;
     uint32_t aph = 0;
@@ -192,19 +197,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (p.tile_prefix[g + 1] <= it) ++g;
       if (g != cur) {
         if (use_hist && cur >= 0) flush(cur);
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        for (int i = et; i < qrows; i += 128) {
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        for (int i = et; i < qrows; i += kEpiThreads) {
           const int q = g * p.qpg + (i >> 5);
           wbuf[i] = (q < p.nq) ? __ldg(p.w + (int64_t)q * kIdxHeads + (i & 31)) : 0.0f;
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        asm volatile("bar.sync 1, 256;" ::: "memory");
         cur = g;
       }
       if (!mbar_wait(acc_full + acc, aph, p.err)) break;
       tc_fence_after();
       const int t = it - p.tile_prefix[g];
       const int e = t * kTileE + row;
-      for (int j = 0; j < p.qpg; ++j) {
+      for (int j = j0; j < j1; ++j) {
         uint32_t r[32];
         tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * N + j * 32), r);
         const float* wj = wbuf + j * 32;
