@@ -239,3 +239,41 @@ def swa_rows(pos: int, window: int, row0_pos: int = 0):
     positions [max(row0_pos, pos - window + 1), pos] (report section 3.2.2)."""
     lo = max(row0_pos, pos - window + 1)
     return lo, pos + 1
+
+
+# ---------------------------------------------------------------- hierarchical sparse indexer
+def hsi_pool(scores_f32, n_vis: int, block: int = 8, max_blocks: int = 2048) -> np.ndarray:
+    """Candidate pool of the Hierarchical Sparse Indexer ("DeepSeek-V4.1-Flash"
+    report, section 2.3.2): each block of `block` consecutive positions gets
+    the maximum index score among its visible positions; the `max_blocks`
+    blocks with the highest block scores are kept (ties to the lower block
+    index, the same selection rule as the entries' top-k).  Returns the kept
+    block indices in ascending order, padded with -1 to `max_blocks`."""
+    s = np.asarray(scores_f32, np.float32)[:n_vis]
+    n_blocks = (n_vis + block - 1) // block
+    bmax = np.full(n_blocks, -np.inf, np.float32)
+    for b in range(n_blocks):
+        bmax[b] = s[b * block:(b + 1) * block].max()
+    return topk(bmax, max_blocks)
+
+
+def pool_positions(pool_blocks, n_vis: int, block: int = 8) -> np.ndarray:
+    """Visible positions covered by the pool blocks, ascending."""
+    b = np.asarray(pool_blocks)
+    b = b[b >= 0]
+    pos = (b[:, None] * block + np.arange(block)[None, :]).ravel()
+    return pos[pos < n_vis]
+
+
+def reindex_topk(k_bf16, q_bf16, w, pool_blocks, n_vis: int, k: int = 512, block: int = 8):
+    """Reindex mode (same section): the layer's own indexer query scores only
+    the pool positions (fp64, rounded to fp32 for the decision) and keeps the
+    top-k of them, ties to the lower position, ascending, -1 padded.
+    Returns (idx [k], fp64 scores of the pool positions, the positions)."""
+    pos = pool_positions(pool_blocks, n_vis, block)
+    sc = index_scores(np.asarray(k_bf16)[pos], q_bf16, w)
+    sel = topk(sc.astype(np.float32), k)
+    out = np.full(k, -1, np.int32)
+    n = int((sel >= 0).sum())
+    out[:n] = pos[sel[:n]]
+    return out, sc, pos
