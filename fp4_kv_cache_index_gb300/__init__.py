@@ -80,6 +80,10 @@ def _load():
         "csa2_index_topk_prefill": ([P, i32, i32, i64, P, P, P, P, P, sz, P], i32),
         "csa2_index_topk_decode_static": ([P, i32, P, P, P, P, P, P], i32),
         "csa2_index_scores_prefill": ([P, i32, i32, i64, P, P, P, i64, P], i32),
+        "csa2_hsi_pool_workspace_bytes": ([i32, i64], sz),
+        "csa2_hsi_pool": ([i32, P, i64, P, i32, i32, P, P, sz, P], i32),
+        "csa2_index_reindex_workspace_bytes": ([P, i32, i32], sz),
+        "csa2_index_topk_reindex_decode": ([P, i32, P, P, P, P, i32, P, P, P, sz, P], i32),
         "csa2_topk_workspace_bytes": ([i32, i64], sz),
         "csa2_topk": ([i32, P, i64, P, i32, P, P, P, P, sz, P], i32),
         "csa2_sparse_attn_workspace_bytes": ([P, i32], sz),
@@ -347,3 +351,44 @@ def csa2_sparse_attn_prefill(cache: Cache, seq: int, pos0: int, q: torch.Tensor,
                                         _ptr(out), _ptr(lse), _stream(stream)),
            "csa2_sparse_attn_prefill")
     return out
+
+
+# ------------------------------------------------------------------ hierarchical sparse indexer
+def csa2_hsi_pool(scores: torch.Tensor, n_valid: Sequence[int], max_blocks: int = 2048,
+                  block: int = 8, pool_blocks: Optional[torch.Tensor] = None,
+                  workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """scores: fp32 [rows, ld] of a Full layer; returns int32 [rows, max_blocks]
+    kept block indices (ascending, -1 padded)."""
+    rows, ld = scores.shape
+    if pool_blocks is None:
+        pool_blocks = torch.empty(rows, max_blocks, dtype=torch.int32, device=scores.device)
+    workspace = _workspace(int(lib.csa2_hsi_pool_workspace_bytes(rows, max(n_valid, default=0))),
+                           scores.device, workspace)
+    _check(lib.csa2_hsi_pool(rows, _ptr(scores), ld, _i64_array(n_valid), block, max_blocks,
+                             _ptr(pool_blocks), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream(stream)),
+           "csa2_hsi_pool")
+    return pool_blocks
+
+
+def csa2_index_topk_reindex_decode(cache: Cache, q_idx: torch.Tensor, w: torch.Tensor,
+                                   pool_blocks: torch.Tensor,
+                                   seq_ids: Optional[Sequence[int]] = None,
+                                   topk_idx: Optional[torch.Tensor] = None,
+                                   topk_score: Optional[torch.Tensor] = None,
+                                   workspace: Optional[torch.Tensor] = None,
+                                   stream=None) -> torch.Tensor:
+    """Reindex-layer top-k inside each query's pool (pool_blocks from
+    csa2_hsi_pool, one row per query); returns int32 [n_queries, topk]."""
+    nq, max_blocks = pool_blocks.shape
+    if topk_idx is None:
+        topk_idx = torch.empty(nq, cache.cfg.topk, dtype=torch.int32, device=q_idx.device)
+    workspace = _workspace(int(lib.csa2_index_reindex_workspace_bytes(cache.handle, nq, max_blocks)),
+                           q_idx.device, workspace)
+    _check(lib.csa2_index_topk_reindex_decode(cache.handle, nq, _ptr(q_idx), _ptr(w),
+                                              _i32_array(seq_ids), _ptr(pool_blocks), max_blocks,
+                                              _ptr(topk_idx), _ptr(topk_score), _ptr(workspace),
+                                              workspace.numel() * workspace.element_size(),
+                                              _stream(stream)),
+           "csa2_index_topk_reindex_decode")
+    return topk_idx

@@ -31,7 +31,8 @@ struct csa2_cache {
   uint8_t* codes;
   uint8_t* scales;
   uint16_t* idxk;
-  CUtensorMap tm_k;
+  CUtensorMap tm_k;    // indexer keys, 128-row boxes (contiguous tiles)
+  CUtensorMap tm_k8;   // indexer keys, 8-row boxes (pool blocks)
   int num_sms;
 };
 
@@ -263,7 +264,8 @@ csa2_status_t csa2_cache_create(const csa2_config_t* cfg, int32_t batch, const i
     delete c;
     return CSA2_ERR_CUDA;
   }
-  if (!make_map(&c->tm_k, c->idxk, (uint64_t)c->total, kIdxDim, 64, 128)) {
+  if (!make_map(&c->tm_k, c->idxk, (uint64_t)c->total, kIdxDim, 64, 128) ||
+      !make_map(&c->tm_k8, c->idxk, (uint64_t)c->total, kIdxDim, 64, kHsiBlock)) {
     delete c;
     return CSA2_ERR_CUDA;
   }
@@ -784,6 +786,164 @@ csa2_status_t csa2_index_topk_decode_static(const csa2_cache_t* c, int32_t nq, c
     for (int i = 0; i < n; ++i) tp.n_valid[i] = c->len[seq_ids ? seq_ids[q0 + i] : q0 + i];
     if (launch_topk(tp, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
   }
+  return st;
+}
+
+// ---------------------------------------------------------------- HSI
+static int64_t hsi_ld_b(int64_t max_valid) {
+  return score_ld((max_valid + kHsiBlock - 1) / kHsiBlock);
+}
+
+size_t csa2_hsi_pool_workspace_bytes(int32_t n_rows, int64_t max_valid) {
+  if (n_rows < 0 || max_valid < 0) return 0;
+  return (size_t)n_rows * (size_t)hsi_ld_b(max_valid) * sizeof(float);
+}
+
+csa2_status_t csa2_hsi_pool(int32_t n_rows, const float* scores, int64_t ld,
+                            const int64_t* n_valid, int32_t block, int32_t max_blocks,
+                            int32_t* pool_blocks, void* workspace, size_t ws_bytes,
+                            csa2_stream_t stream) {
+  if (n_rows < 0 || ld < 0) return CSA2_ERR_INVALID_ARG;
+  if (block != kHsiBlock || max_blocks <= 0 || max_blocks % 16 != 0 || max_blocks > 4096)
+    return CSA2_ERR_UNSUPPORTED;
+  if (n_rows == 0) return CSA2_OK;
+  if (!scores || !n_valid || !pool_blocks || !workspace || !aligned16(workspace))
+    return CSA2_ERR_INVALID_ARG;
+  int64_t max_valid = 0;
+  for (int r = 0; r < n_rows; ++r) {
+    if (n_valid[r] < 0 || n_valid[r] > ld) return CSA2_ERR_INVALID_ARG;
+    max_valid = std::max(max_valid, n_valid[r]);
+  }
+  if (ws_bytes < csa2_hsi_pool_workspace_bytes(n_rows, max_valid)) return CSA2_ERR_CAPACITY;
+  const int64_t ld_b = hsi_ld_b(max_valid);
+  float* bmax = static_cast<float*>(workspace);
+  HsiParams* hp = new (std::nothrow) HsiParams();
+  TopkParams* tp = new (std::nothrow) TopkParams();
+  if (!hp || !tp) { delete hp; delete tp; return CSA2_ERR_OOM; }
+  csa2_status_t st = CSA2_OK;
+  for (int r0 = 0; r0 < n_rows && st == CSA2_OK; r0 += kHsiTab) {
+    const int n = std::min(kHsiTab, n_rows - r0);
+    std::memset(hp, 0, sizeof(HsiParams));
+    hp->rows = n;
+    hp->scores = scores + (int64_t)r0 * ld;
+    hp->ld = ld;
+    hp->bmax = bmax + (int64_t)r0 * ld_b;
+    hp->ld_b = ld_b;
+    for (int i = 0; i < n; ++i) hp->n[i] = n_valid[r0 + i];
+    if (launch_block_max(*hp, S(stream)) != cudaSuccess) { st = CSA2_ERR_CUDA; break; }
+    // the blocks with the highest block scores, ties to the lower block
+    std::memset(tp, 0, sizeof(TopkParams));
+    tp->scores = hp->bmax;
+    tp->ld = ld_b;
+    tp->rows = n;
+    tp->k = max_blocks;
+    tp->idx_out = pool_blocks + (int64_t)r0 * max_blocks;
+    tp->formula = 0;
+    for (int i = 0; i < n; ++i) tp->n_valid[i] = (n_valid[r0 + i] + kHsiBlock - 1) / kHsiBlock;
+    if (launch_topk(*tp, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
+  }
+  delete hp;
+  delete tp;
+  return st;
+}
+
+size_t csa2_index_reindex_workspace_bytes(const csa2_cache_t* c, int32_t n_queries,
+                                          int32_t max_blocks) {
+  if (!c || n_queries < 0 || max_blocks <= 0) return 0;
+  const int64_t slots = (int64_t)max_blocks * kHsiBlock;
+  return (size_t)n_queries * ((size_t)slots * sizeof(float) + kKeyHistBinsHost * 4 +
+                              (size_t)c->cfg.topk * 4) +
+         topk_seg_bytes(n_queries, slots);
+}
+
+csa2_status_t csa2_index_topk_reindex_decode(const csa2_cache_t* c, int32_t nq, const void* q_idx,
+                                             const float* w, const int32_t* seq_ids,
+                                             const int32_t* pool_blocks, int32_t max_blocks,
+                                             int32_t* topk_idx, float* topk_score,
+                                             void* workspace, size_t ws_bytes,
+                                             csa2_stream_t stream) {
+  if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
+  if (max_blocks <= 0 || max_blocks % 16 != 0 || max_blocks > 4096) return CSA2_ERR_UNSUPPORTED;
+  if (nq == 0) return CSA2_OK;
+  csa2_status_t st = check_decode_queries(c, nq, q_idx, w, seq_ids);
+  if (st != CSA2_OK) return st;
+  if (!pool_blocks || !topk_idx || !workspace || !aligned16(workspace)) return CSA2_ERR_INVALID_ARG;
+  if (ws_bytes < csa2_index_reindex_workspace_bytes(c, nq, max_blocks)) return CSA2_ERR_CAPACITY;
+  const int64_t slots = (int64_t)max_blocks * kHsiBlock;
+  float* pscores = static_cast<float*>(workspace);
+  uint32_t* key_hist = reinterpret_cast<uint32_t*>(pscores + (int64_t)nq * slots);
+  int32_t* sel = reinterpret_cast<int32_t*>(key_hist + (int64_t)nq * kKeyHistBinsHost);
+  uint32_t* seg_ws = reinterpret_cast<uint32_t*>(sel + (int64_t)nq * c->cfg.topk);
+  const int k = c->cfg.topk;
+  IndexParams* ip = new (std::nothrow) IndexParams();
+  TopkParams* tp = new (std::nothrow) TopkParams();
+  HsiParams* hp = new (std::nothrow) HsiParams();
+  if (!ip || !tp || !hp) { delete ip; delete tp; delete hp; return CSA2_ERR_OOM; }
+  const uint16_t* qb = static_cast<const uint16_t*>(q_idx);
+  if (cudaMemsetAsync(key_hist, 0, (size_t)nq * kKeyHistBinsHost * 4, S(stream)) != cudaSuccess)
+    st = CSA2_ERR_CUDA;
+  for (int q0 = 0; q0 < nq && st == CSA2_OK; q0 += kMaxIdxGroups) {
+    const int n = std::min(kMaxIdxGroups, nq - q0);
+    // ---- the pool positions' scores (indexer in pool mode)
+    std::memset(ip, 0, sizeof(IndexParams));
+    ip->w = w + (int64_t)q0 * kIdxHeads;
+    ip->scores = pscores + (int64_t)q0 * slots;
+    ip->ld = slots;
+    ip->key_hist = key_hist + (int64_t)q0 * kKeyHistBinsHost;
+    ip->pool = pool_blocks + (int64_t)q0 * max_blocks;
+    ip->pool_blocks = max_blocks;
+    ip->err = c->d_err;
+    ip->nq = n;
+    ip->qpg = 1;
+    ip->n_groups = n;
+    ip->ratio = c->cfg.ratio;
+    ip->tile_prefix[0] = 0;
+    for (int i = 0; i < n; ++i) {
+      const int s = seq_ids ? seq_ids[q0 + i] : q0 + i;
+      ip->entry_base[i] = c->off[s];
+      ip->nvis[i] = (int32_t)c->len[s];
+      ip->tile_prefix[i + 1] = ip->tile_prefix[i] + max_blocks / 16;
+    }
+    CUtensorMap tm_q;
+    if (!make_map(&tm_q, qb + (int64_t)q0 * kIdxHeads * kIdxDim, (uint64_t)n * kIdxHeads,
+                  kIdxDim, 64, 32)) {
+      st = CSA2_ERR_CUDA;
+      break;
+    }
+    const int grid = std::min(c->num_sms, ip->tile_prefix[n]);
+    if (launch_index(*ip, c->tm_k8, tm_q, grid, S(stream)) != cudaSuccess) {
+      st = CSA2_ERR_CUDA;
+      break;
+    }
+    // ---- top-k over the pool slots (ties to the lower slot = lower entry)
+    std::memset(tp, 0, sizeof(TopkParams));
+    tp->scores = ip->scores;
+    tp->ld = slots;
+    tp->rows = n;
+    tp->k = k;
+    tp->idx_out = sel + (int64_t)q0 * k;
+    tp->score_out = topk_score ? topk_score + (int64_t)q0 * k : nullptr;
+    tp->key_hist = ip->key_hist;
+    tp->seg_ws = seg_ws + (size_t)q0 * topk_seg_bytes(1, slots) / sizeof(uint32_t);
+    tp->n_seg = topk_segments(slots);
+    tp->formula = 0;
+    for (int i = 0; i < n; ++i) tp->n_valid[i] = slots;
+    if (launch_topk(*tp, S(stream)) != cudaSuccess) { st = CSA2_ERR_CUDA; break; }
+    // ---- pool slots back to entry indices
+    std::memset(hp, 0, sizeof(HsiParams));
+    hp->rows = n;
+    hp->sel = tp->idx_out;
+    hp->k = k;
+    hp->pool = ip->pool;
+    hp->pool_blocks = max_blocks;
+    hp->out = topk_idx + (int64_t)q0 * k;
+    hp->score_out = tp->score_out;
+    for (int i = 0; i < n; ++i) hp->n[i] = ip->nvis[i];
+    if (launch_pool_map(*hp, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
+  }
+  delete ip;
+  delete tp;
+  delete hp;
   return st;
 }
 

@@ -54,6 +54,8 @@ struct IndexParams {
   float* scores;           // [nq, ld]
   int64_t ld;
   uint32_t* key_hist;      // nullable [nq, 2048] score-key histogram (qpg == 1 only)
+  const int32_t* pool;     // nullable: pool mode, [nq, pool_blocks] block ids (-1 unused)
+  int32_t pool_blocks;     // blocks per pool row (multiple of 16)
   uint32_t* err;
   int32_t nq;
   int32_t qpg;             // queries per group (1 decode, 8 prefill)
@@ -70,6 +72,30 @@ struct IndexParams {
 int index_smem_bytes(int qpg);
 cudaError_t launch_index(const IndexParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_q,
                          int grid, cudaStream_t s);
+
+// ---------------------------------------------------------------- HSI
+constexpr int kHsiBlock = 8;   // positions per block of the candidate pool
+struct HsiParams {
+  int32_t rows;              // <= kHsiTab
+  // block max: bmax[r, b] = max of scores[r, 8 b .. 8 b + 7] over the row's
+  // n[r] positions, for b < ceil(n[r] / 8)
+  const float* scores;
+  int64_t ld;
+  float* bmax;
+  int64_t ld_b;
+  // pool map: out[r, j] = pool[r, s / 8] * 8 + s % 8 for s = sel[r, j];
+  // -1 for unused slots and for entries >= n[r]
+  const int32_t* sel;
+  int32_t k;
+  const int32_t* pool;
+  int32_t pool_blocks;
+  int32_t* out;
+  float* score_out;          // nullable: zeroed where out is -1
+  int64_t n[1024];
+};
+constexpr int kHsiTab = 1024;
+cudaError_t launch_block_max(const HsiParams& p, cudaStream_t s);
+cudaError_t launch_pool_map(const HsiParams& p, cudaStream_t s);
 
 // ---------------------------------------------------------------- top-k
 constexpr int kTopkMaxRowsPerLaunch = 65535;

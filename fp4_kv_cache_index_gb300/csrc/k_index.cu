@@ -12,6 +12,11 @@
 // Decode uses qpg = 1 (each query reads its own sequence); prefill groups 8
 // consecutive queries of one sequence so that a K_I tile feeds 256 columns.
 //
+// Pool mode (Reindex layers of the Hierarchical Sparse Indexer, V4.1 report
+// section 2.3.2): a tile is 16 blocks of 8 consecutive keys named by the
+// query's candidate pool, gathered by 8-row TMA boxes into the same
+// swizzled layout; pool slots past the sequence score -inf.
+//
 // Persistent CTAs walk a balanced contiguous range of (group, tile) items.
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner),
 // warps 2-9 = epilogue (TMEM -> registers -> scores), two warps per TMEM lane
@@ -121,11 +126,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait(k_empty + stage, ph ^ 1, p.err);
       if (!ok) break;
       const int t = it - p.tile_prefix[g];
-      const int64_t row = group_base(p, g) + (int64_t)t * kTileE;
       uint8_t* dst = kbuf + stage * kKStageBytes;
-      mbar_arrive_expect_tx(k_full + stage, kKStageBytes);
-      tma_load_2d(dst, &tm_k, 0, (int32_t)row, k_full + stage);
-      tma_load_2d(dst + kKStageBytes / 2, &tm_k, 64, (int32_t)row, k_full + stage);
+      if (p.pool) {
+        const int32_t* prow = p.pool + (int64_t)g * p.pool_blocks + t * (kTileE / 8);
+        int32_t blk[kTileE / 8];
+        uint32_t n_ok = 0;
+#pragma unroll
+        for (int i = 0; i < kTileE / 8; ++i) {
+          blk[i] = __ldg(prow + i);
+          n_ok += blk[i] >= 0;
+        }
+        mbar_arrive_expect_tx(k_full + stage, n_ok * 8 * kIdxDim * 2);
+#pragma unroll
+        for (int i = 0; i < kTileE / 8; ++i)
+          if (blk[i] >= 0) {
+            const int32_t row = (int32_t)(group_base(p, g) + (int64_t)blk[i] * 8);
+            tma_load_2d(dst + i * 1024, &tm_k, 0, row, k_full + stage);
+            tma_load_2d(dst + kKStageBytes / 2 + i * 1024, &tm_k, 64, row, k_full + stage);
+          }
+      } else {
+        const int64_t row = group_base(p, g) + (int64_t)t * kTileE;
+        mbar_arrive_expect_tx(k_full + stage, kKStageBytes);
+        tma_load_2d(dst, &tm_k, 0, (int32_t)row, k_full + stage);
+        tma_load_2d(dst + kKStageBytes / 2, &tm_k, 64, (int32_t)row, k_full + stage);
+      }
       armed[stage] = ph + 1;
       if (++stage == kStages) { stage = 0; ph ^= 1; }
     }
@@ -217,7 +241,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < 32; ++h) s = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.0f), s);
         const int q = g * p.qpg + j;
-        if (q < p.nq && e < group_nvis_query(p, g, j)) {
+        if (p.pool) {
+          // slot t * 128 + row of the pool; its entry decides validity
+          const int32_t blk = __ldg(p.pool + (int64_t)g * p.pool_blocks + t * (kTileE / 8) + (row >> 3));
+          const int64_t ent = (int64_t)blk * 8 + (row & 7);
+          const float v = (blk >= 0 && ent < group_nvis_query(p, g, j)) ? s : -INFINITY;
+          p.scores[(int64_t)q * p.ld + e] = v;
+          if (use_hist) atomicAdd(hs + (score_key(v) >> 21), 1u);
+        } else if (q < p.nq && e < group_nvis_query(p, g, j)) {
           p.scores[(int64_t)q * p.ld + e] = s;
           if (use_hist) atomicAdd(hs + (score_key(s) >> 21), 1u);
         }

@@ -276,6 +276,47 @@ csa2_status_t csa2_index_scores_prefill(const csa2_cache_t* cache, int32_t seq,
                                         float* scores, int64_t ld,
                                         csa2_stream_t stream);
 
+/* ---- Hierarchical Sparse Indexer and Reindex mode ([V41 sec 2.3.2]) -----
+ * The first Full layer of the decoder also picks a candidate pool: every
+ * block of 8 consecutive entries gets the maximum of its entries' index
+ * scores, and the max_blocks blocks with the highest block scores are kept
+ * (ties to the lower block index); [V41 sec 4.2.1]: 2048 blocks x 8 =
+ * 16384 candidates.  A later Reindex layer scores only the pool with its
+ * own indexer query and selects its own top-k inside it.                  */
+
+/* Workspace bytes of csa2_hsi_pool. */
+size_t csa2_hsi_pool_workspace_bytes(int32_t n_rows, int64_t max_valid);
+
+/* Candidate pool from a Full layer's scores: row r has n_valid[r] scores at
+ * scores + r * ld (the scores csa2_index_scores_decode writes).
+ *   block: must be 8;  max_blocks: a multiple of 16, at most 4096;
+ *   pool_blocks: dev int32 [n_rows, max_blocks], the kept block indices in
+ *   ascending order, -1 padded;  n_valid: host int64 [n_rows].            */
+csa2_status_t csa2_hsi_pool(int32_t n_rows, const float* scores, int64_t ld,
+                            const int64_t* n_valid, int32_t block,
+                            int32_t max_blocks, int32_t* pool_blocks,
+                            void* workspace, size_t workspace_bytes,
+                            csa2_stream_t stream);
+
+/* Workspace bytes of csa2_index_topk_reindex_decode. */
+size_t csa2_index_reindex_workspace_bytes(const csa2_cache_t* cache,
+                                          int32_t n_queries, int32_t max_blocks);
+
+/* Reindex-mode selection for decode queries: the index score of [V4B sec
+ * 4.1] with this layer's q_idx / w, over the entries of the query's pool
+ * blocks only (blocks of 8, entries past the sequence excluded), then the
+ * top-k of those with ties to the lower entry, ascending, -1 padded.
+ *   pool_blocks: dev int32 [n_queries, max_blocks] from csa2_hsi_pool;
+ *   other arguments as for csa2_index_topk_decode.                          */
+csa2_status_t csa2_index_topk_reindex_decode(const csa2_cache_t* cache,
+                                             int32_t n_queries, const void* q_idx,
+                                             const float* w, const int32_t* seq_ids,
+                                             const int32_t* pool_blocks,
+                                             int32_t max_blocks, int32_t* topk_idx,
+                                             float* topk_score, void* workspace,
+                                             size_t workspace_bytes,
+                                             csa2_stream_t stream);
+
 /* Workspace bytes with which csa2_topk splits each row's candidate search
  * over several CTAs (used when key_hist is given), for n_rows rows of at
  * most max_valid scores.  A smaller workspace (or none) is allowed: the
