@@ -55,6 +55,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-hsi", action="store_true",
+                   help="skip the Hierarchical Sparse Indexer / Reindex measurement")
     p.add_argument("--no-graph", action="store_true",
                    help="time eager API calls instead of the captured CUDA graph")
     return p.parse_args(argv)
@@ -451,8 +453,13 @@ def run_csa2(args):
     e2e_elapsed_local = a.elapsed_time(b_) / 1000.0
     e2e_elapsed = max_over_ranks(e2e_elapsed_local, world, dev)
 
-    # ---- accounting
     hbm_peak, peak_kind = measured_peaks()
+    hsi = None
+    if not args.no_hsi:
+        hsi = measure_hsi(C, W, wl, cache, scores, n_valid, dev, stream,
+                          max(3, min(args.steps, 300)), hbm_peak)
+
+    # ---- accounting
     tot_ent = int(n_ent.sum())
     idx_bytes = tot_ent * 256 + B * (32 * 128 * 2 + 32 * 4)
     entry_bytes = 256 + (16 if args.layout == 0 else 32)
@@ -489,6 +496,7 @@ def run_csa2(args):
                 "pipelining": "inputs of step i+1 and outputs of step i-1 copied on a "
                               "second stream while step i computes (pinned host buffers)"},
         "gpu_launches": launches_per_step * args.steps,
+        "hsi_reindex": hsi,
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -499,6 +507,79 @@ def run_csa2(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def measure_hsi(C, W, wl, cache, scores, n_valid, dev, stream, iters, hbm_peak,
+                max_blocks=2048):
+    """Hierarchical Sparse Indexer on the same batch: the candidate pool from
+    the Full layer's scores (block maxima + top-2048 blocks), then one
+    Reindex layer's selection (its own indexer query over the 16,384 pool
+    positions, top-512).  Timed as a CUDA graph replay (both calls) and per
+    call with events; not part of the headline step, which is the configured
+    Full + Reuse group."""
+    import torch
+    B = wl.batch
+    pool = torch.empty(B, max_blocks, dtype=torch.int32, device=dev)
+    pool_ws = torch.empty(max(16, int(C.lib.csa2_hsi_pool_workspace_bytes(B, max(n_valid)))),
+                          dtype=torch.uint8, device=dev)
+    re_ws = torch.empty(max(16, int(C.lib.csa2_index_reindex_workspace_bytes(
+        cache.handle, B, max_blocks))), dtype=torch.uint8, device=dev)
+    q2 = W.dev_q_idx(wl, layer=1)
+    w2 = W.dev_w(wl, layer=1)
+    re_idx = torch.empty(B, 512, dtype=torch.int32, device=dev)
+
+    def run(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        C.csa2_hsi_pool(scores, n_valid, max_blocks, pool_blocks=pool, workspace=pool_ws)
+        if ev is not None:
+            ev[1].record(stream)
+        C.csa2_index_topk_reindex_decode(cache, q2, w2, pool, topk_idx=re_idx, workspace=re_ws)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        run()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for _ in range(3):
+        g.replay()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(iters):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = a.elapsed_time(b) / iters
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(iters)]
+    for i in range(iters):
+        run(evs[i])
+    torch.cuda.synchronize()
+    t_pool = sum(e[0].elapsed_time(e[1]) for e in evs) / iters
+    t_re = sum(e[1].elapsed_time(e[2]) for e in evs) / iters
+    if cache.device_error() != 0:
+        raise RuntimeError("device error word set during the HSI measurement")
+    slots = max_blocks * 8
+    pool_bytes = sum(n_valid) * 4                       # block maxima read the Full scores
+    re_bytes = B * (slots * 256 + 32 * 128 * 2 + 32 * 4)  # pool keys + query + weights
+    return {"max_blocks": max_blocks, "block": 8, "pool_positions": slots,
+            "graph_ms": graph_ms, "pool_ms": t_pool, "reindex_ms": t_re,
+            "reindex_qtok_s": B / (t_re / 1000),
+            "pool_algorithmic_bytes": pool_bytes, "reindex_algorithmic_bytes": re_bytes,
+            "reindex_hbm_gbs": re_bytes / (t_re / 1000) / 1e9,
+            "reindex_hbm_frac": re_bytes / (t_re / 1000) / 1e9 / hbm_peak,
+            "launches": "pool: block max + top-k; reindex: pool-mode indexer + top-k "
+                        "segments + top-k + slot map"}
 
 
 def run_prefill(args):

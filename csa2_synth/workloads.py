@@ -96,14 +96,16 @@ class Workload:
         return normal_bf16(stream_key(self.seed, S_IDXK, seq), first * IDX_DIM,
                            n * IDX_DIM).reshape(n, IDX_DIM)
 
-    def q_idx(self, first: int = 0, n: Optional[int] = None) -> np.ndarray:
+    def q_idx(self, first: int = 0, n: Optional[int] = None, layer: int = 0) -> np.ndarray:
+        """Indexer queries; layer 0 is the Full layer, layer i > 0 the i-th
+        Reindex layer (its own indexer query and weights)."""
         n = self.n_queries() - first if n is None else n
-        return normal_bf16(stream_key(self.seed, S_QIDX, 0), first * IDX_HEADS * IDX_DIM,
+        return normal_bf16(stream_key(self.seed, S_QIDX, layer), first * IDX_HEADS * IDX_DIM,
                            n * IDX_HEADS * IDX_DIM).reshape(n, IDX_HEADS, IDX_DIM)
 
-    def w(self, first: int = 0, n: Optional[int] = None) -> np.ndarray:
+    def w(self, first: int = 0, n: Optional[int] = None, layer: int = 0) -> np.ndarray:
         n = self.n_queries() - first if n is None else n
-        return normal_f32(stream_key(self.seed, S_W, 0), first * IDX_HEADS,
+        return normal_f32(stream_key(self.seed, S_W, layer), first * IDX_HEADS,
                           n * IDX_HEADS).reshape(n, IDX_HEADS)
 
     def q(self, layer: int, first: int = 0, n: Optional[int] = None) -> np.ndarray:
@@ -183,19 +185,19 @@ def dev_idx_k(wl: Workload, seq: int, first: int, n: int):
                        first * IDX_DIM)
 
 
-def dev_q_idx(wl: Workload, first: int = 0, n: Optional[int] = None):
+def dev_q_idx(wl: Workload, first: int = 0, n: Optional[int] = None, layer: int = 0):
     import torch
     from . import device_fill
     n = wl.n_queries() - first if n is None else n
     return device_fill(_dev((n, IDX_HEADS, IDX_DIM), torch.bfloat16),
-                       stream_key(wl.seed, S_QIDX, 0), first * IDX_HEADS * IDX_DIM)
+                       stream_key(wl.seed, S_QIDX, layer), first * IDX_HEADS * IDX_DIM)
 
 
-def dev_w(wl: Workload, first: int = 0, n: Optional[int] = None):
+def dev_w(wl: Workload, first: int = 0, n: Optional[int] = None, layer: int = 0):
     import torch
     from . import device_fill
     n = wl.n_queries() - first if n is None else n
-    return device_fill(_dev((n, IDX_HEADS), torch.float32), stream_key(wl.seed, S_W, 0),
+    return device_fill(_dev((n, IDX_HEADS), torch.float32), stream_key(wl.seed, S_W, layer),
                        first * IDX_HEADS)
 
 

@@ -32,7 +32,7 @@ struct csa2_cache {
   uint8_t* scales;
   uint16_t* idxk;
   CUtensorMap tm_k;    // indexer keys, 128-row boxes (contiguous tiles)
-  CUtensorMap tm_k8;   // indexer keys, 8-row boxes (pool blocks)
+  CUtensorMap tm_k8;   // indexer keys, one 8-key block per box (pool mode)
   int num_sms;
 };
 
@@ -111,6 +111,22 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Indexer keys [rows, 128] bf16 seen as (64 columns, rows, 2 halves): one
+// box of (64, 8, 2) is a whole block of 8 keys, landing in shared memory as
+// two 1 KB 128B-swizzled atoms (columns 0-63, then 64-127).
+bool make_block_map(CUtensorMap* m, const void* base, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows == 0) return false;
+  cuuint64_t gdim[3] = {64, rows, 2};
+  cuuint64_t gstride[2] = {kIdxDim * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)kHsiBlock, 2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstride, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -265,7 +281,7 @@ csa2_status_t csa2_cache_create(const csa2_config_t* cfg, int32_t batch, const i
     return CSA2_ERR_CUDA;
   }
   if (!make_map(&c->tm_k, c->idxk, (uint64_t)c->total, kIdxDim, 64, 128) ||
-      !make_map(&c->tm_k8, c->idxk, (uint64_t)c->total, kIdxDim, 64, kHsiBlock)) {
+      !make_block_map(&c->tm_k8, c->idxk, (uint64_t)c->total)) {
     delete c;
     return CSA2_ERR_CUDA;
   }

@@ -14,11 +14,13 @@
 //
 // Pool mode (Reindex layers of the Hierarchical Sparse Indexer, V4.1 report
 // section 2.3.2): a tile is 16 blocks of 8 consecutive keys named by the
-// query's candidate pool, gathered by 8-row TMA boxes into the same
-// swizzled layout; pool slots past the sequence score -inf.
+// query's candidate pool, one 3-D TMA box per block (2 KB: its two 1 KB
+// swizzled column halves), so the MMA walks 8-row atoms 2 KB apart; pool
+// slots past the sequence score -inf.  Block ids of the next tile are loaded
+// one tile ahead by the producer and by the epilogue.
 //
 // Persistent CTAs walk a balanced contiguous range of (group, tile) items.
-// Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner),
+// Warp roles: warp 0 = TMA producer (lane 0; lanes 0-15 in pool mode), warp 1 = MMA issuer (and TMEM owner),
 // warps 2-9 = epilogue (TMEM -> registers -> scores), two warps per TMEM lane
 // quadrant splitting the queries of a group.  Every wait is bounded.
 #include "csa2_device.cuh"
@@ -105,58 +107,68 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int end = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
   int g0 = 0;
   while (g0 < p.n_groups && p.tile_prefix[g0 + 1] <= begin) ++g0;
+  // pool row of item `it` (whose group is at or after `g`)
+  auto pool_row = [&](int it, int g) -> const int32_t* {
+    while (p.tile_prefix[g + 1] <= it) ++g;
+    return p.pool + (int64_t)g * p.pool_blocks + (it - p.tile_prefix[g]) * (kTileE / 8);
+  };
 
-  if (warp == 0 && lane == 0 && begin < end) {
-    // ------------------------------------------------ TMA producer
+  if (warp == 0 && begin < end) {
+    // ------------------------------------------------ TMA producer (warp 0)
+    // Lane 0 owns the barriers; in pool mode lanes 0-15 each copy one block.
     int g = g0, cur = -1, stage = 0;
     uint32_t ph = 0, qph = 0;
-    uint32_t armed[kStages] = {0, 0, 0, 0};   // phase parity of each stage's last fill + 1
+    uint32_t armed = 0, armed_ph = 0;   // stages filled at least once, parity of the last fill
     bool ok = true;
+    const bool pool_lane = p.pool != nullptr && lane < kTileE / 8;
+    int32_t nxt = pool_lane ? __ldg(pool_row(begin, g0) + lane) : -1;
     for (int it = begin; it < end && ok; ++it) {
       while (p.tile_prefix[g + 1] <= it) ++g;
       if (g != cur) {
-        ok = mbar_wait(q_empty, qph ^ 1, p.err);
+        if (lane == 0) {
+          ok = mbar_wait(q_empty, qph ^ 1, p.err);
+          if (ok) {
+            mbar_arrive_expect_tx(q_full, (uint32_t)(qrows * kIdxDim * 2));
+            tma_load_2d(qbuf, &tm_q, 0, g * qrows, q_full);
+            tma_load_2d(qbuf + qrows * 128, &tm_q, 64, g * qrows, q_full);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
         qph ^= 1;
         if (!ok) break;
-        mbar_arrive_expect_tx(q_full, (uint32_t)(qrows * kIdxDim * 2));
-        tma_load_2d(qbuf, &tm_q, 0, g * qrows, q_full);
-        tma_load_2d(qbuf + qrows * 128, &tm_q, 64, g * qrows, q_full);
         cur = g;
       }
-      ok = mbar_wait(k_empty + stage, ph ^ 1, p.err);
+      if (lane == 0) ok = mbar_wait(k_empty + stage, ph ^ 1, p.err);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      const int t = it - p.tile_prefix[g];
       uint8_t* dst = kbuf + stage * kKStageBytes;
       if (p.pool) {
-        const int32_t* prow = p.pool + (int64_t)g * p.pool_blocks + t * (kTileE / 8);
-        int32_t blk[kTileE / 8];
-        uint32_t n_ok = 0;
-#pragma unroll
-        for (int i = 0; i < kTileE / 8; ++i) {
-          blk[i] = __ldg(prow + i);
-          n_ok += blk[i] >= 0;
+        const int32_t blk = nxt;
+        if (pool_lane && it + 1 < end) nxt = __ldg(pool_row(it + 1, g) + lane);
+        const uint32_t n_ok = (uint32_t)__popc(__ballot_sync(0xffffffffu, blk >= 0));
+        if (lane == 0) mbar_arrive_expect_tx(k_full + stage, n_ok * 8 * kIdxDim * 2);
+        __syncwarp();
+        if (blk >= 0) {
+          const int32_t row = (int32_t)(group_base(p, g) + (int64_t)blk * 8);
+          tma_load_3d(dst + lane * 2048, &tm_k, 0, row, 0, k_full + stage);
         }
-        mbar_arrive_expect_tx(k_full + stage, n_ok * 8 * kIdxDim * 2);
-#pragma unroll
-        for (int i = 0; i < kTileE / 8; ++i)
-          if (blk[i] >= 0) {
-            const int32_t row = (int32_t)(group_base(p, g) + (int64_t)blk[i] * 8);
-            tma_load_2d(dst + i * 1024, &tm_k, 0, row, k_full + stage);
-            tma_load_2d(dst + kKStageBytes / 2 + i * 1024, &tm_k, 64, row, k_full + stage);
-          }
-      } else {
-        const int64_t row = group_base(p, g) + (int64_t)t * kTileE;
+      } else if (lane == 0) {
+        const int64_t row = group_base(p, g) + (int64_t)(it - p.tile_prefix[g]) * kTileE;
         mbar_arrive_expect_tx(k_full + stage, kKStageBytes);
         tma_load_2d(dst, &tm_k, 0, (int32_t)row, k_full + stage);
         tma_load_2d(dst + kKStageBytes / 2, &tm_k, 64, (int32_t)row, k_full + stage);
       }
-      armed[stage] = ph + 1;
+      armed |= 1u << stage;
+      armed_ph = (armed_ph & ~(1u << stage)) | (ph << stage);
       if (++stage == kStages) { stage = 0; ph ^= 1; }
     }
     // make sure no bulk copy is still writing into this CTA's shared memory
-    for (int s = 0; s < kStages; ++s)
-      if (armed[s]) mbar_wait(k_full + s, armed[s] - 1, p.err);
-    if (cur >= 0) mbar_wait(q_full, qph ^ 1, p.err);
+    if (lane == 0) {
+      for (int s = 0; s < kStages; ++s)
+        if (armed & (1u << s)) mbar_wait(k_full + s, (armed_ph >> s) & 1u, p.err);
+      if (cur >= 0) mbar_wait(q_full, qph ^ 1, p.err);
+    }
+    __syncwarp();
   } else if (warp == 1 && lane == 0 && begin < end) {
     // ------------------------------------------------ MMA issuer
     const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)N, false, false);
@@ -177,11 +189,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t a0 = smem_u32(kbuf + stage * kKStageBytes);
       const uint32_t b0 = smem_u32(qbuf);
       const uint32_t d = tmem_base + (uint32_t)(acc * N);
+      // contiguous tiles: column halves 16 KB apart, 8-row atoms 1 KB apart;
+      // pool tiles: halves 1 KB apart inside each block's 2 KB
+      const uint32_t a_half = p.pool ? 1024u : (uint32_t)(kKStageBytes / 2);
+      const uint32_t a_sbo = p.pool ? 2048u : 1024u;
 #pragma unroll
       for (int ks = 0; ks < kIdxDim / 16; ++ks) {
-        const uint32_t ao = (uint32_t)((ks >> 2) * (kKStageBytes / 2) + (ks & 3) * 32);
+        const uint32_t ao = (uint32_t)(ks >> 2) * a_half + (uint32_t)(ks & 3) * 32u;
         const uint32_t bo = (uint32_t)((ks >> 2) * (qrows * 128) + (ks & 3) * 32);
-        umma_bf16(d, sdesc_sw128(a0 + ao, 16, 1024), sdesc_sw128(b0 + bo, 16, 1024), idesc,
+        umma_bf16(d, sdesc_sw128(a0 + ao, 16, a_sbo), sdesc_sw128(b0 + bo, 16, 1024), idesc,
                   ks > 0 ? 1u : 0u);
       }
       umma_commit(k_empty + stage);
@@ -217,8 +233,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int g = g0, cur = -1, acc = 0;
     uint32_t aph = 0;
+    int32_t blk_nxt = (p.pool && begin < end) ? __ldg(pool_row(begin, g0) + (row >> 3)) : -1;
     for (int it = begin; it < end; ++it) {
       while (p.tile_prefix[g + 1] <= it) ++g;
+      const int32_t blk = blk_nxt;
+      if (p.pool && it + 1 < end) blk_nxt = __ldg(pool_row(it + 1, g) + (row >> 3));
       if (g != cur) {
         if (use_hist && cur >= 0) flush(cur);
         asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -243,7 +262,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = g * p.qpg + j;
         if (p.pool) {
           // slot t * 128 + row of the pool; its entry decides validity
-          const int32_t blk = __ldg(p.pool + (int64_t)g * p.pool_blocks + t * (kTileE / 8) + (row >> 3));
           const int64_t ent = (int64_t)blk * 8 + (row & 7);
           const float v = (blk >= 0 && ent < group_nvis_query(p, g, j)) ? s : -INFINITY;
           p.scores[(int64_t)q * p.ld + e] = v;
