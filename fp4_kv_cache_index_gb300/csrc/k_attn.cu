@@ -25,8 +25,8 @@
 // serves as the K-major A of the first product and the MN-major A of the
 // second.  Online softmax (base 2) runs across TMEM lanes: each thread holds
 // one candidate row, per-head maxima and sums use a warp reduce-scatter and a
-// 4-way combine through shared memory; O^T is rescaled in TMEM when a
-// head's running maximum grows.
+// 4-way combine through shared memory; O^T is rescaled in TMEM only when a
+// head's running maximum grows by more than 2^8.
 #include "csa2_device.cuh"
 #include "csa2_kernels.h"
 
@@ -37,6 +37,7 @@ constexpr int kThreads = 512;     // 16 warps
 constexpr int kHG = 64;               // heads per CTA
 constexpr int kRows = 128;            // candidates per tile
 constexpr int kMaxTiles = 2048 / kRows + 1;
+constexpr float kLazyRescale = 8.0f;  // log2 units
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kKvOff = 0;                              // 8 x [128 x 128 B]
@@ -327,14 +328,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     if (tid < kHG) {
+      // The running maximum of a head moves only when a tile's maximum
+      // exceeds it by more than 2^8: O, l and the probabilities all refer to
+      // the same m (exact), probabilities stay below 256, and the O^T rescale
+      // in TMEM is skipped for most tiles.
       const float tmax = fmaxf(fmaxf(sm.red_max[0][tid], sm.red_max[1][tid]),
                                fmaxf(sm.red_max[2][tid], sm.red_max[3][tid]));
       const float mo = sm.m[tid];
-      const float mn = fmaxf(mo, tmax);
-      const float a = (mn == -INFINITY) ? 1.0f : fast_exp2(mo - mn);
-      sm.m[tid] = mn;
+      float a = 1.0f;
+      if (tmax > mo + kLazyRescale) {
+        a = (mo == -INFINITY) ? 0.0f : fast_exp2(mo - tmax);
+        sm.m[tid] = tmax;
+        if (ti > 0) sm.need_rescale = 1;
+      }
       sm.alpha[tid] = a;
-      if (a != 1.0f && ti > 0) sm.need_rescale = 1;
     }
     __syncthreads();
     {

@@ -161,3 +161,82 @@ def test_split_and_single_cta_paths_agree_with_oracle(C, n_q):
             check_attn(o[i], ref)
             assert np.allclose(l[i], rl, atol=1e-3, rtol=0)
     assert cache.device_error() == 0
+
+
+
+def _aligned_cache(C, gains, seed=53):
+    """4096 entries in four ranges of 1024; range j is N(0, 1/16) noise plus
+    gains[j] / 2 times the query of head (s mod 64), so that head's logits in
+    the top-k tile drawn from range j grow with gains[j] (read with twice
+    the usual softmax scale, values stay below about 2 in magnitude)."""
+    n = 4096
+    q = S.normal_bf16(S.stream_key(seed + 2, S.S_Q, 0), 0, 64 * 512).reshape(64, 512)
+    qf = S.bf16_bits_to_f32(q)
+    e = S.normal_f32(S.stream_key(seed, S.S_ENTRIES, 0), 0, n * 512).reshape(n, 512)
+    for j, gain in enumerate(gains):
+        rows = np.arange(j * 1024, (j + 1) * 1024)
+        e[rows] = e[rows] * np.float32(0.25) + np.float32(gain / 2) * qf[rows % 64]
+    cache = C.Cache(C.config(), [n])
+    k = S.normal_bf16(S.stream_key(seed, S.S_IDXK, 0), 0, n * 128).reshape(n, 128)
+    C.csa2_append_entries(cache, [0], [n], f32_dev(e), bf16_dev(k))
+    rng = np.random.default_rng(seed + 1)
+    idx = np.concatenate([np.sort(rng.choice(1024, 128, replace=False)) + 1024 * j
+                          for j in range(4)]).astype(np.int32)[None]
+    swa = S.normal_bf16(S.stream_key(seed + 2, S.S_SWA, 0), 0, 128 * 512).reshape(1, 128, 512)
+    return cache, e, q[None], swa, idx
+
+
+@pytest.mark.parametrize("gains", [(0.0, 0.2, 0.35, 1.0), (1.0, 0.35, 0.2, 0.0)])
+def test_running_max_moves_and_stays(C, gains):
+    """Each head's logits jump tile after tile (its running maximum moves by
+    more than 2^8 at the fully aligned tile and by less at the partly aligned
+    ones), or jump once and fall back: the split and single-CTA paths both
+    match the oracle."""
+    import torch
+    cache, e, q, swa, idx = _aligned_cache(C, gains)
+    scale = np.float32(2 * SCALE)
+    codes, scales = O.quantise(e, 0)
+    _, ref, rl = O.sparse_attention(q[0], codes, scales, 0, idx[0], swa[0], scale)
+    for ws in (None, torch.empty(0, dtype=torch.uint8, device="cuda")):
+        lse = torch.zeros(1, 64, device="cuda")
+        out = C.csa2_sparse_attn_decode(cache, bf16_dev(q), bf16_dev(swa),
+                                        torch.from_numpy(idx).cuda(), float(scale), lse=lse,
+                                        workspace=ws)
+        check_attn(bf16_host(out)[0], ref)
+        assert np.allclose(lse.cpu().numpy()[0], rl, atol=1e-3 * max(1.0, np.abs(rl).max()),
+                           rtol=0)
+    assert cache.device_error() == 0
+
+
+def test_large_values_stay_within_the_probability_rounding_bound(C):
+    """Entries eight times larger everywhere: the probabilities that weight
+    the values are rounded to bf16 for the tensor cores (relative error at
+    most 2^-9, twice over when the running maximum is not the final one), so
+    where large values cancel, an output's error scales with sum_j p_j |kv_j|
+    rather than with |o|.  The bound derived from that arithmetic,
+    2^-8 (sum_j p_j |kv_j| + |o|), holds element by element."""
+    import torch
+    n = 4096
+    cache = C.Cache(C.config(), [n])
+    e = S.normal_f32(S.stream_key(53, S.S_ENTRIES, 0), 0, n * 512).reshape(n, 512) * 8
+    k = S.normal_bf16(S.stream_key(53, S.S_IDXK, 0), 0, n * 128).reshape(n, 128)
+    C.csa2_append_entries(cache, [0], [n], f32_dev(e), bf16_dev(k))
+    rng = np.random.default_rng(54)
+    idx = np.concatenate([np.sort(rng.choice(1024, 128, replace=False)) + 1024 * j
+                          for j in range(4)]).astype(np.int32)[None]
+    q = S.normal_bf16(S.stream_key(55, S.S_Q, 0), 0, 64 * 512).reshape(1, 64, 512)
+    swa = S.normal_bf16(S.stream_key(55, S.S_SWA, 0), 0, 128 * 512).reshape(1, 128, 512)
+    codes, scales = O.quantise(e, 0)
+    _, ref, _ = O.sparse_attention(q[0], codes, scales, 0, idx[0], swa[0], SCALE)
+    kv = np.concatenate([S.bf16_bits_to_f32(swa[0]).astype(np.float64),
+                         O.dequantise(codes, scales, 0)[idx[0]].astype(np.float64)])
+    logit = (S.bf16_bits_to_f32(q[0]).astype(np.float64) @ kv.T) * float(SCALE)
+    pw = np.exp(logit - logit.max(1, keepdims=True))
+    pw /= pw.sum(1, keepdims=True)
+    bound = 2.0 ** -8 * (pw @ np.abs(kv) + np.abs(ref))
+    for ws in (None, torch.empty(0, dtype=torch.uint8, device="cuda")):
+        out = C.csa2_sparse_attn_decode(cache, bf16_dev(q), bf16_dev(swa),
+                                        torch.from_numpy(idx).cuda(), float(SCALE), workspace=ws)
+        g = S.bf16_bits_to_f32(bf16_host(out)[0]).astype(np.float64)
+        assert np.all(np.abs(g - ref) <= bound), float((np.abs(g - ref) / bound).max())
+    assert cache.device_error() == 0
