@@ -75,6 +75,8 @@ def lib():
                 "orc_compress": ([i64, i32, i32, P, P, P], None),
                 "orc_index_scores": ([i64, i32, i32, P, P, P, P], None),
                 "orc_topk": ([i64, P, i32, P], i32),
+                "orc_bf16_round": ([f32], f32),
+                "orc_bf16_round_n": ([i64, P, P], None),
                 "orc_sparse_attention": ([i32, i32, i32, P, P, P, i64, i32, P, i32, P,
                                           f32, P, P, P], None),
             }
@@ -195,6 +197,14 @@ def topk(scores_f32: np.ndarray, k: int) -> np.ndarray:
     return out
 
 
+def bf16_round(x) -> np.ndarray:
+    """fp32 -> nearest bf16 value (ties to even), returned as fp32."""
+    a = _c(np.atleast_1d(x), np.float32)
+    out = np.zeros_like(a)
+    lib().orc_bf16_round_n(a.size, _p(a), _p(out))
+    return out.reshape(np.shape(x))
+
+
 # ---------------------------------------------------------------- attention
 def sparse_attention(q_bf16, codes, scales, layout, idx, swa_bf16, scale):
     """One query: q [heads, dim] over the selected entries (idx, -1 skipped)
@@ -232,6 +242,28 @@ def index_topk(k_bf16, q_bf16, w, k, n_vis=None):
     n_vis = k_bf16.shape[0] if n_vis is None else n_vis
     sc = index_scores(k_bf16[:n_vis], q_bf16, w)
     return topk(sc.astype(np.float32), k), sc
+
+
+def index_topk_bf16(k_bf16, q_bf16, w, k, n_vis=None):
+    """Selection on bf16-rounded scores ("DeepSeek-V4" blog reading, section
+    7): fp64 scores -> fp32 -> bf16, then the top-k with ties (now frequent)
+    to the lower index.  Returns (idx [k], bf16 scores as fp32 [n_vis],
+    fp64 scores [n_vis])."""
+    n_vis = k_bf16.shape[0] if n_vis is None else n_vis
+    sc = index_scores(k_bf16[:n_vis], q_bf16, w)
+    b = bf16_round(sc.astype(np.float32))
+    return topk(b, k), b, sc
+
+
+def recall(selected, reference) -> float:
+    """Fraction of the reference selection (valid indices) that `selected`
+    also holds."""
+    r = np.asarray(reference)
+    r = r[r >= 0]
+    if len(r) == 0:
+        return 1.0
+    s = np.asarray(selected)
+    return float(np.isin(r, s[s >= 0]).sum()) / len(r)
 
 
 def swa_rows(pos: int, window: int, row0_pos: int = 0):

@@ -269,6 +269,31 @@ static int cmp_int(const void* a, const void* b) {
   return (x > y) - (x < y);
 }
 
+/* bf16 rounding of index scores [V4B sec 7: the scores are quantised from
+ * FP32 to BF16 for the selector]: the nearest value whose low 16 fp32 bits
+ * are zero, found by comparing the two neighbours' distances in double; an
+ * exact tie goes to the neighbour whose last kept bit is 0 (IEEE
+ * round-to-nearest-even on the 8-bit significand).  Finite inputs.          */
+float orc_bf16_round(float x) {
+  if (x != x || isinf(x)) return x;
+  uint32_t b;
+  memcpy(&b, &x, 4);
+  const uint32_t lo_b = b & 0xFFFF0000u;    /* toward zero */
+  if (lo_b == b) return x;
+  const uint32_t hi_b = lo_b + 0x10000u;    /* away from zero */
+  float lo, hi;
+  memcpy(&lo, &lo_b, 4);
+  memcpy(&hi, &hi_b, 4);
+  const double dl = fabs((double)x - (double)lo), dh = fabs((double)hi - (double)x);
+  if (dl < dh) return lo;
+  if (dh < dl) return hi;
+  return ((lo_b >> 16) & 1u) ? hi : lo;
+}
+
+void orc_bf16_round_n(int64_t n, const float* in, float* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_round(in[i]);
+}
+
 /* Top-k [V4B sec 4.1, V41 sec 4.2.1: k = 512]: full sort by (score desc,
  * index asc); keep min(k, n); report them in ascending index order, pad -1.  */
 int orc_topk(int64_t n, const float* scores, int k, int32_t* idx_out) {

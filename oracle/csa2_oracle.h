@@ -60,6 +60,8 @@ void   orc_compress(int64_t n_out, int m, int dim, const uint16_t* c_bf16,
 /* ---- indexer and top-k  [V4B sec 4.1 index score], [V41 sec 4.2.1] ------- */
 void   orc_index_scores(int64_t n, int heads, int d, const uint16_t* k_bf16,
                         const uint16_t* q_bf16, const float* w, double* out);
+float  orc_bf16_round(float x);
+void   orc_bf16_round_n(int64_t n, const float* in, float* out);
 int    orc_topk(int64_t n, const float* scores, int k, int32_t* idx_out);
 
 /* ---- sparse shared-KV attention with SWA  [V4B sec 4.1/4.3], [NDT 3.3.1] - */
