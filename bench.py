@@ -55,6 +55,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-bf16-scores", action="store_true",
+                   help="skip the bf16-rounded index score measurement")
     p.add_argument("--no-hsi", action="store_true",
                    help="skip the Hierarchical Sparse Indexer / Reindex measurement")
     p.add_argument("--no-graph", action="store_true",
@@ -454,6 +456,11 @@ def run_csa2(args):
     e2e_elapsed = max_over_ranks(e2e_elapsed_local, world, dev)
 
     hbm_peak, peak_kind = measured_peaks()
+    bf16 = None
+    if not args.no_bf16_scores:
+        bf16 = measure_bf16_scores(C, cache, wl, bufs[0]["q_idx"], bufs[0]["w"], n_valid,
+                                   bufs[0]["topk"], key_hist, topk_ws, dev, stream,
+                                   max(3, min(args.steps, 300)), t_idx, t_topk)
     hsi = None
     if not args.no_hsi:
         hsi = measure_hsi(C, W, wl, cache, scores, n_valid, dev, stream,
@@ -497,6 +504,7 @@ def run_csa2(args):
                               "second stream while step i computes (pinned host buffers)"},
         "gpu_launches": launches_per_step * args.steps,
         "hsi_reindex": hsi,
+        "bf16_scores": bf16,
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -507,6 +515,54 @@ def run_csa2(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def measure_bf16_scores(C, cache, wl, q_idx, w, n_valid, fp32_idx, key_hist, topk_ws, dev,
+                        stream, iters, t_idx32, t_topk32):
+    """The Full layer's selection on bf16-rounded scores (the V4 blog
+    reading's section 7): index scores stored as bf16, top-k over them.
+    Reports its time next to the fp32 selection's, and the recall of the
+    fp32 selection (the step's own top-k of the last timed step)."""
+    import torch
+    B = wl.batch
+    ld = (max(n_valid) + 7) // 8 * 8
+    s16 = torch.empty(B, ld, dtype=torch.bfloat16, device=dev)
+    idx16 = torch.empty(B, 512, dtype=torch.int32, device=dev)
+
+    def run(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        C.csa2_index_scores_decode_bf16(cache, q_idx, w, s16, key_hist=key_hist)
+        if ev is not None:
+            ev[1].record(stream)
+        C.csa2_topk_bf16(s16, n_valid, 512, idx_out=idx16, key_hist=key_hist, workspace=topk_ws)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(iters)]
+    for i in range(iters):
+        run(evs[i])
+    torch.cuda.synchronize()
+    t_idx = sum(e[0].elapsed_time(e[1]) for e in evs) / iters
+    t_topk = sum(e[1].elapsed_time(e[2]) for e in evs) / iters
+    # recall of the fp32 selection, per query (both lists ascending, -1 padded)
+    a = fp32_idx.long()
+    b = idx16.long()
+    hit = torch.zeros(B, device=dev)
+    for r in range(B):
+        ar = a[r][a[r] >= 0]
+        br = b[r][b[r] >= 0]
+        hit[r] = torch.isin(ar, br).float().mean() if ar.numel() else 1.0
+    if cache.device_error() != 0:
+        raise RuntimeError("device error word set during the bf16-score measurement")
+    return {"index_ms": t_idx, "topk_ms": t_topk,
+            "fp32_index_ms": 1000 * t_idx32, "fp32_topk_ms": 1000 * t_topk32,
+            "topk_speedup": (1000 * t_topk32) / t_topk if t_topk > 0 else None,
+            "recall_mean": float(hit.mean()), "recall_min": float(hit.min()),
+            "recall_of": "the fp32 top-512 of the same scores (seeded N(0,1) inputs)"}
 
 
 def measure_hsi(C, W, wl, cache, scores, n_valid, dev, stream, iters, hbm_peak,

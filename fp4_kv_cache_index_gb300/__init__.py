@@ -80,6 +80,9 @@ def _load():
         "csa2_index_topk_prefill": ([P, i32, i32, i64, P, P, P, P, P, sz, P], i32),
         "csa2_index_topk_decode_static": ([P, i32, P, P, P, P, P, P], i32),
         "csa2_index_scores_prefill": ([P, i32, i32, i64, P, P, P, i64, P], i32),
+        "csa2_index_scores_decode_bf16": ([P, i32, P, P, P, P, i64, P, P], i32),
+        "csa2_topk_bf16": ([i32, P, i64, P, i32, P, P, P, P, sz, P], i32),
+        "csa2_index_topk_decode_bf16": ([P, i32, P, P, P, P, P, P, sz, P], i32),
         "csa2_hsi_pool_workspace_bytes": ([i32, i64], sz),
         "csa2_hsi_pool": ([i32, P, i64, P, i32, i32, P, P, sz, P], i32),
         "csa2_index_reindex_workspace_bytes": ([P, i32, i32], sz),
@@ -391,4 +394,52 @@ def csa2_index_topk_reindex_decode(cache: Cache, q_idx: torch.Tensor, w: torch.T
                                               workspace.numel() * workspace.element_size(),
                                               _stream(stream)),
            "csa2_index_topk_reindex_decode")
+    return topk_idx
+
+
+# ------------------------------------------------------------------ bf16-rounded scores
+def csa2_index_scores_decode_bf16(cache: Cache, q_idx: torch.Tensor, w: torch.Tensor,
+                                  scores: torch.Tensor, seq_ids: Optional[Sequence[int]] = None,
+                                  key_hist: Optional[torch.Tensor] = None,
+                                  stream=None) -> torch.Tensor:
+    """scores: bf16 (or int16) [n_queries, ld], ld a multiple of 8."""
+    _check(lib.csa2_index_scores_decode_bf16(cache.handle, q_idx.shape[0], _ptr(q_idx), _ptr(w),
+                                             _i32_array(seq_ids), _ptr(scores), scores.shape[1],
+                                             _ptr(key_hist), _stream(stream)),
+           "csa2_index_scores_decode_bf16")
+    return scores
+
+
+def csa2_topk_bf16(scores: torch.Tensor, n_valid: Sequence[int], k: int,
+                   idx_out: Optional[torch.Tensor] = None,
+                   score_out: Optional[torch.Tensor] = None,
+                   key_hist: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    rows, ld = scores.shape
+    if idx_out is None:
+        idx_out = torch.empty(rows, k, dtype=torch.int32, device=scores.device)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.csa2_topk_bf16(rows, _ptr(scores), ld, _i64_array(n_valid), k, _ptr(key_hist),
+                              _ptr(idx_out), _ptr(score_out), _ptr(workspace), nbytes,
+                              _stream(stream)),
+           "csa2_topk_bf16")
+    return idx_out
+
+
+def csa2_index_topk_decode_bf16(cache: Cache, q_idx: torch.Tensor, w: torch.Tensor,
+                                seq_ids: Optional[Sequence[int]] = None,
+                                topk_idx: Optional[torch.Tensor] = None,
+                                topk_score: Optional[torch.Tensor] = None,
+                                workspace: Optional[torch.Tensor] = None,
+                                stream=None) -> torch.Tensor:
+    nq = q_idx.shape[0]
+    dev = q_idx.device
+    if topk_idx is None:
+        topk_idx = torch.empty(nq, cache.cfg.topk, dtype=torch.int32, device=dev)
+    ws = _workspace(csa2_index_workspace_bytes(cache, nq), dev, workspace)
+    _check(lib.csa2_index_topk_decode_bf16(cache.handle, nq, _ptr(q_idx), _ptr(w),
+                                           _i32_array(seq_ids), _ptr(topk_idx), _ptr(topk_score),
+                                           _ptr(ws), ws.numel() * ws.element_size(),
+                                           _stream(stream)),
+           "csa2_index_topk_decode_bf16")
     return topk_idx

@@ -371,12 +371,16 @@ size_t csa2_topk_workspace_bytes(int32_t n_rows, int64_t max_valid) {
   return topk_seg_bytes(n_rows, max_valid);
 }
 
-csa2_status_t csa2_topk(int32_t n_rows, const float* scores, int64_t ld, const int64_t* n_valid,
+}  // extern "C"
+
+namespace {
+csa2_status_t topk_impl(int32_t n_rows, const void* scores, int64_t ld, const int64_t* n_valid,
                         int32_t k, const uint32_t* key_hist, int32_t* idx_out, float* score_out,
-                        void* workspace, size_t ws_bytes, csa2_stream_t stream) {
+                        void* workspace, size_t ws_bytes, csa2_stream_t stream, bool bf16) {
   if (n_rows < 0 || k <= 0 || k > 4096) return CSA2_ERR_INVALID_ARG;
   if (n_rows == 0) return CSA2_OK;
   if (!scores || !n_valid || !idx_out || ld < 0) return CSA2_ERR_INVALID_ARG;
+  const size_t esz = bf16 ? 2 : 4;
   int64_t max_valid = 0;
   for (int r = 0; r < n_rows; ++r) {
     if (n_valid[r] < 0 || n_valid[r] > ld || n_valid[r] > (int64_t)INT32_MAX)
@@ -391,7 +395,9 @@ csa2_status_t csa2_topk(int32_t n_rows, const float* scores, int64_t ld, const i
     const int nr = std::min(kTopkTab, n_rows - r0);
     TopkParams* p = new (std::nothrow) TopkParams();
     if (!p) return CSA2_ERR_OOM;
-    p->scores = scores + (int64_t)r0 * ld;
+    p->scores = reinterpret_cast<const float*>(static_cast<const uint8_t*>(scores) +
+                                               (size_t)r0 * ld * esz);
+    p->score_bf16 = bf16 ? 1 : 0;
     p->ld = ld;
     p->rows = nr;
     p->k = k;
@@ -410,6 +416,24 @@ csa2_status_t csa2_topk(int32_t n_rows, const float* scores, int64_t ld, const i
   }
   return CSA2_OK;
 }
+}  // namespace
+
+extern "C" {
+
+csa2_status_t csa2_topk(int32_t n_rows, const float* scores, int64_t ld, const int64_t* n_valid,
+                        int32_t k, const uint32_t* key_hist, int32_t* idx_out, float* score_out,
+                        void* workspace, size_t ws_bytes, csa2_stream_t stream) {
+  return topk_impl(n_rows, scores, ld, n_valid, k, key_hist, idx_out, score_out, workspace,
+                   ws_bytes, stream, false);
+}
+
+csa2_status_t csa2_topk_bf16(int32_t n_rows, const uint16_t* scores, int64_t ld,
+                             const int64_t* n_valid, int32_t k, const uint32_t* key_hist,
+                             int32_t* idx_out, float* score_out, void* workspace, size_t ws_bytes,
+                             csa2_stream_t stream) {
+  return topk_impl(n_rows, scores, ld, n_valid, k, key_hist, idx_out, score_out, workspace,
+                   ws_bytes, stream, true);
+}
 
 }  // extern "C"
 
@@ -418,8 +442,10 @@ namespace {
 // Scores of decode queries [q0, q0 + n) into scores (row stride ld): one
 // indexer launch per chunk of up to kMaxIdxGroups queries.
 csa2_status_t run_index_decode(const csa2_cache_t* c, int32_t nq, const void* q_idx,
-                               const float* w, const int32_t* seq_ids, float* scores, int64_t ld,
-                               uint32_t* key_hist, csa2_stream_t stream, IndexParams* ip) {
+                               const float* w, const int32_t* seq_ids, void* scores, int64_t ld,
+                               uint32_t* key_hist, csa2_stream_t stream, IndexParams* ip,
+                               bool bf16 = false) {
+  const size_t esz = bf16 ? 2 : 4;
   const uint16_t* qb = static_cast<const uint16_t*>(q_idx);
   if (key_hist &&
       cudaMemsetAsync(key_hist, 0, (size_t)nq * kKeyHistBinsHost * sizeof(uint32_t), S(stream)) !=
@@ -429,7 +455,8 @@ csa2_status_t run_index_decode(const csa2_cache_t* c, int32_t nq, const void* q_
     const int n = std::min(kMaxIdxGroups, nq - q0);
     std::memset(ip, 0, sizeof(IndexParams));
     ip->w = w + (int64_t)q0 * kIdxHeads;
-    ip->scores = scores + (int64_t)q0 * ld;
+    ip->scores = reinterpret_cast<float*>(static_cast<uint8_t*>(scores) + (size_t)q0 * ld * esz);
+    ip->score_bf16 = bf16 ? 1 : 0;
     ip->ld = ld;
     ip->key_hist = key_hist ? key_hist + (int64_t)q0 * kKeyHistBinsHost : nullptr;
     ip->err = c->d_err;
@@ -493,29 +520,36 @@ csa2_status_t csa2_index_scores_decode(const csa2_cache_t* c, int32_t nq, const 
   return st;
 }
 
-csa2_status_t csa2_index_topk_decode(const csa2_cache_t* c, int32_t nq, const void* q_idx,
+}  // extern "C"
+
+namespace {
+csa2_status_t index_topk_decode_impl(const csa2_cache_t* c, int32_t nq, const void* q_idx,
                                      const float* w, const int32_t* seq_ids, int32_t* topk_idx,
                                      float* topk_score, void* workspace, size_t ws_bytes,
-                                     csa2_stream_t stream) {
+                                     csa2_stream_t stream, bool bf16) {
   if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
   if (nq == 0) return CSA2_OK;
   csa2_status_t st = check_decode_queries(c, nq, q_idx, w, seq_ids);
   if (st != CSA2_OK) return st;
   if (!topk_idx || !workspace || !aligned16(workspace)) return CSA2_ERR_INVALID_ARG;
   if (ws_bytes < csa2_index_workspace_bytes(c, nq)) return CSA2_ERR_CAPACITY;
-  const int64_t ld = score_ld(c->max_cap);
-  float* scores = static_cast<float*>(workspace);
-  uint32_t* key_hist = reinterpret_cast<uint32_t*>(scores + (int64_t)nq * ld);
+  // bf16 rows: a multiple of 8 scores keeps every row 16-byte aligned (and
+  // the bf16 layout never needs more bytes than the fp32 one)
+  const int64_t ld = bf16 ? (c->max_cap + 7) / 8 * 8 : score_ld(c->max_cap);
+  const size_t esz = bf16 ? 2 : 4;
+  uint8_t* scores = static_cast<uint8_t*>(workspace);
+  uint32_t* key_hist = reinterpret_cast<uint32_t*>(scores + (size_t)nq * ld * esz);
   uint32_t* seg_ws = key_hist + (int64_t)nq * kKeyHistBinsHost;
   IndexParams* ip = new (std::nothrow) IndexParams();
   TopkParams* tp = new (std::nothrow) TopkParams();
   if (!ip || !tp) { delete ip; delete tp; return CSA2_ERR_OOM; }
-  st = run_index_decode(c, nq, q_idx, w, seq_ids, scores, ld, key_hist, stream, ip);
+  st = run_index_decode(c, nq, q_idx, w, seq_ids, scores, ld, key_hist, stream, ip, bf16);
   const int k = c->cfg.topk;
   for (int q0 = 0; q0 < nq && st == CSA2_OK; q0 += kTopkTab) {
     const int n = std::min(kTopkTab, nq - q0);
     std::memset(tp, 0, sizeof(TopkParams));
-    tp->scores = scores + (int64_t)q0 * ld;
+    tp->scores = reinterpret_cast<const float*>(scores + (size_t)q0 * ld * esz);
+    tp->score_bf16 = bf16 ? 1 : 0;
     tp->ld = ld;
     tp->rows = n;
     tp->k = k;
@@ -532,6 +566,44 @@ csa2_status_t csa2_index_topk_decode(const csa2_cache_t* c, int32_t nq, const vo
   }
   delete ip;
   delete tp;
+  return st;
+}
+}  // namespace
+
+extern "C" {
+
+csa2_status_t csa2_index_topk_decode(const csa2_cache_t* c, int32_t nq, const void* q_idx,
+                                     const float* w, const int32_t* seq_ids, int32_t* topk_idx,
+                                     float* topk_score, void* workspace, size_t ws_bytes,
+                                     csa2_stream_t stream) {
+  return index_topk_decode_impl(c, nq, q_idx, w, seq_ids, topk_idx, topk_score, workspace,
+                                ws_bytes, stream, false);
+}
+
+csa2_status_t csa2_index_topk_decode_bf16(const csa2_cache_t* c, int32_t nq, const void* q_idx,
+                                          const float* w, const int32_t* seq_ids,
+                                          int32_t* topk_idx, float* topk_score, void* workspace,
+                                          size_t ws_bytes, csa2_stream_t stream) {
+  return index_topk_decode_impl(c, nq, q_idx, w, seq_ids, topk_idx, topk_score, workspace,
+                                ws_bytes, stream, true);
+}
+
+csa2_status_t csa2_index_scores_decode_bf16(const csa2_cache_t* c, int32_t nq, const void* q_idx,
+                                            const float* w, const int32_t* seq_ids,
+                                            uint16_t* scores, int64_t ld, uint32_t* key_hist,
+                                            csa2_stream_t stream) {
+  if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
+  if (nq == 0) return CSA2_OK;
+  csa2_status_t st = check_decode_queries(c, nq, q_idx, w, seq_ids);
+  if (st != CSA2_OK) return st;
+  if (!scores || !aligned16(scores) || ld % 8 != 0) return CSA2_ERR_INVALID_ARG;
+  for (int i = 0; i < nq; ++i)
+    if (c->len[seq_ids ? seq_ids[i] : i] > ld) return CSA2_ERR_CAPACITY;
+  if (key_hist && !aligned16(key_hist)) return CSA2_ERR_INVALID_ARG;
+  IndexParams* ip = new (std::nothrow) IndexParams();
+  if (!ip) return CSA2_ERR_OOM;
+  st = run_index_decode(c, nq, q_idx, w, seq_ids, scores, ld, key_hist, stream, ip, true);
+  delete ip;
   return st;
 }
 

@@ -54,6 +54,7 @@ struct IndexParams {
   float* scores;           // [nq, ld]
   int64_t ld;
   uint32_t* key_hist;      // nullable [nq, 2048] score-key histogram (qpg == 1 only)
+  int32_t score_bf16;      // 1: scores are stored as bf16 (uint16 [nq, ld], nearest even)
   const int32_t* pool;     // nullable: pool mode, [nq, pool_blocks] block ids (-1 unused)
   int32_t pool_blocks;     // blocks per pool row (multiple of 16)
   uint32_t* err;
@@ -112,6 +113,7 @@ struct TopkParams {
   int32_t pre_len;
   int32_t ratio;
   int64_t pos0;
+  int32_t score_bf16;        // 1: scores are bf16 (uint16 [rows, ld])
   uint32_t* seg_ws;          // nullable: per-segment candidate buffers (see topk_seg_bytes)
   int32_t n_seg;             // segments per row when seg_ws is set
   int64_t n_valid[kTopkTab]; // formula == 0: per-row valid counts

@@ -19,6 +19,9 @@
 // slots past the sequence score -inf.  Block ids of the next tile are loaded
 // one tile ahead by the producer and by the epilogue.
 //
+// Scores are stored as fp32, or (selector precision of the V4 blog reading,
+// section 7) rounded to bf16 with the histogram taken on the rounded value.
+//
 // Persistent CTAs walk a balanced contiguous range of (group, tile) items.
 // Warp roles: warp 0 = TMA producer (lane 0; lanes 0-15 in pool mode), warp 1 = MMA issuer (and TMEM owner),
 // warps 2-9 = epilogue (TMEM -> registers -> scores), two warps per TMEM lane
@@ -267,8 +270,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.scores[(int64_t)q * p.ld + e] = v;
           if (use_hist) atomicAdd(hs + (score_key(v) >> 21), 1u);
         } else if (q < p.nq && e < group_nvis_query(p, g, j)) {
-          p.scores[(int64_t)q * p.ld + e] = s;
-          if (use_hist) atomicAdd(hs + (score_key(s) >> 21), 1u);
+          if (p.score_bf16) {
+            // the selector's precision: nearest bf16, its key histogrammed
+            const uint32_t b = float_to_bf16_bits(s);
+            reinterpret_cast<uint16_t*>(p.scores)[(int64_t)q * p.ld + e] = (uint16_t)b;
+            if (use_hist) atomicAdd(hs + (score_key(bf16_bits_to_float(b)) >> 21), 1u);
+          } else {
+            p.scores[(int64_t)q * p.ld + e] = s;
+            if (use_hist) atomicAdd(hs + (score_key(s) >> 21), 1u);
+          }
         }
       }
       tc_fence_before();

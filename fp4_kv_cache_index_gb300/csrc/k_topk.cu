@@ -1,6 +1,7 @@
 // k_topk.cu -- exact top-k of fp32 index scores per query (blog reading of
 // the DeepSeek-V4 report, section 4.1: keep the top-k compressed entries;
-// V4.1 report section 4.2.1: k = 512).
+// V4.1 report section 4.2.1: k = 512), or of bf16-rounded scores (same
+// blog, section 7), read as 16-bit values and handled as their fp32.
 //
 // One CTA per row.  Scores become order-preserving 32-bit keys (-0 folded to
 // +0).  The k-th largest key T is found by a radix select over the digits
@@ -120,20 +121,56 @@ __device__ __forceinline__ void select_bin(Shared& sh, int nbins, uint32_t rem) 
   __syncthreads();
 }
 
-// Each thread takes kPer consecutive scores per chunk (four 16-byte loads in
-// flight when the row is 16-byte aligned).
+// A row of scores: fp32, or bf16 (uint16) when the selector runs on
+// bf16-rounded scores; either way a score is handled as the fp32 of its value.
+struct ScoreRow {
+  const void* base;
+  bool bf16;
+  __device__ __forceinline__ float at(int64_t i) const {
+    return bf16 ? bf16_bits_to_float(__ldg(static_cast<const uint16_t*>(base) + i))
+                : __ldg(static_cast<const float*>(base) + i);
+  }
+  __device__ __forceinline__ bool aligned16() const {
+    return (reinterpret_cast<uintptr_t>(base) & 15u) == 0;
+  }
+  // v[0..7] = scores e .. e + 7 (caller: e % 8 == 0, the row 16-byte aligned)
+  __device__ __forceinline__ void load8(int64_t e, float* v) const {
+    if (bf16) {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + e));
+      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(u[i] << 16);
+        v[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+      }
+    } else {
+      const float4* f4 = reinterpret_cast<const float4*>(static_cast<const float*>(base) + e);
+      const float4 a = __ldg(f4), b = __ldg(f4 + 1);
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+      v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+  }
+};
+
+__device__ __forceinline__ ScoreRow score_row(const TopkParams& p, int row) {
+  ScoreRow r;
+  r.bf16 = p.score_bf16 != 0;
+  r.base = r.bf16 ? static_cast<const void*>(reinterpret_cast<const uint16_t*>(p.scores) +
+                                             (int64_t)row * p.ld)
+                  : static_cast<const void*>(p.scores + (int64_t)row * p.ld);
+  return r;
+}
+
+// Each thread takes kPer consecutive scores per chunk (16-byte loads when
+// the row is 16-byte aligned).
 constexpr int kPer = 8;
-__device__ __forceinline__ void load_run(const float* row, int64_t e, int64_t n, bool vec,
+__device__ __forceinline__ void load_run(const ScoreRow& row, int64_t e, int64_t n, bool vec,
                                          float (&v)[kPer]) {
   if (vec && e + kPer - 1 < n) {
-#pragma unroll
-    for (int q = 0; q < kPer / 4; ++q) {
-      const float4 f = __ldg(reinterpret_cast<const float4*>(row + e) + q);
-      v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
-    }
+    row.load8(e, v);
   } else {
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) v[i] = (e + i < n) ? __ldg(row + e + i) : 0.0f;
+    for (int i = 0; i < kPer; ++i) v[i] = (e + i < n) ? row.at(e + i) : 0.0f;
   }
 }
 
@@ -179,19 +216,16 @@ __global__ void __launch_bounds__(kSegThreads) k_topk_seg(const __grid_constant_
     if (tid == 0) out[0] = 0u;
     return;
   }
-  const float* srow = p.scores + (int64_t)row * p.ld;
+  const ScoreRow srow = score_row(p, row);
   const int64_t e0 = s0 + (int64_t)tid * kSegPer;
   float v[kSegPer];
-  const bool vec = ((reinterpret_cast<uintptr_t>(srow) & 15u) == 0) && e0 + kSegPer <= n;
+  const bool vec = srow.aligned16() && e0 + kSegPer <= n;
   if (vec) {
 #pragma unroll
-    for (int q = 0; q < kSegPer / 4; ++q) {
-      const float4 f = __ldg(reinterpret_cast<const float4*>(srow + e0) + q);
-      v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
-    }
+    for (int q = 0; q < kSegPer / 8; ++q) srow.load8(e0 + 8 * q, v + 8 * q);
   } else {
 #pragma unroll
-    for (int i = 0; i < kSegPer; ++i) v[i] = (e0 + i < n) ? __ldg(srow + e0 + i) : 0.0f;
+    for (int i = 0; i < kSegPer; ++i) v[i] = (e0 + i < n) ? srow.at(e0 + i) : 0.0f;
   }
   // threshold bin: thread t holds bins [4t, 4t + 4)
   const uint4 hv = __ldg(reinterpret_cast<const uint4*>(p.key_hist + (int64_t)row * kBins) + tid);
@@ -260,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
   if (row >= p.rows) return;
   const int64_t n = row_valid_count(p, row);
   const int k = p.k;
-  const float* srow = p.scores + (int64_t)row * p.ld;
+  const ScoreRow srow = score_row(p, row);
   int32_t* orow = p.idx_out + (int64_t)row * k;
   float* osc = p.score_out ? p.score_out + (int64_t)row * k : nullptr;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -268,11 +302,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
   if (n <= k) {
     for (int i = tid; i < k; i += kThreads) {
       orow[i] = (i < n) ? i : -1;
-      if (osc) osc[i] = (i < n) ? key_score(score_key(srow[i])) : 0.0f;
+      if (osc) osc[i] = (i < n) ? key_score(score_key(srow.at(i))) : 0.0f;
     }
     return;
   }
-  const bool vec = ((reinterpret_cast<uintptr_t>(srow) & 15u) == 0);
+  const bool vec = srow.aligned16();
   const int64_t chunk = (int64_t)kThreads * kPer;
 
   // ---- digit 1: keys [31:21]

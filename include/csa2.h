@@ -339,6 +339,39 @@ csa2_status_t csa2_topk(int32_t n_rows, const float* scores, int64_t ld,
                         float* score_out, void* workspace,
                         size_t workspace_bytes, csa2_stream_t stream);
 
+/* ---- bf16-rounded index scores ([V4B sec 7]: the index scores are
+ * quantised from FP32 to BF16 so that the top-k selector runs faster, with
+ * a reported recall of 99.7% of the KV entries the FP32 selection keeps).
+ * A score is the fp32 score of csa2_index_scores_decode rounded to the
+ * nearest bf16 value (ties to even); the selection rule is unchanged (the
+ * k largest, ties -- now frequent -- to the lower index).                  */
+
+/* Scores as bf16: scores is dev uint16 [n_queries, ld] (bf16 bits), ld a
+ * multiple of 8; key_hist (nullable) is the histogram of the rounded
+ * scores' keys.  Other arguments as for csa2_index_scores_decode.          */
+csa2_status_t csa2_index_scores_decode_bf16(const csa2_cache_t* cache,
+                                            int32_t n_queries, const void* q_idx,
+                                            const float* w, const int32_t* seq_ids,
+                                            uint16_t* scores, int64_t ld,
+                                            uint32_t* key_hist, csa2_stream_t stream);
+
+/* csa2_topk over bf16 scores (dev uint16 [n_rows, ld]); score_out (nullable
+ * dev fp32) receives the selected bf16 values.  Same workspace.           */
+csa2_status_t csa2_topk_bf16(int32_t n_rows, const uint16_t* scores, int64_t ld,
+                             const int64_t* n_valid, int32_t k,
+                             const uint32_t* key_hist, int32_t* idx_out,
+                             float* score_out, void* workspace,
+                             size_t workspace_bytes, csa2_stream_t stream);
+
+/* csa2_index_topk_decode on bf16-rounded scores; the same workspace size
+ * (csa2_index_workspace_bytes) suffices.                                   */
+csa2_status_t csa2_index_topk_decode_bf16(const csa2_cache_t* cache,
+                                          int32_t n_queries, const void* q_idx,
+                                          const float* w, const int32_t* seq_ids,
+                                          int32_t* topk_idx, float* topk_score,
+                                          void* workspace, size_t workspace_bytes,
+                                          csa2_stream_t stream);
+
 /* ---- sparse attention -------------------------------------------------- */
 
 /* Workspace bytes of csa2_sparse_attn_decode for n_queries queries. */
