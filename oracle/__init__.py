@@ -226,6 +226,43 @@ def sparse_attention(q_bf16, codes, scales, layout, idx, swa_bf16, scale):
     return out_b, out_d, lse
 
 
+def attention_epilogue(out_d, lse, sink=None, rope_pos=None, rope_base: float = 10000.0,
+                       rope_dims: int = 64):
+    """Epilogue variants of the readout ("DeepSeek-V4" blog reading, section
+    4.3), applied in fp64 to one query's core attention output:
+
+    * attention sink: a per-head learnable logit z'_h whose exp joins the
+      softmax denominator, s_j = exp(l_j) / (sum_k exp(l_k) + exp(z'_h)), so a
+      head's weights may sum to less than 1 (the sink carries no value);
+    * output RoPE(-i): the last `rope_dims` channels of the output, taken as
+      interleaved pairs (2t, 2t+1) with frequency base^(-2t / rope_dims), are
+      rotated by the angle of position -i, so the output carries relative
+      rather than absolute position.
+
+    out_d: fp64 [heads, dim] and lse: fp64 [heads] from sparse_attention
+    (natural log of the denominator without the sink).  Returns
+    (out bf16 bits, out fp64, lse fp64 of the full denominator)."""
+    out = np.array(out_d, np.float64, copy=True)
+    lse = np.asarray(lse, np.float64)
+    if sink is not None:
+        z = np.asarray(sink, np.float64)
+        lse_all = np.logaddexp(lse, z)
+        out *= np.exp(lse - lse_all)[:, None]
+        lse = lse_all
+    if rope_pos is not None:
+        d0 = out.shape[1] - rope_dims
+        t = np.arange(rope_dims // 2, dtype=np.float64)
+        phi = -float(rope_pos) * rope_base ** (-2.0 * t / rope_dims)
+        c, s_ = np.cos(phi), np.sin(phi)
+        a = out[:, d0::2].copy()
+        b = out[:, d0 + 1::2].copy()
+        out[:, d0::2] = a * c - b * s_
+        out[:, d0 + 1::2] = a * s_ + b * c
+    rounded = bf16_round(out.astype(np.float32))
+    bits = (rounded.view(np.uint32) >> 16).astype(np.uint16)
+    return bits, out, lse
+
+
 # ---------------------------------------------------------------- composition
 def visible_entries(n_ent: int, m: int, pos=None) -> int:
     """Entries a query sees: all of them in decode (the query is the newest
