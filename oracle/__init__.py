@@ -247,7 +247,11 @@ def attention_epilogue(out_d, lse, sink=None, rope_pos=None, rope_base: float = 
     if sink is not None:
         z = np.asarray(sink, np.float64)
         lse_all = np.logaddexp(lse, z)
-        out *= np.exp(lse - lse_all)[:, None]
+        # a head with neither candidates nor sink keeps its empty softmax:
+        # output 0, lse -inf (as without a sink)
+        empty = np.isneginf(lse_all)
+        factor = np.exp(lse - np.where(empty, 0.0, lse_all))
+        out *= np.where(empty, 0.0, factor)[:, None]
         lse = lse_all
     if rope_pos is not None:
         d0 = out.shape[1] - rope_dims

@@ -93,3 +93,13 @@ def test_sink_and_rope_commute_and_round_to_bf16():
     _, o2, _ = O.attention_epilogue(tmp, lse, sink=zs)
     assert np.allclose(o1, o2, atol=1e-14)
     assert np.array_equal(bf16_bits_to_f32(b1), O.bf16_round(o1.astype(np.float32)))
+
+
+def test_empty_head_without_sink_stays_empty():
+    out = np.zeros((64, 512))
+    lse = np.full(64, -np.inf)
+    zs = np.full(64, 1.5)
+    zs[3] = -np.inf
+    _, o, l = O.attention_epilogue(out, lse, sink=zs, rope_pos=7)
+    assert np.all(o == 0) and np.all(np.isfinite(o))
+    assert l[3] == -np.inf and np.all(l[np.arange(64) != 3] == 1.5)
