@@ -57,6 +57,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-bf16-scores", action="store_true",
                    help="skip the bf16-rounded index score measurement")
+    p.add_argument("--no-epilogue", action="store_true",
+                   help="skip the sink / output-RoPE readout measurement")
     p.add_argument("--no-hsi", action="store_true",
                    help="skip the Hierarchical Sparse Indexer / Reindex measurement")
     p.add_argument("--no-graph", action="store_true",
@@ -461,6 +463,10 @@ def run_csa2(args):
         bf16 = measure_bf16_scores(C, cache, wl, bufs[0]["q_idx"], bufs[0]["w"], n_valid,
                                    bufs[0]["topk"], key_hist, topk_ws, dev, stream,
                                    max(3, min(args.steps, 300)), t_idx, t_topk)
+    epi = None
+    if not args.no_epilogue:
+        epi = measure_epilogue(C, cache, bufs[0], attn_ws, scale, wl, dev, stream,
+                               max(3, min(args.steps, 300)))
     hsi = None
     if not args.no_hsi:
         hsi = measure_hsi(C, W, wl, cache, scores, n_valid, dev, stream,
@@ -505,6 +511,7 @@ def run_csa2(args):
         "gpu_launches": launches_per_step * args.steps,
         "hsi_reindex": hsi,
         "bf16_scores": bf16,
+        "readout_epilogue": epi,
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -515,6 +522,39 @@ def run_csa2(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def measure_epilogue(C, cache, d, attn_ws, scale, wl, dev, stream, iters):
+    """One layer's readout with the V4 blog reading's section 4.3 variants
+    (a per-head sink logit and the output RoPE(-i) on the last 64 channels)
+    against the plain readout, same inputs, events around each call."""
+    import torch
+    B = wl.batch
+    sink = torch.linspace(-2.0, 2.0, 64, device=dev)
+    pos = torch.full((B,), int(wl.ctx) - 1, dtype=torch.int64, device=dev)
+    out = torch.empty_like(d["outs"][0])
+
+    def timed(**kw):
+        for _ in range(3):
+            C.csa2_sparse_attn_decode(cache, d["qs"][0], d["swas"][0], d["topk"], scale, out=out,
+                                      workspace=attn_ws, **kw)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(iters):
+            C.csa2_sparse_attn_decode(cache, d["qs"][0], d["swas"][0], d["topk"], scale, out=out,
+                                      workspace=attn_ws, **kw)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / iters
+
+    plain = timed()
+    variants = timed(sink=sink, rope_pos=pos)
+    if cache.device_error() != 0:
+        raise RuntimeError("device error word set during the epilogue measurement")
+    return {"plain_layer_ms": plain, "sink_rope_layer_ms": variants,
+            "timed_as": "eager calls, one layer"}
 
 
 def measure_bf16_scores(C, cache, wl, q_idx, w, n_valid, fp32_idx, key_hist, topk_ws, dev,

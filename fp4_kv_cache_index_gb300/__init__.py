@@ -48,6 +48,12 @@ def config(n_heads=64, head_dim=512, idx_heads=32, idx_dim=128, topk=512, swa=12
     return Config(n_heads, head_dim, idx_heads, idx_dim, topk, swa, ratio, layout)
 
 
+class AttnOpts(ctypes.Structure):
+    """csa2_attn_opts_t: attention sink and output RoPE(-i)."""
+    _fields_ = [("sink", ctypes.c_void_p), ("rope_pos", ctypes.c_void_p),
+                ("rope_out", ctypes.c_int32), ("rope_base", ctypes.c_double)]
+
+
 class CacheViews(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("idx_k", ctypes.c_void_p), ("lengths", ctypes.c_void_p),
@@ -83,6 +89,10 @@ def _load():
         "csa2_index_scores_decode_bf16": ([P, i32, P, P, P, P, i64, P, P], i32),
         "csa2_topk_bf16": ([i32, P, i64, P, i32, P, P, P, P, sz, P], i32),
         "csa2_index_topk_decode_bf16": ([P, i32, P, P, P, P, P, P, sz, P], i32),
+        "csa2_sparse_attn_decode_ex": ([P, i32, P, P, P, P, P, ctypes.c_float, P, P, P, sz, P,
+                                        P], i32),
+        "csa2_sparse_attn_prefill_ex": ([P, i32, i32, i64, P, P, i64, i64, P, ctypes.c_float, P,
+                                         P, P, P], i32),
         "csa2_hsi_pool_workspace_bytes": ([i32, i64], sz),
         "csa2_hsi_pool": ([i32, P, i64, P, i32, i32, P, P, sz, P], i32),
         "csa2_index_reindex_workspace_bytes": ([P, i32, i32], sz),
@@ -321,9 +331,13 @@ def csa2_sparse_attn_decode(cache: Cache, q: torch.Tensor, swa_kv: Optional[torc
                             out: Optional[torch.Tensor] = None,
                             lse: Optional[torch.Tensor] = None,
                             workspace: Optional[torch.Tensor] = None,
+                            sink: Optional[torch.Tensor] = None,
+                            rope_pos: Optional[torch.Tensor] = None, rope_base: float = 0.0,
                             stream=None) -> torch.Tensor:
     """workspace=None allocates one of csa2_sparse_attn_workspace_bytes; pass
-    an empty tensor to run without (one CTA per query)."""
+    an empty tensor to run without (one CTA per query).  sink: fp32 [n_heads]
+    per-head sink logits; rope_pos: int64 [n_queries] positions i for the
+    output RoPE(-i)."""
     nq = q.shape[0]
     if out is None:
         out = torch.empty_like(q)
@@ -331,12 +345,16 @@ def csa2_sparse_attn_decode(cache: Cache, q: torch.Tensor, swa_kv: Optional[torc
         workspace = torch.empty(max(16, csa2_sparse_attn_workspace_bytes(cache, nq)),
                                 dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(lib.csa2_sparse_attn_decode(cache.handle, nq, _i32_array(seq_ids), _ptr(q),
-                                       _ptr(swa_kv), _ptr(swa_len), _ptr(topk_idx),
-                                       float(scale), _ptr(out), _ptr(lse),
-                                       _ptr(workspace) if ws_bytes else None, ws_bytes,
-                                       _stream(stream)),
-           "csa2_sparse_attn_decode")
+    args = (cache.handle, nq, _i32_array(seq_ids), _ptr(q), _ptr(swa_kv), _ptr(swa_len),
+            _ptr(topk_idx), float(scale), _ptr(out), _ptr(lse),
+            _ptr(workspace) if ws_bytes else None, ws_bytes)
+    if sink is None and rope_pos is None:
+        _check(lib.csa2_sparse_attn_decode(*args, _stream(stream)), "csa2_sparse_attn_decode")
+    else:
+        opts = AttnOpts(_ptr(sink), _ptr(rope_pos), 1 if rope_pos is not None else 0,
+                        float(rope_base))
+        _check(lib.csa2_sparse_attn_decode_ex(*args, ctypes.byref(opts), _stream(stream)),
+               "csa2_sparse_attn_decode_ex")
     return out
 
 
@@ -344,15 +362,22 @@ def csa2_sparse_attn_prefill(cache: Cache, seq: int, pos0: int, q: torch.Tensor,
                              swa_kv: Optional[torch.Tensor], swa_pos0: int,
                              topk_idx: torch.Tensor, scale: float,
                              out: Optional[torch.Tensor] = None,
-                             lse: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                             lse: Optional[torch.Tensor] = None,
+                             sink: Optional[torch.Tensor] = None, rope_out: bool = False,
+                             rope_base: float = 0.0, stream=None) -> torch.Tensor:
+    """rope_out: rotate the last 64 output channels by RoPE(-(pos0 + i))."""
     nq = q.shape[0]
     if out is None:
         out = torch.empty_like(q)
     n_rows = swa_kv.shape[0] if swa_kv is not None else 0
-    _check(lib.csa2_sparse_attn_prefill(cache.handle, seq, nq, pos0, _ptr(q), _ptr(swa_kv),
-                                        swa_pos0, n_rows, _ptr(topk_idx), float(scale),
-                                        _ptr(out), _ptr(lse), _stream(stream)),
-           "csa2_sparse_attn_prefill")
+    args = (cache.handle, seq, nq, pos0, _ptr(q), _ptr(swa_kv), swa_pos0, n_rows,
+            _ptr(topk_idx), float(scale), _ptr(out), _ptr(lse))
+    if sink is None and not rope_out:
+        _check(lib.csa2_sparse_attn_prefill(*args, _stream(stream)), "csa2_sparse_attn_prefill")
+    else:
+        opts = AttnOpts(_ptr(sink), None, 1 if rope_out else 0, float(rope_base))
+        _check(lib.csa2_sparse_attn_prefill_ex(*args, ctypes.byref(opts), _stream(stream)),
+               "csa2_sparse_attn_prefill_ex")
     return out
 
 

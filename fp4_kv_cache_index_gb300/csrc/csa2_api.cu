@@ -696,10 +696,41 @@ size_t csa2_sparse_attn_workspace_bytes(const csa2_cache_t* c, int32_t n_queries
   return attn_part_bytes(n_queries, c->cfg.n_heads / kAttnHeadGroup);
 }
 
+}  // extern "C"
+
+namespace {
+// Epilogue options into the launch parameters; false when they are invalid.
+bool apply_opts(AttnParams* p, const csa2_attn_opts_t* opts, bool decode, int32_t q0) {
+  p->rope_base = 10000.0;
+  if (!opts) return true;
+  p->sink = opts->sink;
+  if (opts->rope_out) {
+    if (decode && !opts->rope_pos) return false;
+    if (opts->rope_base < 0.0 || opts->rope_base != opts->rope_base) return false;
+    p->rope_out = 1;
+    p->rope_pos = decode ? opts->rope_pos + q0 : nullptr;
+    if (opts->rope_base > 0.0) p->rope_base = opts->rope_base;
+  }
+  return true;
+}
+}  // namespace
+
+extern "C" {
+
 csa2_status_t csa2_sparse_attn_decode(const csa2_cache_t* c, int32_t nq, const int32_t* seq_ids,
                                       const void* q, const void* swa_kv, const int32_t* swa_len,
                                       const int32_t* topk_idx, float scale, void* out, float* lse,
                                       void* workspace, size_t ws_bytes, csa2_stream_t stream) {
+  return csa2_sparse_attn_decode_ex(c, nq, seq_ids, q, swa_kv, swa_len, topk_idx, scale, out, lse,
+                                    workspace, ws_bytes, nullptr, stream);
+}
+
+csa2_status_t csa2_sparse_attn_decode_ex(const csa2_cache_t* c, int32_t nq,
+                                         const int32_t* seq_ids, const void* q,
+                                         const void* swa_kv, const int32_t* swa_len,
+                                         const int32_t* topk_idx, float scale, void* out,
+                                         float* lse, void* workspace, size_t ws_bytes,
+                                         const csa2_attn_opts_t* opts, csa2_stream_t stream) {
   if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
   if (nq == 0) return CSA2_OK;
   const int W = c->cfg.swa;
@@ -738,6 +769,7 @@ csa2_status_t csa2_sparse_attn_decode(const csa2_cache_t* c, int32_t nq, const i
     p->scale_log2 = scale * 1.4426950408889634f;
     p->prefill = 0;
     p->splits = split ? 2 : 1;
+    if (!apply_opts(p, opts, true, q0)) { st = CSA2_ERR_INVALID_ARG; break; }
     if (split) {
       p->part = static_cast<float*>(workspace);
       p->counter = reinterpret_cast<uint32_t*>(
@@ -772,6 +804,16 @@ csa2_status_t csa2_sparse_attn_prefill(const csa2_cache_t* c, int32_t seq, int32
                                        int64_t swa_pos0, int64_t n_swa_rows,
                                        const int32_t* topk_idx, float scale, void* out, float* lse,
                                        csa2_stream_t stream) {
+  return csa2_sparse_attn_prefill_ex(c, seq, nq, pos0, q, swa_kv, swa_pos0, n_swa_rows, topk_idx,
+                                     scale, out, lse, nullptr, stream);
+}
+
+csa2_status_t csa2_sparse_attn_prefill_ex(const csa2_cache_t* c, int32_t seq, int32_t nq,
+                                          int64_t pos0, const void* q, const void* swa_kv,
+                                          int64_t swa_pos0, int64_t n_swa_rows,
+                                          const int32_t* topk_idx, float scale, void* out,
+                                          float* lse, const csa2_attn_opts_t* opts,
+                                          csa2_stream_t stream) {
   if (!c || nq < 0 || seq < 0 || seq >= c->batch || pos0 < 0) return CSA2_ERR_INVALID_ARG;
   if (nq == 0) return CSA2_OK;
   const int W = c->cfg.swa;
@@ -806,9 +848,10 @@ csa2_status_t csa2_sparse_attn_prefill(const csa2_cache_t* c, int32_t seq, int32
   p->pos0 = pos0;
   p->swa_pos0 = swa_pos0;
   p->splits = 1;
-  csa2_status_t st = CSA2_OK;
+  csa2_status_t st = apply_opts(p, opts, false, 0) ? CSA2_OK : CSA2_ERR_INVALID_ARG;
   CUtensorMap tm_q, tm_swa;
-  if (!make_map(&tm_q, q, (uint64_t)nq * H, kHeadDim, 64, kAttnHeadGroup)) st = CSA2_ERR_CUDA;
+  if (st == CSA2_OK && !make_map(&tm_q, q, (uint64_t)nq * H, kHeadDim, 64, kAttnHeadGroup))
+    st = CSA2_ERR_CUDA;
   if (st == CSA2_OK) {
     if (W > 0) {
       if (!make_map(&tm_swa, swa_kv, (uint64_t)n_swa_rows, kHeadDim, 64, 128)) st = CSA2_ERR_CUDA;

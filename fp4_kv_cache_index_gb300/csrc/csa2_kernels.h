@@ -150,6 +150,10 @@ struct AttnParams {
   int32_t pre_len;           // prefill: entries in the sequence
   int64_t pos0;              // prefill: position of query 0
   int64_t swa_pos0;          // prefill: position of swa row 0
+  const float* sink;         // nullable [n_heads]: per-head sink logit z' (units of scale * q.kv)
+  const int64_t* rope_pos;   // decode: [nq] query positions for the output RoPE(-i)
+  int32_t rope_out;          // 1: rotate the last 64 output channels by -position
+  double rope_base;          // RoPE frequency base
   int64_t q_base[kAttnTab];  // decode: entry offset of each query's sequence
   int32_t q_len[kAttnTab];   // decode: entries of each query's sequence
 };

@@ -58,6 +58,7 @@ struct Small {
   uint8_t row_valid[kRows];
   int32_t n_tiles;
   int32_t n_all;
+  float rope_c[32], rope_s[32];  // output RoPE(-i): cos, sin of each channel pair
   int32_t need_rescale;
   int32_t merge;
   uint32_t tmem;
@@ -405,16 +406,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
   }
   // ------------------------------------------------ epilogue
+  // Variants of the blog reading of the DeepSeek-V4 report, section 4.3: a
+  // per-head sink logit z' whose exp joins the softmax denominator (the sink
+  // has no value), and RoPE at position -i on the last 64 output channels
+  // (interleaved pairs, frequency base^(-2t/64)), applied before the bf16
+  // cast.  The angles are formed in fp64 (positions reach 2^20).
+  const bool rope = p.rope_out != 0;
+  if (rope && tid < 32) {
+    const double pos = p.prefill ? (double)(p.pos0 + q) : (double)p.rope_pos[q];
+    double sn, cs;
+    sincos(-pos * pow(p.rope_base, -(double)tid / 32.0), &sn, &cs);
+    sm.rope_c[tid] = (float)cs;
+    sm.rope_s[tid] = (float)sn;
+  }
   __syncthreads();
   const int64_t out_row = (int64_t)q * p.n_heads + hg * kHG;   // first head of this CTA
+  // sink logit of head h in log2 units (-inf: none)
+  auto sink_log2 = [&](int h) -> float {
+    return p.sink ? p.sink[hg * kHG + h] * 1.4426950408889634f : -INFINITY;
+  };
+  // output channel d of head slot c, rotated when it is a RoPE channel
+  // (channel pairs sit in adjacent lanes: every lane of the warp calls this)
+  auto finish = [&](int i, float o) -> float {
+    if (rope && i == 3 && quad >= 2) {
+      const float other = __shfl_xor_sync(0xffffffffu, o, 1);
+      const int t = ((quad - 2) * 32 + lane) >> 1;
+      const float cs = sm.rope_c[t], sn = sm.rope_s[t];
+      o = (lane & 1) ? fmaf(other, sn, o * cs) : fmaf(-other, sn, o * cs);
+    }
+    return o;
+  };
   if (p.splits == 1) {
     if (ok && n_tiles > 0) {
       if (tid < kHG) {
-        const float l = sm.l[tid];
-        sm.alpha[tid] = l > 0.0f ? 1.0f / l : 0.0f;
+        const float l = sm.l[tid], m = sm.m[tid], z = sink_log2(tid);
+        const float M = fmaxf(m, z);
+        const float am = (m == -INFINITY) ? 0.0f : fast_exp2(m - M);
+        const float L = l * am + ((z == -INFINITY) ? 0.0f : fast_exp2(z - M));
+        sm.alpha[tid] = L > 0.0f ? am / L : 0.0f;
         if (p.lse)
-          p.lse[out_row + tid] =
-              l > 0.0f ? (sm.m[tid] + log2f(l)) * 0.69314718055994531f : -INFINITY;
+          p.lse[out_row + tid] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
       }
       __syncthreads();
 #pragma unroll 1
@@ -424,14 +455,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int d = 128 * i + quad * 32 + lane;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float o = __uint_as_float(r[c]) * sm.alpha[16 * hh + c];
+          const float o = finish(i, __uint_as_float(r[c]) * sm.alpha[16 * hh + c]);
           p.out[(out_row + 16 * hh + c) * kHeadDim + d] = (uint16_t)float_to_bf16_bits(o);
         }
       }
     } else if (n_tiles == 0) {
-      // no candidate at all: output 0, lse -inf
+      // no candidate at all: output 0, lse = the sink alone (or -inf)
       for (int i = tid; i < kHG * kHeadDim; i += kThreads) p.out[out_row * kHeadDim + i] = 0;
-      if (p.lse && tid < kHG) p.lse[out_row + tid] = -INFINITY;
+      if (p.lse && tid < kHG)
+        p.lse[out_row + tid] = p.sink ? p.sink[hg * kHG + tid] : -INFINITY;
     }
   } else if (ok) {
     // ---- split-KV: the CTA that finishes second merges.  If the partner has
@@ -471,10 +503,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_ot = __ldcg(other + tid), l_ot = __ldcg(other + kHG + tid);
         const float m0 = split == 0 ? m_me2 : m_ot, m1 = split == 0 ? m_ot : m_me2;
         const float l0 = split == 0 ? l_me : l_ot, l1 = split == 0 ? l_ot : l_me;
-        const float M = fmaxf(m0, m1);
-        const float a0 = (M == -INFINITY) ? 0.0f : fast_exp2(m0 - M);
-        const float a1 = (M == -INFINITY) ? 0.0f : fast_exp2(m1 - M);
-        const float L = a0 * l0 + a1 * l1;
+        const float z = sink_log2(tid);
+        const float M = fmaxf(fmaxf(m0, m1), z);
+        const float a0 = (m0 == -INFINITY) ? 0.0f : fast_exp2(m0 - M);
+        const float a1 = (m1 == -INFINITY) ? 0.0f : fast_exp2(m1 - M);
+        const float L = a0 * l0 + a1 * l1 + ((z == -INFINITY) ? 0.0f : fast_exp2(z - M));
         const float c_me = L > 0.0f ? (split == 0 ? a0 : a1) / L : 0.0f;
         const float c_ot = L > 0.0f ? (split == 0 ? a1 : a0) / L : 0.0f;
         sm.alpha[tid] = (n_tiles > 0) ? c_me : 0.0f;     // weight of this CTA's O
@@ -498,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float o_me = have_me ? sm.alpha[h] * __uint_as_float(r[c]) : 0.0f;
           const float o_ot = w_ot != 0.0f ? w_ot * po[c] : 0.0f;
           // fixed order: split 0's term first
-          const float o = split == 0 ? o_me + o_ot : o_ot + o_me;
+          const float o = finish(i, split == 0 ? o_me + o_ot : o_ot + o_me);
           p.out[(out_row + h) * kHeadDim + d] = (uint16_t)float_to_bf16_bits(o);
         }
       }

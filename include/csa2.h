@@ -424,6 +424,47 @@ csa2_status_t csa2_sparse_attn_prefill(const csa2_cache_t* cache, int32_t seq,
                                        void* out, float* lse,
                                        csa2_stream_t stream);
 
+/* ---- readout epilogue variants ([V4B sec 4.3]) --------------------------
+ * Both are off when the options pointer is NULL or the struct is zeroed.
+ *   sink: nullable dev fp32 [n_heads], a per-head logit z'_h in the units of
+ *     l_j (scale * q . kv); exp(z'_h) joins the softmax denominator, so a
+ *     head's weights sum to less than 1 (the sink has no value):
+ *     out = sum_j exp(l_j) kv_j / (sum_j exp(l_j) + exp(z'_h)), and lse is
+ *     the log of that whole denominator (z'_h alone when nothing is
+ *     selected).
+ *   rope_out: 1 rotates the last 64 channels of each output row by the
+ *     RoPE angle of position -i (channel pairs (448 + 2t, 449 + 2t), angle
+ *     -i * rope_base^(-2t / 64)), so that the output carries relative
+ *     position; i is rope_pos[q] (decode: dev int64 [n_queries], required)
+ *     or pos0 + q (prefill).  rope_base: 0 means 10000.                    */
+typedef struct {
+  const float* sink;
+  const int64_t* rope_pos;
+  int32_t rope_out;
+  double rope_base;
+} csa2_attn_opts_t;
+
+/* csa2_sparse_attn_decode with epilogue options (NULL: none).           */
+csa2_status_t csa2_sparse_attn_decode_ex(const csa2_cache_t* cache,
+                                         int32_t n_queries, const int32_t* seq_ids,
+                                         const void* q, const void* swa_kv,
+                                         const int32_t* swa_len,
+                                         const int32_t* topk_idx, float scale,
+                                         void* out, float* lse, void* workspace,
+                                         size_t workspace_bytes,
+                                         const csa2_attn_opts_t* opts,
+                                         csa2_stream_t stream);
+
+/* csa2_sparse_attn_prefill with epilogue options (NULL: none).          */
+csa2_status_t csa2_sparse_attn_prefill_ex(const csa2_cache_t* cache, int32_t seq,
+                                          int32_t n_queries, int64_t pos0,
+                                          const void* q, const void* swa_kv,
+                                          int64_t swa_pos0, int64_t n_swa_rows,
+                                          const int32_t* topk_idx, float scale,
+                                          void* out, float* lse,
+                                          const csa2_attn_opts_t* opts,
+                                          csa2_stream_t stream);
+
 /* ---- errors ------------------------------------------------------------ */
 
 /* Reads and clears the cache's sticky device error word (synchronises
