@@ -2,6 +2,7 @@
 // cache layout in caller memory, TMA tensor maps, and launch scheduling of
 // the kernels in k_append.cu, k_index.cu, k_topk.cu and k_attn.cu.
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -701,7 +702,6 @@ size_t csa2_sparse_attn_workspace_bytes(const csa2_cache_t* c, int32_t n_queries
 namespace {
 // Epilogue options into the launch parameters; false when they are invalid.
 bool apply_opts(AttnParams* p, const csa2_attn_opts_t* opts, bool decode, int32_t q0) {
-  p->rope_base = 10000.0;
   if (!opts) return true;
   p->sink = opts->sink;
   if (opts->rope_out) {
@@ -709,7 +709,8 @@ bool apply_opts(AttnParams* p, const csa2_attn_opts_t* opts, bool decode, int32_
     if (opts->rope_base < 0.0 || opts->rope_base != opts->rope_base) return false;
     p->rope_out = 1;
     p->rope_pos = decode ? opts->rope_pos + q0 : nullptr;
-    if (opts->rope_base > 0.0) p->rope_base = opts->rope_base;
+    const double base = opts->rope_base > 0.0 ? opts->rope_base : 10000.0;
+    for (int t = 0; t < 32; ++t) p->rope_theta[t] = std::pow(base, -(double)t / 32.0);
   }
   return true;
 }

@@ -153,7 +153,7 @@ struct AttnParams {
   const float* sink;         // nullable [n_heads]: per-head sink logit z' (units of scale * q.kv)
   const int64_t* rope_pos;   // decode: [nq] query positions for the output RoPE(-i)
   int32_t rope_out;          // 1: rotate the last 64 output channels by -position
-  double rope_base;          // RoPE frequency base
+  double rope_theta[32];     // RoPE frequencies base^(-2t/64) of the 32 channel pairs
   int64_t q_base[kAttnTab];  // decode: entry offset of each query's sequence
   int32_t q_len[kAttnTab];   // decode: entries of each query's sequence
 };

@@ -410,14 +410,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   // per-head sink logit z' whose exp joins the softmax denominator (the sink
   // has no value), and RoPE at position -i on the last 64 output channels
   // (interleaved pairs, frequency base^(-2t/64)), applied before the bf16
-  // cast.  The angles are formed in fp64 (positions reach 2^20).
+  // cast.  The angle -i * theta_t (positions reach 2^20) is formed and
+  // reduced modulo 2 pi in fp64, then its sine and cosine are taken in fp32.
   const bool rope = p.rope_out != 0;
   if (rope && tid < 32) {
     const double pos = p.prefill ? (double)(p.pos0 + q) : (double)p.rope_pos[q];
-    double sn, cs;
-    sincos(-pos * pow(p.rope_base, -(double)tid / 32.0), &sn, &cs);
-    sm.rope_c[tid] = (float)cs;
-    sm.rope_s[tid] = (float)sn;
+    const double phi = -pos * p.rope_theta[tid];
+    const double turns = rint(phi * 0.15915494309189535);       // 1 / (2 pi)
+    const float r = (float)fma(-turns, 6.283185307179586, phi);  // in [-pi, pi]
+    float sn, cs;
+    sincosf(r, &sn, &cs);
+    sm.rope_c[tid] = cs;
+    sm.rope_s[tid] = sn;
   }
   __syncthreads();
   const int64_t out_row = (int64_t)q * p.n_heads + hg * kHG;   // first head of this CTA
