@@ -285,6 +285,31 @@ def index_topk(k_bf16, q_bf16, w, k, n_vis=None):
     return topk(sc.astype(np.float32), k), sc
 
 
+def mxfp4_round_bf16(x_bf16) -> np.ndarray:
+    """Rows of 128 bf16 channels onto the OCP MXFP4 grid ("DeepSeek-V4.1-
+    Flash" report, section 2.4.4: FP4 indexer queries and keys; one UE8M0
+    scale per 32 channels, the L32 rule of `quantise`), returned as bf16
+    bits (every E2M1 code times a power-of-two scale is a bf16 value)."""
+    x = np.asarray(x_bf16, np.uint16)
+    shape = x.shape
+    f = (x.astype(np.uint32) << 16).view(np.float32).reshape(-1, shape[-1])
+    codes, scales = quantise(f, LAYOUT_L32_UE8M0)
+    d = dequantise(codes, scales, LAYOUT_L32_UE8M0)
+    return (d.view(np.uint32) >> 16).astype(np.uint16).reshape(shape)
+
+
+def index_topk_mxfp4(k_bf16, q_bf16, w, k, n_vis=None):
+    """Full-layer selection with MXFP4 indexer keys and queries: the keys and
+    every query head rounded to the MXFP4 grid, then the fp64 score of the
+    dequantised values, rounded to fp32 for the top-k.  Returns (idx [k],
+    fp64 scores [n_vis])."""
+    n_vis = k_bf16.shape[0] if n_vis is None else n_vis
+    kq = mxfp4_round_bf16(np.asarray(k_bf16)[:n_vis])
+    qq = mxfp4_round_bf16(q_bf16)
+    sc = index_scores(kq, qq, w)
+    return topk(sc.astype(np.float32), k), sc
+
+
 def index_topk_bf16(k_bf16, q_bf16, w, k, n_vis=None):
     """Selection on bf16-rounded scores ("DeepSeek-V4" blog reading, section
     7): fp64 scores -> fp32 -> bf16, then the top-k with ties (now frequent)
