@@ -39,13 +39,15 @@ class Config(ctypes.Structure):
     _fields_ = [("n_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("idx_heads", ctypes.c_int32), ("idx_dim", ctypes.c_int32),
                 ("topk", ctypes.c_int32), ("swa", ctypes.c_int32),
-                ("ratio", ctypes.c_int32), ("layout", ctypes.c_int32)]
+                ("ratio", ctypes.c_int32), ("layout", ctypes.c_int32),
+                ("idx_layout", ctypes.c_int32)]
 
 
 def config(n_heads=64, head_dim=512, idx_heads=32, idx_dim=128, topk=512, swa=128, ratio=1,
-           layout=CSA2_KV_L32_UE8M0) -> Config:
-    """Layer shapes of the V4.1 report, section 4.2.1, as defaults."""
-    return Config(n_heads, head_dim, idx_heads, idx_dim, topk, swa, ratio, layout)
+           layout=CSA2_KV_L32_UE8M0, idx_layout=0) -> Config:
+    """Layer shapes of the V4.1 report, section 4.2.1, as defaults;
+    idx_layout 1 keeps the indexer keys in MXFP4 (CSA2_IDX_MXFP4)."""
+    return Config(n_heads, head_dim, idx_heads, idx_dim, topk, swa, ratio, layout, idx_layout)
 
 
 class AttnOpts(ctypes.Structure):
@@ -58,7 +60,8 @@ class CacheViews(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("idx_k", ctypes.c_void_p), ("lengths", ctypes.c_void_p),
                 ("entry_offset", ctypes.POINTER(ctypes.c_int64)), ("total", ctypes.c_int64),
-                ("batch", ctypes.c_int32), ("group", ctypes.c_int32)]
+                ("batch", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("idx_codes", ctypes.c_void_p), ("idx_scales", ctypes.c_void_p)]
 
 
 def _load():
@@ -189,10 +192,13 @@ class Cache:
             return self.buffer[o:o + nbytes]
 
         g = v.group
+        mx = bool(v.idx_codes)
         return {
             "codes": sl(v.codes, total * 256).view(total, 256),
             "scales": sl(v.scales, total * (512 // g)).view(total, 512 // g),
-            "idx_k": sl(v.idx_k, total * 256).view(torch.bfloat16).view(total, 128),
+            "idx_k": None if mx else sl(v.idx_k, total * 256).view(torch.bfloat16).view(total, 128),
+            "idx_codes": sl(v.idx_codes, total * 64).view(total, 64) if mx else None,
+            "idx_scales": sl(v.idx_scales, total * 4).view(total, 4) if mx else None,
             "lengths": sl(v.lengths, 4 * self.batch).view(torch.int32),
             "entry_offset": [v.entry_offset[i] for i in range(self.batch + 1)],
             "group": g,

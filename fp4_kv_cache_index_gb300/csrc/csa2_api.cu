@@ -31,7 +31,9 @@ struct csa2_cache {
   uint32_t* d_err;
   uint8_t* codes;
   uint8_t* scales;
-  uint16_t* idxk;
+  uint16_t* idxk;       // CSA2_IDX_BF16 keys
+  uint8_t* idx_codes;   // CSA2_IDX_MXFP4 keys: codes [total, 64], scales [total, 4]
+  uint8_t* idx_scales;
   CUtensorMap tm_k;    // indexer keys, 128-row boxes (contiguous tiles)
   CUtensorMap tm_k8;   // indexer keys, one 8-key block per box (pool mode)
   int num_sms;
@@ -54,11 +56,12 @@ csa2_status_t check_cfg(const csa2_config_t* c) {
   if (c->swa < 0 || c->swa > 128) return CSA2_ERR_UNSUPPORTED;
   if (c->ratio < 1 || c->ratio > 16) return CSA2_ERR_UNSUPPORTED;
   if (c->layout != CSA2_KV_L32_UE8M0 && c->layout != CSA2_KV_L16_E4M3) return CSA2_ERR_UNSUPPORTED;
+  if (c->idx_layout != CSA2_IDX_BF16 && c->idx_layout != CSA2_IDX_MXFP4) return CSA2_ERR_UNSUPPORTED;
   return CSA2_OK;
 }
 
 struct Layout {
-  size_t len_off, err_off, codes_off, scales_off, idxk_off, total;
+  size_t len_off, err_off, codes_off, scales_off, idxk_off, idxs_off, total;
 };
 
 Layout layout_for(const csa2_config_t* c, int64_t total) {
@@ -77,7 +80,16 @@ Layout layout_for(const csa2_config_t* c, int64_t total) {
   L.scales_off = o;
   o = align_up(o + (size_t)total * (kHeadDim / g), kAlign);
   L.idxk_off = o;
-  o = align_up(o + (size_t)total * kIdxDim * 2, kAlign);
+  if (c->idx_layout == CSA2_IDX_MXFP4) {
+    o = align_up(o + (size_t)total * (kIdxDim / 2), kAlign);   // E2M1 codes
+    L.idxs_off = o;
+    // UE8M0 scales; 16 spare bytes: the indexer copies 16-byte aligned
+    // windows of scale words, up to 3 rows past the last one
+    o = align_up(o + (size_t)total * (kIdxDim / 32) + 16, kAlign);
+  } else {
+    o = align_up(o + (size_t)total * kIdxDim * 2, kAlign);
+    L.idxs_off = 0;
+  }
   L.total = o;
   return L;
 }
@@ -139,6 +151,19 @@ csa2_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : C
 
 int64_t score_ld(int64_t n) { return std::max<int64_t>(4, (n + 3) / 4 * 4); }
 
+// The indexer kernel for the cache's key storage (bf16 keys by TMA, or
+// MXFP4 keys by bulk copy and on-chip dequantisation).
+cudaError_t launch_index_any(const csa2_cache* c, IndexParams& ip, const CUtensorMap& tm_q,
+                             int grid, cudaStream_t s) {
+  if (c->cfg.idx_layout == CSA2_IDX_MXFP4) {
+    ip.idx_codes = c->idx_codes;
+    ip.idx_scales = c->idx_scales;
+    ip.idx_total = c->total;
+    return launch_index_fp4(ip, tm_q, grid, s);
+  }
+  return launch_index(ip, c->tm_k, tm_q, grid, s);
+}
+
 // Append / compress segments: rows of one launch grouped by sequence.
 csa2_status_t run_append(csa2_cache* c, int mode, int32_t n_seqs, const int32_t* seq_ids,
                          const int32_t* n_rows_in, const float* entries, const void* c_tok,
@@ -183,6 +208,9 @@ csa2_status_t run_append(csa2_cache* c, int mode, int32_t n_seqs, const int32_t*
     p.codes = c->codes;
     p.scales = c->scales;
     p.cache_idxk = c->idxk;
+    p.idx_mxfp4 = c->cfg.idx_layout == CSA2_IDX_MXFP4 ? 1 : 0;
+    p.idx_codes = c->idx_codes;
+    p.idx_scales = c->idx_scales;
     p.d_len = c->d_len;
     int64_t rows = 0;
     while (i < n_seqs && p.n_segs < kMaxAppendSegs) {
@@ -274,15 +302,18 @@ csa2_status_t csa2_cache_create(const csa2_config_t* cfg, int32_t batch, const i
   c->d_err = reinterpret_cast<uint32_t*>(c->base + L.err_off);
   c->codes = c->base + L.codes_off;
   c->scales = c->base + L.scales_off;
-  c->idxk = reinterpret_cast<uint16_t*>(c->base + L.idxk_off);
+  const bool mx = cfg->idx_layout == CSA2_IDX_MXFP4;
+  c->idxk = mx ? nullptr : reinterpret_cast<uint16_t*>(c->base + L.idxk_off);
+  c->idx_codes = mx ? c->base + L.idxk_off : nullptr;
+  c->idx_scales = mx ? c->base + L.idxs_off : nullptr;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     delete c;
     return CSA2_ERR_CUDA;
   }
-  if (!make_map(&c->tm_k, c->idxk, (uint64_t)c->total, kIdxDim, 64, 128) ||
-      !make_block_map(&c->tm_k8, c->idxk, (uint64_t)c->total)) {
+  if (!mx && (!make_map(&c->tm_k, c->idxk, (uint64_t)c->total, kIdxDim, 64, 128) ||
+              !make_block_map(&c->tm_k8, c->idxk, (uint64_t)c->total))) {
     delete c;
     return CSA2_ERR_CUDA;
   }
@@ -317,6 +348,8 @@ csa2_status_t csa2_cache_views(const csa2_cache_t* c, csa2_cache_views_t* v) {
   v->codes = c->codes;
   v->scales = c->scales;
   v->idx_k = c->idxk;
+  v->idx_codes = c->idx_codes;
+  v->idx_scales = c->idx_scales;
   v->lengths = c->d_len;
   v->entry_offset = c->off.data();
   v->total = c->total;
@@ -481,7 +514,7 @@ csa2_status_t run_index_decode(const csa2_cache_t* c, int32_t nq, const void* q_
     const int tiles = ip->tile_prefix[n];
     if (tiles > 0) {
       const int grid = std::min(c->num_sms, tiles);
-      if (launch_index(*ip, c->tm_k, tm_q, grid, S(stream)) != cudaSuccess) return CSA2_ERR_CUDA;
+      if (launch_index_any(c, *ip, tm_q, grid, S(stream)) != cudaSuccess) return CSA2_ERR_CUDA;
     }
   }
   return CSA2_OK;
@@ -656,7 +689,7 @@ csa2_status_t csa2_index_scores_prefill(const csa2_cache_t* c, int32_t seq, int3
     const int tiles = ip->tile_prefix[groups];
     if (tiles > 0) {
       const int grid = std::min(c->num_sms, tiles);
-      if (launch_index(*ip, c->tm_k, tm_q, grid, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
+      if (launch_index_any(c, *ip, tm_q, grid, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
     }
   }
   delete ip;
@@ -996,6 +1029,7 @@ csa2_status_t csa2_index_topk_reindex_decode(const csa2_cache_t* c, int32_t nq, 
                                              csa2_stream_t stream) {
   if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
   if (max_blocks <= 0 || max_blocks % 16 != 0 || max_blocks > 4096) return CSA2_ERR_UNSUPPORTED;
+  if (c->cfg.idx_layout != CSA2_IDX_BF16) return CSA2_ERR_UNSUPPORTED;   // pool mode: bf16 keys
   if (nq == 0) return CSA2_OK;
   csa2_status_t st = check_decode_queries(c, nq, q_idx, w, seq_ids);
   if (st != CSA2_OK) return st;

@@ -104,6 +104,17 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, int
       : "memory");
 }
 
+// 1-D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of
+// 16), completion on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Generic-proxy shared-memory writes become visible to the async proxy
 // (tensor core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -301,6 +312,14 @@ __device__ __forceinline__ void e2m1x8_to_bf16x8(uint32_t codes, uint32_t (&out)
   out[1] = prmt(l0, h0, 0x7362u);
   out[2] = prmt(l1, h1, 0x5140u);
   out[3] = prmt(l1, h1, 0x7362u);
+}
+
+// Value of an E2M1 code (sign bit 3): 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+__device__ __forceinline__ float e2m1_value(uint32_t code) {
+  const uint32_t m = code & 7u;
+  const float mag = (m < 2u) ? 0.5f * (float)m : __uint_as_float((126u + (m >> 1)) << 23) *
+                                                  (1.0f + 0.5f * (float)(m & 1u));
+  return (code & 8u) ? -mag : mag;
 }
 
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {

@@ -43,6 +43,9 @@ struct AppendParams {
   uint8_t* codes;
   uint8_t* scales;
   uint16_t* cache_idxk;
+  int32_t idx_mxfp4;         // 1: indexer keys quantised to MXFP4 (codes + scales below)
+  uint8_t* idx_codes;
+  uint8_t* idx_scales;
   int32_t* d_len;
 };
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
@@ -55,6 +58,9 @@ struct IndexParams {
   int64_t ld;
   uint32_t* key_hist;      // nullable [nq, 2048] score-key histogram (qpg == 1 only)
   int32_t score_bf16;      // 1: scores are stored as bf16 (uint16 [nq, ld], nearest even)
+  const uint8_t* idx_codes;  // MXFP4 keys (k_index_fp4): E2M1 codes [idx_total, 64]
+  const uint8_t* idx_scales; // MXFP4 keys: UE8M0 scales [idx_total, 4] (+ 16 bytes of padding)
+  int64_t idx_total;         // MXFP4 keys: rows in the cache
   const int32_t* pool;     // nullable: pool mode, [nq, pool_blocks] block ids (-1 unused)
   int32_t pool_blocks;     // blocks per pool row (multiple of 16)
   uint32_t* err;
@@ -73,6 +79,9 @@ struct IndexParams {
 int index_smem_bytes(int qpg);
 cudaError_t launch_index(const IndexParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_q,
                          int grid, cudaStream_t s);
+int index_fp4_smem_bytes(int qpg);
+cudaError_t launch_index_fp4(const IndexParams& p, const CUtensorMap& tm_q, int grid,
+                             cudaStream_t s);
 
 // ---------------------------------------------------------------- HSI
 constexpr int kHsiBlock = 8;   // positions per block of the candidate pool

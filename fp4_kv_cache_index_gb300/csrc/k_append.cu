@@ -127,9 +127,27 @@ __global__ void __launch_bounds__(256) k_append(const __grid_constant__ AppendPa
   }
   *reinterpret_cast<uint2*>(p.codes + dst * kCodeBytes + lane * 8) = make_uint2(lo, hi);
 
-  // ---- indexer key row (256 B): 8 bytes per lane
-  const uint2* ks = reinterpret_cast<const uint2*>(p.idx_k + src * kIdxDim);
-  reinterpret_cast<uint2*>(p.cache_idxk + dst * kIdxDim)[lane] = __ldg(ks + lane);
+  // ---- indexer key row: 4 channels per lane
+  const uint2 kw = __ldg(reinterpret_cast<const uint2*>(p.idx_k + src * kIdxDim) + lane);
+  if (!p.idx_mxfp4) {
+    reinterpret_cast<uint2*>(p.cache_idxk + dst * kIdxDim)[lane] = kw;
+    return;
+  }
+  // MXFP4 (V4.1 report, section 2.4.4): the 32-channel block of this lane is
+  // held by 8 lanes; the scale and codes follow the L32 rule above
+  const float k4[4] = {__uint_as_float(kw.x << 16), __uint_as_float(kw.x & 0xFFFF0000u),
+                       __uint_as_float(kw.y << 16), __uint_as_float(kw.y & 0xFFFF0000u)};
+  float ka = fmaxf(fmaxf(fabsf(k4[0]), fabsf(k4[1])), fmaxf(fabsf(k4[2]), fabsf(k4[3])));
+  ka = fmaxf(ka, __shfl_xor_sync(0xffffffffu, ka, 1));
+  ka = fmaxf(ka, __shfl_xor_sync(0xffffffffu, ka, 2));
+  ka = fmaxf(ka, __shfl_xor_sync(0xffffffffu, ka, 4));
+  const uint32_t kb = ue8m0_for_amax(ka);
+  const float ks = ue8m0_value(kb);
+  uint32_t kc = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) kc |= e2m1_encode(__fdiv_rn(k4[i], ks)) << (4 * i);
+  reinterpret_cast<uint16_t*>(p.idx_codes + dst * (kIdxDim / 2))[lane] = (uint16_t)kc;
+  if ((lane & 7) == 0) p.idx_scales[dst * (kIdxDim / 32) + (lane >> 3)] = (uint8_t)kb;
 }
 
 }  // namespace

@@ -1,0 +1,393 @@
+// k_index_fp4.cu -- CSA2 indexer scores over MXFP4 indexer keys and queries.
+//
+// The V4.1 report (section 2.4.4) keeps the indexer's queries and keys in
+// OCP MXFP4: E2M1 codes with one power-of-two (UE8M0) scale per 32
+// channels, 64 + 4 bytes per 128-channel key (the 68 B of the cache-size
+// breakdown).  The score is the one of the bf16 indexer,
+//     I[q, s] = sum_h w[q, h] * ReLU(q^[q, h] . K^[s]),
+// over the dequantised values q^, K^ (every E2M1 code times its power-of-
+// two scale is a bf16 value, so the dequantisation is exact and the tensor
+// cores compute the same products).
+//
+// Warp roles (448 threads):
+//   warp 0      bulk-copies the raw tiles (128 keys: 8 KB of codes and their
+//               scale words) into a 4-deep ring, and the query tile (TMA);
+//   warps 10-13 convert each raw tile into a 128B-swizzled bf16 K-major
+//               stage (E2M1 -> bf16 by byte permutes, times the scale), and
+//               at every new query group round the query tile in shared
+//               memory to the MXFP4 grid (per head, 32-channel blocks);
+//   warp 1      issues the tcgen05 MMAs (M = 128 keys, N = 32 heads x qpg,
+//               K = 128) from the converted stage and the rounded queries;
+//   warps 2-9   the epilogue of the bf16 indexer (ReLU, head weights, fp32
+//               or bf16 score store, score-key histogram).
+// Every wait is bounded.
+#include "csa2_device.cuh"
+#include "csa2_kernels.h"
+
+namespace csa2 {
+namespace {
+
+constexpr int kTileE = 128;
+constexpr int kRawStages = 4;
+constexpr int kStages = 3;                              // converted bf16 stages
+constexpr int kKStageBytes = kTileE * kIdxDim * 2;      // 32 KB
+constexpr int kRawCodeBytes = kTileE * kIdxDim / 2;     // 8 KB
+constexpr int kRawScaleBytes = 544;                     // (128 + 4) words, 16-byte padded
+constexpr int kRawStageBytes = kRawCodeBytes + kRawScaleBytes;
+constexpr int kThreads = 448;
+constexpr int kEpiThreads = 256;   // warps 2-9
+constexpr int kCvtThreads = 128;   // warps 10-13
+constexpr int kCvtBase = 320;
+
+struct SmemLayout {
+  int raw_off, q_off, w_off, hist_off, bar_off, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int qpg) {
+  SmemLayout L;
+  L.raw_off = kStages * kKStageBytes;
+  L.q_off = L.raw_off + kRawStages * kRawStageBytes;
+  L.q_off = (L.q_off + 1023) & ~1023;
+  L.w_off = L.q_off + qpg * 32 * kIdxDim * 2;
+  L.hist_off = L.w_off + qpg * 32 * 4;
+  L.bar_off = L.hist_off + kKeyHistBins * 4;
+  L.total = L.bar_off + 32 * 8 + 16 + 1024;  // barriers, tmem slot, alignment slack
+  return L;
+}
+
+__device__ __forceinline__ int group_nvis_query(const IndexParams& p, int g, int j) {
+  if (!p.prefill) return p.nvis[g];
+  const int64_t q = (int64_t)g * p.qpg + j;
+  const int64_t v = (p.pos0 + q + 1) / p.ratio;
+  return (int)(v < p.pre_len ? v : p.pre_len);
+}
+
+__device__ __forceinline__ int64_t group_base(const IndexParams& p, int g) {
+  return p.prefill ? p.pre_base : p.entry_base[g];
+}
+
+// First key row of item `it` in group g, the keys it copies (the cache ends
+// at p.idx_total rows) and the first row of its 16-byte aligned scale window.
+struct TileRows {
+  int64_t row0, s0;
+  int32_t nrows;
+};
+__device__ __forceinline__ TileRows tile_rows(const IndexParams& p, int g, int t) {
+  TileRows r;
+  r.row0 = group_base(p, g) + (int64_t)t * kTileE;
+  const int64_t left = p.idx_total - r.row0;
+  r.nrows = (int32_t)(left < kTileE ? left : kTileE);
+  r.s0 = r.row0 & ~(int64_t)3;
+  return r;
+}
+
+// Rounds the 32 channels of block b of query row r (bf16, 128B-swizzled, two
+// 64-channel halves) to the MXFP4 grid in place: UE8M0 scale of the block's
+// largest magnitude (OCP MX), E2M1 code of x / scale (nearest, ties to
+// even, saturating), value = code * scale.
+__device__ __forceinline__ void round_query_block(uint8_t* qbuf, int qrows, int r, int b) {
+  uint8_t* half = qbuf + (b >> 1) * (qrows * 128) + r * 128;
+  uint4 w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int chunk = (b & 1) * 4 + k;
+    w[k] = *reinterpret_cast<const uint4*>(half + ((chunk ^ (r & 7)) << 4));
+  }
+  float x[32];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t u[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[8 * k + 2 * i] = __uint_as_float(u[i] << 16);
+      x[8 * k + 2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+    }
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  const float sc = ue8m0_value(ue8m0_for_amax(amax));
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float a = e2m1_value(e2m1_encode(__fdiv_rn(x[8 * k + 2 * i], sc))) * sc;
+      const float c = e2m1_value(e2m1_encode(__fdiv_rn(x[8 * k + 2 * i + 1], sc))) * sc;
+      u[i] = float_to_bf16_bits(a) | (float_to_bf16_bits(c) << 16);
+    }
+    const int chunk = (b & 1) * 4 + k;
+    *reinterpret_cast<uint4*>(half + ((chunk ^ (r & 7)) << 4)) = make_uint4(u[0], u[1], u[2], u[3]);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_index_fp4(const __grid_constant__ IndexParams p, const __grid_constant__ CUtensorMap tm_q) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const SmemLayout L = smem_layout(p.qpg);
+  uint8_t* kbuf = smem;
+  uint8_t* raw = smem + L.raw_off;
+  uint8_t* qbuf = smem + L.q_off;
+  float* wbuf = reinterpret_cast<float*>(smem + L.w_off);
+  uint32_t* hs = reinterpret_cast<uint32_t*>(smem + L.hist_off);  // score-key histogram
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+  uint64_t* raw_full = bars;            // [kRawStages]
+  uint64_t* raw_empty = bars + 4;       // [kRawStages]
+  uint64_t* k_full = bars + 8;          // [kStages]
+  uint64_t* k_empty = bars + 12;        // [kStages]
+  uint64_t* acc_full = bars + 16;       // [2]
+  uint64_t* acc_empty = bars + 18;      // [2]
+  uint64_t* q_full = bars + 20;
+  uint64_t* q_ready = bars + 21;
+  uint64_t* q_empty = bars + 22;
+  uint64_t* drain = bars + 23;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 32);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = 32 * p.qpg;               // MMA N (columns per accumulator)
+  const int qrows = 32 * p.qpg;
+  const uint32_t tmem_cols = (N * 2 <= 32) ? 32u : (uint32_t)(N * 2);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRawStages; ++i) {
+      mbar_init(raw_full + i, 1);
+      mbar_init(raw_empty + i, kCvtThreads);
+    }
+    for (int i = 0; i < kStages; ++i) { mbar_init(k_full + i, kCvtThreads); mbar_init(k_empty + i, 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, kEpiThreads); }
+    mbar_init(q_full, 1);
+    mbar_init(q_ready, kCvtThreads);
+    mbar_init(q_empty, 1);
+    mbar_init(drain, 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&tm_q);
+  }
+  if (warp == 1) { tmem_alloc(tmem_slot, tmem_cols); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total = p.tile_prefix[p.n_groups];
+  const int begin = (int)(((int64_t)total * blockIdx.x) / gridDim.x);
+  const int end = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
+  int g0 = 0;
+  while (g0 < p.n_groups && p.tile_prefix[g0 + 1] <= begin) ++g0;
+
+  if (warp == 0 && lane == 0 && begin < end) {
+    // ------------------------------------------------ bulk-copy producer
+    int g = g0, cur = -1, rs = 0;
+    uint32_t rph = 0, qph = 0;
+    uint32_t armed = 0, armed_ph = 0;   // raw stages filled at least once, parity of the last fill
+    bool ok = true;
+    for (int it = begin; it < end && ok; ++it) {
+      while (p.tile_prefix[g + 1] <= it) ++g;
+      if (g != cur) {
+        ok = mbar_wait(q_empty, qph ^ 1, p.err);
+        qph ^= 1;
+        if (!ok) break;
+        mbar_arrive_expect_tx(q_full, (uint32_t)(qrows * kIdxDim * 2));
+        tma_load_2d(qbuf, &tm_q, 0, g * qrows, q_full);
+        tma_load_2d(qbuf + qrows * 128, &tm_q, 64, g * qrows, q_full);
+        cur = g;
+      }
+      ok = mbar_wait(raw_empty + rs, rph ^ 1, p.err);
+      if (!ok) break;
+      const TileRows tr = tile_rows(p, g, it - p.tile_prefix[g]);
+      const int64_t s1 = (tr.row0 + tr.nrows + 3) & ~(int64_t)3;
+      const uint32_t code_bytes = (uint32_t)tr.nrows * (kIdxDim / 2);
+      const uint32_t scale_bytes = (uint32_t)(s1 - tr.s0) * 4u;
+      uint8_t* dst = raw + rs * kRawStageBytes;
+      mbar_arrive_expect_tx(raw_full + rs, code_bytes + scale_bytes);
+      bulk_load(dst, p.idx_codes + tr.row0 * (kIdxDim / 2), code_bytes, raw_full + rs);
+      bulk_load(dst + kRawCodeBytes, p.idx_scales + tr.s0 * 4, scale_bytes, raw_full + rs);
+      armed |= 1u << rs;
+      armed_ph = (armed_ph & ~(1u << rs)) | (rph << rs);
+      if (++rs == kRawStages) { rs = 0; rph ^= 1; }
+    }
+    // make sure no bulk copy is still writing into this CTA's shared memory
+    for (int s = 0; s < kRawStages; ++s)
+      if (armed & (1u << s)) mbar_wait(raw_full + s, (armed_ph >> s) & 1u, p.err);
+    if (cur >= 0) mbar_wait(q_full, qph ^ 1, p.err);
+  } else if (warp >= 10 && begin < end) {
+    // ------------------------------------------------ converters
+    const int ct = threadIdx.x - kCvtBase;          // 0..127
+    const int cw = ct >> 5;                         // converter warp 0..3
+    const int b = ct & 3;                           // 32-channel block of the key
+    int g = g0, cur = -1, rs = 0, ks = 0;
+    uint32_t rph = 0, kph = 0, qph = 0;
+    bool ok = true;
+    for (int it = begin; it < end && ok; ++it) {
+      while (p.tile_prefix[g + 1] <= it) ++g;
+      if (g != cur) {
+        // a new query tile: onto the MXFP4 grid before its first MMA
+        ok = mbar_wait(q_full, qph, p.err);
+        qph ^= 1;
+        if (!ok) break;
+        for (int i = ct; i < qrows * 4; i += kCvtThreads) round_query_block(qbuf, qrows, i >> 2, i & 3);
+        fence_proxy_async_smem();
+        mbar_arrive(q_ready);
+        cur = g;
+      }
+      ok = mbar_wait(raw_full + rs, rph, p.err) && mbar_wait(k_empty + ks, kph ^ 1, p.err);
+      if (!ok) break;
+      tc_fence_after();
+      const TileRows tr = tile_rows(p, g, it - p.tile_prefix[g]);
+      const uint8_t* src = raw + rs * kRawStageBytes;
+      const uint32_t* sw = reinterpret_cast<const uint32_t*>(src + kRawCodeBytes) + (tr.row0 - tr.s0);
+      uint8_t* dst = kbuf + ks * kKStageBytes + (b >> 1) * (kKStageBytes / 2);
+#pragma unroll 1
+      for (int pass = 0; pass < 4; ++pass) {
+        const int r = pass * 32 + cw * 8 + (lane >> 2);   // key row of the tile
+        uint4 c4 = make_uint4(0u, 0u, 0u, 0u);
+        uint32_t s2 = 0u;
+        if (r < tr.nrows) {
+          c4 = *reinterpret_cast<const uint4*>(src + r * (kIdxDim / 2) + b * 16);
+          const uint32_t s16 = float_to_bf16_bits(ue8m0_value((sw[r] >> (8 * b)) & 0xFFu));
+          s2 = s16 | (s16 << 16);
+        }
+        const uint32_t words[4] = {c4.x, c4.y, c4.z, c4.w};
+        uint8_t* rowp = dst + r * 128;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint32_t v[4];
+          e2m1x8_to_bf16x8(words[k], v);
+          uint4 o;
+          o.x = bf16x2_mul(v[0], s2); o.y = bf16x2_mul(v[1], s2);
+          o.z = bf16x2_mul(v[2], s2); o.w = bf16x2_mul(v[3], s2);
+          const int chunk = (b & 1) * 4 + k;
+          *reinterpret_cast<uint4*>(rowp + ((chunk ^ (r & 7)) << 4)) = o;
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(k_full + ks);
+      mbar_arrive(raw_empty + rs);
+      if (++rs == kRawStages) { rs = 0; rph ^= 1; }
+      if (++ks == kStages) { ks = 0; kph ^= 1; }
+    }
+  } else if (warp == 1 && lane == 0 && begin < end) {
+    // ------------------------------------------------ MMA issuer
+    const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)N, false, false);
+    int g = g0, cur = -1, stage = 0, acc = 0;
+    uint32_t ph = 0, qph = 0, aph = 0;
+    bool ok = true;
+    for (int it = begin; it < end && ok; ++it) {
+      while (p.tile_prefix[g + 1] <= it) ++g;
+      if (g != cur) {
+        ok = mbar_wait(q_ready, qph, p.err);
+        qph ^= 1;
+        if (!ok) break;
+        cur = g;
+      }
+      ok = mbar_wait(k_full + stage, ph, p.err) && mbar_wait(acc_empty + acc, aph ^ 1, p.err);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(kbuf + stage * kKStageBytes);
+      const uint32_t b0 = smem_u32(qbuf);
+      const uint32_t d = tmem_base + (uint32_t)(acc * N);
+#pragma unroll
+      for (int ks = 0; ks < kIdxDim / 16; ++ks) {
+        const uint32_t ao = (uint32_t)((ks >> 2) * (kKStageBytes / 2) + (ks & 3) * 32);
+        const uint32_t bo = (uint32_t)((ks >> 2) * (qrows * 128) + (ks & 3) * 32);
+        umma_bf16(d, sdesc_sw128(a0 + ao, 16, 1024), sdesc_sw128(b0 + bo, 16, 1024), idesc,
+                  ks > 0 ? 1u : 0u);
+      }
+      umma_commit(k_empty + stage);
+      umma_commit(acc_full + acc);
+      const bool last_of_group = (it + 1 == end) || (p.tile_prefix[g + 1] <= it + 1);
+      if (last_of_group) umma_commit(q_empty);
+      if (++stage == kStages) { stage = 0; ph ^= 1; }
+      if (++acc == 2) { acc = 0; aph ^= 1; }
+    }
+    umma_commit(drain);
+    mbar_wait(drain, 0, p.err);
+  } else if (warp >= 2 && warp < 10) {
+    // ------------------------------------------------ epilogue
+    const int quad = warp & 3;                 // TMEM lane quadrant of this warp
+    const int row = quad * 32 + lane;          // entry within the tile
+    const int et = threadIdx.x - 64;           // 0..255
+    const int half = (warp - 2) >> 2;          // which queries of the group
+    const int jq = (p.qpg + 1) >> 1;
+    const int j0 = half * jq, j1 = min(p.qpg, j0 + jq);
+    const bool use_hist = p.key_hist != nullptr && p.qpg == 1;
+    auto flush = [&](int qq) {
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      for (int i = et; i < kKeyHistBins; i += kEpiThreads) {
+        const uint32_t v = hs[i];
+        if (v) atomicAdd(p.key_hist + (int64_t)qq * kKeyHistBins + i, v);
+        hs[i] = 0u;
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+    };
+    if (use_hist) {
+      for (int i = et; i < kKeyHistBins; i += kEpiThreads) hs[i] = 0u;
+    }
+    int g = g0, cur = -1, acc = 0;
+    uint32_t aph = 0;
+    for (int it = begin; it < end; ++it) {
+      while (p.tile_prefix[g + 1] <= it) ++g;
+      if (g != cur) {
+        if (use_hist && cur >= 0) flush(cur);
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        for (int i = et; i < qrows; i += kEpiThreads) {
+          const int q = g * p.qpg + (i >> 5);
+          wbuf[i] = (q < p.nq) ? __ldg(p.w + (int64_t)q * kIdxHeads + (i & 31)) : 0.0f;
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        cur = g;
+      }
+      if (!mbar_wait(acc_full + acc, aph, p.err)) break;
+      tc_fence_after();
+      const int t = it - p.tile_prefix[g];
+      const int e = t * kTileE + row;
+      for (int j = j0; j < j1; ++j) {
+        uint32_t r[32];
+        tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * N + j * 32), r);
+        const float* wj = wbuf + j * 32;
+        float s = 0.0f;
+#pragma unroll
+        for (int h = 0; h < 32; ++h) s = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.0f), s);
+        const int q = g * p.qpg + j;
+        if (q < p.nq && e < group_nvis_query(p, g, j)) {
+          if (p.score_bf16) {
+            const uint32_t bb = float_to_bf16_bits(s);
+            reinterpret_cast<uint16_t*>(p.scores)[(int64_t)q * p.ld + e] = (uint16_t)bb;
+            if (use_hist) atomicAdd(hs + (score_key(bf16_bits_to_float(bb)) >> 21), 1u);
+          } else {
+            p.scores[(int64_t)q * p.ld + e] = s;
+            if (use_hist) atomicAdd(hs + (score_key(s) >> 21), 1u);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(acc_empty + acc);
+      if (++acc == 2) { acc = 0; aph ^= 1; }
+    }
+    if (use_hist && cur >= 0) flush(cur);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, tmem_cols);
+  }
+}
+
+}  // namespace
+
+int index_fp4_smem_bytes(int qpg) { return smem_layout(qpg).total; }
+
+cudaError_t launch_index_fp4(const IndexParams& p, const CUtensorMap& tm_q, int grid,
+                             cudaStream_t s) {
+  const int smem = index_fp4_smem_bytes(p.qpg);
+  cudaError_t e = cudaFuncSetAttribute(k_index_fp4, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem);
+  if (e != cudaSuccess) return e;
+  k_index_fp4<<<grid, kThreads, smem, s>>>(p, tm_q);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

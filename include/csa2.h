@@ -80,7 +80,16 @@ typedef struct {
   int32_t swa;
   int32_t ratio;
   int32_t layout; /* csa2_kv_layout_t */
+  int32_t idx_layout; /* csa2_idx_layout_t */
 } csa2_config_t;
+
+/* Indexer-key storage.  CSA2_IDX_BF16: 128 bf16 channels (256 B/entry).
+ * CSA2_IDX_MXFP4 ([V41 sec 2.4.4]: FP4 indexer queries and keys in OCP
+ * MXFP4; the 68 B per key of [NDT sec 3.1]): E2M1 codes (64 B, even channel
+ * in the low nibble) + one UE8M0 scale per 32 channels (4 B), the scale
+ * rule of CSA2_KV_L32_UE8M0; the indexer then also rounds each query head
+ * to the MXFP4 grid before scoring.                                        */
+typedef enum { CSA2_IDX_BF16 = 0, CSA2_IDX_MXFP4 = 1 } csa2_idx_layout_t;
 
 typedef struct csa2_cache csa2_cache_t; /* opaque host handle, one per group */
 
@@ -89,12 +98,14 @@ typedef struct csa2_cache csa2_cache_t; /* opaque host handle, one per group */
 typedef struct {
   uint8_t* codes;        /* dev [total, head_dim / 2]                         */
   uint8_t* scales;       /* dev [total, head_dim / group]                     */
-  void* idx_k;           /* dev bf16 [total, idx_dim]                         */
+  void* idx_k;           /* CSA2_IDX_BF16: dev bf16 [total, idx_dim], else NULL */
   int32_t* lengths;      /* dev [batch]: entries appended so far              */
   const int64_t* entry_offset; /* host [batch + 1]                           */
   int64_t total;         /* sum of capacities                                 */
   int32_t batch;
   int32_t group;         /* 32 or 16 channels per scale                       */
+  uint8_t* idx_codes;    /* CSA2_IDX_MXFP4: dev [total, idx_dim / 2], else NULL */
+  uint8_t* idx_scales;   /* CSA2_IDX_MXFP4: dev [total, idx_dim / 32], else NULL */
 } csa2_cache_views_t;
 
 int32_t csa2_version(void);
