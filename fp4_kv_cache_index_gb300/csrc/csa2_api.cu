@@ -1124,7 +1124,7 @@ csa2_status_t csa2_get_device_error(const csa2_cache_t* c, csa2_stream_t stream,
   if (word && cudaMemsetAsync(c->d_err, 0, sizeof(uint32_t), S(stream)) != cudaSuccess)
     return CSA2_ERR_CUDA;
   *device_status = (word & kErrTimeoutBit) ? CSA2_ERR_TIMEOUT
-                   : (word & kErrIndexBit) ? CSA2_ERR_DEVICE
+                   : (word & (kErrIndexBit | kErrRangeBit)) ? CSA2_ERR_DEVICE
                                            : CSA2_OK;
   return CSA2_OK;
 }

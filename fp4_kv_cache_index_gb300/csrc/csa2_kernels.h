@@ -11,6 +11,7 @@ namespace csa2 {
 // Sticky device error word bits (see csa2_get_device_error).
 constexpr uint32_t kErrTimeoutBit = 1u;
 constexpr uint32_t kErrIndexBit = 2u;
+constexpr uint32_t kErrRangeBit = 4u;   // an MXFP4 indexer scale outside 2^-13 .. 2^13
 
 constexpr int kHeadDim = 512;     // main-KV latent / attention head dim
 constexpr int kIdxDim = 128;      // indexer head dim

@@ -5,19 +5,23 @@
 // channels, 64 + 4 bytes per 128-channel key (the 68 B of the cache-size
 // breakdown).  The score is the one of the bf16 indexer,
 //     I[q, s] = sum_h w[q, h] * ReLU(q^[q, h] . K^[s]),
-// over the dequantised values q^, K^ (every E2M1 code times its power-of-
-// two scale is a bf16 value, so the dequantisation is exact and the tensor
-// cores compute the same products).
+// over the dequantised values q^, K^.  An E2M1 value times a scale 2^e is
+// exactly an E5M2 value for e in [-13, 13], so both operands become E5M2
+// bytes (a byte permute per four codes through a per-block table) and the
+// tensor cores take them as kind::f8f6f4 with fp32 accumulation: the same
+// products as the dequantised values, one byte per channel in shared
+// memory.  A block scale outside that range (values below 2^-14 or above
+// 2^16) is clamped into it and reported in the device error word.
 //
-// Warp roles (448 threads):
+// Warp roles (576 threads):
 //   warp 0      bulk-copies the raw tiles (128 keys: 8 KB of codes and their
-//               scale words) into a 4-deep ring, and the query tile (TMA);
-//   warps 10-13 convert each raw tile into a 128B-swizzled bf16 K-major
-//               stage (E2M1 -> bf16 by byte permutes, times the scale), and
-//               at every new query group round the query tile in shared
-//               memory to the MXFP4 grid (per head, 32-channel blocks);
+//               scale words) into a ring 12 deep in decode (4 in prefill,
+//               whose 8-query tiles need the room), and the query tile (TMA);
+//   warps 10-17 convert each raw tile into a 128B-swizzled E5M2 K-major
+//               stage, and at every new query group take the query tile
+//               (bf16) to the MXFP4 grid and on to E5M2;
 //   warp 1      issues the tcgen05 MMAs (M = 128 keys, N = 32 heads x qpg,
-//               K = 128) from the converted stage and the rounded queries;
+//               K = 128 as 4 x 32) from the converted stage and queries;
 //   warps 2-9   the epilogue of the bf16 indexer (ReLU, head weights, fp32
 //               or bf16 score store, score-key histogram).
 // Every wait is bounded.
@@ -28,30 +32,35 @@ namespace csa2 {
 namespace {
 
 constexpr int kTileE = 128;
-constexpr int kRawStages = 4;
-constexpr int kStages = 3;                              // converted bf16 stages
-constexpr int kKStageBytes = kTileE * kIdxDim * 2;      // 32 KB
+constexpr int kRawStagesMax = 12;   // raw ring depth: 12 for decode, 4 for prefill
+constexpr int kStages = 4;                              // converted E5M2 stages
+constexpr int kKStageBytes = kTileE * kIdxDim;          // 16 KB
 constexpr int kRawCodeBytes = kTileE * kIdxDim / 2;     // 8 KB
 constexpr int kRawScaleBytes = 544;                     // (128 + 4) words, 16-byte padded
 constexpr int kRawStageBytes = kRawCodeBytes + kRawScaleBytes;
-constexpr int kThreads = 448;
+constexpr int kThreads = 576;
 constexpr int kEpiThreads = 256;   // warps 2-9
-constexpr int kCvtThreads = 128;   // warps 10-13
+constexpr int kCvtThreads = 256;   // warps 10-17
 constexpr int kCvtBase = 320;
+constexpr int kCvtWarps = kCvtThreads / 32;
+constexpr int kEpiWarps = kEpiThreads / 32;
+
+__host__ __device__ inline int raw_stages(int qpg) { return qpg == 1 ? kRawStagesMax : 4; }
 
 struct SmemLayout {
-  int raw_off, q_off, w_off, hist_off, bar_off, total;
+  int raw_off, q_off, q8_off, w_off, hist_off, bar_off, total;
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int qpg) {
   SmemLayout L;
   L.raw_off = kStages * kKStageBytes;
-  L.q_off = L.raw_off + kRawStages * kRawStageBytes;
+  L.q_off = L.raw_off + raw_stages(qpg) * kRawStageBytes;
   L.q_off = (L.q_off + 1023) & ~1023;
-  L.w_off = L.q_off + qpg * 32 * kIdxDim * 2;
+  L.q8_off = L.q_off + qpg * 32 * kIdxDim * 2;          // E5M2 queries (1024-aligned)
+  L.w_off = L.q8_off + qpg * 32 * kIdxDim;
   L.hist_off = L.w_off + qpg * 32 * 4;
   L.bar_off = L.hist_off + kKeyHistBins * 4;
-  L.total = L.bar_off + 32 * 8 + 16 + 1024;  // barriers, tmem slot, alignment slack
+  L.total = L.bar_off + 48 * 8 + 16 + 1024;  // barriers, tmem slot, alignment slack
   return L;
 }
 
@@ -81,22 +90,29 @@ __device__ __forceinline__ TileRows tile_rows(const IndexParams& p, int g, int t
   return r;
 }
 
-// Rounds the 32 channels of block b of query row r (bf16, 128B-swizzled, two
-// 64-channel halves) to the MXFP4 grid in place: UE8M0 scale of the block's
-// largest magnitude (OCP MX), E2M1 code of x / scale (nearest, ties to
-// even, saturating), value = code * scale.
-__device__ __forceinline__ void round_query_block(uint8_t* qbuf, int qrows, int r, int b) {
-  uint8_t* half = qbuf + (b >> 1) * (qrows * 128) + r * 128;
-  uint4 w[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int chunk = (b & 1) * 4 + k;
-    w[k] = *reinterpret_cast<const uint4*>(half + ((chunk ^ (r & 7)) << 4));
+// E5M2 exponent offset of a UE8M0 byte, clamped to [-13, 13] (flagged).
+__device__ __forceinline__ int block_exp(uint32_t ue8m0, bool nonzero, uint32_t* err) {
+  int e = (int)ue8m0 - 127;
+  if (nonzero && (e < -13 || e > 13)) {
+    set_error(err, kErrRange);
+    e = e < -13 ? -13 : 13;
   }
+  return e;
+}
+
+// Block b (32 channels) of query row r: bf16 in the 128B-swizzled two-half
+// tile -> MXFP4 (UE8M0 scale of the block's largest magnitude, OCP MX;
+// E2M1 code of x / scale, nearest, ties to even, saturating) -> E5M2 bytes
+// in the 128B-swizzled one-row-per-128-bytes tile q8.
+__device__ __forceinline__ void query_block_to_e5m2(const uint8_t* qbuf, uint8_t* q8, int qrows,
+                                                    int r, int b, uint32_t* err) {
+  const uint8_t* half = qbuf + (b >> 1) * (qrows * 128) + r * 128;
   float x[32];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const uint32_t u[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+    const int chunk = (b & 1) * 4 + k;
+    const uint4 w = *reinterpret_cast<const uint4*>(half + ((chunk ^ (r & 7)) << 4));
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       x[8 * k + 2 * i] = __uint_as_float(u[i] << 16);
@@ -106,19 +122,26 @@ __device__ __forceinline__ void round_query_block(uint8_t* qbuf, int qrows, int 
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
-  const float sc = ue8m0_value(ue8m0_for_amax(amax));
+  const uint32_t sb = ue8m0_for_amax(amax);
+  const float sc = ue8m0_value(sb);
+  uint32_t codes[4];
+  uint32_t any = 0;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    uint32_t u[4];
+    uint32_t c = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float a = e2m1_value(e2m1_encode(__fdiv_rn(x[8 * k + 2 * i], sc))) * sc;
-      const float c = e2m1_value(e2m1_encode(__fdiv_rn(x[8 * k + 2 * i + 1], sc))) * sc;
-      u[i] = float_to_bf16_bits(a) | (float_to_bf16_bits(c) << 16);
-    }
-    const int chunk = (b & 1) * 4 + k;
-    *reinterpret_cast<uint4*>(half + ((chunk ^ (r & 7)) << 4)) = make_uint4(u[0], u[1], u[2], u[3]);
+    for (int i = 0; i < 8; ++i) c |= e2m1_encode(__fdiv_rn(x[8 * k + i], sc)) << (4 * i);
+    codes[k] = c;
+    any |= c & 0x77777777u;
   }
+  uint32_t tlo, thi;
+  e5m2_table(block_exp(sb, any != 0, err), tlo, thi);
+  uint32_t o[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) e2m1x8_to_e5m2x8(codes[k], tlo, thi, o[2 * k], o[2 * k + 1]);
+  uint8_t* row = q8 + r * 128;
+  *reinterpret_cast<uint4*>(row + (((2 * b) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+  *reinterpret_cast<uint4*>(row + (((2 * b + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -130,35 +153,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* kbuf = smem;
   uint8_t* raw = smem + L.raw_off;
   uint8_t* qbuf = smem + L.q_off;
+  uint8_t* q8 = smem + L.q8_off;
   float* wbuf = reinterpret_cast<float*>(smem + L.w_off);
   uint32_t* hs = reinterpret_cast<uint32_t*>(smem + L.hist_off);  // score-key histogram
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
-  uint64_t* raw_full = bars;            // [kRawStages]
-  uint64_t* raw_empty = bars + 4;       // [kRawStages]
-  uint64_t* k_full = bars + 8;          // [kStages]
-  uint64_t* k_empty = bars + 12;        // [kStages]
-  uint64_t* acc_full = bars + 16;       // [2]
-  uint64_t* acc_empty = bars + 18;      // [2]
-  uint64_t* q_full = bars + 20;
-  uint64_t* q_ready = bars + 21;
-  uint64_t* q_empty = bars + 22;
-  uint64_t* drain = bars + 23;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 32);
+  uint64_t* raw_full = bars;            // [kRawStagesMax]
+  uint64_t* raw_empty = bars + 12;      // [kRawStagesMax]
+  uint64_t* k_full = bars + 24;         // [kStages]
+  uint64_t* k_empty = bars + 28;        // [kStages]
+  uint64_t* acc_full = bars + 32;       // [2]
+  uint64_t* acc_empty = bars + 34;      // [2]
+  uint64_t* q_full = bars + 36;
+  uint64_t* q_ready = bars + 37;
+  uint64_t* q_empty = bars + 38;
+  uint64_t* drain = bars + 39;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 40);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = 32 * p.qpg;               // MMA N (columns per accumulator)
   const int qrows = 32 * p.qpg;
   const uint32_t tmem_cols = (N * 2 <= 32) ? 32u : (uint32_t)(N * 2);
+  const int n_raw = raw_stages(p.qpg);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kRawStages; ++i) {
+    for (int i = 0; i < n_raw; ++i) {
       mbar_init(raw_full + i, 1);
-      mbar_init(raw_empty + i, kCvtThreads);
+      mbar_init(raw_empty + i, kCvtWarps);
     }
-    for (int i = 0; i < kStages; ++i) { mbar_init(k_full + i, kCvtThreads); mbar_init(k_empty + i, 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, kEpiThreads); }
+    // consumer barriers count warps: each warp arrives once, from lane 0,
+    // after a __syncwarp over its lanes' work
+    for (int i = 0; i < kStages; ++i) { mbar_init(k_full + i, kCvtWarps); mbar_init(k_empty + i, 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, kEpiWarps); }
     mbar_init(q_full, 1);
-    mbar_init(q_ready, kCvtThreads);
+    mbar_init(q_ready, kCvtWarps);
     mbar_init(q_empty, 1);
     mbar_init(drain, 1);
     fence_barrier_init();
@@ -205,16 +232,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       bulk_load(dst + kRawCodeBytes, p.idx_scales + tr.s0 * 4, scale_bytes, raw_full + rs);
       armed |= 1u << rs;
       armed_ph = (armed_ph & ~(1u << rs)) | (rph << rs);
-      if (++rs == kRawStages) { rs = 0; rph ^= 1; }
+      if (++rs == n_raw) { rs = 0; rph ^= 1; }
     }
     // make sure no bulk copy is still writing into this CTA's shared memory
-    for (int s = 0; s < kRawStages; ++s)
+    for (int s = 0; s < n_raw; ++s)
       if (armed & (1u << s)) mbar_wait(raw_full + s, (armed_ph >> s) & 1u, p.err);
     if (cur >= 0) mbar_wait(q_full, qph ^ 1, p.err);
   } else if (warp >= 10 && begin < end) {
     // ------------------------------------------------ converters
-    const int ct = threadIdx.x - kCvtBase;          // 0..127
-    const int cw = ct >> 5;                         // converter warp 0..3
+    const int ct = threadIdx.x - kCvtBase;          // 0..255
+    const int cw = ct >> 5;                         // converter warp 0..7
     const int b = ct & 3;                           // 32-channel block of the key
     int g = g0, cur = -1, rs = 0, ks = 0;
     uint32_t rph = 0, kph = 0, qph = 0;
@@ -226,49 +253,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(q_full, qph, p.err);
         qph ^= 1;
         if (!ok) break;
-        for (int i = ct; i < qrows * 4; i += kCvtThreads) round_query_block(qbuf, qrows, i >> 2, i & 3);
+        for (int i = ct; i < qrows * 4; i += kCvtThreads)
+          query_block_to_e5m2(qbuf, q8, qrows, i >> 2, i & 3, p.err);
         fence_proxy_async_smem();
-        mbar_arrive(q_ready);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_ready);
         cur = g;
       }
       ok = mbar_wait(raw_full + rs, rph, p.err) && mbar_wait(k_empty + ks, kph ^ 1, p.err);
       if (!ok) break;
-      tc_fence_after();
-      const TileRows tr = tile_rows(p, g, it - p.tile_prefix[g]);
+      const int t = it - p.tile_prefix[g];
+      const TileRows tr = tile_rows(p, g, t);
+      // rows holding appended keys (the rest of the copy is unused capacity
+      // or the next sequence: converted as zeros, never range-checked)
+      const int32_t len = p.prefill ? p.pre_len : p.nvis[g];
+      const int32_t live = min(tr.nrows, len - t * kTileE);
       const uint8_t* src = raw + rs * kRawStageBytes;
       const uint32_t* sw = reinterpret_cast<const uint32_t*>(src + kRawCodeBytes) + (tr.row0 - tr.s0);
-      uint8_t* dst = kbuf + ks * kKStageBytes + (b >> 1) * (kKStageBytes / 2);
+      uint8_t* dst = kbuf + ks * kKStageBytes;
 #pragma unroll 1
-      for (int pass = 0; pass < 4; ++pass) {
-        const int r = pass * 32 + cw * 8 + (lane >> 2);   // key row of the tile
+      for (int pass = 0; pass < 2; ++pass) {
+        const int r = pass * 64 + cw * 8 + (lane >> 2);   // key row of the tile
         uint4 c4 = make_uint4(0u, 0u, 0u, 0u);
-        uint32_t s2 = 0u;
-        if (r < tr.nrows) {
+        uint32_t sb = 127u;
+        if (r < live) {
           c4 = *reinterpret_cast<const uint4*>(src + r * (kIdxDim / 2) + b * 16);
-          const uint32_t s16 = float_to_bf16_bits(ue8m0_value((sw[r] >> (8 * b)) & 0xFFu));
-          s2 = s16 | (s16 << 16);
+          sb = (sw[r] >> (8 * b)) & 0xFFu;
         }
-        const uint32_t words[4] = {c4.x, c4.y, c4.z, c4.w};
+        const uint32_t any = (c4.x | c4.y | c4.z | c4.w) & 0x77777777u;
+        uint32_t tlo, thi;
+        e5m2_table(block_exp(sb, any != 0, p.err), tlo, thi);
+        uint32_t o[8];
+        e2m1x8_to_e5m2x8(c4.x, tlo, thi, o[0], o[1]);
+        e2m1x8_to_e5m2x8(c4.y, tlo, thi, o[2], o[3]);
+        e2m1x8_to_e5m2x8(c4.z, tlo, thi, o[4], o[5]);
+        e2m1x8_to_e5m2x8(c4.w, tlo, thi, o[6], o[7]);
         uint8_t* rowp = dst + r * 128;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint32_t v[4];
-          e2m1x8_to_bf16x8(words[k], v);
-          uint4 o;
-          o.x = bf16x2_mul(v[0], s2); o.y = bf16x2_mul(v[1], s2);
-          o.z = bf16x2_mul(v[2], s2); o.w = bf16x2_mul(v[3], s2);
-          const int chunk = (b & 1) * 4 + k;
-          *reinterpret_cast<uint4*>(rowp + ((chunk ^ (r & 7)) << 4)) = o;
-        }
+        *reinterpret_cast<uint4*>(rowp + (((2 * b) ^ (r & 7)) << 4)) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(rowp + (((2 * b + 1) ^ (r & 7)) << 4)) =
+            make_uint4(o[4], o[5], o[6], o[7]);
       }
       fence_proxy_async_smem();
-      mbar_arrive(k_full + ks);
-      mbar_arrive(raw_empty + rs);
-      if (++rs == kRawStages) { rs = 0; rph ^= 1; }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(k_full + ks);
+        mbar_arrive(raw_empty + rs);
+      }
+      if (++rs == n_raw) { rs = 0; rph ^= 1; }
       if (++ks == kStages) { ks = 0; kph ^= 1; }
     }
   } else if (warp == 1 && lane == 0 && begin < end) {
     // ------------------------------------------------ MMA issuer
+    // the f16-kind descriptor: format fields 1 / 1 read as E5M2 / E5M2 here
     const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)N, false, false);
     int g = g0, cur = -1, stage = 0, acc = 0;
     uint32_t ph = 0, qph = 0, aph = 0;
@@ -285,15 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t a0 = smem_u32(kbuf + stage * kKStageBytes);
-      const uint32_t b0 = smem_u32(qbuf);
+      const uint32_t b0 = smem_u32(q8);
       const uint32_t d = tmem_base + (uint32_t)(acc * N);
+      // one 128-byte swizzled row holds all 128 channels: K steps of 32 bytes
 #pragma unroll
-      for (int ks = 0; ks < kIdxDim / 16; ++ks) {
-        const uint32_t ao = (uint32_t)((ks >> 2) * (kKStageBytes / 2) + (ks & 3) * 32);
-        const uint32_t bo = (uint32_t)((ks >> 2) * (qrows * 128) + (ks & 3) * 32);
-        umma_bf16(d, sdesc_sw128(a0 + ao, 16, 1024), sdesc_sw128(b0 + bo, 16, 1024), idesc,
-                  ks > 0 ? 1u : 0u);
-      }
+      for (int ks = 0; ks < kIdxDim / 32; ++ks)
+        umma_e5m2(d, sdesc_sw128(a0 + ks * 32, 16, 1024), sdesc_sw128(b0 + ks * 32, 16, 1024),
+                  idesc, ks > 0 ? 1u : 0u);
       umma_commit(k_empty + stage);
       umma_commit(acc_full + acc);
       const bool last_of_group = (it + 1 == end) || (p.tile_prefix[g + 1] <= it + 1);
@@ -362,7 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(acc_empty + acc);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty + acc);
       if (++acc == 2) { acc = 0; aph ^= 1; }
     }
     if (use_hist && cur >= 0) flush(cur);

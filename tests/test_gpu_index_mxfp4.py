@@ -122,3 +122,18 @@ def test_pool_mode_needs_bf16_keys(C):
     pool = torch.zeros(1, 16, dtype=torch.int32, device="cuda")
     with pytest.raises(C.Csa2Error):
         C.csa2_index_topk_reindex_decode(cache, q, w, pool)
+
+
+def test_out_of_range_scale_is_reported(C):
+    """Keys around 2^20 need a block scale of 2^18, outside the E5M2 fast
+    path's 2^-13 .. 2^13: the indexer clamps it and reports CSA2_ERR_DEVICE."""
+    import torch
+    n = 300
+    cache = C.Cache(C.config(idx_layout=1), [n])
+    k = S.normal_f32(S.stream_key(119, S.S_IDXK, 0), 0, n * 128).reshape(n, 128) * 2.0 ** 20
+    e = S.normal_f32(S.stream_key(119, S.S_ENTRIES, 0), 0, n * 512).reshape(n, 512)
+    C.csa2_append_entries(cache, [0], [n], f32_dev(e), bf16_dev(S.f32_to_bf16_bits(k)))
+    assert cache.device_error() == 0
+    qi, w = _queries(120, 1)
+    C.csa2_index_topk_decode(cache, bf16_dev(qi), f32_dev(w))
+    assert cache.device_error() == 7        # CSA2_ERR_DEVICE
