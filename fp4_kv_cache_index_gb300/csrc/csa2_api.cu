@@ -485,6 +485,8 @@ csa2_status_t run_index_decode(const csa2_cache_t* c, int32_t nq, const void* q_
       cudaMemsetAsync(key_hist, 0, (size_t)nq * kKeyHistBinsHost * sizeof(uint32_t), S(stream)) !=
           cudaSuccess)
     return CSA2_ERR_CUDA;
+  // keys per tile: the MXFP4 decode kernel takes 256, every other path 128
+  const int64_t tile_e = c->cfg.idx_layout == CSA2_IDX_MXFP4 ? 256 : 128;
   for (int q0 = 0; q0 < nq; q0 += kMaxIdxGroups) {
     const int n = std::min(kMaxIdxGroups, nq - q0);
     std::memset(ip, 0, sizeof(IndexParams));
@@ -505,7 +507,7 @@ csa2_status_t run_index_decode(const csa2_cache_t* c, int32_t nq, const void* q_
       const int64_t nv = c->len[s];
       ip->entry_base[i] = c->off[s];
       ip->nvis[i] = (int32_t)nv;
-      ip->tile_prefix[i + 1] = ip->tile_prefix[i] + (int32_t)((nv + 127) / 128);
+      ip->tile_prefix[i + 1] = ip->tile_prefix[i] + (int32_t)((nv + tile_e - 1) / tile_e);
     }
     CUtensorMap tm_q;
     if (!make_map(&tm_q, qb + (int64_t)q0 * kIdxHeads * kIdxDim, (uint64_t)n * kIdxHeads,

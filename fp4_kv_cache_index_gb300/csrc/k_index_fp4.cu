@@ -31,12 +31,15 @@
 namespace csa2 {
 namespace {
 
-constexpr int kTileE = 128;
-constexpr int kRawStagesMax = 12;   // raw ring depth: 12 for decode, 4 for prefill
-constexpr int kStages = 4;                              // converted E5M2 stages
-constexpr int kKStageBytes = kTileE * kIdxDim;          // 16 KB
-constexpr int kRawCodeBytes = kTileE * kIdxDim / 2;     // 8 KB
-constexpr int kRawScaleBytes = 544;                     // (128 + 4) words, 16-byte padded
+// A tile is 256 keys in decode (two M = 128 MMA groups: the per-tile cost of
+// the warp hand-offs, a fixed ~0.3 us, is then spread over twice the keys)
+// and 128 keys in prefill (8 queries per tile already give N = 256).
+constexpr int kTileMax = 256;
+constexpr int kRawStagesMax = 5;
+constexpr int kStagesMax = 3;                           // converted E5M2 stages
+constexpr int kKStageBytes = kTileMax * kIdxDim;        // 32 KB
+constexpr int kRawCodeBytes = kTileMax * kIdxDim / 2;   // 16 KB
+constexpr int kRawScaleBytes = 1056;                    // (256 + 4) words, 16-byte padded
 constexpr int kRawStageBytes = kRawCodeBytes + kRawScaleBytes;
 constexpr int kThreads = 576;
 constexpr int kEpiThreads = 256;   // warps 2-9
@@ -45,7 +48,9 @@ constexpr int kCvtBase = 320;
 constexpr int kCvtWarps = kCvtThreads / 32;
 constexpr int kEpiWarps = kEpiThreads / 32;
 
-__host__ __device__ inline int raw_stages(int qpg) { return qpg == 1 ? kRawStagesMax : 4; }
+__host__ __device__ inline int raw_stages(int qpg) { return qpg == 1 ? kRawStagesMax : 2; }
+__host__ __device__ inline int k_stages(int qpg) { return qpg == 1 ? kStagesMax : 2; }
+__host__ __device__ inline int tile_rows_of(int qpg) { return qpg == 1 ? 256 : 128; }
 
 struct SmemLayout {
   int raw_off, q_off, q8_off, w_off, hist_off, bar_off, total;
@@ -53,7 +58,7 @@ struct SmemLayout {
 
 __host__ __device__ inline SmemLayout smem_layout(int qpg) {
   SmemLayout L;
-  L.raw_off = kStages * kKStageBytes;
+  L.raw_off = k_stages(qpg) * kKStageBytes;
   L.q_off = L.raw_off + raw_stages(qpg) * kRawStageBytes;
   L.q_off = (L.q_off + 1023) & ~1023;
   L.q8_off = L.q_off + qpg * 32 * kIdxDim * 2;          // E5M2 queries (1024-aligned)
@@ -81,11 +86,11 @@ struct TileRows {
   int64_t row0, s0;
   int32_t nrows;
 };
-__device__ __forceinline__ TileRows tile_rows(const IndexParams& p, int g, int t) {
+__device__ __forceinline__ TileRows tile_rows(const IndexParams& p, int g, int t, int tile_e) {
   TileRows r;
-  r.row0 = group_base(p, g) + (int64_t)t * kTileE;
+  r.row0 = group_base(p, g) + (int64_t)t * tile_e;
   const int64_t left = p.idx_total - r.row0;
-  r.nrows = (int32_t)(left < kTileE ? left : kTileE);
+  r.nrows = (int32_t)(left < tile_e ? left : tile_e);
   r.s0 = r.row0 & ~(int64_t)3;
   return r;
 }
@@ -159,21 +164,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* raw_full = bars;            // [kRawStagesMax]
   uint64_t* raw_empty = bars + 12;      // [kRawStagesMax]
-  uint64_t* k_full = bars + 24;         // [kStages]
-  uint64_t* k_empty = bars + 28;        // [kStages]
-  uint64_t* acc_full = bars + 32;       // [2]
-  uint64_t* acc_empty = bars + 34;      // [2]
-  uint64_t* q_full = bars + 36;
-  uint64_t* q_ready = bars + 37;
-  uint64_t* q_empty = bars + 38;
-  uint64_t* drain = bars + 39;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 40);
+  uint64_t* k_full = bars + 24;         // [kStagesMax]
+  uint64_t* k_empty = bars + 28;        // [kStagesMax]
+  uint64_t* acc_full = bars + 32;       // [nacc <= 4]
+  uint64_t* acc_empty = bars + 36;      // [nacc <= 4]
+  uint64_t* q_full = bars + 40;
+  uint64_t* q_ready = bars + 41;
+  uint64_t* q_empty = bars + 42;
+  uint64_t* drain = bars + 43;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 44);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = 32 * p.qpg;               // MMA N (columns per accumulator)
   const int qrows = 32 * p.qpg;
-  const uint32_t tmem_cols = (N * 2 <= 32) ? 32u : (uint32_t)(N * 2);
+  // decode (one query per group): 256-key tiles as two M-groups whose
+  // accumulators sit side by side (2 x 32 columns), 4 accumulators, each
+  // epilogue half takes one M-group; prefill: 128-key tiles, 2 accumulators
+  // of 256 columns, the halves split the 8 queries of every tile
+  const bool two_groups = p.qpg == 1;
+  const int tile_e = tile_rows_of(p.qpg);
+  const int mgroups = tile_e / 128;
+  const int nacc = two_groups ? 4 : 2;
+  const int acc_cols = mgroups * N;
+  const uint32_t tmem_cols = (uint32_t)(nacc * acc_cols) < 32u ? 32u : (uint32_t)(nacc * acc_cols);
   const int n_raw = raw_stages(p.qpg);
+  const int n_k = k_stages(p.qpg);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < n_raw; ++i) {
@@ -182,8 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // consumer barriers count warps: each warp arrives once, from lane 0,
     // after a __syncwarp over its lanes' work
-    for (int i = 0; i < kStages; ++i) { mbar_init(k_full + i, kCvtWarps); mbar_init(k_empty + i, 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, kEpiWarps); }
+    for (int i = 0; i < n_k; ++i) { mbar_init(k_full + i, kCvtWarps); mbar_init(k_empty + i, 1); }
+    for (int i = 0; i < nacc; ++i) {
+      mbar_init(acc_full + i, 1);
+      mbar_init(acc_empty + i, kEpiWarps);
+    }
     mbar_init(q_full, 1);
     mbar_init(q_ready, kCvtWarps);
     mbar_init(q_empty, 1);
@@ -222,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = mbar_wait(raw_empty + rs, rph ^ 1, p.err);
       if (!ok) break;
-      const TileRows tr = tile_rows(p, g, it - p.tile_prefix[g]);
+      const TileRows tr = tile_rows(p, g, it - p.tile_prefix[g], tile_e);
       const int64_t s1 = (tr.row0 + tr.nrows + 3) & ~(int64_t)3;
       const uint32_t code_bytes = (uint32_t)tr.nrows * (kIdxDim / 2);
       const uint32_t scale_bytes = (uint32_t)(s1 - tr.s0) * 4u;
@@ -263,16 +281,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait(raw_full + rs, rph, p.err) && mbar_wait(k_empty + ks, kph ^ 1, p.err);
       if (!ok) break;
       const int t = it - p.tile_prefix[g];
-      const TileRows tr = tile_rows(p, g, t);
+      const TileRows tr = tile_rows(p, g, t, tile_e);
       // rows holding appended keys (the rest of the copy is unused capacity
       // or the next sequence: converted as zeros, never range-checked)
       const int32_t len = p.prefill ? p.pre_len : p.nvis[g];
-      const int32_t live = min(tr.nrows, len - t * kTileE);
+      const int32_t live = min(tr.nrows, len - t * tile_e);
       const uint8_t* src = raw + rs * kRawStageBytes;
       const uint32_t* sw = reinterpret_cast<const uint32_t*>(src + kRawCodeBytes) + (tr.row0 - tr.s0);
       uint8_t* dst = kbuf + ks * kKStageBytes;
 #pragma unroll 1
-      for (int pass = 0; pass < 2; ++pass) {
+      for (int pass = 0; pass < tile_e / 64; ++pass) {
         const int r = pass * 64 + cw * 8 + (lane >> 2);   // key row of the tile
         uint4 c4 = make_uint4(0u, 0u, 0u, 0u);
         uint32_t sb = 127u;
@@ -301,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(raw_empty + rs);
       }
       if (++rs == n_raw) { rs = 0; rph ^= 1; }
-      if (++ks == kStages) { ks = 0; kph ^= 1; }
+      if (++ks == n_k) { ks = 0; kph ^= 1; }
     }
   } else if (warp == 1 && lane == 0 && begin < end) {
     // ------------------------------------------------ MMA issuer
@@ -321,29 +339,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait(k_full + stage, ph, p.err) && mbar_wait(acc_empty + acc, aph ^ 1, p.err);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t a0 = smem_u32(kbuf + stage * kKStageBytes);
       const uint32_t b0 = smem_u32(q8);
-      const uint32_t d = tmem_base + (uint32_t)(acc * N);
       // one 128-byte swizzled row holds all 128 channels: K steps of 32 bytes
+      for (int mg = 0; mg < mgroups; ++mg) {
+        const uint32_t a0 = smem_u32(kbuf + stage * kKStageBytes + mg * 128 * 128);
+        const uint32_t d = tmem_base + (uint32_t)(acc * acc_cols + mg * N);
 #pragma unroll
-      for (int ks = 0; ks < kIdxDim / 32; ++ks)
-        umma_e5m2(d, sdesc_sw128(a0 + ks * 32, 16, 1024), sdesc_sw128(b0 + ks * 32, 16, 1024),
-                  idesc, ks > 0 ? 1u : 0u);
+        for (int ks = 0; ks < kIdxDim / 32; ++ks)
+          umma_e5m2(d, sdesc_sw128(a0 + ks * 32, 16, 1024), sdesc_sw128(b0 + ks * 32, 16, 1024),
+                    idesc, ks > 0 ? 1u : 0u);
+      }
       umma_commit(k_empty + stage);
       umma_commit(acc_full + acc);
       const bool last_of_group = (it + 1 == end) || (p.tile_prefix[g + 1] <= it + 1);
       if (last_of_group) umma_commit(q_empty);
-      if (++stage == kStages) { stage = 0; ph ^= 1; }
-      if (++acc == 2) { acc = 0; aph ^= 1; }
+      if (++stage == n_k) { stage = 0; ph ^= 1; }
+      if (++acc == nacc) { acc = 0; aph ^= 1; }
     }
     umma_commit(drain);
     mbar_wait(drain, 0, p.err);
   } else if (warp >= 2 && warp < 10) {
     // ------------------------------------------------ epilogue
     const int quad = warp & 3;                 // TMEM lane quadrant of this warp
-    const int row = quad * 32 + lane;          // entry within the tile
     const int et = threadIdx.x - 64;           // 0..255
-    const int half = (warp - 2) >> 2;          // which queries of the group
+    const int half = (warp - 2) >> 2;          // M-group (decode) or queries (prefill)
+    const int row = (two_groups ? half * 128 : 0) + quad * 32 + lane;   // key within the tile
     const int jq = (p.qpg + 1) >> 1;
     const int j0 = half * jq, j1 = min(p.qpg, j0 + jq);
     const bool use_hist = p.key_hist != nullptr && p.qpg == 1;
@@ -359,8 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (use_hist) {
       for (int i = et; i < kKeyHistBins; i += kEpiThreads) hs[i] = 0u;
     }
-    int g = g0, cur = -1, acc = 0;
-    uint32_t aph = 0;
+    int g = g0, cur = -1;
+    bool ok = true;
     for (int it = begin; it < end; ++it) {
       while (p.tile_prefix[g + 1] <= it) ++g;
       if (g != cur) {
@@ -373,13 +393,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("bar.sync 1, 256;" ::: "memory");
         cur = g;
       }
-      if (!mbar_wait(acc_full + acc, aph, p.err)) break;
+      const int u = it - begin;
+      if (!ok) continue;
+      const int acc = u % nacc;
+      if (!mbar_wait(acc_full + acc, (uint32_t)((u / nacc) & 1), p.err)) { ok = false; continue; }
       tc_fence_after();
       const int t = it - p.tile_prefix[g];
-      const int e = t * kTileE + row;
-      for (int j = j0; j < j1; ++j) {
+      const int e = t * tile_e + row;
+      const int ja = two_groups ? 0 : j0, jb = two_groups ? 1 : j1;
+      const uint32_t col0 = (uint32_t)(acc * acc_cols + (two_groups ? half * N : 0));
+      for (int j = ja; j < jb; ++j) {
         uint32_t r[32];
-        tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * N + j * 32), r);
+        tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + col0 + (uint32_t)(j * 32), r);
         const float* wj = wbuf + j * 32;
         float s = 0.0f;
 #pragma unroll
@@ -399,7 +424,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty + acc);
-      if (++acc == 2) { acc = 0; aph ^= 1; }
     }
     if (use_hist && cur >= 0) flush(cur);
   }
