@@ -76,6 +76,9 @@ def lib():
                 "orc_index_scores": ([i64, i32, i32, P, P, P, P], None),
                 "orc_topk": ([i64, P, i32, P], i32),
                 "orc_bf16_round": ([f32], f32),
+                "orc_ue8m0_for_amax_e4m3": ([f32], i32),
+                "orc_swa_fp8_quantise": ([i64, P, P, P, P], None),
+                "orc_swa_fp8_dequantise": ([i64, P, P, P, P], None),
                 "orc_bf16_round_n": ([i64, P, P], None),
                 "orc_sparse_attention": ([i32, i32, i32, P, P, P, i64, i32, P, i32, P,
                                           f32, P, P, P], None),
@@ -148,6 +151,37 @@ def dequantise(codes: np.ndarray, scales: np.ndarray, layout: int) -> np.ndarray
     out = np.zeros((n, dim), np.float32)
     lib().orc_dequantise(n, dim, layout, _p(codes), _p(scales), _p(out))
     return out
+
+
+def swa_fp8_quantise(rows_bf16):
+    """bf16 window rows [n, 512] -> FP8 rows: E4M3 codes [n, 448], bf16 RoPE
+    channels [n, 64], UE8M0 scales [n, 8] (one per 64 channels, byte 7
+    unused).  See orc_swa_fp8_quantise for the reading of the format."""
+    x = _c(rows_bf16, np.uint16).reshape(-1, 512)
+    n = x.shape[0]
+    codes = np.zeros((n, 448), np.uint8)
+    rope = np.zeros((n, 64), np.uint16)
+    scales = np.zeros((n, 8), np.uint8)
+    lib().orc_swa_fp8_quantise(n, _p(x), _p(codes), _p(rope), _p(scales))
+    return codes, rope, scales
+
+
+def swa_fp8_dequantise(codes, rope, scales) -> np.ndarray:
+    codes = _c(codes, np.uint8)
+    rope = _c(rope, np.uint16)
+    scales = _c(scales, np.uint8)
+    n = codes.shape[0]
+    out = np.zeros((n, 512), np.float32)
+    lib().orc_swa_fp8_dequantise(n, _p(codes), _p(rope), _p(scales), _p(out))
+    return out
+
+
+def swa_fp8_round_bf16(rows_bf16) -> np.ndarray:
+    """Window rows through FP8 and back, as bf16 bits (every dequantised
+    value is a bf16 value): what the attention reads from an FP8 window."""
+    d = swa_fp8_dequantise(*swa_fp8_quantise(rows_bf16))
+    shape = np.shape(rows_bf16)
+    return (d.view(np.uint32) >> 16).astype(np.uint16).reshape(shape)
 
 
 def entry_bytes(dim: int, layout: int) -> float:

@@ -92,6 +92,64 @@ int orc_ue8m0_for_amax(float amax) {
   return b;
 }
 
+/* FP8 window rows [V41 sec 2.4.4: the SWA KV cache stays FP8; the V4 FP8
+ * row of the cache breakdown (NDT sec 3.1, the PaperTrace reading of V4):
+ * 448 non-RoPE channels in FP8, 64 RoPE channels in bf16, 8 bytes of
+ * scale].  Reading: E4M3 codes with one UE8M0 scale per 64 channels by the
+ * OCP MX rule for E4M3 elements (shared exponent floor(log2 amax) - 8; a
+ * quotient above 448 saturates), byte 7 of the scales unused; the RoPE
+ * channels keep their bf16 bits.  584 bytes per row.                       */
+int orc_ue8m0_for_amax_e4m3(float amax) {
+  if (!(amax > 0.0f)) return 0;
+  int e2;
+  frexp((double)amax, &e2);          /* amax = f * 2^e2, f in [0.5, 1) */
+  int b = (e2 - 1) - 8 + 127;
+  if (b < 0) b = 0;
+  if (b > 254) b = 254;
+  return b;
+}
+
+static float bf16_bits_value(uint16_t b) {
+  const uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+void orc_swa_fp8_quantise(int64_t n, const uint16_t* rows, uint8_t* codes, uint16_t* rope,
+                          uint8_t* scales) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < n; ++r) {
+    const uint16_t* x = rows + r * 512;
+    for (int blk = 0; blk < 7; ++blk) {
+      float amax = 0.0f;
+      for (int c = 64 * blk; c < 64 * blk + 64; ++c) {
+        const float a = fabsf(bf16_bits_value(x[c]));
+        if (a > amax) amax = a;
+      }
+      const int b = orc_ue8m0_for_amax_e4m3(amax);
+      const float s = orc_ue8m0_value(b);
+      scales[r * 8 + blk] = (uint8_t)b;
+      for (int c = 64 * blk; c < 64 * blk + 64; ++c) {
+        const float v = bf16_bits_value(x[c]) / s;
+        const int code = orc_e4m3_encode(fabsf(v));
+        codes[r * 448 + c] = (uint8_t)(code | (signbit(v) ? 0x80 : 0));
+      }
+    }
+    scales[r * 8 + 7] = 0;
+    for (int c = 0; c < 64; ++c) rope[r * 64 + c] = x[448 + c];
+  }
+}
+
+void orc_swa_fp8_dequantise(int64_t n, const uint8_t* codes, const uint16_t* rope,
+                            const uint8_t* scales, float* out) {
+  for (int64_t r = 0; r < n; ++r) {
+    for (int c = 0; c < 448; ++c)
+      out[r * 512 + c] = orc_e4m3_value(codes[r * 448 + c]) * orc_ue8m0_value(scales[r * 8 + c / 64]);
+    for (int c = 0; c < 64; ++c) out[r * 512 + 448 + c] = bf16_bits_value(rope[r * 64 + c]);
+  }
+}
+
 int orc_group(int layout) { return layout == 1 ? 16 : 32; }
 
 static float block_scale(int layout, float amax, uint8_t* byte) {

@@ -43,7 +43,12 @@ float  orc_e4m3_value(int byte);          /* NaN for 0x7f / 0xff               *
 int    orc_e4m3_encode(float v);          /* v >= 0: nearest, ties even, <=448 */
 float  orc_ue8m0_value(int byte);         /* 2^(byte-127), NaN for 0xff        */
 int    orc_ue8m0_for_amax(float amax);    /* OCP MX shared-exponent rule       */
-int    orc_group(int layout);             /* 32 or 16                          */
+int    orc_group(int layout);
+int    orc_ue8m0_for_amax_e4m3(float amax);
+void   orc_swa_fp8_quantise(int64_t n, const uint16_t* rows, uint8_t* codes, uint16_t* rope,
+                            uint8_t* scales);
+void   orc_swa_fp8_dequantise(int64_t n, const uint8_t* codes, const uint16_t* rope,
+                              const uint8_t* scales, float* out);             /* 32 or 16                          */
 void   orc_quantise(int64_t n, int dim, int layout, const float* x,
                     uint8_t* codes, uint8_t* scales);
 void   orc_dequantise(int64_t n, int dim, int layout, const uint8_t* codes,
