@@ -53,7 +53,9 @@ def config(n_heads=64, head_dim=512, idx_heads=32, idx_dim=128, topk=512, swa=12
 class AttnOpts(ctypes.Structure):
     """csa2_attn_opts_t: attention sink and output RoPE(-i)."""
     _fields_ = [("sink", ctypes.c_void_p), ("rope_pos", ctypes.c_void_p),
-                ("rope_out", ctypes.c_int32), ("rope_base", ctypes.c_double)]
+                ("rope_out", ctypes.c_int32), ("rope_base", ctypes.c_double),
+                ("swa_codes", ctypes.c_void_p), ("swa_rope", ctypes.c_void_p),
+                ("swa_scales", ctypes.c_void_p)]
 
 
 class CacheViews(ctypes.Structure):
@@ -96,6 +98,7 @@ def _load():
                                         P], i32),
         "csa2_sparse_attn_prefill_ex": ([P, i32, i32, i64, P, P, i64, i64, P, ctypes.c_float, P,
                                          P, P, P], i32),
+        "csa2_swa_fp8_quantise": ([i64, P, P, P, P, P], i32),
         "csa2_hsi_pool_workspace_bytes": ([i32, i64], sz),
         "csa2_hsi_pool": ([i32, P, i64, P, i32, i32, P, P, sz, P], i32),
         "csa2_index_reindex_workspace_bytes": ([P, i32, i32], sz),
@@ -339,7 +342,7 @@ def csa2_sparse_attn_decode(cache: Cache, q: torch.Tensor, swa_kv: Optional[torc
                             workspace: Optional[torch.Tensor] = None,
                             sink: Optional[torch.Tensor] = None,
                             rope_pos: Optional[torch.Tensor] = None, rope_base: float = 0.0,
-                            stream=None) -> torch.Tensor:
+                            swa_fp8=None, stream=None) -> torch.Tensor:
     """workspace=None allocates one of csa2_sparse_attn_workspace_bytes; pass
     an empty tensor to run without (one CTA per query).  sink: fp32 [n_heads]
     per-head sink logits; rope_pos: int64 [n_queries] positions i for the
@@ -354,11 +357,12 @@ def csa2_sparse_attn_decode(cache: Cache, q: torch.Tensor, swa_kv: Optional[torc
     args = (cache.handle, nq, _i32_array(seq_ids), _ptr(q), _ptr(swa_kv), _ptr(swa_len),
             _ptr(topk_idx), float(scale), _ptr(out), _ptr(lse),
             _ptr(workspace) if ws_bytes else None, ws_bytes)
-    if sink is None and rope_pos is None:
+    if sink is None and rope_pos is None and swa_fp8 is None:
         _check(lib.csa2_sparse_attn_decode(*args, _stream(stream)), "csa2_sparse_attn_decode")
     else:
+        f8 = swa_fp8 if swa_fp8 is not None else (None, None, None)
         opts = AttnOpts(_ptr(sink), _ptr(rope_pos), 1 if rope_pos is not None else 0,
-                        float(rope_base))
+                        float(rope_base), _ptr(f8[0]), _ptr(f8[1]), _ptr(f8[2]))
         _check(lib.csa2_sparse_attn_decode_ex(*args, ctypes.byref(opts), _stream(stream)),
                "csa2_sparse_attn_decode_ex")
     return out
@@ -370,18 +374,23 @@ def csa2_sparse_attn_prefill(cache: Cache, seq: int, pos0: int, q: torch.Tensor,
                              out: Optional[torch.Tensor] = None,
                              lse: Optional[torch.Tensor] = None,
                              sink: Optional[torch.Tensor] = None, rope_out: bool = False,
-                             rope_base: float = 0.0, stream=None) -> torch.Tensor:
-    """rope_out: rotate the last 64 output channels by RoPE(-(pos0 + i))."""
+                             rope_base: float = 0.0, swa_fp8=None, stream=None) -> torch.Tensor:
+    """rope_out: rotate the last 64 output channels by RoPE(-(pos0 + i));
+    swa_fp8: (codes, rope, scales) of csa2_swa_fp8_quantise instead of
+    swa_kv."""
     nq = q.shape[0]
     if out is None:
         out = torch.empty_like(q)
-    n_rows = swa_kv.shape[0] if swa_kv is not None else 0
+    n_rows = swa_fp8[0].shape[0] if swa_fp8 is not None else (
+        swa_kv.shape[0] if swa_kv is not None else 0)
     args = (cache.handle, seq, nq, pos0, _ptr(q), _ptr(swa_kv), swa_pos0, n_rows,
             _ptr(topk_idx), float(scale), _ptr(out), _ptr(lse))
-    if sink is None and not rope_out:
+    if sink is None and not rope_out and swa_fp8 is None:
         _check(lib.csa2_sparse_attn_prefill(*args, _stream(stream)), "csa2_sparse_attn_prefill")
     else:
-        opts = AttnOpts(_ptr(sink), None, 1 if rope_out else 0, float(rope_base))
+        f8 = swa_fp8 if swa_fp8 is not None else (None, None, None)
+        opts = AttnOpts(_ptr(sink), None, 1 if rope_out else 0, float(rope_base),
+                        _ptr(f8[0]), _ptr(f8[1]), _ptr(f8[2]))
         _check(lib.csa2_sparse_attn_prefill_ex(*args, ctypes.byref(opts), _stream(stream)),
                "csa2_sparse_attn_prefill_ex")
     return out
@@ -474,3 +483,17 @@ def csa2_index_topk_decode_bf16(cache: Cache, q_idx: torch.Tensor, w: torch.Tens
                                            _stream(stream)),
            "csa2_index_topk_decode_bf16")
     return topk_idx
+
+
+# ------------------------------------------------------------------ FP8 window rows
+def csa2_swa_fp8_quantise(rows: torch.Tensor, stream=None):
+    """bf16 rows [..., 512] -> (codes u8 [n, 448], rope bf16 [n, 64],
+    scales u8 [n, 8]) with n the number of rows."""
+    r = rows.reshape(-1, 512)
+    n = r.shape[0]
+    codes = torch.empty(n, 448, dtype=torch.uint8, device=rows.device)
+    rope = torch.empty(n, 64, dtype=torch.bfloat16, device=rows.device)
+    scales = torch.empty(n, 8, dtype=torch.uint8, device=rows.device)
+    _check(lib.csa2_swa_fp8_quantise(n, _ptr(r), _ptr(codes), _ptr(rope), _ptr(scales),
+                                     _stream(stream)), "csa2_swa_fp8_quantise")
+    return codes, rope, scales

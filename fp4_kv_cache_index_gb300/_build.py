@@ -13,7 +13,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libcsa2.so")
 SOURCES = ["csa2_api.cu", "k_append.cu", "k_index.cu", "k_index_fp4.cu", "k_topk.cu", "k_attn.cu",
-           "k_hsi.cu"]
+           "k_hsi.cu", "k_swa.cu"]
 HEADERS = ["csa2_device.cuh", "csa2_kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -736,9 +736,19 @@ size_t csa2_sparse_attn_workspace_bytes(const csa2_cache_t* c, int32_t n_queries
 
 namespace {
 // Epilogue options into the launch parameters; false when they are invalid.
-bool apply_opts(AttnParams* p, const csa2_attn_opts_t* opts, bool decode, int32_t q0) {
+bool apply_opts(AttnParams* p, const csa2_attn_opts_t* opts, bool decode, int32_t q0,
+                int64_t row0) {
   if (!opts) return true;
   p->sink = opts->sink;
+  const bool f8 = opts->swa_codes || opts->swa_rope || opts->swa_scales;
+  if (f8) {
+    if (!opts->swa_codes || !opts->swa_rope || !opts->swa_scales || !aligned16(opts->swa_codes) ||
+        !aligned16(opts->swa_rope) || (reinterpret_cast<uintptr_t>(opts->swa_scales) & 7u))
+      return false;
+    p->swa_codes = opts->swa_codes + row0 * 448;
+    p->swa_rope = static_cast<const uint16_t*>(opts->swa_rope) + row0 * 64;
+    p->swa_scales = opts->swa_scales + row0 * 8;
+  }
   if (opts->rope_out) {
     if (decode && !opts->rope_pos) return false;
     if (opts->rope_base < 0.0 || opts->rope_base != opts->rope_base) return false;
@@ -772,7 +782,8 @@ csa2_status_t csa2_sparse_attn_decode_ex(const csa2_cache_t* c, int32_t nq,
   const int W = c->cfg.swa;
   if (!q || !topk_idx || !out || !aligned16(q) || !aligned16(out) || !aligned16(topk_idx))
     return CSA2_ERR_INVALID_ARG;
-  if (W > 0 && (!swa_kv || !aligned16(swa_kv))) return CSA2_ERR_INVALID_ARG;
+  const bool f8 = opts && opts->swa_codes;
+  if (W > 0 && !f8 && (!swa_kv || !aligned16(swa_kv))) return CSA2_ERR_INVALID_ARG;
   if (lse && !aligned16(lse)) return CSA2_ERR_INVALID_ARG;
   if (workspace && !aligned16(workspace)) return CSA2_ERR_INVALID_ARG;
   if (seq_ids)
@@ -805,7 +816,7 @@ csa2_status_t csa2_sparse_attn_decode_ex(const csa2_cache_t* c, int32_t nq,
     p->scale_log2 = scale * 1.4426950408889634f;
     p->prefill = 0;
     p->splits = split ? 2 : 1;
-    if (!apply_opts(p, opts, true, q0)) { st = CSA2_ERR_INVALID_ARG; break; }
+    if (!apply_opts(p, opts, true, q0, (int64_t)q0 * W)) { st = CSA2_ERR_INVALID_ARG; break; }
     if (split) {
       p->part = static_cast<float*>(workspace);
       p->counter = reinterpret_cast<uint32_t*>(
@@ -823,7 +834,7 @@ csa2_status_t csa2_sparse_attn_decode_ex(const csa2_cache_t* c, int32_t nq,
     CUtensorMap tm_q, tm_swa;
     const uint16_t* qb = static_cast<const uint16_t*>(q) + (int64_t)q0 * H * kHeadDim;
     if (!make_map(&tm_q, qb, (uint64_t)n * H, kHeadDim, 64, kAttnHeadGroup)) { st = CSA2_ERR_CUDA; break; }
-    if (W > 0) {
+    if (W > 0 && !f8) {
       const uint16_t* sb = static_cast<const uint16_t*>(swa_kv) + (int64_t)q0 * W * kHeadDim;
       if (!make_map(&tm_swa, sb, (uint64_t)n * W, kHeadDim, 64, 128)) { st = CSA2_ERR_CUDA; break; }
     } else {
@@ -856,9 +867,10 @@ csa2_status_t csa2_sparse_attn_prefill_ex(const csa2_cache_t* c, int32_t seq, in
   if (!q || !topk_idx || !out || !aligned16(q) || !aligned16(out) || !aligned16(topk_idx))
     return CSA2_ERR_INVALID_ARG;
   if (lse && !aligned16(lse)) return CSA2_ERR_INVALID_ARG;
+  const bool f8 = opts && opts->swa_codes;
   if (W > 0) {
-    if (!swa_kv || !aligned16(swa_kv) || swa_pos0 < 0 || swa_pos0 > pos0 || n_swa_rows <= 0 ||
-        pos0 + nq - 1 - swa_pos0 >= n_swa_rows)
+    if ((!f8 && (!swa_kv || !aligned16(swa_kv))) || swa_pos0 < 0 || swa_pos0 > pos0 ||
+        n_swa_rows <= 0 || pos0 + nq - 1 - swa_pos0 >= n_swa_rows)
       return CSA2_ERR_INVALID_ARG;
   }
   const int H = c->cfg.n_heads, k = c->cfg.topk;
@@ -884,12 +896,12 @@ csa2_status_t csa2_sparse_attn_prefill_ex(const csa2_cache_t* c, int32_t seq, in
   p->pos0 = pos0;
   p->swa_pos0 = swa_pos0;
   p->splits = 1;
-  csa2_status_t st = apply_opts(p, opts, false, 0) ? CSA2_OK : CSA2_ERR_INVALID_ARG;
+  csa2_status_t st = apply_opts(p, opts, false, 0, 0) ? CSA2_OK : CSA2_ERR_INVALID_ARG;
   CUtensorMap tm_q, tm_swa;
   if (st == CSA2_OK && !make_map(&tm_q, q, (uint64_t)nq * H, kHeadDim, 64, kAttnHeadGroup))
     st = CSA2_ERR_CUDA;
   if (st == CSA2_OK) {
-    if (W > 0) {
+    if (W > 0 && !f8) {
       if (!make_map(&tm_swa, swa_kv, (uint64_t)n_swa_rows, kHeadDim, 64, 128)) st = CSA2_ERR_CUDA;
     } else {
       tm_swa = tm_q;
@@ -1113,6 +1125,17 @@ csa2_status_t csa2_index_topk_reindex_decode(const csa2_cache_t* c, int32_t nq, 
   delete tp;
   delete hp;
   return st;
+}
+
+csa2_status_t csa2_swa_fp8_quantise(int64_t n_rows, const void* rows, uint8_t* codes, void* rope,
+                                    uint8_t* scales, csa2_stream_t stream) {
+  if (n_rows < 0) return CSA2_ERR_INVALID_ARG;
+  if (n_rows == 0) return CSA2_OK;
+  if (!rows || !codes || !rope || !scales || !aligned16(rows) || !aligned16(codes) ||
+      !aligned16(rope) || (reinterpret_cast<uintptr_t>(scales) & 7u))
+    return CSA2_ERR_INVALID_ARG;
+  return cuda_status(launch_swa_fp8(static_cast<const uint16_t*>(rows), n_rows, codes,
+                                    static_cast<uint16_t*>(rope), scales, S(stream)));
 }
 
 csa2_status_t csa2_get_device_error(const csa2_cache_t* c, csa2_stream_t stream,

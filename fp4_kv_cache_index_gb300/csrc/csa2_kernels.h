@@ -164,9 +164,14 @@ struct AttnParams {
   const int64_t* rope_pos;   // decode: [nq] query positions for the output RoPE(-i)
   int32_t rope_out;          // 1: rotate the last 64 output channels by -position
   double rope_theta[32];     // RoPE frequencies base^(-2t/64) of the 32 channel pairs
+  const uint8_t* swa_codes;  // FP8 window rows (nullable): E4M3 codes [rows, 448]
+  const uint16_t* swa_rope;  //   bf16 RoPE channels [rows, 64]
+  const uint8_t* swa_scales; //   UE8M0 scales [rows, 8]
   int64_t q_base[kAttnTab];  // decode: entry offset of each query's sequence
   int32_t q_len[kAttnTab];   // decode: entries of each query's sequence
 };
+cudaError_t launch_swa_fp8(const uint16_t* rows, int64_t n, uint8_t* codes, uint16_t* rope,
+                           uint8_t* scales, cudaStream_t s);
 int attn_smem_bytes();
 // Workspace of the split-KV decode path: partials and counters.
 size_t attn_part_bytes(int64_t nq, int head_groups);

@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_arrive_expect_tx(&sm.bar_q, kHG * kHeadDim * 2);
     for (int c = 0; c < 8; ++c)
       tma_load_2d(qs + c * (kHG * 128), &tm_q, 64 * c, q * p.n_heads + hg * kHG, &sm.bar_q);
-    if (swa_first) {
+    if (swa_first && !p.swa_codes) {
       mbar_arrive_expect_tx(&sm.bar_kv, kRows * kHeadDim * 2);
       for (int c = 0; c < 8; ++c)
         tma_load_2d(kv + c * (kRows * 128), &tm_swa, 64 * c, swa_row0, &sm.bar_kv);
@@ -239,7 +239,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tile = sm.my_list[ti];
     if (tid == 0) sm.need_rescale = 0;
     // ------------------------------------------------ A: candidate rows -> kv
-    if (tile < 0) {
+    if (tile < 0 && p.swa_codes) {
+      // FP8 window rows: thread (row e, quarter q) dequantises channels
+      // [128 q, 128 q + 128): E4M3 x 2^scale is a bf16 value; the RoPE
+      // channels 448-511 are bf16 already
+      if (tid < kRows) sm.row_valid[tid] = tid < swa_count;
+      const int e = warp * 8 + (lane & 7), qq = lane >> 3;
+      const bool live = e < swa_count;
+      const int64_t row = (int64_t)swa_row0 + e;
+      const int ncb = qq < 3 ? 2 : 1;                  // FP8 column blocks of this thread
+      for (int h = 0; h < ncb; ++h) {
+        const int cb = 2 * qq + h;                     // 64 channels
+        const float sc = live ? ue8m0_value(__ldg(p.swa_scales + row * 8 + cb)) : 0.0f;
+        const uint4* src = reinterpret_cast<const uint4*>(p.swa_codes + row * 448 + 64 * cb);
+        uint8_t* rowp = kv + cb * (kRows * 128) + e * 128;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint4 c = live ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const uint32_t word = w[2 * half + i];
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+                    (__nv_fp8x2_storage_t)((word >> (16 * k)) & 0xFFFFu), __NV_E4M3);
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+                const __nv_bfloat162 bb = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+                o[2 * i + k] = *reinterpret_cast<const uint32_t*>(&bb);
+              }
+            }
+            const int chunk = 2 * v + half;
+            *reinterpret_cast<uint4*>(rowp + ((chunk ^ (e & 7)) << 4)) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        }
+      }
+      if (qq == 3) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.swa_rope + row * 64);
+        uint8_t* rowp = kv + 7 * (kRows * 128) + e * 128;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint4 c = live ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(rowp + ((v ^ (e & 7)) << 4)) = c;
+        }
+      }
+    } else if (tile < 0) {
       // issued at kernel entry
       if (tid < kRows) sm.row_valid[tid] = tid < swa_count;
       ok = mbar_wait(&sm.bar_kv, 0, p.err);

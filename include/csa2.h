@@ -456,7 +456,27 @@ typedef struct {
   const int64_t* rope_pos;
   int32_t rope_out;
   double rope_base;
+  /* FP8 window rows (all three set, or none): the rows of swa_kv in the
+   * format of csa2_swa_fp8_quantise -- E4M3 codes [rows, 448], bf16 RoPE
+   * channels [rows, 64], UE8M0 scales [rows, 8], the same row order as
+   * swa_kv (which is then ignored and may be NULL).                       */
+  const uint8_t* swa_codes;
+  const void* swa_rope;
+  const uint8_t* swa_scales;
 } csa2_attn_opts_t;
+
+/* FP8 window rows ([V41 sec 2.4.4]: the SWA KV cache stays FP8; the row is
+ * the V4 FP8 entry of [NDT sec 3.1]: 448 + 128 + 8 = 584 bytes): for each
+ * bf16 row of 512 channels, channels 0-447 as E4M3 codes with one UE8M0
+ * scale per 64 channels (OCP MX rule for E4M3 elements: exponent of the
+ * block's largest magnitude minus 8; codes of x / scale, nearest even,
+ * saturating at 448), channels 448-511 (RoPE) kept as bf16, scale byte 7
+ * zero.
+ *   rows: dev bf16 [n_rows, 512];  codes: dev u8 [n_rows, 448];  rope: dev
+ *   bf16 [n_rows, 64];  scales: dev u8 [n_rows, 8].  All 16-byte aligned
+ *   (scales: 8).                                                           */
+csa2_status_t csa2_swa_fp8_quantise(int64_t n_rows, const void* rows, uint8_t* codes,
+                                    void* rope, uint8_t* scales, csa2_stream_t stream);
 
 /* csa2_sparse_attn_decode with epilogue options (NULL: none).           */
 csa2_status_t csa2_sparse_attn_decode_ex(const csa2_cache_t* cache,
