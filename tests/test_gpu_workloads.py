@@ -21,35 +21,49 @@ def C():
     return C
 
 
-def _decode_case(C, wid, sample):
+def _decode_case(C, wid, sample, paper=False):
+    """paper=True: the pages' exact cache formats -- E2M1 + E4M3/16 main KV,
+    MXFP4 indexer keys and queries, FP8 window rows."""
     import torch
     wl = W.WORKLOADS[wid]
     n_ent = wl.n_entries()
-    cache = C.Cache(C.config(ratio=wl.ratio), [int(x) for x in n_ent])
+    layout = 1 if paper else 0
+    cache = C.Cache(C.config(ratio=wl.ratio, layout=layout, idx_layout=1 if paper else 0),
+                    [int(x) for x in n_ent])
     W.fill_cache(wl, cache)
     q_idx, w = W.dev_q_idx(wl), W.dev_w(wl)
     idx = C.csa2_index_topk_decode(cache, q_idx, w)
     outs, lses = [], []
     for l in range(wl.layers):
         lse = torch.empty(wl.batch, 64, device="cuda")
-        outs.append(bf16_host(C.csa2_sparse_attn_decode(cache, W.dev_q(wl, l), W.dev_swa(wl, l),
-                                                         idx, float(SCALE), lse=lse)))
+        if paper:
+            f8 = C.csa2_swa_fp8_quantise(W.dev_swa(wl, l))
+            o = C.csa2_sparse_attn_decode(cache, W.dev_q(wl, l), None, idx, float(SCALE),
+                                          lse=lse, swa_fp8=f8)
+        else:
+            o = C.csa2_sparse_attn_decode(cache, W.dev_q(wl, l), W.dev_swa(wl, l), idx,
+                                          float(SCALE), lse=lse)
+        outs.append(bf16_host(o))
         lses.append(lse.cpu().numpy())
     idx = idx.cpu().numpy()
     assert cache.device_error() == 0
     log = []
+    select = O.index_topk_mxfp4 if paper else O.index_topk
     for b in sample:
-        o_idx, o_sc = O.index_topk(wl.idx_k(b), wl.q_idx(b, 1)[0], wl.w(b, 1)[0], 512)
+        o_idx, o_sc = select(wl.idx_k(b), wl.q_idx(b, 1)[0], wl.w(b, 1)[0], 512)
         check_topk(idx[b], o_idx, o_sc, 512, log)
         sel = idx[b][idx[b] >= 0]
-        codes, scales = O.quantise(wl.entry_rows(b, sel), 0)
+        codes, scales = O.quantise(wl.entry_rows(b, sel), layout)
         local = np.arange(len(sel), dtype=np.int32)
         for l in range(wl.layers):
-            _, o, ol = O.sparse_attention(wl.q(l, b, 1)[0], codes, scales, 0, local,
-                                          wl.swa(l, b, 1)[0], SCALE)
+            rows = wl.swa(l, b, 1)[0]
+            if paper:
+                rows = O.swa_fp8_round_bf16(rows)
+            _, o, ol = O.sparse_attention(wl.q(l, b, 1)[0], codes, scales, layout, local,
+                                          rows, SCALE)
             check_attn(outs[l][b], o)
             assert np.allclose(lses[l][b], ol, atol=1e-3, rtol=0)
-    print(f"workload {wid}: near-ties {log}")
+    print(f"workload {wid}{' (paper cache)' if paper else ''}: near-ties {log}")
 
 
 def test_workload0_full(C):
@@ -62,6 +76,14 @@ def test_workload1_full(C):
 
 def test_workload2_sampled(C):
     _decode_case(C, 2, [0, 37, 63])
+
+
+def test_workload2_paper_cache_sampled(C):
+    _decode_case(C, 2, [0, 41, 63], paper=True)
+
+
+def test_workload1_paper_cache_full(C):
+    _decode_case(C, 1, list(range(16)), paper=True)
 
 
 def test_workload3_ragged(C):
