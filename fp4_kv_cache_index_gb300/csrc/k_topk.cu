@@ -190,21 +190,34 @@ __device__ __forceinline__ int64_t row_valid_count(const TopkParams& p, int row)
   return p.n_valid[row];
 }
 
-// Ordered compaction of one segment's candidates (keys in bins >= b1).  512
-// threads, each owning 16 consecutive scores; the score loads and the
-// histogram loads are independent and issued together, and the threshold
-// bin's count travels through shared memory, so a CTA waits on memory once.
-constexpr int kSegThreads = 512;
+// Ordered compaction of one segment's candidates (keys in bins >= b1).  256
+// threads, each owning 32 consecutive scores, in two passes over them:
+// count (after an L2 prefetch issued with the histogram loads), then re-read
+// the 8-score chunks that hold candidates and write them in index order.
+// Holding no scores across the block-wide steps keeps the registers low
+// enough for 8 CTAs per SM: a batch of 64 x 128K scores is one wave.
+constexpr int kSegThreads = 256;
 constexpr int kSegWarps = kSegThreads / 32;
-constexpr int kSegPer = kTopkSegLen / kSegThreads;  // 16
-constexpr int kSegBinsPer = kBins / kSegThreads;    // 4
+constexpr int kSegPer = kTopkSegLen / kSegThreads;  // 32
+constexpr int kSegBinsPer = kBins / kSegThreads;    // 8
 struct SegShared {
   uint32_t warp_sum[kSegWarps];
   uint32_t sel_bin, sel_above, sel_count;
 };
 
-__global__ void __launch_bounds__(kSegThreads) k_topk_seg(const __grid_constant__ TopkParams p,
-                                                          int row0) {
+// Scores e0 + 8q .. e0 + 8q + 7 of the row (0 past n).
+__device__ __forceinline__ void seg_chunk(const ScoreRow& srow, int64_t e0, int q, int64_t n,
+                                          bool vec, float (&v)[8]) {
+  if (vec) {
+    srow.load8(e0 + 8 * q, v);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = (e0 + 8 * q + i < n) ? srow.at(e0 + 8 * q + i) : 0.0f;
+  }
+}
+
+__global__ void __launch_bounds__(kSegThreads, 8) k_topk_seg(const __grid_constant__ TopkParams p,
+                                                             int row0) {
   __shared__ SegShared sh;
   const int row = row0 + blockIdx.y, seg = blockIdx.x, tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
@@ -218,19 +231,18 @@ __global__ void __launch_bounds__(kSegThreads) k_topk_seg(const __grid_constant_
   }
   const ScoreRow srow = score_row(p, row);
   const int64_t e0 = s0 + (int64_t)tid * kSegPer;
-  float v[kSegPer];
   const bool vec = srow.aligned16() && e0 + kSegPer <= n;
-  if (vec) {
-#pragma unroll
-    for (int q = 0; q < kSegPer / 8; ++q) srow.load8(e0 + 8 * q, v + 8 * q);
-  } else {
-#pragma unroll
-    for (int i = 0; i < kSegPer; ++i) v[i] = (e0 + i < n) ? srow.at(e0 + i) : 0.0f;
+  if (e0 < n) {
+    const char* a = static_cast<const char*>(srow.base) + e0 * (srow.bf16 ? 2 : 4);
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
   }
-  // threshold bin: thread t holds bins [4t, 4t + 4)
-  const uint4 hv = __ldg(reinterpret_cast<const uint4*>(p.key_hist + (int64_t)row * kBins) + tid);
-  const uint32_t h[kSegBinsPer] = {hv.x, hv.y, hv.z, hv.w};
-  const uint32_t hs = h[0] + h[1] + h[2] + h[3];
+  // threshold bin: thread t holds bins [8t, 8t + 8)
+  const uint4* hp = reinterpret_cast<const uint4*>(p.key_hist + (int64_t)row * kBins) + 2 * tid;
+  const uint4 ha = __ldg(hp), hb = __ldg(hp + 1);
+  const uint32_t h[kSegBinsPer] = {ha.x, ha.y, ha.z, ha.w, hb.x, hb.y, hb.z, hb.w};
+  uint32_t hs = 0;
+#pragma unroll
+  for (int i = 0; i < kSegBinsPer; ++i) hs += h[i];
   uint32_t suf = hs;  // inclusive suffix over the threads of the warp
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -239,9 +251,9 @@ __global__ void __launch_bounds__(kSegThreads) k_topk_seg(const __grid_constant_
   }
   if (lane == 0) sh.warp_sum[warp] = suf;
   __syncthreads();
-  for (int w = warp + 1; w < kSegWarps; ++w) suf += sh.warp_sum[w];   // bins >= 4 tid
+  for (int w = warp + 1; w < kSegWarps; ++w) suf += sh.warp_sum[w];   // bins >= 8 tid
   const uint32_t k = (uint32_t)p.k;
-  uint32_t above_mine = suf - hs;                                      // bins >= 4 tid + 4
+  uint32_t above_mine = suf - hs;                                      // bins >= 8 tid + 8
 #pragma unroll
   for (int i = kSegBinsPer - 1; i >= 0; --i) {
     if (above_mine < k && above_mine + h[i] >= k) {
@@ -254,10 +266,17 @@ __global__ void __launch_bounds__(kSegThreads) k_topk_seg(const __grid_constant_
   __syncthreads();
   const uint32_t b1 = sh.sel_bin;
   if (sh.sel_above + sh.sel_count > (uint32_t)kCandCap) return;  // the row falls back
-  // ordered compaction
-  uint32_t cnt = 0;
+  // pass 1: which of the 32 scores are candidates
+  uint32_t mask = 0;
 #pragma unroll
-  for (int i = 0; i < kSegPer; ++i) cnt += (e0 + i < n && (score_key(v[i]) >> 21) >= b1);
+  for (int q = 0; q < kSegPer / 8; ++q) {
+    float v[8];
+    seg_chunk(srow, e0, q, n, vec, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (e0 + 8 * q + i < n && (score_key(v[i]) >> 21) >= b1) mask |= 1u << (8 * q + i);
+  }
+  const uint32_t cnt = (uint32_t)__popc(mask);
   uint32_t incl = cnt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -273,14 +292,22 @@ __global__ void __launch_bounds__(kSegThreads) k_topk_seg(const __grid_constant_
     if (w < warp) before += ws;
     total += ws;
   }
+  // pass 2: the chunks holding candidates again, written in index order
   uint32_t pos = before + incl - cnt;
 #pragma unroll
-  for (int i = 0; i < kSegPer; ++i) {
-    const uint32_t key = score_key(v[i]);
-    if (e0 + i < n && (key >> 21) >= b1 && pos < (uint32_t)kCandCap) {
-      out[4 + pos] = key;
-      out[4 + kCandCap + pos] = (uint32_t)(e0 + i);
-      ++pos;
+  for (int q = 0; q < kSegPer / 8; ++q) {
+    if (((mask >> (8 * q)) & 0xFFu) == 0u) continue;
+    float v[8];
+    seg_chunk(srow, e0, q, n, vec, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if ((mask >> (8 * q + i)) & 1u) {
+        if (pos < (uint32_t)kCandCap) {
+          out[4 + pos] = score_key(v[i]);
+          out[4 + kCandCap + pos] = (uint32_t)(e0 + 8 * q + i);
+        }
+        ++pos;
+      }
     }
   }
   if (tid == 0) out[0] = total < (uint32_t)kCandCap ? total : (uint32_t)kCandCap;
