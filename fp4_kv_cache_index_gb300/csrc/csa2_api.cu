@@ -729,7 +729,7 @@ csa2_status_t csa2_index_topk_prefill(const csa2_cache_t* c, int32_t seq, int32_
 
 size_t csa2_sparse_attn_workspace_bytes(const csa2_cache_t* c, int32_t n_queries) {
   if (!c || n_queries < 0) return 0;
-  return attn_part_bytes(n_queries, c->cfg.n_heads / kAttnHeadGroup);
+  return kAttnSplitToken;
 }
 
 }  // extern "C"
@@ -797,8 +797,7 @@ csa2_status_t csa2_sparse_attn_decode_ex(const csa2_cache_t* c, int32_t nq,
   for (int q0 = 0; q0 < nq; q0 += kAttnTab) {
     const int n = std::min(kAttnTab, nq - q0);
     // two CTAs per (query, head group) when one each would leave SMs idle
-    const bool split = workspace && ws_bytes >= attn_part_bytes(n, G) &&
-                       (int64_t)n * G < c->num_sms;
+    const bool split = workspace && ws_bytes >= kAttnSplitToken && (int64_t)n * G < c->num_sms;
     std::memset(p, 0, sizeof(AttnParams));
     p->topk_idx = topk_idx + (int64_t)q0 * k;
     p->swa_len = swa_len ? swa_len + q0 : nullptr;
@@ -817,15 +816,6 @@ csa2_status_t csa2_sparse_attn_decode_ex(const csa2_cache_t* c, int32_t nq,
     p->prefill = 0;
     p->splits = split ? 2 : 1;
     if (!apply_opts(p, opts, true, q0, (int64_t)q0 * W)) { st = CSA2_ERR_INVALID_ARG; break; }
-    if (split) {
-      p->part = static_cast<float*>(workspace);
-      p->counter = reinterpret_cast<uint32_t*>(
-          static_cast<uint8_t*>(workspace) + attn_part_bytes(n, G) - (size_t)n * G * 4);
-      if (cudaMemsetAsync(p->counter, 0, (size_t)n * G * 4, S(stream)) != cudaSuccess) {
-        st = CSA2_ERR_CUDA;
-        break;
-      }
-    }
     for (int i = 0; i < n; ++i) {
       const int s = seq_ids ? seq_ids[q0 + i] : q0 + i;
       p->q_base[i] = c->off[s];

@@ -143,9 +143,7 @@ struct AttnParams {
   const uint8_t* codes;
   const uint8_t* scales;
   uint16_t* out;             // bf16 [nq, n_heads, 512]
-  int32_t splits;            // CTAs per (query, 64-head group): 1 or 2
-  float* part;               // splits == 2: [nq * groups, 2, m | l | O] fp32 partials
-  uint32_t* counter;         // splits == 2: [nq * groups] arrival counters, zero on entry
+  int32_t splits;            // CTAs per (query, 64-head group): 1, or 2 (a cluster)
   float* lse;                // nullable [nq, n_heads]
   uint32_t* err;
   int32_t nq;
@@ -173,9 +171,10 @@ struct AttnParams {
 cudaError_t launch_swa_fp8(const uint16_t* rows, int64_t n, uint8_t* codes, uint16_t* rope,
                            uint8_t* scales, cudaStream_t s);
 int attn_smem_bytes();
-// Workspace of the split-KV decode path: partials and counters.
-size_t attn_part_bytes(int64_t nq, int head_groups);
 constexpr int kAttnHeadGroup = 64;
+// The two-CTA decode split needs no scratch memory: a caller opts in by
+// passing a workspace of at least this many bytes.
+constexpr size_t kAttnSplitToken = 16;
 cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_swa,
                         cudaStream_t s);
 

@@ -9,11 +9,11 @@
 // FP4 before attention (V4.1 report, section 2.4.4).
 //
 // One CTA = one query x 64 heads x one share of the candidate tiles.  With
-// `splits` = 2 (decode with a workspace) the tiles of a query alternate
-// between two CTAs, each writes its unnormalised fp32 partial (running max,
-// sum, O) to the workspace, and the second to finish merges both in a fixed
-// operand order (threadfence + atomic counter, no waiting); with splits = 1 a
-// CTA takes every tile.  Candidates come in tiles of 128 rows: the
+// `splits` = 2 (small decode batches) the tiles of a query alternate between
+// the two CTAs of a cluster, which merge their unnormalised fp32 states
+// (running max, sum, O) exactly through distributed shared memory, each
+// finalising one half of the head dimension; with splits = 1 a CTA takes
+// every tile.  Candidates come in tiles of 128 rows: the
 // window tile (TMA straight into swizzled shared memory) and the top-k tiles
 // (each thread loads a quarter of an entry's 256 B of codes plus its scale
 // bytes into registers, one tile ahead; then E2M1 -> bf16 via byte permutes
@@ -45,7 +45,6 @@ constexpr int kQOff = kKvOff + kRows * kHeadDim * 2;   // 8 x [64 x 128 B]
 constexpr int kPOff = kQOff + kHG * kHeadDim * 2;      // 2 x [64 x 128 B]
 constexpr int kIdxOff = kPOff + kHG * kRows * 2;        // the query's top-k row
 constexpr int kSmallOff = kIdxOff + 2048 * 4;
-constexpr int kPartFloats = 2 * kHG + kHG * kHeadDim;   // m, l, O of one split
 struct Small {
   float red_max[4][kHG];
   float red_sum[4][kHG];
@@ -60,7 +59,6 @@ struct Small {
   int32_t n_all;
   float rope_c[32], rope_s[32];  // output RoPE(-i): cos, sin of each channel pair
   int32_t need_rescale;
-  int32_t merge;
   uint32_t tmem;
   uint64_t bar_q, bar_kv, bar_mma;
 };
@@ -488,8 +486,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     return o;
   };
+  // Output rows go through shared memory: bf16 [64 heads][dw] in the Q
+  // buffer (free after the last S product), then 16-byte stores of each
+  // head's d range [d0, d0 + dw).
+  uint16_t* out_s = reinterpret_cast<uint16_t*>(qs);
+  auto store_rows = [&](int d0, int dw) {
+    const int per_row = dw / 8;
+    for (int k = tid; k < kHG * per_row; k += kThreads) {
+      const int h = k / per_row, c = k % per_row;
+      *reinterpret_cast<uint4*>(p.out + (out_row + h) * kHeadDim + d0 + 8 * c) =
+          *reinterpret_cast<const uint4*>(out_s + h * dw + 8 * c);
+    }
+  };
+  const bool have = ok && n_tiles > 0;
   if (p.splits == 1) {
-    if (ok && n_tiles > 0) {
+    if (have) {
       if (tid < kHG) {
         const float l = sm.l[tid], m = sm.m[tid], z = sink_log2(tid);
         const float M = fmaxf(m, z);
@@ -508,87 +519,102 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const float o = finish(i, __uint_as_float(r[c]) * sm.alpha[16 * hh + c]);
-          p.out[(out_row + 16 * hh + c) * kHeadDim + d] = (uint16_t)float_to_bf16_bits(o);
+          out_s[(16 * hh + c) * kHeadDim + d] = (uint16_t)float_to_bf16_bits(o);
         }
       }
+      __syncthreads();
+      store_rows(0, kHeadDim);
     } else if (n_tiles == 0) {
       // no candidate at all: output 0, lse = the sink alone (or -inf)
       for (int i = tid; i < kHG * kHeadDim; i += kThreads) p.out[out_row * kHeadDim + i] = 0;
       if (p.lse && tid < kHG)
         p.lse[out_row + tid] = p.sink ? p.sink[hg * kHG + tid] : -INFINITY;
     }
-  } else if (ok) {
-    // ---- split-KV: the CTA that finishes second merges.  If the partner has
-    //      already published its partial, this CTA merges at once without
-    //      publishing its own; otherwise it publishes, then counts itself in.
-    float* mine = p.part + ((int64_t)qh * 2 + split) * kPartFloats;
-    float* other = p.part + ((int64_t)qh * 2 + (split ^ 1)) * kPartFloats;
-    if (tid == 0) sm.merge = atomicAdd(p.counter + qh, 0u) == 1u;
-    __syncthreads();
-    if (!sm.merge) {
-    if (tid < kHG) {
-      mine[tid] = n_tiles > 0 ? sm.m[tid] : -INFINITY;
-      mine[kHG + tid] = n_tiles > 0 ? sm.l[tid] : 0.0f;
-    }
-    if (n_tiles > 0) {
+  } else {
+    // ---- split-KV over a cluster of two CTAs (cluster rank = split).  Each
+    //      stages, in its free KV buffer, its unnormalised O^T for the d half
+    //      that the partner finalises; after a cluster barrier each finalises
+    //      its own half d in [256 split, 256 split + 256) from its TMEM and
+    //      the partner's staged copy, with the partner's (m, l) read through
+    //      distributed shared memory:
+    //        out = (a0 * O_0 + a1 * O_1) / (a0 * l0 + a1 * l1),
+    //      operands in split order.  Staging layout [half][warp][4][lane][4
+    //      floats]: a warp's 16-byte accesses are contiguous.
+    const uint32_t peer = (uint32_t)(split ^ 1);
+    float* stage = reinterpret_cast<float*>(kv);
+    if (tid < kHG && !have) { sm.m[tid] = -INFINITY; sm.l[tid] = 0.0f; }
+    if (have) {
 #pragma unroll 1
-      for (int i = 0; i < 4; ++i) {
+      for (int ii = 0; ii < 2; ++ii) {
+        const int i = 2 * (int)peer + ii;
         uint32_t r[16];
         tmem_ld16(tmem + lane_addr + o_col + 64 * i + 16 * hh, r);
-        const int d = 128 * i + quad * 32 + lane;
+        float4* dst = reinterpret_cast<float4*>(stage) + ((ii * 16 + warp) * 4) * 32 + lane;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) mine[2 * kHG + (16 * hh + c) * kHeadDim + d] = __uint_as_float(r[c]);
+        for (int v = 0; v < 4; ++v)
+          dst[32 * v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                    __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
       }
     }
-    __threadfence();
+    cluster_arrive();
+    cluster_wait();
+    if (tid < kHG) {
+      const float m_ot = ld_dsmem_f32(dsmem_addr(smem_u32(&sm.m[tid]), peer));
+      const float l_ot = ld_dsmem_f32(dsmem_addr(smem_u32(&sm.l[tid]), peer));
+      const float m_me = sm.m[tid], l_me = sm.l[tid];
+      const float m0 = split == 0 ? m_me : m_ot, m1 = split == 0 ? m_ot : m_me;
+      const float l0 = split == 0 ? l_me : l_ot, l1 = split == 0 ? l_ot : l_me;
+      const float z = sink_log2(tid);
+      const float M = fmaxf(fmaxf(m0, m1), z);
+      const float a0 = (m0 == -INFINITY) ? 0.0f : fast_exp2(m0 - M);
+      const float a1 = (m1 == -INFINITY) ? 0.0f : fast_exp2(m1 - M);
+      const float L = a0 * l0 + a1 * l1 + ((z == -INFINITY) ? 0.0f : fast_exp2(z - M));
+      const float c_me = L > 0.0f ? (split == 0 ? a0 : a1) / L : 0.0f;
+      const float c_ot = L > 0.0f ? (split == 0 ? a1 : a0) / L : 0.0f;
+      sm.alpha[tid] = have ? c_me : 0.0f;               // weight of this CTA's O
+      sm.red_max[0][tid] = (l_ot > 0.0f) ? c_ot : 0.0f;  // weight of the partner's O
+      if (p.lse && split == 0)
+        p.lse[out_row + tid] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+    }
     __syncthreads();
-    if (tid == 0) sm.merge = atomicAdd(p.counter + qh, 1u) == 1u;
+    // this CTA's O^T first (warp-collective TMEM loads), then all eight
+    // 16-byte reads of the partner's staged half in flight at once, with no
+    // warp-synchronising instruction until they are used
+    uint32_t ro[2][16];
+    if (have) {
+      tmem_ld16(tmem + lane_addr + o_col + 64 * (2 * split) + 16 * hh, ro[0]);
+      tmem_ld16(tmem + lane_addr + o_col + 64 * (2 * split + 1) + 16 * hh, ro[1]);
+    }
+    const uint32_t peer_stage = dsmem_addr(smem_u32(stage), peer);
+    float4 pv[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      pv[k] = ld_dsmem_v4(peer_stage +
+                          (uint32_t)(((((k >> 2) * 16 + warp) * 4 + (k & 3)) * 32 + lane) * 16));
+#pragma unroll
+    for (int ii = 0; ii < 2; ++ii) {
+      const int i = 2 * split + ii;
+      const int d = 128 * i + quad * 32 + lane;
+      const float po[16] = {pv[4 * ii].x,     pv[4 * ii].y,     pv[4 * ii].z,     pv[4 * ii].w,
+                            pv[4 * ii + 1].x, pv[4 * ii + 1].y, pv[4 * ii + 1].z, pv[4 * ii + 1].w,
+                            pv[4 * ii + 2].x, pv[4 * ii + 2].y, pv[4 * ii + 2].z, pv[4 * ii + 2].w,
+                            pv[4 * ii + 3].x, pv[4 * ii + 3].y, pv[4 * ii + 3].z, pv[4 * ii + 3].w};
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int h = 16 * hh + c;
+        const float w_ot = sm.red_max[0][h];
+        const float o_me = have ? sm.alpha[h] * __uint_as_float(ro[ii][c]) : 0.0f;
+        const float o_ot = w_ot != 0.0f ? w_ot * po[c] : 0.0f;
+        // fixed order: split 0's term first
+        const float o = finish(i, split == 0 ? o_me + o_ot : o_ot + o_me);
+        out_s[h * 256 + (d - 256 * split)] = (uint16_t)float_to_bf16_bits(o);
+      }
+    }
+    // the partner's shared memory is read no more: it may exit once it waits
+    cluster_arrive();
     __syncthreads();
-    }
-    if (sm.merge) {
-      __threadfence();
-      // final = (a0 * O_0 + a1 * O_1) / (a0 * l0 + a1 * l1), operands in split
-      // order; this CTA's O comes from TMEM, the partner's from the workspace
-      if (tid < kHG) {
-        const float m_me = sm.m[tid], l_me = n_tiles > 0 ? sm.l[tid] : 0.0f;
-        const float m_me2 = n_tiles > 0 ? m_me : -INFINITY;
-        const float m_ot = __ldcg(other + tid), l_ot = __ldcg(other + kHG + tid);
-        const float m0 = split == 0 ? m_me2 : m_ot, m1 = split == 0 ? m_ot : m_me2;
-        const float l0 = split == 0 ? l_me : l_ot, l1 = split == 0 ? l_ot : l_me;
-        const float z = sink_log2(tid);
-        const float M = fmaxf(fmaxf(m0, m1), z);
-        const float a0 = (m0 == -INFINITY) ? 0.0f : fast_exp2(m0 - M);
-        const float a1 = (m1 == -INFINITY) ? 0.0f : fast_exp2(m1 - M);
-        const float L = a0 * l0 + a1 * l1 + ((z == -INFINITY) ? 0.0f : fast_exp2(z - M));
-        const float c_me = L > 0.0f ? (split == 0 ? a0 : a1) / L : 0.0f;
-        const float c_ot = L > 0.0f ? (split == 0 ? a1 : a0) / L : 0.0f;
-        sm.alpha[tid] = (n_tiles > 0) ? c_me : 0.0f;     // weight of this CTA's O
-        sm.red_max[0][tid] = (l_ot > 0.0f) ? c_ot : 0.0f; // weight of the partner's O
-        if (p.lse) p.lse[out_row + tid] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
-      }
-      __syncthreads();
-      const bool have_me = n_tiles > 0;
-#pragma unroll 1
-      for (int i = 0; i < 4; ++i) {
-        const int d = 128 * i + quad * 32 + lane;
-        float po[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) po[c] = __ldcg(other + 2 * kHG + (16 * hh + c) * kHeadDim + d);
-        uint32_t r[16];
-        if (have_me) tmem_ld16(tmem + lane_addr + o_col + 64 * i + 16 * hh, r);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int h = 16 * hh + c;
-          const float w_ot = sm.red_max[0][h];
-          const float o_me = have_me ? sm.alpha[h] * __uint_as_float(r[c]) : 0.0f;
-          const float o_ot = w_ot != 0.0f ? w_ot * po[c] : 0.0f;
-          // fixed order: split 0's term first
-          const float o = finish(i, split == 0 ? o_me + o_ot : o_ot + o_me);
-          p.out[(out_row + h) * kHeadDim + d] = (uint16_t)float_to_bf16_bits(o);
-        }
-      }
-      if (tid == 0) p.counter[qh] = 0u;   // ready for the next call
-    }
+    store_rows(256 * split, 256);
+    cluster_wait();
   }
   tc_fence_before();
   __syncthreads();
@@ -601,10 +627,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 int attn_smem_bytes() { return kSmemBytes; }
-size_t attn_part_bytes(int64_t nq, int head_groups) {
-  return (size_t)nq * head_groups * (2 * kPartFloats * sizeof(float) + sizeof(uint32_t));
-}
-
 cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_swa,
                         cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -612,8 +634,24 @@ cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tm_q, const CUte
   if (e != cudaSuccess) return e;
   const int64_t blocks = (int64_t)p.nq * (p.n_heads / kHG) * p.splits;
   if (blocks <= 0) return cudaSuccess;
-  k_attn<<<(unsigned)blocks, kThreads, kSmemBytes, s>>>(p, tm_q, tm_swa);
-  return cudaGetLastError();
+  if (p.splits == 1) {
+    k_attn<<<(unsigned)blocks, kThreads, kSmemBytes, s>>>(p, tm_q, tm_swa);
+    return cudaGetLastError();
+  }
+  // splits == 2: the two CTAs of a (query, head group) form a cluster
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_attn, p, tm_q, tm_swa);
 }
 
 }  // namespace csa2

@@ -388,7 +388,9 @@ csa2_status_t csa2_index_topk_decode_bf16(const csa2_cache_t* cache,
 
 /* ---- sparse attention -------------------------------------------------- */
 
-/* Workspace bytes of csa2_sparse_attn_decode for n_queries queries. */
+/* Workspace bytes of csa2_sparse_attn_decode for n_queries queries: a small
+ * constant, since the two-CTA split keeps its partial states on chip and a
+ * workspace only opts in to it. */
 size_t csa2_sparse_attn_workspace_bytes(const csa2_cache_t* cache,
                                         int32_t n_queries);
 
@@ -405,11 +407,12 @@ size_t csa2_sparse_attn_workspace_bytes(const csa2_cache_t* cache,
  *   topk_idx: dev int32 [n_queries, topk] (-1 = unused slot);  seq_ids: host
  *   [n_queries] or NULL (query i reads sequence i);  out: dev bf16
  *   [n_queries, n_heads, head_dim];  lse: nullable dev fp32 [n_queries,
- *   n_heads];  workspace: nullable dev scratch of
- *   csa2_sparse_attn_workspace_bytes(cache, n_queries) bytes -- with it a
- *   small batch spreads each query's candidates over two CTAs whose partial
- *   softmax states are merged exactly (the output is the same function;
- *   without it one CTA per query does all the work).  An index >= the
+ *   n_heads];  workspace: nullable dev buffer of at least
+ *   csa2_sparse_attn_workspace_bytes(cache, n_queries) bytes (not written)
+ *   -- with it a small batch spreads each query's candidates over a cluster
+ *   of two CTAs whose partial softmax states are merged exactly on chip (the
+ *   output is the same function; without it one CTA per query does all the
+ *   work).  An index >= the
  *   sequence's length is skipped and sets CSA2_ERR_DEVICE in the device
  *   error word.                                                             */
 csa2_status_t csa2_sparse_attn_decode(const csa2_cache_t* cache,
