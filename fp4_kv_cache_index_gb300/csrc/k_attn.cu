@@ -13,20 +13,23 @@
 // the two CTAs of a cluster, which merge their unnormalised fp32 states
 // (running max, sum, O) exactly through distributed shared memory, each
 // finalising one half of the head dimension; with splits = 1 a CTA takes
-// every tile.  Candidates come in tiles of 128 rows: the
-// window tile (TMA straight into swizzled shared memory) and the top-k tiles
-// (each thread loads a quarter of an entry's 256 B of codes plus its scale
-// bytes into registers, one tile ahead; then E2M1 -> bf16 via byte permutes
-// and a bf16 scale multiply, written to shared memory in the MMA layout).  With the
-// candidate rows as the MMA M dimension:
+// every tile.  Candidates come in tiles of 128 rows: the window tile (TMA
+// straight into swizzled shared memory) and the top-k tiles (each thread
+// loads 64 code bytes of one entry plus their scale bytes into registers,
+// one tile ahead; then E2M1 -> bf16 via byte permutes and a bf16 scale
+// multiply, written to shared memory in the MMA layout).  With the candidate
+// rows as the MMA M dimension:
 //     S^T[128 x 64]  = KV[128 x 512] * Q[64 x 512]^T        (K-major A and B)
 //     O^T[512 x 64] += KV^T[512 x 128] * P^T[128 x 64]^T     (MN-major A)
 // both on tcgen05 with fp32 accumulators in TMEM; the same swizzled KV tile
 // serves as the K-major A of the first product and the MN-major A of the
-// second.  Online softmax (base 2) runs across TMEM lanes: each thread holds
-// one candidate row, per-head maxima and sums use a warp reduce-scatter and a
-// 4-way combine through shared memory; O^T is rescaled in TMEM only when a
-// head's running maximum grows by more than 2^8.
+// second.  The single KV buffer is refilled in two channel halves: the next
+// tile's first half as soon as the O^T products that read it are done (while
+// the others run), and S^T of that half while the second half is written.
+// Online softmax (base 2) runs across TMEM lanes: each thread holds one
+// candidate row; a head's running maximum moves (with a reduce-scatter over
+// the rows and a rescale of O^T in TMEM) only when a tile holds a logit more
+// than 2^8 above it, and the row sums are kept per thread and reduced once.
 #include "csa2_device.cuh"
 #include "csa2_kernels.h"
 
@@ -58,9 +61,8 @@ struct Small {
   int32_t n_tiles;
   int32_t n_all;
   float rope_c[32], rope_s[32];  // output RoPE(-i): cos, sin of each channel pair
-  int32_t need_rescale;
   uint32_t tmem;
-  uint64_t bar_q, bar_kv, bar_mma;
+  uint64_t bar_q, bar_kv, bar_mma, bar_o[2];
 };
 constexpr int kSmemBytes = kSmallOff + (int)sizeof(Small) + 1024;
 
@@ -146,6 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.bar_q, 1);
     mbar_init(&sm.bar_kv, 1);
     mbar_init(&sm.bar_mma, 1);
+    mbar_init(&sm.bar_o[0], 1);
+    mbar_init(&sm.bar_o[1], 1);
     fence_barrier_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_swa);
@@ -199,62 +203,117 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   const int n_tiles = sm.n_tiles;
 
+  // Candidate rows reach the KV buffer in two halves of four 64-channel
+  // chunks (16 KB each), so that the next tile's first half is written while
+  // the tensor core still reads the second half for O^T, and the first half
+  // of S^T is computed while the second half is written.
+  //
   // Gather of one top-k tile into registers: thread (entry e = 8 warp +
-  // lane % 8, quarter q = lane / 8) loads bytes [64 q, 64 q + 64) of entry e's
-  // codes and the scales of its 128 channels.  Issued one tile ahead, so the
-  // loads are in flight while the previous tile runs on the tensor cores.
+  // lane % 8, quarter q = lane / 8) loads, for each half h, the 32 code bytes
+  // of channel chunk 4 h + q of entry e and that chunk's scale bytes (two
+  // UE8M0 or four E4M3).  Issued one tile ahead, so the loads are in flight
+  // while the tensor core and the softmax work on the current tile.
   const int g_e = warp * 8 + (lane & 7), g_q = lane >> 3;
   uint4 cw[4];
-  uint2 scw;
+  uint32_t scw[2];
   auto prefetch_tile = [&](int j) {
     const int32_t s = idx_s[j * kRows + g_e];
     if (s >= 0) {
       const int64_t row = base + s;
-      const uint4* src = reinterpret_cast<const uint4*>(p.codes + row * kCodeBytes + g_q * 64);
+      const uint8_t* src = p.codes + row * kCodeBytes + g_q * 32;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) cw[i] = __ldg(src + i);
-      if (p.layout == 0)
-        scw = make_uint2(__ldg(reinterpret_cast<const uint32_t*>(p.scales + row * 16) + g_q), 0u);
-      else
-        scw = __ldg(reinterpret_cast<const uint2*>(p.scales + row * 32) + g_q);
+      for (int h = 0; h < 2; ++h) {
+        cw[2 * h] = __ldg(reinterpret_cast<const uint4*>(src + 128 * h));
+        cw[2 * h + 1] = __ldg(reinterpret_cast<const uint4*>(src + 128 * h + 16));
+        if (p.layout == 0)
+          scw[h] = __ldg(reinterpret_cast<const uint16_t*>(p.scales + row * 16 + 8 * h + 2 * g_q));
+        else
+          scw[h] = __ldg(reinterpret_cast<const uint32_t*>(p.scales + row * 32 + 16 * h + 4 * g_q));
+      }
     } else {
 #pragma unroll
       for (int i = 0; i < 4; ++i) cw[i] = make_uint4(0u, 0u, 0u, 0u);
-      scw = make_uint2(0u, 0u);
+      scw[0] = scw[1] = 0u;
     }
   };
+  // the next top-k tile of this CTA's list after position `from`
+  auto next_topk_after = [&](int from) {
+    int j = from + 1;
+    while (j < n_tiles && sm.my_list[j] < 0) ++j;
+    return j;
+  };
 
-  int next_topk = 0;  // position in tile_list of the next tile to gather
-  while (next_topk < n_tiles && sm.my_list[next_topk] < 0) ++next_topk;
-  if (next_topk < n_tiles) prefetch_tile(sm.my_list[next_topk]);
+  // MMA descriptors: bases built once, K steps added to the address field
+  // (all of shared memory is below 2^18 bytes, so the 14-bit field never
+  // carries).  S^T = KV * Q^T: K-major A and B; O^T += KV^T * P^T: MN-major A.
+  const uint64_t d_skv = sdesc_sw128(smem_u32(kv), 16, 1024);
+  const uint64_t d_sq = sdesc_sw128(smem_u32(qs), 16, 1024);
+  const uint64_t d_okv = sdesc_sw128(smem_u32(kv), kRows * 128, 1024);
+  const uint64_t d_op = sdesc_sw128(smem_u32(ps), 16, 1024);
+  constexpr uint32_t id_s = idesc_bf16_f32(128, kHG, false, false);
+  constexpr uint32_t id_o = idesc_bf16_f32(128, kHG, true, false);
+  // S^T K step ks (channels 16 ks .. 16 ks + 15)
+  auto mma_s = [&](int ks) {
+    const uint32_t ao = (uint32_t)((ks >> 2) * (kRows * 128) + (ks & 3) * 32);
+    const uint32_t bo = (uint32_t)((ks >> 2) * (kHG * 128) + (ks & 3) * 32);
+    umma_bf16(tmem + s_col, d_skv + (ao >> 4), d_sq + (bo >> 4), id_s, ks > 0 ? 1u : 0u);
+  };
+  // O^T d-block i (reads KV chunks 2 i, 2 i + 1), K step ks (rows 16 ks ..)
+  auto mma_o = [&](int i, int ks, bool first) {
+    const uint32_t ao = (uint32_t)((2 * i) * (kRows * 128) + ks * 2048);
+    const uint32_t bo = (uint32_t)((ks >> 2) * (kHG * 128) + (ks & 3) * 32);
+    umma_bf16(tmem + o_col + 64 * i, d_okv + (ao >> 4), d_op + (bo >> 4), id_o,
+              (!first || ks > 0) ? 1u : 0u);
+  };
 
-  uint32_t mma_phase = 0;
-  bool ok = true;
-  const int quad = warp & 3, hh = warp >> 2;   // TMEM lane quadrant, 16-head slice
-  const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-
-  for (int ti = 0; ti < n_tiles && ok; ++ti) {
-    const int tile = sm.my_list[ti];
-    if (tid == 0) sm.need_rescale = 0;
-    // ------------------------------------------------ A: candidate rows -> kv
-    if (tile < 0 && p.swa_codes) {
-      // FP8 window rows: thread (row e, quarter q) dequantises channels
-      // [128 q, 128 q + 128): E4M3 x 2^scale is a bf16 value; the RoPE
-      // channels 448-511 are bf16 already
-      if (tid < kRows) sm.row_valid[tid] = tid < swa_count;
-      const int e = warp * 8 + (lane & 7), qq = lane >> 3;
-      const bool live = e < swa_count;
-      const int64_t row = (int64_t)swa_row0 + e;
-      const int ncb = qq < 3 ? 2 : 1;                  // FP8 column blocks of this thread
-      for (int h = 0; h < ncb; ++h) {
-        const int cb = 2 * qq + h;                     // 64 channels
-        const float sc = live ? ue8m0_value(__ldg(p.swa_scales + row * 8 + cb)) : 0.0f;
-        const uint4* src = reinterpret_cast<const uint4*>(p.swa_codes + row * 448 + 64 * cb);
-        uint8_t* rowp = kv + cb * (kRows * 128) + e * 128;
+  // Half h of a tile's rows into the KV buffer (all threads).  Top-k tiles
+  // come from the registers: E2M1 -> bf16 via byte permutes and a bf16 scale
+  // multiply.  FP8 window rows come from global memory: E4M3 x 2^scale is a
+  // bf16 value; the RoPE channels 448-511 are bf16 already.  Written in the
+  // MMA layout (128-byte rows, 16-byte pieces swizzled by row).
+  auto fill_half = [&](int tile, int h, auto&& hook) {
+    const int c = 4 * h + g_q;                       // channel chunk of this thread
+    uint8_t* rowp = kv + c * (kRows * 128) + g_e * 128;
+    if (tile >= 0) {
+      if (h == 0 && tid < kRows) sm.row_valid[tid] = idx_s[tile * kRows + tid] >= 0;
+      const uint32_t words[8] = {cw[2 * h].x,     cw[2 * h].y,     cw[2 * h].z,     cw[2 * h].w,
+                                 cw[2 * h + 1].x, cw[2 * h + 1].y, cw[2 * h + 1].z, cw[2 * h + 1].w};
+      uint32_t s2[4];
+      if (p.layout == 0) {                           // one UE8M0 scale per 32 channels
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          const uint32_t s16 = float_to_bf16_bits(ue8m0_value((scw[h] >> (8 * g)) & 0xFFu));
+          s2[2 * g] = s2[2 * g + 1] = s16 | (s16 << 16);
+        }
+      } else {                                       // one E4M3 scale per 16 channels
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const uint32_t s16 = float_to_bf16_bits(fabsf(e4m3_value((scw[h] >> (8 * g)) & 0xFFu)));
+          s2[g] = s16 | (s16 << 16);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {                  // 8 channels per piece
+        uint32_t v[4];
+        e2m1x8_to_bf16x8(words[k], v);
+        const uint32_t s = s2[k >> 1];
+        uint4 o;
+        o.x = bf16x2_mul(v[0], s); o.y = bf16x2_mul(v[1], s);
+        o.z = bf16x2_mul(v[2], s); o.w = bf16x2_mul(v[3], s);
+        *reinterpret_cast<uint4*>(rowp + ((k ^ (g_e & 7)) << 4)) = o;
+        hook(k);
+      }
+    } else {
+      if (h == 0 && tid < kRows) sm.row_valid[tid] = tid < swa_count;
+      const bool live = g_e < swa_count;
+      const int64_t row = (int64_t)swa_row0 + g_e;
+      if (c < 7) {
+        const float sc = live ? ue8m0_value(__ldg(p.swa_scales + row * 8 + c)) : 0.0f;
+        const uint4* src = reinterpret_cast<const uint4*>(p.swa_codes + row * 448 + 64 * c);
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-          const uint4 c = live ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
-          const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+          const uint4 cc = live ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t w[4] = {cc.x, cc.y, cc.z, cc.w};
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             uint32_t o[4];
@@ -270,187 +329,207 @@ __global__ void __launch_bounds__(kThreads, 1)
                 o[2 * i + k] = *reinterpret_cast<const uint32_t*>(&bb);
               }
             }
-            const int chunk = 2 * v + half;
-            *reinterpret_cast<uint4*>(rowp + ((chunk ^ (e & 7)) << 4)) =
+            const int piece = 2 * v + half;
+            *reinterpret_cast<uint4*>(rowp + ((piece ^ (g_e & 7)) << 4)) =
                 make_uint4(o[0], o[1], o[2], o[3]);
+            hook(piece);
           }
         }
-      }
-      if (qq == 3) {
+      } else {
         const uint4* src = reinterpret_cast<const uint4*>(p.swa_rope + row * 64);
-        uint8_t* rowp = kv + 7 * (kRows * 128) + e * 128;
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-          const uint4 c = live ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(rowp + ((v ^ (e & 7)) << 4)) = c;
-        }
-      }
-    } else if (tile < 0) {
-      // issued at kernel entry
-      if (tid < kRows) sm.row_valid[tid] = tid < swa_count;
-      ok = mbar_wait(&sm.bar_kv, 0, p.err);
-      ok = __syncthreads_and(ok);
-      if (!ok) break;
-    } else {
-      if (tid < kRows) sm.row_valid[tid] = idx_s[tile * kRows + tid] >= 0;
-      // dequantise the registers of this thread: channels [128 q, 128 q + 128)
-      // of entry e, 32 channels (4 words of codes) per step
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t s2a, s2b;
-        if (p.layout == 0) {
-          const uint32_t b = (scw.x >> (8 * i)) & 0xFFu;          // one scale per 32
-          const uint32_t s16 = float_to_bf16_bits(ue8m0_value(b));
-          s2a = s2b = s16 | (s16 << 16);
-        } else {
-          const uint32_t w = i < 2 ? scw.x : scw.y;               // one scale per 16
-          const uint32_t ba = (w >> (16 * (i & 1))) & 0xFFu, bb = (w >> (16 * (i & 1) + 8)) & 0xFFu;
-          const uint32_t sa = float_to_bf16_bits(fabsf(e4m3_value(ba)));
-          const uint32_t sb = float_to_bf16_bits(fabsf(e4m3_value(bb)));
-          s2a = sa | (sa << 16);
-          s2b = sb | (sb << 16);
-        }
-        const uint32_t words[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
-        const int cb = 2 * g_q + (i >> 1);
-        uint8_t* rowp = kv + cb * (kRows * 128) + g_e * 128;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint32_t v[4];
-          e2m1x8_to_bf16x8(words[k], v);
-          const uint32_t s2 = k < 2 ? s2a : s2b;
-          uint4 o;
-          o.x = bf16x2_mul(v[0], s2); o.y = bf16x2_mul(v[1], s2);
-          o.z = bf16x2_mul(v[2], s2); o.w = bf16x2_mul(v[3], s2);
-          const int chunk = (i & 1) * 4 + k;
-          *reinterpret_cast<uint4*>(rowp + ((chunk ^ (g_e & 7)) << 4)) = o;
+          const uint4 cc = live ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(rowp + ((v ^ (g_e & 7)) << 4)) = cc;
+          hook(v);
         }
       }
     }
-    fence_proxy_async_smem();
-    __syncthreads();
+  };
 
-    // ------------------------------------------------ B: S^T = KV * Q^T
-    if (tid == 0) {
-      if (ti == 0) ok = mbar_wait(&sm.bar_q, 0, p.err);
-      tc_fence_after();
-      const uint32_t idesc = idesc_bf16_f32(128, kHG, false, false);
-      const uint32_t a0 = smem_u32(kv), b0 = smem_u32(qs);
-#pragma unroll 4
-      for (int ks = 0; ks < kHeadDim / 16; ++ks) {
-        const uint32_t ao = (uint32_t)((ks >> 2) * (kRows * 128) + (ks & 3) * 32);
-        const uint32_t bo = (uint32_t)((ks >> 2) * (kHG * 128) + (ks & 3) * 32);
-        umma_bf16(tmem + s_col, sdesc_sw128(a0 + ao, 16, 1024), sdesc_sw128(b0 + bo, 16, 1024),
-                  idesc, ks > 0 ? 1u : 0u);
+  uint32_t ph_s = 0;   // parity of bar_mma (S^T done), once per tile
+  bool ok = true;
+  float lsum[16];      // partial sums of l: this thread's rows, heads 16 hh .. 16 hh + 15
+#pragma unroll
+  for (int i = 0; i < 16; ++i) lsum[i] = 0.0f;
+  const int quad = warp & 3, hh = warp >> 2;   // TMEM lane quadrant, 16-head slice
+  const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+
+  auto no_hook = [](int) {};
+
+  // ---- first tile: rows -> KV buffer, then S^T
+  int next_topk = next_topk_after(-1);
+  if (n_tiles > 0) {
+    const int tile = sm.my_list[0];
+    if (next_topk < n_tiles) prefetch_tile(sm.my_list[next_topk]);
+    if (tile < 0 && !p.swa_codes) {
+      // bf16 window rows: loaded by TMA at kernel entry
+      if (tid < kRows) sm.row_valid[tid] = tid < swa_count;
+      if (tid == 0) {
+        ok = mbar_wait(&sm.bar_kv, 0, p.err);
+        ok = mbar_wait(&sm.bar_q, 0, p.err) && ok;
+        tc_fence_after();
+        for (int ks = 0; ks < 32; ++ks) mma_s(ks);
+        umma_commit(&sm.bar_mma);
       }
-      umma_commit(&sm.bar_mma);
+    } else {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        fill_half(tile, h, no_hook);
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+          if (h == 0) ok = mbar_wait(&sm.bar_q, 0, p.err);
+          tc_fence_after();
+          for (int k = 0; k < 16; ++k) mma_s(16 * h + k);
+          if (h == 1) umma_commit(&sm.bar_mma);
+        }
+      }
+      if (tile >= 0) {
+        next_topk = next_topk_after(next_topk);
+        if (next_topk < n_tiles) prefetch_tile(sm.my_list[next_topk]);
+      }
     }
-    if (tile >= 0) {
-      // the registers are free: fetch the next top-k tile behind this one,
-      // while the tensor core works (after the proxy fence, which would
-      // otherwise wait for these loads)
-      ++next_topk;
-      while (next_topk < n_tiles && sm.my_list[next_topk] < 0) ++next_topk;
-      if (next_topk < n_tiles) prefetch_tile(sm.my_list[next_topk]);
-    }
-    ok = mbar_wait(&sm.bar_mma, mma_phase, p.err) && ok;
-    mma_phase ^= 1;
+  }
+
+  for (int ti = 0; ti < n_tiles; ++ti) {
+    // one thread polls the mbarrier, the others wait at the CTA barrier
+    if (tid == 0) ok = mbar_wait(&sm.bar_mma, ph_s, p.err) && ok;
+    ph_s ^= 1;
     ok = __syncthreads_and(ok);
     if (!ok) break;
     tc_fence_after();
 
     // ------------------------------------------------ C: online softmax
+    // Each thread holds one candidate row of S^T for 16 heads.  The running
+    // maximum m of a head moves only when a tile holds a logit above it by
+    // more than 2^8 (log2 units): then the tile maxima are reduced, m is
+    // raised to them, and O^T and the partial sums are rescaled (exact: O,
+    // l and the probabilities all refer to the same m, and probabilities
+    // stay below 256).  Otherwise -- the common case after the first tile --
+    // no reduction is needed at all.  Each thread keeps partial sums of l for
+    // its 16 heads over the rows it has held; they are reduced once, after
+    // the last tile.
     const int row = quad * 32 + lane;
     const bool valid = sm.row_valid[row] != 0;
-    float x[16], v[16];
+    float x[16], mh[16];
+    bool need = false;
     {
       uint32_t r[16];
       tmem_ld16(tmem + lane_addr + s_col + 16 * hh, r);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         x[i] = valid ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
-        v[i] = x[i];
+        mh[i] = sm.m[16 * hh + i];
+        need = need || x[i] > mh[i] + kLazyRescale;
       }
-      const float mx = warp_reduce_scatter16<true>(v, lane);
-      if ((lane & 1) == 0) sm.red_max[quad][16 * hh + (lane >> 1)] = mx;
     }
-    __syncthreads();
-    if (tid < kHG) {
-      // The running maximum of a head moves only when a tile's maximum
-      // exceeds it by more than 2^8: O, l and the probabilities all refer to
-      // the same m (exact), probabilities stay below 256, and the O^T rescale
-      // in TMEM is skipped for most tiles.
-      const float tmax = fmaxf(fmaxf(sm.red_max[0][tid], sm.red_max[1][tid]),
-                               fmaxf(sm.red_max[2][tid], sm.red_max[3][tid]));
-      const float mo = sm.m[tid];
-      float a = 1.0f;
-      if (tmax > mo + kLazyRescale) {
-        a = (mo == -INFINITY) ? 0.0f : fast_exp2(mo - tmax);
-        sm.m[tid] = tmax;
-        if (ti > 0) sm.need_rescale = 1;
+    if (__syncthreads_or(need)) {
+      {
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = x[i];
+        const float mx = warp_reduce_scatter16<true>(v, lane);
+        if ((lane & 1) == 0) sm.red_max[quad][16 * hh + (lane >> 1)] = mx;
       }
-      sm.alpha[tid] = a;
-    }
-    __syncthreads();
-    {
+      __syncthreads();
+      if (tid < kHG) {
+        const float tmax = fmaxf(fmaxf(sm.red_max[0][tid], sm.red_max[1][tid]),
+                                 fmaxf(sm.red_max[2][tid], sm.red_max[3][tid]));
+        const float mo = sm.m[tid];
+        float a = 1.0f;
+        if (tmax > mo + kLazyRescale) {
+          a = (mo == -INFINITY) ? 0.0f : fast_exp2(mo - tmax);
+          sm.m[tid] = tmax;
+        }
+        sm.alpha[tid] = a;
+      }
+      __syncthreads();
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const int h = 16 * hh + i;
-        const float pr = (x[i] == -INFINITY) ? 0.0f : fast_exp2(x[i] - sm.m[h]);
-        const uint32_t pb = float_to_bf16_bits(pr);
-        v[i] = bf16_bits_to_float(pb);
-        // P^T is the K-major B operand: row h, column = candidate row
-        uint8_t* prow = ps + (row >> 6) * (kHG * 128) + h * 128;
-        const int chunk = (row & 63) >> 3;
-        *reinterpret_cast<uint16_t*>(prow + ((chunk ^ (h & 7)) << 4) + (row & 7) * 2) =
-            (uint16_t)pb;
+        lsum[i] *= sm.alpha[16 * hh + i];
+        mh[i] = sm.m[16 * hh + i];
       }
-      const float sum = warp_reduce_scatter16<false>(v, lane);
-      if ((lane & 1) == 0) sm.red_sum[quad][16 * hh + (lane >> 1)] = sum;
-    }
-    __syncthreads();
-    if (tid < kHG)
-      sm.l[tid] = sm.alpha[tid] * sm.l[tid] + ((sm.red_sum[0][tid] + sm.red_sum[1][tid]) +
-                                               (sm.red_sum[2][tid] + sm.red_sum[3][tid]));
-    if (sm.need_rescale) {
-      // O^T lanes are head-dim rows, columns are heads: scale column h by alpha[h]
+      if (ti > 0) {
+        // O^T lanes are head-dim rows, columns are heads: scale column h by alpha[h]
 #pragma unroll 1
-      for (int i = 0; i < 4; ++i) {
-        uint32_t r[16];
-        const uint32_t a = tmem + lane_addr + o_col + 64 * i + 16 * hh;
-        tmem_ld16(a, r);
+        for (int i = 0; i < 4; ++i) {
+          uint32_t r[16];
+          const uint32_t ta = tmem + lane_addr + o_col + 64 * i + 16 * hh;
+          tmem_ld16(ta, r);
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          r[c] = __float_as_uint(__uint_as_float(r[c]) * sm.alpha[16 * hh + c]);
-        tmem_st16(a, r);
+          for (int c = 0; c < 16; ++c)
+            r[c] = __float_as_uint(__uint_as_float(r[c]) * sm.alpha[16 * hh + c]);
+          tmem_st16(ta, r);
+        }
+        tmem_wait_st();
       }
-      tmem_wait_st();
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int h = 16 * hh + i;
+      const float pr = (x[i] == -INFINITY) ? 0.0f : fast_exp2(x[i] - mh[i]);
+      const uint32_t pb = float_to_bf16_bits(pr);
+      lsum[i] += bf16_bits_to_float(pb);
+      // P^T is the K-major B operand: row h, column = candidate row
+      uint8_t* prow = ps + (row >> 6) * (kHG * 128) + h * 128;
+      const int chunk = (row & 63) >> 3;
+      *reinterpret_cast<uint16_t*>(prow + ((chunk ^ (h & 7)) << 4) + (row & 7) * 2) =
+          (uint16_t)pb;
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
 
-    // ------------------------------------------------ D: O^T += KV^T * P^T
+    // ------------------------------------------------ O^T += KV^T * P^T, next tile
+    const bool first = ti == 0;
+    const uint32_t ph_o = (uint32_t)(ti & 1);
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t idesc = idesc_bf16_f32(128, kHG, true, false);
-      const uint32_t a0 = smem_u32(kv), b0 = smem_u32(ps);
-#pragma unroll 1
-      for (int i = 0; i < 4; ++i) {
+      for (int k = 0; k < 16; ++k) mma_o(k >> 3, k & 7, first);
+      umma_commit(&sm.bar_o[0]);
+      for (int k = 16; k < 32; ++k) mma_o(k >> 3, k & 7, first);
+      umma_commit(&sm.bar_o[1]);
+    }
+    if (ti + 1 < n_tiles) {
+      // The next tile (always a top-k tile: the window comes first) replaces
+      // the KV buffer half by half: half 0 once O^T d-blocks 0-1 are done
+      // (while blocks 2-3 run), half 1 once blocks 2-3 are done (while S^T of
+      // half 0 runs).  Suspend-hinted waits: 512 threads spinning on the
+      // barrier would take shared-memory bandwidth from the MMAs.
+      const int tile = sm.my_list[ti + 1];
 #pragma unroll
-        for (int ks = 0; ks < kRows / 16; ++ks) {
-          const uint32_t ao = (uint32_t)((2 * i) * (kRows * 128) + ks * 2048);
-          const uint32_t bo = (uint32_t)((ks >> 2) * (kHG * 128) + (ks & 3) * 32);
-          umma_bf16(tmem + o_col + 64 * i, sdesc_sw128(a0 + ao, kRows * 128, 1024),
-                    sdesc_sw128(b0 + bo, 16, 1024), idesc, (ti > 0 || ks > 0) ? 1u : 0u);
+      for (int h = 0; h < 2; ++h) {
+        ok = mbar_wait_sleep(&sm.bar_o[h], ph_o, p.err) && ok;
+        tc_fence_after();
+        fill_half(tile, h, no_hook);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+          tc_fence_after();
+          for (int k = 0; k < 16; ++k) mma_s(16 * h + k);
+          if (h == 1) umma_commit(&sm.bar_mma);
         }
       }
-      umma_commit(&sm.bar_mma);
+      next_topk = next_topk_after(next_topk);
+      if (next_topk < n_tiles) prefetch_tile(sm.my_list[next_topk]);
+    } else {
+      if (tid == 0) ok = mbar_wait(&sm.bar_o[1], ph_o, p.err) && ok;
+      ok = __syncthreads_and(ok);
+      tc_fence_after();
     }
-    ok = mbar_wait(&sm.bar_mma, mma_phase, p.err);
-    mma_phase ^= 1;
-    ok = __syncthreads_and(ok);
-    tc_fence_after();
   }
+
+  // l of each head: the partial sums reduced over all rows
+  {
+    const float sum = warp_reduce_scatter16<false>(lsum, lane);
+    if ((lane & 1) == 0) sm.red_sum[quad][16 * hh + (lane >> 1)] = sum;
+  }
+  __syncthreads();
+  if (tid < kHG)
+    sm.l[tid] = (sm.red_sum[0][tid] + sm.red_sum[1][tid]) + (sm.red_sum[2][tid] + sm.red_sum[3][tid]);
+  __syncthreads();
   // ------------------------------------------------ epilogue
   // Variants of the blog reading of the DeepSeek-V4 report, section 4.3: a
   // per-head sink logit z' whose exp joins the softmax denominator (the sink
