@@ -54,17 +54,16 @@ struct Small {
   float m[kHG];
   float l[kHG];
   float alpha[kHG];
-  int32_t tile_list[kMaxTiles];  // every tile of the query, window first
   int32_t my_list[kMaxTiles];    // this CTA's share
   int32_t tile_any[kMaxTiles];   // top-k tile holds a usable index
   uint8_t row_valid[kRows];
   int32_t n_tiles;
-  int32_t n_all;
   float rope_c[32], rope_s[32];  // output RoPE(-i): cos, sin of each channel pair
   uint32_t tmem;
-  uint64_t bar_q, bar_kv, bar_mma, bar_o[2];
+  uint64_t bar_q[2], bar_kv[2], bar_mma, bar_o[2];   // [h]: channel half h
 };
 constexpr int kSmemBytes = kSmallOff + (int)sizeof(Small) + 1024;
+
 
 // Reduce-scatter over the 32 lanes of a warp: v[0..15] (16 heads) in, lane L
 // ends with the reduction for head (L >> 1) in v[0].
@@ -144,15 +143,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     swa_count = c < 0 ? 0 : (c > p.swa ? p.swa : c);
   }
 
+  // The window tile is always first in the tile list: the CTA that owns it
+  // (split 0) loads it now, with the query rows, before anything else.  Both
+  // come in two channel halves so that S^T of half 0 can start before half 1
+  // has arrived.
+  const bool swa_first = swa_count > 0 && split == 0;
   if (tid == 0) {
-    mbar_init(&sm.bar_q, 1);
-    mbar_init(&sm.bar_kv, 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&sm.bar_q[h], 1);
+      mbar_init(&sm.bar_kv[h], 1);
+      mbar_init(&sm.bar_o[h], 1);
+    }
     mbar_init(&sm.bar_mma, 1);
-    mbar_init(&sm.bar_o[0], 1);
-    mbar_init(&sm.bar_o[1], 1);
     fence_barrier_init();
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_swa);
+    for (int h = 0; h < 2; ++h) {
+      mbar_arrive_expect_tx(&sm.bar_q[h], kHG * kHeadDim);
+      for (int c = 4 * h; c < 4 * h + 4; ++c)
+        tma_load_2d(qs + c * (kHG * 128), &tm_q, 64 * c, q * p.n_heads + hg * kHG, &sm.bar_q[h]);
+      if (swa_first && !p.swa_codes) {
+        mbar_arrive_expect_tx(&sm.bar_kv[h], kRows * kHeadDim);
+        for (int c = 4 * h; c < 4 * h + 4; ++c)
+          tma_load_2d(kv + c * (kRows * 128), &tm_swa, 64 * c, swa_row0, &sm.bar_kv[h]);
+      }
+    }
   }
   if (tid < kMaxTiles) sm.tile_any[tid] = 0;
   if (tid < kHG) { sm.m[tid] = -INFINITY; sm.l[tid] = 0.0f; }
@@ -163,19 +176,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm.tmem;
   const uint32_t s_col = 0, o_col = 64;   // S^T: 64 columns; O^T: 4 d-tiles x 64
 
-  // the window tile is always first in the tile list: the CTA that owns it
-  // (split 0) starts its load now, before scanning the top-k row
-  const bool swa_first = swa_count > 0 && split == 0;
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&sm.bar_q, kHG * kHeadDim * 2);
-    for (int c = 0; c < 8; ++c)
-      tma_load_2d(qs + c * (kHG * 128), &tm_q, 64 * c, q * p.n_heads + hg * kHG, &sm.bar_q);
-    if (swa_first && !p.swa_codes) {
-      mbar_arrive_expect_tx(&sm.bar_kv, kRows * kHeadDim * 2);
-      for (int c = 0; c < 8; ++c)
-        tma_load_2d(kv + c * (kRows * 128), &tm_swa, 64 * c, swa_row0, &sm.bar_kv);
-    }
-  }
   // the top-k row into shared memory (unusable slots become -1), and which
   // tiles hold at least one usable index
   bool bad = false;
@@ -190,15 +190,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (bad) set_error(p.err, kErrIndex);
   __syncthreads();
-  if (tid == 0) {
-    int n = 0;
-    if (swa_count > 0) sm.tile_list[n++] = -1;
-    for (int j = 0; j < n_topk_tiles; ++j)
-      if (sm.tile_any[j]) sm.tile_list[n++] = j;
-    sm.n_all = n;
-    int m = 0;
-    for (int i = split; i < n; i += p.splits) sm.my_list[m++] = sm.tile_list[i];
-    sm.n_tiles = m;
+  if (warp == 0) {
+    // position of each tile in the query's list (window first, then the
+    // top-k tiles holding a usable index); this CTA takes every splits-th
+    const uint32_t any = __ballot_sync(0xffffffffu, lane < n_topk_tiles && sm.tile_any[lane] != 0);
+    const int w = swa_count > 0 ? 1 : 0;
+    const int n = w + __popc(any);
+    if (lane == 0) {
+      sm.n_tiles = (n - split + p.splits - 1) / p.splits;
+      if (w && split == 0) sm.my_list[0] = -1;
+    }
+    if ((any >> lane) & 1u) {
+      const int pos = w + __popc(any & ((1u << lane) - 1u));
+      if (pos % p.splits == split) sm.my_list[pos / p.splits] = lane;
+    }
   }
   __syncthreads();
   const int n_tiles = sm.n_tiles;
@@ -366,10 +371,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // bf16 window rows: loaded by TMA at kernel entry
       if (tid < kRows) sm.row_valid[tid] = tid < swa_count;
       if (tid == 0) {
-        ok = mbar_wait(&sm.bar_kv, 0, p.err);
-        ok = mbar_wait(&sm.bar_q, 0, p.err) && ok;
-        tc_fence_after();
-        for (int ks = 0; ks < 32; ++ks) mma_s(ks);
+        for (int h = 0; h < 2; ++h) {
+          ok = mbar_wait(&sm.bar_kv[h], 0, p.err) && ok;
+          ok = mbar_wait(&sm.bar_q[h], 0, p.err) && ok;
+          tc_fence_after();
+          for (int k = 0; k < 16; ++k) mma_s(16 * h + k);
+        }
         umma_commit(&sm.bar_mma);
       }
     } else {
@@ -379,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
-          if (h == 0) ok = mbar_wait(&sm.bar_q, 0, p.err);
+          ok = mbar_wait(&sm.bar_q[h], 0, p.err) && ok;
           tc_fence_after();
           for (int k = 0; k < 16; ++k) mma_s(16 * h + k);
           if (h == 1) umma_commit(&sm.bar_mma);
@@ -568,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Output rows go through shared memory: bf16 [64 heads][dw] in the Q
   // buffer (free after the last S product), then 16-byte stores of each
   // head's d range [d0, d0 + dw).
-  uint16_t* out_s = reinterpret_cast<uint16_t*>(qs);
+  uint16_t* out_s = reinterpret_cast<uint16_t*>(qs);   // free after the last S^T
   auto store_rows = [&](int d0, int dw) {
     const int per_row = dw / 8;
     for (int k = tid; k < kHG * per_row; k += kThreads) {
@@ -590,6 +597,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.lse[out_row + tid] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
       }
       __syncthreads();
+      float w_me[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) w_me[c] = sm.alpha[16 * hh + c];
 #pragma unroll 1
       for (int i = 0; i < 4; ++i) {
         uint32_t r[16];
@@ -597,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int d = 128 * i + quad * 32 + lane;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float o = finish(i, __uint_as_float(r[c]) * sm.alpha[16 * hh + c]);
+          const float o = finish(i, __uint_as_float(r[c]) * w_me[c]);
           out_s[(16 * hh + c) * kHeadDim + d] = (uint16_t)float_to_bf16_bits(o);
         }
       }
@@ -664,6 +674,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld16(tmem + lane_addr + o_col + 64 * (2 * split) + 16 * hh, ro[0]);
       tmem_ld16(tmem + lane_addr + o_col + 64 * (2 * split + 1) + 16 * hh, ro[1]);
     }
+    float w_me[16], w_pt[16];   // the weights of this thread's 16 heads, read once
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      w_me[c] = sm.alpha[16 * hh + c];
+      w_pt[c] = sm.red_max[0][16 * hh + c];
+    }
     const uint32_t peer_stage = dsmem_addr(smem_u32(stage), peer);
     float4 pv[8];
 #pragma unroll
@@ -681,9 +697,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         const int h = 16 * hh + c;
-        const float w_ot = sm.red_max[0][h];
-        const float o_me = have ? sm.alpha[h] * __uint_as_float(ro[ii][c]) : 0.0f;
-        const float o_ot = w_ot != 0.0f ? w_ot * po[c] : 0.0f;
+        const float o_me = have ? w_me[c] * __uint_as_float(ro[ii][c]) : 0.0f;
+        const float o_ot = w_pt[c] != 0.0f ? w_pt[c] * po[c] : 0.0f;
         // fixed order: split 0's term first
         const float o = finish(i, split == 0 ? o_me + o_ot : o_ot + o_me);
         out_s[h * 256 + (d - 256 * split)] = (uint16_t)float_to_bf16_bits(o);
