@@ -213,15 +213,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the tensor core still reads the second half for O^T, and the first half
   // of S^T is computed while the second half is written.
   //
-  // Gather of one top-k tile into registers: thread (entry e = 8 warp +
-  // lane % 8, quarter q = lane / 8) loads, for each half h, the 32 code bytes
-  // of channel chunk 4 h + q of entry e and that chunk's scale bytes (two
-  // UE8M0 or four E4M3).  Issued one tile ahead, so the loads are in flight
-  // while the tensor core and the softmax work on the current tile.
-  const int g_e = warp * 8 + (lane & 7), g_q = lane >> 3;
+  // Fill mapping.  Warp 0 issues the MMAs (an issuing thread waits in the
+  // issue for about one MMA time) and writes no rows, so its issues never
+  // hold back the fill.  The other 15 warps (worker w = tid - 32) fill each
+  // half: worker w owns entry 8 (w / 32) + w % 8 (entries 0..119) at chunk
+  // quarter (w % 32) / 8, eight pieces of 8 channels; the 32 (entry,
+  // quarter) pairs of entries 120..127 are spread as one extra piece over
+  // the workers w < 256 (entry 120 + w / 32, quarter (w / 8) % 4, piece
+  // w % 8).
+  //
+  // Gather of one top-k tile into registers: for each half h a worker loads
+  // the 32 code bytes of its chunk 4 h + quarter and that chunk's scale bytes
+  // (two UE8M0 or four E4M3), plus the code word and scale byte of its extra
+  // piece.  Issued one tile ahead, so the loads are in flight while the
+  // tensor core and the softmax work on the current tile.
+  const bool filler = warp > 0;
+  const int wkr = tid - 32;
+  const int g_e = filler ? (wkr >> 5) * 8 + (lane & 7) : 0, g_q = lane >> 3;
+  const bool has_x = filler && wkr < 256;
+  const int x_e = 120 + (wkr >> 5), x_q = (wkr >> 3) & 3, x_k = wkr & 7;   // when has_x
   uint4 cw[4];
-  uint32_t scw[2];
+  uint32_t scw[2], xw[2], xsc[2];
   auto prefetch_tile = [&](int j) {
+    if (!filler) return;
     const int32_t s = idx_s[j * kRows + g_e];
     if (s >= 0) {
       const int64_t row = base + s;
@@ -239,6 +253,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 4; ++i) cw[i] = make_uint4(0u, 0u, 0u, 0u);
       scw[0] = scw[1] = 0u;
+    }
+    if (has_x) {
+      const int32_t sx = idx_s[j * kRows + x_e];
+      if (sx >= 0) {
+        const int64_t row = base + sx;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          xw[h] = __ldg(reinterpret_cast<const uint32_t*>(p.codes + row * kCodeBytes + 128 * h +
+                                                          32 * x_q + 4 * x_k));
+          xsc[h] = (p.layout == 0) ? __ldg(p.scales + row * 16 + 8 * h + 2 * x_q + (x_k >> 2))
+                                   : __ldg(p.scales + row * 32 + 16 * h + 4 * x_q + (x_k >> 1));
+        }
+      } else {
+        xw[0] = xw[1] = xsc[0] = xsc[1] = 0u;
+      }
     }
   };
   // the next top-k tile of this CTA's list after position `from`
@@ -271,84 +300,78 @@ __global__ void __launch_bounds__(kThreads, 1)
               (!first || ks > 0) ? 1u : 0u);
   };
 
-  // Half h of a tile's rows into the KV buffer (all threads).  Top-k tiles
-  // come from the registers: E2M1 -> bf16 via byte permutes and a bf16 scale
-  // multiply.  FP8 window rows come from global memory: E4M3 x 2^scale is a
-  // bf16 value; the RoPE channels 448-511 are bf16 already.  Written in the
-  // MMA layout (128-byte rows, 16-byte pieces swizzled by row).
-  auto fill_half = [&](int tile, int h, auto&& hook) {
-    const int c = 4 * h + g_q;                       // channel chunk of this thread
-    uint8_t* rowp = kv + c * (kRows * 128) + g_e * 128;
+  // Half h of a tile's rows into the KV buffer (the workers; see the fill
+  // mapping).  Top-k tiles come from the registers: E2M1 -> bf16 via byte
+  // permutes and a bf16 scale multiply.  FP8 window rows come from global
+  // memory: E4M3 x 2^scale is a bf16 value; the RoPE channels 448-511 are
+  // bf16 already.  Written in the MMA layout (128-byte rows, 16-byte pieces
+  // swizzled by row).
+  auto piece_at = [&](int e, int c, int k) -> uint4* {
+    return reinterpret_cast<uint4*>(kv + c * (kRows * 128) + e * 128 + ((k ^ (e & 7)) << 4));
+  };
+  auto scale_bf16x2 = [&](uint32_t byte) -> uint32_t {
+    const float sc = (p.layout == 0) ? ue8m0_value(byte) : fabsf(e4m3_value(byte));
+    const uint32_t s16 = float_to_bf16_bits(sc);
+    return s16 | (s16 << 16);
+  };
+  auto e2m1_piece = [&](uint32_t word, uint32_t s2) -> uint4 {
+    uint32_t v[4];
+    e2m1x8_to_bf16x8(word, v);
+    return make_uint4(bf16x2_mul(v[0], s2), bf16x2_mul(v[1], s2), bf16x2_mul(v[2], s2),
+                      bf16x2_mul(v[3], s2));
+  };
+  // eight E4M3 codes (two words) x sc -> eight bf16
+  auto e4m3_piece = [&](uint32_t w0, uint32_t w1, float sc) -> uint4 {
+    const uint32_t w[2] = {w0, w1};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+            (__nv_fp8x2_storage_t)((w[i] >> (16 * k)) & 0xFFFFu), __NV_E4M3);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+        const __nv_bfloat162 bb = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+        o[2 * i + k] = *reinterpret_cast<const uint32_t*>(&bb);
+      }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  };
+  // window piece k of row e, chunk c (FP8 codes + scale, or RoPE bf16)
+  auto window_piece = [&](int e, int c, int k) -> uint4 {
+    const bool live = e < swa_count;
+    if (!live) return make_uint4(0u, 0u, 0u, 0u);
+    const int64_t row = (int64_t)swa_row0 + e;
+    if (c == 7) return __ldg(reinterpret_cast<const uint4*>(p.swa_rope + row * 64) + k);
+    const float sc = ue8m0_value(__ldg(p.swa_scales + row * 8 + c));
+    const uint2 cc = __ldg(reinterpret_cast<const uint2*>(p.swa_codes + row * 448 + 64 * c + 8 * k));
+    return e4m3_piece(cc.x, cc.y, sc);
+  };
+  auto fill_half = [&](int tile, int h) {
+    if (h == 0 && tid < kRows)
+      sm.row_valid[tid] = tile >= 0 ? idx_s[tile * kRows + tid] >= 0 : tid < swa_count;
+    const int c = 4 * h + g_q;                       // channel chunk of this worker
     if (tile >= 0) {
-      if (h == 0 && tid < kRows) sm.row_valid[tid] = idx_s[tile * kRows + tid] >= 0;
-      const uint32_t words[8] = {cw[2 * h].x,     cw[2 * h].y,     cw[2 * h].z,     cw[2 * h].w,
-                                 cw[2 * h + 1].x, cw[2 * h + 1].y, cw[2 * h + 1].z, cw[2 * h + 1].w};
-      uint32_t s2[4];
-      if (p.layout == 0) {                           // one UE8M0 scale per 32 channels
+      if (filler) {
+        const uint32_t words[8] = {cw[2 * h].x,     cw[2 * h].y,     cw[2 * h].z,     cw[2 * h].w,
+                                   cw[2 * h + 1].x, cw[2 * h + 1].y, cw[2 * h + 1].z, cw[2 * h + 1].w};
+        uint32_t s2[4];
+        if (p.layout == 0) {                         // one UE8M0 scale per 32 channels
+          s2[0] = s2[1] = scale_bf16x2(scw[h] & 0xFFu);
+          s2[2] = s2[3] = scale_bf16x2((scw[h] >> 8) & 0xFFu);
+        } else {                                     // one E4M3 scale per 16 channels
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          const uint32_t s16 = float_to_bf16_bits(ue8m0_value((scw[h] >> (8 * g)) & 0xFFu));
-          s2[2 * g] = s2[2 * g + 1] = s16 | (s16 << 16);
+          for (int g = 0; g < 4; ++g) s2[g] = scale_bf16x2((scw[h] >> (8 * g)) & 0xFFu);
         }
-      } else {                                       // one E4M3 scale per 16 channels
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const uint32_t s16 = float_to_bf16_bits(fabsf(e4m3_value((scw[h] >> (8 * g)) & 0xFFu)));
-          s2[g] = s16 | (s16 << 16);
-        }
+        for (int k = 0; k < 8; ++k) *piece_at(g_e, c, k) = e2m1_piece(words[k], s2[k >> 1]);
       }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {                  // 8 channels per piece
-        uint32_t v[4];
-        e2m1x8_to_bf16x8(words[k], v);
-        const uint32_t s = s2[k >> 1];
-        uint4 o;
-        o.x = bf16x2_mul(v[0], s); o.y = bf16x2_mul(v[1], s);
-        o.z = bf16x2_mul(v[2], s); o.w = bf16x2_mul(v[3], s);
-        *reinterpret_cast<uint4*>(rowp + ((k ^ (g_e & 7)) << 4)) = o;
-        hook(k);
-      }
+      if (has_x) *piece_at(x_e, 4 * h + x_q, x_k) = e2m1_piece(xw[h], scale_bf16x2(xsc[h]));
     } else {
-      if (h == 0 && tid < kRows) sm.row_valid[tid] = tid < swa_count;
-      const bool live = g_e < swa_count;
-      const int64_t row = (int64_t)swa_row0 + g_e;
-      if (c < 7) {
-        const float sc = live ? ue8m0_value(__ldg(p.swa_scales + row * 8 + c)) : 0.0f;
-        const uint4* src = reinterpret_cast<const uint4*>(p.swa_codes + row * 448 + 64 * c);
+      if (filler) {
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const uint4 cc = live ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
-          const uint32_t w[4] = {cc.x, cc.y, cc.z, cc.w};
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t o[4];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              const uint32_t word = w[2 * half + i];
-#pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
-                    (__nv_fp8x2_storage_t)((word >> (16 * k)) & 0xFFFFu), __NV_E4M3);
-                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-                const __nv_bfloat162 bb = __floats2bfloat162_rn(f.x * sc, f.y * sc);
-                o[2 * i + k] = *reinterpret_cast<const uint32_t*>(&bb);
-              }
-            }
-            const int piece = 2 * v + half;
-            *reinterpret_cast<uint4*>(rowp + ((piece ^ (g_e & 7)) << 4)) =
-                make_uint4(o[0], o[1], o[2], o[3]);
-            hook(piece);
-          }
-        }
-      } else {
-        const uint4* src = reinterpret_cast<const uint4*>(p.swa_rope + row * 64);
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint4 cc = live ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(rowp + ((v ^ (g_e & 7)) << 4)) = cc;
-          hook(v);
-        }
+        for (int k = 0; k < 8; ++k) *piece_at(g_e, c, k) = window_piece(g_e, c, k);
       }
+      if (has_x) *piece_at(x_e, 4 * h + x_q, x_k) = window_piece(x_e, 4 * h + x_q, x_k);
     }
   };
 
@@ -360,7 +383,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int quad = warp & 3, hh = warp >> 2;   // TMEM lane quadrant, 16-head slice
   const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
 
-  auto no_hook = [](int) {};
 
   // ---- first tile: rows -> KV buffer, then S^T
   int next_topk = next_topk_after(-1);
@@ -382,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        fill_half(tile, h, no_hook);
+        fill_half(tile, h);
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
@@ -502,14 +524,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The next tile (always a top-k tile: the window comes first) replaces
       // the KV buffer half by half: half 0 once O^T d-blocks 0-1 are done
       // (while blocks 2-3 run), half 1 once blocks 2-3 are done (while S^T of
-      // half 0 runs).  Suspend-hinted waits: 512 threads spinning on the
-      // barrier would take shared-memory bandwidth from the MMAs.
+      // half 0 runs).
       const int tile = sm.my_list[ti + 1];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        ok = mbar_wait_sleep(&sm.bar_o[h], ph_o, p.err) && ok;
+        ok = mbar_wait(&sm.bar_o[h], ph_o, p.err) && ok;
         tc_fence_after();
-        fill_half(tile, h, no_hook);
+        fill_half(tile, h);
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
