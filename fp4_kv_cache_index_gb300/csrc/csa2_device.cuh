@@ -272,6 +272,33 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- pinned loads
+// Read-only global loads issued exactly where they are written (volatile
+// asm: the compiler neither sinks them towards their use nor merges them),
+// for prefetches whose results are consumed much later.
+__device__ __forceinline__ uint4 ldg_now_v4(const void* a) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg_now_u32(const void* a) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg_now_u16(const void* a) {
+  unsigned short v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg_now_u8(const void* a) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(a));
+  return v;
+}
+
 // ---------------------------------------------------------------- clusters
 // Rank of this CTA in its cluster (0 outside a cluster launch).
 __device__ __forceinline__ uint32_t cluster_ctarank() {

@@ -242,12 +242,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t* src = p.codes + row * kCodeBytes + g_q * 32;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        cw[2 * h] = __ldg(reinterpret_cast<const uint4*>(src + 128 * h));
-        cw[2 * h + 1] = __ldg(reinterpret_cast<const uint4*>(src + 128 * h + 16));
+        cw[2 * h] = ldg_now_v4(src + 128 * h);
+        cw[2 * h + 1] = ldg_now_v4(src + 128 * h + 16);
         if (p.layout == 0)
-          scw[h] = __ldg(reinterpret_cast<const uint16_t*>(p.scales + row * 16 + 8 * h + 2 * g_q));
+          scw[h] = ldg_now_u16(p.scales + row * 16 + 8 * h + 2 * g_q);
         else
-          scw[h] = __ldg(reinterpret_cast<const uint32_t*>(p.scales + row * 32 + 16 * h + 4 * g_q));
+          scw[h] = ldg_now_u32(p.scales + row * 32 + 16 * h + 4 * g_q);
       }
     } else {
 #pragma unroll
@@ -260,10 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t row = base + sx;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          xw[h] = __ldg(reinterpret_cast<const uint32_t*>(p.codes + row * kCodeBytes + 128 * h +
-                                                          32 * x_q + 4 * x_k));
-          xsc[h] = (p.layout == 0) ? __ldg(p.scales + row * 16 + 8 * h + 2 * x_q + (x_k >> 2))
-                                   : __ldg(p.scales + row * 32 + 16 * h + 4 * x_q + (x_k >> 1));
+          xw[h] = ldg_now_u32(p.codes + row * kCodeBytes + 128 * h + 32 * x_q + 4 * x_k);
+          xsc[h] = (p.layout == 0) ? ldg_now_u8(p.scales + row * 16 + 8 * h + 2 * x_q + (x_k >> 2))
+                                   : ldg_now_u8(p.scales + row * 32 + 16 * h + 4 * x_q + (x_k >> 1));
         }
       } else {
         xw[0] = xw[1] = xsc[0] = xsc[1] = 0u;
