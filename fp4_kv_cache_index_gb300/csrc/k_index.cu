@@ -37,6 +37,7 @@ constexpr int kStages = 4;
 constexpr int kKStageBytes = kTileE * kIdxDim * 2;  // 32 KB
 constexpr int kThreads = 320;
 constexpr int kEpiThreads = 256;   // warps 2-9
+constexpr int kBars = 2 * kStages + 8;   // k full / empty, acc full / empty, q full / empty, drain
 
 struct SmemLayout {
   int q_off, w_off, hist_off, bar_off, total;
@@ -46,9 +47,9 @@ __host__ __device__ inline SmemLayout smem_layout(int qpg) {
   SmemLayout L;
   L.q_off = kStages * kKStageBytes;
   L.w_off = L.q_off + qpg * 32 * kIdxDim * 2;
-  L.hist_off = L.w_off + qpg * 32 * 4;
-  L.bar_off = L.hist_off + kKeyHistBins * 4;
-  L.total = L.bar_off + 16 * 8 + 16 + 1024;  // barriers, tmem slot, alignment slack
+  L.hist_off = L.w_off + (qpg > 2 ? qpg : 2) * 32 * 4;
+  L.bar_off = L.hist_off + (qpg == 1 ? 2 : 1) * kKeyHistBins * 4;   // decode: one per tile group
+  L.total = L.bar_off + kBars * 8 + 16 + 1024;  // barriers, tmem slot, alignment slack
   return L;
 }
 
@@ -63,6 +64,30 @@ __device__ __forceinline__ int64_t group_base(const IndexParams& p, int g) {
   return p.prefill ? p.pre_base : p.entry_base[g];
 }
 
+// Position in the tile list: group g holds tiles [lo, hi).  The parameter
+// tables are read only when the group changes: a dynamic index into the
+// kernel parameters goes through the constant cache, and reading a large
+// table there on every tile kept missing it (several hundred cycles a tile).
+struct GroupCursor {
+  int g, lo, hi;
+  __device__ __forceinline__ void init(const IndexParams& p, int g0) {
+    g = g0;
+    lo = p.tile_prefix[g0];
+    hi = p.tile_prefix[g0 + 1];
+  }
+  // moves to the group of tile `it` (at or after the current one); true if
+  // the group changed
+  __device__ __forceinline__ bool advance(const IndexParams& p, int it) {
+    if (it < hi) return false;
+    do {
+      ++g;
+      lo = hi;
+      hi = p.tile_prefix[g + 1];
+    } while (hi <= it);
+    return true;
+  }
+};
+
 __global__ void __launch_bounds__(kThreads, 1)
     k_index(const __grid_constant__ IndexParams p, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_q) {
@@ -75,14 +100,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* wbuf = reinterpret_cast<float*>(smem + L.w_off);
   uint32_t* hs = reinterpret_cast<uint32_t*>(smem + L.hist_off);  // score-key histogram
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
-  uint64_t* k_full = bars;              // [kStages]
-  uint64_t* k_empty = bars + 4;         // [kStages]
-  uint64_t* acc_full = bars + 8;        // [2]
-  uint64_t* acc_empty = bars + 10;      // [2]
-  uint64_t* q_full = bars + 12;
-  uint64_t* q_empty = bars + 13;
-  uint64_t* drain = bars + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* k_full = bars;                    // [kStages]
+  uint64_t* k_empty = bars + kStages;         // [kStages]
+  uint64_t* acc_full = bars + 2 * kStages;    // [2]
+  uint64_t* acc_empty = acc_full + 2;         // [2]
+  uint64_t* q_full = acc_full + 4;
+  uint64_t* q_empty = acc_full + 5;
+  uint64_t* drain = acc_full + 6;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBars);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = 32 * p.qpg;               // MMA N (columns per accumulator)
@@ -91,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) { mbar_init(k_full + i, 1); mbar_init(k_empty + i, 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, kEpiThreads); }
+    for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, p.qpg == 1 ? kEpiThreads / 2 : kEpiThreads); }
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     mbar_init(drain, 1);
@@ -110,24 +135,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int end = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
   int g0 = 0;
   while (g0 < p.n_groups && p.tile_prefix[g0 + 1] <= begin) ++g0;
-  // pool row of item `it` (whose group is at or after `g`)
-  auto pool_row = [&](int it, int g) -> const int32_t* {
-    while (p.tile_prefix[g + 1] <= it) ++g;
-    return p.pool + (int64_t)g * p.pool_blocks + (it - p.tile_prefix[g]) * (kTileE / 8);
+  // pool row of item `it` (whose group is at or after the cursor's)
+  auto pool_row = [&](int it, GroupCursor c) -> const int32_t* {
+    c.advance(p, it);
+    return p.pool + (int64_t)c.g * p.pool_blocks + (it - c.lo) * (kTileE / 8);
   };
+  GroupCursor c0;
+  c0.init(p, g0);
 
   if (warp == 0 && begin < end) {
     // ------------------------------------------------ TMA producer (warp 0)
     // Lane 0 owns the barriers; in pool mode lanes 0-15 each copy one block.
-    int g = g0, cur = -1, stage = 0;
+    GroupCursor gc = c0;
+    int cur = -1, stage = 0;
+    int64_t gbase = 0;
     uint32_t ph = 0, qph = 0;
     uint32_t armed = 0, armed_ph = 0;   // stages filled at least once, parity of the last fill
     bool ok = true;
     const bool pool_lane = p.pool != nullptr && lane < kTileE / 8;
-    int32_t nxt = pool_lane ? __ldg(pool_row(begin, g0) + lane) : -1;
+    int32_t nxt = pool_lane ? __ldg(pool_row(begin, c0) + lane) : -1;
     for (int it = begin; it < end && ok; ++it) {
-      while (p.tile_prefix[g + 1] <= it) ++g;
+      gc.advance(p, it);
+      const int g = gc.g;
       if (g != cur) {
+        gbase = group_base(p, g);
         if (lane == 0) {
           ok = mbar_wait(q_empty, qph ^ 1, p.err);
           if (ok) {
@@ -147,16 +178,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* dst = kbuf + stage * kKStageBytes;
       if (p.pool) {
         const int32_t blk = nxt;
-        if (pool_lane && it + 1 < end) nxt = __ldg(pool_row(it + 1, g) + lane);
+        if (pool_lane && it + 1 < end) nxt = __ldg(pool_row(it + 1, gc) + lane);
         const uint32_t n_ok = (uint32_t)__popc(__ballot_sync(0xffffffffu, blk >= 0));
         if (lane == 0) mbar_arrive_expect_tx(k_full + stage, n_ok * 8 * kIdxDim * 2);
         __syncwarp();
         if (blk >= 0) {
-          const int32_t row = (int32_t)(group_base(p, g) + (int64_t)blk * 8);
+          const int32_t row = (int32_t)(gbase + (int64_t)blk * 8);
           tma_load_3d(dst + lane * 2048, &tm_k, 0, row, 0, k_full + stage);
         }
       } else if (lane == 0) {
-        const int64_t row = group_base(p, g) + (int64_t)(it - p.tile_prefix[g]) * kTileE;
+        const int64_t row = gbase + (int64_t)(it - gc.lo) * kTileE;
         mbar_arrive_expect_tx(k_full + stage, kKStageBytes);
         tma_load_2d(dst, &tm_k, 0, (int32_t)row, k_full + stage);
         tma_load_2d(dst + kKStageBytes / 2, &tm_k, 64, (int32_t)row, k_full + stage);
@@ -175,11 +206,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1 && lane == 0 && begin < end) {
     // ------------------------------------------------ MMA issuer
     const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)N, false, false);
-    int g = g0, cur = -1, stage = 0, acc = 0;
+    GroupCursor gc = c0;
+    int cur = -1, stage = 0, acc = 0;
     uint32_t ph = 0, qph = 0, aph = 0;
     bool ok = true;
     for (int it = begin; it < end && ok; ++it) {
-      while (p.tile_prefix[g + 1] <= it) ++g;
+      gc.advance(p, it);
+      const int g = gc.g;
       if (g != cur) {
         ok = mbar_wait(q_full, qph, p.err);
         qph ^= 1;
@@ -205,13 +238,86 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       umma_commit(k_empty + stage);
       umma_commit(acc_full + acc);
-      const bool last_of_group = (it + 1 == end) || (p.tile_prefix[g + 1] <= it + 1);
+      const bool last_of_group = (it + 1 == end) || (gc.hi <= it + 1);
       if (last_of_group) umma_commit(q_empty);
       if (++stage == kStages) { stage = 0; ph ^= 1; }
       if (++acc == 2) { acc = 0; aph ^= 1; }
     }
     umma_commit(drain);
     mbar_wait(drain, 0, p.err);
+  } else if (warp >= 2 && p.qpg == 1) {
+    // ------------------------------------------------ epilogue, one query per tile
+    // Two groups of four warps take alternate tiles (group gsel the tiles
+    // begin + gsel + 2k, whose accumulator is gsel), so two tiles' scores are
+    // formed at once; each group keeps its own weights, histogram and named
+    // barrier.  Thread: one entry of the tile (its TMEM lane), 32 heads.
+    const int gsel = (warp - 2) >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int et = (threadIdx.x - 64) & 127;
+    const uint32_t bar_id = 2u + (uint32_t)gsel;
+    uint32_t* hsg = hs + gsel * kKeyHistBins;
+    float* wg = wbuf + gsel * 32;
+    const bool use_hist = p.key_hist != nullptr;
+    auto gsync = [&]() { asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory"); };
+    auto flush = [&](int qq) {
+      gsync();
+      for (int i = et; i < kKeyHistBins; i += 128) {
+        const uint32_t v = hsg[i];
+        if (v) atomicAdd(p.key_hist + (int64_t)qq * kKeyHistBins + i, v);
+        hsg[i] = 0u;
+      }
+      gsync();
+    };
+    if (use_hist)
+      for (int i = et; i < kKeyHistBins; i += 128) hsg[i] = 0u;
+    GroupCursor gc = c0;
+    int cur = -1, nvis = 0;
+    uint32_t aph = 0;
+    int32_t blk_nxt = (p.pool && begin + gsel < end) ? __ldg(pool_row(begin + gsel, c0) + (row >> 3)) : -1;
+    for (int it = begin + gsel; it < end; it += 2) {
+      gc.advance(p, it);
+      const int g = gc.g;
+      const int32_t blk = blk_nxt;
+      if (p.pool && it + 2 < end) blk_nxt = __ldg(pool_row(it + 2, gc) + (row >> 3));
+      if (g != cur) {
+        if (use_hist && cur >= 0) flush(cur);
+        gsync();
+        if (et < 32) wg[et] = (g < p.nq) ? __ldg(p.w + (int64_t)g * kIdxHeads + et) : 0.0f;
+        gsync();
+        cur = g;
+        nvis = group_nvis_query(p, g, 0);
+      }
+      if (!mbar_wait(acc_full + gsel, aph, p.err)) break;
+      tc_fence_after();
+      const int t = it - gc.lo;
+      const int e = t * kTileE + row;
+      uint32_t r[32];
+      tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(gsel * N), r);
+      tc_fence_before();
+      mbar_arrive(acc_empty + gsel);   // the accumulator is free once read
+      aph ^= 1;
+      float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int h = 0; h < 32; ++h) s4[h & 3] = fmaf(wg[h], fmaxf(__uint_as_float(r[h]), 0.0f), s4[h & 3]);
+      const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+      if (p.pool) {
+        const int64_t ent = (int64_t)blk * 8 + (row & 7);
+        const float v = (blk >= 0 && ent < nvis) ? s : -INFINITY;
+        p.scores[(int64_t)g * p.ld + e] = v;
+        if (use_hist) atomicAdd(hsg + (score_key(v) >> 21), 1u);
+      } else if (g < p.nq && e < nvis) {
+        if (p.score_bf16) {
+          const uint32_t b = float_to_bf16_bits(s);
+          reinterpret_cast<uint16_t*>(p.scores)[(int64_t)g * p.ld + e] = (uint16_t)b;
+          if (use_hist) atomicAdd(hsg + (score_key(bf16_bits_to_float(b)) >> 21), 1u);
+        } else {
+          p.scores[(int64_t)g * p.ld + e] = s;
+          if (use_hist) atomicAdd(hsg + (score_key(s) >> 21), 1u);
+        }
+      }
+    }
+    if (use_hist && cur >= 0) flush(cur);
   } else if (warp >= 2) {
     // ------------------------------------------------ epilogue
     const int quad = warp & 3;                 // TMEM lane quadrant of this warp
@@ -234,13 +340,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (use_hist) {
       for (int i = et; i < kKeyHistBins; i += kEpiThreads) hs[i] = 0u;
     }
-    int g = g0, cur = -1, acc = 0;
+    GroupCursor gc = c0;
+    int cur = -1, acc = 0;
     uint32_t aph = 0;
-    int32_t blk_nxt = (p.pool && begin < end) ? __ldg(pool_row(begin, g0) + (row >> 3)) : -1;
+    int32_t blk_nxt = (p.pool && begin < end) ? __ldg(pool_row(begin, c0) + (row >> 3)) : -1;
     for (int it = begin; it < end; ++it) {
-      while (p.tile_prefix[g + 1] <= it) ++g;
+      gc.advance(p, it);
+      const int g = gc.g;
       const int32_t blk = blk_nxt;
-      if (p.pool && it + 1 < end) blk_nxt = __ldg(pool_row(it + 1, g) + (row >> 3));
+      if (p.pool && it + 1 < end) blk_nxt = __ldg(pool_row(it + 1, gc) + (row >> 3));
       if (g != cur) {
         if (use_hist && cur >= 0) flush(cur);
         asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -253,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!mbar_wait(acc_full + acc, aph, p.err)) break;
       tc_fence_after();
-      const int t = it - p.tile_prefix[g];
+      const int t = it - gc.lo;
       const int e = t * kTileE + row;
       for (int j = j0; j < j1; ++j) {
         uint32_t r[32];
