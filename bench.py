@@ -65,7 +65,54 @@ def parse_args(argv=None):
                    help="skip the Hierarchical Sparse Indexer / Reindex measurement")
     p.add_argument("--no-graph", action="store_true",
                    help="time eager API calls instead of the captured CUDA graph")
+    p.add_argument("--micro-batches", type=int, default=2,
+                   help="split the batch into this many micro-batches on their own streams "
+                        "(1: one stream, the whole batch per kernel)")
+    p.add_argument("--index-sms", type=int, default=120,
+                   help="SMs for the indexer's grid when micro-batches > 1 (the rest run "
+                        "the other micro-batch's top-k and readout concurrently)")
+    p.add_argument("--attn-split", action="store_true",
+                   help="with micro-batches, spread each query's readout over two CTAs")
     return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------- micro-batches
+def make_micro_batches(C, cache, wl, bufs0, ld, n_valid, M, split, dev):
+    """Per micro-batch device buffers: contiguous copies of its queries'
+    inputs, its own score / histogram / top-k scratch and its outputs."""
+    import torch
+    B, L = wl.batch, wl.layers
+    mbs = []
+    for m in range(M):
+        lo, hi = B * m // M, B * (m + 1) // M
+        n = hi - lo
+        mbs.append(dict(
+            seq=list(range(lo, hi)), nv=n_valid[lo:hi],
+            q_idx=bufs0["q_idx"][lo:hi].clone(), w=bufs0["w"][lo:hi].clone(),
+            qs=[x[lo:hi].clone() for x in bufs0["qs"]],
+            swas=[x[lo:hi].clone() for x in bufs0["swas"]],
+            scores=torch.empty(n, ld, dtype=torch.float32, device=dev),
+            hist=torch.empty(n, 2048, dtype=torch.int32, device=dev),
+            topk=torch.empty(n, 512, dtype=torch.int32, device=dev),
+            tws=torch.empty(max(16, C.csa2_topk_workspace_bytes(n, max(n_valid))),
+                            dtype=torch.uint8, device=dev),
+            aws=torch.empty(C.csa2_sparse_attn_workspace_bytes(cache, n) if split else 0,
+                            dtype=torch.uint8, device=dev),
+            outs=[torch.empty(n, 64, 512, dtype=torch.bfloat16, device=dev) for _ in range(L)],
+            lses=[torch.empty(n, 64, dtype=torch.float32, device=dev) for _ in range(L)]))
+    return mbs
+
+
+def mb_run(C, cache, d, L, scale):
+    """One micro-batch through the whole path, on the current stream."""
+    C.csa2_index_scores_decode(cache, d["q_idx"], d["w"], d["scores"], seq_ids=d["seq"],
+                               key_hist=d["hist"])
+    C.csa2_topk(d["scores"], d["nv"], 512, idx_out=d["topk"], key_hist=d["hist"],
+                workspace=d["tws"])
+    for l in range(L):
+        C.csa2_sparse_attn_decode(cache, d["qs"][l], d["swas"][l], d["topk"], scale,
+                                  seq_ids=d["seq"], out=d["outs"][l], lse=d["lses"][l],
+                                  workspace=d["aws"])
 
 
 # ---------------------------------------------------------------- distributed helpers
@@ -377,6 +424,55 @@ def run_csa2(args):
     torch.cuda.synchronize()
     barrier(world)
     elapsed = t_start.elapsed_time(t_end) / 1000.0
+    elapsed_single = elapsed
+
+    # ---- the headline schedule: the batch split into micro-batches, each on
+    #      its own stream and in order there, step after step; the indexer's
+    #      grid is capped so that the other micro-batch's latency-bound top-k
+    #      and readout run on the remaining SMs while it streams the keys
+    M = args.micro_batches
+    mbs, mb_streams, graph_steps = None, None, 0
+    if M > 1:
+        mbs = make_micro_batches(C, cache, wl, bufs[0], ld, n_valid, M, args.attn_split, dev)
+        mb_streams = [torch.cuda.Stream() for _ in range(M)]
+
+        def mb_steps(n):
+            main = torch.cuda.current_stream()
+            for s_ in mb_streams:
+                s_.wait_stream(main)
+            for _ in range(n):
+                for s_, d in zip(mb_streams, mbs):
+                    with torch.cuda.stream(s_):
+                        mb_run(C, cache, d, L, scale)
+            for s_ in mb_streams:
+                main.wait_stream(s_)
+
+        cache.set_index_sms(args.index_sms)
+        for _ in range(max(3, args.warmup)):
+            mb_steps(1)
+        torch.cuda.synchronize()
+        graph_steps = max(1, min(args.steps, 20))
+        g_main = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_main):
+            mb_steps(graph_steps)
+        g_rest = None
+        if args.steps % graph_steps:
+            g_rest = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_rest):
+                mb_steps(args.steps % graph_steps)
+        cache.set_index_sms(0)
+        g_main.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        t_start.record(stream)
+        for _ in range(args.steps // graph_steps):
+            g_main.replay()
+        if g_rest is not None:
+            g_rest.replay()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        elapsed = t_start.elapsed_time(t_end) / 1000.0
     clocks = sampler.stop()
 
     # ---- per-kernel split: eager calls with CUDA events around each launch
@@ -397,6 +493,7 @@ def run_csa2(args):
     if cache.device_error() != 0:
         raise RuntimeError("device error word set during the benchmark")
     elapsed_max = max_over_ranks(elapsed, world, dev)
+    single_max = max_over_ranks(elapsed_single, world, dev)
 
     # ---- end to end: every step's inputs go host -> device and its outputs
     #      device -> host inside the timed region, double-buffered the way a
@@ -445,6 +542,71 @@ def run_csa2(args):
                 out_free[b].record(copy_stream)
         stream.wait_stream(copy_stream)
 
+    e2e_note = ("inputs of step i+1 and outputs of step i-1 copied on a second stream "
+                "while step i computes (pinned host buffers)")
+    if M > 1:
+        # the same double-buffered copy pipeline per micro-batch: each has a
+        # compute stream (its path as a CUDA graph per buffer set) and a copy
+        # stream; the micro-batches' pipelines overlap one another
+        sets = [mbs, make_micro_batches(C, cache, wl, bufs[0], ld, n_valid, M,
+                                        args.attn_split, dev)]
+        cache.set_index_sms(args.index_sms)
+        mb_graphs = []
+        for m in range(M):
+            row = []
+            for bset in sets:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    mb_run(C, cache, bset[m], L, scale)
+                row.append(g)
+            mb_graphs.append(row)
+        cache.set_index_sms(0)
+        copy_streams = [torch.cuda.Stream() for _ in range(M)]
+        h_in_mb = [[pin(t) for t in flat(mbs[m], names_in)] for m in range(M)]
+        h_out_mb = [[[torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                      for t in flat(mbs[m], names_out)] for _ in range(2)] for m in range(M)]
+        h2d = sum(t.numel() * t.element_size() for h in h_in_mb for t in h)
+        d2h = sum(t.numel() * t.element_size() for h in h_out_mb for t in h[0])
+
+        def run_e2e(n):
+            ev = lambda: [torch.cuda.Event(), torch.cuda.Event()]
+            in_ready = [ev() for _ in range(M)]
+            done = [ev() for _ in range(M)]
+            out_free = [ev() for _ in range(M)]
+            for s_ in mb_streams + copy_streams:
+                s_.wait_stream(stream)
+            for m in range(M):
+                with torch.cuda.stream(copy_streams[m]):
+                    for h, t in zip(h_in_mb[m], flat(sets[0][m], names_in)):
+                        t.copy_(h, non_blocking=True)
+                    in_ready[m][0].record(copy_streams[m])
+            for i in range(n):
+                b = i % 2
+                for m in range(M):
+                    cs, ps = mb_streams[m], copy_streams[m]
+                    cs.wait_event(in_ready[m][b])
+                    if i >= 2:
+                        cs.wait_event(out_free[m][b])
+                    with torch.cuda.stream(cs):
+                        mb_graphs[m][b].replay()
+                    done[m][b].record(cs)
+                    with torch.cuda.stream(ps):
+                        if i + 1 < n:
+                            if i >= 1:
+                                ps.wait_event(done[m][1 - b])
+                            for h, t in zip(h_in_mb[m], flat(sets[1 - b][m], names_in)):
+                                t.copy_(h, non_blocking=True)
+                            in_ready[m][1 - b].record(ps)
+                        ps.wait_event(done[m][b])
+                        for h, t in zip(h_out_mb[m][b], flat(sets[b][m], names_out)):
+                            h.copy_(t, non_blocking=True)
+                        out_free[m][b].record(ps)
+            for s_ in mb_streams + copy_streams:
+                stream.wait_stream(s_)
+
+        e2e_note = ("per micro-batch: inputs of step i+1 and outputs of step i-1 copied on "
+                    "its copy stream while step i computes on its compute stream (pinned "
+                    "host buffers); the micro-batches' pipelines overlap")
     run_e2e(3)
     torch.cuda.synchronize()
     barrier(world)
@@ -491,7 +653,7 @@ def run_csa2(args):
         traffic = float(rec["dram_bytes_per_launch"])
     # this library's kernels per step: indexer, top-k segments, top-k, one
     # attention launch per layer (workspace memsets are not counted)
-    launches_per_step = (3 + L) * ((B + 1023) // 1024)
+    launches_per_step = (3 + L) * ((B + 1023) // 1024) * max(1, M)
     line = {
         "metric": METRIC, "value": B * world * args.steps / elapsed_max, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -507,12 +669,19 @@ def run_csa2(args):
                      "algorithmic_bytes_per_step": step_bytes},
         "kernel_ms": {"index_scores": 1000 * t_idx, "topk": 1000 * t_topk,
                       "sparse_attn_all_layers": 1000 * t_attn,
-                      "eager_step": eager_ms, "timed_as": "cuda graph replay" if graph is not None
-                      else "eager calls"},
+                      "eager_step": eager_ms,
+                      "timed_as": "eager calls with CUDA events, the whole batch on one stream"},
+        "schedule": {"micro_batches": max(1, M), "streams": max(1, M),
+                     "index_sms": args.index_sms if M > 1 else None,
+                     "attention_split": bool(args.attn_split) if M > 1 else True,
+                     "steps_per_graph": graph_steps if M > 1 else 1},
+        "single_stream": {"value": B * world * args.steps / single_max,
+                          "ms_per_step": 1000 * single_max / args.steps,
+                          "schedule": "whole batch per kernel on one stream, two-CTA readout "
+                                      "split, every SM for the indexer; one CUDA graph per step"},
         "e2e": {"value": B * world * e2e_steps / e2e_elapsed, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "pipelining": "inputs of step i+1 and outputs of step i-1 copied on a "
-                              "second stream while step i computes (pinned host buffers)"},
+                "pipelining": e2e_note},
         "gpu_launches": launches_per_step * args.steps,
         "hsi_reindex": hsi,
         "bf16_scores": bf16,

@@ -79,6 +79,7 @@ def _load():
         "csa2_cache_bytes": ([pcfg, i32, P], sz),
         "csa2_cache_create": ([pcfg, i32, P, P, sz, P, ctypes.POINTER(P)], i32),
         "csa2_cache_destroy": ([P], i32),
+        "csa2_cache_set_index_sms": ([P, i32], i32),
         "csa2_cache_reset": ([P, P], i32),
         "csa2_cache_length": ([P, i32, ctypes.POINTER(i64)], i32),
         "csa2_cache_views": ([P, ctypes.POINTER(CacheViews)], i32),
@@ -181,6 +182,11 @@ class Cache:
 
     def reset(self, stream=None):
         _check(lib.csa2_cache_reset(self.handle, _stream(stream)), "csa2_cache_reset")
+
+    def set_index_sms(self, n_sms: int):
+        """At most n_sms SMs for the indexer's grid (0: all); see
+        csa2_cache_set_index_sms."""
+        _check(lib.csa2_cache_set_index_sms(self.handle, n_sms), "csa2_cache_set_index_sms")
 
     def views(self) -> dict:
         """codes [total, 256] u8, scales [total, 512/g] u8, idx_k [total, 128]

@@ -37,6 +37,7 @@ struct csa2_cache {
   CUtensorMap tm_k;    // indexer keys, 128-row boxes (contiguous tiles)
   CUtensorMap tm_k8;   // indexer keys, one 8-key block per box (pool mode)
   int num_sms;
+  int index_sms;       // SMs the indexer's persistent grid may occupy
 };
 
 namespace {
@@ -312,6 +313,7 @@ csa2_status_t csa2_cache_create(const csa2_config_t* cfg, int32_t batch, const i
     delete c;
     return CSA2_ERR_CUDA;
   }
+  c->index_sms = c->num_sms;
   if (!mx && (!make_map(&c->tm_k, c->idxk, (uint64_t)c->total, kIdxDim, 64, 128) ||
               !make_block_map(&c->tm_k8, c->idxk, (uint64_t)c->total))) {
     delete c;
@@ -328,6 +330,12 @@ csa2_status_t csa2_cache_create(const csa2_config_t* cfg, int32_t batch, const i
 csa2_status_t csa2_cache_destroy(csa2_cache_t* c) {
   if (!c) return CSA2_ERR_INVALID_ARG;
   delete c;
+  return CSA2_OK;
+}
+
+csa2_status_t csa2_cache_set_index_sms(csa2_cache_t* c, int32_t n_sms) {
+  if (!c || n_sms < 0) return CSA2_ERR_INVALID_ARG;
+  c->index_sms = (n_sms == 0 || n_sms > c->num_sms) ? c->num_sms : n_sms;
   return CSA2_OK;
 }
 
@@ -515,7 +523,7 @@ csa2_status_t run_index_decode(const csa2_cache_t* c, int32_t nq, const void* q_
       return CSA2_ERR_CUDA;
     const int tiles = ip->tile_prefix[n];
     if (tiles > 0) {
-      const int grid = std::min(c->num_sms, tiles);
+      const int grid = std::min(c->index_sms, tiles);
       if (launch_index_any(c, *ip, tm_q, grid, S(stream)) != cudaSuccess) return CSA2_ERR_CUDA;
     }
   }
@@ -690,7 +698,7 @@ csa2_status_t csa2_index_scores_prefill(const csa2_cache_t* c, int32_t seq, int3
     }
     const int tiles = ip->tile_prefix[groups];
     if (tiles > 0) {
-      const int grid = std::min(c->num_sms, tiles);
+      const int grid = std::min(c->index_sms, tiles);
       if (launch_index_any(c, *ip, tm_q, grid, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
     }
   }
@@ -1080,7 +1088,7 @@ csa2_status_t csa2_index_topk_reindex_decode(const csa2_cache_t* c, int32_t nq, 
       st = CSA2_ERR_CUDA;
       break;
     }
-    const int grid = std::min(c->num_sms, ip->tile_prefix[n]);
+    const int grid = std::min(c->index_sms, ip->tile_prefix[n]);
     if (launch_index(*ip, c->tm_k8, tm_q, grid, S(stream)) != cudaSuccess) {
       st = CSA2_ERR_CUDA;
       break;

@@ -135,6 +135,17 @@ csa2_status_t csa2_cache_create(const csa2_config_t* cfg, int32_t batch,
 /* Frees the host handle only; the device memory stays the caller's. */
 csa2_status_t csa2_cache_destroy(csa2_cache_t* cache);
 
+/* Upper bound on the SMs that the indexer's persistent grid occupies for
+ * this cache (n_sms = 0 or more than the GPU has: all of them, the default).
+ * A caller that splits a decode batch into micro-batches on separate streams
+ * leaves the other SMs to the latency-bound top-k and attention kernels of
+ * the other micro-batch, which then run concurrently with the bandwidth-
+ * bound indexer (the results do not depend on the setting).  Applies to
+ * indexer launches made after it returns.  CSA2_ERR_INVALID_ARG for a NULL
+ * cache or n_sms < 0.  The pages have no counterpart: this is a scheduling
+ * knob of this implementation, not part of the method.                    */
+csa2_status_t csa2_cache_set_index_sms(csa2_cache_t* cache, int32_t n_sms);
+
 /* Empties every sequence (host lengths and, on `stream`, device lengths). */
 csa2_status_t csa2_cache_reset(csa2_cache_t* cache, csa2_stream_t stream);
 
