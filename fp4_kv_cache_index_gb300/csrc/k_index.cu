@@ -37,7 +37,8 @@ constexpr int kStages = 4;
 constexpr int kKStageBytes = kTileE * kIdxDim * 2;  // 32 KB
 constexpr int kThreads = 320;
 constexpr int kEpiThreads = 256;   // warps 2-9
-constexpr int kBars = 2 * kStages + 8;   // k full / empty, acc full / empty, q full / empty, drain
+constexpr int kMaxAcc = 4;                 // accumulators in TMEM (decode 4, several queries 2)
+constexpr int kBars = 2 * kStages + 2 * kMaxAcc + 4;   // k full / empty, acc full / empty, q full / empty, drain
 
 struct SmemLayout {
   int q_off, w_off, hist_off, bar_off, total;
@@ -102,21 +103,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* k_full = bars;                    // [kStages]
   uint64_t* k_empty = bars + kStages;         // [kStages]
-  uint64_t* acc_full = bars + 2 * kStages;    // [2]
-  uint64_t* acc_empty = acc_full + 2;         // [2]
-  uint64_t* q_full = acc_full + 4;
-  uint64_t* q_empty = acc_full + 5;
-  uint64_t* drain = acc_full + 6;
+  uint64_t* acc_full = bars + 2 * kStages;    // [kMaxAcc]
+  uint64_t* acc_empty = acc_full + kMaxAcc;   // [kMaxAcc]
+  uint64_t* q_full = acc_full + 2 * kMaxAcc;
+  uint64_t* q_empty = q_full + 1;
+  uint64_t* drain = q_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBars);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = 32 * p.qpg;               // MMA N (columns per accumulator)
   const int qrows = 32 * p.qpg;
-  const uint32_t tmem_cols = (N * 2 <= 32) ? 32u : (uint32_t)(N * 2);
+  // decode (one query, N = 32) keeps four accumulators in flight, several
+  // queries per tile (N = 256) two
+  const int nacc = p.qpg == 1 ? 4 : 2;
+  const uint32_t tmem_cols = (N * nacc <= 32) ? 32u : (uint32_t)(N * nacc);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) { mbar_init(k_full + i, 1); mbar_init(k_empty + i, 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, p.qpg == 1 ? kEpiThreads / 2 : kEpiThreads); }
+    for (int i = 0; i < nacc; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, p.qpg == 1 ? kEpiThreads / 2 : kEpiThreads); }
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     mbar_init(drain, 1);
@@ -206,6 +210,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1 && lane == 0 && begin < end) {
     // ------------------------------------------------ MMA issuer
     const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)N, false, false);
+    // contiguous tiles: column halves 16 KB apart, 8-row atoms 1 KB apart;
+    // pool tiles: halves 1 KB apart inside each block's 2 KB.  Descriptor
+    // bases built once; the offsets go into the address field (shared
+    // memory is below 2^18 bytes, so it never carries).
+    const uint32_t a_half = p.pool ? 1024u : (uint32_t)(kKStageBytes / 2);
+    const uint64_t adesc0 = sdesc_sw128(smem_u32(kbuf), 16, p.pool ? 2048u : 1024u);
+    const uint64_t bdesc0 = sdesc_sw128(smem_u32(qbuf), 16, 1024);
     GroupCursor gc = c0;
     int cur = -1, stage = 0, acc = 0;
     uint32_t ph = 0, qph = 0, aph = 0;
@@ -222,26 +233,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait(k_full + stage, ph, p.err) && mbar_wait(acc_empty + acc, aph ^ 1, p.err);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t a0 = smem_u32(kbuf + stage * kKStageBytes);
-      const uint32_t b0 = smem_u32(qbuf);
       const uint32_t d = tmem_base + (uint32_t)(acc * N);
-      // contiguous tiles: column halves 16 KB apart, 8-row atoms 1 KB apart;
-      // pool tiles: halves 1 KB apart inside each block's 2 KB
-      const uint32_t a_half = p.pool ? 1024u : (uint32_t)(kKStageBytes / 2);
-      const uint32_t a_sbo = p.pool ? 2048u : 1024u;
+      const uint64_t adesc = adesc0 + (uint64_t)((stage * kKStageBytes) >> 4);
 #pragma unroll
       for (int ks = 0; ks < kIdxDim / 16; ++ks) {
         const uint32_t ao = (uint32_t)(ks >> 2) * a_half + (uint32_t)(ks & 3) * 32u;
         const uint32_t bo = (uint32_t)((ks >> 2) * (qrows * 128) + (ks & 3) * 32);
-        umma_bf16(d, sdesc_sw128(a0 + ao, 16, a_sbo), sdesc_sw128(b0 + bo, 16, 1024), idesc,
-                  ks > 0 ? 1u : 0u);
+        umma_bf16(d, adesc + (ao >> 4), bdesc0 + (bo >> 4), idesc, ks > 0 ? 1u : 0u);
       }
       umma_commit(k_empty + stage);
       umma_commit(acc_full + acc);
       const bool last_of_group = (it + 1 == end) || (gc.hi <= it + 1);
       if (last_of_group) umma_commit(q_empty);
       if (++stage == kStages) { stage = 0; ph ^= 1; }
-      if (++acc == 2) { acc = 0; aph ^= 1; }
+      if (++acc == nacc) { acc = 0; aph ^= 1; }
     }
     umma_commit(drain);
     mbar_wait(drain, 0, p.err);
@@ -273,7 +278,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = et; i < kKeyHistBins; i += 128) hsg[i] = 0u;
     GroupCursor gc = c0;
     int cur = -1, nvis = 0;
-    uint32_t aph = 0;
     int32_t blk_nxt = (p.pool && begin + gsel < end) ? __ldg(pool_row(begin + gsel, c0) + (row >> 3)) : -1;
     for (int it = begin + gsel; it < end; it += 2) {
       gc.advance(p, it);
@@ -288,15 +292,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         cur = g;
         nvis = group_nvis_query(p, g, 0);
       }
-      if (!mbar_wait(acc_full + gsel, aph, p.err)) break;
+      const int jt = it - begin;
+      const int a = jt & 3;
+      // suspend-hinted wait: a polling epilogue warp would take issue slots
+      // from the producer and MMA warps that share its scheduler
+      if (!mbar_wait_sleep(acc_full + a, (uint32_t)((jt >> 2) & 1), p.err)) break;
       tc_fence_after();
       const int t = it - gc.lo;
       const int e = t * kTileE + row;
       uint32_t r[32];
-      tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(gsel * N), r);
+      tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * N), r);
       tc_fence_before();
-      mbar_arrive(acc_empty + gsel);   // the accumulator is free once read
-      aph ^= 1;
+      mbar_arrive(acc_empty + a);   // the accumulator is free once read
       float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int h = 0; h < 32; ++h) s4[h & 3] = fmaf(wg[h], fmaxf(__uint_as_float(r[h]), 0.0f), s4[h & 3]);
@@ -367,9 +374,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t r[32];
         tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * N + j * 32), r);
         const float* wj = wbuf + j * 32;
-        float s = 0.0f;
+        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // four chains, not one of 32
 #pragma unroll
-        for (int h = 0; h < 32; ++h) s = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.0f), s);
+        for (int h = 0; h < 32; ++h)
+          s4[h & 3] = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.0f), s4[h & 3]);
+        const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         const int q = g * p.qpg + j;
         if (p.pool) {
           // slot t * 128 + row of the pool; its entry decides validity
