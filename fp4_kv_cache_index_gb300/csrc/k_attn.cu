@@ -275,6 +275,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (j < n_tiles && sm.my_list[j] < 0) ++j;
     return j;
   };
+  // L2 prefetch of top-k tile j (one thread per entry: its two 128-byte
+  // code lines and its scale line), a tile before the registers load it
+  auto prefetch_l2 = [&](int j) {
+    const int e = (filler && g_q == 0) ? g_e : (has_x && x_q == 0 && x_k == 0) ? x_e : -1;
+    if (e < 0) return;
+    const int32_t s = idx_s[j * kRows + e];
+    if (s < 0) return;
+    const int64_t row = base + s;
+    const uint8_t* c = p.codes + row * kCodeBytes;
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(c));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(c + 128));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.scales + row * (p.layout == 0 ? 16 : 32)));
+  };
 
   // MMA descriptors: bases built once, K steps added to the address field
   // (all of shared memory is below 2^18 bytes, so the 14-bit field never
@@ -387,7 +400,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   int next_topk = next_topk_after(-1);
   if (n_tiles > 0) {
     const int tile = sm.my_list[0];
-    if (next_topk < n_tiles) prefetch_tile(sm.my_list[next_topk]);
+    if (next_topk < n_tiles) {
+      prefetch_tile(sm.my_list[next_topk]);
+      const int after = next_topk_after(next_topk);
+      if (after < n_tiles) prefetch_l2(sm.my_list[after]);
+    }
     if (tile < 0 && !p.swa_codes) {
       // bf16 window rows: loaded by TMA at kernel entry
       if (tid < kRows) sm.row_valid[tid] = tid < swa_count;
@@ -415,7 +432,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (tile >= 0) {
         next_topk = next_topk_after(next_topk);
-        if (next_topk < n_tiles) prefetch_tile(sm.my_list[next_topk]);
+        if (next_topk < n_tiles) {
+          prefetch_tile(sm.my_list[next_topk]);
+          const int after = next_topk_after(next_topk);
+          if (after < n_tiles) prefetch_l2(sm.my_list[after]);
+        }
       }
     }
   }
@@ -540,7 +561,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       next_topk = next_topk_after(next_topk);
-      if (next_topk < n_tiles) prefetch_tile(sm.my_list[next_topk]);
+      if (next_topk < n_tiles) {
+        prefetch_tile(sm.my_list[next_topk]);
+        const int after = next_topk_after(next_topk);
+        if (after < n_tiles) prefetch_l2(sm.my_list[after]);
+      }
     } else {
       if (tid == 0) ok = mbar_wait(&sm.bar_o[1], ph_o, p.err) && ok;
       ok = __syncthreads_and(ok);
