@@ -37,6 +37,7 @@ constexpr int kStages = 4;
 constexpr int kKStageBytes = kTileE * kIdxDim * 2;  // 32 KB
 constexpr int kThreads = 320;
 constexpr int kEpiThreads = 256;   // warps 2-9
+constexpr int kMaxHalfQ = 4;              // queries per epilogue half (a tile holds <= 8)
 constexpr int kMaxAcc = 4;                 // accumulators in TMEM (decode 4, several queries 2)
 constexpr int kBars = 2 * kStages + 2 * kMaxAcc + 4;   // k full / empty, acc full / empty, q full / empty, drain
 
@@ -350,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     GroupCursor gc = c0;
     int cur = -1, acc = 0;
     uint32_t aph = 0;
+    int nvis[kMaxHalfQ];   // visible entries of this thread's queries in the current group
     int32_t blk_nxt = (p.pool && begin < end) ? __ldg(pool_row(begin, c0) + (row >> 3)) : -1;
     for (int it = begin; it < end; ++it) {
       gc.advance(p, it);
@@ -365,14 +367,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         asm volatile("bar.sync 1, 256;" ::: "memory");
         cur = g;
+#pragma unroll
+        for (int jj = 0; jj < kMaxHalfQ; ++jj)
+          nvis[jj] = (j0 + jj < j1) ? group_nvis_query(p, g, j0 + jj) : 0;
       }
       if (!mbar_wait(acc_full + acc, aph, p.err)) break;
       tc_fence_after();
       const int t = it - gc.lo;
       const int e = t * kTileE + row;
-      for (int j = j0; j < j1; ++j) {
-        uint32_t r[32];
-        tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * N + j * 32), r);
+      // score of query j of the group from its 32 head columns r
+      auto emit = [&](int j, int jj, const uint32_t (&r)[32]) {
         const float* wj = wbuf + j * 32;
         float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // four chains, not one of 32
 #pragma unroll
@@ -380,13 +384,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           s4[h & 3] = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.0f), s4[h & 3]);
         const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         const int q = g * p.qpg + j;
+        const int nv = nvis[jj];
         if (p.pool) {
           // slot t * 128 + row of the pool; its entry decides validity
           const int64_t ent = (int64_t)blk * 8 + (row & 7);
-          const float v = (blk >= 0 && ent < group_nvis_query(p, g, j)) ? s : -INFINITY;
+          const float v = (blk >= 0 && ent < nv) ? s : -INFINITY;
           p.scores[(int64_t)q * p.ld + e] = v;
           if (use_hist) atomicAdd(hs + (score_key(v) >> 21), 1u);
-        } else if (q < p.nq && e < group_nvis_query(p, g, j)) {
+        } else if (q < p.nq && e < nv) {
           if (p.score_bf16) {
             // the selector's precision: nearest bf16, its key histogrammed
             const uint32_t b = float_to_bf16_bits(s);
@@ -396,6 +401,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             p.scores[(int64_t)q * p.ld + e] = s;
             if (use_hist) atomicAdd(hs + (score_key(s) >> 21), 1u);
           }
+        }
+      };
+      const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * N);
+#pragma unroll
+      for (int jj = 0; jj < kMaxHalfQ; jj += 2) {   // two queries' columns under one TMEM wait
+        const int j = j0 + jj;
+        if (j + 1 < j1) {
+          uint32_t ra[32], rb[32];
+          tmem_ld32x2(lane_base + (uint32_t)(j * 32), lane_base + (uint32_t)((j + 1) * 32), ra, rb);
+          emit(j, jj, ra);
+          emit(j + 1, jj + 1, rb);
+        } else if (j < j1) {
+          uint32_t r[32];
+          tmem_ld32(lane_base + (uint32_t)(j * 32), r);
+          emit(j, jj, r);
         }
       }
       tc_fence_before();
@@ -419,6 +439,8 @@ int index_smem_bytes(int qpg) { return smem_layout(qpg).total; }
 
 cudaError_t launch_index(const IndexParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_q,
                          int grid, cudaStream_t s) {
+  // the epilogue covers at most 2 * kMaxHalfQ queries per tile (N <= 256)
+  if (p.qpg < 1 || p.qpg > 2 * kMaxHalfQ) return cudaErrorInvalidValue;
   const int smem = index_smem_bytes(p.qpg);
   cudaError_t e = cudaFuncSetAttribute(k_index, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
