@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t armed = 0, armed_ph = 0;   // stages filled at least once, parity of the last fill
     bool ok = true;
     const bool pool_lane = p.pool != nullptr && lane < kTileE / 8;
+    const uint64_t keys_pol = l2_policy_evict_first();
     int32_t nxt = pool_lane ? __ldg(pool_row(begin, c0) + lane) : -1;
     for (int it = begin; it < end && ok; ++it) {
       gc.advance(p, it);
@@ -189,13 +190,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (blk >= 0) {
           const int32_t row = (int32_t)(gbase + (int64_t)blk * 8);
-          tma_load_3d(dst + lane * 2048, &tm_k, 0, row, 0, k_full + stage);
+          tma_load_3d(dst + lane * 2048, &tm_k, 0, row, 0, k_full + stage, keys_pol);
         }
       } else if (lane == 0) {
         const int64_t row = gbase + (int64_t)(it - gc.lo) * kTileE;
         mbar_arrive_expect_tx(k_full + stage, kKStageBytes);
-        tma_load_2d(dst, &tm_k, 0, (int32_t)row, k_full + stage);
-        tma_load_2d(dst + kKStageBytes / 2, &tm_k, 64, (int32_t)row, k_full + stage);
+        tma_load_2d(dst, &tm_k, 0, (int32_t)row, k_full + stage, keys_pol);
+        tma_load_2d(dst + kKStageBytes / 2, &tm_k, 64, (int32_t)row, k_full + stage, keys_pol);
       }
       armed |= 1u << stage;
       armed_ph = (armed_ph & ~(1u << stage)) | (ph << stage);

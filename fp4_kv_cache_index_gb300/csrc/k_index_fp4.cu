@@ -227,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t rph = 0, qph = 0;
     uint32_t armed = 0, armed_ph = 0;   // raw stages filled at least once, parity of the last fill
     bool ok = true;
+    const uint64_t keys_pol = l2_policy_evict_first();
     for (int it = begin; it < end && ok; ++it) {
       while (p.tile_prefix[g + 1] <= it) ++g;
       if (g != cur) {
@@ -246,8 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t scale_bytes = (uint32_t)(s1 - tr.s0) * 4u;
       uint8_t* dst = raw + rs * kRawStageBytes;
       mbar_arrive_expect_tx(raw_full + rs, code_bytes + scale_bytes);
-      bulk_load(dst, p.idx_codes + tr.row0 * (kIdxDim / 2), code_bytes, raw_full + rs);
-      bulk_load(dst + kRawCodeBytes, p.idx_scales + tr.s0 * 4, scale_bytes, raw_full + rs);
+      bulk_load(dst, p.idx_codes + tr.row0 * (kIdxDim / 2), code_bytes, raw_full + rs, keys_pol);
+      bulk_load(dst + kRawCodeBytes, p.idx_scales + tr.s0 * 4, scale_bytes, raw_full + rs,
+                keys_pol);
       armed |= 1u << rs;
       armed_ph = (armed_ph & ~(1u << rs)) | (rph << rs);
       if (++rs == n_raw) { rs = 0; rph ^= 1; }
