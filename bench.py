@@ -73,6 +73,10 @@ def parse_args(argv=None):
                         "the other micro-batch's top-k and readout concurrently)")
     p.add_argument("--attn-split", action="store_true",
                    help="with micro-batches, spread each query's readout over two CTAs")
+    p.add_argument("--input-sets", type=int, default=4,
+                   help="step i reads input set i mod this (distinct seeded queries, weights "
+                        "and windows, hence distinct selections): no step finds the previous "
+                        "step's readout inputs still in L2")
     return p.parse_args(argv)
 
 
@@ -299,7 +303,10 @@ def workload_config(wl, layout):
             "swa": 128, "layout": "L32_UE8M0" if layout == 0 else "L16_E4M3",
             "outliers": "1% channels x8" if wl.outliers else "none",
             "l2": "inputs larger than L2: every step streams all indexer keys "
-                  f"({int(n.sum()) * 256 / 1e9:.2f} GB) through the 129 MB L2",
+                  f"({int(n.sum()) * 256 / 1e9:.2f} GB, L2 evict-first) through the 129 MB "
+                  "L2, and step i reads input set i mod input_sets (queries, weights, "
+                  "windows; hence selections), so no step finds its readout inputs left "
+                  "in L2 by the step before",
             "parallelism": "replica per GPU (sequences are independent)"}
 
 
@@ -344,29 +351,36 @@ def run_csa2(args):
     cfg = C.config(ratio=wl.ratio, layout=args.layout)
     cache = C.Cache(cfg, [int(x) for x in n_ent], device=dev)
     W.fill_cache(wl, cache)
-    q_idx = W.dev_q_idx(wl)
-    w = W.dev_w(wl)
-    qs = [W.dev_q(wl, l) for l in range(L)]
-    swas = [W.dev_swa(wl, l) for l in range(L)]
+    S = max(2, args.input_sets)
+
+    def make_inputs(s):
+        # set 0 is the workload's own stream; set s > 0 draws the same
+        # distributions from the streams of "layers" past the model's
+        return dict(q_idx=W.dev_q_idx(wl, layer=s), w=W.dev_w(wl, layer=s),
+                    qs=[W.dev_q(wl, L * s + l) for l in range(L)],
+                    swas=[W.dev_swa(wl, L * s + l) for l in range(L)])
+
+    def make_outputs():
+        return dict(topk=torch.empty(B, 512, dtype=torch.int32, device=dev),
+                    outs=[torch.empty(B, 64, 512, dtype=torch.bfloat16, device=dev)
+                          for _ in range(L)],
+                    lses=[torch.empty(B, 64, dtype=torch.float32, device=dev) for _ in range(L)])
+
     ld = max(4, (int(n_ent.max()) + 3) // 4 * 4)
     scores = torch.empty(B, ld, dtype=torch.float32, device=dev)
-    topk = torch.empty(B, 512, dtype=torch.int32, device=dev)
     key_hist = torch.empty(B, 2048, dtype=torch.int32, device=dev)
     topk_ws = torch.empty(max(16, C.csa2_topk_workspace_bytes(B, int(n_ent.max()))),
                           dtype=torch.uint8, device=dev)
-    outs = [torch.empty(B, 64, 512, dtype=torch.bfloat16, device=dev) for _ in range(L)]
-    lses = [torch.empty(B, 64, dtype=torch.float32, device=dev) for _ in range(L)]
     n_valid = [int(x) for x in n_ent]
     attn_ws = torch.empty(max(16, C.csa2_sparse_attn_workspace_bytes(cache, B)),
                           dtype=torch.uint8, device=dev)
     scale = 512 ** -0.5
     stream = torch.cuda.current_stream()
 
-    # two sets of per-step device buffers (inputs and outputs): set 0 for the
-    # device-resident timing, both for the double-buffered end-to-end leg
-    bufs = [dict(q_idx=q_idx, w=w, qs=qs, swas=swas, topk=topk, outs=outs, lses=lses)]
-    bufs.append({k: ([x.clone() for x in v] if isinstance(v, list) else v.clone())
-                 for k, v in bufs[0].items()})
+    # S input sets, step i on set i mod S; outputs double-buffered (set s
+    # writes output buffer s mod 2, the end-to-end leg's two buffer sets)
+    out_sets = [make_outputs(), make_outputs()]
+    bufs = [dict(**make_inputs(s), **out_sets[s % 2]) for s in range(S)]
 
     def step(ev=None, b=0):
         d = bufs[b]
@@ -397,18 +411,17 @@ def run_csa2(args):
         side = torch.cuda.Stream()
         side.wait_stream(stream)
         with torch.cuda.stream(side):
-            step(b=0)
-            step(b=1)
+            for b in range(S):
+                step(b=b)
         stream.wait_stream(side)
         torch.cuda.synchronize()
-        graphs = [torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()]
-        for b in range(2):
+        graphs = [torch.cuda.CUDAGraph() for _ in range(S)]
+        for b in range(S):
             with torch.cuda.graph(graphs[b]):
                 step(b=b)
-        for _ in range(max(3, args.warmup)):
-            graphs[0].replay()
+        for i in range(max(3, args.warmup)):
+            graphs[i % S].replay()
         torch.cuda.synchronize()
-    graph = graphs[0] if graphs else None
 
     barrier(world)
     t_start = torch.cuda.Event(enable_timing=True)
@@ -416,10 +429,10 @@ def run_csa2(args):
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(args.steps):
-        if graph is not None:
-            graph.replay()
+        if graphs is not None:
+            graphs[i % S].replay()
         else:
-            step()
+            step(b=i % S)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -431,17 +444,18 @@ def run_csa2(args):
     #      grid is capped so that the other micro-batch's latency-bound top-k
     #      and readout run on the remaining SMs while it streams the keys
     M = args.micro_batches
-    mbs, mb_streams, graph_steps = None, None, 0
+    mb_sets, mb_streams, graph_steps = None, None, 0
     if M > 1:
-        mbs = make_micro_batches(C, cache, wl, bufs[0], ld, n_valid, M, args.attn_split, dev)
+        mb_sets = [make_micro_batches(C, cache, wl, bufs[s], ld, n_valid, M, args.attn_split, dev)
+                   for s in range(S)]
         mb_streams = [torch.cuda.Stream() for _ in range(M)]
 
         def mb_steps(n):
             main = torch.cuda.current_stream()
             for s_ in mb_streams:
                 s_.wait_stream(main)
-            for _ in range(n):
-                for s_, d in zip(mb_streams, mbs):
+            for i in range(n):
+                for s_, d in zip(mb_streams, mb_sets[i % S]):
                     with torch.cuda.stream(s_):
                         mb_run(C, cache, d, L, scale)
             for s_ in mb_streams:
@@ -449,9 +463,9 @@ def run_csa2(args):
 
         cache.set_index_sms(args.index_sms)
         for _ in range(max(3, args.warmup)):
-            mb_steps(1)
+            mb_steps(S)
         torch.cuda.synchronize()
-        graph_steps = max(1, min(args.steps, 20))
+        graph_steps = max(1, min(args.steps, 20 // S * S))
         g_main = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_main):
             mb_steps(graph_steps)
@@ -483,7 +497,7 @@ def run_csa2(args):
     e_b = torch.cuda.Event(enable_timing=True)
     e_a.record(stream)
     for i in range(n_split):
-        step(evs[i])
+        step(evs[i], b=i % S)
     e_b.record(stream)
     torch.cuda.synchronize()
     eager_ms = e_a.elapsed_time(e_b) / n_split
@@ -504,10 +518,11 @@ def run_csa2(args):
     names_in = ["q_idx", "w", "qs", "swas"]
     names_out = ["topk", "outs", "lses"]
     flat = lambda d, names: [x for n in names for x in (d[n] if isinstance(d[n], list) else [d[n]])]
-    h_in = [pin(t) for t in flat(bufs[0], names_in)]
+    # step i's inputs are input set i mod S, copied from the host
+    h_in = [[pin(t) for t in flat(bufs[s], names_in)] for s in range(S)]
     h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in flat(bufs[0], names_out)]
              for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    h2d = sum(t.numel() * t.element_size() for t in h_in[0])
     d2h = sum(t.numel() * t.element_size() for t in h_out[0])
     copy_stream = torch.cuda.Stream()
 
@@ -516,7 +531,7 @@ def run_csa2(args):
         done = [torch.cuda.Event() for _ in range(2)]
         out_free = [torch.cuda.Event() for _ in range(2)]
         with torch.cuda.stream(copy_stream):
-            for h, d in zip(h_in, flat(bufs[0], names_in)):
+            for h, d in zip(h_in[0], flat(bufs[0], names_in)):
                 d.copy_(h, non_blocking=True)
             in_ready[0].record(copy_stream)
         for i in range(n):
@@ -533,7 +548,7 @@ def run_csa2(args):
                 if i + 1 < n:
                     if i >= 1:
                         copy_stream.wait_event(done[1 - b])
-                    for h, d in zip(h_in, flat(bufs[1 - b], names_in)):
+                    for h, d in zip(h_in[(i + 1) % S], flat(bufs[1 - b], names_in)):
                         d.copy_(h, non_blocking=True)
                     in_ready[1 - b].record(copy_stream)
                 copy_stream.wait_event(done[b])
@@ -548,8 +563,7 @@ def run_csa2(args):
         # the same double-buffered copy pipeline per micro-batch: each has a
         # compute stream (its path as a CUDA graph per buffer set) and a copy
         # stream; the micro-batches' pipelines overlap one another
-        sets = [mbs, make_micro_batches(C, cache, wl, bufs[0], ld, n_valid, M,
-                                        args.attn_split, dev)]
+        sets = [mb_sets[0], mb_sets[1]]
         cache.set_index_sms(args.index_sms)
         mb_graphs = []
         for m in range(M):
@@ -562,10 +576,11 @@ def run_csa2(args):
             mb_graphs.append(row)
         cache.set_index_sms(0)
         copy_streams = [torch.cuda.Stream() for _ in range(M)]
-        h_in_mb = [[pin(t) for t in flat(mbs[m], names_in)] for m in range(M)]
+        h_in_mb = [[[pin(t) for t in flat(mb_sets[s][m], names_in)] for m in range(M)]
+                   for s in range(S)]
         h_out_mb = [[[torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                      for t in flat(mbs[m], names_out)] for _ in range(2)] for m in range(M)]
-        h2d = sum(t.numel() * t.element_size() for h in h_in_mb for t in h)
+                      for t in flat(mb_sets[0][m], names_out)] for _ in range(2)] for m in range(M)]
+        h2d = sum(t.numel() * t.element_size() for h in h_in_mb[0] for t in h)
         d2h = sum(t.numel() * t.element_size() for h in h_out_mb for t in h[0])
 
         def run_e2e(n):
@@ -577,7 +592,7 @@ def run_csa2(args):
                 s_.wait_stream(stream)
             for m in range(M):
                 with torch.cuda.stream(copy_streams[m]):
-                    for h, t in zip(h_in_mb[m], flat(sets[0][m], names_in)):
+                    for h, t in zip(h_in_mb[0][m], flat(sets[0][m], names_in)):
                         t.copy_(h, non_blocking=True)
                     in_ready[m][0].record(copy_streams[m])
             for i in range(n):
@@ -594,7 +609,8 @@ def run_csa2(args):
                         if i + 1 < n:
                             if i >= 1:
                                 ps.wait_event(done[m][1 - b])
-                            for h, t in zip(h_in_mb[m], flat(sets[1 - b][m], names_in)):
+                            for h, t in zip(h_in_mb[(i + 1) % S][m],
+                                            flat(sets[1 - b][m], names_in)):
                                 t.copy_(h, non_blocking=True)
                             in_ready[m][1 - b].record(ps)
                         ps.wait_event(done[m][b])
@@ -654,11 +670,13 @@ def run_csa2(args):
     # this library's kernels per step: indexer, top-k segments, top-k, one
     # attention launch per layer (workspace memsets are not counted)
     launches_per_step = (3 + L) * ((B + 1023) // 1024) * max(1, M)
+    config = workload_config(wl, args.layout)
+    config["input_sets"] = S
     line = {
         "metric": METRIC, "value": B * world * args.steps / elapsed_max, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": workload_config(wl, args.layout),
+        "data": "synthetic", "config": config,
         "roofline": {"kernel": "k_index (indexer scores, tcgen05)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
@@ -808,7 +826,8 @@ def measure_epilogue(C, cache, d, attn_ws, scale, wl, dev, stream, iters):
     if cache.device_error() != 0:
         raise RuntimeError("device error word set during the epilogue measurement")
     return {"plain_layer_ms": plain, "sink_rope_layer_ms": variants,
-            "timed_as": "eager calls, one layer"}
+            "timed_as": "eager calls, one layer, the same inputs every call (their 26 MB "
+                        "stay in L2: a relative figure)"}
 
 
 def measure_bf16_scores(C, cache, wl, q_idx, w, n_valid, fp32_idx, key_hist, topk_ws, dev,

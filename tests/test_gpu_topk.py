@@ -106,3 +106,22 @@ def test_segmented_ragged_rows(C):
                       workspace=ws).cpu().numpy()
     for r, n in enumerate(ns):
         assert np.array_equal(got[r], O.topk(buf[r, :n], 512)), r
+
+
+def test_segmented_unaligned_rows(C):
+    """Segmented candidate search over rows that are not 16-byte aligned (odd
+    row stride), where the segment kernel stages the scores with plain loads
+    instead of asynchronous 16-byte copies."""
+    import torch
+    from tests.test_gpu_index import _key_hist
+    rng = np.random.default_rng(12)
+    ns = [513, 9000, 16385, 70001]
+    ld = 70001 + 2
+    buf = rng.standard_normal((len(ns), ld)).astype(np.float32)
+    kh = np.stack([_key_hist(buf[r, :n]) for r, n in enumerate(ns)]).astype(np.int32)
+    ws = torch.empty(C.csa2_topk_workspace_bytes(len(ns), max(ns)), dtype=torch.uint8,
+                     device="cuda")
+    got = C.csa2_topk(f32_dev(buf), ns, 512, key_hist=torch.from_numpy(kh).cuda(),
+                      workspace=ws).cpu().numpy()
+    for r, n in enumerate(ns):
+        assert np.array_equal(got[r], O.topk(buf[r, :n], 512)), r
