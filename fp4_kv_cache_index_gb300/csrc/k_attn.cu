@@ -123,6 +123,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q = qh / hgs, hg = qh % hgs;
   const int n_topk_tiles = p.topk / kRows;
   const int32_t* idx_row = p.topk_idx + (int64_t)q * p.topk;
+  // the top-k row decides the first gathers: its loads go out before
+  // anything else
+  int32_t idx_pre[2048 / kThreads];
+#pragma unroll
+  for (int j = 0; j < 2048 / kThreads; ++j) {
+    const int i = tid + j * kThreads;
+    idx_pre[j] = i < p.topk ? idx_row[i] : -1;
+  }
 
   // ---- per-query geometry
   int64_t base;
@@ -179,8 +187,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the top-k row into shared memory (unusable slots become -1), and which
   // tiles hold at least one usable index
   bool bad = false;
-  for (int i = tid; i < p.topk; i += kThreads) {
-    int32_t s = idx_row[i];
+#pragma unroll
+  for (int j = 0; j < 2048 / kThreads; ++j) {
+    const int i = tid + j * kThreads;
+    if (i >= p.topk) break;
+    int32_t s = idx_pre[j];
     if (s >= 0 && s < len) sm.tile_any[i / kRows] = 1;
     else {
       if (s >= len) bad = true;
