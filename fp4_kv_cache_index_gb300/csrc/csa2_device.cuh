@@ -106,6 +106,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   }
 }
 
+// ---------------------------------------------------------------- launch order
+// A kernel launched with programmatic stream serialisation may be scheduled
+// while the kernel before it in the stream is still finishing; this waits
+// until that kernel has completed and its memory operations are visible (at
+// once when there is no such predecessor).  Every kernel of this library
+// launched that way calls it before touching global memory.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

@@ -13,6 +13,16 @@ constexpr uint32_t kErrTimeoutBit = 1u;
 constexpr uint32_t kErrIndexBit = 2u;
 constexpr uint32_t kErrRangeBit = 4u;   // an MXFP4 indexer scale outside 2^-13 .. 2^13
 
+// Launch attribute: programmatic stream serialisation (the kernel's launch
+// overlaps the end of the previous kernel in the stream; the kernel waits for
+// it with griddepcontrol.wait before its first global memory access).
+inline cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
 constexpr int kHeadDim = 512;     // main-KV latent / attention head dim
 constexpr int kIdxDim = 128;      // indexer head dim
 constexpr int kIdxHeads = 32;     // indexer heads

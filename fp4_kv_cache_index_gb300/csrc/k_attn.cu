@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Small& sm = *reinterpret_cast<Small*>(smem + kSmallOff);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  griddep_wait();
   const int hgs = p.n_heads / kHG;
   const int split = blockIdx.x % p.splits;
   const int qh = blockIdx.x / p.splits;            // (query, head group)
@@ -784,23 +785,22 @@ cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tm_q, const CUte
   if (e != cudaSuccess) return e;
   const int64_t blocks = (int64_t)p.nq * (p.n_heads / kHG) * p.splits;
   if (blocks <= 0) return cudaSuccess;
-  if (p.splits == 1) {
-    k_attn<<<(unsigned)blocks, kThreads, kSmemBytes, s>>>(p, tm_q, tm_swa);
-    return cudaGetLastError();
-  }
-  // splits == 2: the two CTAs of a (query, head group) form a cluster
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2] = {pdl_attribute(), {}};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (p.splits == 2) {
+    // the two CTAs of a (query, head group) form a cluster
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   return cudaLaunchKernelEx(&cfg, k_attn, p, tm_q, tm_swa);
 }
 

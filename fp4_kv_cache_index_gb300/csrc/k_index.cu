@@ -134,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  griddep_wait();
 
   const int total = p.tile_prefix[p.n_groups];
   const int begin = (int)(((int64_t)total * blockIdx.x) / gridDim.x);
@@ -445,8 +446,15 @@ cudaError_t launch_index(const IndexParams& p, const CUtensorMap& tm_k, const CU
   const int smem = index_smem_bytes(p.qpg);
   cudaError_t e = cudaFuncSetAttribute(k_index, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k_index<<<grid, kThreads, smem, s>>>(p, tm_k, tm_q);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_index, p, tm_k, tm_q);
 }
 
 }  // namespace csa2

@@ -219,6 +219,7 @@ __device__ __forceinline__ void seg_chunk(const ScoreRow& srow, int64_t e0, int 
 __global__ void __launch_bounds__(kSegThreads, 8) k_topk_seg(const __grid_constant__ TopkParams p,
                                                              int row0) {
   __shared__ SegShared sh;
+  griddep_wait();
   const int row = row0 + blockIdx.y, seg = blockIdx.x, tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   if (row >= p.rows) return;
@@ -317,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
                                                        int row0) {
   extern __shared__ uint8_t smem_raw[];
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
+  griddep_wait();
   const int row = row0 + blockIdx.x;
   if (row >= p.rows) return;
   const int64_t n = row_valid_count(p, row);
@@ -554,15 +556,24 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
   const int smem = (int)sizeof(Shared);
   cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   for (int r0 = 0; r0 < p.rows; r0 += kTopkMaxRowsPerLaunch) {
     const int nr = (p.rows - r0 < kTopkMaxRowsPerLaunch) ? p.rows - r0 : kTopkMaxRowsPerLaunch;
     if (p.seg_ws && p.key_hist && p.n_seg > 0) {
-      k_topk_seg<<<dim3(p.n_seg, nr), kSegThreads, 0, s>>>(p, r0);
-      e = cudaGetLastError();
+      cfg.gridDim = dim3((unsigned)p.n_seg, (unsigned)nr);
+      cfg.blockDim = dim3(kSegThreads);
+      cfg.dynamicSmemBytes = 0;
+      e = cudaLaunchKernelEx(&cfg, k_topk_seg, p, r0);
       if (e != cudaSuccess) return e;
     }
-    k_topk<<<nr, kThreads, smem, s>>>(p, r0);
-    e = cudaGetLastError();
+    cfg.gridDim = dim3((unsigned)nr);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    e = cudaLaunchKernelEx(&cfg, k_topk, p, r0);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
