@@ -334,6 +334,14 @@ __device__ __forceinline__ void tmem_wait_st() {
 // Read-only global loads issued exactly where they are written (volatile
 // asm: the compiler neither sinks them towards their use nor merges them),
 // for prefetches whose results are consumed much later.
+// 32 bytes (32-byte aligned) in one 256-bit load.
+__device__ __forceinline__ void ldg_now_v8(const void* a, uint4& lo, uint4& hi) {
+  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y),
+                 "=r"(hi.z), "=r"(hi.w)
+               : "l"(a));
+}
+
 __device__ __forceinline__ uint4 ldg_now_v4(const void* a) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"

@@ -235,7 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // w % 8).
   //
   // Gather of one top-k tile into registers: for each half h a worker loads
-  // the 32 code bytes of its chunk 4 h + quarter and that chunk's scale bytes
+  // the 32 code bytes of its chunk 4 h + quarter (one 256-bit load, so each
+  // 32-byte sector is requested once) and that chunk's scale bytes
   // (two UE8M0 or four E4M3), plus the code word and scale byte of its extra
   // piece.  Issued one tile ahead, so the loads are in flight while the
   // tensor core and the softmax work on the current tile.
@@ -254,8 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t* src = p.codes + row * kCodeBytes + g_q * 32;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        cw[2 * h] = ldg_now_v4(src + 128 * h);
-        cw[2 * h + 1] = ldg_now_v4(src + 128 * h + 16);
+        ldg_now_v8(src + 128 * h, cw[2 * h], cw[2 * h + 1]);   // 32-byte aligned: 256 B rows
         if (p.layout == 0)
           scw[h] = ldg_now_u16(p.scales + row * 16 + 8 * h + 2 * g_q);
         else
