@@ -45,7 +45,7 @@ constexpr float kLazyRescale = 8.0f;  // log2 units
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kKvOff = 0;                              // 8 x [128 x 128 B]
 constexpr int kQOff = kKvOff + kRows * kHeadDim * 2;   // 8 x [64 x 128 B]
-constexpr int kPOff = kQOff + kHG * kHeadDim * 2;      // 2 x [64 x 128 B]
+constexpr int kPOff = kQOff + kHG * kHeadDim * 2;      // [128 x 128 B]
 constexpr int kIdxOff = kPOff + kHG * kRows * 2;        // the query's top-k row
 constexpr int kSmallOff = kIdxOff + 2048 * 4;
 struct Small {
@@ -303,13 +303,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // MMA descriptors: bases built once, K steps added to the address field
   // (all of shared memory is below 2^18 bytes, so the 14-bit field never
-  // carries).  S^T = KV * Q^T: K-major A and B; O^T += KV^T * P^T: MN-major A.
+  // carries).  S^T = KV * Q^T: K-major A and B; O^T += KV^T * P^T: MN-major
+  // A and B (P^T is stored one candidate row of 64 heads per 128 bytes, the
+  // layout in which each thread writes its own row).
   const uint64_t d_skv = sdesc_sw128(smem_u32(kv), 16, 1024);
   const uint64_t d_sq = sdesc_sw128(smem_u32(qs), 16, 1024);
   const uint64_t d_okv = sdesc_sw128(smem_u32(kv), kRows * 128, 1024);
-  const uint64_t d_op = sdesc_sw128(smem_u32(ps), 16, 1024);
+  const uint64_t d_op = sdesc_sw128(smem_u32(ps), kRows * 128, 1024);
   constexpr uint32_t id_s = idesc_bf16_f32(128, kHG, false, false);
-  constexpr uint32_t id_o = idesc_bf16_f32(128, kHG, true, false);
+  constexpr uint32_t id_o = idesc_bf16_f32(128, kHG, true, true);
   // S^T K step ks (channels 16 ks .. 16 ks + 15)
   auto mma_s = [&](int ks) {
     const uint32_t ao = (uint32_t)((ks >> 2) * (kRows * 128) + (ks & 3) * 32);
@@ -319,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // O^T d-block i (reads KV chunks 2 i, 2 i + 1), K step ks (rows 16 ks ..)
   auto mma_o = [&](int i, int ks, bool first) {
     const uint32_t ao = (uint32_t)((2 * i) * (kRows * 128) + ks * 2048);
-    const uint32_t bo = (uint32_t)((ks >> 2) * (kHG * 128) + (ks & 3) * 32);
+    const uint32_t bo = (uint32_t)(ks * 2048);
     umma_bf16(tmem + o_col + 64 * i, d_okv + (ao >> 4), d_op + (bo >> 4), id_o,
               (!first || ks > 0) ? 1u : 0u);
   };
@@ -526,17 +528,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
       }
     }
+    {
+      // P^T as the MN-major B operand: this thread's candidate row holds its
+      // 16 heads in two 16-byte pieces (8 heads each), swizzled by the row
+      uint32_t pk[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int h = 16 * hh + i;
-      const float pr = (x[i] == -INFINITY) ? 0.0f : fast_exp2(x[i] - mh[i]);
-      const uint32_t pb = float_to_bf16_bits(pr);
-      lsum[i] += bf16_bits_to_float(pb);
-      // P^T is the K-major B operand: row h, column = candidate row
-      uint8_t* prow = ps + (row >> 6) * (kHG * 128) + h * 128;
-      const int chunk = (row & 63) >> 3;
-      *reinterpret_cast<uint16_t*>(prow + ((chunk ^ (h & 7)) << 4) + (row & 7) * 2) =
-          (uint16_t)pb;
+      for (int i = 0; i < 8; ++i) {
+        const float p0 = (x[2 * i] == -INFINITY) ? 0.0f : fast_exp2(x[2 * i] - mh[2 * i]);
+        const float p1 =
+            (x[2 * i + 1] == -INFINITY) ? 0.0f : fast_exp2(x[2 * i + 1] - mh[2 * i + 1]);
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);   // .x: head 2i (low half)
+        pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+        lsum[2 * i] += __uint_as_float(pk[i] << 16);
+        lsum[2 * i + 1] += __uint_as_float(pk[i] & 0xFFFF0000u);
+      }
+      uint8_t* prow = ps + row * 128;
+      *reinterpret_cast<uint4*>(prow + (((2 * hh) ^ (row & 7)) << 4)) =
+          make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      *reinterpret_cast<uint4*>(prow + (((2 * hh + 1) ^ (row & 7)) << 4)) =
+          make_uint4(pk[4], pk[5], pk[6], pk[7]);
     }
     fence_proxy_async_smem();
     tc_fence_before();
