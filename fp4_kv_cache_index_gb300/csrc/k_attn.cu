@@ -20,10 +20,10 @@
 // multiply, written to shared memory in the MMA layout).  With the candidate
 // rows as the MMA M dimension:
 //     S^T[128 x 64]  = KV[128 x 512] * Q[64 x 512]^T        (K-major A and B)
-//     O^T[512 x 64] += KV^T[512 x 128] * P^T[128 x 64]^T     (MN-major A)
+//     O^T[512 x 64] += KV^T[512 x 128] * P^T[128 x 64]       (MN-major A and B)
 // both on tcgen05 with fp32 accumulators in TMEM; the same swizzled KV tile
 // serves as the K-major A of the first product and the MN-major A of the
-// second.  The single KV buffer is refilled in two channel halves: the next
+// second, and P^T is written by the softmax one candidate row per thread.  The single KV buffer is refilled in two channel halves: the next
 // tile's first half as soon as the O^T products that read it are done (while
 // the others run), and S^T of that half while the second half is written.
 // Online softmax (base 2) runs across TMEM lanes: each thread holds one
