@@ -23,6 +23,11 @@
  *   - Calls are stream-ordered on `stream` (a cudaStream_t; NULL = legacy
  *     default stream), never synchronise the device and never allocate
  *     device memory.  Scratch memory comes from the caller (`workspace`).
+ *     The indexer, top-k and readout kernels are launched with programmatic
+ *     stream serialisation: a launch may begin while the previous kernel in
+ *     the stream finishes, but each waits for that kernel to complete before
+ *     its first global memory access, so every read and write keeps its
+ *     stream order (also inside captured CUDA graphs).
  *   - Errors found on the host return a status before anything is
  *     launched.  Errors found inside a kernel (a bounded wait that ran out,
  *     an index out of range) set a sticky device error word that
