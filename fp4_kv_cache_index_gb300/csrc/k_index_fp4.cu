@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  griddep_wait();
 
   const int total = p.tile_prefix[p.n_groups];
   const int begin = (int)(((int64_t)total * blockIdx.x) / gridDim.x);
@@ -448,8 +449,15 @@ cudaError_t launch_index_fp4(const IndexParams& p, const CUtensorMap& tm_q, int 
   cudaError_t e = cudaFuncSetAttribute(k_index_fp4, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        smem);
   if (e != cudaSuccess) return e;
-  k_index_fp4<<<grid, kThreads, smem, s>>>(p, tm_q);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_index_fp4, p, tm_q);
 }
 
 }  // namespace csa2

@@ -23,7 +23,7 @@
  *   - Calls are stream-ordered on `stream` (a cudaStream_t; NULL = legacy
  *     default stream), never synchronise the device and never allocate
  *     device memory.  Scratch memory comes from the caller (`workspace`).
- *     The indexer, top-k and readout kernels are launched with programmatic
+ *     The indexers, top-k and readout kernels are launched with programmatic
  *     stream serialisation: a launch may begin while the previous kernel in
  *     the stream finishes, but each waits for that kernel to complete before
  *     its first global memory access, so every read and write keeps its
