@@ -64,3 +64,18 @@ def test_compression_and_pool_arithmetic():
 def test_kv_latent_bound_fits_the_format():
     assert abs(G["kv_latent_dim"] ** 0.5 - G["kv_latent_abs_bound"]) < 0.05
     assert G["kv_latent_abs_bound"] < G["fp4_max_magnitude"]
+
+
+@pytest.mark.parametrize("window", [1, 4, 128])
+@pytest.mark.parametrize("row0", [0, 3, 150])
+def test_window_rows_by_enumeration(window, row0):
+    """The window rows of a query at position p: the last `window` tokens up
+    to and including p, none before the replay start ("DeepSeek-V4.1-Flash"
+    report, section 3.2.2, bounded replay), checked against enumerating the
+    positions one by one."""
+    for p in range(row0, row0 + 400):
+        lo, hi = O.swa_rows(p, window, row0)
+        want = [j for j in range(0, p + 1) if j > p - window and j >= row0]
+        assert list(range(lo, hi)) == want, (p, window, row0)
+    # the window of the 128K workload: 128 rows (the query's own token last)
+    assert O.swa_rows(131071, G["swa_window"]) == (131071 - 127, 131072)
