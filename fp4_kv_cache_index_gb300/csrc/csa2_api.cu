@@ -36,6 +36,9 @@ struct csa2_cache {
   uint8_t* idx_scales;
   CUtensorMap tm_k;    // indexer keys, 128-row boxes (contiguous tiles)
   CUtensorMap tm_k8;   // indexer keys, one 8-key block per box (pool mode)
+  CUtensorMap tm_kc;   // MXFP4 key codes, 128-row boxes
+  CUtensorMap tm_kc8;  // MXFP4 key codes, one 8-key block per box (pool mode)
+  CUtensorMap tm_kc2;  // MXFP4 key codes, two keys per 128-byte row, 128-row boxes
   int num_sms;
   int index_sms;       // SMs the indexer's persistent grid may occupy
 };
@@ -84,8 +87,7 @@ Layout layout_for(const csa2_config_t* c, int64_t total) {
   if (c->idx_layout == CSA2_IDX_MXFP4) {
     o = align_up(o + (size_t)total * (kIdxDim / 2), kAlign);   // E2M1 codes
     L.idxs_off = o;
-    // UE8M0 scales; 16 spare bytes: the indexer copies 16-byte aligned
-    // windows of scale words, up to 3 rows past the last one
+    // UE8M0 scales (16 spare bytes kept so that earlier cache sizes hold)
     o = align_up(o + (size_t)total * (kIdxDim / 32) + 16, kAlign);
   } else {
     o = align_up(o + (size_t)total * kIdxDim * 2, kAlign);
@@ -130,6 +132,24 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// MXFP4 key codes as bytes [rows, row_bytes] (64: one key per row, 64-byte
+// swizzle; 128: two keys per row, 128-byte swizzle), boxes of box_rows rows:
+// the K-major layouts of the block-scaled MMA's operands.
+bool make_code_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t row_bytes,
+                   uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows == 0) return false;
+  cuuint64_t gdim[2] = {row_bytes, rows};
+  cuuint64_t gstride[1] = {row_bytes};
+  cuuint32_t box[2] = {row_bytes, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Indexer keys [rows, 128] bf16 seen as (64 columns, rows, 2 halves): one
 // box of (64, 8, 2) is a whole block of 8 keys, landing in shared memory as
 // two 1 KB 128B-swizzled atoms (columns 0-63, then 64-127).
@@ -152,17 +172,20 @@ csa2_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : C
 
 int64_t score_ld(int64_t n) { return std::max<int64_t>(4, (n + 3) / 4 * 4); }
 
-// The indexer kernel for the cache's key storage (bf16 keys by TMA, or
-// MXFP4 keys by bulk copy and on-chip dequantisation).
+// The indexer kernel for the cache's key storage: bf16 keys (TMA, kind::f16
+// MMAs), or MXFP4 keys (E2M1 codes by TMA, block-scaled kind::mxf4 MMAs,
+// queries rounded to MXFP4 on chip from q_idx).  `pool` selects the
+// pool-mode tensor map of bf16 keys.
 cudaError_t launch_index_any(const csa2_cache* c, IndexParams& ip, const CUtensorMap& tm_q,
-                             int grid, cudaStream_t s) {
+                             const void* q_idx, int grid, cudaStream_t s, bool pool = false) {
   if (c->cfg.idx_layout == CSA2_IDX_MXFP4) {
     ip.idx_codes = c->idx_codes;
     ip.idx_scales = c->idx_scales;
     ip.idx_total = c->total;
-    return launch_index_fp4(ip, tm_q, grid, s);
+    ip.q_idx = static_cast<const uint16_t*>(q_idx);
+    return launch_index_fp4(ip, c->tm_kc, c->tm_kc2, c->tm_kc8, grid, s);
   }
-  return launch_index(ip, c->tm_k, tm_q, grid, s);
+  return launch_index(ip, pool ? c->tm_k8 : c->tm_k, tm_q, grid, s);
 }
 
 // Append / compress segments: rows of one launch grouped by sequence.
@@ -316,6 +339,14 @@ csa2_status_t csa2_cache_create(const csa2_config_t* cfg, int32_t batch, const i
   c->index_sms = c->num_sms;
   if (!mx && (!make_map(&c->tm_k, c->idxk, (uint64_t)c->total, kIdxDim, 64, 128) ||
               !make_block_map(&c->tm_k8, c->idxk, (uint64_t)c->total))) {
+    delete c;
+    return CSA2_ERR_CUDA;
+  }
+  // the two-key view ends at most 64 bytes past the last code row: inside
+  // the cache buffer (the scale region follows)
+  if (mx && (!make_code_map(&c->tm_kc, c->idx_codes, (uint64_t)c->total, kIdxDim / 2, 128) ||
+             !make_code_map(&c->tm_kc8, c->idx_codes, (uint64_t)c->total, kIdxDim / 2, kHsiBlock) ||
+             !make_code_map(&c->tm_kc2, c->idx_codes, (uint64_t)(c->total + 1) / 2, kIdxDim, 128))) {
     delete c;
     return CSA2_ERR_CUDA;
   }
@@ -494,7 +525,8 @@ csa2_status_t run_index_decode(const csa2_cache_t* c, int32_t nq, const void* q_
           cudaSuccess)
     return CSA2_ERR_CUDA;
   // keys per tile: the MXFP4 decode kernel takes 256, every other path 128
-  const int64_t tile_e = c->cfg.idx_layout == CSA2_IDX_MXFP4 ? 256 : 128;
+  const bool mx = c->cfg.idx_layout == CSA2_IDX_MXFP4;
+  const int64_t tile_e = mx ? 256 : 128;
   for (int q0 = 0; q0 < nq; q0 += kMaxIdxGroups) {
     const int n = std::min(kMaxIdxGroups, nq - q0);
     std::memset(ip, 0, sizeof(IndexParams));
@@ -515,16 +547,18 @@ csa2_status_t run_index_decode(const csa2_cache_t* c, int32_t nq, const void* q_
       const int64_t nv = c->len[s];
       ip->entry_base[i] = c->off[s];
       ip->nvis[i] = (int32_t)nv;
-      ip->tile_prefix[i + 1] = ip->tile_prefix[i] + (int32_t)((nv + tile_e - 1) / tile_e);
+      // MXFP4 decode tiles start at an even key row (one row early when the
+      // sequence starts at an odd one)
+      const int64_t lead = (mx && nv > 0) ? (c->off[s] & 1) : 0;
+      ip->tile_prefix[i + 1] = ip->tile_prefix[i] + (int32_t)((nv + lead + tile_e - 1) / tile_e);
     }
     CUtensorMap tm_q;
-    if (!make_map(&tm_q, qb + (int64_t)q0 * kIdxHeads * kIdxDim, (uint64_t)n * kIdxHeads,
-                  kIdxDim, 64, 32))
-      return CSA2_ERR_CUDA;
+    const uint16_t* qn = qb + (int64_t)q0 * kIdxHeads * kIdxDim;
+    if (!make_map(&tm_q, qn, (uint64_t)n * kIdxHeads, kIdxDim, 64, 32)) return CSA2_ERR_CUDA;
     const int tiles = ip->tile_prefix[n];
     if (tiles > 0) {
       const int grid = std::min(c->index_sms, tiles);
-      if (launch_index_any(c, *ip, tm_q, grid, S(stream)) != cudaSuccess) return CSA2_ERR_CUDA;
+      if (launch_index_any(c, *ip, tm_q, qn, grid, S(stream)) != cudaSuccess) return CSA2_ERR_CUDA;
     }
   }
   return CSA2_OK;
@@ -660,7 +694,10 @@ csa2_status_t csa2_index_scores_prefill(const csa2_cache_t* c, int32_t seq, int3
       ld % 4 != 0)
     return CSA2_ERR_INVALID_ARG;
   if (ld < c->len[seq]) return CSA2_ERR_CAPACITY;
-  constexpr int kQpg = 8;   // queries sharing one K_I tile in the MMA (N = 256)
+  // queries sharing one tile of keys in the MMA: 8 (N = 256) on bf16 keys,
+  // 4 (N = 128) on MXFP4 keys, whose tensor memory also holds the scales
+  const bool mx = c->cfg.idx_layout == CSA2_IDX_MXFP4;
+  const int kQpg = mx ? 4 : 8;
   const int m = c->cfg.ratio;
   const int64_t len = c->len[seq];
   const uint16_t* qb = static_cast<const uint16_t*>(q_idx);
@@ -691,15 +728,15 @@ csa2_status_t csa2_index_scores_prefill(const csa2_cache_t* c, int32_t seq, int3
       ip->tile_prefix[g + 1] = ip->tile_prefix[g] + (int32_t)((nv + 127) / 128);
     }
     CUtensorMap tm_q;
-    if (!make_map(&tm_q, qb + (int64_t)q0 * kIdxHeads * kIdxDim, (uint64_t)n * kIdxHeads,
-                  kIdxDim, 64, 32 * kQpg)) {
+    const uint16_t* qn = qb + (int64_t)q0 * kIdxHeads * kIdxDim;
+    if (!make_map(&tm_q, qn, (uint64_t)n * kIdxHeads, kIdxDim, 64, 32 * kQpg)) {
       st = CSA2_ERR_CUDA;
       break;
     }
     const int tiles = ip->tile_prefix[groups];
     if (tiles > 0) {
       const int grid = std::min(c->index_sms, tiles);
-      if (launch_index_any(c, *ip, tm_q, grid, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
+      if (launch_index_any(c, *ip, tm_q, qn, grid, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
     }
   }
   delete ip;
@@ -1041,7 +1078,6 @@ csa2_status_t csa2_index_topk_reindex_decode(const csa2_cache_t* c, int32_t nq, 
                                              csa2_stream_t stream) {
   if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
   if (max_blocks <= 0 || max_blocks % 16 != 0 || max_blocks > 4096) return CSA2_ERR_UNSUPPORTED;
-  if (c->cfg.idx_layout != CSA2_IDX_BF16) return CSA2_ERR_UNSUPPORTED;   // pool mode: bf16 keys
   if (nq == 0) return CSA2_OK;
   csa2_status_t st = check_decode_queries(c, nq, q_idx, w, seq_ids);
   if (st != CSA2_OK) return st;
@@ -1060,6 +1096,10 @@ csa2_status_t csa2_index_topk_reindex_decode(const csa2_cache_t* c, int32_t nq, 
   const uint16_t* qb = static_cast<const uint16_t*>(q_idx);
   if (cudaMemsetAsync(key_hist, 0, (size_t)nq * kKeyHistBinsHost * 4, S(stream)) != cudaSuccess)
     st = CSA2_ERR_CUDA;
+  // tiles of 16 blocks (bf16 keys) or 32 blocks (MXFP4 keys, 256 slots; a
+  // last tile of 16 blocks when max_blocks is not a multiple of 32)
+  const int blocks_per_tile = c->cfg.idx_layout == CSA2_IDX_MXFP4 ? 32 : 16;
+  const int pool_tiles = (max_blocks + blocks_per_tile - 1) / blocks_per_tile;
   for (int q0 = 0; q0 < nq && st == CSA2_OK; q0 += kMaxIdxGroups) {
     const int n = std::min(kMaxIdxGroups, nq - q0);
     // ---- the pool positions' scores (indexer in pool mode)
@@ -1080,16 +1120,16 @@ csa2_status_t csa2_index_topk_reindex_decode(const csa2_cache_t* c, int32_t nq, 
       const int s = seq_ids ? seq_ids[q0 + i] : q0 + i;
       ip->entry_base[i] = c->off[s];
       ip->nvis[i] = (int32_t)c->len[s];
-      ip->tile_prefix[i + 1] = ip->tile_prefix[i] + max_blocks / 16;
+      ip->tile_prefix[i + 1] = ip->tile_prefix[i] + pool_tiles;
     }
     CUtensorMap tm_q;
-    if (!make_map(&tm_q, qb + (int64_t)q0 * kIdxHeads * kIdxDim, (uint64_t)n * kIdxHeads,
-                  kIdxDim, 64, 32)) {
+    const uint16_t* qn = qb + (int64_t)q0 * kIdxHeads * kIdxDim;
+    if (!make_map(&tm_q, qn, (uint64_t)n * kIdxHeads, kIdxDim, 64, 32)) {
       st = CSA2_ERR_CUDA;
       break;
     }
     const int grid = std::min(c->index_sms, ip->tile_prefix[n]);
-    if (launch_index(*ip, c->tm_k8, tm_q, grid, S(stream)) != cudaSuccess) {
+    if (launch_index_any(c, *ip, tm_q, qn, grid, S(stream), true) != cudaSuccess) {
       st = CSA2_ERR_CUDA;
       break;
     }
@@ -1147,7 +1187,7 @@ csa2_status_t csa2_get_device_error(const csa2_cache_t* c, csa2_stream_t stream,
   if (word && cudaMemsetAsync(c->d_err, 0, sizeof(uint32_t), S(stream)) != cudaSuccess)
     return CSA2_ERR_CUDA;
   *device_status = (word & kErrTimeoutBit) ? CSA2_ERR_TIMEOUT
-                   : (word & (kErrIndexBit | kErrRangeBit)) ? CSA2_ERR_DEVICE
+                   : (word & kErrIndexBit) ? CSA2_ERR_DEVICE
                                            : CSA2_OK;
   return CSA2_OK;
 }

@@ -18,7 +18,6 @@ namespace csa2 {
 // index was seen (and skipped).
 constexpr uint32_t kErrTimeout = kErrTimeoutBit;
 constexpr uint32_t kErrIndex = kErrIndexBit;
-constexpr uint32_t kErrRange = kErrRangeBit;
 
 __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bit) {
   if (err) atomicOr(err, bit);
@@ -242,18 +241,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bo
          | ((a_mn_major ? 1u : 0u) << 15)  // A major-ness
          | ((b_mn_major ? 1u : 0u) << 16)  // B major-ness
          | ((N >> 3) << 17) | ((M >> 4) << 24);
-}
-
-// D[tmem] (+)= A[smem] * B[smem]^T with 8-bit operands (kind::f8f6f4, K = 32
-// per instruction); with the instruction descriptor of idesc_bf16_f32 the
-// operand formats read as E5M2.
-__device__ __forceinline__ void umma_e5m2(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
@@ -534,27 +521,6 @@ __device__ __forceinline__ float e2m1_value(uint32_t code) {
   const float mag = (m < 2u) ? 0.5f * (float)m : __uint_as_float((126u + (m >> 1)) << 23) *
                                                   (1.0f + 0.5f * (float)(m & 1u));
   return (code & 8u) ? -mag : mag;
-}
-
-// Byte table of |E2M1 value| * 2^e as E5M2 (e in [-13, 13], every nonzero
-// value then normal): lo = codes 0-3 (0, 0.5, 1, 1.5), hi = codes 4-7 (2, 3,
-// 4, 6).  At e = 0 the bytes are 00 38 3C 3E | 40 42 44 46; scaling by 2^e
-// adds e to the 5-bit exponent field (bits 2-6) of every nonzero entry.
-__device__ __forceinline__ void e5m2_table(int e, uint32_t& lo, uint32_t& hi) {
-  const uint32_t d = ((uint32_t)(e << 2) & 0xFFu) * 0x01010101u;
-  lo = __vadd4(0x3E3C3800u, d & 0xFFFFFF00u);
-  hi = __vadd4(0x46444240u, d);
-}
-
-// Eight E2M1 codes (code i in bits 4i..4i+3) through a table of e5m2_table:
-// E5M2 bytes of codes 0-3 in `lo`, codes 4-7 in `hi` (sign bit 7 from bit 3).
-__device__ __forceinline__ void e2m1x8_to_e5m2x8(uint32_t codes, uint32_t tlo, uint32_t thi,
-                                                 uint32_t& lo, uint32_t& hi) {
-  const uint32_t ev = codes << 4;
-  const uint32_t sg0 = prmt(ev, codes, 0xD9C8u) & 0x80808080u;
-  const uint32_t sg1 = prmt(ev, codes, 0xFBEAu) & 0x80808080u;
-  lo = prmt(tlo, thi, codes & 0x7777u) | sg0;
-  hi = prmt(tlo, thi, (codes >> 16) & 0x7777u) | sg1;
 }
 
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {

@@ -11,7 +11,6 @@ namespace csa2 {
 // Sticky device error word bits (see csa2_get_device_error).
 constexpr uint32_t kErrTimeoutBit = 1u;
 constexpr uint32_t kErrIndexBit = 2u;
-constexpr uint32_t kErrRangeBit = 4u;   // an MXFP4 indexer scale outside 2^-13 .. 2^13
 
 // Launch attribute: programmatic stream serialisation (the kernel's launch
 // overlaps the end of the previous kernel in the stream; the kernel waits for
@@ -69,29 +68,39 @@ struct IndexParams {
   int64_t ld;
   uint32_t* key_hist;      // nullable [nq, 2048] score-key histogram (qpg == 1 only)
   int32_t score_bf16;      // 1: scores are stored as bf16 (uint16 [nq, ld], nearest even)
+  const uint16_t* q_idx;     // MXFP4 keys (k_index_fp4): bf16 queries [nq, 32, 128]
   const uint8_t* idx_codes;  // MXFP4 keys (k_index_fp4): E2M1 codes [idx_total, 64]
-  const uint8_t* idx_scales; // MXFP4 keys: UE8M0 scales [idx_total, 4] (+ 16 bytes of padding)
+  const uint8_t* idx_scales; // MXFP4 keys: UE8M0 scales [idx_total, 4]
   int64_t idx_total;         // MXFP4 keys: rows in the cache
   const int32_t* pool;     // nullable: pool mode, [nq, pool_blocks] block ids (-1 unused)
   int32_t pool_blocks;     // blocks per pool row (multiple of 16)
   uint32_t* err;
   int32_t nq;
-  int32_t qpg;             // queries per group (1 decode, 8 prefill)
+  int32_t qpg;             // queries per group (1 decode, 8 prefill; MXFP4 keys: 4)
   int32_t n_groups;
   int32_t prefill;         // 1: visibility from positions
   int64_t pre_base;        // prefill: entry offset of the sequence
   int64_t pos0;            // prefill: position of query 0
   int32_t pre_len;         // prefill: entries in the sequence
   int32_t ratio;
-  int32_t tile_prefix[kMaxIdxGroups + 1];  // cumulative 128-entry tiles per group
+  int32_t tile_prefix[kMaxIdxGroups + 1];  // cumulative tiles per group (128 entries; the
+                                           // MXFP4 kernel: 256 for one query per group)
   int64_t entry_base[kMaxIdxGroups];       // decode: entry offset of the group's sequence
   int32_t nvis[kMaxIdxGroups];             // decode: visible entries of the group's query
 };
 int index_smem_bytes(int qpg);
 cudaError_t launch_index(const IndexParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_q,
                          int grid, cudaStream_t s);
-int index_fp4_smem_bytes(int qpg);
-cudaError_t launch_index_fp4(const IndexParams& p, const CUtensorMap& tm_q, int grid,
+// MXFP4 keys: tm_kc views the codes as uint8 [idx_total, 64] in boxes of
+// 128 rows and tm_kc8 in boxes of 8 rows (pool blocks), both with the
+// 64-byte swizzle; tm_kc2 views them as [ceil(idx_total / 2), 128] (two keys
+// per row) in boxes of 128 rows with the 128-byte swizzle.  qpg is 1
+// (decode, pool mode) or 4 (prefill).  Decode tiles (no pool) are 256 keys
+// starting at an even key row: a sequence at key row off has
+// ceil((n + off % 2) / 256) tiles.
+int index_fp4_smem_bytes();
+cudaError_t launch_index_fp4(const IndexParams& p, const CUtensorMap& tm_kc,
+                             const CUtensorMap& tm_kc2, const CUtensorMap& tm_kc8, int grid,
                              cudaStream_t s);
 
 // ---------------------------------------------------------------- HSI

@@ -1,29 +1,45 @@
-// k_index_fp4.cu -- CSA2 indexer scores over MXFP4 indexer keys and queries.
+// k_index_fp4.cu -- CSA2 indexer scores over MXFP4 indexer keys and queries,
+// on the block-scaled tensor-core MMA.
 //
 // The V4.1 report (section 2.4.4) keeps the indexer's queries and keys in
 // OCP MXFP4: E2M1 codes with one power-of-two (UE8M0) scale per 32
 // channels, 64 + 4 bytes per 128-channel key (the 68 B of the cache-size
 // breakdown).  The score is the one of the bf16 indexer,
 //     I[q, s] = sum_h w[q, h] * ReLU(q^[q, h] . K^[s]),
-// over the dequantised values q^, K^.  An E2M1 value times a scale 2^e is
-// exactly an E5M2 value for e in [-13, 13], so both operands become E5M2
-// bytes (a byte permute per four codes through a per-block table) and the
-// tensor cores take them as kind::f8f6f4 with fp32 accumulation: the same
-// products as the dequantised values, one byte per channel in shared
-// memory.  A block scale outside that range (values below 2^-14 or above
-// 2^16) is clamped into it and reported in the device error word.
+// over the dequantised values q^, K^.  tcgen05.mma.kind::mxf4.block_scale
+// takes exactly these operands: E2M1 codes from shared memory (two per
+// byte) and one UE8M0 scale per 32 elements of K from tensor memory, with
+// fp32 accumulation, so the cached codes go to the tensor cores as they are.
 //
-// Warp roles (576 threads):
-//   warp 0      bulk-copies the raw tiles (128 keys: 8 KB of codes and their
-//               scale words) into a ring 12 deep in decode (4 in prefill,
-//               whose 8-query tiles need the room), and the query tile (TMA);
-//   warps 10-17 convert each raw tile into a 128B-swizzled E5M2 K-major
-//               stage, and at every new query group take the query tile
-//               (bf16) to the MXFP4 grid and on to E5M2;
-//   warp 1      issues the tcgen05 MMAs (M = 128 keys, N = 32 heads x qpg,
-//               K = 128 as 4 x 32) from the converted stage and queries;
-//   warps 2-9   the epilogue of the bf16 indexer (ReLU, head weights, fp32
-//               or bf16 score store, score-key histogram).
+// Operands of one MMA (M = 128 keys, N = 32 heads x qpg, K = 64):
+//   A  key codes, K-major: with one query per group, rows of two keys
+//      (128 bytes, the 128-byte swizzle, one TMA box of 256 keys; the even
+//      keys at bytes 0-63 of each row, the odd keys at 64-127, so the TMA
+//      moves 128-byte rows); otherwise 64-byte rows of one key with the
+//      64-byte swizzle (a box of 128 keys, or in pool mode one box per block
+//      of 8 keys, exactly one 512-byte swizzle atom); two K steps of 32 bytes
+//      cover the 128 channels;
+//   B  query codes in the same layout, written by the query-preparation
+//      warps (each query head rounded to the MXFP4 grid);
+//   SFA / SFB  scale bytes in tensor memory: a 512-byte atom per 128 rows in
+//      which row 32 q + r holds its four block scales at byte 16 r + 4 q
+//      (tcgen05.cp 32x128b.warpx4 puts 32 lanes x 16 bytes into every lane
+//      quadrant; the MMA reads quadrant q's lanes at column q), the K step
+//      choosing the byte pair (scale id 0 or 2).
+//
+// Warp roles (384 threads):
+//   warp 0      producer: the key-code TMA boxes of each tile and its scale
+//               atoms (scale words loaded into registers four tiles ahead,
+//               stored transposed into the atom layout);
+//   warp 1      MMA issuer (and TMEM owner): per tile the scale-atom copies
+//               into tensor memory, then the MMAs, one accumulator per tile;
+//   warps 2-9   epilogue: ReLU, head weights, fp32 or bf16 score store,
+//               score-key histogram (the bf16 indexer's);
+//   warps 10-11 query preparation: at every new query group the bf16 query
+//               heads are rounded to MXFP4 codes and scales into one of two
+//               B slots, ahead of the MMAs of that group.
+// Tiles: 256 keys (two M = 128 groups) for one query per group (decode and
+// pool mode), 128 keys for four queries per group (prefill, N = 128).
 // Every wait is bounded.
 #include "csa2_device.cuh"
 #include "csa2_kernels.h"
@@ -31,41 +47,51 @@
 namespace csa2 {
 namespace {
 
-// A tile is 256 keys in decode (two M = 128 MMA groups: the per-tile cost of
-// the warp hand-offs, a fixed ~0.3 us, is then spread over twice the keys)
-// and 128 keys in prefill (8 queries per tile already give N = 256).
-constexpr int kTileMax = 256;
-constexpr int kRawStagesMax = 5;
-constexpr int kStagesMax = 3;                           // converted E5M2 stages
-constexpr int kKStageBytes = kTileMax * kIdxDim;        // 32 KB
-constexpr int kRawCodeBytes = kTileMax * kIdxDim / 2;   // 16 KB
-constexpr int kRawScaleBytes = 1056;                    // (256 + 4) words, 16-byte padded
-constexpr int kRawStageBytes = kRawCodeBytes + kRawScaleBytes;
-constexpr int kThreads = 576;
+constexpr int kThreads = 384;
 constexpr int kEpiThreads = 256;   // warps 2-9
-constexpr int kCvtThreads = 256;   // warps 10-17
-constexpr int kCvtBase = 320;
-constexpr int kCvtWarps = kCvtThreads / 32;
 constexpr int kEpiWarps = kEpiThreads / 32;
+constexpr int kPrepBase = 320;     // warps 10-11
+constexpr int kPrepThreads = 64;
+constexpr int kPrepWarps = kPrepThreads / 32;
+#ifndef CSA2_FP4_STAGES
+#define CSA2_FP4_STAGES 8
+#endif
+#ifndef CSA2_FP4_NACC
+#define CSA2_FP4_NACC 4
+#endif
+constexpr int kStages = CSA2_FP4_STAGES;
+constexpr int kTileMax = 256;
+constexpr int kCodeStage = kTileMax * (kIdxDim / 2);   // 16 KB of E2M1 codes
+constexpr int kSfAtom = 512;                           // scales of 128 rows
+constexpr int kStageBytes = kCodeStage + (kTileMax / 128) * kSfAtom;   // 17 KB
+constexpr int kMaxQpg = 4;
+constexpr int kBRows = 32 * kMaxQpg;
+constexpr int kBSlotBytes = 9216;    // 8 KB of query codes + one scale atom (1024-aligned)
+constexpr int kPf = 4;               // tiles of scale words loaded ahead by the producer
+constexpr int kNAcc = CSA2_FP4_NACC;   // accumulators of one query's tiles (64 columns each)
+// tensor-memory columns: accumulators, then the key scales of each
+// accumulator's tile, then the query scales of the two B slots
+constexpr uint32_t kAccCols = 384;     // the accumulators fit below this column
+constexpr uint32_t kSfaCol = kAccCols;           // [kNAcc][2 M-groups][4 columns]
+constexpr uint32_t kSfbCol = kSfaCol + 8 * kNAcc;  // [2 B slots][4 columns]
+constexpr uint32_t kTmemCols = 512;
+static_assert(kNAcc * 64 <= (int)kAccCols && kSfbCol + 8 <= kTmemCols, "tensor memory");
 
-__host__ __device__ inline int raw_stages(int qpg) { return qpg == 1 ? kRawStagesMax : 2; }
-__host__ __device__ inline int k_stages(int qpg) { return qpg == 1 ? kStagesMax : 2; }
-__host__ __device__ inline int tile_rows_of(int qpg) { return qpg == 1 ? 256 : 128; }
+constexpr int kMaxPoolIds = 4096;    // block ids of one query's pool (pool mode)
 
 struct SmemLayout {
-  int raw_off, q_off, q8_off, w_off, hist_off, bar_off, total;
+  int b_off, w_off, hist_off, ids_off, bar_off, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int qpg) {
+__host__ __device__ inline SmemLayout smem_layout() {
   SmemLayout L;
-  L.raw_off = k_stages(qpg) * kKStageBytes;
-  L.q_off = L.raw_off + raw_stages(qpg) * kRawStageBytes;
-  L.q_off = (L.q_off + 1023) & ~1023;
-  L.q8_off = L.q_off + qpg * 32 * kIdxDim * 2;          // E5M2 queries (1024-aligned)
-  L.w_off = L.q8_off + qpg * 32 * kIdxDim;
-  L.hist_off = L.w_off + qpg * 32 * 4;
-  L.bar_off = L.hist_off + kKeyHistBins * 4;
-  L.total = L.bar_off + 48 * 8 + 16 + 1024;  // barriers, tmem slot, alignment slack
+  L.b_off = kStages * kStageBytes;
+  L.w_off = L.b_off + 2 * kBSlotBytes;
+  L.hist_off = L.w_off + kBRows * 4;
+  L.ids_off = L.hist_off + kKeyHistBins * 4;
+  L.bar_off = L.ids_off + kMaxPoolIds * 4;
+  L.total = L.bar_off + 56 * 8 + 16 + 1024;   // barriers, tmem slot, alignment slack
+  static_assert(kStages <= 16 && kNAcc <= 8, "barrier slots");
   return L;
 }
 
@@ -80,136 +106,193 @@ __device__ __forceinline__ int64_t group_base(const IndexParams& p, int g) {
   return p.prefill ? p.pre_base : p.entry_base[g];
 }
 
-// First key row of item `it` in group g, the keys it copies (the cache ends
-// at p.idx_total rows) and the first row of its 16-byte aligned scale window.
-struct TileRows {
-  int64_t row0, s0;
-  int32_t nrows;
-};
-__device__ __forceinline__ TileRows tile_rows(const IndexParams& p, int g, int t, int tile_e) {
-  TileRows r;
-  r.row0 = group_base(p, g) + (int64_t)t * tile_e;
-  const int64_t left = p.idx_total - r.row0;
-  r.nrows = (int32_t)(left < tile_e ? left : tile_e);
-  r.s0 = r.row0 & ~(int64_t)3;
-  return r;
-}
-
-// E5M2 exponent offset of a UE8M0 byte, clamped to [-13, 13] (flagged).
-__device__ __forceinline__ int block_exp(uint32_t ue8m0, bool nonzero, uint32_t* err) {
-  int e = (int)ue8m0 - 127;
-  if (nonzero && (e < -13 || e > 13)) {
-    set_error(err, kErrRange);
-    e = e < -13 ? -13 : 13;
+// Walks the tile list; group g holds tiles [lo, hi) and its keys start at
+// row `base`.  The parameter tables are read only when the group changes: a
+// dynamically indexed kernel parameter is read through the constant cache,
+// and a miss there on every tile costs hundreds of cycles.
+struct Cursor {
+  int g, lo, hi;
+  int64_t base;
+  __device__ __forceinline__ void init(const IndexParams& p, int g0) {
+    g = g0;
+    lo = p.tile_prefix[g0];
+    hi = p.tile_prefix[g0 + 1];
+    base = group_base(p, g0);
   }
-  return e;
+  __device__ __forceinline__ bool advance(const IndexParams& p, int it) {
+    if (it < hi) return false;
+    do {
+      ++g;
+      lo = hi;
+      hi = p.tile_prefix[g + 1];
+    } while (hi <= it);
+    base = group_base(p, g);
+    return true;
+  }
+};
+
+// Shared-memory descriptor of a K-major operand in 64-byte rows with the
+// 64-byte swizzle: 8-row atoms of 512 bytes, one after the other.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;                      // leading byte offset 16 (unused)
+  d |= (uint64_t)(512u >> 4) << 32;            // 8-row groups 512 bytes apart
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;                      // SWIZZLE_64B
+  return d;
 }
 
-// Block b (32 channels) of query row r: bf16 in the 128B-swizzled two-half
-// tile -> MXFP4 (UE8M0 scale of the block's largest magnitude, OCP MX;
-// E2M1 code of x / scale, nearest, ties to even, saturating) -> E5M2 bytes
-// in the 128B-swizzled one-row-per-128-bytes tile q8.
-__device__ __forceinline__ void query_block_to_e5m2(const uint8_t* qbuf, uint8_t* q8, int qrows,
-                                                    int r, int b, uint32_t* err) {
-  const uint8_t* half = qbuf + (b >> 1) * (qrows * 128) + r * 128;
+// Descriptor of a scale atom (32 rows of 16 bytes, no swizzle) for
+// tcgen05.cp 32x128b.
+__device__ __forceinline__ uint64_t sdesc_atom(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(128u >> 4) << 16;
+  d |= (uint64_t)(128u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// 4-byte asynchronous copy global -> shared (src_bytes 0: the word is
+// zero-filled and nothing is read), and an arrival on `bar` once every such
+// copy of this thread has landed (the barrier's count includes it).
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// Instruction descriptor of kind::mxf4 (E2M1 x E2M1, UE8M0 scales, fp32 D,
+// K-major A and B); `sf` (0 or 2) picks the scale byte pair of the K step.
+__device__ __forceinline__ uint32_t idesc_mxf4(uint32_t N, uint32_t sf) {
+  return (sf << 4)               // scale id of B
+         | (1u << 7)             // A = E2M1
+         | (1u << 10)            // B = E2M1
+         | ((N >> 3) << 17)
+         | (1u << 23)            // scale format UE8M0
+         | ((128u >> 4) << 24)   // M = 128
+         | (sf << 29);           // scale id of A
+}
+
+__device__ __forceinline__ void umma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+// Block b (32 channels) of query head row n: bf16 from global memory ->
+// MXFP4 (UE8M0 scale of the block's largest magnitude, OCP MX rule; E2M1
+// code of x / scale, nearest, ties to even, saturating) -> 16 code bytes in
+// the B slot's swizzled row and the scale byte in its atom.
+__device__ __forceinline__ void prep_query_block(const uint16_t* src, bool live, uint8_t* bcodes,
+                                                 uint8_t* batom, int n, int b) {
   float x[32];
+  if (live) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int chunk = (b & 1) * 4 + k;
-    const uint4 w = *reinterpret_cast<const uint4*>(half + ((chunk ^ (r & 7)) << 4));
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+    for (int k = 0; k < 4; ++k) {
+      const uint4 v = __ldg(s4 + k);
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x[8 * k + 2 * i] = __uint_as_float(u[i] << 16);
-      x[8 * k + 2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+      for (int i = 0; i < 4; ++i) {
+        x[8 * k + 2 * i] = __uint_as_float(u[i] << 16);
+        x[8 * k + 2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+      }
     }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] = 0.0f;
   }
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
   const uint32_t sb = ue8m0_for_amax(amax);
   const float sc = ue8m0_value(sb);
-  uint32_t codes[4];
-  uint32_t any = 0;
+  uint32_t c[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    uint32_t c = 0;
+    uint32_t w = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) c |= e2m1_encode(__fdiv_rn(x[8 * k + i], sc)) << (4 * i);
-    codes[k] = c;
-    any |= c & 0x77777777u;
+    for (int i = 0; i < 8; ++i) w |= e2m1_encode(__fdiv_rn(x[8 * k + i], sc)) << (4 * i);
+    c[k] = w;
   }
-  uint32_t tlo, thi;
-  e5m2_table(block_exp(sb, any != 0, err), tlo, thi);
-  uint32_t o[8];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) e2m1x8_to_e5m2x8(codes[k], tlo, thi, o[2 * k], o[2 * k + 1]);
-  uint8_t* row = q8 + r * 128;
-  *reinterpret_cast<uint4*>(row + (((2 * b) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-  *reinterpret_cast<uint4*>(row + (((2 * b + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+  uint8_t* row = bcodes + (n >> 3) * 512 + (n & 7) * 64;
+  *reinterpret_cast<uint4*>(row + ((b ^ ((n >> 1) & 3)) << 4)) = make_uint4(c[0], c[1], c[2], c[3]);
+  batom[(n & 31) * 16 + ((n >> 5) & 3) * 4 + b] = (uint8_t)sb;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    k_index_fp4(const __grid_constant__ IndexParams p, const __grid_constant__ CUtensorMap tm_q) {
+    k_index_fp4(const __grid_constant__ IndexParams p, const __grid_constant__ CUtensorMap tm_kc,
+                const __grid_constant__ CUtensorMap tm_kc2, const __grid_constant__ CUtensorMap tm_kc8) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  const SmemLayout L = smem_layout(p.qpg);
-  uint8_t* kbuf = smem;
-  uint8_t* raw = smem + L.raw_off;
-  uint8_t* qbuf = smem + L.q_off;
-  uint8_t* q8 = smem + L.q8_off;
+  const SmemLayout L = smem_layout();
+  uint8_t* stages = smem;
+  uint8_t* bslots = smem + L.b_off;
   float* wbuf = reinterpret_cast<float*>(smem + L.w_off);
-  uint32_t* hs = reinterpret_cast<uint32_t*>(smem + L.hist_off);  // score-key histogram
+  uint32_t* hs = reinterpret_cast<uint32_t*>(smem + L.hist_off);
+  int32_t* ids_s = reinterpret_cast<int32_t*>(smem + L.ids_off);   // pool ids of the group
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
-  uint64_t* raw_full = bars;            // [kRawStagesMax]
-  uint64_t* raw_empty = bars + 12;      // [kRawStagesMax]
-  uint64_t* k_full = bars + 24;         // [kStagesMax]
-  uint64_t* k_empty = bars + 28;        // [kStagesMax]
-  uint64_t* acc_full = bars + 32;       // [nacc <= 4]
-  uint64_t* acc_empty = bars + 36;      // [nacc <= 4]
-  uint64_t* q_full = bars + 40;
-  uint64_t* q_ready = bars + 41;
-  uint64_t* q_empty = bars + 42;
-  uint64_t* drain = bars + 43;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 44);
+  uint64_t* k_full = bars;                 // [kStages]
+  uint64_t* k_empty = bars + 16;           // [kStages]
+  uint64_t* acc_full = bars + 32;          // [kNAcc]
+  uint64_t* acc_empty = bars + 40;         // [kNAcc]
+  uint64_t* b_full = bars + 48;            // [2]
+  uint64_t* b_empty = bars + 50;           // [2]
+  uint64_t* drain = bars + 52;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 54);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int N = 32 * p.qpg;               // MMA N (columns per accumulator)
-  const int qrows = 32 * p.qpg;
-  // decode (one query per group): 256-key tiles as two M-groups whose
-  // accumulators sit side by side (2 x 32 columns), 4 accumulators, each
-  // epilogue half takes one M-group; prefill: 128-key tiles, 2 accumulators
-  // of 256 columns, the halves split the 8 queries of every tile
-  const bool two_groups = p.qpg == 1;
-  const int tile_e = tile_rows_of(p.qpg);
+  const int N = 32 * p.qpg;                      // MMA N
+  const int tile_e = p.qpg == 1 ? 256 : 128;     // keys per tile
   const int mgroups = tile_e / 128;
-  const int nacc = two_groups ? 4 : 2;
-  const int acc_cols = mgroups * N;
-  const uint32_t tmem_cols = (uint32_t)(nacc * acc_cols) < 32u ? 32u : (uint32_t)(nacc * acc_cols);
-  const int n_raw = raw_stages(p.qpg);
-  const int n_k = k_stages(p.qpg);
+  const int acc_cols = mgroups * N;              // 64 (one query) or 128 (four)
+  const int nacc = acc_cols == 64 ? kNAcc : 2;   // accumulators below kAccCols
+  const bool pool = p.pool != nullptr;
+  const int blocks_per_tile = tile_e / 8;
+  // One query per group over contiguous keys: a tile is 256 keys read as 128
+  // rows of two keys (128 bytes, the 128-byte swizzle), half the TMA rows of
+  // one key per row; M-group 0 takes the even keys of the rows (bytes 0-63),
+  // M-group 1 the odd ones (bytes 64-127).  Such tiles start at an even key
+  // row, so a sequence whose first key row is odd starts one row early
+  // (`shift`, masked).
+  const bool pairs = p.qpg == 1 && !pool;
+  // key of slot sl (M-group sl / 128, TMEM lane sl % 128) relative to the
+  // tile's first key row
+  auto slot_key = [&](int sl) -> int { return pairs ? 2 * (sl & 127) + (sl >> 7) : sl; };
+  auto tile_row0 = [&](const Cursor& c, int it) -> int64_t {
+    return (pairs ? (c.base & ~(int64_t)1) : c.base) + (int64_t)(it - c.lo) * tile_e;
+  };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < n_raw; ++i) {
-      mbar_init(raw_full + i, 1);
-      mbar_init(raw_empty + i, kCvtWarps);
-    }
-    // consumer barriers count warps: each warp arrives once, from lane 0,
-    // after a __syncwarp over its lanes' work
-    for (int i = 0; i < n_k; ++i) { mbar_init(k_full + i, kCvtWarps); mbar_init(k_empty + i, 1); }
-    for (int i = 0; i < nacc; ++i) {
-      mbar_init(acc_full + i, 1);
-      mbar_init(acc_empty + i, kEpiWarps);
-    }
-    mbar_init(q_full, 1);
-    mbar_init(q_ready, kCvtWarps);
-    mbar_init(q_empty, 1);
+    // k_full: the code copies' transaction bytes with lane 0's arrival, plus
+    // one arrival per producer lane once its scale copies have landed
+    for (int i = 0; i < kStages; ++i) { mbar_init(k_full + i, 33); mbar_init(k_empty + i, 1); }
+    for (int i = 0; i < kNAcc; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, kEpiWarps); }
+    for (int i = 0; i < 2; ++i) { mbar_init(b_full + i, kPrepWarps); mbar_init(b_empty + i, 1); }
     mbar_init(drain, 1);
     fence_barrier_init();
-    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kc);
+    tma_prefetch_desc(&tm_kc2);
+    tma_prefetch_desc(&tm_kc8);
   }
-  if (warp == 1) { tmem_alloc(tmem_slot, tmem_cols); tmem_relinquish(); }
+  if (warp == 1) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -221,199 +304,266 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int end = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
   int g0 = 0;
   while (g0 < p.n_groups && p.tile_prefix[g0 + 1] <= begin) ++g0;
+  Cursor c0;
+  c0.init(p, g0);
+  // pool row of tile `it` (its group at or after the cursor's): block ids
+  auto pool_row = [&](int it, Cursor c) -> const int32_t* {
+    c.advance(p, it);
+    return p.pool + (int64_t)c.g * p.pool_blocks + (int64_t)(it - c.lo) * blocks_per_tile;
+  };
+  auto pool_len = [&](int it, Cursor c) -> int {   // valid blocks in tile `it`
+    c.advance(p, it);
+    const int left = p.pool_blocks - (it - c.lo) * blocks_per_tile;
+    return left < blocks_per_tile ? left : blocks_per_tile;
+  };
 
-  if (warp == 0 && lane == 0 && begin < end) {
-    // ------------------------------------------------ bulk-copy producer
-    int g = g0, cur = -1, rs = 0;
-    uint32_t rph = 0, qph = 0;
-    uint32_t armed = 0, armed_ph = 0;   // raw stages filled at least once, parity of the last fill
-    bool ok = true;
+  if (warp == 0 && begin < end) {
+    // ------------------------------------------------ producer
+    // Per tile: the key codes by TMA (one box per M-group, or per block of 8
+    // keys in pool mode) and each key's scale word by a 4-byte asynchronous
+    // copy straight into its place in the scale atom (lane r copies rows
+    // 32 q + r), completing on the stage's barrier: the warp never waits for
+    // a load.  In pool mode the block ids are loaded kPf tiles ahead, slot u
+    // of the ring holding the tiles it = u (mod kPf), the loop unrolled over
+    // the slots so that no register of a load in flight is ever copied.
+    const uint32_t* sw = reinterpret_cast<const uint32_t*>(p.idx_scales);   // one word per key
     const uint64_t keys_pol = l2_policy_evict_first();
-    for (int it = begin; it < end && ok; ++it) {
-      while (p.tile_prefix[g + 1] <= it) ++g;
-      if (g != cur) {
-        ok = mbar_wait(q_empty, qph ^ 1, p.err);
-        qph ^= 1;
+    int32_t pq[kPf];     // pool mode: this lane's block id of tiles it .. it + kPf - 1
+    Cursor pc_id = c0;
+    auto load_ids = [&](int j) -> int32_t {
+      if (!pool || j >= end) return -1;
+      pc_id.advance(p, j);
+      if (lane >= pool_len(j, pc_id)) return -1;
+      return __ldg(pool_row(j, pc_id) + lane);
+    };
+#pragma unroll
+    for (int u = 0; u < kPf; ++u) pq[u] = load_ids(begin + u);
+
+    Cursor gc = c0;
+    int stage = 0;
+    uint32_t ph = 0;
+    uint32_t armed = 0, armed_ph = 0;   // stages filled at least once, parity of the last fill
+    bool ok = true;
+    for (int it0 = begin; it0 < end && ok; it0 += kPf) {
+#pragma unroll
+      for (int u = 0; u < kPf; ++u) {
+        const int it = it0 + u;
+        if (it >= end || !ok) break;
+        gc.advance(p, it);
+        if (lane == 0) ok = mbar_wait(k_empty + stage, ph ^ 1, p.err);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        mbar_arrive_expect_tx(q_full, (uint32_t)(qrows * kIdxDim * 2));
-        tma_load_2d(qbuf, &tm_q, 0, g * qrows, q_full);
-        tma_load_2d(qbuf + qrows * 128, &tm_q, 64, g * qrows, q_full);
-        cur = g;
+        uint8_t* st = stages + stage * kStageBytes;
+        const int64_t base = gc.base;
+        const int32_t blk_lane = pq[u];
+        // scale words into the atoms: row 32 q + r of M-group mg at byte
+        // 16 r + 4 q of that group's atom
+#pragma unroll
+        for (int mg = 0; mg < 2; ++mg) {
+          if (mg >= mgroups) break;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int sl = mg * 128 + 32 * q + lane;     // key slot of the tile
+            int64_t row;
+            if (pool) {
+              const int32_t blk = __shfl_sync(0xffffffffu, blk_lane, sl >> 3);
+              row = blk >= 0 ? base + (int64_t)blk * 8 + (sl & 7) : -1;
+            } else {
+              row = tile_row0(gc, it) + slot_key(sl);
+            }
+            const bool live = row >= 0 && row < p.idx_total;
+            cp_async4(st + kCodeStage + mg * kSfAtom + lane * 16 + q * 4, sw + (live ? row : 0),
+                      live ? 4u : 0u);
+          }
+        }
+        cp_async_arrive_noinc(k_full + stage);
+        if (pool) {
+          const uint32_t n_ok = (uint32_t)__popc(__ballot_sync(0xffffffffu, blk_lane >= 0));
+          if (lane == 0) mbar_arrive_expect_tx(k_full + stage, n_ok * 512u);
+          __syncwarp();
+          if (blk_lane >= 0)
+            tma_load_2d(st + lane * 512, &tm_kc8, 0, (int32_t)(base + (int64_t)blk_lane * 8),
+                        k_full + stage, keys_pol);
+        } else if (lane == 0) {
+          const int64_t row0 = tile_row0(gc, it);
+          mbar_arrive_expect_tx(k_full + stage, (uint32_t)(mgroups * 128 * (kIdxDim / 2)));
+          if (pairs) {
+            tma_load_2d(st, &tm_kc2, 0, (int32_t)(row0 >> 1), k_full + stage, keys_pol);
+          } else {
+            for (int mg = 0; mg < mgroups; ++mg)
+              tma_load_2d(st + mg * 128 * (kIdxDim / 2), &tm_kc, 0, (int32_t)(row0 + mg * 128),
+                          k_full + stage, keys_pol);
+          }
+        }
+        armed |= 1u << stage;
+        armed_ph = (armed_ph & ~(1u << stage)) | (ph << stage);
+        if (++stage == kStages) { stage = 0; ph ^= 1; }
+        pq[u] = load_ids(it + kPf);
       }
-      ok = mbar_wait(raw_empty + rs, rph ^ 1, p.err);
-      if (!ok) break;
-      const TileRows tr = tile_rows(p, g, it - p.tile_prefix[g], tile_e);
-      const int64_t s1 = (tr.row0 + tr.nrows + 3) & ~(int64_t)3;
-      const uint32_t code_bytes = (uint32_t)tr.nrows * (kIdxDim / 2);
-      const uint32_t scale_bytes = (uint32_t)(s1 - tr.s0) * 4u;
-      uint8_t* dst = raw + rs * kRawStageBytes;
-      mbar_arrive_expect_tx(raw_full + rs, code_bytes + scale_bytes);
-      bulk_load(dst, p.idx_codes + tr.row0 * (kIdxDim / 2), code_bytes, raw_full + rs, keys_pol);
-      bulk_load(dst + kRawCodeBytes, p.idx_scales + tr.s0 * 4, scale_bytes, raw_full + rs,
-                keys_pol);
-      armed |= 1u << rs;
-      armed_ph = (armed_ph & ~(1u << rs)) | (rph << rs);
-      if (++rs == n_raw) { rs = 0; rph ^= 1; }
     }
-    // make sure no bulk copy is still writing into this CTA's shared memory
-    for (int s = 0; s < n_raw; ++s)
-      if (armed & (1u << s)) mbar_wait(raw_full + s, (armed_ph >> s) & 1u, p.err);
-    if (cur >= 0) mbar_wait(q_full, qph ^ 1, p.err);
-  } else if (warp >= 10 && begin < end) {
-    // ------------------------------------------------ converters
-    const int ct = threadIdx.x - kCvtBase;          // 0..255
-    const int cw = ct >> 5;                         // converter warp 0..7
-    const int b = ct & 3;                           // 32-channel block of the key
-    int g = g0, cur = -1, rs = 0, ks = 0;
-    uint32_t rph = 0, kph = 0, qph = 0;
+    // no bulk copy may still be writing into this CTA's shared memory
+    if (lane == 0) {
+      for (int s = 0; s < kStages; ++s)
+        if (armed & (1u << s)) mbar_wait(k_full + s, (armed_ph >> s) & 1u, p.err);
+    }
+    __syncwarp();
+  } else if (warp >= kPrepBase / 32 && begin < end) {
+    // ------------------------------------------------ query preparation
+    const int pt = threadIdx.x - kPrepBase;
+    const int qrows = 32 * p.qpg;
+    Cursor gc = c0;
+    int cur = -1, gi = 0;
     bool ok = true;
     for (int it = begin; it < end && ok; ++it) {
-      while (p.tile_prefix[g + 1] <= it) ++g;
-      if (g != cur) {
-        // a new query tile: onto the MXFP4 grid before its first MMA
-        ok = mbar_wait(q_full, qph, p.err);
-        qph ^= 1;
-        if (!ok) break;
-        for (int i = ct; i < qrows * 4; i += kCvtThreads)
-          query_block_to_e5m2(qbuf, q8, qrows, i >> 2, i & 3, p.err);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(q_ready);
-        cur = g;
-      }
-      ok = mbar_wait(raw_full + rs, rph, p.err) && mbar_wait(k_empty + ks, kph ^ 1, p.err);
+      gc.advance(p, it);
+      if (gc.g == cur) continue;
+      cur = gc.g;
+      const int slot = gi & 1;
+      ok = mbar_wait_sleep(b_empty + slot, (uint32_t)(((gi >> 1) & 1) ^ 1), p.err);
       if (!ok) break;
-      const int t = it - p.tile_prefix[g];
-      const TileRows tr = tile_rows(p, g, t, tile_e);
-      // rows holding appended keys (the rest of the copy is unused capacity
-      // or the next sequence: converted as zeros, never range-checked)
-      const int32_t len = p.prefill ? p.pre_len : p.nvis[g];
-      const int32_t live = min(tr.nrows, len - t * tile_e);
-      const uint8_t* src = raw + rs * kRawStageBytes;
-      const uint32_t* sw = reinterpret_cast<const uint32_t*>(src + kRawCodeBytes) + (tr.row0 - tr.s0);
-      uint8_t* dst = kbuf + ks * kKStageBytes;
-#pragma unroll 1
-      for (int pass = 0; pass < tile_e / 64; ++pass) {
-        const int r = pass * 64 + cw * 8 + (lane >> 2);   // key row of the tile
-        uint4 c4 = make_uint4(0u, 0u, 0u, 0u);
-        uint32_t sb = 127u;
-        if (r < live) {
-          c4 = *reinterpret_cast<const uint4*>(src + r * (kIdxDim / 2) + b * 16);
-          sb = (sw[r] >> (8 * b)) & 0xFFu;
-        }
-        const uint32_t any = (c4.x | c4.y | c4.z | c4.w) & 0x77777777u;
-        uint32_t tlo, thi;
-        e5m2_table(block_exp(sb, any != 0, p.err), tlo, thi);
-        uint32_t o[8];
-        e2m1x8_to_e5m2x8(c4.x, tlo, thi, o[0], o[1]);
-        e2m1x8_to_e5m2x8(c4.y, tlo, thi, o[2], o[3]);
-        e2m1x8_to_e5m2x8(c4.z, tlo, thi, o[4], o[5]);
-        e2m1x8_to_e5m2x8(c4.w, tlo, thi, o[6], o[7]);
-        uint8_t* rowp = dst + r * 128;
-        *reinterpret_cast<uint4*>(rowp + (((2 * b) ^ (r & 7)) << 4)) =
-            make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(rowp + (((2 * b + 1) ^ (r & 7)) << 4)) =
-            make_uint4(o[4], o[5], o[6], o[7]);
+      uint8_t* bc = bslots + slot * kBSlotBytes;
+      uint8_t* ba = bc + kBRows * (kIdxDim / 2);
+      for (int i = pt; i < kSfAtom / 4; i += kPrepThreads) reinterpret_cast<uint32_t*>(ba)[i] = 0u;
+      asm volatile("bar.sync 2, 64;" ::: "memory");   // both warps: zeroed before any scale byte
+      for (int item = pt; item < qrows * 4; item += kPrepThreads) {
+        const int n = item >> 2, b = item & 3;
+        const int q = cur * p.qpg + (n >> 5);
+        const bool live = q < p.nq;
+        const uint16_t* src = p.q_idx + ((int64_t)q * kIdxHeads + (n & 31)) * kIdxDim + b * 32;
+        prep_query_block(src, live, bc, ba, n, b);
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(k_full + ks);
-        mbar_arrive(raw_empty + rs);
-      }
-      if (++rs == n_raw) { rs = 0; rph ^= 1; }
-      if (++ks == n_k) { ks = 0; kph ^= 1; }
+      if (lane == 0) mbar_arrive(b_full + slot);
+      ++gi;
     }
   } else if (warp == 1 && lane == 0 && begin < end) {
     // ------------------------------------------------ MMA issuer
-    // the f16-kind descriptor: format fields 1 / 1 read as E5M2 / E5M2 here
-    const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)N, false, false);
-    int g = g0, cur = -1, stage = 0, acc = 0;
-    uint32_t ph = 0, qph = 0, aph = 0;
+    Cursor gc = c0;
+    int cur = -1, gi = -1, stage = 0, acc = 0;
+    uint32_t ph = 0, aph = 0;
     bool ok = true;
     for (int it = begin; it < end && ok; ++it) {
-      while (p.tile_prefix[g + 1] <= it) ++g;
-      if (g != cur) {
-        ok = mbar_wait(q_ready, qph, p.err);
-        qph ^= 1;
+      const bool changed = gc.advance(p, it) || cur < 0;
+      if (changed) {
+        ++gi;
+        cur = gc.g;
+        ok = mbar_wait(b_full + (gi & 1), (uint32_t)((gi >> 1) & 1), p.err);
         if (!ok) break;
-        cur = g;
+        tc_fence_after();
+        uint8_t* ba = bslots + (gi & 1) * kBSlotBytes + kBRows * (kIdxDim / 2);
+        tmem_cp_atom(tmem_base + kSfbCol + 4 * (gi & 1), sdesc_atom(smem_u32(ba)));
       }
       ok = mbar_wait(k_full + stage, ph, p.err) && mbar_wait(acc_empty + acc, aph ^ 1, p.err);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t b0 = smem_u32(q8);
-      // one 128-byte swizzled row holds all 128 channels: K steps of 32 bytes
+      // the scale words arrived by generic-proxy copies; tcgen05.cp reads
+      // them through the async proxy
+      fence_proxy_async_smem();
+      uint8_t* st = stages + stage * kStageBytes;
+      const uint32_t sfa = tmem_base + kSfaCol + (uint32_t)(acc * 8);
+      for (int mg = 0; mg < mgroups; ++mg)
+        tmem_cp_atom(sfa + 4 * mg, sdesc_atom(smem_u32(st + kCodeStage + mg * kSfAtom)));
+      const uint32_t b0 = smem_u32(bslots + (gi & 1) * kBSlotBytes);
+      const uint32_t sfb = tmem_base + kSfbCol + 4 * (gi & 1);
       for (int mg = 0; mg < mgroups; ++mg) {
-        const uint32_t a0 = smem_u32(kbuf + stage * kKStageBytes + mg * 128 * 128);
         const uint32_t d = tmem_base + (uint32_t)(acc * acc_cols + mg * N);
 #pragma unroll
-        for (int ks = 0; ks < kIdxDim / 32; ++ks)
-          umma_e5m2(d, sdesc_sw128(a0 + ks * 32, 16, 1024), sdesc_sw128(b0 + ks * 32, 16, 1024),
-                    idesc, ks > 0 ? 1u : 0u);
+        for (int ks = 0; ks < 2; ++ks) {
+          // key rows: pairs -> the even / odd half of the 128-byte rows
+          const uint64_t ad =
+              pairs ? sdesc_sw128(smem_u32(st) + 64 * mg + 32 * ks, 16, 1024)
+                    : sdesc_sw64(smem_u32(st + mg * 128 * (kIdxDim / 2)) + 32 * ks);
+          umma_mxf4(d, ad, sdesc_sw64(b0 + 32 * ks), idesc_mxf4((uint32_t)N, 2u * ks),
+                    sfa + 4 * mg, sfb, ks > 0 ? 1u : 0u);
+        }
       }
       umma_commit(k_empty + stage);
       umma_commit(acc_full + acc);
-      const bool last_of_group = (it + 1 == end) || (p.tile_prefix[g + 1] <= it + 1);
-      if (last_of_group) umma_commit(q_empty);
-      if (++stage == n_k) { stage = 0; ph ^= 1; }
+      const bool last_of_group = (it + 1 == end) || (gc.hi <= it + 1);
+      if (last_of_group) umma_commit(b_empty + (gi & 1));
+      if (++stage == kStages) { stage = 0; ph ^= 1; }
       if (++acc == nacc) { acc = 0; aph ^= 1; }
     }
     umma_commit(drain);
     mbar_wait(drain, 0, p.err);
   } else if (warp >= 2 && warp < 10) {
     // ------------------------------------------------ epilogue
-    const int quad = warp & 3;                 // TMEM lane quadrant of this warp
+    const int quad = warp & 3;                 // TMEM lane quadrant
     const int et = threadIdx.x - 64;           // 0..255
-    const int half = (warp - 2) >> 2;          // M-group (decode) or queries (prefill)
-    const int row = (two_groups ? half * 128 : 0) + quad * 32 + lane;   // key within the tile
-    const int jq = (p.qpg + 1) >> 1;
-    const int j0 = half * jq, j1 = min(p.qpg, j0 + jq);
+    const int half = (warp - 2) >> 2;          // M-group (one query) or query pair (four)
+    const int row = (p.qpg == 1 ? half * 128 : 0) + quad * 32 + lane;   // slot of the tile
+    const int key = slot_key(row);             // its key, from the tile's first key row
     const bool use_hist = p.key_hist != nullptr && p.qpg == 1;
+    const int qrows = 32 * p.qpg;
+    auto esync = [&]() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
     auto flush = [&](int qq) {
-      asm volatile("bar.sync 1, 256;" ::: "memory");
+      esync();
       for (int i = et; i < kKeyHistBins; i += kEpiThreads) {
         const uint32_t v = hs[i];
         if (v) atomicAdd(p.key_hist + (int64_t)qq * kKeyHistBins + i, v);
         hs[i] = 0u;
       }
-      asm volatile("bar.sync 1, 256;" ::: "memory");
+      esync();
     };
-    if (use_hist) {
+    if (use_hist)
       for (int i = et; i < kKeyHistBins; i += kEpiThreads) hs[i] = 0u;
-    }
-    int g = g0, cur = -1;
-    bool ok = true;
+    Cursor gc = c0;
+    int cur = -1, acc = 0, t_first = 0;
+    uint32_t aph = 0;
+    int nv[2] = {0, 0};   // visible entries of this thread's queries
     for (int it = begin; it < end; ++it) {
-      while (p.tile_prefix[g + 1] <= it) ++g;
+      gc.advance(p, it);
+      const int g = gc.g;
       if (g != cur) {
         if (use_hist && cur >= 0) flush(cur);
-        asm volatile("bar.sync 1, 256;" ::: "memory");
+        esync();
         for (int i = et; i < qrows; i += kEpiThreads) {
           const int q = g * p.qpg + (i >> 5);
           wbuf[i] = (q < p.nq) ? __ldg(p.w + (int64_t)q * kIdxHeads + (i & 31)) : 0.0f;
         }
-        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (pool) {
+          // the block ids of this CTA's tiles of the group, loaded once
+          t_first = (begin > gc.lo ? begin : gc.lo) - gc.lo;
+          const int t_last = (end < gc.hi ? end : gc.hi) - gc.lo;
+          const int i0 = t_first * blocks_per_tile;
+          const int i1 = min(t_last * blocks_per_tile, p.pool_blocks);
+          const int32_t* src = p.pool + (int64_t)g * p.pool_blocks;
+          for (int i = i0 + et; i < i1; i += kEpiThreads) ids_s[i - i0] = __ldg(src + i);
+        }
+        esync();
         cur = g;
+        if (p.qpg == 1) {
+          nv[0] = group_nvis_query(p, g, 0);
+        } else {
+          nv[0] = group_nvis_query(p, g, 2 * half);
+          nv[1] = group_nvis_query(p, g, 2 * half + 1);
+        }
       }
-      const int u = it - begin;
-      if (!ok) continue;
-      const int acc = u % nacc;
-      if (!mbar_wait(acc_full + acc, (uint32_t)((u / nacc) & 1), p.err)) { ok = false; continue; }
+      if (!mbar_wait_sleep(acc_full + acc, aph, p.err)) break;
       tc_fence_after();
-      const int t = it - p.tile_prefix[g];
-      const int e = t * tile_e + row;
-      const int ja = two_groups ? 0 : j0, jb = two_groups ? 1 : j1;
-      const uint32_t col0 = (uint32_t)(acc * acc_cols + (two_groups ? half * N : 0));
-      for (int j = ja; j < jb; ++j) {
-        uint32_t r[32];
-        tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + col0 + (uint32_t)(j * 32), r);
-        const float* wj = wbuf + j * 32;
-        float s = 0.0f;
+      const int t = it - gc.lo;
+      // entry of this slot (pool mode: the pool slot)
+      const int e = t * tile_e + key - (pairs ? (int)(gc.base & 1) : 0);
+      int32_t blk = -1;     // pool mode: the block of this slot
+      if (pool && t * blocks_per_tile + (row >> 3) < p.pool_blocks)
+        blk = ids_s[(t - t_first) * blocks_per_tile + (row >> 3)];
+      const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * acc_cols);
+      auto score_of = [&](const uint32_t (&r)[32], const float* wj) {
+        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int h = 0; h < 32; ++h) s = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.0f), s);
-        const int q = g * p.qpg + j;
-        if (q < p.nq && e < group_nvis_query(p, g, j)) {
+        for (int h = 0; h < 32; ++h) s4[h & 3] = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.0f), s4[h & 3]);
+        return (s4[0] + s4[1]) + (s4[2] + s4[3]);
+      };
+      auto store = [&](int q, int nvis, float s) {
+        if (pool) {
+          const int64_t ent = (int64_t)blk * 8 + (row & 7);
+          const float v = (blk >= 0 && ent < nvis) ? s : -INFINITY;
+          if (e < p.ld) {
+            p.scores[(int64_t)q * p.ld + e] = v;
+            if (use_hist) atomicAdd(hs + (score_key(v) >> 21), 1u);
+          }
+        } else if (q < p.nq && e >= 0 && e < nvis) {
           if (p.score_bf16) {
             const uint32_t bb = float_to_bf16_bits(s);
             reinterpret_cast<uint16_t*>(p.scores)[(int64_t)q * p.ld + e] = (uint16_t)bb;
@@ -423,10 +573,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (use_hist) atomicAdd(hs + (score_key(s) >> 21), 1u);
           }
         }
+      };
+      if (p.qpg == 1) {
+        uint32_t r[32];
+        tmem_ld32(lane_base + (uint32_t)(half * N), r);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty + acc);
+        store(g, nv[0], score_of(r, wbuf));
+      } else {
+        uint32_t ra[32], rb[32];
+        const int j = 2 * half;
+        tmem_ld32x2(lane_base + (uint32_t)(j * 32), lane_base + (uint32_t)((j + 1) * 32), ra, rb);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty + acc);
+        store(g * p.qpg + j, nv[0], score_of(ra, wbuf + j * 32));
+        store(g * p.qpg + j + 1, nv[1], score_of(rb, wbuf + (j + 1) * 32));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty + acc);
+      if (++acc == nacc) { acc = 0; aph ^= 1; }
     }
     if (use_hist && cur >= 0) flush(cur);
   }
@@ -435,17 +600,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, tmem_cols);
+    tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
 }  // namespace
 
-int index_fp4_smem_bytes(int qpg) { return smem_layout(qpg).total; }
+int index_fp4_smem_bytes() { return smem_layout().total; }
 
-cudaError_t launch_index_fp4(const IndexParams& p, const CUtensorMap& tm_q, int grid,
+cudaError_t launch_index_fp4(const IndexParams& p, const CUtensorMap& tm_kc,
+                             const CUtensorMap& tm_kc2, const CUtensorMap& tm_kc8, int grid,
                              cudaStream_t s) {
-  const int smem = index_fp4_smem_bytes(p.qpg);
+  if (p.qpg != 1 && p.qpg != kMaxQpg) return cudaErrorInvalidValue;
+  const int smem = index_fp4_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(k_index_fp4, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        smem);
   if (e != cudaSuccess) return e;
@@ -457,7 +624,7 @@ cudaError_t launch_index_fp4(const IndexParams& p, const CUtensorMap& tm_q, int 
   cudaLaunchAttribute attr[1] = {pdl_attribute()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_index_fp4, p, tm_q);
+  return cudaLaunchKernelEx(&cfg, k_index_fp4, p, tm_kc, tm_kc2, tm_kc8);
 }
 
 }  // namespace csa2

@@ -93,10 +93,8 @@ typedef struct {
  * MXFP4; the 68 B per key of [NDT sec 3.1]): E2M1 codes (64 B, even channel
  * in the low nibble) + one UE8M0 scale per 32 channels (4 B), the scale
  * rule of CSA2_KV_L32_UE8M0; the indexer then also rounds each query head
- * to the MXFP4 grid before scoring.  The tensor cores take the rounded
- * values as E5M2, exact for block scales 2^-13 .. 2^13 (magnitudes from
- * about 2^-14 to 2^16); a block outside is clamped into that range and
- * sets CSA2_ERR_DEVICE in the device error word.                          */
+ * to the MXFP4 grid before scoring.  The tensor cores take the codes and
+ * scales as they are (block-scaled MXFP4 MMAs, fp32 accumulation).        */
 typedef enum { CSA2_IDX_BF16 = 0, CSA2_IDX_MXFP4 = 1 } csa2_idx_layout_t;
 
 typedef struct csa2_cache csa2_cache_t; /* opaque host handle, one per group */

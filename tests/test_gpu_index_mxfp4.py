@@ -114,26 +114,96 @@ def test_prefill_causal(C, pos0, ratio):
     assert cache.device_error() == 0
 
 
-def test_pool_mode_needs_bf16_keys(C):
+def _reindex_case(C, lens, cap, seq_ids, max_blocks, seed):
+    """Full-layer scores over MXFP4 keys -> candidate pool -> Reindex selection
+    with another query, against the oracle on the MXFP4-rounded keys and
+    queries."""
     import torch
-    cache, _ = _fill(C, [100], [100], 118)
-    q = torch.zeros(1, 32, 128, dtype=torch.bfloat16, device="cuda")
-    w = torch.zeros(1, 32, device="cuda")
-    pool = torch.zeros(1, 16, dtype=torch.int32, device="cuda")
-    with pytest.raises(C.Csa2Error):
-        C.csa2_index_topk_reindex_decode(cache, q, w, pool)
-
-
-def test_out_of_range_scale_is_reported(C):
-    """Keys around 2^20 need a block scale of 2^18, outside the E5M2 fast
-    path's 2^-13 .. 2^13: the indexer clamps it and reports CSA2_ERR_DEVICE."""
-    import torch
-    n = 300
-    cache = C.Cache(C.config(idx_layout=1), [n])
-    k = S.normal_f32(S.stream_key(119, S.S_IDXK, 0), 0, n * 128).reshape(n, 128) * 2.0 ** 20
-    e = S.normal_f32(S.stream_key(119, S.S_ENTRIES, 0), 0, n * 512).reshape(n, 512)
-    C.csa2_append_entries(cache, [0], [n], f32_dev(e), bf16_dev(S.f32_to_bf16_bits(k)))
+    cache, ks = _fill(C, lens, [cap] * len(lens), seed)
+    nq = len(seq_ids)
+    qf, wf = _queries(seed + 1, nq)            # the Full layer's indexer query
+    qr, wr = _queries(seed + 2, nq)            # the Reindex layer's own query
+    sc = torch.full((nq, (cap + 3) // 4 * 4), float("nan"), device="cuda")
+    C.csa2_index_scores_decode(cache, bf16_dev(qf), f32_dev(wf), sc, seq_ids)
+    nv = [lens[s] for s in seq_ids]
+    pool_d = C.csa2_hsi_pool(sc, nv, max_blocks=max_blocks)
+    tsc = torch.full((nq, 512), 7.0, device="cuda")
+    idx = C.csa2_index_topk_reindex_decode(cache, bf16_dev(qr), f32_dev(wr), pool_d,
+                                           seq_ids, topk_score=tsc).cpu().numpy()
+    pool = pool_d.cpu().numpy()
+    tsc = tsc.cpu().numpy()
+    log = []
+    for i, s in enumerate(seq_ids):
+        n = lens[s]
+        kq = O.mxfp4_round_bf16(ks[s][:n])
+        qq = O.mxfp4_round_bf16(qr[i])
+        o_idx, o_sc, pos = O.reindex_topk(kq, qq, wr[i], pool[i], n, 512)
+        full = np.full(max(n, 1), -np.inf)
+        full[pos] = o_sc
+        check_topk(idx[i], o_idx, full, 512, log)
+        valid = idx[i] >= 0
+        assert set(idx[i][valid].tolist()) <= set(pos.tolist())
+        if valid.any():
+            assert np.allclose(tsc[i][valid], full[idx[i][valid]], rtol=2e-5,
+                               atol=2e-5 * np.abs(o_sc).max())
+        assert np.all(tsc[i][~valid] == 0)
     assert cache.device_error() == 0
-    qi, w = _queries(120, 1)
-    C.csa2_index_topk_decode(cache, bf16_dev(qi), f32_dev(w))
-    assert cache.device_error() == 7        # CSA2_ERR_DEVICE
+    return log
+
+
+def test_reindex_on_mxfp4_keys(C):
+    """Reindex mode ("DeepSeek-V4.1-Flash" report, section 2.3.2) over the
+    report's FP4 indexer keys (section 2.4.4): pools of 2048 blocks of 8
+    over ragged sequences whose offsets are not multiples of 4."""
+    log = _reindex_case(C, [30000, 16384, 2000, 0, 20001], 30721, [0, 1, 2, 3, 4, 0, 4],
+                        2048, 130)
+    print("near-ties:", log)
+
+
+def test_reindex_on_mxfp4_keys_partial_tile(C):
+    """A pool of 48 blocks: the last 256-slot tile of the MXFP4 indexer holds
+    16 blocks (slots past the pool are neither scored nor stored)."""
+    _reindex_case(C, [3000, 777], 3001, [0, 1, 1], 48, 140)
+
+
+def test_small_context_reindex_equals_full_selection_mxfp4(C):
+    """Fewer blocks than the pool holds: the Reindex selection equals the
+    Full selection of the same query on the same MXFP4 keys, bit for bit."""
+    import torch
+    lens = [12000, 700, 16384]
+    cache, ks = _fill(C, lens, [16384] * 3, 150)
+    qi, w = _queries(151, 3)
+    sc = torch.full((3, 16384), float("nan"), device="cuda")
+    C.csa2_index_scores_decode(cache, bf16_dev(qi), f32_dev(w), sc)
+    pool_d = C.csa2_hsi_pool(sc, lens, max_blocks=2048)
+    s_full = torch.zeros(3, 512, device="cuda")
+    s_re = torch.zeros(3, 512, device="cuda")
+    full = C.csa2_index_topk_decode(cache, bf16_dev(qi), f32_dev(w), topk_score=s_full)
+    re = C.csa2_index_topk_reindex_decode(cache, bf16_dev(qi), f32_dev(w), pool_d,
+                                          topk_score=s_re)
+    assert torch.equal(full, re)
+    assert torch.equal(s_full, s_re)
+
+
+@pytest.mark.parametrize("mag", [2.0 ** 20, 2.0 ** -20])
+def test_extreme_block_scales(C, mag):
+    """Keys around 2^20 (block scale 2^18) or 2^-20 (2^-22): the block-scaled
+    MMAs take any UE8M0 scale, so the scores still match the oracle's fp64
+    score of the rounded values and nothing is flagged."""
+    import torch
+    n = 3000
+    cache = C.Cache(C.config(idx_layout=1), [n])
+    k = S.normal_f32(S.stream_key(119, S.S_IDXK, 0), 0, n * 128).reshape(n, 128) * mag
+    kb = S.f32_to_bf16_bits(k)
+    e = S.normal_f32(S.stream_key(119, S.S_ENTRIES, 0), 0, n * 512).reshape(n, 512)
+    C.csa2_append_entries(cache, [0], [n], f32_dev(e), bf16_dev(kb))
+    qi, w = _queries(120, 2)
+    sc = torch.full((2, n), float("nan"), device="cuda")
+    C.csa2_index_scores_decode(cache, bf16_dev(qi), f32_dev(w), sc, [0, 0])
+    sc = sc.cpu().numpy()
+    idx = C.csa2_index_topk_decode(cache, bf16_dev(qi), f32_dev(w), [0, 0]).cpu().numpy()
+    for i in range(2):
+        o_idx, o_sc = O.index_topk_mxfp4(kb, qi[i], w[i], 512)
+        assert np.allclose(sc[i], o_sc, rtol=2e-5, atol=2e-5 * np.abs(o_sc).max())
+        check_topk(idx[i], o_idx, o_sc, 512)
+    assert cache.device_error() == 0
