@@ -63,6 +63,12 @@ def parse_args(argv=None):
                    help="skip the step over the pages' exact cache formats")
     p.add_argument("--no-hsi", action="store_true",
                    help="skip the Hierarchical Sparse Indexer / Reindex measurement")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the other workloads (decode 0, 1, 3 and prefill 4) in the line")
+    p.add_argument("--no-decoder", action="store_true",
+                   help="skip the pages' 20-layer decoder (Full/Reindex groups) measurement")
+    p.add_argument("--repeats", type=int, default=25,
+                   help="timed regions of --steps steps each; value is the median")
     p.add_argument("--no-graph", action="store_true",
                    help="time eager API calls instead of the captured CUDA graph")
     p.add_argument("--micro-batches", type=int, default=2,
@@ -423,21 +429,32 @@ def run_csa2(args):
             graphs[i % S].replay()
         torch.cuda.synchronize()
 
-    barrier(world)
+    R = max(1, args.repeats)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    t_start.record(stream)
-    for i in range(args.steps):
-        if graphs is not None:
-            graphs[i % S].replay()
-        else:
-            step(b=i % S)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    elapsed = t_start.elapsed_time(t_end) / 1000.0
-    elapsed_single = elapsed
+
+    def timed_region(run_steps):
+        # exactly --steps steps between a barrier + synchronize on both sides
+        barrier(world)
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        run_steps()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return t_start.elapsed_time(t_end) / 1000.0
+
+    def single_steps():
+        for i in range(args.steps):
+            if graphs is not None:
+                graphs[i % S].replay()
+            else:
+                step(b=i % S)
+
+    singles = [timed_region(single_steps) for _ in range(R)]
+    elapsed_single = statistics.median(singles)
+    elapsed = elapsed_single
+    repeats = singles
 
     # ---- the headline schedule: the batch split into micro-batches, each on
     #      its own stream and in order there, step after step; the indexer's
@@ -477,16 +494,15 @@ def run_csa2(args):
         cache.set_index_sms(0)
         g_main.replay()
         torch.cuda.synchronize()
-        barrier(world)
-        t_start.record(stream)
-        for _ in range(args.steps // graph_steps):
-            g_main.replay()
-        if g_rest is not None:
-            g_rest.replay()
-        t_end.record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-        elapsed = t_start.elapsed_time(t_end) / 1000.0
+
+        def mb_timed_steps():
+            for _ in range(args.steps // graph_steps):
+                g_main.replay()
+            if g_rest is not None:
+                g_rest.replay()
+
+        repeats = [timed_region(mb_timed_steps) for _ in range(R)]
+        elapsed = statistics.median(repeats)
     clocks = sampler.stop()
 
     # ---- per-kernel split: eager calls with CUDA events around each launch
@@ -508,6 +524,34 @@ def run_csa2(args):
         raise RuntimeError("device error word set during the benchmark")
     elapsed_max = max_over_ranks(elapsed, world, dev)
     single_max = max_over_ranks(elapsed_single, world, dev)
+    rep_ms = [1000 * max_over_ranks(x, world, dev) / args.steps for x in repeats]
+
+    # the indexer alone on the schedule's capped grid, one micro-batch's
+    # queries (the launch configuration of the headline schedule)
+    sched_idx = None
+    if M > 1:
+        d0 = mb_sets[0][0]
+        cache.set_index_sms(args.index_sms)
+        for _ in range(3):
+            C.csa2_index_scores_decode(cache, d0["q_idx"], d0["w"], d0["scores"], seq_ids=d0["seq"],
+                                       key_hist=d0["hist"])
+        n_si = max(3, min(args.steps, 100))
+        e_si = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_si)]
+        for e in e_si:
+            e[0].record(stream)
+            C.csa2_index_scores_decode(cache, d0["q_idx"], d0["w"], d0["scores"], seq_ids=d0["seq"],
+                                       key_hist=d0["hist"])
+            e[1].record(stream)
+        torch.cuda.synchronize()
+        cache.set_index_sms(0)
+        t_si = statistics.median(e[0].elapsed_time(e[1]) for e in e_si) / 1000.0
+        si_bytes = int(sum(d0["nv"])) * 256 + len(d0["seq"]) * (32 * 128 * 2 + 32 * 4)
+        hbm_pk, _ = measured_peaks()
+        sched_idx = {"sms": args.index_sms, "queries": len(d0["seq"]),
+                     "ms": 1000 * t_si, "achieved": si_bytes / t_si / 1e9,
+                     "frac": si_bytes / t_si / 1e9 / hbm_pk,
+                     "timed_as": "one micro-batch's indexer alone on the schedule's capped "
+                                 "grid (median of per-launch CUDA events)"}
 
     # ---- end to end: every step's inputs go host -> device and its outputs
     #      device -> host inside the timed region, double-buffered the way a
@@ -625,17 +669,22 @@ def run_csa2(args):
                     "host buffers); the micro-batches' pipelines overlap")
     run_e2e(3)
     torch.cuda.synchronize()
-    barrier(world)
     a = torch.cuda.Event(enable_timing=True)
     b_ = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    copy_stream.wait_stream(stream)
-    run_e2e(e2e_steps)
-    b_.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e_elapsed_local = a.elapsed_time(b_) / 1000.0
-    e2e_elapsed = max_over_ranks(e2e_elapsed_local, world, dev)
+
+    def e2e_region():
+        barrier(world)
+        torch.cuda.synchronize()
+        a.record(stream)
+        copy_stream.wait_stream(stream)
+        run_e2e(e2e_steps)
+        b_.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(a.elapsed_time(b_) / 1000.0, world, dev)
+
+    e2e_reps = [e2e_region() for _ in range(R)]
+    e2e_elapsed = statistics.median(e2e_reps)
 
     hbm_peak, peak_kind = measured_peaks()
     # the measurements below read input set 0 and its fp32 selection
@@ -657,6 +706,23 @@ def run_csa2(args):
     if not args.no_hsi:
         hsi = measure_hsi(C, W, wl, cache, scores, n_valid, dev, stream,
                           max(3, min(args.steps, 300)), hbm_peak)
+    # the other workloads and the pages' decoder, each on its own cache
+    configs, decoder = None, None
+    iters = max(5, min(args.steps, 50))
+    if not args.no_configs:
+        configs = {}
+        flush = make_l2_flush(dev)
+        for wid in (0, 1, 3):
+            r = measure_decode_config(C, W, wid, dev, stream, iters, hbm_peak, flush)
+            configs[r["workload"]] = r
+        r = measure_prefill(C, W, 4, args.layout, dev, stream, max(3, min(args.steps, 10)),
+                            max(3, args.warmup))
+        configs[r["workload"]] = r
+        del flush
+        torch.cuda.empty_cache()
+    if not args.no_decoder:
+        decoder = measure_decoder(C, W, dev, stream, iters, hbm_peak)
+        torch.cuda.empty_cache()
 
     # ---- accounting
     tot_ent = int(n_ent.sum())
@@ -675,6 +741,7 @@ def run_csa2(args):
     launches_per_step = (3 + L) * ((B + 1023) // 1024) * max(1, M)
     config = workload_config(wl, args.layout)
     config["input_sets"] = S
+    nominal = 8000.0   # GB/s: the nominal HBM3e figure of the target
     line = {
         "metric": METRIC, "value": B * world * args.steps / elapsed_max, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -684,10 +751,19 @@ def run_csa2(args):
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
                      "peak_kind": f"{peak_kind} (copy bandwidth)",
-                     "algorithmic_bytes_per_launch": idx_bytes},
+                     "frac_nominal": achieved / nominal,
+                     "algorithmic_bytes_per_launch": idx_bytes,
+                     "timed_as": "eager, the whole batch on every SM (median of per-launch "
+                                 "CUDA events on the launching stream)",
+                     "in_schedule": None if sched_idx is None else sched_idx},
         "step_hbm": {"achieved": step_bytes / (ms / 1000) / 1e9, "peak": hbm_peak,
                      "unit": "GB/s", "frac": step_bytes / (ms / 1000) / 1e9 / hbm_peak,
+                     "frac_nominal": step_bytes / (ms / 1000) / 1e9 / nominal,
                      "algorithmic_bytes_per_step": step_bytes},
+        "repeats": {"n": len(rep_ms), "steps_each": args.steps,
+                    "ms_per_step_median": statistics.median(rep_ms),
+                    "ms_per_step_min": min(rep_ms), "ms_per_step_max": max(rep_ms),
+                    "value_is": "the median timed region (max over ranks)"},
         "kernel_ms": {"index_scores": 1000 * t_idx, "topk": 1000 * t_topk,
                       "sparse_attn_all_layers": 1000 * t_attn,
                       "eager_step": eager_ms,
@@ -702,14 +778,23 @@ def run_csa2(args):
                                       "split, every SM for the indexer; one CUDA graph per step"},
         "e2e": {"value": B * world * e2e_steps / e2e_elapsed, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "pipelining": e2e_note},
+                "pipelining": e2e_note,
+                "repeats": {"n": len(e2e_reps), "steps_each": e2e_steps,
+                            "value_min": B * world * e2e_steps / max(e2e_reps),
+                            "value_max": B * world * e2e_steps / min(e2e_reps)}},
         "gpu_launches": launches_per_step * args.steps,
         "hsi_reindex": hsi,
         "bf16_scores": bf16,
         "readout_epilogue": epi,
         "paper_cache": paper,
+        "configs": configs,
+        "decoder": decoder,
         "clocks": clocks,
     }
+    if clocks.get("sm_mhz"):
+        # time x clock: a clock-normalised step time, comparable across runs
+        # whose SM clock differs
+        clocks["ms_per_step_x_sm_mhz"] = ms * clocks["sm_mhz"]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds, args.layout)
     if rank == 0:
@@ -782,6 +867,11 @@ def measure_paper_cache(C, W, wl, dev, stream, iters, hbm_peak):
     torch.cuda.synchronize()
     t_sel = sum(e[0].elapsed_time(e[1]) for e in evs) / iters
     t_attn = sum(e[1].elapsed_time(e[2]) for e in evs) / iters
+    # the MXFP4 indexer alone (its dominant kernel)
+    sc = torch.empty(B, (int(n_ent.max()) + 3) // 4 * 4, dtype=torch.float32, device=dev)
+    hist = torch.empty(B, 2048, dtype=torch.int32, device=dev)
+    t_ix = statistics.median(per_step_ms(
+        lambda: C.csa2_index_scores_decode(cache, q_idx, w, sc, key_hist=hist), iters, stream))
     if cache.device_error() != 0:
         raise RuntimeError("device error word set during the paper-cache measurement")
     tot = int(n_ent.sum())
@@ -793,6 +883,12 @@ def measure_paper_cache(C, W, wl, dev, stream, iters, hbm_peak):
                        "window FP8 (584 B/row)",
             "ms_per_step": ms, "value": B / (ms / 1000), "unit": "query-tokens/s",
             "selection_ms": t_sel, "readout_all_layers_ms": t_attn,
+            "index_ms": t_ix,
+            "index_roofline": {"kernel": "k_index_fp4 (block-scaled MXFP4 MMAs)",
+                               "bound": "hbm", "algorithmic_bytes_per_launch": idx_bytes,
+                               "achieved": idx_bytes / (t_ix / 1000) / 1e9, "peak": hbm_peak,
+                               "unit": "GB/s",
+                               "frac": idx_bytes / (t_ix / 1000) / 1e9 / hbm_peak},
             "algorithmic_bytes_per_step": step_bytes,
             "step_hbm_gbs": step_bytes / (ms / 1000) / 1e9,
             "step_hbm_frac": step_bytes / (ms / 1000) / 1e9 / hbm_peak,
@@ -954,24 +1050,135 @@ def measure_hsi(C, W, wl, cache, scores, n_valid, dev, stream, iters, hbm_peak,
                         "segments + top-k + slot map"}
 
 
-def run_prefill(args):
-    """Chunked prefill of one sequence (workload 4): 8192 new tokens on a
-    131072-token prefix, ratio 2; per step the Full layer's causal index
-    scores and top-512, then the attention of the Full and the Reuse layers."""
+def make_l2_flush(dev, nbytes=512 << 20):
+    """Writes a buffer of 4x the 129 MB L2 (torch's fill kernel, outside the
+    timed events), so that a timed step finds none of its inputs in L2."""
     import torch
+    buf = torch.empty(nbytes // 4, dtype=torch.int32, device=dev)
+    return lambda: buf.fill_(1)
 
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    import fp4_kv_cache_index_gb300 as C
-    from csa2_synth import workloads as W
-    wl = W.WORKLOADS[args.workload]
+
+def per_step_ms(run, n, stream, flush=None):
+    """Device time (ms) of each of n calls of `run`, CUDA events on the
+    launching stream around each; the L2 flushed before each when `flush`."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for a, b in evs:
+        if flush is not None:
+            flush()
+        a.record(stream)
+        run()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def capture(run, stream):
+    """`run` captured as a CUDA graph (warmed on a side stream first)."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        run()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    return g
+
+
+def measure_decode_config(C, W, wid, dev, stream, iters, hbm_peak, flush):
+    """One decode step of workload `wid` at full size (Full layer index +
+    top-k, then every layer's readout), the whole batch on one stream as a
+    CUDA graph; the L2 is flushed before every timed step (the small
+    workloads' inputs fit in L2).  Roofline: HBM on the algorithmic bytes of
+    the step (indexer keys + queries, and per query and layer the selected
+    entries, the window rows, q and out)."""
+    import torch
+    wl = W.WORKLOADS[wid]
+    B, L = wl.batch, wl.layers
+    n_ent = [int(x) for x in wl.n_entries()]
+    cache = C.Cache(C.config(ratio=wl.ratio), n_ent, device=dev)
+    W.fill_cache(wl, cache)
+    q_idx, w = W.dev_q_idx(wl), W.dev_w(wl)
+    qs = [W.dev_q(wl, l) for l in range(L)]
+    swas = [W.dev_swa(wl, l) for l in range(L)]
+    ld = max(4, (max(n_ent) + 3) // 4 * 4)
+    scores = torch.empty(B, ld, dtype=torch.float32, device=dev)
+    hist = torch.empty(B, 2048, dtype=torch.int32, device=dev)
+    tws = torch.empty(max(16, C.csa2_topk_workspace_bytes(B, max(n_ent))), dtype=torch.uint8,
+                      device=dev)
+    aws = torch.empty(max(16, C.csa2_sparse_attn_workspace_bytes(cache, B)), dtype=torch.uint8,
+                      device=dev)
+    topk = torch.empty(B, 512, dtype=torch.int32, device=dev)
+    outs = [torch.empty(B, 64, 512, dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    scale = 512 ** -0.5
+
+    def index():
+        C.csa2_index_scores_decode(cache, q_idx, w, scores, key_hist=hist)
+
+    def select():
+        C.csa2_topk(scores, n_ent, 512, idx_out=topk, key_hist=hist, workspace=tws)
+
+    def readout():
+        for l in range(L):
+            C.csa2_sparse_attn_decode(cache, qs[l], swas[l], topk, scale, out=outs[l],
+                                      workspace=aws)
+
+    def step():
+        index()
+        select()
+        readout()
+
+    for _ in range(3):
+        step()
+    g = capture(step, stream)
+    for _ in range(3):
+        g.replay()
+    t = per_step_ms(g.replay, iters, stream, flush)
+    t_idx = per_step_ms(index, iters, stream, flush)
+    t_sel = per_step_ms(lambda: (index(), select()), iters, stream, flush)
+    t_att = per_step_ms(readout, iters, stream, flush)
+    if cache.device_error() != 0:
+        raise RuntimeError(f"device error word set during workload {wid}")
+    ms = statistics.median(t)
+    ms_idx = statistics.median(t_idx)
+    ms_sel = max(0.0, statistics.median(t_sel) - ms_idx)
+    ms_att = statistics.median(t_att)
+    idx_bytes = sum(n_ent) * 256 + B * (32 * 128 * 2 + 32 * 4)
+    attn_bytes = L * sum(min(512, n) * 272 + 128 * 1024 + 2 * 64 * 1024 for n in n_ent)
+    step_bytes = idx_bytes + attn_bytes
+    gbs = step_bytes / (ms / 1000) / 1e9
+    parts = {"index_scores": ms_idx, "topk": ms_sel, "sparse_attn_all_layers": ms_att}
+    top = max(parts, key=parts.get)
+    del cache
+    return {"workload": wl.name, "batch": B, "entries_per_seq": n_ent if wl.ragged else n_ent[0],
+            "ratio": wl.ratio, "layers": f"1 Full + {L - 1} Reuse", "layout": "L32_UE8M0",
+            "ms_per_step": ms, "ms_per_step_min": min(t), "ms_per_step_max": max(t),
+            "value": B / (ms / 1000), "unit": UNIT, "steps": iters,
+            "roofline": {"bound": "hbm", "algorithmic_bytes_per_step": step_bytes,
+                         "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": gbs / hbm_peak, "frac_nominal": gbs / 8000.0},
+            "kernel_ms": parts,
+            "dominant": {"part": top, "share": parts[top] / sum(parts.values())},
+            "timed_as": "median of per-step CUDA events, one CUDA graph per step, the L2 "
+                        "flushed (512 MB written) before every step; parts timed eagerly the "
+                        "same way (top-k = index + top-k minus index)"}
+
+
+def measure_prefill(C, W, wid, layout, dev, stream, steps, warmup):
+    """Chunked prefill of one sequence: the Full layer's causal index scores
+    and top-512 of every new token, then the readout of the Full and the
+    Reuse layers.  Roofline: the dense bf16 tensor pipe (sustained figure) on
+    the step's FLOPs (indexer over the visible entries, attention over the
+    selected entries and the causal window)."""
+    import torch
+    wl = W.WORKLOADS[wid]
     L, T = wl.layers, wl.n_queries()
     n_ent = int(wl.n_entries()[0])
-    cache = C.Cache(C.config(ratio=wl.ratio, layout=args.layout), [n_ent], device=dev)
+    cache = C.Cache(C.config(ratio=wl.ratio, layout=layout), [n_ent], device=dev)
     W.fill_cache(wl, cache)
     q_idx, w = W.dev_q_idx(wl), W.dev_w(wl)
     qs = [W.dev_q(wl, l) for l in range(L)]
@@ -982,79 +1189,194 @@ def run_prefill(args):
     outs = [torch.empty(T, 64, 512, dtype=torch.bfloat16, device=dev) for _ in range(L)]
     n_valid = [min(n_ent, (wl.pos0 + i + 1) // wl.ratio) for i in range(T)]
     scale = 512 ** -0.5
-    stream = torch.cuda.current_stream()
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
+    def index():
         C.csa2_index_scores_prefill(cache, 0, wl.pos0, q_idx, w, scores)
-        if ev is not None:
-            ev[1].record(stream)
+
+    def select():
         C.csa2_topk(scores, n_valid, 512, idx_out=topk)
-        if ev is not None:
-            ev[2].record(stream)
+
+    def readout():
         for l in range(L):
             C.csa2_sparse_attn_prefill(cache, 0, wl.pos0, qs[l], rows[l], wl.swa_pos0, topk,
                                        scale, out=outs[l])
-        if ev is not None:
-            ev[3].record(stream)
 
-    sampler = ClockSampler(local).start()
-    for _ in range(args.warmup):
-        step()
+    for _ in range(warmup):
+        index()
+        select()
+        readout()
     torch.cuda.synchronize()
-    barrier(world)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for i in range(args.steps):
-        step(evs[i])
-    b.record(stream)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for e in evs:
+        e[0].record(stream)
+        index()
+        e[1].record(stream)
+        select()
+        e[2].record(stream)
+        readout()
+        e[3].record(stream)
     torch.cuda.synchronize()
-    barrier(world)
-    clocks = sampler.stop()
-    elapsed = max_over_ranks(a.elapsed_time(b) / 1000.0, world, dev)
-    t_idx = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps / 1000.0
-    t_topk = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps / 1000.0
-    t_attn = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps / 1000.0
     if cache.device_error() != 0:
-        raise RuntimeError("device error word set during the benchmark")
+        raise RuntimeError("device error word set during the prefill measurement")
+    ms = statistics.median(e[0].elapsed_time(e[3]) for e in evs)
+    t_idx = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+    t_sel = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
+    t_att = statistics.median(e[2].elapsed_time(e[3]) for e in evs)
     idx_flops = 2.0 * 32 * 128 * sum(n_valid)            # visible entries only
     cand = [min(512, n) + min(128, wl.pos0 + i - wl.swa_pos0 + 1) for i, n in enumerate(n_valid)]
     attn_flops = L * 64 * 512 * 4.0 * sum(cand)
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
         if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
     peak = float(peaks.get("bf16_tflops_sustained", 1700.0))
-    ms = 1000 * elapsed / args.steps
+    peak_kind = "measured bf16 cuBLAS, sustained" if "bf16_tflops_sustained" in peaks \
+        else "fallback"
+    tf = lambda f, t: f / (t / 1000) / 1e12
+    parts = {"index_scores": t_idx, "topk": t_sel, "sparse_attn_all_layers": t_att}
+    top = max(parts, key=parts.get)
+    del cache
+    return {"workload": wl.name, "batch": 1, "new_tokens": T, "prefix_tokens": wl.ctx,
+            "entries": n_ent, "ratio": wl.ratio, "layers": f"1 Full + {L - 1} Reuse",
+            "layout": "L32_UE8M0" if layout == 0 else "L16_E4M3",
+            "ms_per_step": ms, "value": T / (ms / 1000), "unit": UNIT, "steps": steps,
+            "roofline": {"bound": "tensor", "flops_per_step": idx_flops + attn_flops,
+                         "achieved": tf(idx_flops + attn_flops, ms), "peak": peak,
+                         "unit": "TFLOP/s", "frac": tf(idx_flops + attn_flops, ms) / peak,
+                         "peak_kind": peak_kind},
+            "parts_tensor_frac": {"index_scores": tf(idx_flops, t_idx) / peak,
+                                  "sparse_attn_all_layers": tf(attn_flops, t_att) / peak},
+            "kernel_ms": parts,
+            "dominant": {"part": top, "share": parts[top] / sum(parts.values())},
+            "timed_as": "median of per-step CUDA events around eager calls (inputs larger "
+                        "than L2: 2.3 GB of scores per step)"}
+
+
+def run_prefill(args):
+    """Chunked prefill of one sequence (workload 4) as its own line: 8192 new
+    tokens on a 131072-token prefix, ratio 2."""
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import fp4_kv_cache_index_gb300 as C
+    from csa2_synth import workloads as W
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(local).start()
+    barrier(world)
+    r = measure_prefill(C, W, args.workload, args.layout, dev, stream, args.steps, args.warmup)
+    barrier(world)
+    clocks = sampler.stop()
+    ms = max_over_ranks(r["ms_per_step"], world, dev)
+    wl = W.WORKLOADS[args.workload]
     line = {
-        "metric": "CSA2 prefill query-tokens/s, 8192 tokens on a 128K prefix; indexer "
-                  "tensor-pipe TFLOP/s vs peak",
-        "value": T * world * args.steps / elapsed, "unit": UNIT, "n_gpus": world,
+        "metric": "CSA2 prefill query-tokens/s, 8192 tokens on a 128K prefix; tensor-pipe "
+                  "TFLOP/s vs peak",
+        "value": r["new_tokens"] * world / (ms / 1000), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "batch": 1, "new_tokens": T, "prefix_tokens": wl.ctx,
-                   "entries": n_ent, "ratio": wl.ratio,
-                   "layers": f"1 Full + {L - 1} Reuse",
-                   "layout": "L32_UE8M0" if args.layout == 0 else "L16_E4M3",
-                   "l2": "inputs larger than L2 (2.3 GB of scores and 4.4 GB of "
-                         "indexer-key reads per step)"},
-        "roofline": {"kernel": "k_index (prefill, 8 queries x 32 heads per MMA tile)",
-                     "bound": "tensor", "achieved": idx_flops / t_idx / 1e12, "peak": peak,
-                     "unit": "TFLOP/s", "frac": idx_flops / t_idx / 1e12 / peak,
-                     "traffic": None, "peak_kind": "measured bf16 cuBLAS, sustained"},
-        "step_tensor": {"achieved": (idx_flops + attn_flops) / (ms / 1000) / 1e12, "peak": peak,
-                        "unit": "TFLOP/s",
-                        "frac": (idx_flops + attn_flops) / (ms / 1000) / 1e12 / peak,
-                        "flops_per_step": idx_flops + attn_flops},
-        "kernel_ms": {"index_scores": 1000 * t_idx, "topk": 1000 * t_topk,
-                      "sparse_attn_all_layers": 1000 * t_attn},
-        "gpu_launches": args.steps * (1 + (T + 1023) // 1024 + L),
+        "config": {k: r[k] for k in ("workload", "batch", "new_tokens", "prefix_tokens",
+                                     "entries", "ratio", "layers", "layout")},
+        "roofline": r["roofline"], "parts_tensor_frac": r["parts_tensor_frac"],
+        "kernel_ms": r["kernel_ms"],
+        "gpu_launches": args.steps * (1 + (wl.n_queries() + 1023) // 1024 + wl.layers),
         "clocks": clocks,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def measure_decoder(C, W, dev, stream, iters, hbm_peak, max_blocks=2048):
+    """The pages' decoder (V4.1 report, section 4.2.1: 20 CSA2 layers at
+    ratio 1 in five groups of four; group 1 = Full + 3 Reuse, groups 2-5 =
+    Reindex + 3 Reuse; a Hierarchical Sparse Indexer pool of 2048 blocks of
+    8) over the pages' cache formats (main KV E2M1 + E4M3/16, indexer keys
+    and queries MXFP4, FP8 window rows), one decode step for batch 64 at
+    128K context: Full index + top-k + pool, 4 x Reindex selection, 20
+    readouts.  Timed as one CUDA graph per step, median over `iters`."""
+    import torch
+    wl = W.WORKLOADS[2]
+    B = wl.batch
+    n_ent = [int(x) for x in wl.n_entries()]
+    cache = C.Cache(C.config(ratio=wl.ratio, layout=1, idx_layout=1), n_ent, device=dev)
+    W.fill_cache(wl, cache)
+    n_layers, n_groups = 20, 5
+    qi = [W.dev_q_idx(wl, layer=g) for g in range(n_groups)]
+    wi = [W.dev_w(wl, layer=g) for g in range(n_groups)]
+    qs = [W.dev_q(wl, l) for l in range(n_layers)]
+    swas = [C.csa2_swa_fp8_quantise(W.dev_swa(wl, l)) for l in range(n_layers)]
+    ld = (max(n_ent) + 3) // 4 * 4
+    scores = torch.empty(B, ld, dtype=torch.float32, device=dev)
+    hist = torch.empty(B, 2048, dtype=torch.int32, device=dev)
+    tws = torch.empty(max(16, C.csa2_topk_workspace_bytes(B, max(n_ent))), dtype=torch.uint8,
+                      device=dev)
+    aws = torch.empty(max(16, C.csa2_sparse_attn_workspace_bytes(cache, B)), dtype=torch.uint8,
+                      device=dev)
+    pool = torch.empty(B, max_blocks, dtype=torch.int32, device=dev)
+    pws = torch.empty(max(16, int(C.lib.csa2_hsi_pool_workspace_bytes(B, max(n_ent)))),
+                      dtype=torch.uint8, device=dev)
+    rws = torch.empty(max(16, int(C.lib.csa2_index_reindex_workspace_bytes(
+        cache.handle, B, max_blocks))), dtype=torch.uint8, device=dev)
+    topks = [torch.empty(B, 512, dtype=torch.int32, device=dev) for _ in range(n_groups)]
+    outs = [torch.empty(B, 64, 512, dtype=torch.bfloat16, device=dev) for _ in range(n_layers)]
+    scale = 512 ** -0.5
+
+    def select(g):
+        if g == 0:
+            C.csa2_index_scores_decode(cache, qi[0], wi[0], scores, key_hist=hist)
+            C.csa2_topk(scores, n_ent, 512, idx_out=topks[0], key_hist=hist, workspace=tws)
+            C.csa2_hsi_pool(scores, n_ent, max_blocks, pool_blocks=pool, workspace=pws)
+        else:
+            C.csa2_index_topk_reindex_decode(cache, qi[g], wi[g], pool, topk_idx=topks[g],
+                                             workspace=rws)
+
+    def readout(g):
+        for l in range(4 * g, 4 * g + 4):
+            C.csa2_sparse_attn_decode(cache, qs[l], None, topks[g], scale, out=outs[l],
+                                      workspace=aws, swa_fp8=swas[l])
+
+    def step():
+        for g in range(n_groups):
+            select(g)
+            readout(g)
+
+    for _ in range(3):
+        step()
+    gr = capture(step, stream)
+    for _ in range(3):
+        gr.replay()
+    t = per_step_ms(gr.replay, iters, stream)
+    t_full = per_step_ms(lambda: select(0), iters, stream)
+    t_re = per_step_ms(lambda: select(1), iters, stream)
+    t_rd = per_step_ms(lambda: readout(1), iters, stream)
+    if cache.device_error() != 0:
+        raise RuntimeError("device error word set during the decoder measurement")
+    ms = statistics.median(t)
+    q_bytes = B * (32 * 128 * 2 + 32 * 4)
+    full_bytes = sum(n_ent) * 68 + q_bytes + sum(n_ent) * 4          # keys, queries, pool's scores
+    re_bytes = B * (max_blocks * 8 * 68) + q_bytes
+    rd_bytes = B * (512 * 288 + 128 * 584 + 2 * 64 * 1024)
+    step_bytes = full_bytes + (n_groups - 1) * re_bytes + n_layers * rd_bytes
+    gbs = step_bytes / (ms / 1000) / 1e9
+    del cache
+    return {"layout": "decoder of 20 layers: [Full + 3 Reuse] + 4 x [Reindex + 3 Reuse], "
+                      "pool of 2048 blocks x 8",
+            "formats": "main KV E2M1 + E4M3/16 (288 B), indexer K MXFP4 (68 B), window FP8 "
+                       "(584 B/row)",
+            "batch": B, "entries_per_seq": n_ent[0],
+            "ms_per_step": ms, "ms_per_step_min": min(t), "ms_per_step_max": max(t),
+            "value": B / (ms / 1000), "unit": "query-tokens/s through the 20 decoder layers",
+            "roofline": {"bound": "hbm", "algorithmic_bytes_per_step": step_bytes,
+                         "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": gbs / hbm_peak, "frac_nominal": gbs / 8000.0},
+            "parts_ms": {"full_selection_and_pool": statistics.median(t_full),
+                         "reindex_selection": statistics.median(t_re),
+                         "readout_4_layers": statistics.median(t_rd)},
+            "timed_as": "median of per-step CUDA events, one CUDA graph per step (keys 17x "
+                        "larger than L2, read evict-first); parts eager"}
 
 
 def main(argv=None):
