@@ -80,6 +80,8 @@ def _load():
         "csa2_cache_create": ([pcfg, i32, P, P, sz, P, ctypes.POINTER(P)], i32),
         "csa2_cache_destroy": ([P], i32),
         "csa2_cache_set_index_sms": ([P, i32], i32),
+        "csa2_cache_set_wait_limit": ([P, i64], i32),
+        "csa2_cache_inject_fault": ([P, i32], i32),
         "csa2_cache_reset": ([P, P], i32),
         "csa2_cache_length": ([P, i32, ctypes.POINTER(i64)], i32),
         "csa2_cache_views": ([P, ctypes.POINTER(CacheViews)], i32),
@@ -187,6 +189,16 @@ class Cache:
         """At most n_sms SMs for the indexer's grid (0: all); see
         csa2_cache_set_index_sms."""
         _check(lib.csa2_cache_set_index_sms(self.handle, n_sms), "csa2_cache_set_index_sms")
+
+    def set_wait_limit(self, cycles: int):
+        """Bounded-wait limit of this cache's kernels in SM cycles (0: the
+        default); see csa2_cache_set_wait_limit."""
+        _check(lib.csa2_cache_set_wait_limit(self.handle, cycles), "csa2_cache_set_wait_limit")
+
+    def inject_fault(self, fault: int):
+        """0: none; 1: the indexers issue no key loads (tests of the timeout
+        path); see csa2_cache_inject_fault."""
+        _check(lib.csa2_cache_inject_fault(self.handle, fault), "csa2_cache_inject_fault")
 
     def views(self) -> dict:
         """codes [total, 256] u8, scales [total, 512/g] u8, idx_k [total, 128]

@@ -41,6 +41,8 @@ struct csa2_cache {
   CUtensorMap tm_kc2;  // MXFP4 key codes, two keys per 128-byte row, 128-row boxes
   int num_sms;
   int index_sms;       // SMs the indexer's persistent grid may occupy
+  int64_t wait_cycles; // bounded-wait limit of the kernels (0: their default)
+  int32_t inject;      // fault injection for tests (kInjectNoKeyLoads)
 };
 
 namespace {
@@ -337,6 +339,8 @@ csa2_status_t csa2_cache_create(const csa2_config_t* cfg, int32_t batch, const i
     return CSA2_ERR_CUDA;
   }
   c->index_sms = c->num_sms;
+  c->wait_cycles = 0;
+  c->inject = 0;
   if (!mx && (!make_map(&c->tm_k, c->idxk, (uint64_t)c->total, kIdxDim, 64, 128) ||
               !make_block_map(&c->tm_k8, c->idxk, (uint64_t)c->total))) {
     delete c;
@@ -367,6 +371,19 @@ csa2_status_t csa2_cache_destroy(csa2_cache_t* c) {
 csa2_status_t csa2_cache_set_index_sms(csa2_cache_t* c, int32_t n_sms) {
   if (!c || n_sms < 0) return CSA2_ERR_INVALID_ARG;
   c->index_sms = (n_sms == 0 || n_sms > c->num_sms) ? c->num_sms : n_sms;
+  return CSA2_OK;
+}
+
+csa2_status_t csa2_cache_set_wait_limit(csa2_cache_t* c, int64_t cycles) {
+  if (!c || cycles < 0) return CSA2_ERR_INVALID_ARG;
+  c->wait_cycles = cycles;
+  return CSA2_OK;
+}
+
+csa2_status_t csa2_cache_inject_fault(csa2_cache_t* c, int32_t fault) {
+  if (!c || (fault != CSA2_FAULT_NONE && fault != CSA2_FAULT_INDEX_NO_KEY_LOADS))
+    return CSA2_ERR_INVALID_ARG;
+  c->inject = fault == CSA2_FAULT_INDEX_NO_KEY_LOADS ? kInjectNoKeyLoads : 0;
   return CSA2_OK;
 }
 
@@ -541,6 +558,8 @@ csa2_status_t run_index_decode(const csa2_cache_t* c, int32_t nq, const void* q_
     ip->n_groups = n;
     ip->prefill = 0;
     ip->ratio = c->cfg.ratio;
+    ip->wait_cycles = c->wait_cycles;
+    ip->inject = c->inject;
     ip->tile_prefix[0] = 0;
     for (int i = 0; i < n; ++i) {
       const int s = seq_ids ? seq_ids[q0 + i] : q0 + i;
@@ -721,6 +740,8 @@ csa2_status_t csa2_index_scores_prefill(const csa2_cache_t* c, int32_t seq, int3
     ip->pos0 = pos0 + q0;
     ip->pre_len = (int32_t)len;
     ip->ratio = m;
+    ip->wait_cycles = c->wait_cycles;
+    ip->inject = c->inject;
     ip->tile_prefix[0] = 0;
     for (int g = 0; g < groups; ++g) {
       const int64_t last = std::min<int64_t>((int64_t)g * kQpg + kQpg, n) - 1;
@@ -860,6 +881,7 @@ csa2_status_t csa2_sparse_attn_decode_ex(const csa2_cache_t* c, int32_t nq,
     p->scale_log2 = scale * 1.4426950408889634f;
     p->prefill = 0;
     p->splits = split ? 2 : 1;
+    p->wait_cycles = c->wait_cycles;
     if (!apply_opts(p, opts, true, q0, (int64_t)q0 * W)) { st = CSA2_ERR_INVALID_ARG; break; }
     for (int i = 0; i < n; ++i) {
       const int s = seq_ids ? seq_ids[q0 + i] : q0 + i;
@@ -931,6 +953,7 @@ csa2_status_t csa2_sparse_attn_prefill_ex(const csa2_cache_t* c, int32_t seq, in
   p->pos0 = pos0;
   p->swa_pos0 = swa_pos0;
   p->splits = 1;
+  p->wait_cycles = c->wait_cycles;
   csa2_status_t st = apply_opts(p, opts, false, 0, 0) ? CSA2_OK : CSA2_ERR_INVALID_ARG;
   CUtensorMap tm_q, tm_swa;
   if (st == CSA2_OK && !make_map(&tm_q, q, (uint64_t)nq * H, kHeadDim, 64, kAttnHeadGroup))
@@ -1115,6 +1138,8 @@ csa2_status_t csa2_index_topk_reindex_decode(const csa2_cache_t* c, int32_t nq, 
     ip->qpg = 1;
     ip->n_groups = n;
     ip->ratio = c->cfg.ratio;
+    ip->wait_cycles = c->wait_cycles;
+    ip->inject = c->inject;
     ip->tile_prefix[0] = 0;
     for (int i = 0; i < n; ++i) {
       const int s = seq_ids ? seq_ids[q0 + i] : q0 + i;

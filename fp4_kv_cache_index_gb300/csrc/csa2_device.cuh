@@ -23,8 +23,12 @@ __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bit) {
   if (err) atomicOr(err, bit);
 }
 
-// ~2^31 cycles (about one second at GB300 clocks) before a wait gives up.
+// ~2^31 cycles (about one second at GB300 clocks) before a wait gives up,
+// unless the launch sets a limit of its own (csa2_cache_set_wait_limit).
 constexpr long long kWaitCycles = 1ll << 31;
+__device__ __forceinline__ long long wait_limit(long long cycles) {
+  return cycles > 0 ? cycles : kWaitCycles;
+}
 
 // ---------------------------------------------------------------- smem / mbarrier
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -79,26 +83,28 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 }
 
 // mbar_wait for consumers that usually wait long: suspending try_wait.
-__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t* err) {
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                                long long limit = kWaitCycles) {
   if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       set_error(err, kErrTimeout);
       return false;
     }
   }
 }
 
-// Waits for the phase with the given parity; gives up after kWaitCycles,
+// Waits for the phase with the given parity; gives up after `limit` cycles,
 // records kErrTimeout and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                          long long limit = kWaitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       set_error(err, kErrTimeout);
       return false;
     }

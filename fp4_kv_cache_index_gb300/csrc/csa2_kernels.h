@@ -62,6 +62,10 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 
 // ---------------------------------------------------------------- indexer
 constexpr int kMaxIdxGroups = 1024;
+// Fault injection for tests of the timeout path: the indexer's producer
+// issues no key loads, so the MMA and epilogue waits run out with nothing in
+// flight (no copy, no MMA).
+constexpr int32_t kInjectNoKeyLoads = 1;
 struct IndexParams {
   const float* w;          // [nq, 32]
   float* scores;           // [nq, ld]
@@ -83,6 +87,8 @@ struct IndexParams {
   int64_t pos0;            // prefill: position of query 0
   int32_t pre_len;         // prefill: entries in the sequence
   int32_t ratio;
+  int64_t wait_cycles;     // bounded-wait limit in cycles (0: the default, ~2^31)
+  int32_t inject;          // kInjectNoKeyLoads: the producer issues no key loads (tests)
   int32_t tile_prefix[kMaxIdxGroups + 1];  // cumulative tiles per group (128 entries; the
                                            // MXFP4 kernel: 256 for one query per group)
   int64_t entry_base[kMaxIdxGroups];       // decode: entry offset of the group's sequence
@@ -184,6 +190,7 @@ struct AttnParams {
   const uint8_t* swa_codes;  // FP8 window rows (nullable): E4M3 codes [rows, 448]
   const uint16_t* swa_rope;  //   bf16 RoPE channels [rows, 64]
   const uint8_t* swa_scales; //   UE8M0 scales [rows, 8]
+  int64_t wait_cycles;       // bounded-wait limit in cycles (0: the default, ~2^31)
   int64_t q_base[kAttnTab];  // decode: entry offset of each query's sequence
   int32_t q_len[kAttnTab];   // decode: entries of each query's sequence
 };

@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   griddep_wait();
+  const long long wl = wait_limit(p.wait_cycles);   // bounded-wait limit (cycles)
   const int hgs = p.n_heads / kHG;
   const int split = blockIdx.x % p.splits;
   const int qh = blockIdx.x / p.splits;            // (query, head group)
@@ -424,8 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid < kRows) sm.row_valid[tid] = tid < swa_count;
       if (tid == 0) {
         for (int h = 0; h < 2; ++h) {
-          ok = mbar_wait(&sm.bar_kv[h], 0, p.err) && ok;
-          ok = mbar_wait(&sm.bar_q[h], 0, p.err) && ok;
+          ok = mbar_wait(&sm.bar_kv[h], 0, p.err, wl) && ok;
+          ok = mbar_wait(&sm.bar_q[h], 0, p.err, wl) && ok;
           tc_fence_after();
           for (int k = 0; k < 16; ++k) mma_s(16 * h + k);
         }
@@ -438,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
-          ok = mbar_wait(&sm.bar_q[h], 0, p.err) && ok;
+          ok = mbar_wait(&sm.bar_q[h], 0, p.err, wl) && ok;
           tc_fence_after();
           for (int k = 0; k < 16; ++k) mma_s(16 * h + k);
           if (h == 1) umma_commit(&sm.bar_mma);
@@ -457,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   for (int ti = 0; ti < n_tiles; ++ti) {
     // one thread polls the mbarrier, the others wait at the CTA barrier
-    if (tid == 0) ok = mbar_wait(&sm.bar_mma, ph_s, p.err) && ok;
+    if (tid == 0) ok = mbar_wait(&sm.bar_mma, ph_s, p.err, wl) && ok;
     ph_s ^= 1;
     ok = __syncthreads_and(ok);
     if (!ok) break;
@@ -570,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tile = sm.my_list[ti + 1];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        ok = mbar_wait(&sm.bar_o[h], ph_o, p.err) && ok;
+        ok = mbar_wait(&sm.bar_o[h], ph_o, p.err, wl) && ok;
         tc_fence_after();
         fill_half(tile, h);
         fence_proxy_async_smem();
@@ -589,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (after < n_tiles) prefetch_l2(sm.my_list[after]);
       }
     } else {
-      if (tid == 0) ok = mbar_wait(&sm.bar_o[1], ph_o, p.err) && ok;
+      if (tid == 0) ok = mbar_wait(&sm.bar_o[1], ph_o, p.err, wl) && ok;
       ok = __syncthreads_and(ok);
       tc_fence_after();
     }

@@ -135,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   griddep_wait();
+  const long long wl = wait_limit(p.wait_cycles);   // bounded-wait limit (cycles)
 
   const int total = p.tile_prefix[p.n_groups];
   const int begin = (int)(((int64_t)total * blockIdx.x) / gridDim.x);
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (g != cur) {
         gbase = group_base(p, g);
         if (lane == 0) {
-          ok = mbar_wait(q_empty, qph ^ 1, p.err);
+          ok = mbar_wait(q_empty, qph ^ 1, p.err, wl);
           if (ok) {
             mbar_arrive_expect_tx(q_full, (uint32_t)(qrows * kIdxDim * 2));
             tma_load_2d(qbuf, &tm_q, 0, g * qrows, q_full);
@@ -179,9 +180,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         cur = g;
       }
-      if (lane == 0) ok = mbar_wait(k_empty + stage, ph ^ 1, p.err);
+      if (lane == 0) ok = mbar_wait(k_empty + stage, ph ^ 1, p.err, wl);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
+      if (p.inject & kInjectNoKeyLoads) {   // tests: nothing arrives on k_full
+        if (++stage == kStages) { stage = 0; ph ^= 1; }
+        continue;
+      }
       uint8_t* dst = kbuf + stage * kKStageBytes;
       if (p.pool) {
         const int32_t blk = nxt;
@@ -206,8 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // make sure no bulk copy is still writing into this CTA's shared memory
     if (lane == 0) {
       for (int s = 0; s < kStages; ++s)
-        if (armed & (1u << s)) mbar_wait(k_full + s, (armed_ph >> s) & 1u, p.err);
-      if (cur >= 0) mbar_wait(q_full, qph ^ 1, p.err);
+        if (armed & (1u << s)) mbar_wait(k_full + s, (armed_ph >> s) & 1u, p.err, wl);
+      if (cur >= 0) mbar_wait(q_full, qph ^ 1, p.err, wl);
     }
     __syncwarp();
   } else if (warp == 1 && lane == 0 && begin < end) {
@@ -228,12 +233,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       gc.advance(p, it);
       const int g = gc.g;
       if (g != cur) {
-        ok = mbar_wait(q_full, qph, p.err);
+        ok = mbar_wait(q_full, qph, p.err, wl);
         qph ^= 1;
         if (!ok) break;
         cur = g;
       }
-      ok = mbar_wait(k_full + stage, ph, p.err) && mbar_wait(acc_empty + acc, aph ^ 1, p.err);
+      ok = mbar_wait(k_full + stage, ph, p.err, wl) && mbar_wait(acc_empty + acc, aph ^ 1, p.err, wl);
       if (!ok) break;
       tc_fence_after();
       const uint32_t d = tmem_base + (uint32_t)(acc * N);
@@ -252,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (++acc == nacc) { acc = 0; aph ^= 1; }
     }
     umma_commit(drain);
-    mbar_wait(drain, 0, p.err);
+    mbar_wait(drain, 0, p.err, wl);
   } else if (warp >= 2 && p.qpg == 1) {
     // ------------------------------------------------ epilogue, one query per tile
     // Two groups of four warps take alternate tiles (group gsel the tiles
@@ -299,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int a = jt & 3;
       // suspend-hinted wait: a polling epilogue warp would take issue slots
       // from the producer and MMA warps that share its scheduler
-      if (!mbar_wait_sleep(acc_full + a, (uint32_t)((jt >> 2) & 1), p.err)) break;
+      if (!mbar_wait_sleep(acc_full + a, (uint32_t)((jt >> 2) & 1), p.err, wl)) break;
       tc_fence_after();
       const int t = it - gc.lo;
       const int e = t * kTileE + row;
@@ -373,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int jj = 0; jj < kMaxHalfQ; ++jj)
           nvis[jj] = (j0 + jj < j1) ? group_nvis_query(p, g, j0 + jj) : 0;
       }
-      if (!mbar_wait(acc_full + acc, aph, p.err)) break;
+      if (!mbar_wait(acc_full + acc, aph, p.err, wl)) break;
       tc_fence_after();
       const int t = it - gc.lo;
       const int e = t * kTileE + row;

@@ -298,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   griddep_wait();
+  const long long wl = wait_limit(p.wait_cycles);   // bounded-wait limit (cycles)
 
   const int total = p.tile_prefix[p.n_groups];
   const int begin = (int)(((int64_t)total * blockIdx.x) / gridDim.x);
@@ -350,9 +351,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int it = it0 + u;
         if (it >= end || !ok) break;
         gc.advance(p, it);
-        if (lane == 0) ok = mbar_wait(k_empty + stage, ph ^ 1, p.err);
+        if (lane == 0) ok = mbar_wait(k_empty + stage, ph ^ 1, p.err, wl);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
+        if (p.inject & kInjectNoKeyLoads) {   // tests: nothing arrives on k_full
+          if (++stage == kStages) { stage = 0; ph ^= 1; }
+          continue;
+        }
         uint8_t* st = stages + stage * kStageBytes;
         const int64_t base = gc.base;
         const int32_t blk_lane = pq[u];
@@ -404,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // no bulk copy may still be writing into this CTA's shared memory
     if (lane == 0) {
       for (int s = 0; s < kStages; ++s)
-        if (armed & (1u << s)) mbar_wait(k_full + s, (armed_ph >> s) & 1u, p.err);
+        if (armed & (1u << s)) mbar_wait(k_full + s, (armed_ph >> s) & 1u, p.err, wl);
     }
     __syncwarp();
   } else if (warp >= kPrepBase / 32 && begin < end) {
@@ -419,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (gc.g == cur) continue;
       cur = gc.g;
       const int slot = gi & 1;
-      ok = mbar_wait_sleep(b_empty + slot, (uint32_t)(((gi >> 1) & 1) ^ 1), p.err);
+      ok = mbar_wait_sleep(b_empty + slot, (uint32_t)(((gi >> 1) & 1) ^ 1), p.err, wl);
       if (!ok) break;
       uint8_t* bc = bslots + slot * kBSlotBytes;
       uint8_t* ba = bc + kBRows * (kIdxDim / 2);
@@ -448,13 +453,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (changed) {
         ++gi;
         cur = gc.g;
-        ok = mbar_wait(b_full + (gi & 1), (uint32_t)((gi >> 1) & 1), p.err);
+        ok = mbar_wait(b_full + (gi & 1), (uint32_t)((gi >> 1) & 1), p.err, wl);
         if (!ok) break;
         tc_fence_after();
         uint8_t* ba = bslots + (gi & 1) * kBSlotBytes + kBRows * (kIdxDim / 2);
         tmem_cp_atom(tmem_base + kSfbCol + 4 * (gi & 1), sdesc_atom(smem_u32(ba)));
       }
-      ok = mbar_wait(k_full + stage, ph, p.err) && mbar_wait(acc_empty + acc, aph ^ 1, p.err);
+      ok = mbar_wait(k_full + stage, ph, p.err, wl) && mbar_wait(acc_empty + acc, aph ^ 1, p.err, wl);
       if (!ok) break;
       tc_fence_after();
       // the scale words arrived by generic-proxy copies; tcgen05.cp reads
@@ -486,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (++acc == nacc) { acc = 0; aph ^= 1; }
     }
     umma_commit(drain);
-    mbar_wait(drain, 0, p.err);
+    mbar_wait(drain, 0, p.err, wl);
   } else if (warp >= 2 && warp < 10) {
     // ------------------------------------------------ epilogue
     const int quad = warp & 3;                 // TMEM lane quadrant
@@ -540,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           nv[1] = group_nvis_query(p, g, 2 * half + 1);
         }
       }
-      if (!mbar_wait_sleep(acc_full + acc, aph, p.err)) break;
+      if (!mbar_wait_sleep(acc_full + acc, aph, p.err, wl)) break;
       tc_fence_after();
       const int t = it - gc.lo;
       // entry of this slot (pool mode: the pool slot)

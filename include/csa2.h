@@ -149,6 +149,25 @@ csa2_status_t csa2_cache_destroy(csa2_cache_t* cache);
  * knob of this implementation, not part of the method.                    */
 csa2_status_t csa2_cache_set_index_sms(csa2_cache_t* cache, int32_t n_sms);
 
+/* Upper bound, in SM clock cycles, on every bounded wait inside the
+ * indexer and readout kernels launched for this cache after the call
+ * (cycles = 0 restores the default of 2^31, about one second).  A wait that
+ * runs out records CSA2_ERR_TIMEOUT in the device error word, waits (within
+ * the same bound) for the copies its CTA has in flight, frees its tensor
+ * memory and ends the kernel, so the context stays usable.
+ * CSA2_ERR_INVALID_ARG for a NULL cache or cycles < 0.  The pages have no
+ * counterpart: this is a watchdog of this implementation.                 */
+csa2_status_t csa2_cache_set_wait_limit(csa2_cache_t* cache, int64_t cycles);
+
+/* Fault injection for tests of the timeout path (the pages have no
+ * counterpart).  CSA2_FAULT_INDEX_NO_KEY_LOADS: the indexers' producer warp
+ * issues no key loads, so their MMA and epilogue waits run out with no copy
+ * and no MMA in flight; the scores are then not written and the device
+ * error word reads CSA2_ERR_TIMEOUT.  CSA2_FAULT_NONE switches it off.
+ * Applies to launches made after the call.                                */
+typedef enum { CSA2_FAULT_NONE = 0, CSA2_FAULT_INDEX_NO_KEY_LOADS = 1 } csa2_fault_t;
+csa2_status_t csa2_cache_inject_fault(csa2_cache_t* cache, int32_t fault);
+
 /* Empties every sequence (host lengths and, on `stream`, device lengths). */
 csa2_status_t csa2_cache_reset(csa2_cache_t* cache, csa2_stream_t stream);
 

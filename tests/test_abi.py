@@ -89,3 +89,5 @@ def test_host_argument_errors(lib):
                                      None, 0, None) == 1
     st = ctypes.c_int32()
     assert L.csa2_get_device_error(None, None, ctypes.byref(st)) == 1
+    assert L.csa2_cache_set_wait_limit(None, 100) == 1
+    assert L.csa2_cache_inject_fault(None, 0) == 1
