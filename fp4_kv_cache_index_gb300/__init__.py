@@ -19,7 +19,10 @@ from typing import Optional, Sequence
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libcsa2.so")
+# CSA2_DEBUG=1 loads the bounds-checked build (libcsa2_debug.so, built by
+# _build.build(debug=True)); otherwise the normal one.
+LIB_PATH = os.path.join(_HERE, "libcsa2_debug.so" if os.environ.get("CSA2_DEBUG") == "1"
+                        else "libcsa2.so")
 
 CSA2_KV_L32_UE8M0 = 0
 CSA2_KV_L16_E4M3 = 1

@@ -1,4 +1,7 @@
-"""Builds the CSA2 CUDA library (libcsa2.so) in-tree with nvcc for sm_103a."""
+"""Builds the CSA2 CUDA library (libcsa2.so) in-tree with nvcc for sm_103a,
+and on request its bounds-checked variant (libcsa2_debug.so, -DCSA2_DEBUG:
+every checked index outside its buffer is recorded in the device error word
+and the access skipped)."""
 from __future__ import annotations
 
 import concurrent.futures as cf
@@ -12,6 +15,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libcsa2.so")
+DEBUG_BUILD = os.path.join(ROOT, "_build_debug")
+DEBUG_LIB = os.path.join(PKG, "libcsa2_debug.so")
 SOURCES = ["csa2_api.cu", "k_append.cu", "k_index.cu", "k_index_fp4.cu", "k_topk.cu", "k_attn.cu",
            "k_hsi.cu", "k_swa.cu"]
 HEADERS = ["csa2_device.cuh", "csa2_kernels.h"]
@@ -41,14 +46,16 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          debug: bool = False) -> str:
+    bdir, lib = (DEBUG_BUILD, DEBUG_LIB) if debug else (BUILD, LIB)
+    os.makedirs(bdir, exist_ok=True)
     headers = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "csa2.h")]
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + (["-DCSA2_DEBUG"] if debug else [])
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(bdir, src.replace(".cu", ".o"))
         if force or ptxas_info or _stale(o, [s] + headers):
             jobs.append([nvcc(), *_flags(extra), "-c", s, "-o", o])
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
@@ -58,16 +65,16 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             print(r.stdout + r.stderr)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    objs = [os.path.join(BUILD, s.replace(".cu", ".o")) for s in SOURCES]
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".{os.getpid()}.tmp"
+    objs = [os.path.join(bdir, s.replace(".cu", ".o")) for s in SOURCES]
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".{os.getpid()}.tmp"
         cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
                "-Xlinker", "-rpath", "-Xlinker", cuda_lib_dir()]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 def build_synth(force: bool = False) -> str:

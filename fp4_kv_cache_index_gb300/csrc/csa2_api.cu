@@ -8,8 +8,22 @@
 #include <new>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "csa2.h"
 #include "csa2_kernels.h"
+
+namespace {
+// One NVTX range per C call, named after the call (shows in Nsight
+// timelines; without an attached tool the push and pop return at once).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+}  // namespace
+#define CSA2_RANGE() NvtxRange csa2_nvtx_range_(__func__)
 
 // Scratch of csa2_index_topk_decode_static, for callers that cannot allocate:
 // a fixed array in the library's device image (one per GPU that loads it).
@@ -238,6 +252,8 @@ csa2_status_t run_append(csa2_cache* c, int mode, int32_t n_seqs, const int32_t*
     p.idx_codes = c->idx_codes;
     p.idx_scales = c->idx_scales;
     p.d_len = c->d_len;
+    p.total = c->total;
+    p.err = c->d_err;
     int64_t rows = 0;
     while (i < n_seqs && p.n_segs < kMaxAppendSegs) {
       const int32_t s = seq_ids[i];
@@ -295,6 +311,7 @@ size_t csa2_cache_bytes(const csa2_config_t* cfg, int32_t batch, const int64_t* 
 csa2_status_t csa2_cache_create(const csa2_config_t* cfg, int32_t batch, const int64_t* capacity,
                                 void* dev_mem, size_t bytes, csa2_stream_t stream,
                                 csa2_cache_t** out) {
+  CSA2_RANGE();
   if (!out) return CSA2_ERR_INVALID_ARG;
   *out = nullptr;
   csa2_status_t st = check_cfg(cfg);
@@ -363,24 +380,28 @@ csa2_status_t csa2_cache_create(const csa2_config_t* cfg, int32_t batch, const i
 }
 
 csa2_status_t csa2_cache_destroy(csa2_cache_t* c) {
+  CSA2_RANGE();
   if (!c) return CSA2_ERR_INVALID_ARG;
   delete c;
   return CSA2_OK;
 }
 
 csa2_status_t csa2_cache_set_index_sms(csa2_cache_t* c, int32_t n_sms) {
+  CSA2_RANGE();
   if (!c || n_sms < 0) return CSA2_ERR_INVALID_ARG;
   c->index_sms = (n_sms == 0 || n_sms > c->num_sms) ? c->num_sms : n_sms;
   return CSA2_OK;
 }
 
 csa2_status_t csa2_cache_set_wait_limit(csa2_cache_t* c, int64_t cycles) {
+  CSA2_RANGE();
   if (!c || cycles < 0) return CSA2_ERR_INVALID_ARG;
   c->wait_cycles = cycles;
   return CSA2_OK;
 }
 
 csa2_status_t csa2_cache_inject_fault(csa2_cache_t* c, int32_t fault) {
+  CSA2_RANGE();
   if (!c || (fault != CSA2_FAULT_NONE && fault != CSA2_FAULT_INDEX_NO_KEY_LOADS))
     return CSA2_ERR_INVALID_ARG;
   c->inject = fault == CSA2_FAULT_INDEX_NO_KEY_LOADS ? kInjectNoKeyLoads : 0;
@@ -388,18 +409,21 @@ csa2_status_t csa2_cache_inject_fault(csa2_cache_t* c, int32_t fault) {
 }
 
 csa2_status_t csa2_cache_reset(csa2_cache_t* c, csa2_stream_t stream) {
+  CSA2_RANGE();
   if (!c) return CSA2_ERR_INVALID_ARG;
   std::fill(c->len.begin(), c->len.end(), 0);
   return cuda_status(cudaMemsetAsync(c->d_len, 0, sizeof(int32_t) * c->batch, S(stream)));
 }
 
 csa2_status_t csa2_cache_length(const csa2_cache_t* c, int32_t seq, int64_t* n) {
+  CSA2_RANGE();
   if (!c || !n || seq < 0 || seq >= c->batch) return CSA2_ERR_INVALID_ARG;
   *n = c->len[seq];
   return CSA2_OK;
 }
 
 csa2_status_t csa2_cache_views(const csa2_cache_t* c, csa2_cache_views_t* v) {
+  CSA2_RANGE();
   if (!c || !v) return CSA2_ERR_INVALID_ARG;
   v->codes = c->codes;
   v->scales = c->scales;
@@ -416,6 +440,7 @@ csa2_status_t csa2_cache_views(const csa2_cache_t* c, csa2_cache_views_t* v) {
 
 csa2_status_t csa2_compress(int32_t ratio, int64_t n_out, int32_t dim, const void* c_tok,
                             const float* z_tok, float* out, csa2_stream_t stream) {
+  CSA2_RANGE();
   if (ratio < 1 || ratio > 16 || n_out < 0 || dim <= 0 || dim % 16 != 0 || dim > kHeadDim)
     return ratio > 16 || dim > kHeadDim ? CSA2_ERR_UNSUPPORTED : CSA2_ERR_INVALID_ARG;
   if (n_out == 0) return CSA2_OK;
@@ -438,6 +463,7 @@ csa2_status_t csa2_compress(int32_t ratio, int64_t n_out, int32_t dim, const voi
 csa2_status_t csa2_append_entries(csa2_cache_t* c, int32_t n_seqs, const int32_t* seq_ids,
                                   const int32_t* n_new, const float* entries, const void* idx_k,
                                   csa2_stream_t stream) {
+  CSA2_RANGE();
   return run_append(c, 1, n_seqs, seq_ids, n_new, entries, nullptr, nullptr, idx_k, nullptr,
                     stream);
 }
@@ -445,6 +471,7 @@ csa2_status_t csa2_append_entries(csa2_cache_t* c, int32_t n_seqs, const int32_t
 csa2_status_t csa2_append_tokens(csa2_cache_t* c, int32_t n_seqs, const int32_t* seq_ids,
                                  const int32_t* n_tok, const void* c_tok, const float* z_tok,
                                  const void* idx_k, float* entries_out, csa2_stream_t stream) {
+  CSA2_RANGE();
   return run_append(c, 2, n_seqs, seq_ids, n_tok, nullptr, c_tok, z_tok, idx_k, entries_out,
                     stream);
 }
@@ -513,6 +540,7 @@ extern "C" {
 csa2_status_t csa2_topk(int32_t n_rows, const float* scores, int64_t ld, const int64_t* n_valid,
                         int32_t k, const uint32_t* key_hist, int32_t* idx_out, float* score_out,
                         void* workspace, size_t ws_bytes, csa2_stream_t stream) {
+  CSA2_RANGE();
   return topk_impl(n_rows, scores, ld, n_valid, k, key_hist, idx_out, score_out, workspace,
                    ws_bytes, stream, false);
 }
@@ -521,6 +549,7 @@ csa2_status_t csa2_topk_bf16(int32_t n_rows, const uint16_t* scores, int64_t ld,
                              const int64_t* n_valid, int32_t k, const uint32_t* key_hist,
                              int32_t* idx_out, float* score_out, void* workspace, size_t ws_bytes,
                              csa2_stream_t stream) {
+  CSA2_RANGE();
   return topk_impl(n_rows, scores, ld, n_valid, k, key_hist, idx_out, score_out, workspace,
                    ws_bytes, stream, true);
 }
@@ -602,6 +631,7 @@ extern "C" {
 csa2_status_t csa2_index_scores_decode(const csa2_cache_t* c, int32_t nq, const void* q_idx,
                                        const float* w, const int32_t* seq_ids, float* scores,
                                        int64_t ld, uint32_t* key_hist, csa2_stream_t stream) {
+  CSA2_RANGE();
   if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
   if (nq == 0) return CSA2_OK;
   csa2_status_t st = check_decode_queries(c, nq, q_idx, w, seq_ids);
@@ -658,6 +688,7 @@ csa2_status_t index_topk_decode_impl(const csa2_cache_t* c, int32_t nq, const vo
                          : nullptr;
     tp->n_seg = use_seg ? topk_segments(c->max_cap) : 0;
     tp->formula = 0;
+    tp->err = c->d_err;
     for (int i = 0; i < n; ++i) tp->n_valid[i] = c->len[seq_ids ? seq_ids[q0 + i] : q0 + i];
     if (launch_topk(*tp, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
   }
@@ -673,6 +704,7 @@ csa2_status_t csa2_index_topk_decode(const csa2_cache_t* c, int32_t nq, const vo
                                      const float* w, const int32_t* seq_ids, int32_t* topk_idx,
                                      float* topk_score, void* workspace, size_t ws_bytes,
                                      csa2_stream_t stream) {
+  CSA2_RANGE();
   return index_topk_decode_impl(c, nq, q_idx, w, seq_ids, topk_idx, topk_score, workspace,
                                 ws_bytes, stream, false);
 }
@@ -681,6 +713,7 @@ csa2_status_t csa2_index_topk_decode_bf16(const csa2_cache_t* c, int32_t nq, con
                                           const float* w, const int32_t* seq_ids,
                                           int32_t* topk_idx, float* topk_score, void* workspace,
                                           size_t ws_bytes, csa2_stream_t stream) {
+  CSA2_RANGE();
   return index_topk_decode_impl(c, nq, q_idx, w, seq_ids, topk_idx, topk_score, workspace,
                                 ws_bytes, stream, true);
 }
@@ -689,6 +722,7 @@ csa2_status_t csa2_index_scores_decode_bf16(const csa2_cache_t* c, int32_t nq, c
                                             const float* w, const int32_t* seq_ids,
                                             uint16_t* scores, int64_t ld, uint32_t* key_hist,
                                             csa2_stream_t stream) {
+  CSA2_RANGE();
   if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
   if (nq == 0) return CSA2_OK;
   csa2_status_t st = check_decode_queries(c, nq, q_idx, w, seq_ids);
@@ -707,6 +741,7 @@ csa2_status_t csa2_index_scores_decode_bf16(const csa2_cache_t* c, int32_t nq, c
 csa2_status_t csa2_index_scores_prefill(const csa2_cache_t* c, int32_t seq, int32_t nq,
                                         int64_t pos0, const void* q_idx, const float* w,
                                         float* scores, int64_t ld, csa2_stream_t stream) {
+  CSA2_RANGE();
   if (!c || nq < 0 || seq < 0 || seq >= c->batch || pos0 < 0) return CSA2_ERR_INVALID_ARG;
   if (nq == 0) return CSA2_OK;
   if (!q_idx || !w || !scores || !aligned16(q_idx) || !aligned16(w) || !aligned16(scores) ||
@@ -768,6 +803,7 @@ csa2_status_t csa2_index_topk_prefill(const csa2_cache_t* c, int32_t seq, int32_
                                       const void* q_idx, const float* w, int32_t* topk_idx,
                                       float* topk_score, void* workspace, size_t ws_bytes,
                                       csa2_stream_t stream) {
+  CSA2_RANGE();
   if (!c || nq < 0 || seq < 0 || seq >= c->batch || pos0 < 0) return CSA2_ERR_INVALID_ARG;
   if (nq == 0) return CSA2_OK;
   if (!topk_idx || !workspace || !aligned16(workspace)) return CSA2_ERR_INVALID_ARG;
@@ -785,6 +821,7 @@ csa2_status_t csa2_index_topk_prefill(const csa2_cache_t* c, int32_t seq, int32_
   tp->idx_out = topk_idx;
   tp->score_out = topk_score;
   tp->formula = 1;
+  tp->err = c->d_err;
   tp->pre_len = (int32_t)c->len[seq];
   tp->ratio = c->cfg.ratio;
   tp->pos0 = pos0;
@@ -833,6 +870,7 @@ csa2_status_t csa2_sparse_attn_decode(const csa2_cache_t* c, int32_t nq, const i
                                       const void* q, const void* swa_kv, const int32_t* swa_len,
                                       const int32_t* topk_idx, float scale, void* out, float* lse,
                                       void* workspace, size_t ws_bytes, csa2_stream_t stream) {
+  CSA2_RANGE();
   return csa2_sparse_attn_decode_ex(c, nq, seq_ids, q, swa_kv, swa_len, topk_idx, scale, out, lse,
                                     workspace, ws_bytes, nullptr, stream);
 }
@@ -843,6 +881,7 @@ csa2_status_t csa2_sparse_attn_decode_ex(const csa2_cache_t* c, int32_t nq,
                                          const int32_t* topk_idx, float scale, void* out,
                                          float* lse, void* workspace, size_t ws_bytes,
                                          const csa2_attn_opts_t* opts, csa2_stream_t stream) {
+  CSA2_RANGE();
   if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
   if (nq == 0) return CSA2_OK;
   const int W = c->cfg.swa;
@@ -908,6 +947,7 @@ csa2_status_t csa2_sparse_attn_prefill(const csa2_cache_t* c, int32_t seq, int32
                                        int64_t swa_pos0, int64_t n_swa_rows,
                                        const int32_t* topk_idx, float scale, void* out, float* lse,
                                        csa2_stream_t stream) {
+  CSA2_RANGE();
   return csa2_sparse_attn_prefill_ex(c, seq, nq, pos0, q, swa_kv, swa_pos0, n_swa_rows, topk_idx,
                                      scale, out, lse, nullptr, stream);
 }
@@ -918,6 +958,7 @@ csa2_status_t csa2_sparse_attn_prefill_ex(const csa2_cache_t* c, int32_t seq, in
                                           const int32_t* topk_idx, float scale, void* out,
                                           float* lse, const csa2_attn_opts_t* opts,
                                           csa2_stream_t stream) {
+  CSA2_RANGE();
   if (!c || nq < 0 || seq < 0 || seq >= c->batch || pos0 < 0) return CSA2_ERR_INVALID_ARG;
   if (nq == 0) return CSA2_OK;
   const int W = c->cfg.swa;
@@ -990,6 +1031,7 @@ csa2_status_t csa2_index_topk_decode_static(const csa2_cache_t* c, int32_t nq, c
                                             const float* w, const int32_t* seq_ids,
                                             int32_t* topk_idx, float* topk_score,
                                             csa2_stream_t stream) {
+  CSA2_RANGE();
   if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
   if (nq == 0) return CSA2_OK;
   csa2_status_t st = check_decode_queries(c, nq, q_idx, w, seq_ids);
@@ -1020,6 +1062,7 @@ csa2_status_t csa2_index_topk_decode_static(const csa2_cache_t* c, int32_t nq, c
     tp.seg_ws = nullptr;   // one CTA per row: no segment scratch
     tp.n_seg = 0;
     tp.formula = 0;
+    tp.err = c->d_err;
     for (int i = 0; i < n; ++i) tp.n_valid[i] = c->len[seq_ids ? seq_ids[q0 + i] : q0 + i];
     if (launch_topk(tp, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
   }
@@ -1040,6 +1083,7 @@ csa2_status_t csa2_hsi_pool(int32_t n_rows, const float* scores, int64_t ld,
                             const int64_t* n_valid, int32_t block, int32_t max_blocks,
                             int32_t* pool_blocks, void* workspace, size_t ws_bytes,
                             csa2_stream_t stream) {
+  CSA2_RANGE();
   if (n_rows < 0 || ld < 0) return CSA2_ERR_INVALID_ARG;
   if (block != kHsiBlock || max_blocks <= 0 || max_blocks % 16 != 0 || max_blocks > 4096)
     return CSA2_ERR_UNSUPPORTED;
@@ -1099,6 +1143,7 @@ csa2_status_t csa2_index_topk_reindex_decode(const csa2_cache_t* c, int32_t nq, 
                                              int32_t* topk_idx, float* topk_score,
                                              void* workspace, size_t ws_bytes,
                                              csa2_stream_t stream) {
+  CSA2_RANGE();
   if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
   if (max_blocks <= 0 || max_blocks % 16 != 0 || max_blocks > 4096) return CSA2_ERR_UNSUPPORTED;
   if (nq == 0) return CSA2_OK;
@@ -1170,6 +1215,7 @@ csa2_status_t csa2_index_topk_reindex_decode(const csa2_cache_t* c, int32_t nq, 
     tp->seg_ws = seg_ws + (size_t)q0 * topk_seg_bytes(1, slots) / sizeof(uint32_t);
     tp->n_seg = topk_segments(slots);
     tp->formula = 0;
+    tp->err = c->d_err;
     for (int i = 0; i < n; ++i) tp->n_valid[i] = slots;
     if (launch_topk(*tp, S(stream)) != cudaSuccess) { st = CSA2_ERR_CUDA; break; }
     // ---- pool slots back to entry indices
@@ -1181,6 +1227,7 @@ csa2_status_t csa2_index_topk_reindex_decode(const csa2_cache_t* c, int32_t nq, 
     hp->pool_blocks = max_blocks;
     hp->out = topk_idx + (int64_t)q0 * k;
     hp->score_out = tp->score_out;
+    hp->err = c->d_err;
     for (int i = 0; i < n; ++i) hp->n[i] = ip->nvis[i];
     if (launch_pool_map(*hp, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
   }
@@ -1192,6 +1239,7 @@ csa2_status_t csa2_index_topk_reindex_decode(const csa2_cache_t* c, int32_t nq, 
 
 csa2_status_t csa2_swa_fp8_quantise(int64_t n_rows, const void* rows, uint8_t* codes, void* rope,
                                     uint8_t* scales, csa2_stream_t stream) {
+  CSA2_RANGE();
   if (n_rows < 0) return CSA2_ERR_INVALID_ARG;
   if (n_rows == 0) return CSA2_OK;
   if (!rows || !codes || !rope || !scales || !aligned16(rows) || !aligned16(codes) ||
@@ -1203,6 +1251,7 @@ csa2_status_t csa2_swa_fp8_quantise(int64_t n_rows, const void* rows, uint8_t* c
 
 csa2_status_t csa2_get_device_error(const csa2_cache_t* c, csa2_stream_t stream,
                                     int32_t* device_status) {
+  CSA2_RANGE();
   if (!c || !device_status) return CSA2_ERR_INVALID_ARG;
   uint32_t word = 0;
   if (cudaMemcpyAsync(&word, c->d_err, sizeof(word), cudaMemcpyDeviceToHost, S(stream)) !=

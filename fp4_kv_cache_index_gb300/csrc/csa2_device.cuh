@@ -23,6 +23,17 @@ __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bit) {
   if (err) atomicOr(err, bit);
 }
 
+// Bounds checks of the CSA2_DEBUG build (libcsa2_debug.so): a computed index
+// that falls outside its buffer records kErrIndex in the device error word
+// and the access is skipped.  In the normal build the check is `true` and
+// compiles away.
+#ifdef CSA2_DEBUG
+#define CSA2_IN_BOUNDS(cond, err) \
+  ((cond) ? true : (::csa2::set_error((err), ::csa2::kErrIndex), false))
+#else
+#define CSA2_IN_BOUNDS(cond, err) true
+#endif
+
 // ~2^31 cycles (about one second at GB300 clocks) before a wait gives up,
 // unless the launch sets a limit of its own (csa2_cache_set_wait_limit).
 constexpr long long kWaitCycles = 1ll << 31;

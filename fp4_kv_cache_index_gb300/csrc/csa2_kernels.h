@@ -57,6 +57,8 @@ struct AppendParams {
   uint8_t* idx_codes;
   uint8_t* idx_scales;
   int32_t* d_len;
+  int64_t total;             // cache rows (bounds checks of the debug build)
+  uint32_t* err;             // nullable device error word
 };
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 
@@ -127,6 +129,7 @@ struct HsiParams {
   int32_t pool_blocks;
   int32_t* out;
   float* score_out;          // nullable: zeroed where out is -1
+  uint32_t* err;             // nullable device error word (debug-build checks)
   int64_t n[1024];
 };
 constexpr int kHsiTab = 1024;
@@ -151,6 +154,7 @@ struct TopkParams {
   int32_t score_bf16;        // 1: scores are bf16 (uint16 [rows, ld])
   uint32_t* seg_ws;          // nullable: per-segment candidate buffers (see topk_seg_bytes)
   int32_t n_seg;             // segments per row when seg_ws is set
+  uint32_t* err;             // nullable device error word (debug-build checks)
   int64_t n_valid[kTopkTab]; // formula == 0: per-row valid counts
 };
 // Segmented candidate compaction (rows with a score-key histogram): scratch

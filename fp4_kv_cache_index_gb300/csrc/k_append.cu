@@ -77,6 +77,7 @@ __global__ void __launch_bounds__(256) k_append(const __grid_constant__ AppendPa
   const int dim = p.dim;
   const int c0 = lane * 16;
   if (c0 >= dim) return;
+  if (p.mode != 0 && !CSA2_IN_BOUNDS(dst >= 0 && dst < p.total, p.err)) return;
 
   float x[16];
   if (p.mode == 1) {

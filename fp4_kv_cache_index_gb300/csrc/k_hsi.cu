@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(256) k_block_max(const __grid_constant__ HsiPa
     } else {
       for (int i = 0; i < kHsiBlock && e0 + i < n; ++i) m = fmaxf(m, __ldg(row + e0 + i));
     }
-    p.bmax[(int64_t)r * p.ld_b + b] = m;
+    if (CSA2_IN_BOUNDS(b < p.ld_b, p.err)) p.bmax[(int64_t)r * p.ld_b + b] = m;
   }
 }
 

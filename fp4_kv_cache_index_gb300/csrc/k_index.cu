@@ -319,9 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.pool) {
         const int64_t ent = (int64_t)blk * 8 + (row & 7);
         const float v = (blk >= 0 && ent < nvis) ? s : -INFINITY;
-        p.scores[(int64_t)g * p.ld + e] = v;
-        if (use_hist) atomicAdd(hsg + (score_key(v) >> 21), 1u);
-      } else if (g < p.nq && e < nvis) {
+        if (CSA2_IN_BOUNDS(e < p.ld, p.err)) {
+          p.scores[(int64_t)g * p.ld + e] = v;
+          if (use_hist) atomicAdd(hsg + (score_key(v) >> 21), 1u);
+        }
+      } else if (g < p.nq && e < nvis && CSA2_IN_BOUNDS(e < p.ld, p.err)) {
         if (p.score_bf16) {
           const uint32_t b = float_to_bf16_bits(s);
           reinterpret_cast<uint16_t*>(p.scores)[(int64_t)g * p.ld + e] = (uint16_t)b;
@@ -396,9 +398,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           // slot t * 128 + row of the pool; its entry decides validity
           const int64_t ent = (int64_t)blk * 8 + (row & 7);
           const float v = (blk >= 0 && ent < nv) ? s : -INFINITY;
-          p.scores[(int64_t)q * p.ld + e] = v;
-          if (use_hist) atomicAdd(hs + (score_key(v) >> 21), 1u);
-        } else if (q < p.nq && e < nv) {
+          if (CSA2_IN_BOUNDS(e < p.ld, p.err)) {
+            p.scores[(int64_t)q * p.ld + e] = v;
+            if (use_hist) atomicAdd(hs + (score_key(v) >> 21), 1u);
+          }
+        } else if (q < p.nq && e < nv && CSA2_IN_BOUNDS(e < p.ld, p.err)) {
           if (p.score_bf16) {
             // the selector's precision: nearest bf16, its key histogrammed
             const uint32_t b = float_to_bf16_bits(s);

@@ -568,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             p.scores[(int64_t)q * p.ld + e] = v;
             if (use_hist) atomicAdd(hs + (score_key(v) >> 21), 1u);
           }
-        } else if (q < p.nq && e >= 0 && e < nvis) {
+        } else if (q < p.nq && e >= 0 && e < nvis && CSA2_IN_BOUNDS(e < p.ld, p.err)) {
           if (p.score_bf16) {
             const uint32_t bb = float_to_bf16_bits(s);
             reinterpret_cast<uint16_t*>(p.scores)[(int64_t)q * p.ld + e] = (uint16_t)bb;

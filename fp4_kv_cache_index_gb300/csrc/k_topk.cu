@@ -459,8 +459,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
       const bool is_gt = key > T, is_eq = key == T;
       if (is_gt || (is_eq && q_before < need_eq)) {
         const uint32_t pos = g_before + (q_before < need_eq ? q_before : need_eq);
-        orow[pos] = sh.u.cand.idx[i];
-        if (osc) osc[pos] = key_score(key);
+        if (CSA2_IN_BOUNDS(pos >= 0 && pos < k, p.err)) {
+          orow[pos] = sh.u.cand.idx[i];
+          if (osc) osc[pos] = key_score(key);
+        }
       }
       g_before += is_gt;
       q_before += is_eq;
@@ -530,8 +532,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
       const bool is_gt = key[i] > T, is_eq = key[i] == T;
       if (is_gt || (is_eq && q_before < need_eq)) {
         const uint32_t pos = g_before + (q_before < need_eq ? q_before : need_eq);
-        orow[pos] = (int32_t)(e + i);
-        if (osc) osc[pos] = key_score(key[i]);
+        if (CSA2_IN_BOUNDS(pos >= 0 && pos < k && e + i < n, p.err)) {
+          orow[pos] = (int32_t)(e + i);
+          if (osc) osc[pos] = key_score(key[i]);
+        }
       }
       g_before += is_gt;
       q_before += is_eq;

@@ -91,3 +91,13 @@ def test_host_argument_errors(lib):
     assert L.csa2_get_device_error(None, None, ctypes.byref(st)) == 1
     assert L.csa2_cache_set_wait_limit(None, 100) == 1
     assert L.csa2_cache_inject_fault(None, 0) == 1
+
+
+def test_every_entry_point_opens_an_nvtx_range():
+    """Each C call that can launch or touch the device is wrapped in an NVTX
+    range named after it (CSA2_RANGE as its first statement)."""
+    src = open(os.path.join(ROOT, "fp4_kv_cache_index_gb300", "csrc", "csa2_api.cu")).read()
+    defs = re.findall(r"\ncsa2_status_t (csa2_\w+)\([^)]*\)\s*\{\n(.*)\n", src)
+    assert len(defs) >= 25
+    for name, first in defs:
+        assert first.strip() == "CSA2_RANGE();", name
