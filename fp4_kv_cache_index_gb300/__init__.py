@@ -96,6 +96,7 @@ def _load():
         "csa2_index_topk_decode": ([P, i32, P, P, P, P, P, P, sz, P], i32),
         "csa2_index_topk_prefill": ([P, i32, i32, i64, P, P, P, P, P, sz, P], i32),
         "csa2_index_topk_decode_static": ([P, i32, P, P, P, P, P, P], i32),
+        "csa2_index_topk": ([P, i32, P, P, P, P, P, P, P, sz, P], i32),
         "csa2_index_scores_prefill": ([P, i32, i32, i64, P, P, P, i64, P], i32),
         "csa2_index_scores_decode_bf16": ([P, i32, P, P, P, P, i64, P, P], i32),
         "csa2_topk_bf16": ([i32, P, i64, P, i32, P, P, P, P, sz, P], i32),
@@ -300,6 +301,25 @@ def csa2_index_topk_decode(cache: Cache, q_idx: torch.Tensor, w: torch.Tensor,
                                       _i32_array(seq_ids), _ptr(topk_idx), _ptr(topk_score),
                                       _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "csa2_index_topk_decode")
+    return topk_idx
+
+
+def csa2_index_topk(cache: Cache, q_idx: torch.Tensor, w: torch.Tensor,
+                    seq_of_q: Optional[Sequence[int]], q_pos: Sequence[int],
+                    topk_idx: Optional[torch.Tensor] = None,
+                    topk_score: Optional[torch.Tensor] = None,
+                    workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Selection for queries at token positions q_pos of sequences seq_of_q
+    (host lists; seq_of_q None: query i reads sequence i)."""
+    nq = q_idx.shape[0]
+    dev = q_idx.device
+    if topk_idx is None:
+        topk_idx = torch.empty(nq, cache.cfg.topk, dtype=torch.int32, device=dev)
+    ws = _workspace(csa2_index_workspace_bytes(cache, nq), dev, workspace)
+    _check(lib.csa2_index_topk(cache.handle, nq, _ptr(q_idx), _ptr(w), _i32_array(seq_of_q),
+                               _i64_array(q_pos), _ptr(topk_idx), _ptr(topk_score), _ptr(ws),
+                               ws.numel() * ws.element_size(), _stream(stream)),
+           "csa2_index_topk")
     return topk_idx
 
 

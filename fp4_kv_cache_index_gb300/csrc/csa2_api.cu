@@ -560,10 +560,18 @@ namespace {
 
 // Scores of decode queries [q0, q0 + n) into scores (row stride ld): one
 // indexer launch per chunk of up to kMaxIdxGroups queries.
+// Entries query i sees: its sequence's appended entries, or with a token
+// position those causally visible there, (s + 1) * ratio - 1 <= pos.
+int64_t visible_of(const csa2_cache_t* c, int32_t s, const int64_t* q_pos, int i) {
+  const int64_t len = c->len[s];
+  if (!q_pos) return len;
+  return std::min<int64_t>(len, (q_pos[i] + 1) / c->cfg.ratio);
+}
+
 csa2_status_t run_index_decode(const csa2_cache_t* c, int32_t nq, const void* q_idx,
                                const float* w, const int32_t* seq_ids, void* scores, int64_t ld,
                                uint32_t* key_hist, csa2_stream_t stream, IndexParams* ip,
-                               bool bf16 = false) {
+                               bool bf16 = false, const int64_t* q_pos = nullptr) {
   const size_t esz = bf16 ? 2 : 4;
   const uint16_t* qb = static_cast<const uint16_t*>(q_idx);
   if (key_hist &&
@@ -592,7 +600,7 @@ csa2_status_t run_index_decode(const csa2_cache_t* c, int32_t nq, const void* q_
     ip->tile_prefix[0] = 0;
     for (int i = 0; i < n; ++i) {
       const int s = seq_ids ? seq_ids[q0 + i] : q0 + i;
-      const int64_t nv = c->len[s];
+      const int64_t nv = visible_of(c, s, q_pos, q0 + i);
       ip->entry_base[i] = c->off[s];
       ip->nvis[i] = (int32_t)nv;
       // MXFP4 decode tiles start at an even key row (one row early when the
@@ -653,11 +661,15 @@ namespace {
 csa2_status_t index_topk_decode_impl(const csa2_cache_t* c, int32_t nq, const void* q_idx,
                                      const float* w, const int32_t* seq_ids, int32_t* topk_idx,
                                      float* topk_score, void* workspace, size_t ws_bytes,
-                                     csa2_stream_t stream, bool bf16) {
+                                     csa2_stream_t stream, bool bf16,
+                                     const int64_t* q_pos = nullptr) {
   if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
   if (nq == 0) return CSA2_OK;
   csa2_status_t st = check_decode_queries(c, nq, q_idx, w, seq_ids);
   if (st != CSA2_OK) return st;
+  if (q_pos)
+    for (int i = 0; i < nq; ++i)
+      if (q_pos[i] < 0) return CSA2_ERR_INVALID_ARG;
   if (!topk_idx || !workspace || !aligned16(workspace)) return CSA2_ERR_INVALID_ARG;
   if (ws_bytes < csa2_index_workspace_bytes(c, nq)) return CSA2_ERR_CAPACITY;
   // bf16 rows: a multiple of 8 scores keeps every row 16-byte aligned (and
@@ -670,7 +682,7 @@ csa2_status_t index_topk_decode_impl(const csa2_cache_t* c, int32_t nq, const vo
   IndexParams* ip = new (std::nothrow) IndexParams();
   TopkParams* tp = new (std::nothrow) TopkParams();
   if (!ip || !tp) { delete ip; delete tp; return CSA2_ERR_OOM; }
-  st = run_index_decode(c, nq, q_idx, w, seq_ids, scores, ld, key_hist, stream, ip, bf16);
+  st = run_index_decode(c, nq, q_idx, w, seq_ids, scores, ld, key_hist, stream, ip, bf16, q_pos);
   const int k = c->cfg.topk;
   for (int q0 = 0; q0 < nq && st == CSA2_OK; q0 += kTopkTab) {
     const int n = std::min(kTopkTab, nq - q0);
@@ -689,7 +701,8 @@ csa2_status_t index_topk_decode_impl(const csa2_cache_t* c, int32_t nq, const vo
     tp->n_seg = use_seg ? topk_segments(c->max_cap) : 0;
     tp->formula = 0;
     tp->err = c->d_err;
-    for (int i = 0; i < n; ++i) tp->n_valid[i] = c->len[seq_ids ? seq_ids[q0 + i] : q0 + i];
+    for (int i = 0; i < n; ++i)
+      tp->n_valid[i] = visible_of(c, seq_ids ? seq_ids[q0 + i] : q0 + i, q_pos, q0 + i);
     if (launch_topk(*tp, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
   }
   delete ip;
@@ -707,6 +720,16 @@ csa2_status_t csa2_index_topk_decode(const csa2_cache_t* c, int32_t nq, const vo
   CSA2_RANGE();
   return index_topk_decode_impl(c, nq, q_idx, w, seq_ids, topk_idx, topk_score, workspace,
                                 ws_bytes, stream, false);
+}
+
+csa2_status_t csa2_index_topk(const csa2_cache_t* c, int32_t nq, const void* q_idx,
+                              const float* w, const int32_t* seq_of_q, const int64_t* q_pos,
+                              int32_t* topk_idx, float* topk_score, void* workspace,
+                              size_t ws_bytes, csa2_stream_t stream) {
+  CSA2_RANGE();
+  if (!q_pos) return CSA2_ERR_INVALID_ARG;
+  return index_topk_decode_impl(c, nq, q_idx, w, seq_of_q, topk_idx, topk_score, workspace,
+                                ws_bytes, stream, false, q_pos);
 }
 
 csa2_status_t csa2_index_topk_decode_bf16(const csa2_cache_t* c, int32_t nq, const void* q_idx,
@@ -1011,20 +1034,30 @@ csa2_status_t csa2_sparse_attn_prefill_ex(const csa2_cache_t* c, int32_t seq, in
   return st;
 }
 
-// Device address of g_static_scratch on the current device, looked up once
-// per device (host code cannot use the symbol itself as a device pointer).
-static void* static_scratch_ptr() {
+// Device address of g_static_scratch for the current device (host code
+// cannot use the symbol itself as a device pointer).  It is looked up again
+// on every call made while `stream` is not being captured, so a new context
+// (after a device reset) gets its own address; a call during a capture uses
+// the address the last uncaptured call found and is refused with
+// CSA2_ERR_UNSUPPORTED when there is none (the lookup may load the module,
+// which a capture must not contain).
+static csa2_status_t static_scratch_ptr(cudaStream_t stream, void** out) {
   static std::mutex mu;
   static void* ptrs[64] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CSA2_ERR_CUDA;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return CSA2_ERR_CUDA;
   std::lock_guard<std::mutex> lock(mu);
-  if (!ptrs[dev]) {
+  if (cs == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return CSA2_ERR_CUDA;
     ptrs[dev] = p;
+  } else if (!ptrs[dev]) {
+    return CSA2_ERR_UNSUPPORTED;
   }
-  return ptrs[dev];
+  *out = ptrs[dev];
+  return CSA2_OK;
 }
 
 csa2_status_t csa2_index_topk_decode_static(const csa2_cache_t* c, int32_t nq, const void* q_idx,
@@ -1040,8 +1073,9 @@ csa2_status_t csa2_index_topk_decode_static(const csa2_cache_t* c, int32_t nq, c
   const int64_t ld = score_ld(c->max_cap);
   const size_t need = (size_t)nq * ((size_t)ld * sizeof(float) + kKeyHistBinsHost * sizeof(uint32_t));
   if (need > CSA2_STATIC_SCRATCH_BYTES) return CSA2_ERR_CAPACITY;
-  void* scratch = static_scratch_ptr();
-  if (!scratch) return CSA2_ERR_CUDA;
+  void* scratch = nullptr;
+  st = static_scratch_ptr(S(stream), &scratch);
+  if (st != CSA2_OK) return st;
   float* scores = static_cast<float*>(scratch);
   uint32_t* key_hist = reinterpret_cast<uint32_t*>(scores + (int64_t)nq * ld);
   // parameter blocks on the stack: this path touches no heap

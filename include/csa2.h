@@ -265,27 +265,49 @@ csa2_status_t csa2_index_topk_decode(const csa2_cache_t* cache,
                                      void* workspace, size_t workspace_bytes,
                                      csa2_stream_t stream);
 
+/* Full-mode selection for queries at any token positions of any sequences
+ * (decode queries and prefill chunks of several sequences in one call):
+ * query i belongs to sequence seq_of_q[i] and sits at absolute token
+ * position q_pos[i]; it sees entry s iff (s + 1) * ratio - 1 <= q_pos[i]
+ * and s is appended ([V41 sec 2.3.2] "causally visible"; [V4B sec 4.3]).
+ * Same score, top-k and output rules as csa2_index_topk_decode (a decode
+ * query is q_pos = its sequence's last token, seeing every entry).
+ *   seq_of_q: host [n_queries] (NULL: query i reads sequence i);  q_pos:
+ *   host int64 [n_queries], >= 0;  other arguments and the workspace as for
+ *   csa2_index_topk_decode.  One query per tile of the tensor-core indexer:
+ *   a long chunk of consecutive positions of one sequence is scored faster
+ *   by csa2_index_topk_prefill (eight queries per tile).                   */
+csa2_status_t csa2_index_topk(const csa2_cache_t* cache, int32_t n_queries,
+                              const void* q_idx, const float* w, const int32_t* seq_of_q,
+                              const int64_t* q_pos, int32_t* topk_idx, float* topk_score,
+                              void* workspace, size_t workspace_bytes, csa2_stream_t stream);
+
 /* The same selection as csa2_index_topk_decode for callers that cannot
  * allocate device memory.  The pages have no counterpart: this is an
  * integration entry point, not part of the method.
  *
- * Some callers cannot call cudaMalloc or hand over a workspace: code that
- * runs while a CUDA graph is being captured (allocation is not a capturable
- * operation), runtimes that own every byte of device memory through their
- * own pool and give kernels no scratch, and plain C hosts that want a
+ * Some callers cannot call cudaMalloc or hand over a workspace: serving
+ * runtimes that own every byte of device memory through their own pool and
+ * hand kernels no scratch (so that the memory budget is fixed and nothing
+ * fragments it), latency-critical loops in which an allocation, which may
+ * synchronise the device, is not acceptable, and plain C hosts that want a
  * single call with nothing to size or free.  This entry point keeps its
  * scratch (fp32 scores and score-key histograms) in a fixed array inside
- * the library, CSA2_STATIC_SCRATCH_BYTES long; every GPU that loads the
- * library holds that array until the process exits.
+ * the library, CSA2_STATIC_SCRATCH_BYTES long.  A GPU holds that array from
+ * the first use of the library's device code on it (at the latest the first
+ * call of this entry point) until the process exits.
  *   - Requests needing more than the array (n_queries * (4 * ld + 8192)
  *     bytes, ld = the longest capacity rounded up to a multiple of 4) return
  *     CSA2_ERR_CAPACITY and launch nothing.
- *   - The first call on a device looks the array's device address up
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
- *   - Every call uses the same array, so two calls that overlap on the GPU
- *     (different streams without ordering between them) race; calls on one
- *     stream are safe.
+ *   - A call made while `stream` is not being captured looks the array's
+ *     device address up (cudaGetSymbolAddress) with the current device; the
+ *     first call on a device does this set-up, so make it before any stream
+ *     capture: a first call during a capture returns CSA2_ERR_UNSUPPORTED
+ *     and launches nothing.
+ *   - Every call uses the same array, which keeps what the last call left
+ *     there (each call first zeroes the histograms it accumulates into, on
+ *     `stream`); two calls that overlap on the GPU (different streams
+ *     without ordering between them) race, calls on one stream are safe.
  *   - Allocates nothing: no cudaMalloc / cudaFree, no host heap.
  * Arguments and outputs as for csa2_index_topk_decode.                     */
 #define CSA2_STATIC_SCRATCH_BYTES ((size_t)48 << 20)
