@@ -192,6 +192,7 @@ void orc_quantise(int64_t n, int dim, int layout, const float* x, uint8_t* codes
 void orc_dequantise(int64_t n, int dim, int layout, const uint8_t* codes,
                     const uint8_t* scales, float* out) {
   const int g = orc_group(layout), nb = dim / g;
+#pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < n; ++r)
     for (int ch = 0; ch < dim; ++ch) {
       uint8_t byte = codes[r * (dim / 2) + ch / 2];

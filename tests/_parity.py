@@ -5,6 +5,11 @@ import numpy as np
 # Attention outputs (bf16): max-abs and mean-abs bounds of the parity bar.
 ATTN_MAX_ABS = 1e-2
 ATTN_MEAN_ABS = 1e-3
+# lse = ln(sum_j exp(l_j)): the readout sums the probabilities rounded to
+# bf16, the operands of its PV product (relative error <= 2^-9 each), so the
+# sum is within a relative 2^-9 of the exact one and lse within 2^-9 (plus
+# the fp32 summation error).
+LSE_ABS = 2.0 ** -9 + 1e-5
 # Top-k sets: an index may differ only when its oracle score is within this
 # relative distance of the oracle's k-th score (fp32 accumulation order on
 # the tensor cores differs from the fp64 oracle).
@@ -49,6 +54,15 @@ def check_topk(gpu_idx, oracle_idx, oracle_scores, k, log=None):
         if log is not None:
             log.append((int(i), float(oracle_scores[i]), float(kth)))
     return len(diff)
+
+
+def check_lse(gpu_lse, oracle_lse, where=""):
+    g = np.asarray(gpu_lse, np.float64)
+    o = np.asarray(oracle_lse, np.float64)
+    fin = np.isfinite(o)
+    assert np.array_equal(np.isfinite(g), fin), where
+    err = np.abs(g[fin] - o[fin])
+    assert err.size == 0 or err.max() <= LSE_ABS, f"{where} lse max err {err.max()}"
 
 
 def check_attn(gpu_out_bf16_bits, oracle_out_f64, strict=False):

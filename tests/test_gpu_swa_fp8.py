@@ -9,7 +9,7 @@ import pytest
 
 import csa2_synth as S
 import oracle as O
-from tests._parity import bf16_dev, bf16_host, check_attn, f32_dev
+from tests._parity import bf16_dev, bf16_host, check_attn, f32_dev, check_lse
 
 pytestmark = pytest.mark.gpu
 SCALE = np.float32(512 ** -0.5)
@@ -82,7 +82,7 @@ def test_decode_over_fp8_window(C, layout):
             rows = O.swa_fp8_round_bf16(swa[i, :swa_len[i]])
             _, o, ol = O.sparse_attention(q[i], codes, scales, layout, idx[i], rows, SCALE)
             check_attn(out[i], o)
-            assert np.allclose(lse[i], ol, atol=1e-3, rtol=0)
+            check_lse(lse[i], ol)
     assert cache.device_error() == 0
 
 

@@ -9,7 +9,7 @@ import pytest
 
 import oracle as O
 from csa2_synth import workloads as W
-from tests._parity import bf16_host, check_attn, check_topk
+from tests._parity import bf16_host, check_attn, check_topk, check_lse
 
 pytestmark = pytest.mark.gpu
 SCALE = np.float32(512 ** -0.5)
@@ -21,9 +21,12 @@ def C():
     return C
 
 
-def _decode_case(C, wid, sample, paper=False):
+def _decode_case(C, wid, sample, paper=False, select_all=False):
     """paper=True: the pages' exact cache formats -- E2M1 + E4M3/16 main KV,
-    MXFP4 indexer keys and queries, FP8 window rows."""
+    MXFP4 indexer keys and queries, FP8 window rows.  The readouts of the
+    queries in `sample` are checked; the top-k sets of every query when
+    `select_all` (the keys then come from the seeded generator's device
+    twin, bit-identical to its numpy form, to keep the host time short)."""
     import torch
     wl = W.WORKLOADS[wid]
     n_ent = wl.n_entries()
@@ -49,9 +52,14 @@ def _decode_case(C, wid, sample, paper=False):
     assert cache.device_error() == 0
     log = []
     select = O.index_topk_mxfp4 if paper else O.index_topk
-    for b in sample:
-        o_idx, o_sc = select(wl.idx_k(b), wl.q_idx(b, 1)[0], wl.w(b, 1)[0], 512)
+    checked = range(wl.batch) if select_all else sample
+    q_all, w_all = wl.q_idx(), wl.w()
+    for b in checked:
+        n = int(n_ent[b])
+        keys = bf16_host(W.dev_idx_k(wl, b, 0, n)) if select_all else wl.idx_k(b)
+        o_idx, o_sc = select(keys, q_all[b], w_all[b], 512)
         check_topk(idx[b], o_idx, o_sc, 512, log)
+    for b in sample:
         sel = idx[b][idx[b] >= 0]
         codes, scales = O.quantise(wl.entry_rows(b, sel), layout)
         local = np.arange(len(sel), dtype=np.int32)
@@ -62,7 +70,7 @@ def _decode_case(C, wid, sample, paper=False):
             _, o, ol = O.sparse_attention(wl.q(l, b, 1)[0], codes, scales, layout, local,
                                           rows, SCALE)
             check_attn(outs[l][b], o)
-            assert np.allclose(lses[l][b], ol, atol=1e-3, rtol=0)
+            check_lse(lses[l][b], ol, f"query {b} layer {l}")
     print(f"workload {wid}{' (paper cache)' if paper else ''}: near-ties {log}")
 
 
@@ -74,12 +82,17 @@ def test_workload1_full(C):
     _decode_case(C, 1, list(range(16)))
 
 
-def test_workload2_sampled(C):
-    _decode_case(C, 2, [0, 37, 63])
+# all 64 selections; the readouts of 16 queries spread over the batch (both
+# split halves of the two-CTA readout, first and last query)
+READOUT_SAMPLE = [0, 1, 5, 9, 14, 18, 23, 27, 32, 37, 41, 46, 50, 55, 59, 63]
 
 
-def test_workload2_paper_cache_sampled(C):
-    _decode_case(C, 2, [0, 41, 63], paper=True)
+def test_workload2_selections_and_readouts(C):
+    _decode_case(C, 2, READOUT_SAMPLE, select_all=True)
+
+
+def test_workload2_paper_cache(C):
+    _decode_case(C, 2, READOUT_SAMPLE, paper=True, select_all=True)
 
 
 def test_workload1_paper_cache_full(C):
@@ -98,7 +111,14 @@ def test_workload4_prefill_sampled(C):
     W.fill_cache(wl, cache)
     nq = wl.n_queries()
     idx = C.csa2_index_topk_prefill(cache, 0, wl.pos0, W.dev_q_idx(wl), W.dev_w(wl))
-    sample = [0, 1, 2, 1000, 4095, 4096, 6001, nq - 1]
+    # 64 queries: the first MMA group of eight, both sides of group
+    # boundaries (8 g - 1, 8 g) spread over the chunk, both sides of the
+    # 1024-row top-k launch tables, the middle, and the last query
+    rng = np.random.default_rng(4)
+    groups = sorted(rng.choice(np.arange(2, 1023), size=24, replace=False).tolist())
+    sample = sorted(set(list(range(8)) + [8 * g - 1 for g in groups] + [8 * g for g in groups]
+                        + [1023, 1024, 2047, 2048, 4095, 4096, 6143, 6144, 8190, nq - 1]))
+    assert len(sample) >= 64
     outs = []
     for l in range(wl.layers):
         out = C.csa2_sparse_attn_prefill(cache, 0, wl.pos0, W.dev_q(wl, l), W.dev_swa(wl, l),
