@@ -46,13 +46,13 @@ struct csa2_cache {
   uint8_t* codes;
   uint8_t* scales;
   uint16_t* idxk;       // CSA2_IDX_BF16 keys
-  uint8_t* idx_codes;   // CSA2_IDX_MXFP4 keys: codes [total, 64], scales [total, 4]
+  uint8_t* idx_codes;   // CSA2_IDX_MXFP4 keys: codes [idx_rows, 64], scales [idx_rows, 4]
   uint8_t* idx_scales;
+  int64_t idx_rows;     // total rounded up to whole 256-key chunks (MXFP4 keys)
   CUtensorMap tm_k;    // indexer keys, 128-row boxes (contiguous tiles)
   CUtensorMap tm_k8;   // indexer keys, one 8-key block per box (pool mode)
-  CUtensorMap tm_kc;   // MXFP4 key codes, 128-row boxes
+  CUtensorMap tm_kq;   // MXFP4 key codes, 128-key tiles in the permuted row order
   CUtensorMap tm_kc8;  // MXFP4 key codes, one 8-key block per box (pool mode)
-  CUtensorMap tm_kc2;  // MXFP4 key codes, two keys per 128-byte row, 128-row boxes
   int num_sms;
   int index_sms;       // SMs the indexer's persistent grid may occupy
   int64_t wait_cycles; // bounded-wait limit of the kernels (0: their default)
@@ -84,6 +84,9 @@ struct Layout {
   size_t len_off, err_off, codes_off, scales_off, idxk_off, idxs_off, total;
 };
 
+// Rows of the MXFP4 key arrays: the entries rounded up to 256-key chunks.
+int64_t mxfp4_rows(int64_t total) { return (total + 255) / 256 * 256; }
+
 Layout layout_for(const csa2_config_t* c, int64_t total) {
   Layout L;
   const int g = c->layout == CSA2_KV_L16_E4M3 ? 16 : 32;
@@ -101,10 +104,13 @@ Layout layout_for(const csa2_config_t* c, int64_t total) {
   o = align_up(o + (size_t)total * (kHeadDim / g), kAlign);
   L.idxk_off = o;
   if (c->idx_layout == CSA2_IDX_MXFP4) {
-    o = align_up(o + (size_t)total * (kIdxDim / 2), kAlign);   // E2M1 codes
+    // E2M1 codes and UE8M0 scales, each holding whole 256-key chunks (the
+    // indexer reads keys in aligned 256-key tiles; rows past `total` are
+    // never valid entries)
+    const size_t rows = (size_t)mxfp4_rows(total);
+    o = align_up(o + rows * (kIdxDim / 2), kAlign);
     L.idxs_off = o;
-    // UE8M0 scales (16 spare bytes kept so that earlier cache sizes hold)
-    o = align_up(o + (size_t)total * (kIdxDim / 32) + 16, kAlign);
+    o = align_up(o + rows * (kIdxDim / 32), kAlign);
   } else {
     o = align_up(o + (size_t)total * kIdxDim * 2, kAlign);
     L.idxs_off = 0;
@@ -166,6 +172,27 @@ bool make_code_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t row
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// MXFP4 key codes in aligned 128-key tiles with their rows permuted: key
+// 4 r + q of a tile (r < 32, q < 4) lands in shared-memory row 32 q + r (64-
+// byte rows, the 64-byte swizzle).  With the keys in that order, the tile's
+// UE8M0 scale words in their natural order are exactly the scale atom of
+// the block-scaled MMA (row 32 q + r at byte 16 r + 4 q), so a tile's scales
+// are one contiguous copy.  The view is (64 bytes, r, q, tile) with strides
+// (1, 256, 64, 8192); rows must be a multiple of 128.  (The box's rows are
+// exactly one swizzle span wide: with a wider swizzle than the row, the TMA
+// would lay each row out at the swizzle span.)
+bool make_perm_map(CUtensorMap* m, const void* base, int64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows <= 0 || rows % 128 != 0) return false;
+  cuuint64_t gdim[4] = {64, 32, 4, (cuuint64_t)(rows / 128)};
+  cuuint64_t gstride[3] = {256, 64, 8192};
+  cuuint32_t box[4] = {64, 32, 4, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), gdim, gstride, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Indexer keys [rows, 128] bf16 seen as (64 columns, rows, 2 halves): one
 // box of (64, 8, 2) is a whole block of 8 keys, landing in shared memory as
 // two 1 KB 128B-swizzled atoms (columns 0-63, then 64-127).
@@ -199,7 +226,7 @@ cudaError_t launch_index_any(const csa2_cache* c, IndexParams& ip, const CUtenso
     ip.idx_scales = c->idx_scales;
     ip.idx_total = c->total;
     ip.q_idx = static_cast<const uint16_t*>(q_idx);
-    return launch_index_fp4(ip, c->tm_kc, c->tm_kc2, c->tm_kc8, grid, s);
+    return launch_index_fp4(ip, c->tm_kq, c->tm_kc8, grid, s);
   }
   return launch_index(ip, pool ? c->tm_k8 : c->tm_k, tm_q, grid, s);
 }
@@ -349,6 +376,7 @@ csa2_status_t csa2_cache_create(const csa2_config_t* cfg, int32_t batch, const i
   c->idxk = mx ? nullptr : reinterpret_cast<uint16_t*>(c->base + L.idxk_off);
   c->idx_codes = mx ? c->base + L.idxk_off : nullptr;
   c->idx_scales = mx ? c->base + L.idxs_off : nullptr;
+  c->idx_rows = mx ? mxfp4_rows(c->total) : 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -363,11 +391,8 @@ csa2_status_t csa2_cache_create(const csa2_config_t* cfg, int32_t batch, const i
     delete c;
     return CSA2_ERR_CUDA;
   }
-  // the two-key view ends at most 64 bytes past the last code row: inside
-  // the cache buffer (the scale region follows)
-  if (mx && (!make_code_map(&c->tm_kc, c->idx_codes, (uint64_t)c->total, kIdxDim / 2, 128) ||
-             !make_code_map(&c->tm_kc8, c->idx_codes, (uint64_t)c->total, kIdxDim / 2, kHsiBlock) ||
-             !make_code_map(&c->tm_kc2, c->idx_codes, (uint64_t)(c->total + 1) / 2, kIdxDim, 128))) {
+  if (mx && (!make_perm_map(&c->tm_kq, c->idx_codes, c->idx_rows) ||
+             !make_code_map(&c->tm_kc8, c->idx_codes, (uint64_t)c->total, kIdxDim / 2, kHsiBlock))) {
     delete c;
     return CSA2_ERR_CUDA;
   }
@@ -603,9 +628,9 @@ csa2_status_t run_index_decode(const csa2_cache_t* c, int32_t nq, const void* q_
       const int64_t nv = visible_of(c, s, q_pos, q0 + i);
       ip->entry_base[i] = c->off[s];
       ip->nvis[i] = (int32_t)nv;
-      // MXFP4 decode tiles start at an even key row (one row early when the
-      // sequence starts at an odd one)
-      const int64_t lead = (mx && nv > 0) ? (c->off[s] & 1) : 0;
+      // MXFP4 decode tiles are aligned 256-key chunks: a sequence starting
+      // inside one begins `lead` keys into its first tile
+      const int64_t lead = (mx && nv > 0) ? (c->off[s] & 255) : 0;
       ip->tile_prefix[i + 1] = ip->tile_prefix[i] + (int32_t)((nv + lead + tile_e - 1) / tile_e);
     }
     CUtensorMap tm_q;
@@ -804,7 +829,10 @@ csa2_status_t csa2_index_scores_prefill(const csa2_cache_t* c, int32_t seq, int3
     for (int g = 0; g < groups; ++g) {
       const int64_t last = std::min<int64_t>((int64_t)g * kQpg + kQpg, n) - 1;
       const int64_t nv = std::min<int64_t>(len, (ip->pos0 + last + 1) / m);
-      ip->tile_prefix[g + 1] = ip->tile_prefix[g] + (int32_t)((nv + 127) / 128);
+      // MXFP4 tiles are aligned 128-key chunks (the first one `lead` keys
+      // before the sequence start)
+      const int64_t lead = (mx && nv > 0) ? (c->off[seq] & 127) : 0;
+      ip->tile_prefix[g + 1] = ip->tile_prefix[g] + (int32_t)((nv + lead + 127) / 128);
     }
     CUtensorMap tm_q;
     const uint16_t* qn = qb + (int64_t)q0 * kIdxHeads * kIdxDim;

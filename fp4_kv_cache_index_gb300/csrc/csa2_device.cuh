@@ -185,6 +185,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, int
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, int32_t c0, int32_t c1,
+                                            int32_t c2, int32_t c3, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "l"(pol)
+      : "memory");
+}
+
 // 1-D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of
 // 16), completion on `bar`.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
@@ -560,6 +570,34 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Indexer score of one entry from its 32 head logits r (fp32 bits) and the
+// query's head weights w (shared memory, 16-byte aligned):
+//     sum_h w[h] * max(r[h], 0)
+// summed in four fp32 chains (chain c takes heads h = c mod 4, in order),
+// then (c0 + c1) + (c2 + c3).  Chains (0, 1) and (2, 3) run as the two lanes
+// of packed f32x2 FMAs (each lane an fp32 fma, round to nearest), which
+// halves the FMA issues; the ReLU stays one fmax per head.
+__device__ __forceinline__ float relu_dot32(const float* w, const uint32_t (&r)[32]) {
+  uint64_t a = 0, b = 0;   // (c0, c1), (c2, c3); +0.0f bits
+#pragma unroll
+  for (int h = 0; h < 32; h += 4) {
+    const float4 wv = *reinterpret_cast<const float4*>(w + h);
+    uint64_t w01, w23, x01, x23;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(w01) : "f"(wv.x), "f"(wv.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(w23) : "f"(wv.z), "f"(wv.w));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x01)
+        : "f"(fmaxf(__uint_as_float(r[h]), 0.0f)), "f"(fmaxf(__uint_as_float(r[h + 1]), 0.0f)));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x23)
+        : "f"(fmaxf(__uint_as_float(r[h + 2]), 0.0f)), "f"(fmaxf(__uint_as_float(r[h + 3]), 0.0f)));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(w01), "l"(x01));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(b) : "l"(w23), "l"(x23));
+  }
+  float c0, c1, c2, c3;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(c0), "=f"(c1) : "l"(a));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(c2), "=f"(c3) : "l"(b));
+  return (c0 + c1) + (c2 + c3);
 }
 
 }  // namespace csa2

@@ -99,17 +99,18 @@ struct IndexParams {
 int index_smem_bytes(int qpg);
 cudaError_t launch_index(const IndexParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_q,
                          int grid, cudaStream_t s);
-// MXFP4 keys: tm_kc views the codes as uint8 [idx_total, 64] in boxes of
-// 128 rows and tm_kc8 in boxes of 8 rows (pool blocks), both with the
-// 64-byte swizzle; tm_kc2 views them as [ceil(idx_total / 2), 128] (two keys
-// per row) in boxes of 128 rows with the 128-byte swizzle.  qpg is 1
-// (decode, pool mode) or 4 (prefill).  Decode tiles (no pool) are 256 keys
-// starting at an even key row: a sequence at key row off has
-// ceil((n + off % 2) / 256) tiles.
+// MXFP4 keys (codes [idx_rows, 64], scales [idx_rows, 4], idx_rows a
+// multiple of 256): tm_kq views the codes as aligned 128-key tiles in the
+// permuted row order of the kernel (key 4 r + q of a tile in shared-memory
+// row 32 q + r, 64-byte rows, 64-byte swizzle), tm_kc8 as [idx_total, 64]
+// in boxes of 8 rows (pool blocks, 64-byte swizzle).  qpg is 1 (decode,
+// pool mode) or 4 (prefill).  Decode tiles (no pool) are the aligned 256-key
+// chunks: a sequence at key row off has ceil((n + off % 256) / 256) tiles;
+// prefill tiles the aligned 128-key chunks, ceil((n + off % 128) / 128) per
+// group.
 int index_fp4_smem_bytes();
-cudaError_t launch_index_fp4(const IndexParams& p, const CUtensorMap& tm_kc,
-                             const CUtensorMap& tm_kc2, const CUtensorMap& tm_kc8, int grid,
-                             cudaStream_t s);
+cudaError_t launch_index_fp4(const IndexParams& p, const CUtensorMap& tm_kq,
+                             const CUtensorMap& tm_kc8, int grid, cudaStream_t s);
 
 // ---------------------------------------------------------------- HSI
 constexpr int kHsiBlock = 8;   // positions per block of the candidate pool

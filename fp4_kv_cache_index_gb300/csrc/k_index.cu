@@ -23,9 +23,13 @@
 // section 7) rounded to bf16 with the histogram taken on the rounded value.
 //
 // Persistent CTAs walk a balanced contiguous range of (group, tile) items.
-// Warp roles: warp 0 = TMA producer (lane 0; lanes 0-15 in pool mode), warp 1 = MMA issuer (and TMEM owner),
-// warps 2-9 = epilogue (TMEM -> registers -> scores), two warps per TMEM lane
-// quadrant splitting the queries of a group.  Every wait is bounded.
+// Warp roles: warp 0 = TMA producer (lane 0; lanes 0-15 in pool mode), warp 1
+// = MMA issuer (and TMEM owner), then the epilogue warps (TMEM -> registers
+// -> scores): eight with one query per group (two sets of four taking
+// alternate tiles), sixteen with several (four warps per TMEM lane quadrant,
+// each taking a quarter of the group's queries, so that the ReLU and head sums
+// of a tile's 256 columns run on every scheduler with enough warps to cover
+// the TMEM load latency).  Every wait is bounded.
 #include "csa2_device.cuh"
 #include "csa2_kernels.h"
 
@@ -35,9 +39,7 @@ namespace {
 constexpr int kTileE = 128;
 constexpr int kStages = 4;
 constexpr int kKStageBytes = kTileE * kIdxDim * 2;  // 32 KB
-constexpr int kThreads = 320;
-constexpr int kEpiThreads = 256;   // warps 2-9
-constexpr int kMaxHalfQ = 4;              // queries per epilogue half (a tile holds <= 8)
+constexpr int kMaxQpg = 8;                 // queries per group (N <= 256)
 constexpr int kMaxAcc = 4;                 // accumulators in TMEM (decode 4, several queries 2)
 constexpr int kBars = 2 * kStages + 2 * kMaxAcc + 4;   // k full / empty, acc full / empty, q full / empty, drain
 
@@ -90,9 +92,14 @@ struct GroupCursor {
   }
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+// kEpiW epilogue warps: 8 for one query per group, 16 for several.
+template <int kEpiW>
+__global__ void __launch_bounds__(64 + 32 * kEpiW, 1)
     k_index(const __grid_constant__ IndexParams p, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_q) {
+  constexpr int kEpiThreads = 32 * kEpiW;
+  constexpr int kParts = kEpiW / 4;                      // warps per TMEM lane quadrant
+  constexpr int kMaxQ = (kMaxQpg + kParts - 1) / kParts;   // queries of one epilogue thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -121,7 +128,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) { mbar_init(k_full + i, 1); mbar_init(k_empty + i, 1); }
-    for (int i = 0; i < nacc; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, p.qpg == 1 ? kEpiThreads / 2 : kEpiThreads); }
+    // acc_empty: decode, every thread of the set of four warps that took the
+    // tile; several queries, one arrival per epilogue warp
+    for (int i = 0; i < nacc; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, p.qpg == 1 ? 128 : kEpiW); }
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     mbar_init(drain, 1);
@@ -258,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     umma_commit(drain);
     mbar_wait(drain, 0, p.err, wl);
-  } else if (warp >= 2 && p.qpg == 1) {
+  } else if (kEpiW == 8 && warp >= 2 && p.qpg == 1) {
     // ------------------------------------------------ epilogue, one query per tile
     // Two groups of four warps take alternate tiles (group gsel the tiles
     // begin + gsel + 2k, whose accumulator is gsel), so two tiles' scores are
@@ -312,10 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * N), r);
       tc_fence_before();
       mbar_arrive(acc_empty + a);   // the accumulator is free once read
-      float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-      for (int h = 0; h < 32; ++h) s4[h & 3] = fmaf(wg[h], fmaxf(__uint_as_float(r[h]), 0.0f), s4[h & 3]);
-      const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+      const float s = relu_dot32(wg, r);
       if (p.pool) {
         const int64_t ent = (int64_t)blk * 8 + (row & 7);
         const float v = (blk >= 0 && ent < nvis) ? s : -INFINITY;
@@ -339,20 +345,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ epilogue
     const int quad = warp & 3;                 // TMEM lane quadrant of this warp
     const int row = quad * 32 + lane;          // entry within the tile
-    const int et = threadIdx.x - 64;           // 0..255
-    const int half = (warp - 2) >> 2;          // which queries of the group
-    const int jq = (p.qpg + 1) >> 1;
-    const int j0 = half * jq, j1 = min(p.qpg, j0 + jq);
+    const int et = threadIdx.x - 64;           // 0 .. kEpiThreads - 1
+    const int part = (warp - 2) >> 2;          // which queries of the group
+    const int jq = (p.qpg + kParts - 1) / kParts;
+    const int j0 = part * jq, j1 = min(p.qpg, j0 + jq);
     const bool use_hist = p.key_hist != nullptr && p.qpg == 1;
     // adds this CTA's counts of query `qq` to the global histogram, clears hs
+    auto esync = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); };
     auto flush = [&](int qq) {
-      asm volatile("bar.sync 1, 256;" ::: "memory");
+      esync();
       for (int i = et; i < kKeyHistBins; i += kEpiThreads) {
         const uint32_t v = hs[i];
         if (v) atomicAdd(p.key_hist + (int64_t)qq * kKeyHistBins + i, v);
         hs[i] = 0u;
       }
-      asm volatile("bar.sync 1, 256;" ::: "memory");
+      esync();
     };
     if (use_hist) {
       for (int i = et; i < kKeyHistBins; i += kEpiThreads) hs[i] = 0u;
@@ -360,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     GroupCursor gc = c0;
     int cur = -1, acc = 0;
     uint32_t aph = 0;
-    int nvis[kMaxHalfQ];   // visible entries of this thread's queries in the current group
+    int nvis[kMaxQ];   // visible entries of this thread's queries in the current group
     int32_t blk_nxt = (p.pool && begin < end) ? __ldg(pool_row(begin, c0) + (row >> 3)) : -1;
     for (int it = begin; it < end; ++it) {
       gc.advance(p, it);
@@ -369,15 +376,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.pool && it + 1 < end) blk_nxt = __ldg(pool_row(it + 1, gc) + (row >> 3));
       if (g != cur) {
         if (use_hist && cur >= 0) flush(cur);
-        asm volatile("bar.sync 1, 256;" ::: "memory");
+        esync();
         for (int i = et; i < qrows; i += kEpiThreads) {
           const int q = g * p.qpg + (i >> 5);
           wbuf[i] = (q < p.nq) ? __ldg(p.w + (int64_t)q * kIdxHeads + (i & 31)) : 0.0f;
         }
-        asm volatile("bar.sync 1, 256;" ::: "memory");
+        esync();
         cur = g;
 #pragma unroll
-        for (int jj = 0; jj < kMaxHalfQ; ++jj)
+        for (int jj = 0; jj < kMaxQ; ++jj)
           nvis[jj] = (j0 + jj < j1) ? group_nvis_query(p, g, j0 + jj) : 0;
       }
       if (!mbar_wait(acc_full + acc, aph, p.err, wl)) break;
@@ -386,12 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int e = t * kTileE + row;
       // score of query j of the group from its 32 head columns r
       auto emit = [&](int j, int jj, const uint32_t (&r)[32]) {
-        const float* wj = wbuf + j * 32;
-        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // four chains, not one of 32
-#pragma unroll
-        for (int h = 0; h < 32; ++h)
-          s4[h & 3] = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.0f), s4[h & 3]);
-        const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        const float s = relu_dot32(wbuf + j * 32, r);
         const int q = g * p.qpg + j;
         const int nv = nvis[jj];
         if (p.pool) {
@@ -415,22 +417,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * N);
-#pragma unroll
-      for (int jj = 0; jj < kMaxHalfQ; jj += 2) {   // two queries' columns under one TMEM wait
-        const int j = j0 + jj;
-        if (j + 1 < j1) {
-          uint32_t ra[32], rb[32];
-          tmem_ld32x2(lane_base + (uint32_t)(j * 32), lane_base + (uint32_t)((j + 1) * 32), ra, rb);
-          emit(j, jj, ra);
-          emit(j + 1, jj + 1, rb);
-        } else if (j < j1) {
-          uint32_t r[32];
-          tmem_ld32(lane_base + (uint32_t)(j * 32), r);
-          emit(j, jj, r);
+      // the accumulator is free once this warp's last columns are read
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty + acc);
+      };
+      if constexpr (kMaxQ == 2) {
+        // one query's 32 columns at a time (the register budget of sixteen
+        // epilogue warps); the other warps of the scheduler cover the loads
+        uint32_t r[32];
+        if (j0 < j1) tmem_ld32(lane_base + (uint32_t)(j0 * 32), r);
+        if (j0 + 1 >= j1) release();
+        if (j0 < j1) emit(j0, 0, r);
+        if (j0 + 1 < j1) {
+          tmem_ld32(lane_base + (uint32_t)((j0 + 1) * 32), r);
+          release();
+          emit(j0 + 1, 1, r);
         }
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < kMaxQ; jj += 2) {   // two queries' columns under one TMEM wait
+          const int j = j0 + jj;
+          if (j + 1 < j1) {
+            uint32_t ra[32], rb[32];
+            tmem_ld32x2(lane_base + (uint32_t)(j * 32), lane_base + (uint32_t)((j + 1) * 32), ra, rb);
+            emit(j, jj, ra);
+            emit(j + 1, jj + 1, rb);
+          } else if (j < j1) {
+            uint32_t r[32];
+            tmem_ld32(lane_base + (uint32_t)(j * 32), r);
+            emit(j, jj, r);
+          }
+        }
+        release();
       }
-      tc_fence_before();
-      mbar_arrive(acc_empty + acc);
       if (++acc == 2) { acc = 0; aph ^= 1; }
     }
     if (use_hist && cur >= 0) flush(cur);
@@ -450,20 +471,22 @@ int index_smem_bytes(int qpg) { return smem_layout(qpg).total; }
 
 cudaError_t launch_index(const IndexParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_q,
                          int grid, cudaStream_t s) {
-  // the epilogue covers at most 2 * kMaxHalfQ queries per tile (N <= 256)
-  if (p.qpg < 1 || p.qpg > 2 * kMaxHalfQ) return cudaErrorInvalidValue;
+  // the epilogue covers at most kMaxQpg queries per tile (N <= 256)
+  if (p.qpg < 1 || p.qpg > kMaxQpg) return cudaErrorInvalidValue;
   const int smem = index_smem_bytes(p.qpg);
-  cudaError_t e = cudaFuncSetAttribute(k_index, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int epi_warps = p.qpg == 1 ? 8 : 16;
+  auto* kern = p.qpg == 1 ? k_index<8> : k_index<16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3((unsigned)(64 + 32 * epi_warps));
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1] = {pdl_attribute()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_index, p, tm_k, tm_q);
+  return cudaLaunchKernelEx(&cfg, kern, p, tm_k, tm_q);
 }
 
 }  // namespace csa2

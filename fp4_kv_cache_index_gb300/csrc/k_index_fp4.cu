@@ -12,13 +12,14 @@
 // fp32 accumulation, so the cached codes go to the tensor cores as they are.
 //
 // Operands of one MMA (M = 128 keys, N = 32 heads x qpg, K = 64):
-//   A  key codes, K-major: with one query per group, rows of two keys
-//      (128 bytes, the 128-byte swizzle, one TMA box of 256 keys; the even
-//      keys at bytes 0-63 of each row, the odd keys at 64-127, so the TMA
-//      moves 128-byte rows); otherwise 64-byte rows of one key with the
-//      64-byte swizzle (a box of 128 keys, or in pool mode one box per block
-//      of 8 keys, exactly one 512-byte swizzle atom); two K steps of 32 bytes
-//      cover the 128 channels;
+//   A  key codes, K-major, 64-byte rows with the 64-byte swizzle.
+//      Contiguous keys come in aligned tiles of 128 or 256 keys whose rows
+//      are permuted: key 128 h + 4 r + q of the tile (r < 32, q < 4) is row
+//      32 q + r of M-group h (one TMA box per M-group), so that the tile's
+//      scale words, copied in their natural order, are already the scale
+//      atoms below.  In pool mode one box per block of 8 keys (exactly one
+//      512-byte swizzle atom), in pool order.  Two K steps of 32 bytes cover
+//      the 128 channels;
 //   B  query codes in the same layout, written by the query-preparation
 //      warps (each query head rounded to the MXFP4 grid);
 //   SFA / SFB  scale bytes in tensor memory: a 512-byte atom per 128 rows in
@@ -28,9 +29,10 @@
 //      choosing the byte pair (scale id 0 or 2).
 //
 // Warp roles (384 threads):
-//   warp 0      producer: the key-code TMA boxes of each tile and its scale
-//               atoms (scale words loaded into registers four tiles ahead,
-//               stored transposed into the atom layout);
+//   warp 0      producer: per tile one TMA box of key codes and one bulk
+//               copy of its scale words (contiguous tiles), or a box per
+//               block and a 4-byte copy per scale word into its atom place
+//               (pool mode);
 //   warp 1      MMA issuer (and TMEM owner): per tile the scale-atom copies
 //               into tensor memory, then the MMAs, one accumulator per tile;
 //   warps 2-9   epilogue: ReLU, head weights, fp32 or bf16 score store,
@@ -221,14 +223,17 @@ __device__ __forceinline__ void prep_query_block(const uint16_t* src, bool live,
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
-  const uint32_t sb = ue8m0_for_amax(amax);
-  const float sc = ue8m0_value(sb);
+  const uint32_t sb = ue8m0_for_amax(amax);   // 0 .. 252 for finite maxima
+  // x / 2^(sb - 127) as x * 2^(127 - sb): the reciprocal (byte 254 - sb) is
+  // an exact normal power of two, so the product is the correctly rounded
+  // quotient
+  const float inv = ue8m0_value(254u - sb);
   uint32_t c[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     uint32_t w = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) w |= e2m1_encode(__fdiv_rn(x[8 * k + i], sc)) << (4 * i);
+    for (int i = 0; i < 8; ++i) w |= e2m1_encode(__fmul_rn(x[8 * k + i], inv)) << (4 * i);
     c[k] = w;
   }
   uint8_t* row = bcodes + (n >> 3) * 512 + (n & 7) * 64;
@@ -237,8 +242,8 @@ __device__ __forceinline__ void prep_query_block(const uint16_t* src, bool live,
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    k_index_fp4(const __grid_constant__ IndexParams p, const __grid_constant__ CUtensorMap tm_kc,
-                const __grid_constant__ CUtensorMap tm_kc2, const __grid_constant__ CUtensorMap tm_kc8) {
+    k_index_fp4(const __grid_constant__ IndexParams p, const __grid_constant__ CUtensorMap tm_kq,
+                const __grid_constant__ CUtensorMap tm_kc8) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -266,31 +271,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nacc = acc_cols == 64 ? kNAcc : 2;   // accumulators below kAccCols
   const bool pool = p.pool != nullptr;
   const int blocks_per_tile = tile_e / 8;
-  // One query per group over contiguous keys: a tile is 256 keys read as 128
-  // rows of two keys (128 bytes, the 128-byte swizzle), half the TMA rows of
-  // one key per row; M-group 0 takes the even keys of the rows (bytes 0-63),
-  // M-group 1 the odd ones (bytes 64-127).  Such tiles start at an even key
-  // row, so a sequence whose first key row is odd starts one row early
-  // (`shift`, masked).
-  const bool pairs = p.qpg == 1 && !pool;
-  // key of slot sl (M-group sl / 128, TMEM lane sl % 128) relative to the
-  // tile's first key row
-  auto slot_key = [&](int sl) -> int { return pairs ? 2 * (sl & 127) + (sl >> 7) : sl; };
+  // Contiguous keys: tiles are aligned chunks of tile_e key rows, so a
+  // sequence starting inside a chunk begins `lead` keys into its first tile
+  // (masked); slot sl (M-group sl / 128, TMEM lane sl % 128) holds the key
+  // (sl & ~127) + 4 (sl & 31) + (sl >> 5) % 4 of the tile.  Pool mode: slot
+  // sl is pool slot sl of the tile, no permutation.
+  const bool perm = !pool;
+  auto slot_key = [&](int sl) -> int {
+    return perm ? (sl & ~127) + 4 * (sl & 31) + ((sl >> 5) & 3) : sl;
+  };
+  auto lead_of = [&](const Cursor& c) -> int { return perm ? (int)(c.base & (tile_e - 1)) : 0; };
   auto tile_row0 = [&](const Cursor& c, int it) -> int64_t {
-    return (pairs ? (c.base & ~(int64_t)1) : c.base) + (int64_t)(it - c.lo) * tile_e;
+    return (perm ? (c.base & ~(int64_t)(tile_e - 1)) : c.base) + (int64_t)(it - c.lo) * tile_e;
   };
 
   if (threadIdx.x == 0) {
-    // k_full: the code copies' transaction bytes with lane 0's arrival, plus
-    // one arrival per producer lane once its scale copies have landed
-    for (int i = 0; i < kStages; ++i) { mbar_init(k_full + i, 33); mbar_init(k_empty + i, 1); }
+    // k_full: the copies' transaction bytes with lane 0's arrival, plus in
+    // pool mode one arrival per producer lane once its scale copies landed
+    for (int i = 0; i < kStages; ++i) { mbar_init(k_full + i, pool ? 33 : 1); mbar_init(k_empty + i, 1); }
     for (int i = 0; i < kNAcc; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, kEpiWarps); }
     for (int i = 0; i < 2; ++i) { mbar_init(b_full + i, kPrepWarps); mbar_init(b_empty + i, 1); }
     mbar_init(drain, 1);
     fence_barrier_init();
-    tma_prefetch_desc(&tm_kc);
-    tma_prefetch_desc(&tm_kc2);
-    tma_prefetch_desc(&tm_kc8);
+    tma_prefetch_desc(pool ? &tm_kc8 : &tm_kq);
   }
   if (warp == 1) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
   tc_fence_before();
@@ -320,13 +323,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 && begin < end) {
     // ------------------------------------------------ producer
-    // Per tile: the key codes by TMA (one box per M-group, or per block of 8
-    // keys in pool mode) and each key's scale word by a 4-byte asynchronous
-    // copy straight into its place in the scale atom (lane r copies rows
-    // 32 q + r), completing on the stage's barrier: the warp never waits for
-    // a load.  In pool mode the block ids are loaded kPf tiles ahead, slot u
-    // of the ring holding the tiles it = u (mod kPf), the loop unrolled over
-    // the slots so that no register of a load in flight is ever copied.
+    // Contiguous tiles: lane 0 issues one TMA box of key codes and one bulk
+    // copy of the tile's scale words (their natural order is the atom
+    // layout of the permuted rows).  Pool mode: one box per block of 8 keys
+    // and each key's scale word by a 4-byte asynchronous copy straight into
+    // its place in the scale atom (lane r copies rows 32 q + r), completing
+    // on the stage's barrier; the block ids are loaded kPf tiles ahead, slot
+    // u of the ring holding the tiles it = u (mod kPf), the loop unrolled
+    // over the slots so that no register of a load in flight is ever
+    // copied.  The warp never waits for a load.
     const uint32_t* sw = reinterpret_cast<const uint32_t*>(p.idx_scales);   // one word per key
     const uint64_t keys_pol = l2_policy_evict_first();
     int32_t pq[kPf];     // pool mode: this lane's block id of tiles it .. it + kPf - 1
@@ -359,46 +364,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
         uint8_t* st = stages + stage * kStageBytes;
-        const int64_t base = gc.base;
-        const int32_t blk_lane = pq[u];
-        // scale words into the atoms: row 32 q + r of M-group mg at byte
-        // 16 r + 4 q of that group's atom
-#pragma unroll
-        for (int mg = 0; mg < 2; ++mg) {
-          if (mg >= mgroups) break;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int sl = mg * 128 + 32 * q + lane;     // key slot of the tile
-            int64_t row;
-            if (pool) {
-              const int32_t blk = __shfl_sync(0xffffffffu, blk_lane, sl >> 3);
-              row = blk >= 0 ? base + (int64_t)blk * 8 + (sl & 7) : -1;
-            } else {
-              row = tile_row0(gc, it) + slot_key(sl);
-            }
-            const bool live = row >= 0 && row < p.idx_total;
-            cp_async4(st + kCodeStage + mg * kSfAtom + lane * 16 + q * 4, sw + (live ? row : 0),
-                      live ? 4u : 0u);
+        if (!pool) {
+          if (lane == 0) {
+            const int64_t row0 = tile_row0(gc, it);   // a multiple of tile_e
+            const int32_t chunk = (int32_t)(row0 / 128);
+            mbar_arrive_expect_tx(k_full + stage, (uint32_t)(mgroups * (128 * (kIdxDim / 2) + kSfAtom)));
+            for (int mg = 0; mg < mgroups; ++mg)
+              tma_load_4d(st + mg * 128 * (kIdxDim / 2), &tm_kq, 0, 0, 0, chunk + mg, k_full + stage,
+                          keys_pol);
+            bulk_load(st + kCodeStage, sw + row0, (uint32_t)(mgroups * kSfAtom), k_full + stage);
           }
-        }
-        cp_async_arrive_noinc(k_full + stage);
-        if (pool) {
+        } else {
+          const int64_t base = gc.base;
+          const int32_t blk_lane = pq[u];
+          // scale words into the atoms: row 32 q + r of M-group mg at byte
+          // 16 r + 4 q of that group's atom
+#pragma unroll
+          for (int mg = 0; mg < 2; ++mg) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int sl = mg * 128 + 32 * q + lane;     // pool slot of the tile
+              const int32_t blk = __shfl_sync(0xffffffffu, blk_lane, sl >> 3);
+              const int64_t row = blk >= 0 ? base + (int64_t)blk * 8 + (sl & 7) : -1;
+              const bool live = row >= 0 && row < p.idx_total;
+              cp_async4(st + kCodeStage + mg * kSfAtom + lane * 16 + q * 4, sw + (live ? row : 0),
+                        live ? 4u : 0u);
+            }
+          }
+          cp_async_arrive_noinc(k_full + stage);
           const uint32_t n_ok = (uint32_t)__popc(__ballot_sync(0xffffffffu, blk_lane >= 0));
           if (lane == 0) mbar_arrive_expect_tx(k_full + stage, n_ok * 512u);
           __syncwarp();
           if (blk_lane >= 0)
             tma_load_2d(st + lane * 512, &tm_kc8, 0, (int32_t)(base + (int64_t)blk_lane * 8),
                         k_full + stage, keys_pol);
-        } else if (lane == 0) {
-          const int64_t row0 = tile_row0(gc, it);
-          mbar_arrive_expect_tx(k_full + stage, (uint32_t)(mgroups * 128 * (kIdxDim / 2)));
-          if (pairs) {
-            tma_load_2d(st, &tm_kc2, 0, (int32_t)(row0 >> 1), k_full + stage, keys_pol);
-          } else {
-            for (int mg = 0; mg < mgroups; ++mg)
-              tma_load_2d(st + mg * 128 * (kIdxDim / 2), &tm_kc, 0, (int32_t)(row0 + mg * 128),
-                          k_full + stage, keys_pol);
-          }
         }
         armed |= 1u << stage;
         armed_ph = (armed_ph & ~(1u << stage)) | (ph << stage);
@@ -444,6 +443,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 && lane == 0 && begin < end) {
     // ------------------------------------------------ MMA issuer
+    // Shared-memory descriptors built once; a tile's offsets go into the
+    // start-address field (16-byte units; shared memory is below 2^18
+    // bytes, so the field never carries).  A: 64-byte rows, M-group h 8 KB
+    // further, K step ks 32 bytes further.
+    const uint64_t a_desc0 = sdesc_sw64(smem_u32(stages));
+    const uint32_t a_mg = (uint32_t)(128 * (kIdxDim / 2)) >> 4;
+    const uint64_t b_desc0 = sdesc_sw64(smem_u32(bslots));
+    const uint64_t atom_desc0 = sdesc_atom(smem_u32(stages + kCodeStage));
+    const uint32_t idesc_k0 = idesc_mxf4((uint32_t)N, 0u), idesc_k1 = idesc_mxf4((uint32_t)N, 2u);
     Cursor gc = c0;
     int cur = -1, gi = -1, stage = 0, acc = 0;
     uint32_t ph = 0, aph = 0;
@@ -462,26 +470,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait(k_full + stage, ph, p.err, wl) && mbar_wait(acc_empty + acc, aph ^ 1, p.err, wl);
       if (!ok) break;
       tc_fence_after();
-      // the scale words arrived by generic-proxy copies; tcgen05.cp reads
-      // them through the async proxy
-      fence_proxy_async_smem();
-      uint8_t* st = stages + stage * kStageBytes;
+      // pool mode: the scale words arrived by generic-proxy copies, which
+      // tcgen05.cp reads through the async proxy (bulk copies are async)
+      if (pool) fence_proxy_async_smem();
+      const uint32_t so = (uint32_t)(stage * kStageBytes) >> 4;   // stage offset, 16-byte units
       const uint32_t sfa = tmem_base + kSfaCol + (uint32_t)(acc * 8);
       for (int mg = 0; mg < mgroups; ++mg)
-        tmem_cp_atom(sfa + 4 * mg, sdesc_atom(smem_u32(st + kCodeStage + mg * kSfAtom)));
-      const uint32_t b0 = smem_u32(bslots + (gi & 1) * kBSlotBytes);
+        tmem_cp_atom(sfa + 4 * mg, atom_desc0 + so + (uint32_t)(mg * (kSfAtom >> 4)));
+      const uint32_t bo = (uint32_t)((gi & 1) * kBSlotBytes) >> 4;
       const uint32_t sfb = tmem_base + kSfbCol + 4 * (gi & 1);
       for (int mg = 0; mg < mgroups; ++mg) {
         const uint32_t d = tmem_base + (uint32_t)(acc * acc_cols + mg * N);
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          // key rows: pairs -> the even / odd half of the 128-byte rows
-          const uint64_t ad =
-              pairs ? sdesc_sw128(smem_u32(st) + 64 * mg + 32 * ks, 16, 1024)
-                    : sdesc_sw64(smem_u32(st + mg * 128 * (kIdxDim / 2)) + 32 * ks);
-          umma_mxf4(d, ad, sdesc_sw64(b0 + 32 * ks), idesc_mxf4((uint32_t)N, 2u * ks),
-                    sfa + 4 * mg, sfb, ks > 0 ? 1u : 0u);
-        }
+        for (int ks = 0; ks < 2; ++ks)
+          umma_mxf4(d, a_desc0 + so + (uint32_t)(mg * a_mg + 2 * ks), b_desc0 + bo + (uint32_t)(2 * ks),
+                    ks ? idesc_k1 : idesc_k0, sfa + 4 * mg, sfb, ks > 0 ? 1u : 0u);
       }
       umma_commit(k_empty + stage);
       umma_commit(acc_full + acc);
@@ -549,16 +552,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int t = it - gc.lo;
       // entry of this slot (pool mode: the pool slot)
-      const int e = t * tile_e + key - (pairs ? (int)(gc.base & 1) : 0);
+      const int e = t * tile_e + key - lead_of(gc);
       int32_t blk = -1;     // pool mode: the block of this slot
       if (pool && t * blocks_per_tile + (row >> 3) < p.pool_blocks)
         blk = ids_s[(t - t_first) * blocks_per_tile + (row >> 3)];
       const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * acc_cols);
       auto score_of = [&](const uint32_t (&r)[32], const float* wj) {
-        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-        for (int h = 0; h < 32; ++h) s4[h & 3] = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.0f), s4[h & 3]);
-        return (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        return relu_dot32(wj, r);
       };
       auto store = [&](int q, int nvis, float s) {
         if (pool) {
@@ -613,9 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int index_fp4_smem_bytes() { return smem_layout().total; }
 
-cudaError_t launch_index_fp4(const IndexParams& p, const CUtensorMap& tm_kc,
-                             const CUtensorMap& tm_kc2, const CUtensorMap& tm_kc8, int grid,
-                             cudaStream_t s) {
+cudaError_t launch_index_fp4(const IndexParams& p, const CUtensorMap& tm_kq,
+                             const CUtensorMap& tm_kc8, int grid, cudaStream_t s) {
   if (p.qpg != 1 && p.qpg != kMaxQpg) return cudaErrorInvalidValue;
   const int smem = index_fp4_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(k_index_fp4, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -629,7 +628,7 @@ cudaError_t launch_index_fp4(const IndexParams& p, const CUtensorMap& tm_kc,
   cudaLaunchAttribute attr[1] = {pdl_attribute()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_index_fp4, p, tm_kc, tm_kc2, tm_kc8);
+  return cudaLaunchKernelEx(&cfg, k_index_fp4, p, tm_kq, tm_kc8);
 }
 
 }  // namespace csa2
