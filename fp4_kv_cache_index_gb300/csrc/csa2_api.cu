@@ -48,7 +48,7 @@ struct csa2_cache {
   uint16_t* idxk;       // CSA2_IDX_BF16 keys
   uint8_t* idx_codes;   // CSA2_IDX_MXFP4 keys: codes [idx_rows, 64], scales [idx_rows, 4]
   uint8_t* idx_scales;
-  int64_t idx_rows;     // total rounded up to whole 256-key chunks (MXFP4 keys)
+  int64_t idx_rows;     // total rounded up to whole 512-key chunks (MXFP4 keys)
   CUtensorMap tm_k;    // indexer keys, 128-row boxes (contiguous tiles)
   CUtensorMap tm_k8;   // indexer keys, one 8-key block per box (pool mode)
   CUtensorMap tm_kq;   // MXFP4 key codes, 128-key tiles in the permuted row order
@@ -84,8 +84,8 @@ struct Layout {
   size_t len_off, err_off, codes_off, scales_off, idxk_off, idxs_off, total;
 };
 
-// Rows of the MXFP4 key arrays: the entries rounded up to 256-key chunks.
-int64_t mxfp4_rows(int64_t total) { return (total + 255) / 256 * 256; }
+// Rows of the MXFP4 key arrays: the entries rounded up to 512-key chunks.
+int64_t mxfp4_rows(int64_t total) { return (total + 511) / 512 * 512; }
 
 Layout layout_for(const csa2_config_t* c, int64_t total) {
   Layout L;
@@ -104,9 +104,9 @@ Layout layout_for(const csa2_config_t* c, int64_t total) {
   o = align_up(o + (size_t)total * (kHeadDim / g), kAlign);
   L.idxk_off = o;
   if (c->idx_layout == CSA2_IDX_MXFP4) {
-    // E2M1 codes and UE8M0 scales, each holding whole 256-key chunks (the
-    // indexer reads keys in aligned 256-key tiles; rows past `total` are
-    // never valid entries)
+    // E2M1 codes and UE8M0 scales, each holding whole 512-key chunks (the
+    // indexer reads keys in aligned tiles of up to 512 keys; rows past
+    // `total` are never valid entries)
     const size_t rows = (size_t)mxfp4_rows(total);
     o = align_up(o + rows * (kIdxDim / 2), kAlign);
     L.idxs_off = o;
@@ -603,9 +603,9 @@ csa2_status_t run_index_decode(const csa2_cache_t* c, int32_t nq, const void* q_
       cudaMemsetAsync(key_hist, 0, (size_t)nq * kKeyHistBinsHost * sizeof(uint32_t), S(stream)) !=
           cudaSuccess)
     return CSA2_ERR_CUDA;
-  // keys per tile: the MXFP4 decode kernel takes 256, every other path 128
+  // keys per tile: the MXFP4 decode kernel takes 512, every other path 128
   const bool mx = c->cfg.idx_layout == CSA2_IDX_MXFP4;
-  const int64_t tile_e = mx ? 256 : 128;
+  const int64_t tile_e = mx ? 512 : 128;
   for (int q0 = 0; q0 < nq; q0 += kMaxIdxGroups) {
     const int n = std::min(kMaxIdxGroups, nq - q0);
     std::memset(ip, 0, sizeof(IndexParams));
@@ -628,9 +628,9 @@ csa2_status_t run_index_decode(const csa2_cache_t* c, int32_t nq, const void* q_
       const int64_t nv = visible_of(c, s, q_pos, q0 + i);
       ip->entry_base[i] = c->off[s];
       ip->nvis[i] = (int32_t)nv;
-      // MXFP4 decode tiles are aligned 256-key chunks: a sequence starting
+      // MXFP4 decode tiles are aligned 512-key chunks: a sequence starting
       // inside one begins `lead` keys into its first tile
-      const int64_t lead = (mx && nv > 0) ? (c->off[s] & 255) : 0;
+      const int64_t lead = (mx && nv > 0) ? (c->off[s] & 511) : 0;
       ip->tile_prefix[i + 1] = ip->tile_prefix[i] + (int32_t)((nv + lead + tile_e - 1) / tile_e);
     }
     CUtensorMap tm_q;

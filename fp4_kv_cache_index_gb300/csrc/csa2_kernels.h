@@ -100,12 +100,12 @@ int index_smem_bytes(int qpg);
 cudaError_t launch_index(const IndexParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_q,
                          int grid, cudaStream_t s);
 // MXFP4 keys (codes [idx_rows, 64], scales [idx_rows, 4], idx_rows a
-// multiple of 256): tm_kq views the codes as aligned 128-key tiles in the
+// multiple of 512): tm_kq views the codes as aligned 128-key tiles in the
 // permuted row order of the kernel (key 4 r + q of a tile in shared-memory
 // row 32 q + r, 64-byte rows, 64-byte swizzle), tm_kc8 as [idx_total, 64]
 // in boxes of 8 rows (pool blocks, 64-byte swizzle).  qpg is 1 (decode,
-// pool mode) or 4 (prefill).  Decode tiles (no pool) are the aligned 256-key
-// chunks: a sequence at key row off has ceil((n + off % 256) / 256) tiles;
+// pool mode) or 4 (prefill).  Decode tiles (no pool) are the aligned 512-key
+// chunks: a sequence at key row off has ceil((n + off % 512) / 512) tiles;
 // prefill tiles the aligned 128-key chunks, ceil((n + off % 128) / 128) per
 // group.
 int index_fp4_smem_bytes();

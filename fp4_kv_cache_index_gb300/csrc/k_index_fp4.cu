@@ -33,15 +33,23 @@
 //               copy of its scale words (contiguous tiles), or a box per
 //               block and a 4-byte copy per scale word into its atom place
 //               (pool mode);
-//   warp 1      MMA issuer (and TMEM owner): per tile the scale-atom copies
-//               into tensor memory, then the MMAs, one accumulator per tile;
+//   warp 1      MMA issuer (and TMEM owner): per tile the MMAs, one
+//               accumulator per tile, once its key scales are in place;
 //   warps 2-9   epilogue: ReLU, head weights, fp32 or bf16 score store,
 //               score-key histogram (the bf16 indexer's);
 //   warps 10-11 query preparation: at every new query group the bf16 query
 //               heads are rounded to MXFP4 codes and scales into one of two
-//               B slots, ahead of the MMAs of that group.
-// Tiles: 256 keys (two M = 128 groups) for one query per group (decode and
-// pool mode), 128 keys for four queries per group (prefill, N = 128).
+//               B slots, ahead of the MMAs of that group;
+//   warp 12     scale copies of decode tiles: per tile, once it has
+//               landed, the key scale atoms into its stage's scale columns
+//               (tcgen05.cp; the stage's previous tile was read by MMAs that
+//               completed before the stage was refilled), signalled to the
+//               MMA issuer by a commit (a single thread issuing every tcgen05
+//               instruction of a tile was the decode kernel's bound).  In
+//               pool mode and prefill the MMA issuer copies them itself.
+// Tiles: 512 keys (four M = 128 groups) for one query per group over
+// contiguous keys (decode), 256 pool slots (two M-groups) in pool mode, 128
+// keys for four queries per group (prefill, N = 128).
 // Every wait is bounded.
 #include "csa2_device.cuh"
 #include "csa2_kernels.h"
@@ -49,35 +57,35 @@
 namespace csa2 {
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 416;
 constexpr int kEpiThreads = 256;   // warps 2-9
 constexpr int kEpiWarps = kEpiThreads / 32;
 constexpr int kPrepBase = 320;     // warps 10-11
+constexpr int kSfWarp = 12;        // scale-atom copies
 constexpr int kPrepThreads = 64;
 constexpr int kPrepWarps = kPrepThreads / 32;
 #ifndef CSA2_FP4_STAGES
-#define CSA2_FP4_STAGES 8
-#endif
-#ifndef CSA2_FP4_NACC
-#define CSA2_FP4_NACC 4
+#define CSA2_FP4_STAGES 5
 #endif
 constexpr int kStages = CSA2_FP4_STAGES;
-constexpr int kTileMax = 256;
-constexpr int kCodeStage = kTileMax * (kIdxDim / 2);   // 16 KB of E2M1 codes
+constexpr int kTileMax = 512;
+constexpr int kCodeStage = kTileMax * (kIdxDim / 2);   // 32 KB of E2M1 codes
 constexpr int kSfAtom = 512;                           // scales of 128 rows
-constexpr int kStageBytes = kCodeStage + (kTileMax / 128) * kSfAtom;   // 17 KB
+constexpr int kStageBytes = kCodeStage + (kTileMax / 128) * kSfAtom;   // 34 KB
 constexpr int kMaxQpg = 4;
 constexpr int kBRows = 32 * kMaxQpg;
 constexpr int kBSlotBytes = 9216;    // 8 KB of query codes + one scale atom (1024-aligned)
 constexpr int kPf = 4;               // tiles of scale words loaded ahead by the producer
-constexpr int kNAcc = CSA2_FP4_NACC;   // accumulators of one query's tiles (64 columns each)
-// tensor-memory columns: accumulators, then the key scales of each
-// accumulator's tile, then the query scales of the two B slots
-constexpr uint32_t kAccCols = 384;     // the accumulators fit below this column
-constexpr uint32_t kSfaCol = kAccCols;           // [kNAcc][2 M-groups][4 columns]
-constexpr uint32_t kSfbCol = kSfaCol + 8 * kNAcc;  // [2 B slots][4 columns]
+constexpr int kNAcc = 4;               // accumulators at most
+// tensor-memory columns: accumulators (as many as fit below kAccCols, at
+// most kNAcc), then the key scales of each stage's tile (4 columns per
+// M-group), then the query scales of the two B slots
+constexpr uint32_t kAccCols = 384;
+constexpr uint32_t kSfaCols = 16 * kStages;        // [kStages][4 M-groups][4 columns]
+constexpr uint32_t kSfaCol = kAccCols;
+constexpr uint32_t kSfbCol = kSfaCol + kSfaCols;   // [2 B slots][4 columns]
 constexpr uint32_t kTmemCols = 512;
-static_assert(kNAcc * 64 <= (int)kAccCols && kSfbCol + 8 <= kTmemCols, "tensor memory");
+static_assert(kSfbCol + 8 <= kTmemCols, "tensor memory");
 
 constexpr int kMaxPoolIds = 4096;    // block ids of one query's pool (pool mode)
 
@@ -92,8 +100,8 @@ __host__ __device__ inline SmemLayout smem_layout() {
   L.hist_off = L.w_off + kBRows * 4;
   L.ids_off = L.hist_off + kKeyHistBins * 4;
   L.bar_off = L.ids_off + kMaxPoolIds * 4;
-  L.total = L.bar_off + 56 * 8 + 16 + 1024;   // barriers, tmem slot, alignment slack
-  static_assert(kStages <= 16 && kNAcc <= 8, "barrier slots");
+  L.total = L.bar_off + 64 * 8 + 16 + 1024;   // barriers, tmem slot, alignment slack
+  static_assert(kStages <= 6 && kNAcc <= 8, "barrier slots");
   return L;
 }
 
@@ -261,15 +269,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* b_full = bars + 48;            // [2]
   uint64_t* b_empty = bars + 50;           // [2]
   uint64_t* drain = bars + 52;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 54);
+  uint64_t* sf_drain = bars + 53;
+  uint64_t* sf_full = bars + 56;           // [kStages]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 62);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = 32 * p.qpg;                      // MMA N
-  const int tile_e = p.qpg == 1 ? 256 : 128;     // keys per tile
-  const int mgroups = tile_e / 128;
-  const int acc_cols = mgroups * N;              // 64 (one query) or 128 (four)
-  const int nacc = acc_cols == 64 ? kNAcc : 2;   // accumulators below kAccCols
   const bool pool = p.pool != nullptr;
+  // keys (pool slots) per tile: 512 for one query over contiguous keys, 256
+  // in pool mode, 128 for four queries
+  const int tile_e = p.qpg == 1 ? (pool ? 256 : 512) : 128;
+  const int mgroups = tile_e / 128;
+  const int acc_cols = mgroups * N;              // 128, 64 or 128 columns
+  const int nacc = min(kNAcc, (int)kAccCols / acc_cols);   // 3, 4 or 3 accumulators
   const int blocks_per_tile = tile_e / 8;
   // Contiguous keys: tiles are aligned chunks of tile_e key rows, so a
   // sequence starting inside a chunk begins `lead` keys into its first tile
@@ -277,6 +289,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (sl & ~127) + 4 (sl & 31) + (sl >> 5) % 4 of the tile.  Pool mode: slot
   // sl is pool slot sl of the tile, no permutation.
   const bool perm = !pool;
+  // decode over contiguous keys: the key scale copies run on their own warp
+  // (elsewhere the epilogue bounds the pipeline and the MMA issuer copies
+  // them itself)
+  const bool sf_warp = perm && p.qpg == 1;
   auto slot_key = [&](int sl) -> int {
     return perm ? (sl & ~127) + 4 * (sl & 31) + ((sl >> 5) & 3) : sl;
   };
@@ -291,7 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kStages; ++i) { mbar_init(k_full + i, pool ? 33 : 1); mbar_init(k_empty + i, 1); }
     for (int i = 0; i < kNAcc; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, kEpiWarps); }
     for (int i = 0; i < 2; ++i) { mbar_init(b_full + i, kPrepWarps); mbar_init(b_empty + i, 1); }
+    for (int i = 0; i < kStages; ++i) mbar_init(sf_full + i, 1);
     mbar_init(drain, 1);
+    mbar_init(sf_drain, 1);
     fence_barrier_init();
     tma_prefetch_desc(pool ? &tm_kc8 : &tm_kq);
   }
@@ -411,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (armed & (1u << s)) mbar_wait(k_full + s, (armed_ph >> s) & 1u, p.err, wl);
     }
     __syncwarp();
-  } else if (warp >= kPrepBase / 32 && begin < end) {
+  } else if (warp >= kPrepBase / 32 && warp < kSfWarp && begin < end) {
     // ------------------------------------------------ query preparation
     const int pt = threadIdx.x - kPrepBase;
     const int qrows = 32 * p.qpg;
@@ -441,6 +459,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(b_full + slot);
       ++gi;
     }
+  } else if (warp == kSfWarp && lane == 0 && sf_warp && begin < end) {
+    // ------------------------------------------------ scale copies
+    const uint64_t atom_desc0 = sdesc_atom(smem_u32(stages + kCodeStage));
+    int stage = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int it = begin; it < end && ok; ++it) {
+      ok = mbar_wait(k_full + stage, ph, p.err, wl);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t so = (uint32_t)(stage * kStageBytes) >> 4;
+      const uint32_t sfa = tmem_base + kSfaCol + (uint32_t)(stage * 16);
+      for (int mg = 0; mg < mgroups; ++mg)
+        tmem_cp_atom(sfa + 4 * mg, atom_desc0 + so + (uint32_t)(mg * (kSfAtom >> 4)));
+      umma_commit(sf_full + stage);
+      if (++stage == kStages) { stage = 0; ph ^= 1; }
+    }
+    umma_commit(sf_drain);
+    mbar_wait(sf_drain, 0, p.err, wl);
   } else if (warp == 1 && lane == 0 && begin < end) {
     // ------------------------------------------------ MMA issuer
     // Shared-memory descriptors built once; a tile's offsets go into the
@@ -467,16 +504,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* ba = bslots + (gi & 1) * kBSlotBytes + kBRows * (kIdxDim / 2);
         tmem_cp_atom(tmem_base + kSfbCol + 4 * (gi & 1), sdesc_atom(smem_u32(ba)));
       }
-      ok = mbar_wait(k_full + stage, ph, p.err, wl) && mbar_wait(acc_empty + acc, aph ^ 1, p.err, wl);
+      // the tile's codes have landed, its key scales are in tensor memory
+      // and its accumulator is free
+      ok = mbar_wait(k_full + stage, ph, p.err, wl) &&
+           (!sf_warp || mbar_wait(sf_full + stage, ph, p.err, wl)) &&
+           mbar_wait(acc_empty + acc, aph ^ 1, p.err, wl);
       if (!ok) break;
       tc_fence_after();
-      // pool mode: the scale words arrived by generic-proxy copies, which
-      // tcgen05.cp reads through the async proxy (bulk copies are async)
-      if (pool) fence_proxy_async_smem();
       const uint32_t so = (uint32_t)(stage * kStageBytes) >> 4;   // stage offset, 16-byte units
-      const uint32_t sfa = tmem_base + kSfaCol + (uint32_t)(acc * 8);
-      for (int mg = 0; mg < mgroups; ++mg)
-        tmem_cp_atom(sfa + 4 * mg, atom_desc0 + so + (uint32_t)(mg * (kSfAtom >> 4)));
+      const uint32_t sfa = tmem_base + kSfaCol + (uint32_t)(stage * 16);
+      if (!sf_warp) {
+        // pool mode: the scale words arrived by generic-proxy copies, which
+        // tcgen05.cp reads through the async proxy
+        if (pool) fence_proxy_async_smem();
+        for (int mg = 0; mg < mgroups; ++mg)
+          tmem_cp_atom(sfa + 4 * mg, atom_desc0 + so + (uint32_t)(mg * (kSfAtom >> 4)));
+      }
       const uint32_t bo = (uint32_t)((gi & 1) * kBSlotBytes) >> 4;
       const uint32_t sfb = tmem_base + kSfbCol + 4 * (gi & 1);
       for (int mg = 0; mg < mgroups; ++mg) {
@@ -499,9 +542,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ epilogue
     const int quad = warp & 3;                 // TMEM lane quadrant
     const int et = threadIdx.x - 64;           // 0..255
-    const int half = (warp - 2) >> 2;          // M-group (one query) or query pair (four)
-    const int row = (p.qpg == 1 ? half * 128 : 0) + quad * 32 + lane;   // slot of the tile
-    const int key = slot_key(row);             // its key, from the tile's first key row
+    // one query: warps 2-5 take the first half of the tile's M-groups, warps
+    // 6-9 the second half (one or two M-groups each); four queries: warps
+    // 2-5 the queries 0-1, warps 6-9 the queries 2-3 of the one M-group
+    const int half = (warp - 2) >> 2;
+    const int mgh = p.qpg == 1 ? mgroups / 2 : 1;   // M-groups of one epilogue thread
+    const int slot0 = (p.qpg == 1 ? half * mgh * 128 : 0) + quad * 32 + lane;   // its first slot
     const bool use_hist = p.key_hist != nullptr && p.qpg == 1;
     const int qrows = 32 * p.qpg;
     auto esync = [&]() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
@@ -551,17 +597,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_sleep(acc_full + acc, aph, p.err, wl)) break;
       tc_fence_after();
       const int t = it - gc.lo;
-      // entry of this slot (pool mode: the pool slot)
-      const int e = t * tile_e + key - lead_of(gc);
-      int32_t blk = -1;     // pool mode: the block of this slot
-      if (pool && t * blocks_per_tile + (row >> 3) < p.pool_blocks)
-        blk = ids_s[(t - t_first) * blocks_per_tile + (row >> 3)];
+      const int lead = lead_of(gc);
       const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * acc_cols);
-      auto score_of = [&](const uint32_t (&r)[32], const float* wj) {
-        return relu_dot32(wj, r);
-      };
-      auto store = [&](int q, int nvis, float s) {
+      // score s of query q at slot `row` of the tile: entry e (pool mode: the
+      // pool slot, whose block decides validity)
+      auto store = [&](int row, int q, int nvis, float s) {
+        const int e = t * tile_e + slot_key(row) - lead;
         if (pool) {
+          int32_t blk = -1;
+          if (t * blocks_per_tile + (row >> 3) < p.pool_blocks)
+            blk = ids_s[(t - t_first) * blocks_per_tile + (row >> 3)];
           const int64_t ent = (int64_t)blk * 8 + (row & 7);
           const float v = (blk >= 0 && ent < nvis) ? s : -INFINITY;
           if (e < p.ld) {
@@ -579,13 +624,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
-      if (p.qpg == 1) {
+      if (p.qpg == 1 && mgh == 1) {
         uint32_t r[32];
         tmem_ld32(lane_base + (uint32_t)(half * N), r);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acc_empty + acc);
-        store(g, nv[0], score_of(r, wbuf));
+        store(slot0, g, nv[0], relu_dot32(wbuf, r));
+      } else if (p.qpg == 1) {
+        // M-groups 2 half and 2 half + 1: columns N apart
+        uint32_t ra[32], rb[32];
+        const uint32_t c0 = (uint32_t)(2 * half * N);
+        tmem_ld32x2(lane_base + c0, lane_base + c0 + (uint32_t)N, ra, rb);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty + acc);
+        store(slot0, g, nv[0], relu_dot32(wbuf, ra));
+        store(slot0 + 128, g, nv[0], relu_dot32(wbuf, rb));
       } else {
         uint32_t ra[32], rb[32];
         const int j = 2 * half;
@@ -593,8 +648,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acc_empty + acc);
-        store(g * p.qpg + j, nv[0], score_of(ra, wbuf + j * 32));
-        store(g * p.qpg + j + 1, nv[1], score_of(rb, wbuf + (j + 1) * 32));
+        store(slot0, g * p.qpg + j, nv[0], relu_dot32(wbuf + j * 32, ra));
+        store(slot0, g * p.qpg + j + 1, nv[1], relu_dot32(wbuf + (j + 1) * 32, rb));
       }
       if (++acc == nacc) { acc = 0; aph ^= 1; }
     }
