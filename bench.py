@@ -74,7 +74,7 @@ def parse_args(argv=None):
     p.add_argument("--micro-batches", type=int, default=2,
                    help="split the batch into this many micro-batches on their own streams "
                         "(1: one stream, the whole batch per kernel)")
-    p.add_argument("--index-sms", type=int, default=120,
+    p.add_argument("--index-sms", type=int, default=104,
                    help="SMs for the indexer's grid when micro-batches > 1 (the rest run "
                         "the other micro-batch's top-k and readout concurrently)")
     p.add_argument("--attn-split", action="store_true",
@@ -1170,8 +1170,9 @@ def measure_decode_config(C, W, wid, dev, stream, iters, hbm_peak, flush):
 
 def measure_prefill(C, W, wid, layout, dev, stream, steps, warmup):
     """Chunked prefill of one sequence: the Full layer's causal index scores
-    and top-512 of every new token, then the readout of the Full and the
-    Reuse layers.  Roofline: the dense bf16 tensor pipe (sustained figure) on
+    (with each token's score-key histogram, built by the indexer's epilogue)
+    and top-512 of every new token from them, then the readout of the Full
+    and the Reuse layers.  Roofline: the dense bf16 tensor pipe (sustained figure) on
     the step's FLOPs (indexer over the visible entries, attention over the
     selected entries and the causal window)."""
     import torch
@@ -1186,15 +1187,16 @@ def measure_prefill(C, W, wid, layout, dev, stream, steps, warmup):
     ld = (n_ent + 3) // 4 * 4
     scores = torch.empty(T, ld, dtype=torch.float32, device=dev)
     topk = torch.empty(T, 512, dtype=torch.int32, device=dev)
+    hist = torch.empty(T, 2048, dtype=torch.int32, device=dev)
     outs = [torch.empty(T, 64, 512, dtype=torch.bfloat16, device=dev) for _ in range(L)]
     n_valid = [min(n_ent, (wl.pos0 + i + 1) // wl.ratio) for i in range(T)]
     scale = 512 ** -0.5
 
     def index():
-        C.csa2_index_scores_prefill(cache, 0, wl.pos0, q_idx, w, scores)
+        C.csa2_index_scores_prefill(cache, 0, wl.pos0, q_idx, w, scores, key_hist=hist)
 
     def select():
-        C.csa2_topk(scores, n_valid, 512, idx_out=topk)
+        C.csa2_topk(scores, n_valid, 512, idx_out=topk, key_hist=hist)
 
     def readout():
         for l in range(L):

@@ -97,7 +97,8 @@ def _load():
         "csa2_index_topk_prefill": ([P, i32, i32, i64, P, P, P, P, P, sz, P], i32),
         "csa2_index_topk_decode_static": ([P, i32, P, P, P, P, P, P], i32),
         "csa2_index_topk": ([P, i32, P, P, P, P, P, P, P, sz, P], i32),
-        "csa2_index_scores_prefill": ([P, i32, i32, i64, P, P, P, i64, P], i32),
+        "csa2_index_scores_prefill": ([P, i32, i32, i64, P, P, P, i64, P, P], i32),
+        "csa2_index_prefill_workspace_bytes": ([P, i32, i32], sz),
         "csa2_index_scores_decode_bf16": ([P, i32, P, P, P, P, i64, P, P], i32),
         "csa2_topk_bf16": ([i32, P, i64, P, i32, P, P, P, P, sz, P], i32),
         "csa2_index_topk_decode_bf16": ([P, i32, P, P, P, P, P, P, sz, P], i32),
@@ -324,12 +325,18 @@ def csa2_index_topk(cache: Cache, q_idx: torch.Tensor, w: torch.Tensor,
 
 
 def csa2_index_scores_prefill(cache: Cache, seq: int, pos0: int, q_idx: torch.Tensor,
-                              w: torch.Tensor, scores: torch.Tensor, stream=None):
-    """scores: fp32 [n_queries, ld] (ld a multiple of 4, >= the length)."""
+                              w: torch.Tensor, scores: torch.Tensor,
+                              key_hist: Optional[torch.Tensor] = None, stream=None):
+    """scores: fp32 [n_queries, ld] (ld a multiple of 4, >= the length);
+    key_hist: int32 [n_queries, 2048] score-key histograms (bf16 keys)."""
     _check(lib.csa2_index_scores_prefill(cache.handle, seq, q_idx.shape[0], pos0, _ptr(q_idx),
-                                         _ptr(w), _ptr(scores), scores.shape[1],
+                                         _ptr(w), _ptr(scores), scores.shape[1], _ptr(key_hist),
                                          _stream(stream)), "csa2_index_scores_prefill")
     return scores
+
+
+def csa2_index_prefill_workspace_bytes(cache: Cache, seq: int, n_queries: int) -> int:
+    return int(lib.csa2_index_prefill_workspace_bytes(cache.handle, seq, n_queries))
 
 
 def csa2_index_topk_prefill(cache: Cache, seq: int, pos0: int, q_idx: torch.Tensor,
@@ -341,9 +348,7 @@ def csa2_index_topk_prefill(cache: Cache, seq: int, pos0: int, q_idx: torch.Tens
     dev = q_idx.device
     if topk_idx is None:
         topk_idx = torch.empty(nq, cache.cfg.topk, dtype=torch.int32, device=dev)
-    cap = cache.views()["entry_offset"]
-    ld = max(4, (cap[seq + 1] - cap[seq] + 3) // 4 * 4)
-    ws = _workspace(nq * ld * 4, dev, workspace)
+    ws = _workspace(csa2_index_prefill_workspace_bytes(cache, seq, nq), dev, workspace)
     _check(lib.csa2_index_topk_prefill(cache.handle, seq, nq, pos0, _ptr(q_idx), _ptr(w),
                                        _ptr(topk_idx), _ptr(topk_score), _ptr(ws),
                                        ws.numel() * ws.element_size(), _stream(stream)),

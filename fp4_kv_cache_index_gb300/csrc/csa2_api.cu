@@ -508,6 +508,13 @@ size_t csa2_index_workspace_bytes(const csa2_cache_t* c, int32_t n_queries) {
          topk_seg_bytes(n_queries, c->max_cap);
 }
 
+size_t csa2_index_prefill_workspace_bytes(const csa2_cache_t* c, int32_t seq, int32_t n_queries) {
+  if (!c || seq < 0 || seq >= c->batch || n_queries < 0) return 0;
+  size_t b = (size_t)n_queries * (size_t)score_ld(c->cap[seq]) * sizeof(float);
+  if (c->cfg.idx_layout == CSA2_IDX_BF16) b += (size_t)n_queries * kKeyHistBinsHost * sizeof(uint32_t);
+  return b;
+}
+
 size_t csa2_topk_workspace_bytes(int32_t n_rows, int64_t max_valid) {
   if (n_rows < 0 || max_valid < 0) return 0;
   return topk_seg_bytes(n_rows, max_valid);
@@ -603,9 +610,9 @@ csa2_status_t run_index_decode(const csa2_cache_t* c, int32_t nq, const void* q_
       cudaMemsetAsync(key_hist, 0, (size_t)nq * kKeyHistBinsHost * sizeof(uint32_t), S(stream)) !=
           cudaSuccess)
     return CSA2_ERR_CUDA;
-  // keys per tile: the MXFP4 decode kernel takes 512, every other path 128
+  // keys per decode tile: 512 for MXFP4 keys, 256 for bf16 keys
   const bool mx = c->cfg.idx_layout == CSA2_IDX_MXFP4;
-  const int64_t tile_e = mx ? 512 : 128;
+  const int64_t tile_e = mx ? 512 : 256;
   for (int q0 = 0; q0 < nq; q0 += kMaxIdxGroups) {
     const int n = std::min(kMaxIdxGroups, nq - q0);
     std::memset(ip, 0, sizeof(IndexParams));
@@ -788,17 +795,25 @@ csa2_status_t csa2_index_scores_decode_bf16(const csa2_cache_t* c, int32_t nq, c
 
 csa2_status_t csa2_index_scores_prefill(const csa2_cache_t* c, int32_t seq, int32_t nq,
                                         int64_t pos0, const void* q_idx, const float* w,
-                                        float* scores, int64_t ld, csa2_stream_t stream) {
+                                        float* scores, int64_t ld, uint32_t* key_hist,
+                                        csa2_stream_t stream) {
   CSA2_RANGE();
   if (!c || nq < 0 || seq < 0 || seq >= c->batch || pos0 < 0) return CSA2_ERR_INVALID_ARG;
   if (nq == 0) return CSA2_OK;
   if (!q_idx || !w || !scores || !aligned16(q_idx) || !aligned16(w) || !aligned16(scores) ||
-      ld % 4 != 0)
+      ld % 4 != 0 || (key_hist && !aligned16(key_hist)))
     return CSA2_ERR_INVALID_ARG;
   if (ld < c->len[seq]) return CSA2_ERR_CAPACITY;
   // queries sharing one tile of keys in the MMA: 8 (N = 256) on bf16 keys,
   // 4 (N = 128) on MXFP4 keys, whose tensor memory also holds the scales
   const bool mx = c->cfg.idx_layout == CSA2_IDX_MXFP4;
+  // the score-key histograms come from the bf16 indexer's epilogue (the
+  // MXFP4 kernel's shared memory has no room for eight of them)
+  if (key_hist && mx) return CSA2_ERR_UNSUPPORTED;
+  if (key_hist &&
+      cudaMemsetAsync(key_hist, 0, (size_t)nq * kKeyHistBinsHost * sizeof(uint32_t), S(stream)) !=
+          cudaSuccess)
+    return CSA2_ERR_CUDA;
   const int kQpg = mx ? 4 : 8;
   const int m = c->cfg.ratio;
   const int64_t len = c->len[seq];
@@ -814,6 +829,7 @@ csa2_status_t csa2_index_scores_prefill(const csa2_cache_t* c, int32_t seq, int3
     ip->w = w + (int64_t)q0 * kIdxHeads;
     ip->scores = scores + (int64_t)q0 * ld;
     ip->ld = ld;
+    ip->key_hist = key_hist ? key_hist + (int64_t)q0 * kKeyHistBinsHost : nullptr;
     ip->err = c->d_err;
     ip->nq = n;
     ip->qpg = kQpg;
@@ -858,14 +874,21 @@ csa2_status_t csa2_index_topk_prefill(const csa2_cache_t* c, int32_t seq, int32_
   if (!c || nq < 0 || seq < 0 || seq >= c->batch || pos0 < 0) return CSA2_ERR_INVALID_ARG;
   if (nq == 0) return CSA2_OK;
   if (!topk_idx || !workspace || !aligned16(workspace)) return CSA2_ERR_INVALID_ARG;
+  if (ws_bytes < csa2_index_prefill_workspace_bytes(c, seq, nq)) return CSA2_ERR_CAPACITY;
   const int64_t ld = score_ld(c->cap[seq]);
-  if (ws_bytes < (size_t)nq * (size_t)ld * sizeof(float)) return CSA2_ERR_CAPACITY;
+  // workspace: scores [nq, ld], then (bf16 keys) the score-key histograms
+  // [nq, 2048] that the indexer builds for the top-k's first digit
   float* scores = static_cast<float*>(workspace);
-  csa2_status_t st = csa2_index_scores_prefill(c, seq, nq, pos0, q_idx, w, scores, ld, stream);
+  uint32_t* key_hist = c->cfg.idx_layout == CSA2_IDX_BF16
+                           ? reinterpret_cast<uint32_t*>(scores + (size_t)nq * ld)
+                           : nullptr;
+  csa2_status_t st =
+      csa2_index_scores_prefill(c, seq, nq, pos0, q_idx, w, scores, ld, key_hist, stream);
   if (st != CSA2_OK) return st;
   TopkParams* tp = new (std::nothrow) TopkParams();
   if (!tp) return CSA2_ERR_OOM;
   tp->scores = scores;
+  tp->key_hist = key_hist;
   tp->ld = ld;
   tp->rows = nq;
   tp->k = c->cfg.topk;

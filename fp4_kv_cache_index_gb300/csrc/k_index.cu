@@ -5,12 +5,14 @@
 //     I[q, s] = sum_h w[q, h] * ReLU(q_idx[q, h] . K_I[s])
 // with 32 heads of dim 128 (V4.1 report, section 4.2.1).
 //
-// Mapping: one MMA tile is D[128 entries x 32*qpg] = K_I[128 x 128] *
+// Mapping: one MMA is D[128 entries x 32*qpg] = K_I[128 x 128] *
 // Q[32*qpg x 128]^T (M = 128 entries, N = heads of qpg queries, K = 128), bf16
 // operands from 128B-swizzled shared memory, fp32 accumulators in TMEM.  The
 // ReLU and the head-weighted sum run in the epilogue on the accumulator rows.
-// Decode uses qpg = 1 (each query reads its own sequence); prefill groups 8
-// consecutive queries of one sequence so that a K_I tile feeds 256 columns.
+// Decode uses qpg = 1 (each query reads its own sequence) with tiles of two
+// such M-groups (256 keys: half the per-tile waits and commits of the MMA
+// issuer per key); prefill groups 8 consecutive queries of one sequence so
+// that a 128-key K_I tile feeds 256 columns.
 //
 // Pool mode (Reindex layers of the Hierarchical Sparse Indexer, V4.1 report
 // section 2.3.2): a tile is 16 blocks of 8 consecutive keys named by the
@@ -36,12 +38,22 @@
 namespace csa2 {
 namespace {
 
-constexpr int kTileE = 128;
-constexpr int kStages = 4;
-constexpr int kKStageBytes = kTileE * kIdxDim * 2;  // 32 KB
+constexpr int kTileE = 128;                          // keys of one M-group
+constexpr int kMGroupBytes = kTileE * kIdxDim * 2;   // 32 KB
+constexpr int kMaxStages = 4;
 constexpr int kMaxQpg = 8;                 // queries per group (N <= 256)
 constexpr int kMaxAcc = 4;                 // accumulators in TMEM (decode 4, several queries 2)
-constexpr int kBars = 2 * kStages + 2 * kMaxAcc + 4;   // k full / empty, acc full / empty, q full / empty, drain
+constexpr int kBars = 2 * kMaxStages + 2 * kMaxAcc + 4;   // k full / empty, acc full / empty, q full / empty, drain
+
+// One query per group: stages of two M-groups (decode tiles are 256
+// contiguous keys; a pool tile, 16 blocks of 8, fills one); several
+// queries: stages of one M-group (128-key tiles).  Three stages either way
+// (with several queries the score-key histograms of the group's queries
+// take the room of a fourth).
+__host__ __device__ constexpr int stages_of(int) { return 3; }
+__host__ __device__ constexpr int stage_bytes_of(int qpg) {
+  return qpg == 1 ? 2 * kMGroupBytes : kMGroupBytes;
+}
 
 struct SmemLayout {
   int q_off, w_off, hist_off, bar_off, total;
@@ -49,10 +61,11 @@ struct SmemLayout {
 
 __host__ __device__ inline SmemLayout smem_layout(int qpg) {
   SmemLayout L;
-  L.q_off = kStages * kKStageBytes;
+  L.q_off = stages_of(qpg) * stage_bytes_of(qpg);
   L.w_off = L.q_off + qpg * 32 * kIdxDim * 2;
   L.hist_off = L.w_off + (qpg > 2 ? qpg : 2) * 32 * 4;
-  L.bar_off = L.hist_off + (qpg == 1 ? 2 : 1) * kKeyHistBins * 4;   // decode: one per tile group
+  // one histogram per epilogue set (one query per group) or per query
+  L.bar_off = L.hist_off + (qpg == 1 ? 2 : qpg) * kKeyHistBins * 4;
   L.total = L.bar_off + kBars * 8 + 16 + 1024;  // barriers, tmem slot, alignment slack
   return L;
 }
@@ -109,9 +122,9 @@ __global__ void __launch_bounds__(64 + 32 * kEpiW, 1)
   float* wbuf = reinterpret_cast<float*>(smem + L.w_off);
   uint32_t* hs = reinterpret_cast<uint32_t*>(smem + L.hist_off);  // score-key histogram
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
-  uint64_t* k_full = bars;                    // [kStages]
-  uint64_t* k_empty = bars + kStages;         // [kStages]
-  uint64_t* acc_full = bars + 2 * kStages;    // [kMaxAcc]
+  uint64_t* k_full = bars;                    // [n_stages]
+  uint64_t* k_empty = bars + kMaxStages;      // [n_stages]
+  uint64_t* acc_full = bars + 2 * kMaxStages; // [kMaxAcc]
   uint64_t* acc_empty = acc_full + kMaxAcc;   // [kMaxAcc]
   uint64_t* q_full = acc_full + 2 * kMaxAcc;
   uint64_t* q_empty = q_full + 1;
@@ -119,15 +132,21 @@ __global__ void __launch_bounds__(64 + 32 * kEpiW, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBars);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int N = 32 * p.qpg;               // MMA N (columns per accumulator)
+  const int N = 32 * p.qpg;               // MMA N (columns per M-group)
   const int qrows = 32 * p.qpg;
-  // decode (one query, N = 32) keeps four accumulators in flight, several
-  // queries per tile (N = 256) two
+  const int n_stages = stages_of(p.qpg), stage_bytes = stage_bytes_of(p.qpg);
+  // decode tiles: two M-groups of 128 contiguous keys; pool and several
+  // queries: one
+  const int mgroups = (p.qpg == 1 && !p.pool) ? 2 : 1;
+  const int tile_e = kTileE * mgroups;
+  const int acc_cols = mgroups * N;
+  // one query (N = 32) keeps four accumulators in flight, several queries
+  // per tile (N = 256) two
   const int nacc = p.qpg == 1 ? 4 : 2;
-  const uint32_t tmem_cols = (N * nacc <= 32) ? 32u : (uint32_t)(N * nacc);
+  const uint32_t tmem_cols = (acc_cols * nacc <= 32) ? 32u : (uint32_t)(acc_cols * nacc);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) { mbar_init(k_full + i, 1); mbar_init(k_empty + i, 1); }
+    for (int i = 0; i < n_stages; ++i) { mbar_init(k_full + i, 1); mbar_init(k_empty + i, 1); }
     // acc_empty: decode, every thread of the set of four warps that took the
     // tile; several queries, one arrival per epilogue warp
     for (int i = 0; i < nacc; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, p.qpg == 1 ? 128 : kEpiW); }
@@ -193,10 +212,10 @@ __global__ void __launch_bounds__(64 + 32 * kEpiW, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       if (p.inject & kInjectNoKeyLoads) {   // tests: nothing arrives on k_full
-        if (++stage == kStages) { stage = 0; ph ^= 1; }
+        if (++stage == n_stages) { stage = 0; ph ^= 1; }
         continue;
       }
-      uint8_t* dst = kbuf + stage * kKStageBytes;
+      uint8_t* dst = kbuf + stage * stage_bytes;
       if (p.pool) {
         const int32_t blk = nxt;
         if (pool_lane && it + 1 < end) nxt = __ldg(pool_row(it + 1, gc) + lane);
@@ -208,18 +227,23 @@ __global__ void __launch_bounds__(64 + 32 * kEpiW, 1)
           tma_load_3d(dst + lane * 2048, &tm_k, 0, row, 0, k_full + stage, keys_pol);
         }
       } else if (lane == 0) {
-        const int64_t row = gbase + (int64_t)(it - gc.lo) * kTileE;
-        mbar_arrive_expect_tx(k_full + stage, kKStageBytes);
-        tma_load_2d(dst, &tm_k, 0, (int32_t)row, k_full + stage, keys_pol);
-        tma_load_2d(dst + kKStageBytes / 2, &tm_k, 64, (int32_t)row, k_full + stage, keys_pol);
+        // each M-group: its two 64-channel column halves
+        const int64_t row = gbase + (int64_t)(it - gc.lo) * tile_e;
+        mbar_arrive_expect_tx(k_full + stage, (uint32_t)(mgroups * kMGroupBytes));
+        for (int mg = 0; mg < mgroups; ++mg) {
+          uint8_t* d = dst + mg * kMGroupBytes;
+          const int32_t r = (int32_t)(row + mg * kTileE);
+          tma_load_2d(d, &tm_k, 0, r, k_full + stage, keys_pol);
+          tma_load_2d(d + kMGroupBytes / 2, &tm_k, 64, r, k_full + stage, keys_pol);
+        }
       }
       armed |= 1u << stage;
       armed_ph = (armed_ph & ~(1u << stage)) | (ph << stage);
-      if (++stage == kStages) { stage = 0; ph ^= 1; }
+      if (++stage == n_stages) { stage = 0; ph ^= 1; }
     }
     // make sure no bulk copy is still writing into this CTA's shared memory
     if (lane == 0) {
-      for (int s = 0; s < kStages; ++s)
+      for (int s = 0; s < n_stages; ++s)
         if (armed & (1u << s)) mbar_wait(k_full + s, (armed_ph >> s) & 1u, p.err, wl);
       if (cur >= 0) mbar_wait(q_full, qph ^ 1, p.err, wl);
     }
@@ -231,7 +255,7 @@ __global__ void __launch_bounds__(64 + 32 * kEpiW, 1)
     // pool tiles: halves 1 KB apart inside each block's 2 KB.  Descriptor
     // bases built once; the offsets go into the address field (shared
     // memory is below 2^18 bytes, so it never carries).
-    const uint32_t a_half = p.pool ? 1024u : (uint32_t)(kKStageBytes / 2);
+    const uint32_t a_half = p.pool ? 1024u : (uint32_t)(kMGroupBytes / 2);
     const uint64_t adesc0 = sdesc_sw128(smem_u32(kbuf), 16, p.pool ? 2048u : 1024u);
     const uint64_t bdesc0 = sdesc_sw128(smem_u32(qbuf), 16, 1024);
     GroupCursor gc = c0;
@@ -250,19 +274,22 @@ __global__ void __launch_bounds__(64 + 32 * kEpiW, 1)
       ok = mbar_wait(k_full + stage, ph, p.err, wl) && mbar_wait(acc_empty + acc, aph ^ 1, p.err, wl);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t d = tmem_base + (uint32_t)(acc * N);
-      const uint64_t adesc = adesc0 + (uint64_t)((stage * kKStageBytes) >> 4);
+      const uint64_t adesc = adesc0 + (uint64_t)((stage * stage_bytes) >> 4);
+      for (int mg = 0; mg < mgroups; ++mg) {
+        const uint32_t d = tmem_base + (uint32_t)(acc * acc_cols + mg * N);
 #pragma unroll
-      for (int ks = 0; ks < kIdxDim / 16; ++ks) {
-        const uint32_t ao = (uint32_t)(ks >> 2) * a_half + (uint32_t)(ks & 3) * 32u;
-        const uint32_t bo = (uint32_t)((ks >> 2) * (qrows * 128) + (ks & 3) * 32);
-        umma_bf16(d, adesc + (ao >> 4), bdesc0 + (bo >> 4), idesc, ks > 0 ? 1u : 0u);
+        for (int ks = 0; ks < kIdxDim / 16; ++ks) {
+          const uint32_t ao = (uint32_t)(mg * kMGroupBytes) + (uint32_t)(ks >> 2) * a_half +
+                              (uint32_t)(ks & 3) * 32u;
+          const uint32_t bo = (uint32_t)((ks >> 2) * (qrows * 128) + (ks & 3) * 32);
+          umma_bf16(d, adesc + (ao >> 4), bdesc0 + (bo >> 4), idesc, ks > 0 ? 1u : 0u);
+        }
       }
       umma_commit(k_empty + stage);
       umma_commit(acc_full + acc);
       const bool last_of_group = (it + 1 == end) || (gc.hi <= it + 1);
       if (last_of_group) umma_commit(q_empty);
-      if (++stage == kStages) { stage = 0; ph ^= 1; }
+      if (++stage == n_stages) { stage = 0; ph ^= 1; }
       if (++acc == nacc) { acc = 0; aph ^= 1; }
     }
     umma_commit(drain);
@@ -316,28 +343,42 @@ __global__ void __launch_bounds__(64 + 32 * kEpiW, 1)
       if (!mbar_wait_sleep(acc_full + a, (uint32_t)((jt >> 2) & 1), p.err, wl)) break;
       tc_fence_after();
       const int t = it - gc.lo;
-      const int e = t * kTileE + row;
-      uint32_t r[32];
-      tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * N), r);
-      tc_fence_before();
-      mbar_arrive(acc_empty + a);   // the accumulator is free once read
-      const float s = relu_dot32(wg, r);
-      if (p.pool) {
-        const int64_t ent = (int64_t)blk * 8 + (row & 7);
-        const float v = (blk >= 0 && ent < nvis) ? s : -INFINITY;
-        if (CSA2_IN_BOUNDS(e < p.ld, p.err)) {
-          p.scores[(int64_t)g * p.ld + e] = v;
-          if (use_hist) atomicAdd(hsg + (score_key(v) >> 21), 1u);
+      const uint32_t ta = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * acc_cols);
+      // entry row + 128 mg of the tile: score s
+      auto store = [&](int mg, float s) {
+        const int e = t * tile_e + mg * kTileE + row;
+        if (p.pool) {
+          const int64_t ent = (int64_t)blk * 8 + (row & 7);
+          const float v = (blk >= 0 && ent < nvis) ? s : -INFINITY;
+          if (CSA2_IN_BOUNDS(e < p.ld, p.err)) {
+            p.scores[(int64_t)g * p.ld + e] = v;
+            if (use_hist) atomicAdd(hsg + (score_key(v) >> 21), 1u);
+          }
+        } else if (g < p.nq && e < nvis && CSA2_IN_BOUNDS(e < p.ld, p.err)) {
+          if (p.score_bf16) {
+            const uint32_t b = float_to_bf16_bits(s);
+            reinterpret_cast<uint16_t*>(p.scores)[(int64_t)g * p.ld + e] = (uint16_t)b;
+            if (use_hist) atomicAdd(hsg + (score_key(bf16_bits_to_float(b)) >> 21), 1u);
+          } else {
+            p.scores[(int64_t)g * p.ld + e] = s;
+            if (use_hist) atomicAdd(hsg + (score_key(s) >> 21), 1u);
+          }
         }
-      } else if (g < p.nq && e < nvis && CSA2_IN_BOUNDS(e < p.ld, p.err)) {
-        if (p.score_bf16) {
-          const uint32_t b = float_to_bf16_bits(s);
-          reinterpret_cast<uint16_t*>(p.scores)[(int64_t)g * p.ld + e] = (uint16_t)b;
-          if (use_hist) atomicAdd(hsg + (score_key(bf16_bits_to_float(b)) >> 21), 1u);
-        } else {
-          p.scores[(int64_t)g * p.ld + e] = s;
-          if (use_hist) atomicAdd(hsg + (score_key(s) >> 21), 1u);
-        }
+      };
+      if (mgroups == 2) {
+        // both M-groups of the tile: columns 0 and N of its accumulator
+        uint32_t ra[32], rb[32];
+        tmem_ld32x2(ta, ta + (uint32_t)N, ra, rb);
+        tc_fence_before();
+        mbar_arrive(acc_empty + a);   // the accumulator is free once read
+        store(0, relu_dot32(wg, ra));
+        store(1, relu_dot32(wg, rb));
+      } else {
+        uint32_t r[32];
+        tmem_ld32(ta, r);
+        tc_fence_before();
+        mbar_arrive(acc_empty + a);
+        store(0, relu_dot32(wg, r));
       }
     }
     if (use_hist && cur >= 0) flush(cur);
@@ -349,20 +390,24 @@ __global__ void __launch_bounds__(64 + 32 * kEpiW, 1)
     const int part = (warp - 2) >> 2;          // which queries of the group
     const int jq = (p.qpg + kParts - 1) / kParts;
     const int j0 = part * jq, j1 = min(p.qpg, j0 + jq);
-    const bool use_hist = p.key_hist != nullptr && p.qpg == 1;
-    // adds this CTA's counts of query `qq` to the global histogram, clears hs
+    // score-key histograms: one per query of the group, hs[j][bin]
+    const bool use_hist = p.key_hist != nullptr;
+    const int hbins = p.qpg * kKeyHistBins;
+    // adds this CTA's counts of group `gg`'s queries to the global
+    // histograms and clears hs
     auto esync = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); };
-    auto flush = [&](int qq) {
+    auto flush = [&](int gg) {
       esync();
-      for (int i = et; i < kKeyHistBins; i += kEpiThreads) {
+      for (int i = et; i < hbins; i += kEpiThreads) {
         const uint32_t v = hs[i];
-        if (v) atomicAdd(p.key_hist + (int64_t)qq * kKeyHistBins + i, v);
+        const int q = gg * p.qpg + i / kKeyHistBins;
+        if (v && q < p.nq) atomicAdd(p.key_hist + (int64_t)q * kKeyHistBins + (i % kKeyHistBins), v);
         hs[i] = 0u;
       }
       esync();
     };
     if (use_hist) {
-      for (int i = et; i < kKeyHistBins; i += kEpiThreads) hs[i] = 0u;
+      for (int i = et; i < hbins; i += kEpiThreads) hs[i] = 0u;
     }
     GroupCursor gc = c0;
     int cur = -1, acc = 0;
@@ -390,7 +435,7 @@ __global__ void __launch_bounds__(64 + 32 * kEpiW, 1)
       if (!mbar_wait(acc_full + acc, aph, p.err, wl)) break;
       tc_fence_after();
       const int t = it - gc.lo;
-      const int e = t * kTileE + row;
+      const int e = t * tile_e + row;
       // score of query j of the group from its 32 head columns r
       auto emit = [&](int j, int jj, const uint32_t (&r)[32]) {
         const float s = relu_dot32(wbuf + j * 32, r);
@@ -402,21 +447,22 @@ __global__ void __launch_bounds__(64 + 32 * kEpiW, 1)
           const float v = (blk >= 0 && ent < nv) ? s : -INFINITY;
           if (CSA2_IN_BOUNDS(e < p.ld, p.err)) {
             p.scores[(int64_t)q * p.ld + e] = v;
-            if (use_hist) atomicAdd(hs + (score_key(v) >> 21), 1u);
+            if (use_hist) atomicAdd(hs + j * kKeyHistBins + (score_key(v) >> 21), 1u);
           }
         } else if (q < p.nq && e < nv && CSA2_IN_BOUNDS(e < p.ld, p.err)) {
+          uint32_t* hq = hs + j * kKeyHistBins;
           if (p.score_bf16) {
             // the selector's precision: nearest bf16, its key histogrammed
             const uint32_t b = float_to_bf16_bits(s);
             reinterpret_cast<uint16_t*>(p.scores)[(int64_t)q * p.ld + e] = (uint16_t)b;
-            if (use_hist) atomicAdd(hs + (score_key(bf16_bits_to_float(b)) >> 21), 1u);
+            if (use_hist) atomicAdd(hq + (score_key(bf16_bits_to_float(b)) >> 21), 1u);
           } else {
             p.scores[(int64_t)q * p.ld + e] = s;
-            if (use_hist) atomicAdd(hs + (score_key(s) >> 21), 1u);
+            if (use_hist) atomicAdd(hq + (score_key(s) >> 21), 1u);
           }
         }
       };
-      const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * N);
+      const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * acc_cols);
       // the accumulator is free once this warp's last columns are read
       auto release = [&]() {
         tc_fence_before();

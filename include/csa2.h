@@ -324,7 +324,11 @@ csa2_status_t csa2_index_topk_decode_static(const csa2_cache_t* cache,
  * complete, (s + 1) * ratio - 1 <= pos0 + i ([V41 sec 2.3.2] "causally
  * visible"; [V4B sec 4.3]).  Same score, top-k and output rules as decode.
  *   q_idx: dev bf16 [n_queries, idx_heads, idx_dim];  w: dev fp32
- *   [n_queries, idx_heads];  topk_idx: dev int32 [n_queries, topk].        */
+ *   [n_queries, idx_heads];  topk_idx: dev int32 [n_queries, topk];
+ *   workspace: dev, 16-byte aligned, at least
+ *   csa2_index_prefill_workspace_bytes(cache, seq, n_queries) bytes (else
+ *   CSA2_ERR_CAPACITY): the scores, and with bf16 indexer keys the score-key
+ *   histograms the indexer builds for the top-k.                           */
 csa2_status_t csa2_index_topk_prefill(const csa2_cache_t* cache, int32_t seq,
                                       int32_t n_queries, int64_t pos0,
                                       const void* q_idx, const float* w,
@@ -332,18 +336,29 @@ csa2_status_t csa2_index_topk_prefill(const csa2_cache_t* cache, int32_t seq,
                                       void* workspace, size_t workspace_bytes,
                                       csa2_stream_t stream);
 
+/* Workspace bytes of csa2_index_topk_prefill for n_queries queries of
+ * sequence seq: n_queries * 4 * ld (ld = the sequence's capacity rounded up
+ * to a multiple of 4), plus n_queries * 8192 with bf16 indexer keys.  0 for
+ * invalid arguments.                                                       */
+size_t csa2_index_prefill_workspace_bytes(const csa2_cache_t* cache, int32_t seq,
+                                          int32_t n_queries);
+
 /* Index scores only for a prefill chunk (the scoring step of
  * csa2_index_topk_prefill): query i at position pos0 + i, scores[i * ld + s]
  * for every entry s visible to it ((s + 1) * ratio - 1 <= pos0 + i);
  * other entries are left untouched.  Eight consecutive queries share each
- * tile of indexer keys on the tensor cores.
+ * tile of indexer keys on the tensor cores (four with MXFP4 keys).
  *   scores: dev fp32 [n_queries, ld], ld >= the sequence's length and a
- *   multiple of 4;  other arguments as for csa2_index_topk_prefill.         */
+ *   multiple of 4;  key_hist: NULL or dev uint32 [n_queries, 2048], 16-byte
+ *   aligned: zeroed, then query i's row counts its visible scores by the
+ *   top 11 bits of their order-preserving key (the histogram csa2_topk
+ *   takes); bf16 indexer keys only (MXFP4 keys: CSA2_ERR_UNSUPPORTED);
+ *   other arguments as for csa2_index_topk_prefill.                        */
 csa2_status_t csa2_index_scores_prefill(const csa2_cache_t* cache, int32_t seq,
                                         int32_t n_queries, int64_t pos0,
                                         const void* q_idx, const float* w,
                                         float* scores, int64_t ld,
-                                        csa2_stream_t stream);
+                                        uint32_t* key_hist, csa2_stream_t stream);
 
 /* ---- Hierarchical Sparse Indexer and Reindex mode ([V41 sec 2.3.2]) -----
  * The first Full layer of the decoder also picks a candidate pool: every

@@ -76,6 +76,9 @@ def test_host_argument_errors(lib):
     assert L.csa2_cache_create(ctypes.byref(_cfg()), 1, caps, ctypes.c_void_p(0x1000), 64, None,
                                ctypes.byref(out)) == 3
     assert L.csa2_cache_destroy(None) == 1
+    # workspace sizes of an invalid request are 0
+    assert L.csa2_index_prefill_workspace_bytes(None, 0, 8) == 0
+    assert L.csa2_index_workspace_bytes(None, 8) == 0
     assert L.csa2_compress(0, 4, 512, None, None, None, None) == 1
     assert L.csa2_compress(2, 0, 512, None, None, None, None) == 0
     assert L.csa2_compress(32, 4, 512, None, None, None, None) == 2

@@ -90,6 +90,31 @@ def test_prefill_causal(C, pos0, ratio):
         check_topk(idx[i], o_idx, o_sc, 512)
 
 
+def test_prefill_scores_and_key_histogram(C):
+    """csa2_index_scores_prefill with score-key histograms (eight queries per
+    tile, each with its own histogram): every query's histogram exactly that
+    of its visible scores, across a chunk whose queries straddle groups of
+    eight and see different numbers of entries, and the top-k from the
+    histograms identical to the top-k without them."""
+    import torch
+    n_ent, ratio, pos0, nq = 3000, 2, 5000, 45
+    cache, ks = _fill(C, [n_ent], 3072, 28, ratio=ratio)
+    qi, w = _queries(29, nq)
+    ld = 3072
+    sc = torch.full((nq, ld), float("nan"), device="cuda")
+    kh = torch.full((nq, 2048), 7, dtype=torch.int32, device="cuda")   # zeroed by the call
+    C.csa2_index_scores_prefill(cache, 0, pos0, bf16_dev(qi), f32_dev(w), sc, key_hist=kh)
+    sc_h, kh_h = sc.cpu().numpy(), kh.cpu().numpy()
+    nv = [O.visible_entries(n_ent, ratio, pos0 + i) for i in range(nq)]
+    assert len(set(nv)) > 1
+    for i in range(nq):
+        assert np.all(np.isnan(sc_h[i, nv[i]:]))
+        assert np.array_equal(kh_h[i], _key_hist(sc_h[i, :nv[i]])), i
+    a = C.csa2_topk(sc, nv, 512, key_hist=kh).cpu().numpy()
+    b = C.csa2_topk(sc, nv, 512).cpu().numpy()
+    assert np.array_equal(a, b)
+
+
 def _key_hist(scores):
     u = np.ascontiguousarray(scores, np.float32).view(np.uint32).copy()
     u[(u << np.uint32(1)) == 0] = 0

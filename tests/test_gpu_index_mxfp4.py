@@ -114,6 +114,20 @@ def test_prefill_causal(C, pos0, ratio):
     assert cache.device_error() == 0
 
 
+def test_prefill_histograms_need_bf16_keys(C):
+    """The prefill score-key histograms come from the bf16 indexer only: with
+    MXFP4 keys the request is refused (the selection above builds its own)."""
+    import torch
+    cache, _ = _fill(C, [600], [600], 118)
+    qi, w = _queries(119, 4)
+    sc = torch.empty(4, 600, device="cuda")
+    kh = torch.zeros(4, 2048, dtype=torch.int32, device="cuda")
+    with pytest.raises(C.Csa2Error, match="UNSUPPORTED"):
+        C.csa2_index_scores_prefill(cache, 0, 700, bf16_dev(qi), f32_dev(w), sc, key_hist=kh)
+    C.csa2_index_scores_prefill(cache, 0, 700, bf16_dev(qi), f32_dev(w), sc)
+    assert cache.device_error() == 0
+
+
 def _reindex_case(C, lens, cap, seq_ids, max_blocks, seed):
     """Full-layer scores over MXFP4 keys -> candidate pool -> Reindex selection
     with another query, against the oracle on the MXFP4-rounded keys and
