@@ -74,7 +74,7 @@ def parse_args(argv=None):
     p.add_argument("--micro-batches", type=int, default=2,
                    help="split the batch into this many micro-batches on their own streams "
                         "(1: one stream, the whole batch per kernel)")
-    p.add_argument("--index-sms", type=int, default=104,
+    p.add_argument("--index-sms", type=int, default=112,
                    help="SMs for the indexer's grid when micro-batches > 1 (the rest run "
                         "the other micro-batch's top-k and readout concurrently)")
     p.add_argument("--attn-split", action="store_true",
@@ -113,10 +113,16 @@ def make_micro_batches(C, cache, wl, bufs0, ld, n_valid, M, split, dev):
     return mbs
 
 
-def mb_run(C, cache, d, L, scale):
-    """One micro-batch through the whole path, on the current stream."""
+def mb_run(C, cache, d, L, scale, before_index=None, after_index=None):
+    """One micro-batch through the whole path, on the current stream;
+    before_index / after_index: called around the indexer launch (the
+    schedule orders the micro-batches' indexers there)."""
+    if before_index is not None:
+        before_index()
     C.csa2_index_scores_decode(cache, d["q_idx"], d["w"], d["scores"], seq_ids=d["seq"],
                                key_hist=d["hist"])
+    if after_index is not None:
+        after_index()
     C.csa2_topk(d["scores"], d["nv"], 512, idx_out=d["topk"], key_hist=d["hist"],
                 workspace=d["tws"])
     for l in range(L):
@@ -459,7 +465,11 @@ def run_csa2(args):
     # ---- the headline schedule: the batch split into micro-batches, each on
     #      its own stream and in order there, step after step; the indexer's
     #      grid is capped so that the other micro-batch's latency-bound top-k
-    #      and readout run on the remaining SMs while it streams the keys
+    #      and readout run on the remaining SMs while it streams the keys.
+    #      The indexers of the micro-batches run one after the other (each
+    #      waits for the previous one's completion event): a persistent grid
+    #      whose CTAs start while another indexer still holds SMs would
+    #      finish late
     M = args.micro_batches
     mb_sets, mb_streams, graph_steps = None, None, 0
     if M > 1:
@@ -471,10 +481,21 @@ def run_csa2(args):
             main = torch.cuda.current_stream()
             for s_ in mb_streams:
                 s_.wait_stream(main)
+            prev = [None]
+
+            def before():
+                if prev[0] is not None:
+                    torch.cuda.current_stream().wait_event(prev[0])
+
+            def after():
+                ev = torch.cuda.Event()
+                ev.record(torch.cuda.current_stream())
+                prev[0] = ev
+
             for i in range(n):
                 for s_, d in zip(mb_streams, mb_sets[i % S]):
                     with torch.cuda.stream(s_):
-                        mb_run(C, cache, d, L, scale)
+                        mb_run(C, cache, d, L, scale, before, after)
             for s_ in mb_streams:
                 main.wait_stream(s_)
 
@@ -771,6 +792,7 @@ def run_csa2(args):
         "schedule": {"micro_batches": max(1, M), "streams": max(1, M),
                      "index_sms": args.index_sms if M > 1 else None,
                      "attention_split": bool(args.attn_split) if M > 1 else True,
+                     "indexers_serialised": M > 1,
                      "steps_per_graph": graph_steps if M > 1 else 1},
         "single_stream": {"value": B * world * args.steps / single_max,
                           "ms_per_step": 1000 * single_max / args.steps,
