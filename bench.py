@@ -113,22 +113,32 @@ def make_micro_batches(C, cache, wl, bufs0, ld, n_valid, M, split, dev):
     return mbs
 
 
-def mb_run(C, cache, d, L, scale, before_index=None, after_index=None):
-    """One micro-batch through the whole path, on the current stream;
-    before_index / after_index: called around the indexer launch (the
-    schedule orders the micro-batches' indexers there)."""
-    if before_index is not None:
-        before_index()
+def mb_index(C, cache, d):
+    """One micro-batch's indexer scores, on the current stream."""
     C.csa2_index_scores_decode(cache, d["q_idx"], d["w"], d["scores"], seq_ids=d["seq"],
                                key_hist=d["hist"])
-    if after_index is not None:
-        after_index()
+
+
+def mb_rest(C, cache, d, L, scale):
+    """One micro-batch's top-k and readout layers, on the current stream."""
     C.csa2_topk(d["scores"], d["nv"], 512, idx_out=d["topk"], key_hist=d["hist"],
                 workspace=d["tws"])
     for l in range(L):
         C.csa2_sparse_attn_decode(cache, d["qs"][l], d["swas"][l], d["topk"], scale,
                                   seq_ids=d["seq"], out=d["outs"][l], lse=d["lses"][l],
                                   workspace=d["aws"])
+
+
+def mb_run(C, cache, d, L, scale, before_index=None, after_index=None):
+    """One micro-batch through the whole path, on the current stream;
+    before_index / after_index: called around the indexer launch (the
+    schedule orders the micro-batches' indexers there)."""
+    if before_index is not None:
+        before_index()
+    mb_index(C, cache, d)
+    if after_index is not None:
+        after_index()
+    mb_rest(C, cache, d, L, scale)
 
 
 # ---------------------------------------------------------------- distributed helpers
@@ -630,14 +640,19 @@ def run_csa2(args):
         # stream; the micro-batches' pipelines overlap one another
         sets = [mb_sets[0], mb_sets[1]]
         cache.set_index_sms(args.index_sms)
+        # per micro-batch and buffer set: the indexer and the rest as two
+        # graphs, so that the micro-batches' indexers can be ordered by events
+        # (as in the device-timed schedule)
         mb_graphs = []
         for m in range(M):
             row = []
             for bset in sets:
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g):
-                    mb_run(C, cache, bset[m], L, scale)
-                row.append(g)
+                gi, gr = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gi):
+                    mb_index(C, cache, bset[m])
+                with torch.cuda.graph(gr):
+                    mb_rest(C, cache, bset[m], L, scale)
+                row.append((gi, gr))
             mb_graphs.append(row)
         cache.set_index_sms(0)
         copy_streams = [torch.cuda.Stream() for _ in range(M)]
@@ -660,6 +675,7 @@ def run_csa2(args):
                     for h, t in zip(h_in_mb[0][m], flat(sets[0][m], names_in)):
                         t.copy_(h, non_blocking=True)
                     in_ready[m][0].record(copy_streams[m])
+            prev_index = None
             for i in range(n):
                 b = i % 2
                 for m in range(M):
@@ -667,8 +683,14 @@ def run_csa2(args):
                     cs.wait_event(in_ready[m][b])
                     if i >= 2:
                         cs.wait_event(out_free[m][b])
+                    if prev_index is not None:
+                        cs.wait_event(prev_index)
+                    gi, gr = mb_graphs[m][b]
                     with torch.cuda.stream(cs):
-                        mb_graphs[m][b].replay()
+                        gi.replay()
+                        prev_index = torch.cuda.Event()
+                        prev_index.record(cs)
+                        gr.replay()
                     done[m][b].record(cs)
                     with torch.cuda.stream(ps):
                         if i + 1 < n:
@@ -687,7 +709,8 @@ def run_csa2(args):
 
         e2e_note = ("per micro-batch: inputs of step i+1 and outputs of step i-1 copied on "
                     "its copy stream while step i computes on its compute stream (pinned "
-                    "host buffers); the micro-batches' pipelines overlap")
+                    "host buffers); the micro-batches' pipelines overlap, their indexers "
+                    "ordered one after the other as in the device-timed schedule")
     run_e2e(3)
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
