@@ -120,13 +120,12 @@ def mb_index(C, cache, d):
 
 
 def mb_rest(C, cache, d, L, scale):
-    """One micro-batch's top-k and readout layers, on the current stream."""
+    """One micro-batch's top-k and readout layers (one launch for the group's
+    layers), on the current stream."""
     C.csa2_topk(d["scores"], d["nv"], 512, idx_out=d["topk"], key_hist=d["hist"],
                 workspace=d["tws"])
-    for l in range(L):
-        C.csa2_sparse_attn_decode(cache, d["qs"][l], d["swas"][l], d["topk"], scale,
-                                  seq_ids=d["seq"], out=d["outs"][l], lse=d["lses"][l],
-                                  workspace=d["aws"])
+    C.csa2_sparse_attn_decode_layers(cache, d["qs"], d["swas"], d["topk"], scale, d["outs"],
+                                     d["lses"], seq_ids=d["seq"], workspace=d["aws"])
 
 
 def mb_run(C, cache, d, L, scale, before_index=None, after_index=None):
@@ -414,9 +413,8 @@ def run_csa2(args):
         C.csa2_topk(scores, n_valid, 512, idx_out=d["topk"], key_hist=key_hist, workspace=topk_ws)
         if ev is not None:
             ev[2].record(stream)
-        for l in range(L):
-            C.csa2_sparse_attn_decode(cache, d["qs"][l], d["swas"][l], d["topk"], scale,
-                                      out=d["outs"][l], lse=d["lses"][l], workspace=attn_ws)
+        C.csa2_sparse_attn_decode_layers(cache, d["qs"], d["swas"], d["topk"], scale, d["outs"],
+                                         d["lses"], workspace=attn_ws)
         if ev is not None:
             ev[3].record(stream)
 
@@ -782,7 +780,7 @@ def run_csa2(args):
         traffic = float(rec["dram_bytes_per_launch"])
     # this library's kernels per step: indexer, top-k segments, top-k, one
     # attention launch per layer (workspace memsets are not counted)
-    launches_per_step = (3 + L) * ((B + 1023) // 1024) * max(1, M)
+    launches_per_step = 4 * ((B + 1023) // 1024) * max(1, M)   # index, 2 x top-k, readout
     config = workload_config(wl, args.layout)
     config["input_sets"] = S
     nominal = 8000.0   # GB/s: the nominal HBM3e figure of the target
@@ -877,9 +875,8 @@ def measure_paper_cache(C, W, wl, dev, stream, iters, hbm_peak):
         C.csa2_index_topk_decode(cache, q_idx, w, topk_idx=topk, workspace=ws)
         if ev is not None:
             ev[1].record(stream)
-        for l in range(L):
-            C.csa2_sparse_attn_decode(cache, qs[l], None, topk, scale, out=outs[l],
-                                      workspace=attn_ws, swa_fp8=swas[l])
+        C.csa2_sparse_attn_decode_layers(cache, qs, None, topk, scale, outs, None,
+                                         workspace=attn_ws, swa_fp8s=swas)
         if ev is not None:
             ev[2].record(stream)
 
@@ -1168,9 +1165,7 @@ def measure_decode_config(C, W, wid, dev, stream, iters, hbm_peak, flush):
         C.csa2_topk(scores, n_ent, 512, idx_out=topk, key_hist=hist, workspace=tws)
 
     def readout():
-        for l in range(L):
-            C.csa2_sparse_attn_decode(cache, qs[l], swas[l], topk, scale, out=outs[l],
-                                      workspace=aws)
+        C.csa2_sparse_attn_decode_layers(cache, qs, swas, topk, scale, outs, None, workspace=aws)
 
     def step():
         index()
@@ -1381,9 +1376,9 @@ def measure_decoder(C, W, dev, stream, iters, hbm_peak, max_blocks=2048):
                                              workspace=rws)
 
     def readout(g):
-        for l in range(4 * g, 4 * g + 4):
-            C.csa2_sparse_attn_decode(cache, qs[l], None, topks[g], scale, out=outs[l],
-                                      workspace=aws, swa_fp8=swas[l])
+        ls = slice(4 * g, 4 * g + 4)
+        C.csa2_sparse_attn_decode_layers(cache, qs[ls], None, topks[g], scale, outs[ls], None,
+                                         workspace=aws, swa_fp8s=swas[ls])
 
     def step():
         for g in range(n_groups):

@@ -104,6 +104,8 @@ def _load():
         "csa2_index_topk_decode_bf16": ([P, i32, P, P, P, P, P, P, sz, P], i32),
         "csa2_sparse_attn_decode_ex": ([P, i32, P, P, P, P, P, ctypes.c_float, P, P, P, sz, P,
                                         P], i32),
+        "csa2_sparse_attn_decode_layers": ([P, i32, i32, P, P, P, P, P, ctypes.c_float, P, P, P, sz,
+                                            P, P], i32),
         "csa2_sparse_attn_prefill_ex": ([P, i32, i32, i64, P, P, i64, i64, P, ctypes.c_float, P,
                                          P, P, P], i32),
         "csa2_swa_fp8_quantise": ([i64, P, P, P, P, P], i32),
@@ -412,6 +414,50 @@ def csa2_sparse_attn_decode(cache: Cache, q: torch.Tensor, swa_kv: Optional[torc
         _check(lib.csa2_sparse_attn_decode_ex(*args, ctypes.byref(opts), _stream(stream)),
                "csa2_sparse_attn_decode_ex")
     return out
+
+
+def csa2_sparse_attn_decode_layers(cache: Cache, qs: Sequence[torch.Tensor],
+                                   swa_kvs: Optional[Sequence[Optional[torch.Tensor]]],
+                                   topk_idx: torch.Tensor, scale: float,
+                                   outs: Sequence[torch.Tensor],
+                                   lses: Optional[Sequence[Optional[torch.Tensor]]] = None,
+                                   swa_len: Optional[torch.Tensor] = None,
+                                   seq_ids: Optional[Sequence[int]] = None,
+                                   workspace: Optional[torch.Tensor] = None,
+                                   sinks: Optional[Sequence[Optional[torch.Tensor]]] = None,
+                                   rope_pos: Optional[torch.Tensor] = None, rope_base: float = 0.0,
+                                   swa_fp8s=None, stream=None):
+    """The readout of several layers of a group in one launch (per layer:
+    queries, window rows or their FP8 form, sink, outputs); workspace as for
+    csa2_sparse_attn_decode."""
+    L = len(qs)
+    nq = qs[0].shape[0]
+    if workspace is None:
+        workspace = torch.empty(max(16, csa2_sparse_attn_workspace_bytes(cache, nq)),
+                                dtype=torch.uint8, device=qs[0].device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    arr = lambda xs: (ctypes.c_void_p * L)(*[_ptr(x) for x in xs])
+    swa_arr = arr(swa_kvs) if swa_kvs is not None else None
+    lse_arr = arr(lses) if lses is not None else None
+    keep = []
+    opts_arr = None
+    if sinks is not None or rope_pos is not None or swa_fp8s is not None:
+        ptrs = []
+        for l in range(L):
+            f8 = swa_fp8s[l] if swa_fp8s is not None and swa_fp8s[l] is not None else (None, None, None)
+            o = AttnOpts(_ptr(sinks[l] if sinks is not None else None), _ptr(rope_pos),
+                         1 if rope_pos is not None else 0, float(rope_base),
+                         _ptr(f8[0]), _ptr(f8[1]), _ptr(f8[2]))
+            keep.append(o)
+            ptrs.append(ctypes.cast(ctypes.pointer(o), ctypes.c_void_p))
+        opts_arr = (ctypes.c_void_p * L)(*ptrs)
+    _check(lib.csa2_sparse_attn_decode_layers(cache.handle, L, nq, _i32_array(seq_ids), arr(qs),
+                                              swa_arr, _ptr(swa_len), _ptr(topk_idx),
+                                              float(scale), arr(outs), lse_arr,
+                                              _ptr(workspace) if ws_bytes else None, ws_bytes,
+                                              opts_arr, _stream(stream)),
+           "csa2_sparse_attn_decode_layers")
+    return outs
 
 
 def csa2_sparse_attn_prefill(cache: Cache, seq: int, pos0: int, q: torch.Tensor,

@@ -84,6 +84,8 @@ struct Layout {
   size_t len_off, err_off, codes_off, scales_off, idxk_off, idxs_off, total;
 };
 
+static_assert(CSA2_MAX_ATTN_LAYERS == kAttnMaxLayers, "layers of one readout launch");
+
 // Rows of the MXFP4 key arrays: the entries rounded up to 512-key chunks.
 int64_t mxfp4_rows(int64_t total) { return (total + 511) / 512 * 512; }
 
@@ -913,18 +915,21 @@ size_t csa2_sparse_attn_workspace_bytes(const csa2_cache_t* c, int32_t n_queries
 
 namespace {
 // Epilogue options into the launch parameters; false when they are invalid.
-bool apply_opts(AttnParams* p, const csa2_attn_opts_t* opts, bool decode, int32_t q0,
-                int64_t row0) {
+// Epilogue options of layer `ly` of a launch (sink, FP8 window rows), and
+// the launch's output RoPE (shared by its layers); false when they are
+// invalid.
+bool apply_opts(AttnParams* p, AttnLayer* ly, const csa2_attn_opts_t* opts, bool decode,
+                int32_t q0, int64_t row0) {
   if (!opts) return true;
-  p->sink = opts->sink;
+  ly->sink = opts->sink;
   const bool f8 = opts->swa_codes || opts->swa_rope || opts->swa_scales;
   if (f8) {
     if (!opts->swa_codes || !opts->swa_rope || !opts->swa_scales || !aligned16(opts->swa_codes) ||
         !aligned16(opts->swa_rope) || (reinterpret_cast<uintptr_t>(opts->swa_scales) & 7u))
       return false;
-    p->swa_codes = opts->swa_codes + row0 * 448;
-    p->swa_rope = static_cast<const uint16_t*>(opts->swa_rope) + row0 * 64;
-    p->swa_scales = opts->swa_scales + row0 * 8;
+    ly->swa_codes = opts->swa_codes + row0 * 448;
+    ly->swa_rope = static_cast<const uint16_t*>(opts->swa_rope) + row0 * 64;
+    ly->swa_scales = opts->swa_scales + row0 * 8;
   }
   if (opts->rope_out) {
     if (decode && !opts->rope_pos) return false;
@@ -956,14 +961,37 @@ csa2_status_t csa2_sparse_attn_decode_ex(const csa2_cache_t* c, int32_t nq,
                                          float* lse, void* workspace, size_t ws_bytes,
                                          const csa2_attn_opts_t* opts, csa2_stream_t stream) {
   CSA2_RANGE();
-  if (!c || nq < 0) return CSA2_ERR_INVALID_ARG;
+  return csa2_sparse_attn_decode_layers(c, 1, nq, seq_ids, &q, &swa_kv, swa_len, topk_idx, scale,
+                                        &out, &lse, workspace, ws_bytes, &opts, stream);
+}
+
+csa2_status_t csa2_sparse_attn_decode_layers(const csa2_cache_t* c, int32_t n_layers, int32_t nq,
+                                             const int32_t* seq_ids, const void* const* q,
+                                             const void* const* swa_kv, const int32_t* swa_len,
+                                             const int32_t* topk_idx, float scale,
+                                             void* const* out, float* const* lse,
+                                             void* workspace, size_t ws_bytes,
+                                             const csa2_attn_opts_t* const* opts,
+                                             csa2_stream_t stream) {
+  CSA2_RANGE();
+  if (!c || nq < 0 || n_layers < 1 || n_layers > CSA2_MAX_ATTN_LAYERS || !q || !out)
+    return CSA2_ERR_INVALID_ARG;
   if (nq == 0) return CSA2_OK;
   const int W = c->cfg.swa;
-  if (!q || !topk_idx || !out || !aligned16(q) || !aligned16(out) || !aligned16(topk_idx))
-    return CSA2_ERR_INVALID_ARG;
-  const bool f8 = opts && opts->swa_codes;
-  if (W > 0 && !f8 && (!swa_kv || !aligned16(swa_kv))) return CSA2_ERR_INVALID_ARG;
-  if (lse && !aligned16(lse)) return CSA2_ERR_INVALID_ARG;
+  if (!topk_idx || !aligned16(topk_idx)) return CSA2_ERR_INVALID_ARG;
+  const csa2_attn_opts_t* o0 = opts ? opts[0] : nullptr;
+  for (int l = 0; l < n_layers; ++l) {
+    const csa2_attn_opts_t* ol = opts ? opts[l] : nullptr;
+    if (!q[l] || !out[l] || !aligned16(q[l]) || !aligned16(out[l])) return CSA2_ERR_INVALID_ARG;
+    const bool f8 = ol && ol->swa_codes;
+    const void* sw = swa_kv ? swa_kv[l] : nullptr;
+    if (W > 0 && !f8 && (!sw || !aligned16(sw))) return CSA2_ERR_INVALID_ARG;
+    if (lse && lse[l] && !aligned16(lse[l])) return CSA2_ERR_INVALID_ARG;
+    // the output RoPE is one setting for the launch: every layer the same
+    const bool r0 = o0 && o0->rope_out, rl = ol && ol->rope_out;
+    if (r0 != rl || (rl && (ol->rope_pos != o0->rope_pos || ol->rope_base != o0->rope_base)))
+      return CSA2_ERR_INVALID_ARG;
+  }
   if (workspace && !aligned16(workspace)) return CSA2_ERR_INVALID_ARG;
   if (seq_ids)
     for (int i = 0; i < nq; ++i)
@@ -971,19 +999,20 @@ csa2_status_t csa2_sparse_attn_decode_ex(const csa2_cache_t* c, int32_t nq,
   if (!seq_ids && nq > c->batch) return CSA2_ERR_INVALID_ARG;
   const int H = c->cfg.n_heads, k = c->cfg.topk, G = H / kAttnHeadGroup;
   AttnParams* p = new (std::nothrow) AttnParams();
-  if (!p) return CSA2_ERR_OOM;
+  AttnMaps* maps = new (std::nothrow) AttnMaps();
+  if (!p || !maps) { delete p; delete maps; return CSA2_ERR_OOM; }
   csa2_status_t st = CSA2_OK;
-  for (int q0 = 0; q0 < nq; q0 += kAttnTab) {
+  for (int q0 = 0; q0 < nq && st == CSA2_OK; q0 += kAttnTab) {
     const int n = std::min(kAttnTab, nq - q0);
     // two CTAs per (query, head group) when one each would leave SMs idle
-    const bool split = workspace && ws_bytes >= kAttnSplitToken && (int64_t)n * G < c->num_sms;
+    const bool split = workspace && ws_bytes >= kAttnSplitToken &&
+                       (int64_t)n_layers * n * G < c->num_sms;
     std::memset(p, 0, sizeof(AttnParams));
     p->topk_idx = topk_idx + (int64_t)q0 * k;
     p->swa_len = swa_len ? swa_len + q0 : nullptr;
     p->codes = c->codes;
     p->scales = c->scales;
-    p->out = static_cast<uint16_t*>(out) + (int64_t)q0 * H * kHeadDim;
-    p->lse = lse ? lse + (int64_t)q0 * H : nullptr;
+    p->n_layers = n_layers;
     p->err = c->d_err;
     p->nq = n;
     p->n_heads = H;
@@ -995,24 +1024,33 @@ csa2_status_t csa2_sparse_attn_decode_ex(const csa2_cache_t* c, int32_t nq,
     p->prefill = 0;
     p->splits = split ? 2 : 1;
     p->wait_cycles = c->wait_cycles;
-    if (!apply_opts(p, opts, true, q0, (int64_t)q0 * W)) { st = CSA2_ERR_INVALID_ARG; break; }
     for (int i = 0; i < n; ++i) {
       const int s = seq_ids ? seq_ids[q0 + i] : q0 + i;
       p->q_base[i] = c->off[s];
       p->q_len[i] = (int32_t)c->len[s];
     }
-    CUtensorMap tm_q, tm_swa;
-    const uint16_t* qb = static_cast<const uint16_t*>(q) + (int64_t)q0 * H * kHeadDim;
-    if (!make_map(&tm_q, qb, (uint64_t)n * H, kHeadDim, 64, kAttnHeadGroup)) { st = CSA2_ERR_CUDA; break; }
-    if (W > 0 && !f8) {
-      const uint16_t* sb = static_cast<const uint16_t*>(swa_kv) + (int64_t)q0 * W * kHeadDim;
-      if (!make_map(&tm_swa, sb, (uint64_t)n * W, kHeadDim, 64, 128)) { st = CSA2_ERR_CUDA; break; }
-    } else {
-      tm_swa = tm_q;
+    for (int l = 0; l < n_layers && st == CSA2_OK; ++l) {
+      AttnLayer& ly = p->layer[l];
+      const csa2_attn_opts_t* ol = opts ? opts[l] : nullptr;
+      ly.out = static_cast<uint16_t*>(out[l]) + (int64_t)q0 * H * kHeadDim;
+      ly.lse = (lse && lse[l]) ? lse[l] + (int64_t)q0 * H : nullptr;
+      if (!apply_opts(p, &ly, ol, true, q0, (int64_t)q0 * W)) { st = CSA2_ERR_INVALID_ARG; break; }
+      const uint16_t* qb = static_cast<const uint16_t*>(q[l]) + (int64_t)q0 * H * kHeadDim;
+      if (!make_map(&maps->q[l], qb, (uint64_t)n * H, kHeadDim, 64, kAttnHeadGroup)) {
+        st = CSA2_ERR_CUDA;
+        break;
+      }
+      if (W > 0 && !(ol && ol->swa_codes)) {
+        const uint16_t* sb = static_cast<const uint16_t*>(swa_kv[l]) + (int64_t)q0 * W * kHeadDim;
+        if (!make_map(&maps->swa[l], sb, (uint64_t)n * W, kHeadDim, 64, 128)) { st = CSA2_ERR_CUDA; break; }
+      } else {
+        maps->swa[l] = maps->q[l];
+      }
     }
-    if (launch_attn(*p, tm_q, tm_swa, S(stream)) != cudaSuccess) { st = CSA2_ERR_CUDA; break; }
+    if (st == CSA2_OK && launch_attn(*p, *maps, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
   }
   delete p;
+  delete maps;
   return st;
 }
 
@@ -1052,8 +1090,9 @@ csa2_status_t csa2_sparse_attn_prefill_ex(const csa2_cache_t* c, int32_t seq, in
   p->topk_idx = topk_idx;
   p->codes = c->codes;
   p->scales = c->scales;
-  p->out = static_cast<uint16_t*>(out);
-  p->lse = lse;
+  p->n_layers = 1;
+  p->layer[0].out = static_cast<uint16_t*>(out);
+  p->layer[0].lse = lse;
   p->err = c->d_err;
   p->nq = nq;
   p->n_heads = H;
@@ -1069,19 +1108,23 @@ csa2_status_t csa2_sparse_attn_prefill_ex(const csa2_cache_t* c, int32_t seq, in
   p->swa_pos0 = swa_pos0;
   p->splits = 1;
   p->wait_cycles = c->wait_cycles;
-  csa2_status_t st = apply_opts(p, opts, false, 0, 0) ? CSA2_OK : CSA2_ERR_INVALID_ARG;
-  CUtensorMap tm_q, tm_swa;
-  if (st == CSA2_OK && !make_map(&tm_q, q, (uint64_t)nq * H, kHeadDim, 64, kAttnHeadGroup))
+  csa2_status_t st =
+      apply_opts(p, &p->layer[0], opts, false, 0, 0) ? CSA2_OK : CSA2_ERR_INVALID_ARG;
+  AttnMaps* maps = new (std::nothrow) AttnMaps();
+  if (!maps) st = CSA2_ERR_OOM;
+  if (st == CSA2_OK && !make_map(&maps->q[0], q, (uint64_t)nq * H, kHeadDim, 64, kAttnHeadGroup))
     st = CSA2_ERR_CUDA;
   if (st == CSA2_OK) {
     if (W > 0 && !f8) {
-      if (!make_map(&tm_swa, swa_kv, (uint64_t)n_swa_rows, kHeadDim, 64, 128)) st = CSA2_ERR_CUDA;
+      if (!make_map(&maps->swa[0], swa_kv, (uint64_t)n_swa_rows, kHeadDim, 64, 128))
+        st = CSA2_ERR_CUDA;
     } else {
-      tm_swa = tm_q;
+      maps->swa[0] = maps->q[0];
     }
   }
-  if (st == CSA2_OK && launch_attn(*p, tm_q, tm_swa, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
+  if (st == CSA2_OK && launch_attn(*p, *maps, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;
   delete p;
+  delete maps;
   return st;
 }
 

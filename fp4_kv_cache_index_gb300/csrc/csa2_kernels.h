@@ -167,14 +167,29 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
 
 // ---------------------------------------------------------------- attention
 constexpr int kAttnTab = 1024;
+constexpr int kAttnMaxLayers = 8;
+// What differs between the layers of one readout launch (the layers of a
+// group share the cache, the selection and the windows' geometry).
+struct AttnLayer {
+  uint16_t* out;             // bf16 [nq, n_heads, 512]
+  float* lse;                // nullable [nq, n_heads]
+  const float* sink;         // nullable [n_heads]: per-head sink logit z' (units of scale * q.kv)
+  const uint8_t* swa_codes;  // FP8 window rows (nullable): E4M3 codes [rows, 448]
+  const uint16_t* swa_rope;  //   bf16 RoPE channels [rows, 64]
+  const uint8_t* swa_scales; //   UE8M0 scales [rows, 8]
+};
+// The layers' query rows and bf16 window rows as TMA tensor maps.
+struct AttnMaps {
+  CUtensorMap q[kAttnMaxLayers];
+  CUtensorMap swa[kAttnMaxLayers];
+};
 struct AttnParams {
   const int32_t* topk_idx;   // [nq, topk]
   const int32_t* swa_len;    // decode: nullable [nq]
   const uint8_t* codes;
   const uint8_t* scales;
-  uint16_t* out;             // bf16 [nq, n_heads, 512]
+  int32_t n_layers;          // layers of the launch; blocks are (layer, query, head group, split)
   int32_t splits;            // CTAs per (query, 64-head group): 1, or 2 (a cluster)
-  float* lse;                // nullable [nq, n_heads]
   uint32_t* err;
   int32_t nq;
   int32_t n_heads;
@@ -188,14 +203,11 @@ struct AttnParams {
   int32_t pre_len;           // prefill: entries in the sequence
   int64_t pos0;              // prefill: position of query 0
   int64_t swa_pos0;          // prefill: position of swa row 0
-  const float* sink;         // nullable [n_heads]: per-head sink logit z' (units of scale * q.kv)
   const int64_t* rope_pos;   // decode: [nq] query positions for the output RoPE(-i)
   int32_t rope_out;          // 1: rotate the last 64 output channels by -position
   double rope_theta[32];     // RoPE frequencies base^(-2t/64) of the 32 channel pairs
-  const uint8_t* swa_codes;  // FP8 window rows (nullable): E4M3 codes [rows, 448]
-  const uint16_t* swa_rope;  //   bf16 RoPE channels [rows, 64]
-  const uint8_t* swa_scales; //   UE8M0 scales [rows, 8]
   int64_t wait_cycles;       // bounded-wait limit in cycles (0: the default, ~2^31)
+  AttnLayer layer[kAttnMaxLayers];
   int64_t q_base[kAttnTab];  // decode: entry offset of each query's sequence
   int32_t q_len[kAttnTab];   // decode: entries of each query's sequence
 };
@@ -206,7 +218,6 @@ constexpr int kAttnHeadGroup = 64;
 // The two-CTA decode split needs no scratch memory: a caller opts in by
 // passing a workspace of at least this many bytes.
 constexpr size_t kAttnSplitToken = 16;
-cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_swa,
-                        cudaStream_t s);
+cudaError_t launch_attn(const AttnParams& p, const AttnMaps& maps, cudaStream_t s);
 
 }  // namespace csa2

@@ -8,7 +8,10 @@
 // KV into a single joint sparse attention"); entries are dequantised from
 // FP4 before attention (V4.1 report, section 2.4.4).
 //
-// One CTA = one query x 64 heads x one share of the candidate tiles.  With
+// One CTA = one query x 64 heads x one share of the candidate tiles of one
+// layer (a launch may hold several layers of a group, which share the cache,
+// the selection and the window geometry: their CTAs pack the SMs without a
+// launch boundary between the layers).  With
 // `splits` = 2 (small decode batches) the tiles of a query alternate between
 // the two CTAs of a cluster, which merge their unnormalised fp32 states
 // (running max, sum, O) exactly through distributed shared memory, each
@@ -105,8 +108,7 @@ __device__ __forceinline__ float warp_reduce_scatter16(float (&v)[16], int lane)
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    k_attn(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_q,
-           const __grid_constant__ CUtensorMap tm_swa) {
+    k_attn(const __grid_constant__ AttnParams p, const __grid_constant__ AttnMaps maps) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -120,8 +122,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_wait();
   const long long wl = wait_limit(p.wait_cycles);   // bounded-wait limit (cycles)
   const int hgs = p.n_heads / kHG;
-  const int split = blockIdx.x % p.splits;
-  const int qh = blockIdx.x / p.splits;            // (query, head group)
+  // blocks of one launch: (layer, query, head group, split)
+  const int per_layer = p.nq * hgs * p.splits;
+  const int layer = (int)blockIdx.x / per_layer;
+  const int bid = (int)blockIdx.x - layer * per_layer;
+  const int split = bid % p.splits;
+  const int qh = bid / p.splits;                   // (query, head group)
+  const AttnLayer& ly = p.layer[layer];
+  const CUtensorMap* tm_q = &maps.q[layer];
+  const CUtensorMap* tm_swa = &maps.swa[layer];
   const int q = qh / hgs, hg = qh % hgs;
   const int n_topk_tiles = p.topk / kRows;
   const int32_t* idx_row = p.topk_idx + (int64_t)q * p.topk;
@@ -169,11 +178,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int h = 0; h < 2; ++h) {
       mbar_arrive_expect_tx(&sm.bar_q[h], kHG * kHeadDim);
       for (int c = 4 * h; c < 4 * h + 4; ++c)
-        tma_load_2d(qs + c * (kHG * 128), &tm_q, 64 * c, q * p.n_heads + hg * kHG, &sm.bar_q[h]);
-      if (swa_first && !p.swa_codes) {
+        tma_load_2d(qs + c * (kHG * 128), tm_q, 64 * c, q * p.n_heads + hg * kHG, &sm.bar_q[h]);
+      if (swa_first && !ly.swa_codes) {
         mbar_arrive_expect_tx(&sm.bar_kv[h], kRows * kHeadDim);
         for (int c = 4 * h; c < 4 * h + 4; ++c)
-          tma_load_2d(kv + c * (kRows * 128), &tm_swa, 64 * c, swa_row0, &sm.bar_kv[h]);
+          tma_load_2d(kv + c * (kRows * 128), tm_swa, 64 * c, swa_row0, &sm.bar_kv[h]);
       }
     }
   }
@@ -368,9 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool live = e < swa_count;
     if (!live) return make_uint4(0u, 0u, 0u, 0u);
     const int64_t row = (int64_t)swa_row0 + e;
-    if (c == 7) return __ldg(reinterpret_cast<const uint4*>(p.swa_rope + row * 64) + k);
-    const float sc = ue8m0_value(__ldg(p.swa_scales + row * 8 + c));
-    const uint2 cc = __ldg(reinterpret_cast<const uint2*>(p.swa_codes + row * 448 + 64 * c + 8 * k));
+    if (c == 7) return __ldg(reinterpret_cast<const uint4*>(ly.swa_rope + row * 64) + k);
+    const float sc = ue8m0_value(__ldg(ly.swa_scales + row * 8 + c));
+    const uint2 cc = __ldg(reinterpret_cast<const uint2*>(ly.swa_codes + row * 448 + 64 * c + 8 * k));
     return e4m3_piece(cc.x, cc.y, sc);
   };
   auto fill_half = [&](int tile, int h) {
@@ -420,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int after = next_topk_after(next_topk);
       if (after < n_tiles) prefetch_l2(sm.my_list[after]);
     }
-    if (tile < 0 && !p.swa_codes) {
+    if (tile < 0 && !ly.swa_codes) {
       // bf16 window rows: loaded by TMA at kernel entry
       if (tid < kRows) sm.row_valid[tid] = tid < swa_count;
       if (tid == 0) {
@@ -627,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t out_row = (int64_t)q * p.n_heads + hg * kHG;   // first head of this CTA
   // sink logit of head h in log2 units (-inf: none)
   auto sink_log2 = [&](int h) -> float {
-    return p.sink ? p.sink[hg * kHG + h] * 1.4426950408889634f : -INFINITY;
+    return ly.sink ? ly.sink[hg * kHG + h] * 1.4426950408889634f : -INFINITY;
   };
   // output channel d of head slot c, rotated when it is a RoPE channel
   // (channel pairs sit in adjacent lanes: every lane of the warp calls this)
@@ -648,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int per_row = dw / 8;
     for (int k = tid; k < kHG * per_row; k += kThreads) {
       const int h = k / per_row, c = k % per_row;
-      *reinterpret_cast<uint4*>(p.out + (out_row + h) * kHeadDim + d0 + 8 * c) =
+      *reinterpret_cast<uint4*>(ly.out + (out_row + h) * kHeadDim + d0 + 8 * c) =
           *reinterpret_cast<const uint4*>(out_s + h * dw + 8 * c);
     }
   };
@@ -661,8 +670,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float am = (m == -INFINITY) ? 0.0f : fast_exp2(m - M);
         const float L = l * am + ((z == -INFINITY) ? 0.0f : fast_exp2(z - M));
         sm.alpha[tid] = L > 0.0f ? am / L : 0.0f;
-        if (p.lse)
-          p.lse[out_row + tid] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+        if (ly.lse)
+          ly.lse[out_row + tid] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
       }
       __syncthreads();
       float w_me[16];
@@ -683,9 +692,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       store_rows(0, kHeadDim);
     } else if (n_tiles == 0) {
       // no candidate at all: output 0, lse = the sink alone (or -inf)
-      for (int i = tid; i < kHG * kHeadDim; i += kThreads) p.out[out_row * kHeadDim + i] = 0;
-      if (p.lse && tid < kHG)
-        p.lse[out_row + tid] = p.sink ? p.sink[hg * kHG + tid] : -INFINITY;
+      for (int i = tid; i < kHG * kHeadDim; i += kThreads) ly.out[out_row * kHeadDim + i] = 0;
+      if (ly.lse && tid < kHG)
+        ly.lse[out_row + tid] = ly.sink ? ly.sink[hg * kHG + tid] : -INFINITY;
     }
   } else {
     // ---- split-KV over a cluster of two CTAs (cluster rank = split).  Each
@@ -730,8 +739,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float c_ot = L > 0.0f ? (split == 0 ? a1 : a0) / L : 0.0f;
       sm.alpha[tid] = have ? c_me : 0.0f;               // weight of this CTA's O
       sm.red_max[0][tid] = (l_ot > 0.0f) ? c_ot : 0.0f;  // weight of the partner's O
-      if (p.lse && split == 0)
-        p.lse[out_row + tid] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+      if (ly.lse && split == 0)
+        ly.lse[out_row + tid] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
     }
     __syncthreads();
     // this CTA's O^T first (warp-collective TMEM loads), then all eight
@@ -789,12 +798,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 int attn_smem_bytes() { return kSmemBytes; }
-cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_swa,
-                        cudaStream_t s) {
+cudaError_t launch_attn(const AttnParams& p, const AttnMaps& maps, cudaStream_t s) {
+  if (p.n_layers < 1 || p.n_layers > kAttnMaxLayers) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int64_t blocks = (int64_t)p.nq * (p.n_heads / kHG) * p.splits;
+  const int64_t blocks = (int64_t)p.n_layers * p.nq * (p.n_heads / kHG) * p.splits;
   if (blocks <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
@@ -812,7 +821,7 @@ cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tm_q, const CUte
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  return cudaLaunchKernelEx(&cfg, k_attn, p, tm_q, tm_swa);
+  return cudaLaunchKernelEx(&cfg, k_attn, p, maps);
 }
 
 }  // namespace csa2

@@ -562,6 +562,35 @@ csa2_status_t csa2_sparse_attn_decode_ex(const csa2_cache_t* cache,
                                          const csa2_attn_opts_t* opts,
                                          csa2_stream_t stream);
 
+/* Decode readout of n_layers layers of one group in one launch: the
+ * layers share the cache, the queries' sequences and windows' geometry
+ * (seq_ids, swa_len) and the selection (topk_idx, e.g. a Full layer and its
+ * Reuse layers, [V41 sec 2.3.1]), each has its own queries, window rows,
+ * outputs and epilogue options.  Layer l's out / lse are exactly those of
+ * csa2_sparse_attn_decode_ex with q[l], swa_kv[l], out[l], lse[l],
+ * opts[l]; one launch lets the layers' CTAs fill the SMs without a kernel
+ * boundary between the layers.
+ *   n_layers: 1 .. CSA2_MAX_ATTN_LAYERS;  q, out: host arrays of n_layers
+ *   device pointers;  swa_kv: host array of n_layers device pointers
+ *   (entries NULL for FP8 windows), or NULL when there is no window;  lse:
+ *   host array of n_layers nullable device pointers, or NULL;  opts: host
+ *   array of n_layers nullable option pointers, or NULL -- the output RoPE
+ *   settings (rope_out, rope_pos, rope_base) must be the same in every
+ *   layer, else CSA2_ERR_INVALID_ARG;  other arguments as for
+ *   csa2_sparse_attn_decode (the workspace's two-CTA split counts the CTAs
+ *   of all layers).                                                        */
+#define CSA2_MAX_ATTN_LAYERS 8
+csa2_status_t csa2_sparse_attn_decode_layers(const csa2_cache_t* cache, int32_t n_layers,
+                                             int32_t n_queries, const int32_t* seq_ids,
+                                             const void* const* q,
+                                             const void* const* swa_kv,
+                                             const int32_t* swa_len,
+                                             const int32_t* topk_idx, float scale,
+                                             void* const* out, float* const* lse,
+                                             void* workspace, size_t workspace_bytes,
+                                             const csa2_attn_opts_t* const* opts,
+                                             csa2_stream_t stream);
+
 /* csa2_sparse_attn_prefill with epilogue options (NULL: none).          */
 csa2_status_t csa2_sparse_attn_prefill_ex(const csa2_cache_t* cache, int32_t seq,
                                           int32_t n_queries, int64_t pos0,

@@ -79,6 +79,10 @@ def test_host_argument_errors(lib):
     # workspace sizes of an invalid request are 0
     assert L.csa2_index_prefill_workspace_bytes(None, 0, 8) == 0
     assert L.csa2_index_workspace_bytes(None, 8) == 0
+    # several readout layers: a null cache or a bad layer count is refused
+    # before any launch
+    assert L.csa2_sparse_attn_decode_layers(None, 2, 1, None, None, None, None, None, 1.0, None,
+                                            None, None, 0, None, None) == 1
     assert L.csa2_compress(0, 4, 512, None, None, None, None) == 1
     assert L.csa2_compress(2, 0, 512, None, None, None, None) == 0
     assert L.csa2_compress(32, 4, 512, None, None, None, None) == 2

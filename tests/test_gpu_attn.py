@@ -240,3 +240,85 @@ def test_large_values_stay_within_the_probability_rounding_bound(C):
         g = S.bf16_bits_to_f32(bf16_host(out)[0]).astype(np.float64)
         assert np.all(np.abs(g - ref) <= bound), float((np.abs(g - ref) / bound).max())
     assert cache.device_error() == 0
+
+
+@pytest.mark.parametrize("split", [False, True])
+def test_layers_in_one_launch_equal_separate_calls(C, split):
+    """csa2_sparse_attn_decode_layers: four layers of a group (own queries,
+    windows, outputs; one selection) in one launch give, layer by layer,
+    exactly the outputs and lse of separate csa2_sparse_attn_decode calls,
+    with and without the two-CTA split; layer 2 checked against the
+    oracle."""
+    import torch
+    rng = np.random.default_rng(71)
+    lens = [900, 2000, 3000]
+    cache, ents = _cache(C, lens, 3072, 72)
+    nq, L = len(lens), 4
+    qs = [S.normal_bf16(S.stream_key(73, S.S_Q, l), 0, nq * 64 * 512).reshape(nq, 64, 512)
+          for l in range(L)]
+    swas = [S.normal_bf16(S.stream_key(73, S.S_SWA, l), 0, nq * 128 * 512).reshape(nq, 128, 512)
+            for l in range(L)]
+    swa_len = torch.tensor([128, 7, 64], dtype=torch.int32, device="cuda")
+    idx = np.stack([_sel(rng, n) for n in lens])
+    idx_d = torch.from_numpy(idx).cuda()
+    ws = None if split else torch.empty(0, dtype=torch.uint8, device="cuda")
+    q_d = [bf16_dev(x) for x in qs]
+    s_d = [bf16_dev(x) for x in swas]
+    outs = [torch.empty(nq, 64, 512, dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    lses = [torch.empty(nq, 64, device="cuda") for _ in range(L)]
+    C.csa2_sparse_attn_decode_layers(cache, q_d, s_d, idx_d, float(SCALE), outs, lses,
+                                     swa_len=swa_len, workspace=ws)
+    for l in range(L):
+        lse1 = torch.empty(nq, 64, device="cuda")
+        o1 = C.csa2_sparse_attn_decode(cache, q_d[l], s_d[l], idx_d, float(SCALE),
+                                       swa_len=swa_len, lse=lse1, workspace=ws)
+        assert torch.equal(o1.view(torch.int16), outs[l].view(torch.int16)), l
+        assert torch.equal(lse1, lses[l]), l
+    o = bf16_host(outs[2])
+    ln = swa_len.cpu().numpy()
+    for i in range(nq):
+        codes, scales = O.quantise(ents[i], 0)
+        _, ref, rl = O.sparse_attention(qs[2][i], codes, scales, 0, idx[i], swas[2][i, :ln[i]], SCALE)
+        check_attn(o[i], ref)
+        check_lse(lses[2].cpu().numpy()[i], rl)
+    assert cache.device_error() == 0
+
+
+def test_layers_epilogue_options_per_layer(C):
+    """Per-layer sinks and FP8 window rows in one launch equal the separate
+    calls with the same options; the output RoPE must be one setting for
+    the launch."""
+    import torch
+    rng = np.random.default_rng(81)
+    lens = [1500, 600]
+    cache, _ = _cache(C, lens, 1536, 82)
+    nq, L = len(lens), 3
+    qs = [bf16_dev(S.normal_bf16(S.stream_key(83, S.S_Q, l), 0, nq * 64 * 512).reshape(nq, 64, 512))
+          for l in range(L)]
+    rows = [bf16_dev(S.normal_bf16(S.stream_key(83, S.S_SWA, l), 0, nq * 128 * 512).reshape(nq * 128, 512))
+            for l in range(L)]
+    f8 = [C.csa2_swa_fp8_quantise(r) for r in rows]
+    sinks = [torch.linspace(-1.0 - l, 1.0 + l, 64, device="cuda") for l in range(L)]
+    pos = torch.tensor([4000, 123456], dtype=torch.int64, device="cuda")
+    idx_d = torch.from_numpy(np.stack([_sel(rng, n) for n in lens])).cuda()
+    outs = [torch.empty(nq, 64, 512, dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    lses = [torch.empty(nq, 64, device="cuda") for _ in range(L)]
+    C.csa2_sparse_attn_decode_layers(cache, qs, [None] * L, idx_d, float(SCALE), outs, lses,
+                                     sinks=sinks, rope_pos=pos, swa_fp8s=f8)
+    for l in range(L):
+        lse1 = torch.empty(nq, 64, device="cuda")
+        o1 = C.csa2_sparse_attn_decode(cache, qs[l], None, idx_d, float(SCALE), lse=lse1,
+                                       sink=sinks[l], rope_pos=pos, swa_fp8=f8[l])
+        assert torch.equal(o1.view(torch.int16), outs[l].view(torch.int16)), l
+        assert torch.equal(lse1, lses[l]), l
+    # RoPE on some layers only: refused before any launch
+    with pytest.raises(C.Csa2Error, match="INVALID_ARG"):
+        opts = [C.AttnOpts(None, C._ptr(pos), 1, 0.0, None, None, None),
+                C.AttnOpts(None, None, 0, 0.0, None, None, None)]
+        import ctypes
+        arr = lambda xs: (ctypes.c_void_p * 2)(*[C._ptr(x) for x in xs])
+        oarr = (ctypes.c_void_p * 2)(*[ctypes.cast(ctypes.pointer(o), ctypes.c_void_p) for o in opts])
+        C._check(C.lib.csa2_sparse_attn_decode_layers(
+            cache.handle, 2, nq, None, arr(qs[:2]), arr(rows[:2]), None, C._ptr(idx_d),
+            float(SCALE), arr(outs[:2]), None, None, 0, oarr, C._stream(None)), "layers")
+    assert cache.device_error() == 0
