@@ -25,6 +25,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -87,29 +88,55 @@ def parse_args(argv=None):
 
 
 # ---------------------------------------------------------------- micro-batches
+def packed(specs, dev):
+    """One device buffer holding tensors of the given (shape, dtype) at
+    256-byte aligned offsets: (the uint8 buffer, the tensors as views)."""
+    import torch
+    offs, o = [], 0
+    for shape, dt in specs:
+        offs.append(o)
+        nbytes = math.prod(shape) * torch.empty((), dtype=dt).element_size()
+        o = (o + nbytes + 255) // 256 * 256
+    buf = torch.empty(max(o, 16), dtype=torch.uint8, device=dev)
+    views = []
+    for (shape, dt), off in zip(specs, offs):
+        nbytes = math.prod(shape) * torch.empty((), dtype=dt).element_size()
+        views.append(buf[off:off + nbytes].view(dt).view(shape))
+    return buf, views
+
+
 def make_micro_batches(C, cache, wl, bufs0, ld, n_valid, M, split, dev):
-    """Per micro-batch device buffers: contiguous copies of its queries'
-    inputs, its own score / histogram / top-k scratch and its outputs."""
+    """Per micro-batch device buffers: its queries' inputs (the indexer's
+    queries and weights, the layers' queries and windows) packed in one
+    buffer, its outputs (selection, the layers' outputs and lse) in another,
+    so that the end-to-end pipeline moves each with one copy, and its own
+    score / histogram / top-k scratch."""
     import torch
     B, L = wl.batch, wl.layers
     mbs = []
     for m in range(M):
         lo, hi = B * m // M, B * (m + 1) // M
         n = hi - lo
+        srcs = [bufs0["q_idx"][lo:hi], bufs0["w"][lo:hi]] + [x[lo:hi] for x in bufs0["qs"]] + \
+               [x[lo:hi] for x in bufs0["swas"]]
+        in_buf, ins = packed([(tuple(t.shape), t.dtype) for t in srcs], dev)
+        for v, t in zip(ins, srcs):
+            v.copy_(t)
+        out_buf, outv = packed([((n, 512), torch.int32)] +
+                               [((n, 64, 512), torch.bfloat16)] * L +
+                               [((n, 64), torch.float32)] * L, dev)
         mbs.append(dict(
             seq=list(range(lo, hi)), nv=n_valid[lo:hi],
-            q_idx=bufs0["q_idx"][lo:hi].clone(), w=bufs0["w"][lo:hi].clone(),
-            qs=[x[lo:hi].clone() for x in bufs0["qs"]],
-            swas=[x[lo:hi].clone() for x in bufs0["swas"]],
+            in_buf=in_buf, out_buf=out_buf,
+            q_idx=ins[0], w=ins[1], qs=ins[2:2 + L], swas=ins[2 + L:2 + 2 * L],
             scores=torch.empty(n, ld, dtype=torch.float32, device=dev),
             hist=torch.empty(n, 2048, dtype=torch.int32, device=dev),
-            topk=torch.empty(n, 512, dtype=torch.int32, device=dev),
+            topk=outv[0],
             tws=torch.empty(max(16, C.csa2_topk_workspace_bytes(n, max(n_valid))),
                             dtype=torch.uint8, device=dev),
             aws=torch.empty(C.csa2_sparse_attn_workspace_bytes(cache, n) if split else 0,
                             dtype=torch.uint8, device=dev),
-            outs=[torch.empty(n, 64, 512, dtype=torch.bfloat16, device=dev) for _ in range(L)],
-            lses=[torch.empty(n, 64, dtype=torch.float32, device=dev) for _ in range(L)]))
+            outs=outv[1:1 + L], lses=outv[1 + L:1 + 2 * L]))
     return mbs
 
 
@@ -654,6 +681,9 @@ def run_csa2(args):
             mb_graphs.append(row)
         cache.set_index_sms(0)
         copy_streams = [torch.cuda.Stream() for _ in range(M)]
+        # one packed buffer of inputs and one of outputs per micro-batch: one
+        # copy each way per micro-batch and step
+        names_in, names_out = ["in_buf"], ["out_buf"]
         h_in_mb = [[[pin(t) for t in flat(mb_sets[s][m], names_in)] for m in range(M)]
                    for s in range(S)]
         h_out_mb = [[[torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
