@@ -15,17 +15,18 @@
 // that a 128-key K_I tile feeds 256 columns.
 //
 // Pool mode (Reindex layers of the Hierarchical Sparse Indexer, V4.1 report
-// section 2.3.2): a tile is 16 blocks of 8 consecutive keys named by the
-// query's candidate pool, one 3-D TMA box per block (2 KB: its two 1 KB
-// swizzled column halves), so the MMA walks 8-row atoms 2 KB apart; pool
-// slots past the sequence score -inf.  Block ids of the next tile are loaded
-// one tile ahead by the producer and by the epilogue.
+// section 2.3.2): a tile is 32 blocks of 8 consecutive keys named by the
+// query's candidate pool (two M-groups of 16 blocks; a pool of an odd number
+// of 16-block halves ends with a half tile), one 3-D TMA box per block (2 KB:
+// its two 1 KB swizzled column halves), so the MMA walks 8-row atoms 2 KB
+// apart; pool slots past the sequence score -inf.  Block ids of the next
+// tile are loaded one tile ahead by the producer and by the epilogue.
 //
 // Scores are stored as fp32, or (selector precision of the V4 blog reading,
 // section 7) rounded to bf16 with the histogram taken on the rounded value.
 //
 // Persistent CTAs walk a balanced contiguous range of (group, tile) items.
-// Warp roles: warp 0 = TMA producer (lane 0; lanes 0-15 in pool mode), warp 1
+// Warp roles: warp 0 = TMA producer (lane 0; every lane in pool mode), warp 1
 // = MMA issuer (and TMEM owner), then the epilogue warps (TMEM -> registers
 // -> scores): eight with one query per group (two sets of four taking
 // alternate tiles), sixteen with several (four warps per TMEM lane quadrant,
@@ -46,7 +47,7 @@ constexpr int kMaxAcc = 4;                 // accumulators in TMEM (decode 4, se
 constexpr int kBars = 2 * kMaxStages + 2 * kMaxAcc + 4;   // k full / empty, acc full / empty, q full / empty, drain
 
 // One query per group: stages of two M-groups (decode tiles are 256
-// contiguous keys; a pool tile, 16 blocks of 8, fills one); several
+// contiguous keys, pool tiles 32 blocks of 8); several
 // queries: stages of one M-group (128-key tiles).  Three stages either way
 // (with several queries the score-key histograms of the group's queries
 // take the room of a fourth).
@@ -135,9 +136,9 @@ __global__ void __launch_bounds__(64 + 32 * kEpiW, 1)
   const int N = 32 * p.qpg;               // MMA N (columns per M-group)
   const int qrows = 32 * p.qpg;
   const int n_stages = stages_of(p.qpg), stage_bytes = stage_bytes_of(p.qpg);
-  // decode tiles: two M-groups of 128 contiguous keys; pool and several
-  // queries: one
-  const int mgroups = (p.qpg == 1 && !p.pool) ? 2 : 1;
+  // one query: two M-groups of 128 keys (contiguous, or 16 pool blocks
+  // each); several queries: one
+  const int mgroups = p.qpg == 1 ? 2 : 1;
   const int tile_e = kTileE * mgroups;
   const int acc_cols = mgroups * N;
   // one query (N = 32) keeps four accumulators in flight, several queries
@@ -170,26 +171,28 @@ __global__ void __launch_bounds__(64 + 32 * kEpiW, 1)
   const int end = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
   int g0 = 0;
   while (g0 < p.n_groups && p.tile_prefix[g0 + 1] <= begin) ++g0;
-  // pool row of item `it` (whose group is at or after the cursor's)
-  auto pool_row = [&](int it, GroupCursor c) -> const int32_t* {
+  // block b of pool tile `it` (whose group is at or after the cursor's), or
+  // -1 past the pool's end
+  auto pool_blk = [&](int it, GroupCursor c, int b) -> int32_t {
     c.advance(p, it);
-    return p.pool + (int64_t)c.g * p.pool_blocks + (it - c.lo) * (kTileE / 8);
+    const int i = (it - c.lo) * (tile_e / 8) + b;
+    return i < p.pool_blocks ? __ldg(p.pool + (int64_t)c.g * p.pool_blocks + i) : -1;
   };
   GroupCursor c0;
   c0.init(p, g0);
 
   if (warp == 0 && begin < end) {
     // ------------------------------------------------ TMA producer (warp 0)
-    // Lane 0 owns the barriers; in pool mode lanes 0-15 each copy one block.
+    // Lane 0 owns the barriers; in pool mode every lane copies one block.
     GroupCursor gc = c0;
     int cur = -1, stage = 0;
     int64_t gbase = 0;
     uint32_t ph = 0, qph = 0;
     uint32_t armed = 0, armed_ph = 0;   // stages filled at least once, parity of the last fill
     bool ok = true;
-    const bool pool_lane = p.pool != nullptr && lane < kTileE / 8;
+    const bool pool_lane = p.pool != nullptr && lane < tile_e / 8;
     const uint64_t keys_pol = l2_policy_evict_first();
-    int32_t nxt = pool_lane ? __ldg(pool_row(begin, c0) + lane) : -1;
+    int32_t nxt = pool_lane ? pool_blk(begin, c0, lane) : -1;
     for (int it = begin; it < end && ok; ++it) {
       gc.advance(p, it);
       const int g = gc.g;
@@ -218,7 +221,7 @@ __global__ void __launch_bounds__(64 + 32 * kEpiW, 1)
       uint8_t* dst = kbuf + stage * stage_bytes;
       if (p.pool) {
         const int32_t blk = nxt;
-        if (pool_lane && it + 1 < end) nxt = __ldg(pool_row(it + 1, gc) + lane);
+        if (pool_lane && it + 1 < end) nxt = pool_blk(it + 1, gc, lane);
         const uint32_t n_ok = (uint32_t)__popc(__ballot_sync(0xffffffffu, blk >= 0));
         if (lane == 0) mbar_arrive_expect_tx(k_full + stage, n_ok * 8 * kIdxDim * 2);
         __syncwarp();
@@ -322,12 +325,21 @@ __global__ void __launch_bounds__(64 + 32 * kEpiW, 1)
       for (int i = et; i < kKeyHistBins; i += 128) hsg[i] = 0u;
     GroupCursor gc = c0;
     int cur = -1, nvis = 0;
-    int32_t blk_nxt = (p.pool && begin + gsel < end) ? __ldg(pool_row(begin + gsel, c0) + (row >> 3)) : -1;
+    // pool mode: the blocks of this thread's slots (row and 128 + row) of
+    // the next tile of its set
+    int32_t blk_nxt[2] = {-1, -1};
+    if (p.pool && begin + gsel < end) {
+      blk_nxt[0] = pool_blk(begin + gsel, c0, row >> 3);
+      blk_nxt[1] = pool_blk(begin + gsel, c0, 16 + (row >> 3));
+    }
     for (int it = begin + gsel; it < end; it += 2) {
       gc.advance(p, it);
       const int g = gc.g;
-      const int32_t blk = blk_nxt;
-      if (p.pool && it + 2 < end) blk_nxt = __ldg(pool_row(it + 2, gc) + (row >> 3));
+      const int32_t blk[2] = {blk_nxt[0], blk_nxt[1]};
+      if (p.pool && it + 2 < end) {
+        blk_nxt[0] = pool_blk(it + 2, gc, row >> 3);
+        blk_nxt[1] = pool_blk(it + 2, gc, 16 + (row >> 3));
+      }
       if (g != cur) {
         if (use_hist && cur >= 0) flush(cur);
         gsync();
@@ -348,9 +360,10 @@ __global__ void __launch_bounds__(64 + 32 * kEpiW, 1)
       auto store = [&](int mg, float s) {
         const int e = t * tile_e + mg * kTileE + row;
         if (p.pool) {
-          const int64_t ent = (int64_t)blk * 8 + (row & 7);
-          const float v = (blk >= 0 && ent < nvis) ? s : -INFINITY;
-          if (CSA2_IN_BOUNDS(e < p.ld, p.err)) {
+          // slots past the pool (the second half of a half tile) are not stored
+          const int64_t ent = (int64_t)blk[mg] * 8 + (row & 7);
+          const float v = (blk[mg] >= 0 && ent < nvis) ? s : -INFINITY;
+          if (e < p.ld) {
             p.scores[(int64_t)g * p.ld + e] = v;
             if (use_hist) atomicAdd(hsg + (score_key(v) >> 21), 1u);
           }
@@ -413,12 +426,12 @@ __global__ void __launch_bounds__(64 + 32 * kEpiW, 1)
     int cur = -1, acc = 0;
     uint32_t aph = 0;
     int nvis[kMaxQ];   // visible entries of this thread's queries in the current group
-    int32_t blk_nxt = (p.pool && begin < end) ? __ldg(pool_row(begin, c0) + (row >> 3)) : -1;
+    int32_t blk_nxt = (p.pool && begin < end) ? pool_blk(begin, c0, row >> 3) : -1;
     for (int it = begin; it < end; ++it) {
       gc.advance(p, it);
       const int g = gc.g;
       const int32_t blk = blk_nxt;
-      if (p.pool && it + 1 < end) blk_nxt = __ldg(pool_row(it + 1, gc) + (row >> 3));
+      if (p.pool && it + 1 < end) blk_nxt = pool_blk(it + 1, gc, row >> 3);
       if (g != cur) {
         if (use_hist && cur >= 0) flush(cur);
         esync();
@@ -445,7 +458,7 @@ __global__ void __launch_bounds__(64 + 32 * kEpiW, 1)
           // slot t * 128 + row of the pool; its entry decides validity
           const int64_t ent = (int64_t)blk * 8 + (row & 7);
           const float v = (blk >= 0 && ent < nv) ? s : -INFINITY;
-          if (CSA2_IN_BOUNDS(e < p.ld, p.err)) {
+          if (e < p.ld) {
             p.scores[(int64_t)q * p.ld + e] = v;
             if (use_hist) atomicAdd(hs + j * kKeyHistBins + (score_key(v) >> 21), 1u);
           }

@@ -94,7 +94,11 @@ def test_pool_against_the_oracles_scores(C):
         _check_pool_near_ties(pool[i], o_pool, bs)
 
 
-def test_reindex_matches_oracle(C):
+@pytest.mark.parametrize("max_blocks", [2048, 48])
+def test_reindex_matches_oracle(C, max_blocks):
+    """Reindex selection against the oracle; 48 blocks = one tile of 32 and a
+    half tile of 16, whose second half must write nothing (scores of the
+    next query's row)."""
     import torch
     lens = [30000, 16384, 2000, 0, 20001]
     cache, ks = _fill(C, lens, 30720, 75)
@@ -104,7 +108,7 @@ def test_reindex_matches_oracle(C):
     qr, wr = _queries(77, nq)            # the Reindex layer's own query
     sc = _full_scores(C, cache, qf, wf, seq_ids, 30720)
     nv = [lens[s] for s in seq_ids]
-    pool_d = C.csa2_hsi_pool(sc, nv, max_blocks=2048)
+    pool_d = C.csa2_hsi_pool(sc, nv, max_blocks=max_blocks)
     tsc = torch.full((nq, 512), 7.0, device="cuda")
     idx = C.csa2_index_topk_reindex_decode(cache, bf16_dev(qr), f32_dev(wr), pool_d,
                                            seq_ids, topk_score=tsc).cpu().numpy()
