@@ -1242,7 +1242,7 @@ def measure_prefill(C, W, wid, layout, dev, stream, steps, warmup):
     """Chunked prefill of one sequence: the Full layer's causal index scores
     (with each token's score-key histogram, built by the indexer's epilogue)
     and top-512 of every new token from them, then the readout of the Full
-    and the Reuse layers.  Roofline: the dense bf16 tensor pipe (sustained figure) on
+    and the Reuse layers (one launch).  Roofline: the dense bf16 tensor pipe (sustained figure) on
     the step's FLOPs (indexer over the visible entries, attention over the
     selected entries and the causal window)."""
     import torch
@@ -1269,9 +1269,8 @@ def measure_prefill(C, W, wid, layout, dev, stream, steps, warmup):
         C.csa2_topk(scores, n_valid, 512, idx_out=topk, key_hist=hist)
 
     def readout():
-        for l in range(L):
-            C.csa2_sparse_attn_prefill(cache, 0, wl.pos0, qs[l], rows[l], wl.swa_pos0, topk,
-                                       scale, out=outs[l])
+        C.csa2_sparse_attn_prefill_layers(cache, 0, wl.pos0, qs, rows, wl.swa_pos0, topk, scale,
+                                          outs)
 
     for _ in range(warmup):
         index()

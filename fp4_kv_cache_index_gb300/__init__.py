@@ -108,6 +108,8 @@ def _load():
                                             P, P], i32),
         "csa2_sparse_attn_prefill_ex": ([P, i32, i32, i64, P, P, i64, i64, P, ctypes.c_float, P,
                                          P, P, P], i32),
+        "csa2_sparse_attn_prefill_layers": ([P, i32, i32, i32, i64, P, P, i64, i64, P,
+                                             ctypes.c_float, P, P, P, P], i32),
         "csa2_swa_fp8_quantise": ([i64, P, P, P, P, P], i32),
         "csa2_hsi_pool_workspace_bytes": ([i32, i64], sz),
         "csa2_hsi_pool": ([i32, P, i64, P, i32, i32, P, P, sz, P], i32),
@@ -486,6 +488,47 @@ def csa2_sparse_attn_prefill(cache: Cache, seq: int, pos0: int, q: torch.Tensor,
         _check(lib.csa2_sparse_attn_prefill_ex(*args, ctypes.byref(opts), _stream(stream)),
                "csa2_sparse_attn_prefill_ex")
     return out
+
+
+def csa2_sparse_attn_prefill_layers(cache: Cache, seq: int, pos0: int,
+                                    qs: Sequence[torch.Tensor],
+                                    swa_kvs: Optional[Sequence[Optional[torch.Tensor]]],
+                                    swa_pos0: int, topk_idx: torch.Tensor, scale: float,
+                                    outs: Sequence[torch.Tensor],
+                                    lses: Optional[Sequence[Optional[torch.Tensor]]] = None,
+                                    sinks: Optional[Sequence[Optional[torch.Tensor]]] = None,
+                                    rope_out: bool = False, rope_base: float = 0.0,
+                                    swa_fp8s=None, stream=None):
+    """The prefill readout of several layers of a group in one launch (per
+    layer: queries, window rows or their FP8 form, sink, outputs)."""
+    L = len(qs)
+    nq = qs[0].shape[0]
+    n_rows = 0
+    for l in range(L):
+        if swa_fp8s is not None and swa_fp8s[l] is not None:
+            n_rows = swa_fp8s[l][0].shape[0]
+        elif swa_kvs is not None and swa_kvs[l] is not None:
+            n_rows = swa_kvs[l].shape[0]
+    arr = lambda xs: (ctypes.c_void_p * L)(*[_ptr(x) for x in xs])
+    swa_arr = arr(swa_kvs) if swa_kvs is not None else None
+    lse_arr = arr(lses) if lses is not None else None
+    keep = []
+    opts_arr = None
+    if sinks is not None or rope_out or swa_fp8s is not None:
+        ptrs = []
+        for l in range(L):
+            f8 = swa_fp8s[l] if swa_fp8s is not None and swa_fp8s[l] is not None else (None, None, None)
+            o = AttnOpts(_ptr(sinks[l] if sinks is not None else None), None,
+                         1 if rope_out else 0, float(rope_base),
+                         _ptr(f8[0]), _ptr(f8[1]), _ptr(f8[2]))
+            keep.append(o)
+            ptrs.append(ctypes.cast(ctypes.pointer(o), ctypes.c_void_p))
+        opts_arr = (ctypes.c_void_p * L)(*ptrs)
+    _check(lib.csa2_sparse_attn_prefill_layers(cache.handle, seq, L, nq, pos0, arr(qs), swa_arr,
+                                               swa_pos0, n_rows, _ptr(topk_idx), float(scale),
+                                               arr(outs), lse_arr, opts_arr, _stream(stream)),
+           "csa2_sparse_attn_prefill_layers")
+    return outs
 
 
 # ------------------------------------------------------------------ hierarchical sparse indexer

@@ -1071,28 +1071,47 @@ csa2_status_t csa2_sparse_attn_prefill_ex(const csa2_cache_t* c, int32_t seq, in
                                           float* lse, const csa2_attn_opts_t* opts,
                                           csa2_stream_t stream) {
   CSA2_RANGE();
-  if (!c || nq < 0 || seq < 0 || seq >= c->batch || pos0 < 0) return CSA2_ERR_INVALID_ARG;
+  return csa2_sparse_attn_prefill_layers(c, seq, 1, nq, pos0, &q, &swa_kv, swa_pos0, n_swa_rows,
+                                         topk_idx, scale, &out, &lse, &opts, stream);
+}
+
+csa2_status_t csa2_sparse_attn_prefill_layers(const csa2_cache_t* c, int32_t seq, int32_t n_layers,
+                                              int32_t nq, int64_t pos0, const void* const* q,
+                                              const void* const* swa_kv, int64_t swa_pos0,
+                                              int64_t n_swa_rows, const int32_t* topk_idx,
+                                              float scale, void* const* out, float* const* lse,
+                                              const csa2_attn_opts_t* const* opts,
+                                              csa2_stream_t stream) {
+  CSA2_RANGE();
+  if (!c || nq < 0 || seq < 0 || seq >= c->batch || pos0 < 0 || n_layers < 1 ||
+      n_layers > CSA2_MAX_ATTN_LAYERS || !q || !out)
+    return CSA2_ERR_INVALID_ARG;
   if (nq == 0) return CSA2_OK;
   const int W = c->cfg.swa;
-  if (!q || !topk_idx || !out || !aligned16(q) || !aligned16(out) || !aligned16(topk_idx))
+  if (!topk_idx || !aligned16(topk_idx)) return CSA2_ERR_INVALID_ARG;
+  if (W > 0 && (swa_pos0 < 0 || swa_pos0 > pos0 || n_swa_rows <= 0 ||
+                pos0 + nq - 1 - swa_pos0 >= n_swa_rows))
     return CSA2_ERR_INVALID_ARG;
-  if (lse && !aligned16(lse)) return CSA2_ERR_INVALID_ARG;
-  const bool f8 = opts && opts->swa_codes;
-  if (W > 0) {
-    if ((!f8 && (!swa_kv || !aligned16(swa_kv))) || swa_pos0 < 0 || swa_pos0 > pos0 ||
-        n_swa_rows <= 0 || pos0 + nq - 1 - swa_pos0 >= n_swa_rows)
-      return CSA2_ERR_INVALID_ARG;
+  const csa2_attn_opts_t* o0 = opts ? opts[0] : nullptr;
+  for (int l = 0; l < n_layers; ++l) {
+    const csa2_attn_opts_t* ol = opts ? opts[l] : nullptr;
+    if (!q[l] || !out[l] || !aligned16(q[l]) || !aligned16(out[l])) return CSA2_ERR_INVALID_ARG;
+    if (lse && lse[l] && !aligned16(lse[l])) return CSA2_ERR_INVALID_ARG;
+    const bool f8 = ol && ol->swa_codes;
+    const void* sw = swa_kv ? swa_kv[l] : nullptr;
+    if (W > 0 && !f8 && (!sw || !aligned16(sw))) return CSA2_ERR_INVALID_ARG;
+    const bool r0 = o0 && o0->rope_out, rl = ol && ol->rope_out;
+    if (r0 != rl || (rl && ol->rope_base != o0->rope_base)) return CSA2_ERR_INVALID_ARG;
   }
   const int H = c->cfg.n_heads, k = c->cfg.topk;
   AttnParams* p = new (std::nothrow) AttnParams();
-  if (!p) return CSA2_ERR_OOM;
+  AttnMaps* maps = new (std::nothrow) AttnMaps();
+  if (!p || !maps) { delete p; delete maps; return CSA2_ERR_OOM; }
   std::memset(p, 0, sizeof(AttnParams));
   p->topk_idx = topk_idx;
   p->codes = c->codes;
   p->scales = c->scales;
-  p->n_layers = 1;
-  p->layer[0].out = static_cast<uint16_t*>(out);
-  p->layer[0].lse = lse;
+  p->n_layers = n_layers;
   p->err = c->d_err;
   p->nq = nq;
   p->n_heads = H;
@@ -1108,18 +1127,24 @@ csa2_status_t csa2_sparse_attn_prefill_ex(const csa2_cache_t* c, int32_t seq, in
   p->swa_pos0 = swa_pos0;
   p->splits = 1;
   p->wait_cycles = c->wait_cycles;
-  csa2_status_t st =
-      apply_opts(p, &p->layer[0], opts, false, 0, 0) ? CSA2_OK : CSA2_ERR_INVALID_ARG;
-  AttnMaps* maps = new (std::nothrow) AttnMaps();
-  if (!maps) st = CSA2_ERR_OOM;
-  if (st == CSA2_OK && !make_map(&maps->q[0], q, (uint64_t)nq * H, kHeadDim, 64, kAttnHeadGroup))
-    st = CSA2_ERR_CUDA;
-  if (st == CSA2_OK) {
-    if (W > 0 && !f8) {
-      if (!make_map(&maps->swa[0], swa_kv, (uint64_t)n_swa_rows, kHeadDim, 64, 128))
+  csa2_status_t st = CSA2_OK;
+  for (int l = 0; l < n_layers && st == CSA2_OK; ++l) {
+    AttnLayer& ly = p->layer[l];
+    const csa2_attn_opts_t* ol = opts ? opts[l] : nullptr;
+    ly.out = static_cast<uint16_t*>(out[l]);
+    ly.lse = lse ? lse[l] : nullptr;
+    if (!apply_opts(p, &ly, ol, false, 0, 0)) { st = CSA2_ERR_INVALID_ARG; break; }
+    if (!make_map(&maps->q[l], q[l], (uint64_t)nq * H, kHeadDim, 64, kAttnHeadGroup)) {
+      st = CSA2_ERR_CUDA;
+      break;
+    }
+    if (W > 0 && !(ol && ol->swa_codes)) {
+      if (!make_map(&maps->swa[l], swa_kv[l], (uint64_t)n_swa_rows, kHeadDim, 64, 128)) {
         st = CSA2_ERR_CUDA;
+        break;
+      }
     } else {
-      maps->swa[0] = maps->q[0];
+      maps->swa[l] = maps->q[l];
     }
   }
   if (st == CSA2_OK && launch_attn(*p, *maps, S(stream)) != cudaSuccess) st = CSA2_ERR_CUDA;

@@ -601,6 +601,24 @@ csa2_status_t csa2_sparse_attn_prefill_ex(const csa2_cache_t* cache, int32_t seq
                                           const csa2_attn_opts_t* opts,
                                           csa2_stream_t stream);
 
+/* Prefill readout of n_layers layers of one group in one launch, as
+ * csa2_sparse_attn_decode_layers is for decode: layer l's out / lse are
+ * exactly those of csa2_sparse_attn_prefill_ex with q[l], swa_kv[l], out[l],
+ * lse[l], opts[l]; the chunk (seq, pos0, n_queries), the window rows'
+ * geometry (swa_pos0, n_swa_rows) and topk_idx are shared; the layers'
+ * CTAs fill the SMs without a launch boundary between the layers.  Arrays
+ * as for csa2_sparse_attn_decode_layers (the output RoPE base the same in
+ * every layer).                                                           */
+csa2_status_t csa2_sparse_attn_prefill_layers(const csa2_cache_t* cache, int32_t seq,
+                                              int32_t n_layers, int32_t n_queries,
+                                              int64_t pos0, const void* const* q,
+                                              const void* const* swa_kv, int64_t swa_pos0,
+                                              int64_t n_swa_rows, const int32_t* topk_idx,
+                                              float scale, void* const* out,
+                                              float* const* lse,
+                                              const csa2_attn_opts_t* const* opts,
+                                              csa2_stream_t stream);
+
 /* ---- errors ------------------------------------------------------------ */
 
 /* Reads and clears the cache's sticky device error word (synchronises

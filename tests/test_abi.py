@@ -83,6 +83,8 @@ def test_host_argument_errors(lib):
     # before any launch
     assert L.csa2_sparse_attn_decode_layers(None, 2, 1, None, None, None, None, None, 1.0, None,
                                             None, None, 0, None, None) == 1
+    assert L.csa2_sparse_attn_prefill_layers(None, 0, 2, 1, 0, None, None, 0, 0, None, 1.0,
+                                             None, None, None, None) == 1
     assert L.csa2_compress(0, 4, 512, None, None, None, None) == 1
     assert L.csa2_compress(2, 0, 512, None, None, None, None) == 0
     assert L.csa2_compress(32, 4, 512, None, None, None, None) == 2
