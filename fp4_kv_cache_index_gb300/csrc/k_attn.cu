@@ -193,7 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem;
-  const uint32_t s_col = 0, o_col = 64;   // S^T: 64 columns; O^T: 4 d-tiles x 64
+  // S^T: two accumulators of 64 columns (even and odd K steps), summed by
+  // the softmax; O^T: 4 d-tiles x 64 columns
+  const uint32_t s_col = 0, o_col = 128;
 
   // the top-k row into shared memory (unusable slots become -1), and which
   // tiles hold at least one usable index
@@ -322,13 +324,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint64_t d_op = sdesc_sw128(smem_u32(ps), kRows * 128, 1024);
   constexpr uint32_t id_s = idesc_bf16_f32(128, kHG, false, false);
   constexpr uint32_t id_o = idesc_bf16_f32(128, kHG, true, true);
-  // S^T K step ks (channels 16 ks .. 16 ks + 15)
+  // S^T K step ks (channels 16 ks .. 16 ks + 15).  Consecutive steps go to
+  // two accumulators in turn: an MMA into the accumulator that the previous
+  // one still writes waits for it, one into the other does not.
   auto mma_s = [&](int ks) {
     const uint32_t ao = (uint32_t)((ks >> 2) * (kRows * 128) + (ks & 3) * 32);
     const uint32_t bo = (uint32_t)((ks >> 2) * (kHG * 128) + (ks & 3) * 32);
-    umma_bf16(tmem + s_col, d_skv + (ao >> 4), d_sq + (bo >> 4), id_s, ks > 0 ? 1u : 0u);
+    umma_bf16(tmem + s_col + 64 * (ks & 1), d_skv + (ao >> 4), d_sq + (bo >> 4), id_s,
+              ks > 1 ? 1u : 0u);
   };
-  // O^T d-block i (reads KV chunks 2 i, 2 i + 1), K step ks (rows 16 ks ..)
+  // O^T d-block i (reads KV chunks 2 i, 2 i + 1), K step ks (rows 16 ks ..);
+  // issued with the two d-blocks of a half in turn, for the same reason
   auto mma_o = [&](int i, int ks, bool first) {
     const uint32_t ao = (uint32_t)((2 * i) * (kRows * 128) + ks * 2048);
     const uint32_t bo = (uint32_t)(ks * 2048);
@@ -488,11 +494,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     float x[16], mh[16];
     bool need = false;
     {
-      uint32_t r[16];
-      tmem_ld16(tmem + lane_addr + s_col + 16 * hh, r);
+      uint32_t r[16], r2[16];
+      tmem_ld16x2(tmem + lane_addr + s_col + 16 * hh, tmem + lane_addr + s_col + 64 + 16 * hh,
+                  r, r2);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        x[i] = valid ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
+        x[i] = valid ? (__uint_as_float(r[i]) + __uint_as_float(r2[i])) * p.scale_log2
+                     : -INFINITY;
         mh[i] = sm.m[16 * hh + i];
         need = need || x[i] > mh[i] + kLazyRescale;
       }
@@ -567,9 +575,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t ph_o = (uint32_t)(ti & 1);
     if (tid == 0) {
       tc_fence_after();
-      for (int k = 0; k < 16; ++k) mma_o(k >> 3, k & 7, first);
+      for (int k = 0; k < 16; ++k) mma_o(k & 1, k >> 1, first);
       umma_commit(&sm.bar_o[0]);
-      for (int k = 16; k < 32; ++k) mma_o(k >> 3, k & 7, first);
+      for (int k = 0; k < 16; ++k) mma_o(2 + (k & 1), k >> 1, first);
       umma_commit(&sm.bar_o[1]);
     }
     if (ti + 1 < n_tiles) {

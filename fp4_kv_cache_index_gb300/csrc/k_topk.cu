@@ -107,6 +107,22 @@ __device__ __forceinline__ void hist_add_aggregated(uint32_t* hist, bool active,
     atomicAdd(hist + bin, (uint32_t)__popc(peers));
 }
 
+// "The key of f lies in a digit-1 bin >= b1", on the raw bits of f.  For b1
+// above the bin of +0 (b1 > 1024) the keys >= b1 << 21 are exactly the
+// floats whose bits, read as a signed integer, are >= (b1 << 21) & 0x7FFFFFFF:
+// negative floats and -0 (whose key equals that of +0) fall below it, +NaN
+// above, as their keys do.  Otherwise the key itself is formed.
+struct BinTest {
+  uint32_t b1;
+  int32_t t;
+  bool fast;
+  __device__ __forceinline__ explicit BinTest(uint32_t b)
+      : b1(b), t((int32_t)((b << 21) & 0x7FFFFFFFu)), fast(b > 1024u) {}
+  __device__ __forceinline__ bool operator()(float f) const {
+    return fast ? (int32_t)__float_as_uint(f) >= t : (score_key(f) >> 21) >= b1;
+  }
+};
+
 // Bin holding the rem-th largest key counted in hist (nbins <= 2 * kThreads);
 // records it and the count strictly above it.
 __device__ __forceinline__ void select_bin(Shared& sh, int nbins, uint32_t rem) {
@@ -268,6 +284,8 @@ __global__ void __launch_bounds__(kSegThreads, 8) k_topk_seg(const __grid_consta
   const uint32_t b1 = sh.sel_bin;
   if (sh.sel_above + sh.sel_count > (uint32_t)kCandCap) return;  // the row falls back
   // pass 1: which of the 32 scores are candidates
+  const BinTest in_bins(b1);
+  const int lim = (int)(n - e0 > kSegPer ? kSegPer : n - e0);   // e0 < n here or lim <= 0
   uint32_t mask = 0;
 #pragma unroll
   for (int q = 0; q < kSegPer / 8; ++q) {
@@ -275,7 +293,7 @@ __global__ void __launch_bounds__(kSegThreads, 8) k_topk_seg(const __grid_consta
     seg_chunk(srow, e0, q, n, vec, v);
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      if (e0 + 8 * q + i < n && (score_key(v[i]) >> 21) >= b1) mask |= 1u << (8 * q + i);
+      mask |= (uint32_t)(8 * q + i < lim && in_bins(v[i])) << (8 * q + i);
   }
   const uint32_t cnt = (uint32_t)__popc(mask);
   uint32_t incl = cnt;
@@ -395,28 +413,47 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
     }
     __syncthreads();
   } else if (n_cand <= (uint32_t)kCandCap) {
-    // ---- ordered compaction of every key in bins >= b1
+    // ---- ordered compaction of every key in bins >= b1: two runs of kPer
+    //      scores per thread (a and b, one chunk apart) share one block-wide
+    //      scan, their counts packed in one word (a chunk holds at most 8192)
+    const BinTest in_bins(b1);
     uint32_t base = 0;
-    for (int64_t c0 = 0; c0 < n; c0 += chunk) {
-      const int64_t e = c0 + (int64_t)tid * kPer;
-      float v[kPer];
-      load_run(srow, e, n, vec, v);
-      uint32_t key[kPer], cnt = 0;
+    for (int64_t c0 = 0; c0 < n; c0 += 2 * chunk) {
+      const int64_t ea = c0 + (int64_t)tid * kPer, eb = ea + chunk;
+      const int la = (int)(n - ea < 0 ? 0 : (n - ea > kPer ? kPer : n - ea));
+      const int lb = (int)(n - eb < 0 ? 0 : (n - eb > kPer ? kPer : n - eb));
+      float va[kPer], vb[kPer];
+      load_run(srow, ea, n, vec, va);
+      load_run(srow, eb, n, vec, vb);
+      uint32_t ma = 0u, mb = 0u;
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
-        key[i] = score_key(v[i]);
-        cnt += (e + i < n && (key[i] >> 21) >= b1);
+        ma |= (uint32_t)(i < la && in_bins(va[i])) << i;
+        mb |= (uint32_t)(i < lb && in_bins(vb[i])) << i;
       }
+      const uint32_t ca = (uint32_t)__popc(ma), cb = (uint32_t)__popc(mb);
       uint32_t tot;
-      uint32_t pos = base + block_prefix_sum(cnt, sh, tot) - cnt;
+      const uint32_t incl = block_prefix_sum(ca | (cb << 16), sh, tot);
+      uint32_t pa = base + (incl & 0xFFFFu) - ca;
+      uint32_t pb = base + (tot & 0xFFFFu) + (incl >> 16) - cb;
 #pragma unroll
-      for (int i = 0; i < kPer; ++i)
-        if (e + i < n && (key[i] >> 21) >= b1 && pos < (uint32_t)kCandCap) {
-          sh.u.cand.key[pos] = key[i];
-          sh.u.cand.idx[pos] = (int32_t)(e + i);
-          ++pos;
+      for (int i = 0; i < kPer; ++i) {
+        if ((ma >> i) & 1u) {
+          if (pa < (uint32_t)kCandCap) {
+            sh.u.cand.key[pa] = score_key(va[i]);
+            sh.u.cand.idx[pa] = (int32_t)(ea + i);
+          }
+          ++pa;
         }
-      base += tot;
+        if ((mb >> i) & 1u) {
+          if (pb < (uint32_t)kCandCap) {
+            sh.u.cand.key[pb] = score_key(vb[i]);
+            sh.u.cand.idx[pb] = (int32_t)(eb + i);
+          }
+          ++pb;
+        }
+      }
+      base += (tot & 0xFFFFu) + (tot >> 16);
     }
   }
   if (n_cand <= (uint32_t)kCandCap) {
