@@ -1352,7 +1352,8 @@ def run_prefill(args):
                                      "entries", "ratio", "layers", "layout")},
         "roofline": r["roofline"], "parts_tensor_frac": r["parts_tensor_frac"],
         "kernel_ms": r["kernel_ms"],
-        "gpu_launches": args.steps * (1 + (wl.n_queries() + 1023) // 1024 + wl.layers),
+        # the indexer, one top-k launch per 1024 rows, one readout launch
+        "gpu_launches": args.steps * (1 + (wl.n_queries() + 1023) // 1024 + 1),
         "clocks": clocks,
     }
     if rank == 0:

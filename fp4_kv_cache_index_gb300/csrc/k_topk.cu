@@ -26,13 +26,16 @@
 namespace csa2 {
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
+// Row kernel: kT threads per row, 1024 (one row per SM, for a few long
+// rows) or 512 (two rows per SM, for many rows: one row's block-wide steps
+// overlap the other's loads).
 constexpr int kBins = 2048;
 constexpr int kCandCap = 8192;
 constexpr int kSubHists = 8;
+constexpr int kTopkManyRows = 512;   // rows of a launch from which kT = 512
 
 
+template <int kT>
 struct Shared {
   uint32_t hist[kBins];
   union {
@@ -42,13 +45,15 @@ struct Shared {
     } cand;
     uint32_t sub[kSubHists][kBins];
   } u;
-  uint32_t warp_sum[kWarps];
+  uint32_t warp_sum[kT / 32];
   uint32_t sel_bin;
   uint32_t sel_above;
 };
 
 // Inclusive suffix sum over the block (thread t gets the sum over t' >= t).
-__device__ __forceinline__ uint32_t block_suffix_sum(uint32_t v, Shared& sh) {
+template <int kT>
+__device__ __forceinline__ uint32_t block_suffix_sum(uint32_t v, Shared<kT>& sh) {
+  constexpr int kWarps = kT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -58,13 +63,13 @@ __device__ __forceinline__ uint32_t block_suffix_sum(uint32_t v, Shared& sh) {
   if (lane == 0) sh.warp_sum[warp] = v;
   __syncthreads();
   if (warp == 0) {
-    uint32_t w = sh.warp_sum[lane];
+    uint32_t w = lane < kWarps ? sh.warp_sum[lane] : 0u;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t n = __shfl_down_sync(0xffffffffu, w, o);
       if (lane + o < 32) w += n;
     }
-    sh.warp_sum[lane] = w;
+    if (lane < kWarps) sh.warp_sum[lane] = w;
   }
   __syncthreads();
   const uint32_t later = (warp + 1 < kWarps) ? sh.warp_sum[warp + 1] : 0u;
@@ -73,7 +78,10 @@ __device__ __forceinline__ uint32_t block_suffix_sum(uint32_t v, Shared& sh) {
 }
 
 // Inclusive prefix sum over the block; `total` gets the block sum.
-__device__ __forceinline__ uint32_t block_prefix_sum(uint32_t v, Shared& sh, uint32_t& total) {
+template <int kT>
+__device__ __forceinline__ uint32_t block_prefix_sum(uint32_t v, Shared<kT>& sh,
+                                                     uint32_t& total) {
+  constexpr int kWarps = kT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -83,13 +91,13 @@ __device__ __forceinline__ uint32_t block_prefix_sum(uint32_t v, Shared& sh, uin
   if (lane == 31) sh.warp_sum[warp] = v;
   __syncthreads();
   if (warp == 0) {
-    uint32_t w = sh.warp_sum[lane];
+    uint32_t w = lane < kWarps ? sh.warp_sum[lane] : 0u;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t n = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += n;
     }
-    sh.warp_sum[lane] = w;
+    if (lane < kWarps) sh.warp_sum[lane] = w;
   }
   __syncthreads();
   const uint32_t before = warp ? sh.warp_sum[warp - 1] : 0u;
@@ -123,17 +131,28 @@ struct BinTest {
   }
 };
 
-// Bin holding the rem-th largest key counted in hist (nbins <= 2 * kThreads);
-// records it and the count strictly above it.
-__device__ __forceinline__ void select_bin(Shared& sh, int nbins, uint32_t rem) {
-  const int t = threadIdx.x;
-  const uint32_t h0 = (2 * t < nbins) ? sh.hist[2 * t] : 0u;
-  const uint32_t h1 = (2 * t + 1 < nbins) ? sh.hist[2 * t + 1] : 0u;
-  const uint32_t suf = block_suffix_sum(h0 + h1, sh);  // bins >= 2t
-  const uint32_t suf1 = suf - h0;                        // bins >= 2t+1
-  const uint32_t suf2 = suf1 - h1;                       // bins >= 2t+2
-  if (2 * t + 1 < nbins && suf1 >= rem && suf2 < rem) { sh.sel_bin = 2 * t + 1; sh.sel_above = suf2; }
-  if (2 * t < nbins && suf >= rem && suf1 < rem) { sh.sel_bin = 2 * t; sh.sel_above = suf1; }
+// Bin holding the rem-th largest key counted in hist (nbins = 1024 or 2048,
+// a multiple of kT: thread t holds bins [nb t, nb t + nb)); records it and
+// the count strictly above it.
+template <int kT>
+__device__ __forceinline__ void select_bin(Shared<kT>& sh, int nbins, uint32_t rem) {
+  constexpr int kMaxB = kBins / kT;
+  const int t = threadIdx.x, nb = nbins / kT;
+  uint32_t h[kMaxB], mine = 0u;
+#pragma unroll
+  for (int j = 0; j < kMaxB; ++j) {
+    h[j] = j < nb ? sh.hist[nb * t + j] : 0u;
+    mine += h[j];
+  }
+  const uint32_t suf = block_suffix_sum<kT>(mine, sh);   // bins >= nb t
+  uint32_t above = suf - mine;                             // bins >= nb t + nb
+#pragma unroll
+  for (int j = kMaxB - 1; j >= 0; --j) {
+    if (j < nb) {
+      if (above < rem && above + h[j] >= rem) { sh.sel_bin = nb * t + j; sh.sel_above = above; }
+      above += h[j];
+    }
+  }
   __syncthreads();
 }
 
@@ -190,8 +209,9 @@ __device__ __forceinline__ void load_run(const ScoreRow& row, int64_t e, int64_t
   }
 }
 
+template <int kT>
 __device__ __forceinline__ void clear(uint32_t* h, int n) {
-  for (int i = threadIdx.x; i < n; i += kThreads) h[i] = 0u;
+  for (int i = threadIdx.x; i < n; i += kT) h[i] = 0u;
   __syncthreads();
 }
 
@@ -332,10 +352,12 @@ __global__ void __launch_bounds__(kSegThreads, 8) k_topk_seg(const __grid_consta
   if (tid == 0) out[0] = total < (uint32_t)kCandCap ? total : (uint32_t)kCandCap;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ TopkParams p,
-                                                       int row0) {
+template <int kT>
+__global__ void __launch_bounds__(kT, 1024 / kT) k_topk(const __grid_constant__ TopkParams p,
+                                                         int row0) {
+  constexpr int kThreads = kT;
   extern __shared__ uint8_t smem_raw[];
-  Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
+  Shared<kT>& sh = *reinterpret_cast<Shared<kT>*>(smem_raw);
   griddep_wait();
   const int row = row0 + blockIdx.x;
   if (row >= p.rows) return;
@@ -362,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
     for (int i = tid; i < kBins; i += kThreads) sh.hist[i] = hrow[i];
     __syncthreads();
   } else {
-    clear(&sh.u.sub[0][0], kSubHists * kBins);
+    clear<kT>(&sh.u.sub[0][0], kSubHists * kBins);
     uint32_t* mine = sh.u.sub[warp & (kSubHists - 1)];
     for (int64_t c0 = 0; c0 < n; c0 += chunk) {
       const int64_t e = c0 + (int64_t)tid * kPer;
@@ -381,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
     }
     __syncthreads();
   }
-  select_bin(sh, kBins, (uint32_t)k);
+  select_bin<kT>(sh, kBins, (uint32_t)k);
   const uint32_t b1 = sh.sel_bin;
   uint32_t above = sh.sel_above;
   const uint32_t n_cand = above + sh.hist[b1];
@@ -393,10 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
     //      counts are read at once (one segment per thread), their exclusive
     //      prefix goes to sh.hist (free until digit 2), and each candidate
     //      position finds its segment by binary search
-    const int nseg = (int)((n + kTopkSegLen - 1) / kTopkSegLen);   // <= kThreads
+    const int nseg = (int)((n + kTopkSegLen - 1) / kTopkSegLen);   // <= kT (host)
     const uint32_t cnt = (tid < nseg) ? p.seg_ws[((int64_t)row * p.n_seg + tid) * kSegWords] : 0u;
     uint32_t tot;
-    const uint32_t incl = block_prefix_sum(cnt, sh, tot);
+    const uint32_t incl = block_prefix_sum<kT>(cnt, sh, tot);
     if (tid < nseg) sh.hist[tid] = incl - cnt;
     __syncthreads();
     for (uint32_t pos = tid; pos < tot && pos < (uint32_t)kCandCap; pos += kThreads) {
@@ -433,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
       }
       const uint32_t ca = (uint32_t)__popc(ma), cb = (uint32_t)__popc(mb);
       uint32_t tot;
-      const uint32_t incl = block_prefix_sum(ca | (cb << 16), sh, tot);
+      const uint32_t incl = block_prefix_sum<kT>(ca | (cb << 16), sh, tot);
       uint32_t pa = base + (incl & 0xFFFFu) - ca;
       uint32_t pb = base + (tot & 0xFFFFu) + (incl >> 16) - cb;
 #pragma unroll
@@ -458,29 +480,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
   }
   if (n_cand <= (uint32_t)kCandCap) {
     // ---- digit 2 (bits [20:10]) and digit 3 (bits [9:0]) on the candidates
-    clear(sh.hist, kBins);
+    clear<kT>(sh.hist, kBins);
     for (uint32_t i = tid; i < n_cand; i += kThreads) {
       const uint32_t key = sh.u.cand.key[i];
       if ((key >> 21) == b1) atomicAdd(sh.hist + ((key >> 10) & 0x7FFu), 1u);
     }
     __syncthreads();
-    select_bin(sh, kBins, (uint32_t)k - above);
+    select_bin<kT>(sh, kBins, (uint32_t)k - above);
     const uint32_t p2 = (b1 << 11) | sh.sel_bin;
     above += sh.sel_above;
     __syncthreads();
-    clear(sh.hist, 1024);
+    clear<kT>(sh.hist, 1024);
     for (uint32_t i = tid; i < n_cand; i += kThreads) {
       const uint32_t key = sh.u.cand.key[i];
       if ((key >> 10) == p2) atomicAdd(sh.hist + (key & 0x3FFu), 1u);
     }
     __syncthreads();
-    select_bin(sh, 1024, (uint32_t)k - above);
+    select_bin<kT>(sh, 1024, (uint32_t)k - above);
     T = (p2 << 10) | sh.sel_bin;
     above += sh.sel_above;
     __syncthreads();
     // ---- emission from the candidates (already in index order)
     const uint32_t need_eq = (uint32_t)k - above;
-    const uint32_t per = (n_cand + kThreads - 1) / kThreads;  // <= 8
+    const uint32_t per = (n_cand + kThreads - 1) / kThreads;  // <= 8192 / kT
     const uint32_t i0 = tid * per;
     uint32_t gt = 0, eq = 0;
     for (uint32_t i = i0; i < i0 + per && i < n_cand; ++i) {
@@ -489,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
     }
     uint32_t tot;
     const uint32_t packed = gt | (eq << 16);
-    const uint32_t before = block_prefix_sum(packed, sh, tot) - packed;
+    const uint32_t before = block_prefix_sum<kT>(packed, sh, tot) - packed;
     uint32_t g_before = before & 0xFFFFu, q_before = before >> 16;
     for (uint32_t i = i0; i < i0 + per && i < n_cand; ++i) {
       const uint32_t key = sh.u.cand.key[i];
@@ -509,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
 
   // ---- crowded bin: digits 2 and 3 re-read the row
   uint32_t prefix = b1;
-  clear(sh.hist, kBins);
+  clear<kT>(sh.hist, kBins);
   for (int64_t c0 = 0; c0 < n; c0 += chunk) {
     const int64_t e = c0 + (int64_t)tid * kPer;
     float v[kPer];
@@ -521,11 +543,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
     }
   }
   __syncthreads();
-  select_bin(sh, kBins, (uint32_t)k - above);
+  select_bin<kT>(sh, kBins, (uint32_t)k - above);
   prefix = (prefix << 11) | sh.sel_bin;
   above += sh.sel_above;
   __syncthreads();
-  clear(sh.hist, kBins);
+  clear<kT>(sh.hist, kBins);
   for (int64_t c0 = 0; c0 < n; c0 += chunk) {
     const int64_t e = c0 + (int64_t)tid * kPer;
     float v[kPer];
@@ -537,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
     }
   }
   __syncthreads();
-  select_bin(sh, 1024, (uint32_t)k - above);
+  select_bin<kT>(sh, 1024, (uint32_t)k - above);
   T = (prefix << 10) | sh.sel_bin;
   above += sh.sel_above;
   __syncthreads();
@@ -560,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
     }
     uint32_t tot;
     const uint32_t packed = gt | (eq << 16);
-    const uint32_t before = block_prefix_sum(packed, sh, tot) - packed;
+    const uint32_t before = block_prefix_sum<kT>(packed, sh, tot) - packed;
     uint32_t g_before = base_gt + (before & 0xFFFFu);
     uint32_t q_before = base_eq + (before >> 16);
 #pragma unroll
@@ -594,8 +616,16 @@ size_t topk_seg_bytes(int32_t rows, int64_t max_valid) {
 }
 
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
-  const int smem = (int)sizeof(Shared);
-  cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // many rows: two 512-thread rows per SM; few (long) rows, or more than 512
+  // segments a row (one per thread when the row reads them back): one row of
+  // 1024 threads per SM
+  const bool seg = p.seg_ws && p.key_hist && p.n_seg > 0;
+  const bool many = p.rows >= kTopkManyRows && !(seg && p.n_seg > 512);
+  const int smem = many ? (int)sizeof(Shared<512>) : (int)sizeof(Shared<1024>);
+  cudaError_t e = many ? cudaFuncSetAttribute(k_topk<512>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                       : cudaFuncSetAttribute(k_topk<1024>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.stream = s;
@@ -604,7 +634,7 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
   cfg.numAttrs = 1;
   for (int r0 = 0; r0 < p.rows; r0 += kTopkMaxRowsPerLaunch) {
     const int nr = (p.rows - r0 < kTopkMaxRowsPerLaunch) ? p.rows - r0 : kTopkMaxRowsPerLaunch;
-    if (p.seg_ws && p.key_hist && p.n_seg > 0) {
+    if (seg) {
       cfg.gridDim = dim3((unsigned)p.n_seg, (unsigned)nr);
       cfg.blockDim = dim3(kSegThreads);
       cfg.dynamicSmemBytes = 0;
@@ -612,9 +642,10 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
       if (e != cudaSuccess) return e;
     }
     cfg.gridDim = dim3((unsigned)nr);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(many ? 512 : 1024);
     cfg.dynamicSmemBytes = (size_t)smem;
-    e = cudaLaunchKernelEx(&cfg, k_topk, p, r0);
+    e = many ? cudaLaunchKernelEx(&cfg, k_topk<512>, p, r0)
+             : cudaLaunchKernelEx(&cfg, k_topk<1024>, p, r0);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

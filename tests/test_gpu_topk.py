@@ -125,3 +125,33 @@ def test_segmented_unaligned_rows(C):
                       workspace=ws).cpu().numpy()
     for r, n in enumerate(ns):
         assert np.array_equal(got[r], O.topk(buf[r, :n], 512)), r
+
+
+@pytest.mark.parametrize("mode", ["plain", "key_hist", "segments"])
+def test_many_rows_two_per_sm(C, mode):
+    """A launch of 512 rows or more runs 512 threads a row, two rows per SM:
+    rows of every kind and length (empty, below, at and above k, crowded,
+    ties, signed zeros), with the row kernel's own histogram, with the
+    score-key histogram, and with segments read back."""
+    import torch
+    from tests.test_gpu_index import _key_hist
+    rng = np.random.default_rng(23)
+    kinds = ["normal", "ints", "equal", "crowded", "signed_zero", "relu_like"]
+    lens = [0, 5, 511, 512, 513, 3000, 8193, 20000]
+    R, ld = 640, 20004
+    buf = np.zeros((R, ld), np.float32)
+    ns = []
+    for r in range(R):
+        n = lens[r % len(lens)]
+        buf[r, :n] = _rows(kinds[(r // len(lens)) % len(kinds)], max(n, 1), rng)[:n]
+        ns.append(n)
+    kh = ws = None
+    if mode != "plain":
+        kh = torch.from_numpy(np.stack([_key_hist(buf[r, :n]) for r, n in enumerate(ns)])
+                              .astype(np.int32)).cuda()
+    if mode == "segments":
+        ws = torch.empty(C.csa2_topk_workspace_bytes(R, max(ns)), dtype=torch.uint8,
+                         device="cuda")
+    got = C.csa2_topk(f32_dev(buf), ns, 512, key_hist=kh, workspace=ws).cpu().numpy()
+    for r, n in enumerate(ns):
+        assert np.array_equal(got[r], O.topk(buf[r, :n], 512)), r
