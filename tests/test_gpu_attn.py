@@ -366,3 +366,65 @@ def test_layers_epilogue_options_per_layer(C):
             cache.handle, 2, nq, None, arr(qs[:2]), arr(rows[:2]), None, C._ptr(idx_d),
             float(SCALE), arr(outs[:2]), None, None, 0, oarr, C._stream(None)), "layers")
     assert cache.device_error() == 0
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_batch_equals_chunked_launches(C, fp8):
+    """A readout launch of more (query, layer) items than SMs gives, bit for
+    bit, the outputs and lse of launches over chunks of its queries, over
+    queries with no entry and no window row (no tile at all), short and full
+    windows, bf16 or FP8 window rows; a sample of queries is checked against
+    the oracle."""
+    import torch
+    rng = np.random.default_rng(101 + fp8)
+    nq, L = 170, 2
+    lens = [int(x) for x in rng.integers(0, 1200, nq)]
+    for i in range(0, nq, 17):
+        lens[i] = 0
+    cache, ents = _cache(C, lens, 1200, 102)
+    swl = rng.integers(0, 129, nq).astype(np.int32)
+    swl[::17] = 0                            # with lens[i] = 0: no tile
+    swl[5::17] = 128
+    qs = [S.normal_bf16(S.stream_key(103, S.S_Q, l), 0, nq * 64 * 512).reshape(nq, 64, 512)
+          for l in range(L)]
+    swas = [S.normal_bf16(S.stream_key(103, S.S_SWA, l), 0, nq * 128 * 512).reshape(nq, 128, 512)
+            for l in range(L)]
+    idx = np.stack([_sel(rng, n) for n in lens])
+    idx_d = torch.from_numpy(idx).cuda()
+    q_d = [bf16_dev(x) for x in qs]
+    s_d = [bf16_dev(x) for x in swas]
+    f8 = [C.csa2_swa_fp8_quantise(x) for x in s_d] if fp8 else None
+    swl_d = torch.from_numpy(swl).cuda()
+    no_split = torch.empty(0, dtype=torch.uint8, device="cuda")
+
+    def run(lo, hi):
+        outs = [torch.empty(hi - lo, 64, 512, dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+        lses = [torch.empty(hi - lo, 64, device="cuda") for _ in range(L)]
+        f8s = None if f8 is None else [tuple(t[lo * 128:hi * 128] for t in f) for f in f8]
+        C.csa2_sparse_attn_decode_layers(
+            cache, [x[lo:hi] for x in q_d], None if fp8 else [x[lo:hi] for x in s_d],
+            idx_d[lo:hi], float(SCALE), outs, lses, swa_len=swl_d[lo:hi],
+            seq_ids=list(range(lo, hi)), workspace=no_split, swa_fp8s=f8s)
+        return outs, lses
+
+    outs, lses = run(0, nq)
+    for lo in range(0, nq, 30):
+        hi = min(nq, lo + 30)
+        o1, l1 = run(lo, hi)
+        for l in range(L):
+            assert torch.equal(o1[l].view(torch.int16), outs[l][lo:hi].view(torch.int16)), (lo, l)
+            assert torch.equal(l1[l], lses[l][lo:hi]), (lo, l)
+    o = bf16_host(outs[1])
+    ls = lses[1].cpu().numpy()
+    for i in (0, 5, 22, 100, 169):
+        if lens[i] == 0 and swl[i] == 0:
+            assert np.all(o[i] == 0) and np.all(np.isneginf(ls[i]))
+            continue
+        rows = swas[1][i, :swl[i]]
+        if fp8:
+            rows = O.swa_fp8_round_bf16(rows)
+        codes, scales = O.quantise(ents[i], 0)
+        _, ref, rl = O.sparse_attention(qs[1][i], codes, scales, 0, idx[i], rows, SCALE)
+        check_attn(o[i], ref)
+        check_lse(ls[i], rl)
+    assert cache.device_error() == 0
