@@ -284,14 +284,15 @@ def test_layers_in_one_launch_equal_separate_calls(C, split):
     assert cache.device_error() == 0
 
 
-@pytest.mark.parametrize("ratio", [1, 2])
-def test_prefill_layers_in_one_launch_equal_separate_calls(C, ratio):
+@pytest.mark.parametrize("ratio,fp8", [(1, False), (2, False), (2, True)])
+def test_prefill_layers_in_one_launch_equal_separate_calls(C, ratio, fp8):
     """csa2_sparse_attn_prefill_layers: three layers of a chunk (own queries,
-    window rows, sinks and outputs; one selection; output RoPE on) in one
-    launch give, layer by layer, exactly the outputs and lse of separate
-    csa2_sparse_attn_prefill calls; layer 1 checked against the oracle."""
+    window rows -- bf16 or FP8 --, sinks and outputs; one selection; output
+    RoPE on) in one launch give, layer by layer, exactly the outputs and lse
+    of separate csa2_sparse_attn_prefill calls; layer 1 checked against the
+    oracle."""
     import torch
-    rng = np.random.default_rng(91 + ratio)
+    rng = np.random.default_rng(91 + ratio + 10 * fp8)
     n_ent = 900
     cache, ents = _cache(C, [n_ent], 1024, 92, ratio=ratio)
     nq, pos0, L = 30, 1700 if ratio == 2 else 850, 3
@@ -306,13 +307,15 @@ def test_prefill_layers_in_one_launch_equal_separate_calls(C, ratio):
     q_d, r_d, s_d = [bf16_dev(x) for x in qs], [bf16_dev(x) for x in rows], [f32_dev(x) for x in sinks]
     outs = [torch.empty(nq, 64, 512, dtype=torch.bfloat16, device="cuda") for _ in range(L)]
     lses = [torch.empty(nq, 64, device="cuda") for _ in range(L)]
-    C.csa2_sparse_attn_prefill_layers(cache, 0, pos0, q_d, r_d, swa_pos0, idx_d, float(SCALE),
-                                      outs, lses, sinks=s_d, rope_out=True, rope_base=5e5)
+    f8 = [C.csa2_swa_fp8_quantise(x) for x in r_d] if fp8 else None
+    C.csa2_sparse_attn_prefill_layers(cache, 0, pos0, q_d, None if fp8 else r_d, swa_pos0, idx_d,
+                                      float(SCALE), outs, lses, sinks=s_d, rope_out=True,
+                                      rope_base=5e5, swa_fp8s=f8)
     for l in range(L):
         lse1 = torch.empty(nq, 64, device="cuda")
-        o1 = C.csa2_sparse_attn_prefill(cache, 0, pos0, q_d[l], r_d[l], swa_pos0, idx_d,
-                                        float(SCALE), lse=lse1, sink=s_d[l], rope_out=True,
-                                        rope_base=5e5)
+        o1 = C.csa2_sparse_attn_prefill(cache, 0, pos0, q_d[l], None if fp8 else r_d[l], swa_pos0,
+                                        idx_d, float(SCALE), lse=lse1, sink=s_d[l], rope_out=True,
+                                        rope_base=5e5, swa_fp8=f8[l] if fp8 else None)
         assert torch.equal(o1.view(torch.int16), outs[l].view(torch.int16)), l
         assert torch.equal(lse1, lses[l]), l
     out = bf16_host(outs[1])
@@ -320,8 +323,10 @@ def test_prefill_layers_in_one_launch_equal_separate_calls(C, ratio):
     codes, scales = O.quantise(ents[0], 0)
     for i in range(0, nq, 3):
         lo, hi = O.swa_rows(pos0 + i, 128, swa_pos0)
-        _, o, ol = O.sparse_attention(qs[1][i], codes, scales, 0, idx[i],
-                                      rows[1][lo - swa_pos0:hi - swa_pos0], SCALE)
+        win = rows[1][lo - swa_pos0:hi - swa_pos0]
+        if fp8:
+            win = O.swa_fp8_round_bf16(win)
+        _, o, ol = O.sparse_attention(qs[1][i], codes, scales, 0, idx[i], win, SCALE)
         _, o2, ol2 = O.attention_epilogue(o, ol, sink=sinks[1], rope_pos=pos0 + i, rope_base=5e5)
         check_attn(out[i], o2)
         check_lse(lse[i], ol2)
