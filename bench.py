@@ -661,25 +661,12 @@ def run_csa2(args):
                 "while step i computes (pinned host buffers)")
     if M > 1:
         # the same double-buffered copy pipeline per micro-batch: each has a
-        # compute stream (its path as a CUDA graph per buffer set) and a copy
-        # stream; the micro-batches' pipelines overlap one another
+        # compute stream and a copy stream; the micro-batches' pipelines
+        # overlap one another, their indexers ordered one after the other by
+        # events (as in the device-timed schedule).  With graphs (the
+        # default) a run of steps -- copies, events and API calls -- is
+        # captured as one CUDA graph, like the device-timed steps
         sets = [mb_sets[0], mb_sets[1]]
-        cache.set_index_sms(args.index_sms)
-        # per micro-batch and buffer set: the indexer and the rest as two
-        # graphs, so that the micro-batches' indexers can be ordered by events
-        # (as in the device-timed schedule)
-        mb_graphs = []
-        for m in range(M):
-            row = []
-            for bset in sets:
-                gi, gr = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-                with torch.cuda.graph(gi):
-                    mb_index(C, cache, bset[m])
-                with torch.cuda.graph(gr):
-                    mb_rest(C, cache, bset[m], L, scale)
-                row.append((gi, gr))
-            mb_graphs.append(row)
-        cache.set_index_sms(0)
         copy_streams = [torch.cuda.Stream() for _ in range(M)]
         # one packed buffer of inputs and one of outputs per micro-batch: one
         # copy each way per micro-batch and step
@@ -691,13 +678,14 @@ def run_csa2(args):
         h2d = sum(t.numel() * t.element_size() for h in h_in_mb[0] for t in h)
         d2h = sum(t.numel() * t.element_size() for h in h_out_mb for t in h[0])
 
-        def run_e2e(n):
+        def e2e_pipeline(n):
+            main = torch.cuda.current_stream()
+            for s_ in mb_streams + copy_streams:
+                s_.wait_stream(main)
             ev = lambda: [torch.cuda.Event(), torch.cuda.Event()]
             in_ready = [ev() for _ in range(M)]
             done = [ev() for _ in range(M)]
             out_free = [ev() for _ in range(M)]
-            for s_ in mb_streams + copy_streams:
-                s_.wait_stream(stream)
             for m in range(M):
                 with torch.cuda.stream(copy_streams[m]):
                     for h, t in zip(h_in_mb[0][m], flat(sets[0][m], names_in)):
@@ -713,12 +701,11 @@ def run_csa2(args):
                         cs.wait_event(out_free[m][b])
                     if prev_index is not None:
                         cs.wait_event(prev_index)
-                    gi, gr = mb_graphs[m][b]
                     with torch.cuda.stream(cs):
-                        gi.replay()
+                        mb_index(C, cache, sets[b][m])
                         prev_index = torch.cuda.Event()
                         prev_index.record(cs)
-                        gr.replay()
+                        mb_rest(C, cache, sets[b][m], L, scale)
                     done[m][b].record(cs)
                     with torch.cuda.stream(ps):
                         if i + 1 < n:
@@ -733,13 +720,46 @@ def run_csa2(args):
                             h.copy_(t, non_blocking=True)
                         out_free[m][b].record(ps)
             for s_ in mb_streams + copy_streams:
-                stream.wait_stream(s_)
+                main.wait_stream(s_)
+
+        cache.set_index_sms(args.index_sms)
+        e2e_pipeline(3)
+        torch.cuda.synchronize()
+        e2e_graphs = {}
+        if graphs is not None:
+            # a graph of up to 20 steps replayed; a shorter one for the rest
+            g_len = min(20, e2e_steps)
+            try:
+                for n_g in sorted({g_len, e2e_steps % g_len} - {0}):
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g):
+                        e2e_pipeline(n_g)
+                    e2e_graphs[n_g] = g
+            except RuntimeError as exc:   # host copies not capturable here: eager
+                torch.cuda.synchronize()
+                e2e_graphs = {}
+                print(f"end-to-end steps run eagerly ({exc})", file=sys.stderr)
+        cache.set_index_sms(0)
+
+        def run_e2e(n):
+            if not e2e_graphs:
+                cache.set_index_sms(args.index_sms)
+                e2e_pipeline(n)
+                cache.set_index_sms(0)
+                return
+            g_len = max(e2e_graphs)
+            for _ in range(n // g_len):
+                e2e_graphs[g_len].replay()
+            if n % g_len:
+                e2e_graphs[n % g_len].replay()
 
         e2e_note = ("per micro-batch: inputs of step i+1 and outputs of step i-1 copied on "
                     "its copy stream while step i computes on its compute stream (pinned "
                     "host buffers); the micro-batches' pipelines overlap, their indexers "
-                    "ordered one after the other as in the device-timed schedule")
-    run_e2e(3)
+                    "ordered one after the other as in the device-timed schedule; " +
+                    ("runs of up to 20 steps (their copies, events and API calls) as one "
+                     "CUDA graph" if e2e_graphs else "eager API calls"))
+    run_e2e(e2e_steps if M > 1 else 3)
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b_ = torch.cuda.Event(enable_timing=True)
