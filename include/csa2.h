@@ -566,10 +566,13 @@ csa2_status_t csa2_sparse_attn_decode_ex(const csa2_cache_t* cache,
  * layers share the cache, the queries' sequences and windows' geometry
  * (seq_ids, swa_len) and the selection (topk_idx, e.g. a Full layer and its
  * Reuse layers, [V41 sec 2.3.1]), each has its own queries, window rows,
- * outputs and epilogue options.  Layer l's out / lse are exactly those of
- * csa2_sparse_attn_decode_ex with q[l], swa_kv[l], out[l], lse[l],
- * opts[l]; one launch lets the layers' CTAs fill the SMs without a kernel
- * boundary between the layers.
+ * outputs and epilogue options.  Layer l's out / lse are those of
+ * csa2_sparse_attn_decode_ex with q[l], swa_kv[l], out[l], lse[l], opts[l]
+ * -- bit for bit when both launches split a query's candidates over the
+ * same number of CTAs (with a workspace the two-CTA split follows the
+ * launch's CTA count, so a launch of several layers may not split where one
+ * of a single layer does, and then differ in the last bits); one launch lets the
+ * layers' CTAs fill the SMs without a kernel boundary between the layers.
  *   n_layers: 1 .. CSA2_MAX_ATTN_LAYERS;  q, out: host arrays of n_layers
  *   device pointers;  swa_kv: host array of n_layers device pointers
  *   (entries NULL for FP8 windows), or NULL when there is no window;  lse:

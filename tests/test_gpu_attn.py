@@ -134,11 +134,12 @@ def test_prefill_window_band(C, ratio):
         check_attn(out[i], o)
 
 
-@pytest.mark.parametrize("n_q", [3, 200])
+@pytest.mark.parametrize("n_q", [3, 50, 200])
 def test_split_and_single_cta_paths_agree_with_oracle(C, n_q):
-    """With a workspace, a small batch splits each query's candidate tiles
-    over two CTAs and merges their softmax states; without one (or for a
-    large batch) one CTA takes every tile.  Both match the oracle."""
+    """With a workspace, a small batch (3 or 50 queries) splits each query's
+    candidate tiles over two CTAs and merges their softmax states; without
+    one (or for a large batch: 200 queries) one CTA takes every tile.  Both
+    match the oracle."""
     import torch
     rng = np.random.default_rng(n_q)
     lens = [int(x) for x in rng.integers(100, 3000, n_q)]
