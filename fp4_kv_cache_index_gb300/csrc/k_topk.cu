@@ -448,16 +448,26 @@ __global__ void __launch_bounds__(kT, 1024 / kT) k_topk(const __grid_constant__ 
       load_run(srow, ea, n, vec, va);
       load_run(srow, eb, n, vec, vb);
       uint32_t ma = 0u, mb = 0u;
+      if (la == kPer && lb == kPer) {   // every chunk but the row's last
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        ma |= (uint32_t)(i < la && in_bins(va[i])) << i;
-        mb |= (uint32_t)(i < lb && in_bins(vb[i])) << i;
+        for (int i = 0; i < kPer; ++i) {
+          ma |= (uint32_t)in_bins(va[i]) << i;
+          mb |= (uint32_t)in_bins(vb[i]) << i;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          ma |= (uint32_t)(i < la && in_bins(va[i])) << i;
+          mb |= (uint32_t)(i < lb && in_bins(vb[i])) << i;
+        }
       }
       const uint32_t ca = (uint32_t)__popc(ma), cb = (uint32_t)__popc(mb);
       uint32_t tot;
       const uint32_t incl = block_prefix_sum<kT>(ca | (cb << 16), sh, tot);
       uint32_t pa = base + (incl & 0xFFFFu) - ca;
       uint32_t pb = base + (tot & 0xFFFFu) + (incl >> 16) - cb;
+      base += (tot & 0xFFFFu) + (tot >> 16);
+      if ((ma | mb) == 0u) continue;    // most runs hold no candidate
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
         if ((ma >> i) & 1u) {
@@ -475,7 +485,6 @@ __global__ void __launch_bounds__(kT, 1024 / kT) k_topk(const __grid_constant__ 
           ++pb;
         }
       }
-      base += (tot & 0xFFFFu) + (tot >> 16);
     }
   }
   if (n_cand <= (uint32_t)kCandCap) {
