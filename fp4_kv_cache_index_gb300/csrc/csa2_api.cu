@@ -1365,8 +1365,12 @@ csa2_status_t csa2_index_topk_reindex_decode(const csa2_cache_t* c, int32_t nq, 
     tp->idx_out = sel + (int64_t)q0 * k;
     tp->score_out = topk_score ? topk_score + (int64_t)q0 * k : nullptr;
     tp->key_hist = ip->key_hist;
-    tp->seg_ws = seg_ws + (size_t)q0 * topk_seg_bytes(1, slots) / sizeof(uint32_t);
-    tp->n_seg = topk_segments(slots);
+    // a pool of at most two segments (16384 slots) is compacted by the row
+    // kernel itself in one block-wide pass: one launch instead of two
+    const bool use_seg = topk_segments(slots) > 2;
+    tp->seg_ws = use_seg ? seg_ws + (size_t)q0 * topk_seg_bytes(1, slots) / sizeof(uint32_t)
+                         : nullptr;
+    tp->n_seg = use_seg ? topk_segments(slots) : 0;
     tp->formula = 0;
     tp->err = c->d_err;
     for (int i = 0; i < n; ++i) tp->n_valid[i] = slots;
