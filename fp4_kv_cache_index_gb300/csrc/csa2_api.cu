@@ -538,7 +538,7 @@ csa2_status_t topk_impl(int32_t n_rows, const void* scores, int64_t ld, const in
       return CSA2_ERR_INVALID_ARG;
     max_valid = std::max(max_valid, n_valid[r]);
   }
-  const bool seg = key_hist && workspace && aligned16(workspace) &&
+  const bool seg = key_hist && workspace && aligned16(workspace) && topk_segments(max_valid) > 2 &&
                    ws_bytes >= topk_seg_bytes(n_rows, max_valid) &&
                    topk_segments(max_valid) <= 1024;
   const int n_seg = topk_segments(max_valid);
@@ -729,7 +729,9 @@ csa2_status_t index_topk_decode_impl(const csa2_cache_t* c, int32_t nq, const vo
     tp->idx_out = topk_idx + (int64_t)q0 * k;
     tp->score_out = topk_score ? topk_score + (int64_t)q0 * k : nullptr;
     tp->key_hist = key_hist + (int64_t)q0 * kKeyHistBinsHost;
-    const bool use_seg = topk_segments(c->max_cap) <= 1024;
+    // segments pay from three on: rows of up to two (16384 scores) are
+    // compacted by the row kernel in one block-wide pass, one launch
+    const bool use_seg = topk_segments(c->max_cap) <= 1024 && topk_segments(c->max_cap) > 2;
     tp->seg_ws = use_seg ? seg_ws + (size_t)q0 * topk_seg_bytes(1, c->max_cap) / sizeof(uint32_t)
                          : nullptr;
     tp->n_seg = use_seg ? topk_segments(c->max_cap) : 0;

@@ -402,9 +402,10 @@ csa2_status_t csa2_index_topk_reindex_decode(const csa2_cache_t* cache,
                                              csa2_stream_t stream);
 
 /* Workspace bytes with which csa2_topk splits each row's candidate search
- * over several CTAs (used when key_hist is given), for n_rows rows of at
- * most max_valid scores.  A smaller workspace (or none) is allowed: the
- * selection is the same, one CTA per row.                                   */
+ * over several CTAs (used when key_hist is given and rows hold more than
+ * 16384 scores), for n_rows rows of at most max_valid scores.  A smaller
+ * workspace (or none) is allowed: the selection is the same, one CTA per
+ * row.                                                                      */
 size_t csa2_topk_workspace_bytes(int32_t n_rows, int64_t max_valid);
 
 /* Stand-alone top-k over caller scores (the selection step of the indexer):
