@@ -1006,9 +1006,11 @@ csa2_status_t csa2_sparse_attn_decode_layers(const csa2_cache_t* c, int32_t n_la
   csa2_status_t st = CSA2_OK;
   for (int q0 = 0; q0 < nq && st == CSA2_OK; q0 += kAttnTab) {
     const int n = std::min(kAttnTab, nq - q0);
-    // two CTAs per (query, head group) when one each would leave SMs idle
+    // two CTAs per (query, head group) when the pairs still fit the SMs in
+    // one wave: a second wave of split CTAs costs more than unsplit CTAs
+    // leaving some SMs idle
     const bool split = workspace && ws_bytes >= kAttnSplitToken &&
-                       (int64_t)n_layers * n * G < c->num_sms;
+                       2 * (int64_t)n_layers * n * G <= c->num_sms;
     std::memset(p, 0, sizeof(AttnParams));
     p->topk_idx = topk_idx + (int64_t)q0 * k;
     p->swa_len = swa_len ? swa_len + q0 : nullptr;
