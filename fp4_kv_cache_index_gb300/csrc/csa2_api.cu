@@ -1321,9 +1321,10 @@ csa2_status_t csa2_index_topk_reindex_decode(const csa2_cache_t* c, int32_t nq, 
   const uint16_t* qb = static_cast<const uint16_t*>(q_idx);
   if (cudaMemsetAsync(key_hist, 0, (size_t)nq * kKeyHistBinsHost * 4, S(stream)) != cudaSuccess)
     st = CSA2_ERR_CUDA;
-  // tiles of 32 blocks (256 slots; a last tile of 16 blocks when max_blocks
-  // is not a multiple of 32)
-  const int blocks_per_tile = 32;
+  // tiles of 32 blocks (256 slots) over bf16 keys, of 64 blocks (512 slots)
+  // over MXFP4 keys; a last tile holds what remains of max_blocks (a
+  // multiple of 16)
+  const int blocks_per_tile = c->cfg.idx_layout == CSA2_IDX_MXFP4 ? 64 : 32;
   const int pool_tiles = (max_blocks + blocks_per_tile - 1) / blocks_per_tile;
   for (int q0 = 0; q0 < nq && st == CSA2_OK; q0 += kMaxIdxGroups) {
     const int n = std::min(kMaxIdxGroups, nq - q0);

@@ -48,7 +48,7 @@
 //               instruction of a tile was the decode kernel's bound).  In
 //               pool mode and prefill the MMA issuer copies them itself.
 // Tiles: 512 keys (four M = 128 groups) for one query per group over
-// contiguous keys (decode), 256 pool slots (two M-groups) in pool mode, 128
+// contiguous keys (decode), 512 pool slots (four M-groups) in pool mode, 128
 // keys for four queries per group (prefill, N = 128).
 // Every wait is bounded.
 #include "csa2_device.cuh"
@@ -276,9 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = 32 * p.qpg;                      // MMA N
   const bool pool = p.pool != nullptr;
-  // keys (pool slots) per tile: 512 for one query over contiguous keys, 256
-  // in pool mode, 128 for four queries
-  const int tile_e = p.qpg == 1 ? (pool ? 256 : 512) : 128;
+  // keys (pool slots) per tile: 512 for one query (contiguous keys, or 64
+  // pool blocks of 8), 128 for four queries
+  const int tile_e = p.qpg == 1 ? 512 : 128;
   const int mgroups = tile_e / 128;
   const int acc_cols = mgroups * N;              // 128, 64 or 128 columns
   const int nacc = min(kNAcc, (int)kAccCols / acc_cols);   // 3, 4 or 3 accumulators
@@ -352,16 +352,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // copied.  The warp never waits for a load.
     const uint32_t* sw = reinterpret_cast<const uint32_t*>(p.idx_scales);   // one word per key
     const uint64_t keys_pol = l2_policy_evict_first();
-    int32_t pq[kPf];     // pool mode: this lane's block id of tiles it .. it + kPf - 1
+    // pool mode: this lane's block ids (blocks lane and lane + 32) of tiles
+    // it .. it + kPf - 1
+    int32_t pq[kPf][2];
     Cursor pc_id = c0;
-    auto load_ids = [&](int j) -> int32_t {
+    auto load_ids = [&](int j, int h) -> int32_t {
       if (!pool || j >= end) return -1;
       pc_id.advance(p, j);
-      if (lane >= pool_len(j, pc_id)) return -1;
-      return __ldg(pool_row(j, pc_id) + lane);
+      if (lane + 32 * h >= pool_len(j, pc_id)) return -1;
+      return __ldg(pool_row(j, pc_id) + lane + 32 * h);
     };
 #pragma unroll
-    for (int u = 0; u < kPf; ++u) pq[u] = load_ids(begin + u);
+    for (int u = 0; u < kPf; ++u) {
+      pq[u][0] = load_ids(begin + u, 0);
+      pq[u][1] = load_ids(begin + u, 1);
+    }
 
     Cursor gc = c0;
     int stage = 0;
@@ -394,15 +399,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
           const int64_t base = gc.base;
-          const int32_t blk_lane = pq[u];
+          const int32_t blk_lo = pq[u][0], blk_hi = pq[u][1];   // blocks lane, lane + 32
           // scale words into the atoms: row 32 q + r of M-group mg at byte
-          // 16 r + 4 q of that group's atom
+          // 16 r + 4 q of that group's atom; the slot's block is mg 16 +
+          // 4 q + lane / 8, in the first half of the tile for mg < 2
 #pragma unroll
-          for (int mg = 0; mg < 2; ++mg) {
+          for (int mg = 0; mg < 4; ++mg) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const int sl = mg * 128 + 32 * q + lane;     // pool slot of the tile
-              const int32_t blk = __shfl_sync(0xffffffffu, blk_lane, sl >> 3);
+              const int32_t blk = __shfl_sync(0xffffffffu, mg < 2 ? blk_lo : blk_hi, (sl >> 3) & 31);
               const int64_t row = blk >= 0 ? base + (int64_t)blk * 8 + (sl & 7) : -1;
               const bool live = row >= 0 && row < p.idx_total;
               cp_async4(st + kCodeStage + mg * kSfAtom + lane * 16 + q * 4, sw + (live ? row : 0),
@@ -410,17 +416,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           cp_async_arrive_noinc(k_full + stage);
-          const uint32_t n_ok = (uint32_t)__popc(__ballot_sync(0xffffffffu, blk_lane >= 0));
+          const uint32_t n_ok = (uint32_t)__popc(__ballot_sync(0xffffffffu, blk_lo >= 0)) +
+                                (uint32_t)__popc(__ballot_sync(0xffffffffu, blk_hi >= 0));
           if (lane == 0) mbar_arrive_expect_tx(k_full + stage, n_ok * 512u);
           __syncwarp();
-          if (blk_lane >= 0)
-            tma_load_2d(st + lane * 512, &tm_kc8, 0, (int32_t)(base + (int64_t)blk_lane * 8),
+          if (blk_lo >= 0)
+            tma_load_2d(st + lane * 512, &tm_kc8, 0, (int32_t)(base + (int64_t)blk_lo * 8),
+                        k_full + stage, keys_pol);
+          if (blk_hi >= 0)
+            tma_load_2d(st + (lane + 32) * 512, &tm_kc8, 0, (int32_t)(base + (int64_t)blk_hi * 8),
                         k_full + stage, keys_pol);
         }
         armed |= 1u << stage;
         armed_ph = (armed_ph & ~(1u << stage)) | (ph << stage);
         if (++stage == kStages) { stage = 0; ph ^= 1; }
-        pq[u] = load_ids(it + kPf);
+        pq[u][0] = load_ids(it + kPf, 0);
+        pq[u][1] = load_ids(it + kPf, 1);
       }
     }
     // no bulk copy may still be writing into this CTA's shared memory

@@ -174,10 +174,12 @@ def test_reindex_on_mxfp4_keys(C):
     print("near-ties:", log)
 
 
-def test_reindex_on_mxfp4_keys_partial_tile(C):
-    """A pool of 48 blocks: the last 256-slot tile of the MXFP4 indexer holds
-    16 blocks (slots past the pool are neither scored nor stored)."""
-    _reindex_case(C, [3000, 777], 3001, [0, 1, 1], 48, 140)
+@pytest.mark.parametrize("max_blocks", [48, 80])
+def test_reindex_on_mxfp4_keys_partial_tile(C, max_blocks):
+    """Pools of 48 and 80 blocks: the last 512-slot tile of the MXFP4 indexer
+    holds 48 or 16 blocks (slots past the pool are neither scored nor
+    stored)."""
+    _reindex_case(C, [3000, 777], 3001, [0, 1, 1], max_blocks, 140)
 
 
 def test_small_context_reindex_equals_full_selection_mxfp4(C):
